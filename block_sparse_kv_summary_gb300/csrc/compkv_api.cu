@@ -1,0 +1,440 @@
+// C-ABI entry points of libcompkv.so: argument validation, the scratch layout,
+// and the launch sequence of each call.  See include/compkv.h for the contract.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/compkv.h"
+#include "compkv_launch.h"
+
+using namespace compkv;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+compkv_status fail(compkv_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+constexpr int kMaxSelectBlocks = 49152;  // keys of one (sequence, head) held in shared memory
+
+struct Layout {
+  std::vector<int> cap_blocks;
+  std::vector<int64_t> seq_row0;
+  std::vector<int> chunk0, nchunk;
+  int64_t rows_per_layer = 0;
+  int total_chunks = 0;
+  int max_cap_blocks = 0;
+  int K = 0, splits = 0;
+  size_t off_status = 0, off_counter = 0, off_chunk_rec = 0, off_chunk_z = 0, off_chunk_u = 0, off_split = 0,
+         off_sel = 0, total = 0;
+};
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+compkv_status make_layout(const compkv_config* c, Layout* L) {
+  if (!c) return fail(COMPKV_ERR_INVALID_ARG, "config is NULL");
+  if (c->num_layers < 1) return fail(COMPKV_ERR_INVALID_ARG, "num_layers must be >= 1 (got %d)", c->num_layers);
+  if (c->batch < 1 || c->batch > kMaxBatch)
+    return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "batch must be in 1..%d (got %d)", kMaxBatch, c->batch);
+  if (c->num_kv_heads < 1 || c->num_kv_heads > 32)
+    return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "num_kv_heads must be in 1..32 (got %d)", c->num_kv_heads);
+  if (!(c->group_size == 1 || c->group_size == 2 || c->group_size == 4 || c->group_size == 8))
+    return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "group_size must be 1, 2, 4 or 8 (got %d)", c->group_size);
+  if (!(c->head_dim == 64 || c->head_dim == 128))
+    return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "head_dim must be 64 or 128 (got %d)", c->head_dim);
+  if (c->block_size != kBlock) return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "block_size must be 16 (got %d)", c->block_size);
+  if (!is_pow2(c->r) || c->r > c->head_dim || c->head_dim % c->r)
+    return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "r must be a power of two dividing head_dim (got %d)", c->r);
+  if (c->budget_tokens % kBlock || c->budget_tokens / kBlock < 3 || c->budget_tokens / kBlock > 4096)
+    return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "budget_tokens must be a multiple of 16 in 48..65536 (got %d)",
+                c->budget_tokens);
+  L->cap_blocks.resize(c->batch);
+  for (int s = 0; s < c->batch; ++s) {
+    const int cap = c->capacity_tokens ? c->capacity_tokens[s] : c->max_tokens;
+    if (cap < kBlock || cap % kBlock)
+      return fail(COMPKV_ERR_INVALID_ARG, "capacity of sequence %d must be a positive multiple of 16 (got %d)", s, cap);
+    if (cap / kBlock > kMaxSelectBlocks)
+      return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "capacity of sequence %d exceeds %d tokens", s, kMaxSelectBlocks * kBlock);
+    L->cap_blocks[s] = cap / kBlock;
+  }
+  const int H = c->num_kv_heads, G = c->group_size, d = c->head_dim;
+  L->seq_row0.resize(c->batch);
+  L->chunk0.resize(c->batch);
+  L->nchunk.resize(c->batch);
+  int64_t row = 0;
+  int64_t ch = 0;
+  L->max_cap_blocks = 0;
+  for (int s = 0; s < c->batch; ++s) {
+    L->seq_row0[s] = row;
+    row += (int64_t)H * L->cap_blocks[s];
+    L->nchunk[s] = (L->cap_blocks[s] + kChunk - 1) / kChunk;
+    L->chunk0[s] = (int)ch;
+    ch += (int64_t)H * L->nchunk[s];
+    if (L->cap_blocks[s] > L->max_cap_blocks) L->max_cap_blocks = L->cap_blocks[s];
+  }
+  if (ch > (int64_t)1 << 30) return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "too many scoring work items");
+  L->rows_per_layer = row;
+  L->total_chunks = (int)ch;
+  L->K = c->budget_tokens / kBlock;
+  L->splits = (L->K + kSplitBlocks - 1) / kSplitBlocks;
+  const size_t rec = (size_t)G * (4 + d) * sizeof(float);
+  size_t off = 0;
+  L->off_status = off;
+  off = round256(off + 16);
+  L->off_counter = off;
+  off = round256(off + (size_t)c->batch * H * sizeof(int));
+  L->off_chunk_rec = off;
+  off = round256(off + (size_t)L->total_chunks * rec);
+  L->off_chunk_z = off;
+  off = round256(off + (size_t)L->total_chunks * G * kChunk * sizeof(float));
+  L->off_chunk_u = off;
+  off = round256(off + (size_t)L->total_chunks * G * kChunk * sizeof(float));
+  L->off_split = off;
+  off = round256(off + (size_t)c->batch * H * L->splits * rec);
+  L->off_sel = off;
+  off = round256(off + (size_t)c->batch * H * L->K * sizeof(int));
+  L->total = off;
+  return COMPKV_OK;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+}  // namespace
+
+struct ProfSlot {
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> pending;
+  double ms = 0.0;
+  int64_t count = 0;
+};
+
+struct compkv_ctx {
+  compkv_config cfg;
+  compkv_buffers buf;
+  Layout lay;
+  int64_t launches = 0;
+  bool prof = false;
+  ProfSlot slots[COMPKV_KERNEL_FAMILIES];
+  std::vector<cudaEvent_t> pool;
+  ~compkv_ctx() {
+    for (auto& sl : slots)
+      for (auto& pr : sl.pending) {
+        cudaEventDestroy(pr.first);
+        cudaEventDestroy(pr.second);
+      }
+    for (auto e : pool) cudaEventDestroy(e);
+  }
+};
+
+namespace {
+
+LayerArgs base_args(const compkv_ctx* c, int layer) {
+  LayerArgs a;
+  memset(&a, 0, sizeof(a));
+  const int d = c->cfg.head_dim, r = c->cfg.r;
+  const int64_t rows = c->lay.rows_per_layer * (int64_t)layer;
+  a.k = reinterpret_cast<__nv_bfloat16*>(c->buf.k) + rows * kBlock * d;
+  a.v = reinterpret_cast<__nv_bfloat16*>(c->buf.v) + rows * kBlock * d;
+  a.kbar = c->buf.kbar + rows * d;
+  a.vbar = c->buf.vbar + rows * d;
+  a.dbar = c->buf.dbar + rows * r;
+  a.seq_len = c->buf.seq_len + (int64_t)layer * c->cfg.batch;
+  a.B = c->cfg.batch;
+  a.Hkv = c->cfg.num_kv_heads;
+  a.G = c->cfg.group_size;
+  a.d = d;
+  a.r = r;
+  a.K = c->lay.K;
+  a.splits = c->lay.splits;
+  a.len_add = 0;
+  char* sc = reinterpret_cast<char*>(c->buf.scratch);
+  a.status = reinterpret_cast<int*>(sc + c->lay.off_status);
+  a.head_counter = reinterpret_cast<int*>(sc + c->lay.off_counter);
+  a.chunk_rec = reinterpret_cast<float*>(sc + c->lay.off_chunk_rec);
+  a.chunk_z = reinterpret_cast<float*>(sc + c->lay.off_chunk_z);
+  a.chunk_u = reinterpret_cast<float*>(sc + c->lay.off_chunk_u);
+  a.split_rec = reinterpret_cast<float*>(sc + c->lay.off_split);
+  a.sel = reinterpret_cast<int*>(sc + c->lay.off_sel);
+  for (int s = 0; s < c->cfg.batch; ++s) {
+    a.seq_row0[s] = c->lay.seq_row0[s];
+    a.cap_blocks[s] = c->lay.cap_blocks[s];
+    a.chunk0[s] = c->lay.chunk0[s];
+    a.nchunk[s] = c->lay.nchunk[s];
+  }
+  return a;
+}
+
+compkv_status check_call(const compkv_ctx* c, int layer) {
+  if (!c) return fail(COMPKV_ERR_INVALID_ARG, "context is NULL");
+  if (layer < 0 || layer >= c->cfg.num_layers)
+    return fail(COMPKV_ERR_INVALID_ARG, "layer %d out of range [0, %d)", layer, c->cfg.num_layers);
+  return COMPKV_OK;
+}
+
+compkv_status check_ptr(const void* p, const char* name, size_t align) {
+  if (!p) return fail(COMPKV_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned(p, align)) return fail(COMPKV_ERR_INVALID_ARG, "%s must be %zu-byte aligned", name, align);
+  return COMPKV_OK;
+}
+
+compkv_status cuda_status(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return COMPKV_OK;
+  return fail(COMPKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+#define COMPKV_TRY(x)                    \
+  do {                                   \
+    compkv_status _st = (x);             \
+    if (_st != COMPKV_OK) return _st;    \
+  } while (0)
+
+cudaEvent_t take_event(compkv_ctx* c) {
+  if (!c->pool.empty()) {
+    cudaEvent_t e = c->pool.back();
+    c->pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Launch one kernel (counted), bracketed by events when profiling is on.
+template <class F>
+compkv_status launch(compkv_ctx* c, int family, cudaStream_t st, const char* what, F&& fn) {
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (c->prof) {
+    e0 = take_event(c);
+    e1 = take_event(c);
+    if (e0 && e1) cudaEventRecord(e0, st);
+  }
+  const cudaError_t e = fn();
+  if (e != cudaSuccess) {
+    if (e0) c->pool.push_back(e0);
+    if (e1) c->pool.push_back(e1);
+    return cuda_status(e, what);
+  }
+  if (e0 && e1) {
+    cudaEventRecord(e1, st);
+    c->slots[family].pending.emplace_back(e0, e1);
+  }
+  c->launches += 1;
+  return COMPKV_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int64_t compkv_rows_per_layer(const compkv_config* cfg) {
+  Layout L;
+  if (make_layout(cfg, &L) != COMPKV_OK) return 0;
+  return L.rows_per_layer;
+}
+
+size_t compkv_scratch_bytes(const compkv_config* cfg) {
+  Layout L;
+  if (make_layout(cfg, &L) != COMPKV_OK) return 0;
+  return L.total;
+}
+
+compkv_status compkv_init(const compkv_config* cfg, const compkv_buffers* bufs, compkv_ctx** out) {
+  g_last_error[0] = 0;
+  if (!out) return fail(COMPKV_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  Layout L;
+  COMPKV_TRY(make_layout(cfg, &L));
+  if (!bufs) return fail(COMPKV_ERR_INVALID_ARG, "buffers are NULL");
+  COMPKV_TRY(check_ptr(bufs->k, "k", 16));
+  COMPKV_TRY(check_ptr(bufs->v, "v", 16));
+  COMPKV_TRY(check_ptr(bufs->kbar, "kbar", 16));
+  COMPKV_TRY(check_ptr(bufs->vbar, "vbar", 16));
+  COMPKV_TRY(check_ptr(bufs->dbar, "dbar", 16));
+  COMPKV_TRY(check_ptr(bufs->seq_len, "seq_len", 4));
+  COMPKV_TRY(check_ptr(bufs->scratch, "scratch", 256));
+  if (bufs->scratch_bytes < L.total)
+    return fail(COMPKV_ERR_INVALID_ARG, "scratch_bytes %zu < required %zu", bufs->scratch_bytes, L.total);
+  compkv_ctx* c = new (std::nothrow) compkv_ctx();
+  if (!c) return fail(COMPKV_ERR_INVALID_ARG, "out of host memory");
+  c->cfg = *cfg;
+  c->cfg.capacity_tokens = nullptr;  // copied into the layout
+  c->buf = *bufs;
+  c->lay = L;
+  cudaError_t e = cudaMemsetAsync(bufs->scratch, 0, L.total, 0);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(0);
+  if (e != cudaSuccess) {
+    delete c;
+    return cuda_status(e, "zeroing scratch");
+  }
+  *out = c;
+  return COMPKV_OK;
+}
+
+compkv_status compkv_row_offset(const compkv_ctx* c, int layer, int seq, int head, int64_t* first_row,
+                                int* capacity_blocks) {
+  COMPKV_TRY(check_call(c, layer));
+  if (seq < 0 || seq >= c->cfg.batch || head < 0 || head >= c->cfg.num_kv_heads)
+    return fail(COMPKV_ERR_INVALID_ARG, "sequence %d / head %d out of range", seq, head);
+  if (first_row)
+    *first_row = c->lay.rows_per_layer * layer + c->lay.seq_row0[seq] + (int64_t)head * c->lay.cap_blocks[seq];
+  if (capacity_blocks) *capacity_blocks = c->lay.cap_blocks[seq];
+  return COMPKV_OK;
+}
+
+compkv_status compkv_prefill(compkv_ctx* c, int layer, const int* lens, void* stream) {
+  COMPKV_TRY(check_call(c, layer));
+  if (!lens) return fail(COMPKV_ERR_INVALID_ARG, "lens is NULL");
+  LayerArgs a = base_args(c, layer);
+  for (int s = 0; s < c->cfg.batch; ++s) {
+    if (lens[s] < 0 || lens[s] > c->lay.cap_blocks[s] * kBlock)
+      return fail(COMPKV_ERR_CAPACITY, "lens[%d] = %d outside [0, %d]", s, lens[s], c->lay.cap_blocks[s] * kBlock);
+    a.lens[s] = lens[s];
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  COMPKV_TRY(launch(c, COMPKV_KERNEL_PREFILL, st, "prefill launch",
+                    [&] { return launch_prefill(a, c->lay.rows_per_layer, st); }));
+  return COMPKV_OK;
+}
+
+compkv_status compkv_append(compkv_ctx* c, int layer, const void* k_new, const void* v_new, void* stream) {
+  COMPKV_TRY(check_call(c, layer));
+  COMPKV_TRY(check_ptr(k_new, "k_new", 16));
+  COMPKV_TRY(check_ptr(v_new, "v_new", 16));
+  LayerArgs a = base_args(c, layer);
+  a.k_new = reinterpret_cast<const __nv_bfloat16*>(k_new);
+  a.v_new = reinterpret_cast<const __nv_bfloat16*>(v_new);
+  cudaStream_t st = (cudaStream_t)stream;
+  COMPKV_TRY(launch(c, COMPKV_KERNEL_APPEND, st, "append launch", [&] { return launch_append(a, st); }));
+  return COMPKV_OK;
+}
+
+compkv_status compkv_score_select(compkv_ctx* c, int layer, const float* q, int* sel, float* scores, void* stream) {
+  COMPKV_TRY(check_call(c, layer));
+  COMPKV_TRY(check_ptr(q, "q", 16));
+  COMPKV_TRY(check_ptr(sel, "sel", 16));
+  if (scores) COMPKV_TRY(check_ptr(scores, "scores", 16));
+  LayerArgs a = base_args(c, layer);
+  a.q = q;
+  a.sel = sel;
+  a.scores = scores;
+  a.score_stride = c->lay.max_cap_blocks;
+  cudaStream_t st = (cudaStream_t)stream;
+  COMPKV_TRY(launch(c, COMPKV_KERNEL_SCORE, st, "score launch",
+                    [&] { return launch_score(a, kModeScore, c->lay.total_chunks, st); }));
+  COMPKV_TRY(launch(c, COMPKV_KERNEL_SELECT, st, "select launch",
+                    [&] { return launch_select(a, c->lay.max_cap_blocks, st); }));
+  return COMPKV_OK;
+}
+
+compkv_status compkv_attend(compkv_ctx* c, int layer, const float* q, const int* sel, float* out, void* stream) {
+  COMPKV_TRY(check_call(c, layer));
+  COMPKV_TRY(check_ptr(q, "q", 16));
+  COMPKV_TRY(check_ptr(sel, "sel", 16));
+  COMPKV_TRY(check_ptr(out, "out", 16));
+  LayerArgs a = base_args(c, layer);
+  a.q = q;
+  a.sel = const_cast<int*>(sel);
+  a.out = out;
+  cudaStream_t st = (cudaStream_t)stream;
+  COMPKV_TRY(launch(c, COMPKV_KERNEL_SCORE, st, "score launch",
+                    [&] { return launch_score(a, kModeComp, c->lay.total_chunks, st); }));
+  COMPKV_TRY(launch(c, COMPKV_KERNEL_ATTEND, st, "attend launch", [&] { return launch_attend(a, st); }));
+  return COMPKV_OK;
+}
+
+compkv_status compkv_decode(compkv_ctx* c, int layer, const float* q, const void* k_new, const void* v_new, float* out,
+                            int* sel, void* stream) {
+  COMPKV_TRY(check_call(c, layer));
+  COMPKV_TRY(check_ptr(q, "q", 16));
+  COMPKV_TRY(check_ptr(k_new, "k_new", 16));
+  COMPKV_TRY(check_ptr(v_new, "v_new", 16));
+  COMPKV_TRY(check_ptr(out, "out", 16));
+  if (sel) COMPKV_TRY(check_ptr(sel, "sel", 16));
+  LayerArgs a = base_args(c, layer);
+  a.q = q;
+  a.k_new = reinterpret_cast<const __nv_bfloat16*>(k_new);
+  a.v_new = reinterpret_cast<const __nv_bfloat16*>(v_new);
+  a.out = out;
+  if (sel) a.sel = sel;
+  cudaStream_t st = (cudaStream_t)stream;
+  COMPKV_TRY(launch(c, COMPKV_KERNEL_APPEND, st, "append launch", [&] { return launch_append(a, st); }));
+  COMPKV_TRY(launch(c, COMPKV_KERNEL_SCORE, st, "score launch",
+                    [&] { return launch_score(a, kModeScore | kModeComp, c->lay.total_chunks, st); }));
+  COMPKV_TRY(launch(c, COMPKV_KERNEL_SELECT, st, "select launch",
+                    [&] { return launch_select(a, c->lay.max_cap_blocks, st); }));
+  COMPKV_TRY(launch(c, COMPKV_KERNEL_ATTEND, st, "attend launch", [&] { return launch_attend(a, st); }));
+  return COMPKV_OK;
+}
+
+compkv_status compkv_device_status(compkv_ctx* c, void* stream) {
+  if (!c) return fail(COMPKV_ERR_INVALID_ARG, "context is NULL");
+  cudaStream_t st = (cudaStream_t)stream;
+  COMPKV_TRY(cuda_status(cudaStreamSynchronize(st), "stream synchronize"));
+  int h[4] = {0, 0, 0, 0};
+  int* dev = reinterpret_cast<int*>(reinterpret_cast<char*>(c->buf.scratch) + c->lay.off_status);
+  COMPKV_TRY(cuda_status(cudaMemcpyAsync(h, dev, sizeof(h), cudaMemcpyDeviceToHost, st), "status read"));
+  COMPKV_TRY(cuda_status(cudaStreamSynchronize(st), "stream synchronize"));
+  if (h[0] == 0) return COMPKV_OK;
+  COMPKV_TRY(cuda_status(cudaMemsetAsync(dev, 0, sizeof(h), st), "status clear"));
+  COMPKV_TRY(cuda_status(cudaStreamSynchronize(st), "stream synchronize"));
+  return fail((compkv_status)h[0], "device status %d (sequence %d, head %d, site %d)", h[0], h[1], h[2], h[3]);
+}
+
+int64_t compkv_launch_count(const compkv_ctx* c) { return c ? c->launches : 0; }
+
+compkv_status compkv_profile_enable(compkv_ctx* c, int enable) {
+  if (!c) return fail(COMPKV_ERR_INVALID_ARG, "context is NULL");
+  c->prof = enable != 0;
+  return COMPKV_OK;
+}
+
+compkv_status compkv_profile_read(compkv_ctx* c, int family, double* total_ms, int64_t* launches) {
+  if (!c) return fail(COMPKV_ERR_INVALID_ARG, "context is NULL");
+  if (family < 0 || family >= COMPKV_KERNEL_FAMILIES) return fail(COMPKV_ERR_INVALID_ARG, "bad kernel family %d", family);
+  ProfSlot& sl = c->slots[family];
+  for (auto& pr : sl.pending) {
+    COMPKV_TRY(cuda_status(cudaEventSynchronize(pr.second), "event synchronize"));
+    float ms = 0.f;
+    COMPKV_TRY(cuda_status(cudaEventElapsedTime(&ms, pr.first, pr.second), "event elapsed"));
+    sl.ms += ms;
+    sl.count += 1;
+    c->pool.push_back(pr.first);
+    c->pool.push_back(pr.second);
+  }
+  sl.pending.clear();
+  if (total_ms) *total_ms = sl.ms;
+  if (launches) *launches = sl.count;
+  sl.ms = 0.0;
+  sl.count = 0;
+  return COMPKV_OK;
+}
+
+const char* compkv_last_error(void) { return g_last_error; }
+
+const char* compkv_status_string(compkv_status s) {
+  switch (s) {
+    case COMPKV_OK: return "COMPKV_OK";
+    case COMPKV_ERR_INVALID_ARG: return "COMPKV_ERR_INVALID_ARG";
+    case COMPKV_ERR_UNSUPPORTED_SHAPE: return "COMPKV_ERR_UNSUPPORTED_SHAPE";
+    case COMPKV_ERR_CAPACITY: return "COMPKV_ERR_CAPACITY";
+    case COMPKV_ERR_CUDA: return "COMPKV_ERR_CUDA";
+    case COMPKV_ERR_TIMEOUT: return "COMPKV_ERR_TIMEOUT";
+    case COMPKV_ERR_BAD_SELECTION: return "COMPKV_ERR_BAD_SELECTION";
+    case COMPKV_ERR_INTERNAL: return "COMPKV_ERR_INTERNAL";
+  }
+  return "COMPKV_UNKNOWN";
+}
+
+void compkv_destroy(compkv_ctx* c) { delete c; }
+
+}  // extern "C"

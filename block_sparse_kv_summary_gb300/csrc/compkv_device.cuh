@@ -1,0 +1,185 @@
+// Device-side building blocks of the CompKV decode-step kernels (sm_103a).
+//
+// The launch-argument struct, the scratch record layout, inline-PTX wrappers
+// for mbarriers and 1-D bulk (TMA) copies into shared memory, bounded waits
+// that report through the device status word, and warp reductions.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace compkv {
+
+constexpr int kBlock = 16;        // tokens per KV block (CompKV, "전제와 한계": block size 16)
+constexpr int kMaxBatch = 64;     // sequences per call (launch arguments hold per-sequence tables)
+constexpr int kChunk = 64;        // blocks per scoring work item
+constexpr int kSplitBlocks = 8;   // selected blocks per attention work item
+constexpr int kMaxG = 8;
+
+// Device status word codes (mirrors compkv_status).
+enum DevErr : int {
+  kDevOk = 0,
+  kDevCapacity = 3,
+  kDevTimeout = 5,
+  kDevBadSelection = 6,
+  kDevInternal = 7,
+};
+
+// Per-call arguments, passed by value (fits the kernel parameter space).
+struct LayerArgs {
+  // cache of this layer (row 0 = first row of the layer)
+  __nv_bfloat16* k;
+  __nv_bfloat16* v;
+  float* kbar;
+  float* vbar;
+  float* dbar;
+  int* seq_len;               // [B] of this layer
+  // inputs / outputs of the call
+  const float* q;             // [B][Hkv*G][d]
+  const __nv_bfloat16* k_new; // [B][Hkv][d]
+  const __nv_bfloat16* v_new;
+  float* out;                 // [B][Hkv*G][d]
+  int* sel;                   // [B][Hkv][K]
+  float* scores;              // [B][Hkv][score_stride] or null
+  int score_stride;
+  // shape
+  int B, Hkv, G, d, r, K;
+  int splits;                 // attention work items per (sequence, head)
+  int len_add;                // tokens to add to seq_len when reading it
+  // scratch
+  int* status;                // [4]: code, sequence, head, site
+  int* head_counter;          // [B*Hkv]
+  float* chunk_rec;           // [total chunk records][G][4 + d]
+  float* chunk_z;             // [total chunk records][G][kChunk]  zbar per block
+  float* chunk_u;             // [total chunk records][G][kChunk]  exp(a - m_a) * sigma2
+  float* split_rec;           // [B*Hkv*splits][G][4 + d]
+  // ragged tables
+  int64_t seq_row0[kMaxBatch];   // first row of (s, head 0) relative to the layer
+  int cap_blocks[kMaxBatch];     // capacity of sequence s in blocks
+  int chunk0[kMaxBatch];         // first chunk record of (s, head 0)
+  int nchunk[kMaxBatch];         // chunk records per (s, head) = ceil(cap / kChunk)
+  int lens[kMaxBatch];           // prefill lengths (compkv_prefill only)
+};
+
+__device__ __forceinline__ int64_t row_of(const LayerArgs& a, int s, int h, int b) {
+  return a.seq_row0[s] + (int64_t)h * a.cap_blocks[s] + b;
+}
+__device__ __forceinline__ int rec_stride(const LayerArgs& a) { return a.G * (4 + a.d); }
+
+// ---------------------------------------------------------------- status
+__device__ __forceinline__ void set_error(int* status, int code, int s, int h, int site) {
+  if (atomicCAS(status, 0, code) == 0) {
+    status[1] = s;
+    status[2] = h;
+    status[3] = site;
+  }
+}
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for phase `parity` of `bar`; gives up after a bounded number of polls
+// (each try_wait itself blocks for a hardware-defined time slice), records
+// a timeout in the status word and returns false.
+constexpr uint32_t kWaitPolls = 1u << 22;
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status, int s, int h,
+                                                  int site) {
+  for (uint32_t i = 0; i < kWaitPolls; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  set_error(status, kDevTimeout, s, h, site);
+  // give copies still in flight a second bounded chance to land before the CTA exits
+  for (uint32_t i = 0; i < kWaitPolls; ++i)
+    if (mbar_try_wait(bar, parity)) break;
+  return false;
+}
+
+// ---------------------------------------------------------------- math helpers
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
+}
+
+// bf16 x N -> float x N (N = 2 or 4), from an 8- or 4-byte aligned address.
+template <int N>
+__device__ __forceinline__ void load_bf16(const __nv_bfloat16* p, float* f);
+template <>
+__device__ __forceinline__ void load_bf16<4>(const __nv_bfloat16* p, float* f) {
+  uint2 u = *reinterpret_cast<const uint2*>(p);
+  float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u.x));
+  float2 b = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u.y));
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+}
+template <>
+__device__ __forceinline__ void load_bf16<2>(const __nv_bfloat16* p, float* f) {
+  uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+  float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u));
+  f[0] = a.x; f[1] = a.y;
+}
+template <int N>
+__device__ __forceinline__ void store_bf16_raw(__nv_bfloat16* dst, const __nv_bfloat16* src);
+template <>
+__device__ __forceinline__ void store_bf16_raw<4>(__nv_bfloat16* dst, const __nv_bfloat16* src) {
+  *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(src);
+}
+template <>
+__device__ __forceinline__ void store_bf16_raw<2>(__nv_bfloat16* dst, const __nv_bfloat16* src) {
+  *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(src);
+}
+
+// Tokens held by sequence s in this call.  seq_len is caller memory: a value
+// outside [0, capacity] is reported and clamped so no access leaves the rows.
+__device__ __forceinline__ int seq_tokens(const LayerArgs& a, int s) {
+  int L = a.seq_len[s] + a.len_add;
+  const int cap = a.cap_blocks[s] * kBlock;
+  if (L < 0 || L > cap) {
+    set_error(a.status, kDevCapacity, s, -1, 2);
+    L = L < 0 ? 0 : cap;
+  }
+  return L;
+}
+__device__ __forceinline__ int ceil_blocks(int L) { return (L + kBlock - 1) / kBlock; }
+
+}  // namespace compkv

@@ -1,0 +1,204 @@
+/*
+ * compkv.h -- C ABI of the CompKV decode-step library (libcompkv.so).
+ *
+ * CompKV (onedev.kr/papers/157) is a compensation-aware block-sparse attention
+ * for autoregressive decoding.  Per decode step, for every (sequence, KV head):
+ *   1. the 16-token block that receives the new token gets its summary
+ *      {|b|, kbar_b, Dbar_b, vbar_b} recomputed and the new K/V is packed into
+ *      the cache  (section "어떻게 쓰나" / how it is used: the fused "update the
+ *      current block's statistics and pack the new K/V" kernel; the summary is
+ *      defined in section "무엇과 다른가" / how it differs);
+ *   2. every block is scored from its summary (same section):
+ *        zbar_{g,b}   = q_g . kbar_b / sqrt(d)
+ *        sigma2_{g,b} = (1/d) sum_t (sum_{i in G_t} q_{g,i}^2) (Dbar_b)_t
+ *        phat_{g,b}   = |b| exp(zbar + sigma2/2) / sum_c |c| exp(zbar_c + sigma2_c/2)
+ *        S_b          = sum_g phat_{g,b} sigma2_{g,b}
+ *   3. the sink block and the two most recent blocks are always selected and
+ *      count against the K-block budget; the rest of the budget goes to the
+ *      highest S_b, ties to the lower block index (same section);
+ *   4. exact attention over the selected blocks' bf16 K/V, and
+ *   5. Mean compensation: each unselected block adds |b| exp(zbar_{g,b}) vbar_b
+ *      to the numerator and |b| exp(zbar_{g,b}) to the denominator; both parts
+ *      share one normaliser (sections "무엇과 다른가" and "어떻게 동작하나").
+ *
+ * Everything (the bf16 cache, the fp32 summaries, the scratch) lives in the
+ * memory of one GPU.  The library allocates no device memory: every device
+ * buffer below is owned by the caller.  Every call is asynchronous on the
+ * caller's CUDA stream (passed as `void*`, a cudaStream_t; NULL = legacy
+ * default stream) and returns after enqueueing its kernels.
+ *
+ * Shapes.  B = batch (sequences), Hkv = KV heads, G = query heads per KV head
+ * (query head j reads KV head j / G), d = head dim (64 or 128), r = variance
+ * groups (r divides d; group t = coordinates [t*d/r, (t+1)*d/r)), block = 16
+ * tokens, K = budget_tokens / 16 selected blocks, L = tokens of a sequence,
+ * N = ceil(L / 16) blocks (the last may be partial).
+ *
+ * Cache layout ("rows").  One row = one 16-token block of one (layer,
+ * sequence, KV head).  Row index of block b of (layer l, sequence s, head h):
+ *     l * rows_per_layer + seq_row0[s] + h * cap_blocks[s] + b
+ * where cap_blocks[s] = capacity_tokens[s] / 16 (or max_tokens / 16 for every
+ * sequence), seq_row0[s] = Hkv * sum_{s' < s} cap_blocks[s'] and
+ * rows_per_layer = Hkv * sum_s cap_blocks[s].  compkv_row_offset() returns the
+ * first row of a (layer, sequence, head).  Per row:
+ *     k, v   : bf16 [16][d]  (token j of block b at position 16 b + j)
+ *     kbar   : fp32 [d]      mean key of the block's tokens
+ *     vbar   : fp32 [d]      mean value
+ *     dbar   : fp32 [r]      per group, mean over its coordinates of the
+ *                            within-block population variance of the keys
+ * |b| is implicit: 16 for every block but the last, L - 16 (N - 1) for it.
+ * seq_len: int32 [num_layers][B], device memory, the tokens held by each
+ * (layer, sequence); compkv_append and compkv_decode increment it.
+ *
+ * Queries q: fp32 [B][Hkv*G][d].  New tokens k_new, v_new: bf16 [B][Hkv][d].
+ * Outputs out: fp32 [B][Hkv*G][d].  Selections sel: int32 [B][Hkv][K], the
+ * selected block indices ascending, padded with -1 when N < K.
+ *
+ * Errors.  Argument and shape problems are detected on the host and returned
+ * synchronously (nothing is enqueued); compkv_last_error() then describes the
+ * problem.  Problems found by a kernel (a sequence at capacity, an invalid
+ * selection passed to compkv_attend, a bounded wait that ran out) set a status
+ * word in the scratch buffer; compkv_device_status() synchronises the stream,
+ * reads it and clears it.  No call throws, aborts or falls back to the CPU.
+ *
+ * Threading: a compkv_ctx may be used from one host thread at a time; calls on
+ * one context must be ordered on one stream (they share the scratch buffer).
+ */
+#ifndef COMPKV_H
+#define COMPKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  COMPKV_OK = 0,
+  COMPKV_ERR_INVALID_ARG = 1,      /* null pointer, bad layer index, bad size      */
+  COMPKV_ERR_UNSUPPORTED_SHAPE = 2,/* d not 64/128, r does not divide d, G > 8 ... */
+  COMPKV_ERR_CAPACITY = 3,         /* a sequence would exceed its capacity          */
+  COMPKV_ERR_CUDA = 4,             /* a CUDA runtime call failed                    */
+  COMPKV_ERR_TIMEOUT = 5,          /* a bounded device-side wait ran out            */
+  COMPKV_ERR_BAD_SELECTION = 6,    /* compkv_attend got indices not ascending / out of range */
+  COMPKV_ERR_INTERNAL = 7          /* a device-side consistency check failed (a bug)       */
+} compkv_status;
+
+typedef struct {
+  int num_layers;               /* >= 1                                             */
+  int batch;                    /* B, 1..64                                         */
+  int num_kv_heads;             /* Hkv >= 1                                         */
+  int group_size;               /* G, 1..8                                          */
+  int head_dim;                 /* d, 64 or 128                                     */
+  int block_size;               /* must be 16 (the page's block size)               */
+  int r;                        /* variance groups, 1..d, divides d, power of two   */
+  int budget_tokens;            /* multiple of 16, K = budget/16 >= 3               */
+  int max_tokens;               /* per-sequence capacity (multiple of 16) when      */
+                                /* capacity_tokens is NULL                          */
+  const int *capacity_tokens;   /* optional host array [batch], each a multiple of  */
+                                /* 16: ragged per-sequence capacities; copied       */
+} compkv_config;
+
+typedef struct {
+  void  *k;                     /* bf16 [num_layers * rows_per_layer][16][d]         */
+  void  *v;                     /* bf16, same shape                                 */
+  float *kbar;                  /* fp32 [num_layers * rows_per_layer][d]            */
+  float *vbar;                  /* fp32 [num_layers * rows_per_layer][d]            */
+  float *dbar;                  /* fp32 [num_layers * rows_per_layer][r]            */
+  int   *seq_len;               /* int32 [num_layers][batch]                        */
+  void  *scratch;               /* compkv_scratch_bytes() bytes, 256-byte aligned,  */
+                                /* zero-filled by compkv_init                       */
+  size_t scratch_bytes;
+} compkv_buffers;
+
+typedef struct compkv_ctx compkv_ctx;
+
+/* Rows of one layer (rows_per_layer, see "Cache layout"); 0 on a bad config. */
+int64_t compkv_rows_per_layer(const compkv_config *cfg);
+
+/* Bytes of device scratch a context of this configuration needs; 0 on a bad config. */
+size_t compkv_scratch_bytes(const compkv_config *cfg);
+
+/* Validate cfg and bufs, zero the scratch (synchronously) and create a context.
+ * The library keeps the pointers; the caller keeps ownership of every buffer
+ * and must keep them alive until compkv_destroy. */
+compkv_status compkv_init(const compkv_config *cfg, const compkv_buffers *bufs, compkv_ctx **out);
+
+/* First row of (layer, seq, head) and that sequence's capacity in blocks. */
+compkv_status compkv_row_offset(const compkv_ctx *ctx, int layer, int seq, int head,
+                                int64_t *first_row, int *capacity_blocks);
+
+/* Bulk build: the caller has written tokens [0, lens[s]) of every sequence of
+ * `layer` into k/v; compute the summaries of all their blocks and set
+ * seq_len[layer][s] = lens[s].  lens: host int32 [batch], 0 <= lens[s] <= capacity.
+ * (The page keeps the summaries up to date token by token; a bulk build over
+ * whole blocks is the same definition applied to a prefilled cache.) */
+compkv_status compkv_prefill(compkv_ctx *ctx, int layer, const int *lens, void *stream);
+
+/* Step 1 alone: write token seq_len into every (sequence, head) of `layer`,
+ * recompute the summary of the block that holds it from its tokens, and
+ * increment seq_len.  k_new, v_new: device bf16 [B][Hkv][d].  A sequence at
+ * capacity is left unchanged and raises COMPKV_ERR_CAPACITY in the device status. */
+compkv_status compkv_append(compkv_ctx *ctx, int layer, const void *k_new, const void *v_new,
+                            void *stream);
+
+/* Steps 2-3: scores and selection for the current cache.  q: device fp32
+ * [B][Hq][d].  sel: device int32 [B][Hkv][K] (required).  scores: optional
+ * device fp32 [B][Hkv][max_cap_blocks] receiving S_b for b < N (NULL to skip);
+ * max_cap_blocks = the largest capacity in blocks. */
+compkv_status compkv_score_select(compkv_ctx *ctx, int layer, const float *q, int *sel,
+                                  float *scores, void *stream);
+
+/* Steps 4-5 for a given selection: exact attention over the listed blocks and
+ * Mean compensation for every other block, jointly normalised.  sel: device
+ * int32 [B][Hkv][K], ascending, entries in [0, N), padded with -1.  A
+ * non-ascending or out-of-range entry is skipped and raises
+ * COMPKV_ERR_BAD_SELECTION in the device status.  out: device fp32 [B][Hq][d]. */
+compkv_status compkv_attend(compkv_ctx *ctx, int layer, const float *q, const int *sel,
+                            float *out, void *stream);
+
+/* Steps 1-5 fused: append (k_new, v_new), score, select and attend, reading
+ * every block summary once.  sel: optional device int32 [B][Hkv][K] that
+ * receives the selection (NULL to skip). */
+compkv_status compkv_decode(compkv_ctx *ctx, int layer, const float *q, const void *k_new,
+                            const void *v_new, float *out, int *sel, void *stream);
+
+/* Synchronise `stream`, read and clear the device status word.  Returns
+ * COMPKV_OK or the first device-side error since the last call. */
+compkv_status compkv_device_status(compkv_ctx *ctx, void *stream);
+
+/* Kernel launches enqueued by this context since compkv_init (host counter). */
+int64_t compkv_launch_count(const compkv_ctx *ctx);
+
+/* Per-kernel timing (tracing aid, off by default).  While enabled, every
+ * kernel the context launches is bracketed by two CUDA events on the launch
+ * stream.  compkv_profile_read() synchronises on the recorded events and
+ * returns, for one kernel family, the summed device time in milliseconds and
+ * the number of launches since the last read (then resets them).  Families:
+ * COMPKV_KERNEL_PREFILL, _APPEND, _SCORE, _SELECT, _ATTEND, _DECODE.  Events
+ * are host-side CUDA objects; no device memory is allocated. */
+enum {
+  COMPKV_KERNEL_PREFILL = 0,
+  COMPKV_KERNEL_APPEND = 1,
+  COMPKV_KERNEL_SCORE = 2,
+  COMPKV_KERNEL_SELECT = 3,
+  COMPKV_KERNEL_ATTEND = 4,
+  COMPKV_KERNEL_DECODE = 5,
+  COMPKV_KERNEL_FAMILIES = 6
+};
+compkv_status compkv_profile_enable(compkv_ctx *ctx, int enable);
+compkv_status compkv_profile_read(compkv_ctx *ctx, int family, double *total_ms, int64_t *launches);
+
+/* Description of the last error returned on this host thread ("" if none). */
+const char *compkv_last_error(void);
+
+/* Name of a status code. */
+const char *compkv_status_string(compkv_status s);
+
+/* Free the context (host memory only; caller buffers are untouched). */
+void compkv_destroy(compkv_ctx *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* COMPKV_H */

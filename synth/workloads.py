@@ -47,6 +47,7 @@ class Workload:
     s_lo: float = 0.05
     s_hi: float = 1.0
     ragged: tuple | None = None  # (lo, hi) for per-sequence lengths
+    lengths: tuple | None = None # explicit per-sequence lengths (test edge cases)
     needles: int = 3
     seed: int = 20261202
 
@@ -84,6 +85,8 @@ def seed_for(base: int, *counters: int) -> int:
 
 def sequence_lengths(wl: Workload) -> list[int]:
     """Prefill length of every sequence (shared by all layers)."""
+    if wl.lengths is not None:
+        return [int(x) for x in wl.lengths]
     if wl.ragged is None:
         return [wl.context] * wl.batch
     rng = np.random.Generator(np.random.PCG64(seed_for(wl.seed, 7)))

@@ -1,0 +1,174 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle, small sizes.
+
+Selections must match bit for bit (inputs carry the 1e-4 score-gap
+guarantee), summaries and scores within 1e-4 relative, attention outputs
+within 2e-3 absolute.  Sizes span several 64-block scoring items with a
+ragged tail, partial last blocks, N <= K, N < 3, and every (d, G, r) family.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import synth
+from harness import (TOL_OUT, Run, check_scores, check_step, check_summaries, f64)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    import block_sparse_kv_summary_gb300 as P
+    P.build()
+    P.lib()
+
+
+def test_tiny_workload_decode():
+    wl = synth.WORKLOADS["tiny"]
+    run = Run(wl)
+    for (l, s, h) in run.heads:
+        check_summaries(run, l, s, h)
+    q, sel, out, res = run.decode_step(0)
+    check_step(run, 0, sel, out, res)
+    for (l, s, h) in run.heads:
+        check_summaries(run, l, s, h)
+    assert run.cache.seq_len.cpu().tolist() == [[1025]]
+    assert run.cache.device_status() == 0
+    # the planted needles (soft check: reported, not pinned)
+    hits = 0
+    for h in range(wl.num_kv_heads):
+        pos = synth.workloads.needle_positions(wl, 0, 0, h, 1024)
+        hits += sum(p // 16 in set(res[(0, h)].sel.tolist()) for p in pos)
+    print(f"needle blocks selected: {hits} of {3 * wl.num_kv_heads}")
+
+
+SHAPES = [
+    dict(head_dim=64, group_size=4, r=4, num_kv_heads=2),
+    dict(head_dim=128, group_size=4, r=4, num_kv_heads=3),
+    dict(head_dim=128, group_size=8, r=128, num_kv_heads=2),
+    dict(head_dim=128, group_size=1, r=1, num_kv_heads=2),
+    dict(head_dim=128, group_size=2, r=2, num_kv_heads=1),
+    dict(head_dim=64, group_size=8, r=64, num_kv_heads=1),
+    dict(head_dim=128, group_size=4, r=16, num_kv_heads=2),
+]
+
+
+def _ragged(shape, lengths=(1, 37, 2049, 4100), budget=128, steps=18):
+    return synth.Workload("ragged", 1, len(lengths), shape["num_kv_heads"], shape["group_size"],
+                          shape["head_dim"], shape["r"], 0, budget, steps, lengths=tuple(lengths))
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: f"d{s['head_dim']}G{s['group_size']}r{s['r']}")
+def test_decode_ragged_steps(shape):
+    wl = _ragged(shape)
+    run = Run(wl)
+    for (l, s, h) in run.heads:
+        check_summaries(run, l, s, h)
+    for step in range(wl.steps):
+        q, sel, out, res = run.decode_step(0)
+        check_step(run, 0, sel, out, res)
+    for (l, s, h) in run.heads:
+        check_summaries(run, l, s, h)
+    assert run.cache.seq_len.cpu().tolist() == [[L + wl.steps for L in wl.lengths]]
+    assert run.cache.device_status() == 0
+
+
+@pytest.mark.parametrize("budget", [48, 64, 256])
+def test_budgets_and_forced_only(budget):
+    # K = 3 selects only the forced blocks; larger budgets span several attention items
+    wl = _ragged(SHAPES[1], lengths=(5, 600, 1800), budget=budget, steps=3)
+    run = Run(wl)
+    for step in range(wl.steps):
+        q, sel, out, res = run.decode_step(0)
+        check_step(run, 0, sel, out, res)
+
+
+def test_score_select_api_scores():
+    wl = _ragged(SHAPES[1], lengths=(70, 3000, 5000), budget=256, steps=2)
+    run = Run(wl)
+    run.decode_step(0)
+    # score the current cache with fresh queries through compkv_score_select
+    k_new, v_new = run.new_tokens(0, 1)
+    run.oracle_append(0, k_new, v_new)
+    run.cache.append(0, k_new, v_new)
+    q, results = run.choose_queries(0, 1)
+    scores = torch.zeros((wl.batch, wl.num_kv_heads, run.cache.max_cap_blocks), device="cuda")
+    sel = run.cache.score_select(0, q, scores=scores)
+    S = f64(scores)
+    for (s, h), res in results.items():
+        N = len(res.scores.S)
+        check_scores(S[s, h, :N], res.scores.S)
+        exp = np.full(wl.K_blocks, -1)
+        exp[:len(res.sel)] = res.sel
+        assert np.array_equal(sel[s, h].cpu().numpy(), exp)
+    assert run.cache.device_status() == 0
+
+
+def test_attend_api_arbitrary_selections():
+    wl = _ragged(SHAPES[2], lengths=(3, 200, 1000, 3000), budget=160, steps=1)
+    run = Run(wl)
+    rng = np.random.default_rng(5)
+    K = wl.K_blocks
+    for trial in range(4):
+        q = torch.from_numpy(synth.step_queries(wl, 0, 100 + trial)).cuda()
+        sel = np.full((wl.batch, wl.num_kv_heads, K), -1, dtype=np.int32)
+        for (l, s, h), st in run.states.items():
+            N = O.num_blocks(st.L)
+            cnt = [0, min(N, K), min(N, 1), int(rng.integers(0, min(N, K) + 1))][trial]
+            pick = np.sort(rng.choice(N, size=cnt, replace=False))
+            sel[s, h, :cnt] = pick
+        sel_t = torch.from_numpy(sel).cuda()
+        out = f64(run.cache.attend(0, q, sel_t))
+        qh = q.cpu().numpy().astype(np.float64)
+        G = wl.group_size
+        for (l, s, h), st in run.states.items():
+            chosen = [b for b in sel[s, h] if b >= 0]
+            ref = O.compkv_attend(qh[s, h * G:(h + 1) * G], st.K[:st.L], st.V[:st.L], chosen, st.n, st.kbar, st.vbar)
+            assert np.abs(out[s, h * G:(h + 1) * G] - ref).max() <= TOL_OUT
+    assert run.cache.device_status() == 0
+
+
+def test_append_api_matches_oracle():
+    wl = _ragged(SHAPES[0], lengths=(14, 16, 31), budget=64, steps=20)
+    run = Run(wl)
+    for step in range(wl.steps):
+        k_new, v_new = run.new_tokens(0, step)
+        run.oracle_append(0, k_new, v_new)
+        run.cache.append(0, k_new, v_new)
+        torch.cuda.synchronize()
+        for (l, s, h), st in run.states.items():
+            N = O.num_blocks(st.L)
+            check_summaries(run, l, s, h, blocks=[N - 1])
+            kv, vv = run.cache.token_view(l, s, h)
+            assert np.array_equal(f64(kv[st.L - 1]), st.K[st.L - 1])
+            assert np.array_equal(f64(vv[st.L - 1]), st.V[st.L - 1])
+    assert run.cache.seq_len.cpu().tolist() == [[14 + 20, 16 + 20, 31 + 20]]
+
+
+def test_device_errors_are_reported():
+    import block_sparse_kv_summary_gb300 as P
+    wl = _ragged(SHAPES[0], lengths=(30, 32), budget=64, steps=1)
+    run = Run(wl)
+    # capacities are 32 and 48 tokens: fill sequence 0 to capacity, then overflow it
+    k_new, v_new = run.new_tokens(0, 0)
+    run.cache.append(0, k_new, v_new)
+    run.cache.append(0, k_new, v_new)
+    assert run.cache.device_status() == 0
+    run.cache.append(0, k_new, v_new)                # sequence 0 is full: left unchanged
+    assert run.cache.device_status() == 3            # COMPKV_ERR_CAPACITY
+    assert run.cache.device_status() == 0            # the read cleared it
+    assert run.cache.seq_len.cpu().tolist() == [[32, 35]]
+    # a selection that is not ascending
+    q = torch.zeros((wl.batch, wl.num_kv_heads * wl.group_size, wl.head_dim), device="cuda")
+    sel = torch.full((wl.batch, wl.num_kv_heads, wl.K_blocks), -1, dtype=torch.int32, device="cuda")
+    sel[0, 0, 0] = 1
+    sel[0, 0, 1] = 0
+    run.cache.attend(0, q, sel)
+    assert run.cache.device_status() == 6            # COMPKV_ERR_BAD_SELECTION
+    # host-side validation: nothing is enqueued
+    with pytest.raises(P.CompKVError):
+        run.cache.attend(5, q, sel)
+    with pytest.raises(ValueError):
+        run.cache.attend(0, q[:, :1], sel)
