@@ -28,6 +28,8 @@ class CompKVCache:
         self.device = torch.device(device)
         if self.device.type != "cuda":
             raise RuntimeError("CompKVCache lives in GPU memory; the library has no CPU path")
+        if self.device.index is None:
+            self.device = torch.device("cuda", torch.cuda.current_device())
         caps = [capacity_tokens] * batch if isinstance(capacity_tokens, int) else list(capacity_tokens)
         self.cfg = C.make_config(num_layers, batch, num_kv_heads, group_size, head_dim, r,
                                  budget_tokens, capacity_tokens=caps)

@@ -25,7 +25,7 @@ compkv_status fail(compkv_status st, const char* fmt, ...) {
   return st;
 }
 
-constexpr int kMaxSelectBlocks = 49152;  // keys of one (sequence, head) held in shared memory
+constexpr size_t kMaxSmem = 232448;  // 227 KiB of shared memory per CTA
 
 struct Layout {
   std::vector<int> cap_blocks;
@@ -35,8 +35,10 @@ struct Layout {
   int total_chunks = 0;
   int max_cap_blocks = 0;
   int K = 0, splits = 0;
-  size_t off_status = 0, off_counter = 0, off_chunk_rec = 0, off_chunk_z = 0, off_chunk_u = 0, off_split = 0,
-         off_sel = 0, total = 0;
+  int units = 0, total_items = 0, region_bytes = 0;
+  std::vector<int> items;  // the fused kernel's work queue (unit-major)
+  size_t off_status = 0, off_queue = 0, off_bcount = 0, off_dcount = 0, off_ready = 0, off_items = 0,
+         off_chunk_rec = 0, off_chunk_z = 0, off_chunk_u = 0, off_split = 0, off_sel = 0, total = 0;
 };
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -64,8 +66,6 @@ compkv_status make_layout(const compkv_config* c, Layout* L) {
     const int cap = c->capacity_tokens ? c->capacity_tokens[s] : c->max_tokens;
     if (cap < kBlock || cap % kBlock)
       return fail(COMPKV_ERR_INVALID_ARG, "capacity of sequence %d must be a positive multiple of 16 (got %d)", s, cap);
-    if (cap / kBlock > kMaxSelectBlocks)
-      return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "capacity of sequence %d exceeds %d tokens", s, kMaxSelectBlocks * kBlock);
     L->cap_blocks[s] = cap / kBlock;
   }
   const int H = c->num_kv_heads, G = c->group_size, d = c->head_dim;
@@ -86,14 +86,42 @@ compkv_status make_layout(const compkv_config* c, Layout* L) {
   if (ch > (int64_t)1 << 30) return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "too many scoring work items");
   L->rows_per_layer = row;
   L->total_chunks = (int)ch;
+  if (fused_smem_bytes(d, c->r, G, L->max_cap_blocks) > kMaxSmem)
+    return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "a sequence capacity of %d blocks does not fit the selection in shared memory",
+                L->max_cap_blocks);
+  L->region_bytes = fused_region_bytes(d, c->r, G, L->max_cap_blocks);
   L->K = c->budget_tokens / kBlock;
-  L->splits = (L->K + kSplitBlocks - 1) / kSplitBlocks;
+  L->splits = (L->K + kAttendBlocks - 1) / kAttendBlocks;
+  L->units = c->batch * H;
+  // work queue: scoring items of unit u, then the attention items of unit u - 1
+  L->items.clear();
+  auto emit_score = [&](int u) {
+    const int s = u / H;
+    for (int ch = 0; ch < L->nchunk[s]; ++ch) L->items.push_back((u << 20) | ch);
+  };
+  auto emit_attend = [&](int u) {
+    for (int p = 0; p < L->splits; ++p) L->items.push_back((int)(0x80000000u | ((unsigned)u << 20) | (unsigned)p));
+  };
+  for (int u = 0; u < L->units; ++u) {
+    emit_score(u);
+    if (u >= 1) emit_attend(u - 1);
+  }
+  emit_attend(L->units - 1);
+  L->total_items = (int)L->items.size();
   const size_t rec = (size_t)G * (4 + d) * sizeof(float);
   size_t off = 0;
   L->off_status = off;
   off = round256(off + 16);
-  L->off_counter = off;
-  off = round256(off + (size_t)c->batch * H * sizeof(int));
+  L->off_queue = off;
+  off = round256(off + 2 * sizeof(int));
+  L->off_bcount = off;
+  off = round256(off + (size_t)L->units * sizeof(int));
+  L->off_dcount = off;
+  off = round256(off + (size_t)L->units * sizeof(int));
+  L->off_ready = off;
+  off = round256(off + (size_t)L->units * sizeof(int));
+  L->off_items = off;
+  off = round256(off + (size_t)L->total_items * sizeof(int));
   L->off_chunk_rec = off;
   off = round256(off + (size_t)L->total_chunks * rec);
   L->off_chunk_z = off;
@@ -123,6 +151,8 @@ struct compkv_ctx {
   compkv_buffers buf;
   Layout lay;
   int64_t launches = 0;
+  int epoch = 0;
+  int sms = 0;
   bool prof = false;
   ProfSlot slots[COMPKV_KERNEL_FAMILIES];
   std::vector<cudaEvent_t> pool;
@@ -159,7 +189,14 @@ LayerArgs base_args(const compkv_ctx* c, int layer) {
   a.len_add = 0;
   char* sc = reinterpret_cast<char*>(c->buf.scratch);
   a.status = reinterpret_cast<int*>(sc + c->lay.off_status);
-  a.head_counter = reinterpret_cast<int*>(sc + c->lay.off_counter);
+  a.items = reinterpret_cast<const int*>(sc + c->lay.off_items);
+  a.total_items = c->lay.total_items;
+  a.ticket = reinterpret_cast<int*>(sc + c->lay.off_queue);
+  a.done = a.ticket + 1;
+  a.bcount = reinterpret_cast<int*>(sc + c->lay.off_bcount);
+  a.dcount = reinterpret_cast<int*>(sc + c->lay.off_dcount);
+  a.ready = reinterpret_cast<int*>(sc + c->lay.off_ready);
+  a.region_bytes = c->lay.region_bytes;
   a.chunk_rec = reinterpret_cast<float*>(sc + c->lay.off_chunk_rec);
   a.chunk_z = reinterpret_cast<float*>(sc + c->lay.off_chunk_z);
   a.chunk_u = reinterpret_cast<float*>(sc + c->lay.off_chunk_u);
@@ -232,6 +269,11 @@ compkv_status launch(compkv_ctx* c, int family, cudaStream_t st, const char* wha
   return COMPKV_OK;
 }
 
+int fused_grid(const compkv_ctx* c) {
+  const int g = c->sms > 0 ? c->sms : 1;
+  return g < c->lay.total_items ? g : c->lay.total_items;
+}
+
 }  // namespace
 
 extern "C" {
@@ -271,10 +313,16 @@ compkv_status compkv_init(const compkv_config* cfg, const compkv_buffers* bufs, 
   c->buf = *bufs;
   c->lay = L;
   cudaError_t e = cudaMemsetAsync(bufs->scratch, 0, L.total, 0);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(reinterpret_cast<char*>(bufs->scratch) + L.off_items, L.items.data(),
+                        L.items.size() * sizeof(int), cudaMemcpyHostToDevice, 0);
   if (e == cudaSuccess) e = cudaStreamSynchronize(0);
+  int dev = 0;
+  if (e == cudaSuccess) e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) {
     delete c;
-    return cuda_status(e, "zeroing scratch");
+    return cuda_status(e, "initialising scratch");
   }
   *out = c;
   return COMPKV_OK;
@@ -329,10 +377,9 @@ compkv_status compkv_score_select(compkv_ctx* c, int layer, const float* q, int*
   a.scores = scores;
   a.score_stride = c->lay.max_cap_blocks;
   cudaStream_t st = (cudaStream_t)stream;
-  COMPKV_TRY(launch(c, COMPKV_KERNEL_SCORE, st, "score launch",
-                    [&] { return launch_score(a, kModeScore, c->lay.total_chunks, st); }));
-  COMPKV_TRY(launch(c, COMPKV_KERNEL_SELECT, st, "select launch",
-                    [&] { return launch_select(a, c->lay.max_cap_blocks, st); }));
+  a.epoch = ++c->epoch;
+  COMPKV_TRY(launch(c, COMPKV_KERNEL_SCORE, st, "score/select launch",
+                    [&] { return launch_fused(a, kFusedScoreSelect, fused_grid(c), st); }));
   return COMPKV_OK;
 }
 
@@ -346,9 +393,9 @@ compkv_status compkv_attend(compkv_ctx* c, int layer, const float* q, const int*
   a.sel = const_cast<int*>(sel);
   a.out = out;
   cudaStream_t st = (cudaStream_t)stream;
-  COMPKV_TRY(launch(c, COMPKV_KERNEL_SCORE, st, "score launch",
-                    [&] { return launch_score(a, kModeComp, c->lay.total_chunks, st); }));
-  COMPKV_TRY(launch(c, COMPKV_KERNEL_ATTEND, st, "attend launch", [&] { return launch_attend(a, st); }));
+  a.epoch = ++c->epoch;
+  COMPKV_TRY(launch(c, COMPKV_KERNEL_ATTEND, st, "attend launch",
+                    [&] { return launch_fused(a, kFusedAttend, fused_grid(c), st); }));
   return COMPKV_OK;
 }
 
@@ -367,12 +414,9 @@ compkv_status compkv_decode(compkv_ctx* c, int layer, const float* q, const void
   a.out = out;
   if (sel) a.sel = sel;
   cudaStream_t st = (cudaStream_t)stream;
-  COMPKV_TRY(launch(c, COMPKV_KERNEL_APPEND, st, "append launch", [&] { return launch_append(a, st); }));
-  COMPKV_TRY(launch(c, COMPKV_KERNEL_SCORE, st, "score launch",
-                    [&] { return launch_score(a, kModeScore | kModeComp, c->lay.total_chunks, st); }));
-  COMPKV_TRY(launch(c, COMPKV_KERNEL_SELECT, st, "select launch",
-                    [&] { return launch_select(a, c->lay.max_cap_blocks, st); }));
-  COMPKV_TRY(launch(c, COMPKV_KERNEL_ATTEND, st, "attend launch", [&] { return launch_attend(a, st); }));
+  a.epoch = ++c->epoch;
+  COMPKV_TRY(launch(c, COMPKV_KERNEL_DECODE, st, "decode launch",
+                    [&] { return launch_fused(a, kFusedDecode, fused_grid(c), st); }));
   return COMPKV_OK;
 }
 

@@ -14,7 +14,6 @@ namespace compkv {
 constexpr int kBlock = 16;        // tokens per KV block (CompKV, "전제와 한계": block size 16)
 constexpr int kMaxBatch = 64;     // sequences per call (launch arguments hold per-sequence tables)
 constexpr int kChunk = 64;        // blocks per scoring work item
-constexpr int kSplitBlocks = 8;   // selected blocks per attention work item
 constexpr int kMaxG = 8;
 
 // Device status word codes (mirrors compkv_status).
@@ -49,11 +48,20 @@ struct LayerArgs {
   int len_add;                // tokens to add to seq_len when reading it
   // scratch
   int* status;                // [4]: code, sequence, head, site
-  int* head_counter;          // [B*Hkv]
   float* chunk_rec;           // [total chunk records][G][4 + d]
   float* chunk_z;             // [total chunk records][G][kChunk]  zbar per block
   float* chunk_u;             // [total chunk records][G][kChunk]  exp(a - m_a) * sigma2
   float* split_rec;           // [B*Hkv*splits][G][4 + d]
+  // persistent work queue of the fused kernel
+  const int* items;           // [total_items] encoded work items (type | unit | index)
+  int total_items;
+  int* ticket;                // next ticket
+  int* done;                  // CTAs that have left the queue
+  int* bcount;                // [B*Hkv] scoring items finished, per unit
+  int* dcount;                // [B*Hkv] attention items finished, per unit
+  int* ready;                 // [B*Hkv] epoch at which the unit was scored and selected
+  int epoch;                  // launch counter of this context (> 0)
+  int region_bytes;           // per-stage shared-memory region
   // ragged tables
   int64_t seq_row0[kMaxBatch];   // first row of (s, head 0) relative to the layer
   int cap_blocks[kMaxBatch];     // capacity of sequence s in blocks
