@@ -53,6 +53,8 @@ _SIGNATURES = [
     ("compkv_score_select", c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
     ("compkv_attend", c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
     ("compkv_decode", c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    ("compkv_decode_static", c_int, [POINTER(compkv_config), POINTER(compkv_buffers), c_int, c_void_p, c_void_p,
+                                     c_void_p, c_void_p, c_void_p, c_void_p]),
     ("compkv_device_status", c_int, [c_void_p, c_void_p]),
     ("compkv_launch_count", c_int64, [c_void_p]),
     ("compkv_profile_enable", c_int, [c_void_p, c_int]),
@@ -150,6 +152,16 @@ def compkv_attend(ctx, layer, q, sel, out, stream):
 
 def compkv_decode(ctx, layer, q, k_new, v_new, out, sel, stream):
     _check(lib().compkv_decode(ctx, layer, q, k_new, v_new, out, sel, stream), "compkv_decode")
+
+
+COMPKV_STATIC_SCRATCH_BYTES = 16 << 20
+
+
+def compkv_decode_static(cfg, bufs, layer, q, k_new, v_new, out, sel, stream):
+    """compkv_decode without a context, on the library's own static scratch
+    (bufs.scratch is ignored); see include/compkv.h."""
+    _check(lib().compkv_decode_static(ctypes.byref(cfg), ctypes.byref(bufs), layer, q, k_new, v_new, out, sel,
+                                      stream), "compkv_decode_static")
 
 
 def compkv_device_status(ctx, stream) -> int:

@@ -482,3 +482,64 @@ const char* compkv_status_string(compkv_status s) {
 void compkv_destroy(compkv_ctx* c) { delete c; }
 
 }  // extern "C"
+
+// Records `what: detail` as this thread's last error (for other translation units).
+compkv_status compkv_internal_fail(compkv_status st, const char* what, const char* detail) {
+  return fail(st, "%s: %s", what, detail);
+}
+
+// Decode step with a scratch buffer supplied by the caller of this function
+// instead of by a context: used by the scratch-free entry point
+// (static_scratch.cu).  The queue, counters and status at the start of the
+// scratch are zeroed and the work queue is uploaded on `stream` before the
+// launch, so consecutive calls that share the buffer start clean.
+compkv_status compkv_internal_decode_in(const compkv_config* cfg, const compkv_buffers* bufs, void* scratch,
+                                        size_t scratch_bytes, int layer, const float* q, const void* k_new,
+                                        const void* v_new, float* out, int* sel, void* stream) {
+  g_last_error[0] = 0;
+  Layout L;
+  COMPKV_TRY(make_layout(cfg, &L));
+  if (L.total > scratch_bytes)
+    return fail(COMPKV_ERR_UNSUPPORTED_SHAPE,
+                "this configuration needs %zu bytes of scratch; the library's static scratch holds %zu", L.total,
+                scratch_bytes);
+  if (!bufs) return fail(COMPKV_ERR_INVALID_ARG, "buffers are NULL");
+  if (layer < 0 || layer >= cfg->num_layers)
+    return fail(COMPKV_ERR_INVALID_ARG, "layer %d out of range [0, %d)", layer, cfg->num_layers);
+  COMPKV_TRY(check_ptr(bufs->k, "k", 16));
+  COMPKV_TRY(check_ptr(bufs->v, "v", 16));
+  COMPKV_TRY(check_ptr(bufs->kbar, "kbar", 16));
+  COMPKV_TRY(check_ptr(bufs->vbar, "vbar", 16));
+  COMPKV_TRY(check_ptr(bufs->dbar, "dbar", 16));
+  COMPKV_TRY(check_ptr(bufs->seq_len, "seq_len", 4));
+  COMPKV_TRY(check_ptr(scratch, "scratch", 256));
+  COMPKV_TRY(check_ptr(q, "q", 16));
+  COMPKV_TRY(check_ptr(k_new, "k_new", 16));
+  COMPKV_TRY(check_ptr(v_new, "v_new", 16));
+  COMPKV_TRY(check_ptr(out, "out", 16));
+  if (sel) COMPKV_TRY(check_ptr(sel, "sel", 16));
+  compkv_ctx c;
+  c.cfg = *cfg;
+  c.cfg.capacity_tokens = nullptr;
+  c.buf = *bufs;
+  c.buf.scratch = scratch;
+  c.buf.scratch_bytes = scratch_bytes;
+  c.lay = L;
+  int dev = 0;
+  COMPKV_TRY(cuda_status(cudaGetDevice(&dev), "cudaGetDevice"));
+  COMPKV_TRY(cuda_status(cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev), "SM count"));
+  cudaStream_t st = (cudaStream_t)stream;
+  COMPKV_TRY(cuda_status(cudaMemsetAsync(scratch, 0, L.off_items, st), "clearing scratch"));
+  COMPKV_TRY(cuda_status(cudaMemcpyAsync(reinterpret_cast<char*>(scratch) + L.off_items, L.items.data(),
+                                         L.items.size() * sizeof(int), cudaMemcpyHostToDevice, st),
+                         "uploading the work queue"));
+  LayerArgs a = base_args(&c, layer);
+  a.q = q;
+  a.k_new = reinterpret_cast<const __nv_bfloat16*>(k_new);
+  a.v_new = reinterpret_cast<const __nv_bfloat16*>(v_new);
+  a.out = out;
+  if (sel) a.sel = sel;
+  a.epoch = 1;  // the ready tags were just cleared
+  COMPKV_TRY(cuda_status(launch_fused(a, kFusedDecode, fused_grid(&c), st), "decode launch"));
+  return COMPKV_OK;
+}

@@ -163,6 +163,32 @@ compkv_status compkv_attend(compkv_ctx *ctx, int layer, const float *q, const in
 compkv_status compkv_decode(compkv_ctx *ctx, int layer, const float *q, const void *k_new,
                             const void *v_new, float *out, int *sel, void *stream);
 
+/* Scratch-free decode step.  The CompKV page has no counterpart to this call;
+ * it exists for callers that cannot allocate device memory at the time they
+ * decode (an engine that reserved the whole GPU for its cache pool at
+ * start-up and hands plug-ins no allocator, code under a hard memory budget
+ * where a new allocation would fail or synchronise the device, or a host
+ * application that owns the CUDA context and forbids its plug-ins to
+ * allocate).  It does exactly what compkv_decode does for `layer`, without a
+ * context: `cfg` and `bufs` are as for compkv_init, except that bufs->scratch
+ * and bufs->scratch_bytes are ignored.  The scratch is instead a device array
+ * of COMPKV_STATIC_SCRATCH_BYTES (16 MiB) inside the library, which every GPU
+ * that loads the library holds until the process exits.  A configuration
+ * whose compkv_scratch_bytes() exceeds that size is rejected with
+ * COMPKV_ERR_UNSUPPORTED_SHAPE and a message naming both sizes.  The call
+ * allocates nothing; it enqueues a clear of the array's counters, a copy of
+ * its work queue and the kernel on `stream`.  The first call on each device
+ * (with that device current) looks up the array's device address once; make
+ * that first call before any stream capture.  All calls share the one array,
+ * so calls whose work overlaps on the GPU (different streams, or several host
+ * threads) race and corrupt each other: order them on one stream.  Its
+ * device-side checks (a sequence at capacity) have no status read-back:
+ * check capacities on the host.  Returns host-side errors like compkv_decode. */
+#define COMPKV_STATIC_SCRATCH_BYTES (16u << 20)
+compkv_status compkv_decode_static(const compkv_config *cfg, const compkv_buffers *bufs, int layer,
+                                   const float *q, const void *k_new, const void *v_new, float *out,
+                                   int *sel, void *stream);
+
 /* Synchronise `stream`, read and clear the device status word.  Returns
  * COMPKV_OK or the first device-side error since the last call. */
 compkv_status compkv_device_status(compkv_ctx *ctx, void *stream);
