@@ -35,10 +35,11 @@ struct Layout {
   int total_chunks = 0;
   int max_cap_blocks = 0;
   int K = 0, splits = 0;
-  int units = 0, total_items = 0, region_bytes = 0;
-  std::vector<int> items;  // the fused kernel's work queue (unit-major)
-  size_t off_status = 0, off_queue = 0, off_bcount = 0, off_dcount = 0, off_ready = 0, off_items = 0,
-         off_chunk_rec = 0, off_chunk_z = 0, off_chunk_u = 0, off_split = 0, off_sel = 0, total = 0;
+  int units = 0, total_items = 0, phase1_items = 0, region_bytes = 0, stages = 0, bm_words = 0;
+  std::vector<int> items;  // the fused kernel's work queue
+  size_t off_status = 0, off_queue = 0, off_s1count = 0, off_mcount = 0, off_ready = 0, off_items = 0,
+         off_chunk_rec = 0, off_chunk_z = 0, off_chunk_u = 0, off_split = 0, off_unit_ref = 0, off_unit_acc = 0,
+         off_unit_nsel = 0, off_bitmap = 0, off_sel = 0, total = 0;
 };
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -86,52 +87,48 @@ compkv_status make_layout(const compkv_config* c, Layout* L) {
   if (ch > (int64_t)1 << 30) return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "too many scoring work items");
   L->rows_per_layer = row;
   L->total_chunks = (int)ch;
-  if (fused_smem_bytes(d, c->r, G, L->max_cap_blocks) > kMaxSmem)
+  L->stages = fused_stages(d, c->r, G, L->max_cap_blocks, kMaxSmem);
+  if (fused_smem_bytes(d, c->r, G, L->max_cap_blocks, L->stages) > kMaxSmem)
     return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "a sequence capacity of %d blocks does not fit the selection in shared memory",
                 L->max_cap_blocks);
   L->region_bytes = fused_region_bytes(d, c->r, G, L->max_cap_blocks);
   L->K = c->budget_tokens / kBlock;
   L->splits = (L->K + kAttendBlocks - 1) / kAttendBlocks;
   L->units = c->batch * H;
-  // work queue: scoring items of unit u, then the attention items of unit u - 1
+  L->bm_words = (L->max_cap_blocks + 31) / 32;
+  // work queue: phase 1 = every unit's scoring items; phase 2 = per unit its
+  // attention items, then its compensation items.  Code: type | unit | index.
   L->items.clear();
-  auto emit_score = [&](int u) {
-    const int s = u / H;
-    for (int ch = 0; ch < L->nchunk[s]; ++ch) L->items.push_back((u << 20) | ch);
-  };
-  auto emit_attend = [&](int u) {
-    for (int p = 0; p < L->splits; ++p) L->items.push_back((int)(0x80000000u | ((unsigned)u << 20) | (unsigned)p));
-  };
+  auto code = [](unsigned type, unsigned u, unsigned index) { return (int)((type << 30) | (u << 18) | index); };
+  for (int u = 0; u < L->units; ++u)
+    for (int ch = 0; ch < L->nchunk[u / H]; ++ch) L->items.push_back(code(0, u, ch));
+  L->phase1_items = (int)L->items.size();
   for (int u = 0; u < L->units; ++u) {
-    emit_score(u);
-    if (u >= 1) emit_attend(u - 1);
+    for (int p = 0; p < L->splits; ++p) L->items.push_back(code(1, u, p));
+    const int n2 = (L->cap_blocks[u / H] + kChunk2 - 1) / kChunk2;
+    for (int ch = 0; ch < n2; ++ch) L->items.push_back(code(2, u, ch));
   }
-  emit_attend(L->units - 1);
   L->total_items = (int)L->items.size();
-  const size_t rec = (size_t)G * (4 + d) * sizeof(float);
   size_t off = 0;
-  L->off_status = off;
-  off = round256(off + 16);
-  L->off_queue = off;
-  off = round256(off + 2 * sizeof(int));
-  L->off_bcount = off;
-  off = round256(off + (size_t)L->units * sizeof(int));
-  L->off_dcount = off;
-  off = round256(off + (size_t)L->units * sizeof(int));
-  L->off_ready = off;
-  off = round256(off + (size_t)L->units * sizeof(int));
-  L->off_items = off;
-  off = round256(off + (size_t)L->total_items * sizeof(int));
-  L->off_chunk_rec = off;
-  off = round256(off + (size_t)L->total_chunks * rec);
-  L->off_chunk_z = off;
-  off = round256(off + (size_t)L->total_chunks * G * kChunk * sizeof(float));
-  L->off_chunk_u = off;
-  off = round256(off + (size_t)L->total_chunks * G * kChunk * sizeof(float));
-  L->off_split = off;
-  off = round256(off + (size_t)c->batch * H * L->splits * rec);
-  L->off_sel = off;
-  off = round256(off + (size_t)c->batch * H * L->K * sizeof(int));
+  auto region = [&](size_t* o, size_t bytes) {
+    *o = off;
+    off = round256(off + bytes);
+  };
+  region(&L->off_status, 16);
+  region(&L->off_queue, 2 * sizeof(int));
+  region(&L->off_s1count, (size_t)L->units * sizeof(int));
+  region(&L->off_mcount, (size_t)L->units * sizeof(int));
+  region(&L->off_ready, (size_t)L->units * sizeof(int));
+  region(&L->off_items, (size_t)L->total_items * sizeof(int));  // everything before is zeroed per fresh start
+  region(&L->off_chunk_rec, (size_t)L->total_chunks * G * 4 * sizeof(float));
+  region(&L->off_chunk_z, (size_t)L->total_chunks * G * kChunk * sizeof(float));
+  region(&L->off_chunk_u, (size_t)L->total_chunks * G * kChunk * sizeof(float));
+  region(&L->off_split, (size_t)L->units * L->splits * G * (4 + d) * sizeof(float));
+  region(&L->off_unit_ref, (size_t)L->units * G * sizeof(float));
+  region(&L->off_unit_acc, (size_t)L->units * G * (d + 4) * sizeof(float));
+  region(&L->off_unit_nsel, (size_t)L->units * sizeof(int));
+  region(&L->off_bitmap, (size_t)L->units * L->bm_words * sizeof(unsigned));
+  region(&L->off_sel, (size_t)L->units * L->K * sizeof(int));
   L->total = off;
   return COMPKV_OK;
 }
@@ -186,21 +183,26 @@ LayerArgs base_args(const compkv_ctx* c, int layer) {
   a.r = r;
   a.K = c->lay.K;
   a.splits = c->lay.splits;
-  a.len_add = 0;
   char* sc = reinterpret_cast<char*>(c->buf.scratch);
   a.status = reinterpret_cast<int*>(sc + c->lay.off_status);
   a.items = reinterpret_cast<const int*>(sc + c->lay.off_items);
   a.total_items = c->lay.total_items;
   a.ticket = reinterpret_cast<int*>(sc + c->lay.off_queue);
   a.done = a.ticket + 1;
-  a.bcount = reinterpret_cast<int*>(sc + c->lay.off_bcount);
-  a.dcount = reinterpret_cast<int*>(sc + c->lay.off_dcount);
+  a.s1count = reinterpret_cast<int*>(sc + c->lay.off_s1count);
+  a.mcount = reinterpret_cast<int*>(sc + c->lay.off_mcount);
   a.ready = reinterpret_cast<int*>(sc + c->lay.off_ready);
   a.region_bytes = c->lay.region_bytes;
+  a.stages = c->lay.stages;
   a.chunk_rec = reinterpret_cast<float*>(sc + c->lay.off_chunk_rec);
   a.chunk_z = reinterpret_cast<float*>(sc + c->lay.off_chunk_z);
   a.chunk_u = reinterpret_cast<float*>(sc + c->lay.off_chunk_u);
   a.split_rec = reinterpret_cast<float*>(sc + c->lay.off_split);
+  a.unit_ref = reinterpret_cast<float*>(sc + c->lay.off_unit_ref);
+  a.unit_acc = reinterpret_cast<float*>(sc + c->lay.off_unit_acc);
+  a.unit_nsel = reinterpret_cast<int*>(sc + c->lay.off_unit_nsel);
+  a.bitmap = reinterpret_cast<unsigned*>(sc + c->lay.off_bitmap);
+  a.bm_words = c->lay.bm_words;
   a.sel = reinterpret_cast<int*>(sc + c->lay.off_sel);
   for (int s = 0; s < c->cfg.batch; ++s) {
     a.seq_row0[s] = c->lay.seq_row0[s];
@@ -378,6 +380,7 @@ compkv_status compkv_score_select(compkv_ctx* c, int layer, const float* q, int*
   a.score_stride = c->lay.max_cap_blocks;
   cudaStream_t st = (cudaStream_t)stream;
   a.epoch = ++c->epoch;
+  a.total_items = c->lay.phase1_items;
   COMPKV_TRY(launch(c, COMPKV_KERNEL_SCORE, st, "score/select launch",
                     [&] { return launch_fused(a, kFusedScoreSelect, fused_grid(c), st); }));
   return COMPKV_OK;

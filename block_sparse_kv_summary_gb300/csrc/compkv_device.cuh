@@ -13,7 +13,8 @@ namespace compkv {
 
 constexpr int kBlock = 16;        // tokens per KV block (CompKV, "전제와 한계": block size 16)
 constexpr int kMaxBatch = 64;     // sequences per call (launch arguments hold per-sequence tables)
-constexpr int kChunk = 64;        // blocks per scoring work item
+constexpr int kChunk = 64;        // blocks per scoring work item (and per scoring record)
+constexpr int kChunk2 = 128;      // blocks per compensation work item
 constexpr int kMaxG = 8;
 
 // Device status word codes (mirrors compkv_status).
@@ -44,24 +45,29 @@ struct LayerArgs {
   int score_stride;
   // shape
   int B, Hkv, G, d, r, K;
-  int splits;                 // attention work items per (sequence, head)
-  int len_add;                // tokens to add to seq_len when reading it
+  int splits;                 // attention work items per unit (sequence, head)
   // scratch
   int* status;                // [4]: code, sequence, head, site
-  float* chunk_rec;           // [total chunk records][G][4 + d]
-  float* chunk_z;             // [total chunk records][G][kChunk]  zbar per block
-  float* chunk_u;             // [total chunk records][G][kChunk]  exp(a - m_a) * sigma2
-  float* split_rec;           // [B*Hkv*splits][G][4 + d]
+  float* chunk_rec;           // [chunk records][G][4]: max a, sum e^(a - max a), max(ln|b| + zbar), -
+  float* chunk_z;             // [chunk records][G][kChunk]  zbar per block
+  float* chunk_u;             // [chunk records][G][kChunk]  e^(a - max a) * sigma2 per block
+  float* split_rec;           // [units][splits][G][4 + d]: m, l, -, -, acc[d]
+  float* unit_ref;            // [units][G]  reference exponent of the compensation weights
+  float* unit_acc;            // [units][G][d + 4]: sum_b w vbar_b, then sum_b w at [d]
+  int* unit_nsel;             // [units] selected blocks
+  unsigned* bitmap;           // [units][bm_words] selected-block bitmap
+  int bm_words;
   // persistent work queue of the fused kernel
-  const int* items;           // [total_items] encoded work items (type | unit | index)
-  int total_items;
+  const int* items;           // encoded work items (type | unit | index)
+  int total_items;            // items of this launch (a prefix of the queue)
   int* ticket;                // next ticket
   int* done;                  // CTAs that have left the queue
-  int* bcount;                // [B*Hkv] scoring items finished, per unit
-  int* dcount;                // [B*Hkv] attention items finished, per unit
-  int* ready;                 // [B*Hkv] epoch at which the unit was scored and selected
+  int* s1count;               // [units] scoring items finished
+  int* mcount;                // [units] attention + compensation items finished
+  int* ready;                 // [units] epoch at which the unit was selected
   int epoch;                  // launch counter of this context (> 0)
   int region_bytes;           // per-stage shared-memory region
+  int stages;                 // 2 or 3
   // ragged tables
   int64_t seq_row0[kMaxBatch];   // first row of (s, head 0) relative to the layer
   int cap_blocks[kMaxBatch];     // capacity of sequence s in blocks
@@ -73,7 +79,6 @@ struct LayerArgs {
 __device__ __forceinline__ int64_t row_of(const LayerArgs& a, int s, int h, int b) {
   return a.seq_row0[s] + (int64_t)h * a.cap_blocks[s] + b;
 }
-__device__ __forceinline__ int rec_stride(const LayerArgs& a) { return a.G * (4 + a.d); }
 
 // ---------------------------------------------------------------- status
 __device__ __forceinline__ void set_error(int* status, int code, int s, int h, int site) {
@@ -177,17 +182,6 @@ __device__ __forceinline__ void store_bf16_raw<2>(__nv_bfloat16* dst, const __nv
   *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(src);
 }
 
-// Tokens held by sequence s in this call.  seq_len is caller memory: a value
-// outside [0, capacity] is reported and clamped so no access leaves the rows.
-__device__ __forceinline__ int seq_tokens(const LayerArgs& a, int s) {
-  int L = a.seq_len[s] + a.len_add;
-  const int cap = a.cap_blocks[s] * kBlock;
-  if (L < 0 || L > cap) {
-    set_error(a.status, kDevCapacity, s, -1, 2);
-    L = L < 0 ? 0 : cap;
-  }
-  return L;
-}
 __device__ __forceinline__ int ceil_blocks(int L) { return (L + kBlock - 1) / kBlock; }
 
 }  // namespace compkv

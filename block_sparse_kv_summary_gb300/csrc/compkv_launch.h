@@ -26,6 +26,7 @@ cudaError_t launch_append(const LayerArgs& a, cudaStream_t st);
 cudaError_t launch_fused(const LayerArgs& a, int mode, int grid, cudaStream_t st);
 
 int fused_region_bytes(int D, int r, int G, int max_cap_blocks);
-size_t fused_smem_bytes(int D, int r, int G, int max_cap_blocks);
+int fused_stages(int D, int r, int G, int max_cap_blocks, size_t smem_limit);
+size_t fused_smem_bytes(int D, int r, int G, int max_cap_blocks, int stages);
 
 }  // namespace compkv
