@@ -58,6 +58,7 @@ _SIGNATURES = [
     ("compkv_device_status", c_int, [c_void_p, c_void_p]),
     ("compkv_launch_count", c_int64, [c_void_p]),
     ("compkv_profile_enable", c_int, [c_void_p, c_int]),
+    ("compkv_trace", c_int, [c_void_p, c_void_p, c_size_t]),
     ("compkv_profile_read", c_int, [c_void_p, c_int, POINTER(ctypes.c_double), POINTER(c_int64)]),
     ("compkv_last_error", c_char_p, []),
     ("compkv_status_string", c_char_p, [c_int]),
@@ -186,6 +187,11 @@ def compkv_profile_read(ctx, family):
     ms, n = ctypes.c_double(), c_int64()
     _check(lib().compkv_profile_read(ctx, fam, ctypes.byref(ms), ctypes.byref(n)), "compkv_profile_read")
     return ms.value, n.value
+
+
+def compkv_trace(ctx, buf, nbytes):
+    """Record the fused kernel's work items into device buffer `buf` (0: off)."""
+    _check(lib().compkv_trace(ctx, buf, nbytes), "compkv_trace")
 
 
 def compkv_destroy(ctx):

@@ -150,6 +150,8 @@ struct compkv_ctx {
   int64_t launches = 0;
   int epoch = 0;
   int sms = 0;
+  unsigned long long* trace = nullptr;
+  int trace_cap = 0;
   bool prof = false;
   ProfSlot slots[COMPKV_KERNEL_FAMILIES];
   std::vector<cudaEvent_t> pool;
@@ -193,6 +195,8 @@ LayerArgs base_args(const compkv_ctx* c, int layer) {
   a.mcount = reinterpret_cast<int*>(sc + c->lay.off_mcount);
   a.ready = reinterpret_cast<int*>(sc + c->lay.off_ready);
   a.region_bytes = c->lay.region_bytes;
+  a.trace = c->trace;
+  a.trace_cap = c->trace_cap;
   a.stages = c->lay.stages;
   a.chunk_rec = reinterpret_cast<float*>(sc + c->lay.off_chunk_rec);
   a.chunk_z = reinterpret_cast<float*>(sc + c->lay.off_chunk_z);
@@ -438,6 +442,21 @@ compkv_status compkv_device_status(compkv_ctx* c, void* stream) {
 }
 
 int64_t compkv_launch_count(const compkv_ctx* c) { return c ? c->launches : 0; }
+
+compkv_status compkv_trace(compkv_ctx* c, void* buf, size_t bytes) {
+  if (!c) return fail(COMPKV_ERR_INVALID_ARG, "context is NULL");
+  if (!buf) {
+    c->trace = nullptr;
+    c->trace_cap = 0;
+    return COMPKV_OK;
+  }
+  COMPKV_TRY(check_ptr(buf, "trace buffer", 8));
+  if (bytes < 8 + 40) return fail(COMPKV_ERR_INVALID_ARG, "trace buffer of %zu bytes holds no record", bytes);
+  c->trace = reinterpret_cast<unsigned long long*>(buf);
+  const size_t cap = (bytes - 8) / 40;
+  c->trace_cap = cap > 0x7fffffff ? 0x7fffffff : (int)cap;
+  return COMPKV_OK;
+}
 
 compkv_status compkv_profile_enable(compkv_ctx* c, int enable) {
   if (!c) return fail(COMPKV_ERR_INVALID_ARG, "context is NULL");

@@ -68,6 +68,9 @@ struct LayerArgs {
   int epoch;                  // launch counter of this context (> 0)
   int region_bytes;           // per-stage shared-memory region
   int stages;                 // 2 or 3
+  // optional trace of the fused kernel's work items (null: off)
+  unsigned long long* trace;  // [0] = records written, then records of 5 words
+  int trace_cap;              // records that fit
   // ragged tables
   int64_t seq_row0[kMaxBatch];   // first row of (s, head 0) relative to the layer
   int cap_blocks[kMaxBatch];     // capacity of sequence s in blocks
@@ -78,6 +81,27 @@ struct LayerArgs {
 
 __device__ __forceinline__ int64_t row_of(const LayerArgs& a, int s, int h, int b) {
   return a.seq_row0[s] + (int64_t)h * a.cap_blocks[s] + b;
+}
+
+// ---------------------------------------------------------------- tracing
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// One trace record: (cta << 32 | type << 24 | index), unit, t0, t1, t2 (ns).
+__device__ __forceinline__ void trace_record(const LayerArgs& a, int type, int unit, int index, unsigned long long t0,
+                                             unsigned long long t1, unsigned long long t2) {
+  if (!a.trace) return;
+  const unsigned long long i = atomicAdd(a.trace, 1ull);
+  if (i >= (unsigned long long)a.trace_cap) return;
+  unsigned long long* r = a.trace + 1 + 5 * i;
+  r[0] = ((unsigned long long)blockIdx.x << 32) | ((unsigned long long)(type & 0xff) << 24) | (unsigned)(index & 0xffffff);
+  r[1] = (unsigned long long)unit;
+  r[2] = t0;
+  r[3] = t1;
+  r[4] = t2;
 }
 
 // ---------------------------------------------------------------- status

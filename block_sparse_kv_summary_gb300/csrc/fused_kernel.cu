@@ -52,8 +52,9 @@ constexpr int kCW = kAttendBlocks;       // consumer warps (one selected block e
 constexpr int kCT = kCW * 32;            // consumer threads
 constexpr int kFusedThreads = kCT + 32;  // + the producer warp
 constexpr int kMaxStages = 3;
-constexpr int kBins = 2048;
-constexpr int kListCap = 512;
+constexpr int kBins = 4096;     // shared histogram of the radix select
+constexpr int kPrivBins = 256;  // per-warp histogram of its first (exponent) digit
+constexpr int kRankCap = 128;   // a threshold digit holding at most this many keys is ranked directly
 // queue item types (bits 31:30 of an item code) and extra slot types
 constexpr int kItemScore = 0, kItemAttend = 1, kItemComp = 2;
 constexpr int kSlotSelect = 3, kSlotMerge = 4, kSlotEnd = 5;
@@ -66,12 +67,15 @@ struct Slot {
 // ------------------------------------------------------------------ layout
 __host__ __device__ inline int align_up(int x, int a) { return (x + a - 1) / a * a; }
 
-__host__ __device__ inline int fused_score_bytes(int D, int r) { return kChunk * (D + r) * 4 + D * 4; }
+// scoring item region: kbar rows | Dbar rows | q of the unit (G x D) | the new block's vbar
+__host__ __device__ inline int fused_score_bytes(int D, int r, int G) { return kChunk * (D + r) * 4 + G * D * 4 + D * 4; }
 __host__ __device__ inline int fused_comp_bytes(int D) { return kChunk2 * D * 4; }
+// select scratch: keys | hist | per-warp hist | rank list (key, index) | item factors | bitmap words | word bases
 __host__ __device__ inline int fused_select_bytes(int max_cap_blocks, int G) {
   const int nch = (max_cap_blocks + kChunk - 1) / kChunk;
-  return align_up(max_cap_blocks, 4) * 4 + kBins * 4 + kListCap * 8 + align_up(nch * G, 4) * 4 +
-         align_up((max_cap_blocks + 31) / 32, 4) * 4;
+  const int words = align_up((max_cap_blocks + 31) / 32, 4);
+  return align_up(max_cap_blocks, 4) * 4 + kBins * 4 + kCW * kPrivBins * 4 + kRankCap * 8 +
+         align_up(nch * G, 4) * 4 + 2 * words * 4;
 }
 __host__ __device__ inline int fused_merge_bytes(int D, int G) { return kCW * G * (D + 2) * 4; }
 
@@ -107,7 +111,7 @@ __host__ __device__ inline FusedSmem fused_layout(int D, int r, int G, int regio
 }
 
 int fused_region_bytes(int D, int r, int G, int max_cap_blocks) {
-  int R = fused_score_bytes(D, r);
+  int R = fused_score_bytes(D, r, G);
   const int c = fused_comp_bytes(D), s = fused_select_bytes(max_cap_blocks, G), m = fused_merge_bytes(D, G);
   R = R > c ? R : c;
   R = R > s ? R : s;
@@ -126,7 +130,7 @@ size_t fused_smem_bytes(int D, int r, int G, int max_cap_blocks, int stages) {
 
 // misc ints in shared memory
 enum Misc { kMFlag = 0, kMCount = 1, kMDigit = 2, kMAbove = 3, kMList = 4, kMBad = 5, kMScan = 8 /* 17 ints */,
-            kMLse = 32 /* 8 floats */, kMRef = 40 /* 8 floats */ };
+            kMLse = 32 /* 8 floats */, kMRef = 40 /* 8 floats */, kMWaitT = 48 /* 2 ints */ };
 
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kCT) : "memory"); }
 
@@ -219,8 +223,25 @@ __device__ __forceinline__ bool wait_ready(const LayerArgs& a, int unit, int* mi
   consumer_sync();
   const bool ok = misc[kMFlag] == 0;
   consumer_sync();
+  if (threadIdx.x == 0) reinterpret_cast<unsigned long long*>(misc + kMWaitT)[0] = global_ns();
   return ok;
 }
+
+// Optional sub-phase markers for timing studies (compiled in only with
+// -DCOMPKV_TRACE_PHASES; they need a trace buffer set with compkv_trace).
+#ifdef COMPKV_TRACE_PHASES
+#define COMPKV_PHASE(a, id, unit)                                                           \
+  do {                                                                                      \
+    if (threadIdx.x == 0) {                                                                 \
+      const unsigned long long _t = global_ns();                                            \
+      trace_record((a), 32 + (id), (unit), 0, _t, _t, _t);                                  \
+    }                                                                                       \
+  } while (0)
+#else
+#define COMPKV_PHASE(a, id, unit) \
+  do {                            \
+  } while (0)
+#endif
 
 // ================================================================== producer
 template <int D, int G, int MODE>
@@ -286,15 +307,20 @@ __device__ void producer(const LayerArgs& a, unsigned char* sm, const FusedSmem&
     uint32_t bytes = 0;
     const int s = sl.unit / a.Hkv, h = sl.unit % a.Hkv;
     const bool dbar_bulk = (MODE & kFScore) && ((a.r & 3) == 0);
-    if (sl.type == kItemScore && sl.nt > 0)
-      bytes = (uint32_t)sl.nt * D * 4u + (dbar_bulk ? (uint32_t)sl.nt * a.r * 4u : 0u);
+    if (sl.type == kItemScore && sl.nb > 0)
+      bytes = (uint32_t)sl.nt * D * 4u + (dbar_bulk ? (uint32_t)sl.nt * a.r * 4u : 0u) + (uint32_t)G * D * 4u;
     if (sl.type == kItemComp && sl.nt > 0) bytes = (uint32_t)sl.nt * D * 4u;
     mbar_arrive_expect_tx(&full[st], bytes);
     if (bytes) {
       const int64_t row0 = row_of(a, s, h, sl.b0);
       if (sl.type == kItemScore) {
-        bulk_g2s(region, a.kbar + row0 * D, (uint32_t)sl.nt * D * 4u, &full[st]);
-        if (dbar_bulk) bulk_g2s(region + kChunk * D * 4, a.dbar + row0 * a.r, (uint32_t)sl.nt * a.r * 4u, &full[st]);
+        if (sl.nt > 0) {
+          bulk_g2s(region, a.kbar + row0 * D, (uint32_t)sl.nt * D * 4u, &full[st]);
+          if (dbar_bulk)
+            bulk_g2s(region + kChunk * D * 4, a.dbar + row0 * a.r, (uint32_t)sl.nt * a.r * 4u, &full[st]);
+        }
+        bulk_g2s(region + kChunk * (D + a.r) * 4, a.q + ((int64_t)s * a.Hkv * G + (int64_t)h * G) * D,
+                 (uint32_t)G * D * 4u, &full[st]);
       } else {
         bulk_g2s(region, a.vbar + row0 * D, (uint32_t)sl.nt * D * 4u, &full[st]);
       }
@@ -316,6 +342,10 @@ __device__ void producer(const LayerArgs& a, unsigned char* sm, const FusedSmem&
       pub_type[sk] = -1;
     }
   };
+  // a SELECT queued in this ring: no new tickets are claimed until it has run,
+  // so the CTA does not sit on other units' items while it selects
+  int sel_st = -1;
+  uint32_t sel_use = 0;
   auto pop_follow = [&]() {
     const Slot sl = make_slot(fq_type[0], fq_unit[0], 0);
     for (int i = 1; i < fq_n; ++i) {
@@ -323,16 +353,26 @@ __device__ void producer(const LayerArgs& a, unsigned char* sm, const FusedSmem&
       fq_unit[i - 1] = fq_unit[i];
     }
     --fq_n;
+    if (sl.type == kSlotSelect) {
+      sel_st = st;
+      sel_use = uses[st];
+    }
     publish(sl);
   };
 
   bool drained = false;
-  int t = atomicAdd(a.ticket, 1);
+  int t = -1;
   for (;;) {
     if (fq_n > 0) {
       pop_follow();
       continue;
     }
+    if (sel_st >= 0) {
+      mbar_wait_bounded(&empty[sel_st], sel_use & 1, a.status, -1, -1, 44);
+      sel_st = -1;
+    }
+    const unsigned long long tp0 = a.trace ? global_ns() : 0ull;
+    if (t < 0) t = atomicAdd(a.ticket, 1);
     if (t >= a.total_items) break;
     const int code = __ldg(a.items + t);
     const int type = (code >> 30) & 3, u = (code >> 18) & 0xfff, index = code & 0x3ffff;
@@ -341,10 +381,9 @@ __device__ void producer(const LayerArgs& a, unsigned char* sm, const FusedSmem&
       drained = true;
       continue;
     }
-    const Slot sl = make_slot(type, u, index);
-    const int t_next = atomicAdd(a.ticket, 1);
-    publish(sl);
-    t = t_next;
+    publish(make_slot(type, u, index));
+    if (a.trace) trace_record(a, 16 + type, u, index, tp0, tp0, global_ns());
+    t = -1;
   }
   for (;;) {
     drain();
@@ -352,6 +391,35 @@ __device__ void producer(const LayerArgs& a, unsigned char* sm, const FusedSmem&
     while (fq_n > 0) pop_follow();
   }
   publish(make_slot(kSlotEnd, 0, 0));
+}
+
+// Sum of NVAL values over the LPB lanes of a lane group (LPB a power of two,
+// NVAL <= LPB): halving steps exchange half of the values, the remaining
+// steps add.  On return the lane holds the total of value index `idx`; lanes
+// whose `j` is a multiple of LPB / NVAL hold each index exactly once.
+template <int NVAL, int LPB>
+__device__ __forceinline__ float transpose_reduce_lanes(float (&v)[NVAL], int j, int& idx) {
+  int c = NVAL;
+  idx = 0;
+#pragma unroll
+  for (int off = LPB / 2; off > 0; off >>= 1) {
+    if (c > 1) {
+      const bool up = (j & off) != 0;
+#pragma unroll
+      for (int i = 0; i < NVAL / 2; ++i) {
+        if (i < c / 2) {
+          const float send = up ? v[i] : v[i + c / 2];
+          const float keep = up ? v[i + c / 2] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+        }
+      }
+      if (up) idx += c / 2;
+      c >>= 1;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+    }
+  }
+  return v[0];
 }
 
 // ================================================================== S item: scoring
@@ -368,14 +436,11 @@ __device__ void score_item(const LayerArgs& a, const Slot& sl, unsigned char* re
   const int rec = chunk_record(a, s, h, sl.index);
   float* sk = reinterpret_cast<float*>(region);
   float* sd = sk + kChunk * D;
-  float* svnew = sd + kChunk * r;
-  float* sq = reinterpret_cast<float*>(sm + lay.q);
-  float* sqsq = reinterpret_cast<float*>(sm + lay.qsq);
+  const float* sq = sd + kChunk * r;  // the unit's queries, staged with the rows
+  float* svnew = sd + kChunk * r + G * D;
   float* zs = reinterpret_cast<float*>(sm + lay.zs);
   float* ss = reinterpret_cast<float*>(sm + lay.ss);
   const int64_t row0 = row_of(a, s, h, b0);
-  const float* qg = a.q + ((int64_t)s * a.Hkv * G + (int64_t)h * G) * D;
-  for (int i = tid; i < G * D; i += kCT) sq[i] = qg[i];
   if (SCORE && (r & 3))
     for (int i = tid; i < sl.nt * r; i += kCT) sd[i] = a.dbar[row0 * r + i];
   if (sl.append && warp == 0) {
@@ -398,25 +463,17 @@ __device__ void score_item(const LayerArgs& a, const Slot& sl, unsigned char* re
     for (int i = lane; i < r; i += 32) a.dbar[row * r + i] = db[i];
   }
   consumer_sync();
-  if (SCORE) {
-    const int gs = D / r;
-    for (int i = tid; i < G * r; i += kCT) {
-      const int g = i / r, t = i % r;
-      float acc = 0.f;
-      for (int j = 0; j < gs; ++j) {
-        const float x = sq[g * D + t * gs + j];
-        acc = fmaf(x, x, acc);
-      }
-      sqsq[i] = acc;
-    }
-    consumer_sync();
-  }
-  // ---- zbar (and sigma2), LPB lanes per block, shuffle-reduced
+  COMPKV_PHASE(a, 1, u);
+  // ---- zbar and sigma2, LPB lanes per block, shuffle-reduced.  sigma2 is
+  // accumulated per lane as sum_i q_{g,i}^2 Dbar_{t(i)} over the lane's
+  // coordinates (the same sum as sum_t Qsq_{g,t} Dbar_t, regrouped).
   {
     constexpr int LPB = (G * D / 16 > 32) ? 32 : 16;
     constexpr int NV = D / LPB;
     constexpr int BPW = 32 / LPB;
+    constexpr int RUNS = NV / 4 > 0 ? NV / 4 : 1;  // runs of 4 consecutive coordinates per lane
     const int j = lane % LPB, sub = lane / LPB;
+    const int gs = D / r;
     float qr[G][NV];
 #pragma unroll
     for (int g = 0; g < G; ++g)
@@ -425,6 +482,22 @@ __device__ void score_item(const LayerArgs& a, const Slot& sl, unsigned char* re
         const int c = (NV == 8) ? (i < 4 ? 4 * j + i : D / 2 + 4 * j + (i - 4)) : NV * j + i;
         qr[g][i] = sq[g * D + c];
       }
+    // with groups of >= 4 coordinates each run lies in one group: pre-sum q^2 per run
+    const bool coarse = gs >= 4 && NV >= 4;
+    float qrun[G][RUNS];
+    int trun[RUNS];
+#pragma unroll
+    for (int k = 0; k < RUNS; ++k) {
+      const int c0 = (NV == 8) ? (k == 0 ? 4 * j : D / 2 + 4 * j) : NV * j;
+      trun[k] = c0 / gs;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float t = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4 && i < NV; ++i) t = fmaf(qr[g][4 * k + i], qr[g][4 * k + i], t);
+        qrun[g][k] = t;
+      }
+    }
     for (int base = warp * BPW; base < nb; base += kCW * BPW) {
       const int blk = base + sub;
       const bool valid = blk < nb;
@@ -451,31 +524,45 @@ __device__ void score_item(const LayerArgs& a, const Slot& sl, unsigned char* re
         for (int i = 0; i < NV; ++i) zacc[g] = fmaf(qr[g][i], kv[i], zacc[g]);
       }
       if (SCORE) {
-        for (int t = j; t < r; t += LPB) {
-          const float dv = sd[rb * r + t];
+        if (coarse) {
 #pragma unroll
-          for (int g = 0; g < G; ++g) sacc[g] = fmaf(sqsq[g * r + t], dv, sacc[g]);
+          for (int k = 0; k < RUNS; ++k) {
+            const float dv = sd[rb * r + trun[k]];
+#pragma unroll
+            for (int g = 0; g < G; ++g) sacc[g] = fmaf(qrun[g][k], dv, sacc[g]);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < NV; ++i) {
+            const int c = (NV == 8) ? (i < 4 ? 4 * j + i : D / 2 + 4 * j + (i - 4)) : NV * j + i;
+            const float dv = sd[rb * r + c / gs];
+#pragma unroll
+            for (int g = 0; g < G; ++g) sacc[g] = fmaf(qr[g][i] * qr[g][i], dv, sacc[g]);
+          }
         }
       }
+      // transposed reduction over the block's LPB lanes: each halving step
+      // exchanges half of the values, so 2G values cost ~2G shuffles
+      constexpr int NVAL = SCORE ? 2 * G : G;
+      float vals[NVAL];
 #pragma unroll
-      for (int o = LPB / 2; o > 0; o >>= 1) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          zacc[g] += __shfl_xor_sync(0xffffffffu, zacc[g], o);
-          if (SCORE) sacc[g] += __shfl_xor_sync(0xffffffffu, sacc[g], o);
-        }
+      for (int g = 0; g < G; ++g) {
+        vals[g] = zacc[g];
+        if (SCORE) vals[(G + g) % NVAL] = sacc[g];
       }
-      if (j == 0 && valid) {
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          zs[g * kChunk + blk] = zacc[g] * InvSqrt<D>::v;
-          if (SCORE) ss[g * kChunk + blk] = sacc[g] / (float)D;
-        }
+      int vidx;
+      const float tot = transpose_reduce_lanes<NVAL, LPB>(vals, j, vidx);
+      if (valid && (j & ((LPB / NVAL > 0 ? LPB / NVAL : 1) - 1)) == 0) {
+        if (vidx < G)
+          zs[vidx * kChunk + blk] = tot * InvSqrt<D>::v;
+        else
+          ss[(vidx - G) * kChunk + blk] = tot / (float)D;
       }
     }
   }
   consumer_sync();
   // ---- per query head: item max and sum of e^a, u per block, max of ln|b| + zbar
+  COMPKV_PHASE(a, 3, u);
   if (warp < G) {
     const int g = warp;
     float av[2], cv[2];
@@ -523,25 +610,24 @@ __device__ void score_item(const LayerArgs& a, const Slot& sl, unsigned char* re
   }
 }
 
-// Unit reference exponent M_g = max over its items of max(ln|b| + zbar), and
-// a zeroed compensation accumulator.  Consumers; ends synchronised.
-template <int D, int G>
-__device__ void prepare_comp(const LayerArgs& a, int u, int s, int h, int N, int* misc) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nch = (N + kChunk - 1) / kChunk;
-  const int rec0 = chunk_record(a, s, h, 0);
-  if (warp < G) {
-    float m = -INFINITY;
-    for (int c = lane; c < nch; c += 32) m = fmaxf(m, __ldcg(a.chunk_rec + ((int64_t)(rec0 + c) * G + warp) * 4 + 2));
-    m = warp_max(m);
-    if (lane == 0) a.unit_ref[u * G + warp] = m;
-  }
-  for (int i = tid; i < G * (D + 4); i += kCT) a.unit_acc[(int64_t)u * G * (D + 4) + i] = 0.f;
-}
-
 // ================================================================== SELECT follow-up
-template <int D, int G>
-__device__ void select_unit(const LayerArgs& a, const Slot& sl, unsigned char* region, int* misc) {
+// Runs once per unit when its last scoring item is done:
+//   1. per query head, from the items' records (max a, sum e^(a - max a),
+//      max(ln|b| + zbar)): LSE_g, the factors exp(max a - LSE_g) and the
+//      compensation reference M_g = max_b (ln|b| + zbar);
+//   2. S_b = sum_g u_{g,b} exp(max a - LSE_g) as uint32 keys (S_b >= 0);
+//   3. F = {0, N-2, N-1}, then the K-3 largest keys of blocks 1..N-3 by an
+//      MSB-first radix select (digits: bits 30:20, 19:9, 8:0), equal keys by
+//      increasing block index; a threshold digit holding <= 128 keys is
+//      resolved by ranking them directly;
+//   4. the ascending list, the bitmap and the count; the compensation
+//      accumulator cleared; the unit published as ready.
+// With a caller-given selection (attend mode) steps 2-3 are replaced by
+// validating the list and building the bitmap from it.
+template <int D, int G, int MODE>
+__device__ void follow_select(const LayerArgs& a, const Slot& sl, unsigned char* region, int* misc) {
+  constexpr bool SEL = (MODE & kFSelect) != 0;
+  constexpr bool COMP = (MODE & kFComp) != 0;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int u = sl.unit, s = u / a.Hkv, h = u % a.Hkv;
   const int N = sl.N, K = a.K;
@@ -549,245 +635,327 @@ __device__ void select_unit(const LayerArgs& a, const Slot& sl, unsigned char* r
   const int rec0 = chunk_record(a, s, h, 0);
   uint32_t* keys = reinterpret_cast<uint32_t*>(region);
   uint32_t* hist = keys + align_up(a.cap_blocks[s], 4);
-  uint32_t* lkey = hist + kBins;
-  int* lidx = reinterpret_cast<int*>(lkey + kListCap);
-  float* fch = reinterpret_cast<float*>(lidx + kListCap);
+  uint32_t* phist = hist + kBins;
+  uint32_t* lkey = phist + kCW * kPrivBins;
+  int* lidx = reinterpret_cast<int*>(lkey + kRankCap);
+  float* fch = reinterpret_cast<float*>(lidx + kRankCap);
+  unsigned* words = reinterpret_cast<unsigned*>(fch + align_up(((a.cap_blocks[s] + kChunk - 1) / kChunk) * G, 4));
+  int* wbase = reinterpret_cast<int*>(words + align_up((a.cap_blocks[s] + 31) / 32, 4));
   float* lse = reinterpret_cast<float*>(misc + kMLse);
   int* selrow = a.sel + (int64_t)u * K;
 
-  // 1. LSE_g from the items' (max, sum) pairs, four items in flight per lane
+  // ---- 1. one float4 record per (item, head); eight items in flight per lane
   if (warp < G) {
     const int g = warp;
-    float M = -INFINITY, S = 0.f;
-    for (int c0 = lane; c0 < nch; c0 += 128) {
-      float mv[4], lv[4];
+    float M = -INFINITY, S = 0.f, MC = -INFINITY;
+    float ma_keep[8];  // this lane's first eight items' max a, for the factors below
+    for (int c0 = lane; c0 < nch; c0 += 256) {
+      float4 rv[8];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < 8; ++k) {
         const int c = c0 + 32 * k;
-        const float* rg = a.chunk_rec + ((int64_t)(rec0 + c) * G + g) * 4;
-        mv[k] = c < nch ? __ldcg(rg) : -INFINITY;
-        lv[k] = c < nch ? __ldcg(rg + 1) : 0.f;
+        rv[k] = c < nch ? __ldcg(reinterpret_cast<const float4*>(a.chunk_rec + ((int64_t)(rec0 + c) * G + g) * 4))
+                        : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+      }
+      if (c0 == lane) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) ma_keep[k] = rv[k].x;
       }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        if (mv[k] == -INFINITY) continue;
-        const float mn = fmaxf(M, mv[k]);
-        S = (M == -INFINITY ? 0.f : S * expf(M - mn)) + lv[k] * expf(mv[k] - mn);
-        M = mn;
+      for (int k = 0; k < 8; ++k) {
+        MC = fmaxf(MC, rv[k].z);
+        if (SEL && rv[k].x != -INFINITY) {
+          const float mn = fmaxf(M, rv[k].x);
+          S = (M == -INFINITY ? 0.f : S * expf(M - mn)) + rv[k].y * expf(rv[k].x - mn);
+          M = mn;
+        }
       }
     }
+    MC = warp_max(MC);
+    if (SEL) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float M2 = __shfl_xor_sync(0xffffffffu, M, o), S2 = __shfl_xor_sync(0xffffffffu, S, o);
-      const float Mn = fmaxf(M, M2);
-      if (Mn != -INFINITY) {
-        S = (M == -INFINITY ? 0.f : S * expf(M - Mn)) + (M2 == -INFINITY ? 0.f : S2 * expf(M2 - Mn));
-        M = Mn;
+      for (int o = 16; o > 0; o >>= 1) {
+        const float M2 = __shfl_xor_sync(0xffffffffu, M, o), S2 = __shfl_xor_sync(0xffffffffu, S, o);
+        const float Mn = fmaxf(M, M2);
+        if (Mn != -INFINITY) {
+          S = (M == -INFINITY ? 0.f : S * expf(M - Mn)) + (M2 == -INFINITY ? 0.f : S2 * expf(M2 - Mn));
+          M = Mn;
+        }
       }
-    }
-    if (lane == 0) lse[g] = M + logf(S);
-  }
-  consumer_sync();
-  for (int i = tid; i < nch * G; i += kCT) {
-    const int c = i / G, g = i % G;
-    fch[i] = expf(__ldcg(a.chunk_rec + ((int64_t)(rec0 + c) * G + g) * 4) - lse[g]);
-  }
-  for (int i = tid; i < kBins; i += kCT) hist[i] = 0;
-  consumer_sync();
-  // 2. S_b = sum_g u_{g,b} exp(m_a - LSE_g) as order-preserving keys; four blocks per thread
-  float* scores = a.scores ? a.scores + (int64_t)u * a.score_stride : nullptr;
-  for (int b4 = 4 * tid; b4 < N; b4 += 4 * kCT) {
-    const int c = b4 / kChunk, o = b4 % kChunk;
-    float4 S = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float lg = M + logf(S);
+      if (lane == 0) lse[g] = lg;
+      // factors exp(max a - LSE_g) of this lane's items
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float4 uu = __ldcg(reinterpret_cast<const float4*>(a.chunk_u + ((int64_t)(rec0 + c) * G + g) * kChunk + o));
-      const float f = fch[c * G + g];
-      S.x = fmaf(uu.x, f, S.x);
-      S.y = fmaf(uu.y, f, S.y);
-      S.z = fmaf(uu.z, f, S.z);
-      S.w = fmaf(uu.w, f, S.w);
-    }
-    const float sv[4] = {fmaxf(S.x, 0.f), fmaxf(S.y, 0.f), fmaxf(S.z, 0.f), fmaxf(S.w, 0.f)};
-#pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if (b4 + k < N) {
-        keys[b4 + k] = __float_as_uint(sv[k]);
-        if (scores) scores[b4 + k] = sv[k];
+      for (int k = 0; k < 8; ++k) {
+        const int c = lane + 32 * k;
+        if (c < nch) fch[c * G + g] = expf(ma_keep[k] - lg);
       }
+      for (int c = lane + 256; c < nch; c += 32)
+        fch[c * G + g] = expf(__ldcg(a.chunk_rec + ((int64_t)(rec0 + c) * G + g) * 4) - lg);
+    }
+    if (COMP && lane == 0) a.unit_ref[u * G + g] = MC;
   }
-  consumer_sync();
-  if (N > K) {
-    // 3. radix select of the K-3 largest candidates (blocks 1..N-3), 11/11/10-bit digits
-    int need = K - 3;
-    uint32_t prefix = 0, pmask = 0;
-    bool done = need == 0;
-    const int cand_lo = 1, cand_hi = N - 3;
-    for (int level = 0; level < 3 && !done; ++level) {
-      const int shift = level == 0 ? 21 : (level == 1 ? 10 : 0);
-      const int nbins = level == 2 ? 1024 : 2048;
-      const uint32_t dmask = (uint32_t)nbins - 1;
-      if (level > 0) {
-        for (int i = tid; i < kBins; i += kCT) hist[i] = 0;
-        consumer_sync();
-      }
-      for (int b = cand_lo + tid; b <= cand_hi; b += kCT) {
-        const uint32_t key = keys[b];
-        if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
-      }
-      consumer_sync();
-      {
-        const int per = (nbins + kCT - 1) / kCT;
-        int loc = 0;
-        for (int i = 0; i < per; ++i) {
-          const int bin = nbins - 1 - per * tid - i;
-          if (bin >= 0) loc += (int)hist[bin];
-        }
-        int total;
-        const int before = consumer_scan(loc, misc + kMScan, &total);
-        if (before < need && need <= before + loc) {
-          int run = before;
-          for (int i = 0; i < per; ++i) {
-            const int bin = nbins - 1 - per * tid - i;
-            if (bin < 0) break;
-            const int c = (int)hist[bin];
-            if (run < need && need <= run + c) {
-              misc[kMDigit] = bin;
-              misc[kMAbove] = run;
-            }
-            run += c;
-          }
-        }
-        if (tid == 0) misc[kMList] = 0;
-      }
-      consumer_sync();
-      const uint32_t Dg = (uint32_t)misc[kMDigit];
-      const int above = misc[kMAbove];
-      const int cntD = (int)hist[Dg];
-      for (int b = cand_lo + tid; b <= cand_hi; b += kCT) {
-        const uint32_t key = keys[b];
-        if ((key & pmask) == prefix && ((key >> shift) & dmask) > Dg) keys[b] = key | 0x80000000u;
-      }
-      need -= above;
-      prefix |= Dg << shift;
-      pmask |= dmask << shift;
-      if (cntD == need) {
-        for (int b = cand_lo + tid; b <= cand_hi; b += kCT)
-          if ((keys[b] & pmask) == prefix) keys[b] |= 0x80000000u;
-        done = true;
-      } else if (cntD <= kListCap) {
-        for (int b = cand_lo + tid; b <= cand_hi; b += kCT) {
-          const uint32_t key = keys[b];
-          if ((key & pmask) == prefix) {
-            const int p = atomicAdd(misc + kMList, 1);
-            lkey[p] = key;
-            lidx[p] = b;
-          }
-        }
-        consumer_sync();
-        const int n = misc[kMList];
-        for (int e = tid; e < n; e += kCT) {
-          const uint32_t k0 = lkey[e];
-          const int i0 = lidx[e];
-          int rank = 0;
-          for (int f = 0; f < n; ++f) {
-            const uint32_t kf = lkey[f];
-            rank += (kf > k0) || (kf == k0 && lidx[f] < i0);
-          }
-          if (rank < need) keys[i0] = k0 | 0x80000000u;
-        }
-        done = true;
-      }
-      consumer_sync();
-    }
-    if (!done) {
-      // all remaining candidates carry the same key: take the `need` lowest indices
-      const int span = cand_hi - cand_lo + 1;
-      const int per = (span + kCT - 1) / kCT;
-      const int lo = cand_lo + min(span, tid * per), hi = cand_lo + min(span, tid * per + per);
-      int cnt = 0;
-      for (int b = lo; b < hi; ++b) cnt += (keys[b] & pmask) == prefix;
-      int total;
-      int rk = consumer_scan(cnt, misc + kMScan, &total);
-      for (int b = lo; b < hi; ++b)
-        if ((keys[b] & pmask) == prefix) {
-          if (rk < need) keys[b] |= 0x80000000u;
-          ++rk;
-        }
-      consumer_sync();
-    }
-    if (tid == 0) {
-      keys[0] |= 0x80000000u;
-      keys[N - 2] |= 0x80000000u;
-      keys[N - 1] |= 0x80000000u;
-    }
-  } else {
-    for (int b = tid; b < N; b += kCT) keys[b] |= 0x80000000u;
-  }
-  consumer_sync();
-  // 4. ascending list (padded with -1), bitmap, count
-  {
-    const int per = (N + kCT - 1) / kCT;
-    const int lo = min(N, tid * per), hi = min(N, tid * per + per);
-    int cnt = 0;
-    for (int b = lo; b < hi; ++b) cnt += keys[b] >> 31;
-    int total;
-    int pos = consumer_scan(cnt, misc + kMScan, &total);
-    const int want = N < K ? N : K;
-    if (tid == 0 && total != want) set_error(a.status, kDevInternal, s, h, 50);
-    for (int b = lo; b < hi; ++b)
-      if ((keys[b] >> 31) && pos < K) selrow[pos++] = b;
-    for (int i = want + tid; i < K; i += kCT) selrow[i] = -1;
-    if (tid == 0) a.unit_nsel[u] = total;
-    for (int w = tid; w < (N + 31) / 32; w += kCT) {
-      unsigned bits = 0;
-      for (int j = 0; j < 32; ++j) {
-        const int b = 32 * w + j;
-        if (b < N) bits |= (keys[b] >> 31) << j;
-      }
-      a.bitmap[(int64_t)u * a.bm_words + w] = bits;
-    }
-  }
-}
-
-// ================================================================== selection given by the caller
-template <int D, int G>
-__device__ void bitmap_unit(const LayerArgs& a, const Slot& sl, unsigned char* region, int* misc) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int u = sl.unit, s = u / a.Hkv, h = u % a.Hkv;
-  const int N = sl.N, K = a.K;
-  unsigned* bm = reinterpret_cast<unsigned*>(region);
-  const int words = (N + 31) / 32;
-  const int* selrow = a.sel + (int64_t)u * K;
-  for (int w = tid; w < words; w += kCT) bm[w] = 0u;
-  if (tid == 0) {
+  if (COMP)
+    for (int i = tid; i < G * (D + 4); i += kCT) a.unit_acc[(int64_t)u * G * (D + 4) + i] = 0.f;
+  if (SEL)
+    for (int i = tid; i < kCW * kPrivBins; i += kCT) phist[i] = 0;
+  if (!SEL && tid == 0) {
     misc[kMCount] = 0;
     misc[kMBad] = 0;
   }
   consumer_sync();
-  int cnt = 0, bad = 0;
-  for (int i = tid; i < K; i += kCT) {
-    const int e = __ldcg(selrow + i);
-    const int prev = i > 0 ? __ldcg(selrow + i - 1) : -1;
-    const bool ok = e >= 0 && e < N && (i == 0 || (prev >= 0 && prev < e));
-    if (ok) {
-      atomicOr(&bm[e >> 5], 1u << (e & 31));
-      ++cnt;
+  COMPKV_PHASE(a, 11, u);
+
+  if (!SEL) {
+    // ---- caller-given selection: validate, count, bitmap
+    unsigned* bm = keys;
+    const int words = (N + 31) / 32;
+    for (int w = tid; w < words; w += kCT) bm[w] = 0u;
+    consumer_sync();
+    int cnt = 0, bad = 0;
+    for (int i = tid; i < K; i += kCT) {
+      const int e = __ldcg(selrow + i);
+      const int prev = i > 0 ? __ldcg(selrow + i - 1) : -1;
+      const bool ok = e >= 0 && e < N && (i == 0 || (prev >= 0 && prev < e));
+      if (ok) {
+        atomicOr(&bm[e >> 5], 1u << (e & 31));
+        ++cnt;
+      }
+      bad |= (e >= 0 && !ok) || e < -1;
     }
-    bad |= (e >= 0 && !ok) || e < -1;
+    cnt = __reduce_add_sync(0xffffffffu, cnt);
+    bad = __reduce_or_sync(0xffffffffu, bad);
+    if (lane == 0) {
+      if (cnt) atomicAdd(misc + kMCount, cnt);
+      if (bad) misc[kMBad] = 1;
+    }
+    consumer_sync();
+    if (tid == 0) {
+      a.unit_nsel[u] = misc[kMCount];
+      if (misc[kMBad]) set_error(a.status, kDevBadSelection, s, h, 61);
+    }
+    for (int w = tid; w < words; w += kCT) a.bitmap[(int64_t)u * a.bm_words + w] = bm[w];
+  } else {
+    // ---- 2. S_b keys, several four-block groups in flight per thread
+    float* scores = a.scores ? a.scores + (int64_t)u * a.score_stride : nullptr;
+    constexpr int QB = G >= 8 ? 1 : (G >= 4 ? 3 : 6);
+    for (int q0 = 4 * tid; q0 < N; q0 += 4 * kCT * QB) {
+      float4 uu[QB][G];
+#pragma unroll
+      for (int k = 0; k < QB; ++k) {
+        const int b4 = q0 + 4 * kCT * k;
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+          uu[k][g] = b4 < N ? __ldcg(reinterpret_cast<const float4*>(
+                                  a.chunk_u + ((int64_t)(rec0 + b4 / kChunk) * G + g) * kChunk + (b4 % kChunk)))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < QB; ++k) {
+        const int b4 = q0 + 4 * kCT * k;
+        if (b4 >= N) continue;
+        const int c = b4 / kChunk;
+        float4 S = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float f = fch[c * G + g];
+          S.x = fmaf(uu[k][g].x, f, S.x);
+          S.y = fmaf(uu[k][g].y, f, S.y);
+          S.z = fmaf(uu[k][g].z, f, S.z);
+          S.w = fmaf(uu[k][g].w, f, S.w);
+        }
+        const float sv[4] = {fmaxf(S.x, 0.f), fmaxf(S.y, 0.f), fmaxf(S.z, 0.f), fmaxf(S.w, 0.f)};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (b4 + i < N) {
+            keys[b4 + i] = __float_as_uint(sv[i]);
+            if (scores) scores[b4 + i] = sv[i];
+          }
+      }
+    }
+    consumer_sync();
+    COMPKV_PHASE(a, 12, u);
+    if (N > K) {
+      // ---- 3. radix select; bit 31 of a key marks it selected (values are >= +0,
+      // bit 31 clear).  Digits: the exponent (bits 30:23, per-warp histograms),
+      // then bits 22:12 and 11:0 (shared histogram, few keys left).
+      int need = K - 3;
+      uint32_t prefix = 0, pmask = 0x80000000u;
+      bool done = need == 0;
+      const int cand_lo = 1, cand_hi = N - 3;
+      for (int level = 0; level < 3 && !done; ++level) {
+        const int shift = level == 0 ? 23 : (level == 1 ? 12 : 0);
+        const int nbins = level == 0 ? kPrivBins : (level == 1 ? 2048 : 4096);
+        const uint32_t dmask = (uint32_t)nbins - 1;
+        if (level == 0) {
+          uint32_t* mine = phist + warp * kPrivBins;
+          for (int b = cand_lo + tid; b <= cand_hi; b += kCT) atomicAdd(&mine[keys[b] >> 23], 1u);
+          consumer_sync();
+          for (int i = tid; i < kPrivBins; i += kCT) {
+            uint32_t t = 0;
+#pragma unroll
+            for (int w = 0; w < kCW; ++w) t += phist[w * kPrivBins + i];
+            hist[i] = t;
+          }
+        } else {
+          for (int i = tid; i < nbins; i += kCT) hist[i] = 0;
+          consumer_sync();
+          for (int b = cand_lo + tid; b <= cand_hi; b += kCT) {
+            const uint32_t key = keys[b];
+            if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
+          }
+        }
+        consumer_sync();
+        if (warp == 0) {
+          // the digit at which the count of larger-or-equal keys reaches `need`
+          const int per = nbins / 32;
+          int loc = 0;
+          for (int i = 0; i < per; ++i) loc += (int)hist[nbins - 1 - per * lane - i];
+          int incl = loc;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+          }
+          const int before = incl - loc;
+          if (before < need && need <= incl) {
+            int run = before;
+            for (int i = 0; i < per; ++i) {
+              const int bin = nbins - 1 - per * lane - i;
+              const int c = (int)hist[bin];
+              if (run < need && need <= run + c) {
+                misc[kMDigit] = bin;
+                misc[kMAbove] = run;
+              }
+              run += c;
+            }
+          }
+          if (lane == 0) misc[kMList] = 0;
+        }
+        consumer_sync();
+        const uint32_t Dg = (uint32_t)misc[kMDigit];
+        const int above = misc[kMAbove];
+        const int cntD = (int)hist[Dg];
+        for (int b = cand_lo + tid; b <= cand_hi; b += kCT) {
+          const uint32_t key = keys[b];
+          if ((key & pmask) == prefix && ((key >> shift) & dmask) > Dg) keys[b] = key | 0x80000000u;
+        }
+        need -= above;
+        prefix |= Dg << shift;
+        pmask |= dmask << shift;
+        if (cntD == need) {
+          for (int b = cand_lo + tid; b <= cand_hi; b += kCT)
+            if ((keys[b] & pmask) == prefix) keys[b] |= 0x80000000u;
+          done = true;
+        } else if (cntD <= kRankCap) {
+          for (int b = cand_lo + tid; b <= cand_hi; b += kCT) {
+            const uint32_t key = keys[b];
+            if ((key & pmask) == prefix) {
+              const int p = atomicAdd(misc + kMList, 1);
+              lkey[p] = key;
+              lidx[p] = b;
+            }
+          }
+          consumer_sync();
+          const int n = misc[kMList];
+          for (int e = tid; e < n; e += kCT) {
+            const uint32_t k0 = lkey[e];
+            const int i0 = lidx[e];
+            int rank = 0;
+            for (int f = 0; f < n; ++f) {
+              const uint32_t kf = lkey[f];
+              rank += (kf > k0) || (kf == k0 && lidx[f] < i0);
+            }
+            if (rank < need) keys[i0] = k0 | 0x80000000u;
+          }
+          done = true;
+        }
+        consumer_sync();
+        COMPKV_PHASE(a, 13, u);
+      }
+      if (!done) {
+        // all remaining candidates carry the same key: take the `need` lowest indices
+        const int span = cand_hi - cand_lo + 1;
+        const int per = (span + kCT - 1) / kCT;
+        const int lo = cand_lo + min(span, tid * per), hi = cand_lo + min(span, tid * per + per);
+        int cnt = 0;
+        for (int b = lo; b < hi; ++b) cnt += (keys[b] & pmask) == prefix;
+        int total;
+        int rk = consumer_scan(cnt, misc + kMScan, &total);
+        for (int b = lo; b < hi; ++b)
+          if ((keys[b] & pmask) == prefix) {
+            if (rk < need) keys[b] |= 0x80000000u;
+            ++rk;
+          }
+        consumer_sync();
+      }
+      if (tid == 0) {
+        keys[0] |= 0x80000000u;
+        keys[N - 2] |= 0x80000000u;
+        keys[N - 1] |= 0x80000000u;
+      }
+    } else {
+      for (int b = tid; b < N; b += kCT) keys[b] |= 0x80000000u;
+    }
+    consumer_sync();
+    COMPKV_PHASE(a, 14, u);
+    // ---- 4. bitmap words by ballot, their prefix counts, then the ascending list
+    const int nw = (N + 31) / 32;
+    for (int w = warp; w < nw; w += kCW) {
+      const int b = 32 * w + lane;
+      const unsigned word = __ballot_sync(0xffffffffu, b < N && (keys[b] >> 31));
+      if (lane == 0) {
+        words[w] = word;
+        a.bitmap[(int64_t)u * a.bm_words + w] = word;
+      }
+    }
+    consumer_sync();
+    if (warp == 0) {
+      const int per = (nw + 31) / 32;
+      int loc = 0;
+      for (int i = 0; i < per; ++i) {
+        const int w = per * lane + i;
+        if (w < nw) loc += __popc(words[w]);
+      }
+      int incl = loc;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int run = incl - loc;
+      for (int i = 0; i < per; ++i) {
+        const int w = per * lane + i;
+        if (w < nw) {
+          wbase[w] = run;
+          run += __popc(words[w]);
+        }
+      }
+      if (lane == 31) {
+        const int want = N < K ? N : K;
+        if (incl != want) set_error(a.status, kDevInternal, s, h, 50);
+        a.unit_nsel[u] = incl;
+      }
+    }
+    consumer_sync();
+    for (int w = warp; w < nw; w += kCW) {
+      const unsigned word = words[w];
+      if ((word >> lane) & 1u) {
+        const int pos = wbase[w] + __popc(word & ((1u << lane) - 1u));
+        if (pos < K) selrow[pos] = 32 * w + lane;
+      }
+    }
+    {
+      const int want = N < K ? N : K;
+      for (int i = want + tid; i < K; i += kCT) selrow[i] = -1;
+    }
   }
-  cnt = __reduce_add_sync(0xffffffffu, cnt);
-  bad = __reduce_or_sync(0xffffffffu, bad);
-  if (lane == 0) {
-    if (cnt) atomicAdd(misc + kMCount, cnt);
-    if (bad) misc[kMBad] = 1;
-  }
+  // ---- publish: the CTA barrier orders every thread's writes before thread 0's release
   consumer_sync();
   if (tid == 0) {
-    a.unit_nsel[u] = misc[kMCount];
-    if (misc[kMBad]) set_error(a.status, kDevBadSelection, s, h, 61);
+    fence_gpu();
+    st_release(a.ready + u, a.epoch);
   }
-  for (int w = tid; w < words; w += kCT) a.bitmap[(int64_t)u * a.bm_words + w] = bm[w];
 }
 
 // ================================================================== A item: exact attention
@@ -859,58 +1027,95 @@ __device__ void attend_item(const LayerArgs& a, const Slot& sl, unsigned char* r
     if (e >= 0 && e < N && (my_i == 0 || (prev >= 0 && prev < e))) b = e;
   }
   if (b >= 0) {
+    // one block per warp: its 16 keys, then its 16 values, each fetched in one round
+    constexpr int W = V / 2;  // 32-bit words of this lane's V bf16 coordinates
+    constexpr int NG = kBlock / TG;
     const int n = (b == N - 1) ? L - kBlock * b : kBlock;
     const int64_t row = row_of(a, s, h, b);
-    const __nv_bfloat16* kp = a.k + row * kBlock * D + lane * V;
-    const __nv_bfloat16* vp = a.v + row * kBlock * D + lane * V;
-    for (int j0 = 0; j0 < kBlock; j0 += TG) {
+    const unsigned* kp = reinterpret_cast<const unsigned*>(a.k + row * kBlock * D + lane * V);
+    const unsigned* vp = reinterpret_cast<const unsigned*>(a.v + row * kBlock * D + lane * V);
+    unsigned raw[kBlock][W];
+#pragma unroll
+    for (int j = 0; j < kBlock; ++j) {
+      if (W == 2) {
+        const uint2 w = __ldcg(reinterpret_cast<const uint2*>(kp + j * (D / 2)));
+        raw[j][0] = w.x;
+        raw[j][W - 1] = w.y;
+      } else {
+        raw[j][0] = __ldcg(kp + j * (D / 2));
+      }
+    }
+    // logits: lane holds z of (token jj, head gl) for each group of TG tokens
+    float zl[NG];
+    const int idx = lane & (P - 1);
+    const int jj = idx / G, gl = idx % G;
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi) {
       float part[P];
 #pragma unroll
-      for (int jj = 0; jj < TG; ++jj) {
+      for (int t = 0; t < TG; ++t) {
         float kf[V];
-        load_bf16_cg<V>(kp + (j0 + jj) * D, kf);
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+          const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[gi * TG + t][w]));
+          kf[2 * w] = x.x;
+          kf[2 * w + 1] = x.y;
+        }
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          float t = 0.f;
+          float acc_t = 0.f;
 #pragma unroll
-          for (int i = 0; i < V; ++i) t = fmaf(qr[g][i], kf[i], t);
-          part[jj * G + g] = t;
+          for (int i = 0; i < V; ++i) acc_t = fmaf(qr[g][i], kf[i], acc_t);
+          part[t * G + g] = acc_t;
         }
       }
-      const float z = transpose_reduce<P>(part, lane);
-      const int idx = lane & (P - 1);
-      const int jj = idx / G, gl = idx % G;
-      const bool valid = j0 + jj < n;
-      float gm = valid ? z : -INFINITY;
+      zl[gi] = transpose_reduce<P>(part, lane);
+    }
+    // block max per head, weights, denominators
+    float zmax = -INFINITY;
 #pragma unroll
-      for (int o = G; o < P; o <<= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
-      float mn_l = 0.f;
-      float scale[G];
+    for (int gi = 0; gi < NG; ++gi)
+      if (gi * TG + jj < n) zmax = fmaxf(zmax, zl[gi]);
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float gmg = __shfl_sync(0xffffffffu, gm, g);
-        const float mn = fmaxf(m[g], gmg);
-        scale[g] = (m[g] == -INFINITY) ? 0.f : expf(m[g] - mn);
-        m[g] = mn;
-        if (g == gl) mn_l = mn;
+    for (int o = G; o < P; o <<= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
+    float pl[NG];
+    float psum = 0.f;
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi) {
+      pl[gi] = (gi * TG + jj < n) ? expf(zl[gi] - zmax) : 0.f;
+      psum += pl[gi];
+    }
+#pragma unroll
+    for (int o = G; o < P; o <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      m[g] = __shfl_sync(0xffffffffu, zmax, g);
+      l[g] = __shfl_sync(0xffffffffu, psum, g);
+    }
+#pragma unroll
+    for (int j = 0; j < kBlock; ++j) {
+      if (W == 2) {
+        const uint2 w = __ldcg(reinterpret_cast<const uint2*>(vp + j * (D / 2)));
+        raw[j][0] = w.x;
+        raw[j][W - 1] = w.y;
+      } else {
+        raw[j][0] = __ldcg(vp + j * (D / 2));
       }
-      const float pz = (valid && mn_l != -INFINITY) ? expf(z - mn_l) : 0.f;
-      float ps = pz;
+    }
 #pragma unroll
-      for (int o = G; o < P; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        l[g] = l[g] * scale[g] + __shfl_sync(0xffffffffu, ps, g);
-#pragma unroll
-        for (int i = 0; i < V; ++i) acc[g][i] *= scale[g];
-      }
+    for (int gi = 0; gi < NG; ++gi) {
 #pragma unroll
       for (int t = 0; t < TG; ++t) {
         float vf[V];
-        load_bf16_cg<V>(vp + (j0 + t) * D, vf);
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+          const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[gi * TG + t][w]));
+          vf[2 * w] = x.x;
+          vf[2 * w + 1] = x.y;
+        }
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float pg = __shfl_sync(0xffffffffu, pz, t * G + g);
+          const float pg = __shfl_sync(0xffffffffu, pl[gi], t * G + g);
 #pragma unroll
           for (int i = 0; i < V; ++i) acc[g][i] = fmaf(pg, vf[i], acc[g][i]);
         }
@@ -1118,6 +1323,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_kernel(LayerArgs a) {
       const Slot sl = slots[st];
       if (sl.type == kSlotEnd) break;
       unsigned char* region = sm + lay.region[st];
+      unsigned long long t_item = 0;
+      if (a.trace && tid == 0) {
+        t_item = global_ns();
+        reinterpret_cast<unsigned long long*>(misc + kMWaitT)[0] = t_item;
+      }
       switch (sl.type) {
         case kItemScore:
           score_item<D, G, MODE>(a, sl, region, sm, lay);
@@ -1128,18 +1338,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_kernel(LayerArgs a) {
         case kItemComp:
           if (MODE & kFAttend) comp_item<D, G, MODE>(a, sl, region, sm, lay, misc);
           break;
-        case kSlotSelect: {
-          const int s = sl.unit / a.Hkv, h = sl.unit % a.Hkv;
-          if (MODE & kFSelect)
-            select_unit<D, G>(a, sl, region, misc);
-          else
-            bitmap_unit<D, G>(a, sl, region, misc);
-          if (MODE & kFComp) prepare_comp<D, G>(a, sl.unit, s, h, sl.N, misc);
-          __threadfence();
-          consumer_sync();
-          if (tid == 0) st_release(a.ready + sl.unit, a.epoch);
+        case kSlotSelect:
+          follow_select<D, G, MODE>(a, sl, region, misc);
           break;
-        }
         case kSlotMerge:
           merge_unit<D, G>(a, sl);
           break;
@@ -1147,7 +1348,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1) fused_kernel(LayerArgs a) {
           break;
       }
       consumer_sync();
-      if (tid == 0) mbar_arrive(&empty[st]);
+      if (tid == 0) {
+        mbar_arrive(&empty[st]);
+        if (a.trace)
+          trace_record(a, sl.type, sl.unit, sl.index, t_item, reinterpret_cast<unsigned long long*>(misc + kMWaitT)[0],
+                       global_ns());
+      }
       uses[st]++;
       st = (st + 1 == a.stages) ? 0 : st + 1;
     }

@@ -213,6 +213,18 @@ enum {
   COMPKV_KERNEL_FAMILIES = 6
 };
 compkv_status compkv_profile_enable(compkv_ctx *ctx, int enable);
+
+/* Work-item trace of the fused decode kernel (tracing aid, off by default).
+ * buf: caller device memory, 8-byte aligned, `bytes` long; word 0 counts the
+ * records written (the caller zeroes it before the launches it wants to
+ * trace) and record i occupies words 1 + 5i .. 5 + 5i:
+ *   (cta << 32 | type << 24 | index), unit, t0, t1, t2   (%globaltimer ns)
+ * Consumer records (type 0 scoring, 1 attention, 2 compensation, 3 select,
+ * 4 merge): t0 = item received, t1 = end of the wait for its unit (= t0 when
+ * it waits for nothing), t2 = item done.  Producer records (type 16 + item
+ * type): t0 = before claiming the next ticket, t2 = item published.  Records
+ * beyond the capacity are dropped.  buf = NULL switches tracing off. */
+compkv_status compkv_trace(compkv_ctx *ctx, void *buf, size_t bytes);
 compkv_status compkv_profile_read(compkv_ctx *ctx, int family, double *total_ms, int64_t *launches);
 
 /* Description of the last error returned on this host thread ("" if none). */
