@@ -34,12 +34,12 @@ struct Layout {
   int64_t rows_per_layer = 0;
   int total_chunks = 0;
   int max_cap_blocks = 0;
-  int K = 0, splits = 0;
-  int units = 0, total_items = 0, phase1_items = 0, region_bytes = 0, stages = 0, bm_words = 0;
-  std::vector<int> items;  // the fused kernel's work queue
-  size_t off_status = 0, off_queue = 0, off_s1count = 0, off_mcount = 0, off_ready = 0, off_items = 0,
-         off_chunk_rec = 0, off_chunk_z = 0, off_chunk_u = 0, off_split = 0, off_unit_ref = 0, off_unit_acc = 0,
-         off_unit_nsel = 0, off_bitmap = 0, off_sel = 0, total = 0;
+  std::vector<int> n2_first, nchunk2, ns_first;
+  int n2_items = 0, ns_items = 0;
+  int K = 0, splits = 0, units = 0, key_stride = 0;
+  size_t off_status = 0, off_lnew = 0, off_mcount = 0, off_s2count = 0, off_unit_hist = 0, off_chunk_rec = 0,
+         off_chunk_z = 0, off_chunk_u = 0, off_split = 0, off_unit_ref = 0, off_unit_acc = 0, off_unit_nsel = 0,
+         off_skeys = 0, off_sel = 0, total = 0;
 };
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -73,8 +73,10 @@ compkv_status make_layout(const compkv_config* c, Layout* L) {
   L->seq_row0.resize(c->batch);
   L->chunk0.resize(c->batch);
   L->nchunk.resize(c->batch);
-  int64_t row = 0;
-  int64_t ch = 0;
+  L->n2_first.resize(c->batch);
+  L->nchunk2.resize(c->batch);
+  L->ns_first.resize(c->batch);
+  int64_t row = 0, ch = 0, ch2 = 0, chs = 0;
   L->max_cap_blocks = 0;
   for (int s = 0; s < c->batch; ++s) {
     L->seq_row0[s] = row;
@@ -82,44 +84,36 @@ compkv_status make_layout(const compkv_config* c, Layout* L) {
     L->nchunk[s] = (L->cap_blocks[s] + kChunk - 1) / kChunk;
     L->chunk0[s] = (int)ch;
     ch += (int64_t)H * L->nchunk[s];
+    L->nchunk2[s] = (L->cap_blocks[s] + kChunk2 - 1) / kChunk2;
+    L->n2_first[s] = (int)ch2;
+    ch2 += (int64_t)H * L->nchunk2[s];
+    L->ns_first[s] = (int)chs;
+    chs += (int64_t)H * ((L->nchunk[s] + 7) / 8);
     if (L->cap_blocks[s] > L->max_cap_blocks) L->max_cap_blocks = L->cap_blocks[s];
   }
-  if (ch > (int64_t)1 << 30) return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "too many scoring work items");
+  // grids of the scoring and compensation kernels (x dimension)
+  if (ch > 0x7fffffff || ch2 > 0x7fffffff) return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "too many scoring work items");
   L->rows_per_layer = row;
   L->total_chunks = (int)ch;
-  L->stages = fused_stages(d, c->r, G, L->max_cap_blocks, kMaxSmem);
-  if (fused_smem_bytes(d, c->r, G, L->max_cap_blocks, L->stages) > kMaxSmem)
+  L->n2_items = (int)ch2;
+  L->ns_items = (int)chs;
+  L->key_stride = (L->max_cap_blocks + 3) & ~3;
+  if (chain_smem_bytes(d, c->r, G, L->key_stride) > kMaxSmem)
     return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "a sequence capacity of %d blocks does not fit the selection in shared memory",
                 L->max_cap_blocks);
-  L->region_bytes = fused_region_bytes(d, c->r, G, L->max_cap_blocks);
   L->K = c->budget_tokens / kBlock;
   L->splits = (L->K + kAttendBlocks - 1) / kAttendBlocks;
   L->units = c->batch * H;
-  L->bm_words = (L->max_cap_blocks + 31) / 32;
-  // work queue: phase 1 = every unit's scoring items; phase 2 = per unit its
-  // attention items, then its compensation items.  Code: type | unit | index.
-  L->items.clear();
-  auto code = [](unsigned type, unsigned u, unsigned index) { return (int)((type << 30) | (u << 18) | index); };
-  for (int u = 0; u < L->units; ++u)
-    for (int ch = 0; ch < L->nchunk[u / H]; ++ch) L->items.push_back(code(0, u, ch));
-  L->phase1_items = (int)L->items.size();
-  for (int u = 0; u < L->units; ++u) {
-    for (int p = 0; p < L->splits; ++p) L->items.push_back(code(1, u, p));
-    const int n2 = (L->cap_blocks[u / H] + kChunk2 - 1) / kChunk2;
-    for (int ch = 0; ch < n2; ++ch) L->items.push_back(code(2, u, ch));
-  }
-  L->total_items = (int)L->items.size();
   size_t off = 0;
   auto region = [&](size_t* o, size_t bytes) {
     *o = off;
     off = round256(off + bytes);
   };
   region(&L->off_status, 16);
-  region(&L->off_queue, 2 * sizeof(int));
-  region(&L->off_s1count, (size_t)L->units * sizeof(int));
+  region(&L->off_lnew, (size_t)c->batch * sizeof(int));
   region(&L->off_mcount, (size_t)L->units * sizeof(int));
-  region(&L->off_ready, (size_t)L->units * sizeof(int));
-  region(&L->off_items, (size_t)L->total_items * sizeof(int));  // everything before is zeroed per fresh start
+  region(&L->off_s2count, (size_t)L->units * sizeof(int));
+  region(&L->off_unit_hist, (size_t)L->units * 256 * sizeof(unsigned));  // everything before chunk_rec is zeroed per fresh start
   region(&L->off_chunk_rec, (size_t)L->total_chunks * G * 4 * sizeof(float));
   region(&L->off_chunk_z, (size_t)L->total_chunks * G * kChunk * sizeof(float));
   region(&L->off_chunk_u, (size_t)L->total_chunks * G * kChunk * sizeof(float));
@@ -127,7 +121,7 @@ compkv_status make_layout(const compkv_config* c, Layout* L) {
   region(&L->off_unit_ref, (size_t)L->units * G * sizeof(float));
   region(&L->off_unit_acc, (size_t)L->units * G * (d + 4) * sizeof(float));
   region(&L->off_unit_nsel, (size_t)L->units * sizeof(int));
-  region(&L->off_bitmap, (size_t)L->units * L->bm_words * sizeof(unsigned));
+  region(&L->off_skeys, (size_t)L->units * L->key_stride * sizeof(uint32_t));
   region(&L->off_sel, (size_t)L->units * L->K * sizeof(int));
   L->total = off;
   return COMPKV_OK;
@@ -148,8 +142,6 @@ struct compkv_ctx {
   compkv_buffers buf;
   Layout lay;
   int64_t launches = 0;
-  int epoch = 0;
-  int sms = 0;
   unsigned long long* trace = nullptr;
   int trace_cap = 0;
   bool prof = false;
@@ -187,17 +179,17 @@ LayerArgs base_args(const compkv_ctx* c, int layer) {
   a.splits = c->lay.splits;
   char* sc = reinterpret_cast<char*>(c->buf.scratch);
   a.status = reinterpret_cast<int*>(sc + c->lay.off_status);
-  a.items = reinterpret_cast<const int*>(sc + c->lay.off_items);
-  a.total_items = c->lay.total_items;
-  a.ticket = reinterpret_cast<int*>(sc + c->lay.off_queue);
-  a.done = a.ticket + 1;
-  a.s1count = reinterpret_cast<int*>(sc + c->lay.off_s1count);
+  a.lnew = reinterpret_cast<int*>(sc + c->lay.off_lnew);
   a.mcount = reinterpret_cast<int*>(sc + c->lay.off_mcount);
-  a.ready = reinterpret_cast<int*>(sc + c->lay.off_ready);
-  a.region_bytes = c->lay.region_bytes;
+  a.s2count = reinterpret_cast<int*>(sc + c->lay.off_s2count);
+  a.unit_hist = reinterpret_cast<unsigned*>(sc + c->lay.off_unit_hist);
+  a.skeys = reinterpret_cast<uint32_t*>(sc + c->lay.off_skeys);
+  a.key_stride = c->lay.key_stride;
+  a.total_chunks = c->lay.total_chunks;
+  a.n2_items = c->lay.n2_items;
+  a.ns_items = c->lay.ns_items;
   a.trace = c->trace;
   a.trace_cap = c->trace_cap;
-  a.stages = c->lay.stages;
   a.chunk_rec = reinterpret_cast<float*>(sc + c->lay.off_chunk_rec);
   a.chunk_z = reinterpret_cast<float*>(sc + c->lay.off_chunk_z);
   a.chunk_u = reinterpret_cast<float*>(sc + c->lay.off_chunk_u);
@@ -205,14 +197,15 @@ LayerArgs base_args(const compkv_ctx* c, int layer) {
   a.unit_ref = reinterpret_cast<float*>(sc + c->lay.off_unit_ref);
   a.unit_acc = reinterpret_cast<float*>(sc + c->lay.off_unit_acc);
   a.unit_nsel = reinterpret_cast<int*>(sc + c->lay.off_unit_nsel);
-  a.bitmap = reinterpret_cast<unsigned*>(sc + c->lay.off_bitmap);
-  a.bm_words = c->lay.bm_words;
   a.sel = reinterpret_cast<int*>(sc + c->lay.off_sel);
   for (int s = 0; s < c->cfg.batch; ++s) {
     a.seq_row0[s] = c->lay.seq_row0[s];
     a.cap_blocks[s] = c->lay.cap_blocks[s];
     a.chunk0[s] = c->lay.chunk0[s];
     a.nchunk[s] = c->lay.nchunk[s];
+    a.n2_first[s] = c->lay.n2_first[s];
+    a.ns_first[s] = c->lay.ns_first[s];
+    a.nchunk2[s] = c->lay.nchunk2[s];
   }
   return a;
 }
@@ -252,9 +245,9 @@ cudaEvent_t take_event(compkv_ctx* c) {
   return e;
 }
 
-// Launch one kernel (counted), bracketed by events when profiling is on.
+// Launch `kernels` kernels (counted), bracketed by events when profiling is on.
 template <class F>
-compkv_status launch(compkv_ctx* c, int family, cudaStream_t st, const char* what, F&& fn) {
+compkv_status launch(compkv_ctx* c, int family, cudaStream_t st, const char* what, F&& fn, int kernels = 1) {
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   if (c->prof) {
     e0 = take_event(c);
@@ -271,13 +264,15 @@ compkv_status launch(compkv_ctx* c, int family, cudaStream_t st, const char* wha
     cudaEventRecord(e1, st);
     c->slots[family].pending.emplace_back(e0, e1);
   }
-  c->launches += 1;
+  c->launches += kernels;
   return COMPKV_OK;
 }
 
-int fused_grid(const compkv_ctx* c) {
-  const int g = c->sms > 0 ? c->sms : 1;
-  return g < c->lay.total_items ? g : c->lay.total_items;
+compkv_status launch_chain(compkv_ctx* c, int family, const LayerArgs& a, int mode, cudaStream_t st, const char* what) {
+  return launch(
+      c, family, st, what,
+      [&] { return launch_decode_chain(a, mode, st, 1); },
+      chain_kernels(mode));
 }
 
 }  // namespace
@@ -319,13 +314,7 @@ compkv_status compkv_init(const compkv_config* cfg, const compkv_buffers* bufs, 
   c->buf = *bufs;
   c->lay = L;
   cudaError_t e = cudaMemsetAsync(bufs->scratch, 0, L.total, 0);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(reinterpret_cast<char*>(bufs->scratch) + L.off_items, L.items.data(),
-                        L.items.size() * sizeof(int), cudaMemcpyHostToDevice, 0);
   if (e == cudaSuccess) e = cudaStreamSynchronize(0);
-  int dev = 0;
-  if (e == cudaSuccess) e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) {
     delete c;
     return cuda_status(e, "initialising scratch");
@@ -383,10 +372,7 @@ compkv_status compkv_score_select(compkv_ctx* c, int layer, const float* q, int*
   a.scores = scores;
   a.score_stride = c->lay.max_cap_blocks;
   cudaStream_t st = (cudaStream_t)stream;
-  a.epoch = ++c->epoch;
-  a.total_items = c->lay.phase1_items;
-  COMPKV_TRY(launch(c, COMPKV_KERNEL_SCORE, st, "score/select launch",
-                    [&] { return launch_fused(a, kFusedScoreSelect, fused_grid(c), st); }));
+  COMPKV_TRY(launch_chain(c, COMPKV_KERNEL_SCORE, a, kFusedScoreSelect, st, "score/select launch"));
   return COMPKV_OK;
 }
 
@@ -400,9 +386,7 @@ compkv_status compkv_attend(compkv_ctx* c, int layer, const float* q, const int*
   a.sel = const_cast<int*>(sel);
   a.out = out;
   cudaStream_t st = (cudaStream_t)stream;
-  a.epoch = ++c->epoch;
-  COMPKV_TRY(launch(c, COMPKV_KERNEL_ATTEND, st, "attend launch",
-                    [&] { return launch_fused(a, kFusedAttend, fused_grid(c), st); }));
+  COMPKV_TRY(launch_chain(c, COMPKV_KERNEL_ATTEND, a, kFusedAttend, st, "attend launch"));
   return COMPKV_OK;
 }
 
@@ -421,9 +405,7 @@ compkv_status compkv_decode(compkv_ctx* c, int layer, const float* q, const void
   a.out = out;
   if (sel) a.sel = sel;
   cudaStream_t st = (cudaStream_t)stream;
-  a.epoch = ++c->epoch;
-  COMPKV_TRY(launch(c, COMPKV_KERNEL_DECODE, st, "decode launch",
-                    [&] { return launch_fused(a, kFusedDecode, fused_grid(c), st); }));
+  COMPKV_TRY(launch_chain(c, COMPKV_KERNEL_DECODE, a, kFusedDecode, st, "decode launch"));
   return COMPKV_OK;
 }
 
@@ -451,9 +433,10 @@ compkv_status compkv_trace(compkv_ctx* c, void* buf, size_t bytes) {
     return COMPKV_OK;
   }
   COMPKV_TRY(check_ptr(buf, "trace buffer", 8));
-  if (bytes < 8 + 40) return fail(COMPKV_ERR_INVALID_ARG, "trace buffer of %zu bytes holds no record", bytes);
+  const size_t header = 8;
+  if (bytes < header + 64) return fail(COMPKV_ERR_INVALID_ARG, "trace buffer of %zu bytes holds no record", bytes);
   c->trace = reinterpret_cast<unsigned long long*>(buf);
-  const size_t cap = (bytes - 8) / 40;
+  const size_t cap = (bytes - header) / 64;
   c->trace_cap = cap > 0x7fffffff ? 0x7fffffff : (int)cap;
   return COMPKV_OK;
 }
@@ -512,9 +495,9 @@ compkv_status compkv_internal_fail(compkv_status st, const char* what, const cha
 
 // Decode step with a scratch buffer supplied by the caller of this function
 // instead of by a context: used by the scratch-free entry point
-// (static_scratch.cu).  The queue, counters and status at the start of the
-// scratch are zeroed and the work queue is uploaded on `stream` before the
-// launch, so consecutive calls that share the buffer start clean.
+// (static_scratch.cu).  The status word and counters at the start of the
+// scratch are zeroed on `stream` before the launches, so consecutive calls
+// that share the buffer start clean.
 compkv_status compkv_internal_decode_in(const compkv_config* cfg, const compkv_buffers* bufs, void* scratch,
                                         size_t scratch_bytes, int layer, const float* q, const void* k_new,
                                         const void* v_new, float* out, int* sel, void* stream) {
@@ -547,21 +530,14 @@ compkv_status compkv_internal_decode_in(const compkv_config* cfg, const compkv_b
   c.buf.scratch = scratch;
   c.buf.scratch_bytes = scratch_bytes;
   c.lay = L;
-  int dev = 0;
-  COMPKV_TRY(cuda_status(cudaGetDevice(&dev), "cudaGetDevice"));
-  COMPKV_TRY(cuda_status(cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev), "SM count"));
   cudaStream_t st = (cudaStream_t)stream;
-  COMPKV_TRY(cuda_status(cudaMemsetAsync(scratch, 0, L.off_items, st), "clearing scratch"));
-  COMPKV_TRY(cuda_status(cudaMemcpyAsync(reinterpret_cast<char*>(scratch) + L.off_items, L.items.data(),
-                                         L.items.size() * sizeof(int), cudaMemcpyHostToDevice, st),
-                         "uploading the work queue"));
+  COMPKV_TRY(cuda_status(cudaMemsetAsync(scratch, 0, L.off_chunk_rec, st), "clearing scratch"));
   LayerArgs a = base_args(&c, layer);
   a.q = q;
   a.k_new = reinterpret_cast<const __nv_bfloat16*>(k_new);
   a.v_new = reinterpret_cast<const __nv_bfloat16*>(v_new);
   a.out = out;
   if (sel) a.sel = sel;
-  a.epoch = 1;  // the ready tags were just cleared
-  COMPKV_TRY(cuda_status(launch_fused(a, kFusedDecode, fused_grid(&c), st), "decode launch"));
+  COMPKV_TRY(cuda_status(launch_decode_chain(a, kFusedDecode, st, 1), "decode launch"));
   return COMPKV_OK;
 }

@@ -48,29 +48,28 @@ struct LayerArgs {
   int splits;                 // attention work items per unit (sequence, head)
   // scratch
   int* status;                // [4]: code, sequence, head, site
+  int* lnew;                  // [B] tokens of each sequence in this call (after its append)
   float* chunk_rec;           // [chunk records][G][4]: max a, sum e^(a - max a), max(ln|b| + zbar), -
   float* chunk_z;             // [chunk records][G][kChunk]  zbar per block
   float* chunk_u;             // [chunk records][G][kChunk]  e^(a - max a) * sigma2 per block
   float* split_rec;           // [units][splits][G][4 + d]: m, l, -, -, acc[d]
   float* unit_ref;            // [units][G]  reference exponent of the compensation weights
-  float* unit_acc;            // [units][G][d + 4]: sum_b w vbar_b, then sum_b w at [d]
+  float* unit_acc;            // [units][G][d + 4]: sum_b w vbar_b over all blocks, then sum_b w at [d]
   int* unit_nsel;             // [units] selected blocks
-  unsigned* bitmap;           // [units][bm_words] selected-block bitmap
-  int bm_words;
-  // persistent work queue of the fused kernel
-  const int* items;           // encoded work items (type | unit | index)
-  int total_items;            // items of this launch (a prefix of the queue)
-  int* ticket;                // next ticket
-  int* done;                  // CTAs that have left the queue
-  int* s1count;               // [units] scoring items finished
-  int* mcount;                // [units] attention + compensation items finished
-  int* ready;                 // [units] epoch at which the unit was selected
-  int epoch;                  // launch counter of this context (> 0)
-  int region_bytes;           // per-stage shared-memory region
-  int stages;                 // 2 or 3
-  // optional trace of the fused kernel's work items (null: off)
-  unsigned long long* trace;  // [0] = records written, then records of 5 words
-  int trace_cap;              // records that fit
+  uint32_t* skeys;            // [units][key_stride] S_b as order-preserving keys
+  int key_stride;             // max capacity in blocks, rounded up to a multiple of 4
+  unsigned* unit_hist;        // [units][256] exponent histogram of the keys (reset by its reader)
+  int* s2count;               // [units] S items finished (reset by the last)
+  int* mcount;                // [units] attention items finished (reset by the last)
+  int total_chunks;           // scoring items of the layer (64 blocks)
+  int ns_items;               // S items of the layer (512 blocks)
+  int n2_items;               // compensation items of the layer (128 blocks)
+  int ns_first[kMaxBatch];    // first S item of (s, head 0)
+  int n2_first[kMaxBatch];    // first compensation item of (s, head 0)
+  int nchunk2[kMaxBatch];     // compensation items per (s, head)
+  // optional trace of the work items (null: off)
+  unsigned long long* trace;  // see compkv_trace
+  int trace_cap;
   // ragged tables
   int64_t seq_row0[kMaxBatch];   // first row of (s, head 0) relative to the layer
   int cap_blocks[kMaxBatch];     // capacity of sequence s in blocks
@@ -88,20 +87,6 @@ __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
-}
-
-// One trace record: (cta << 32 | type << 24 | index), unit, t0, t1, t2 (ns).
-__device__ __forceinline__ void trace_record(const LayerArgs& a, int type, int unit, int index, unsigned long long t0,
-                                             unsigned long long t1, unsigned long long t2) {
-  if (!a.trace) return;
-  const unsigned long long i = atomicAdd(a.trace, 1ull);
-  if (i >= (unsigned long long)a.trace_cap) return;
-  unsigned long long* r = a.trace + 1 + 5 * i;
-  r[0] = ((unsigned long long)blockIdx.x << 32) | ((unsigned long long)(type & 0xff) << 24) | (unsigned)(index & 0xffffff);
-  r[1] = (unsigned long long)unit;
-  r[2] = t0;
-  r[3] = t1;
-  r[4] = t2;
 }
 
 // ---------------------------------------------------------------- status
@@ -140,22 +125,25 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// Test for completion of phase `parity`; a waiting thread is suspended (it
+// issues nothing) until the phase completes or about kSuspendNs pass.
+constexpr uint32_t kSuspendNs = 1000000;
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendNs)
       : "memory");
   return ok != 0;
 }
 
 // Wait for phase `parity` of `bar`; gives up after a bounded number of polls
-// (each try_wait itself blocks for a hardware-defined time slice), records
-// a timeout in the status word and returns false.
-constexpr uint32_t kWaitPolls = 1u << 22;
+// (a few seconds at most), records a timeout in the status word and returns
+// false.
+constexpr uint32_t kWaitPolls = 1u << 12;
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status, int s, int h,
                                                   int site) {
   for (uint32_t i = 0; i < kWaitPolls; ++i)

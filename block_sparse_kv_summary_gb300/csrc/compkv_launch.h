@@ -8,7 +8,7 @@
 
 namespace compkv {
 
-// Parts of the decode step a fused launch runs.
+// Parts of the decode step a launch chain runs.
 enum FusedFlags : int {
   kFAppend = 1,   // pack the new token and recompute the open block's summary
   kFScore = 2,    // sigma2, a = ln|b| + zbar + sigma2/2 and the per-item logsumexp parts
@@ -19,14 +19,20 @@ enum FusedFlags : int {
 constexpr int kFusedDecode = kFAppend | kFScore | kFComp | kFSelect | kFAttend;
 constexpr int kFusedScoreSelect = kFScore | kFSelect;
 constexpr int kFusedAttend = kFComp | kFAttend;
-constexpr int kAttendBlocks = 12;  // selected blocks per attention work item (= consumer warps)
+constexpr int kAttendBlocks = 8;  // selected blocks per attention CTA (one per warp)
 
 cudaError_t launch_prefill(const LayerArgs& a, int64_t rows_per_layer, cudaStream_t st);
 cudaError_t launch_append(const LayerArgs& a, cudaStream_t st);
-cudaError_t launch_fused(const LayerArgs& a, int mode, int grid, cudaStream_t st);
 
-int fused_region_bytes(int D, int r, int G, int max_cap_blocks);
-int fused_stages(int D, int r, int G, int max_cap_blocks, size_t smem_limit);
-size_t fused_smem_bytes(int D, int r, int G, int max_cap_blocks, int stages);
+// The decode step as three kernels on `st` (score; select and compensation;
+// attend), chained with programmatic dependent launch.  `mode` is one of
+// kFusedDecode, kFusedScoreSelect (score, select) or kFusedAttend (score for
+// zbar, compensation, attend a caller-given selection).  `first_pdl` lets the
+// first kernel overlap the tail of the previous work on the stream.
+cudaError_t launch_decode_chain(const LayerArgs& a, int mode, cudaStream_t st, int first_pdl);
+// Kernels a chain of `mode` launches.
+inline int chain_kernels(int mode) { return (mode & kFAttend) ? 3 : 2; }
+// Largest dynamic shared memory the chain asks for.
+size_t chain_smem_bytes(int D, int r, int G, int key_stride);
 
 }  // namespace compkv

@@ -176,8 +176,8 @@ compkv_status compkv_decode(compkv_ctx *ctx, int layer, const float *q, const vo
  * that loads the library holds until the process exits.  A configuration
  * whose compkv_scratch_bytes() exceeds that size is rejected with
  * COMPKV_ERR_UNSUPPORTED_SHAPE and a message naming both sizes.  The call
- * allocates nothing; it enqueues a clear of the array's counters, a copy of
- * its work queue and the kernel on `stream`.  The first call on each device
+ * allocates nothing; it enqueues a clear of the array's status word and
+ * counters and the decode kernels on `stream`.  The first call on each device
  * (with that device current) looks up the array's device address once; make
  * that first call before any stream capture.  All calls share the one array,
  * so calls whose work overlaps on the GPU (different streams, or several host
@@ -214,16 +214,27 @@ enum {
 };
 compkv_status compkv_profile_enable(compkv_ctx *ctx, int enable);
 
-/* Work-item trace of the fused decode kernel (tracing aid, off by default).
- * buf: caller device memory, 8-byte aligned, `bytes` long; word 0 counts the
- * records written (the caller zeroes it before the launches it wants to
- * trace) and record i occupies words 1 + 5i .. 5 + 5i:
- *   (cta << 32 | type << 24 | index), unit, t0, t1, t2   (%globaltimer ns)
- * Consumer records (type 0 scoring, 1 attention, 2 compensation, 3 select,
- * 4 merge): t0 = item received, t1 = end of the wait for its unit (= t0 when
- * it waits for nothing), t2 = item done.  Producer records (type 16 + item
- * type): t0 = before claiming the next ticket, t2 = item published.  Records
- * beyond the capacity are dropped.  buf = NULL switches tracing off. */
+/* Work-item trace of the decode kernels (tracing aid, off by default).
+ * buf: caller device memory, 8-byte aligned, `bytes` long, zeroed by the
+ * caller before a traced call.  Word 0 is unused; record slot i occupies
+ * words 1 + 8 i .. 8 + 8 i, for i < (bytes - 8) / 64 (slots beyond are not
+ * written):
+ *   (cta << 32 | type << 24 | index), unit, t0, t1, t2, x0, x1, x2
+ * (times in %globaltimer ns; a scoring CTA's x0 = end of its wait for the
+ * previous kernel, x1 = first half of its rows landed, x2 = first half scored).
+ * unit = sequence * Hkv + head.  With C scoring items (64 blocks), S
+ * S items (512 blocks), I compensation items (128 blocks), U units and A
+ * attention CTAs, slots [0, C) hold the scoring CTAs (type 0: t0 start, t1
+ * its rows scored, t2 done), [C, C + S + I) the S items (type 7) and the
+ * compensation items (type 2) (t0 start, t1 end of the wait for the scoring
+ * kernel, t2 done), [C + S + I, ... + U) each unit's selection (type 3, t0 =
+ * t1 start), then the attention CTAs (type 1, or 4 for the CTA that merged
+ * the unit: t0 start, t1 end of the wait for the selection, x0 partial
+ * computed, x1 partial stored), then 32 per unit for the selection's phases
+ * (type 5: index = phase, t0..t1 its span; type 6: index = radix level, t0 =
+ * keys at the threshold digit, t1 = list length or -1).  A slot a call does
+ * not use stays as the caller left it.
+ * buf = NULL switches tracing off. */
 compkv_status compkv_trace(compkv_ctx *ctx, void *buf, size_t bytes);
 compkv_status compkv_profile_read(compkv_ctx *ctx, int family, double *total_ms, int64_t *launches);
 
