@@ -2,6 +2,7 @@
 // and the launch sequence of each call.  See include/compkv.h for the contract.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -34,12 +35,13 @@ struct Layout {
   int64_t rows_per_layer = 0;
   int total_chunks = 0;
   int max_cap_blocks = 0;
-  std::vector<int> n2_first, nchunk2, ns_first;
-  int n2_items = 0, ns_items = 0;
+  std::vector<int> ns_first;
+  int ns_items = 0;
   int K = 0, splits = 0, units = 0, key_stride = 0;
-  size_t off_status = 0, off_lnew = 0, off_mcount = 0, off_s2count = 0, off_unit_hist = 0, off_chunk_rec = 0,
-         off_chunk_z = 0, off_chunk_u = 0, off_split = 0, off_unit_ref = 0, off_unit_acc = 0, off_unit_nsel = 0,
-         off_skeys = 0, off_sel = 0, total = 0;
+  size_t off_status = 0, off_lnew = 0, off_mcount = 0, off_hist12 = 0, off_chunk_rec = 0, off_chunk_z = 0,
+         off_chunk_u = 0, off_unit_ref = 0, off_unit_acc = 0, off_comp_part = 0, off_unit_nsel = 0,
+         off_skeys = 0,
+         off_sel = 0, total = 0;
 };
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -73,10 +75,8 @@ compkv_status make_layout(const compkv_config* c, Layout* L) {
   L->seq_row0.resize(c->batch);
   L->chunk0.resize(c->batch);
   L->nchunk.resize(c->batch);
-  L->n2_first.resize(c->batch);
-  L->nchunk2.resize(c->batch);
   L->ns_first.resize(c->batch);
-  int64_t row = 0, ch = 0, ch2 = 0, chs = 0;
+  int64_t row = 0, ch = 0, chs = 0;
   L->max_cap_blocks = 0;
   for (int s = 0; s < c->batch; ++s) {
     L->seq_row0[s] = row;
@@ -84,25 +84,23 @@ compkv_status make_layout(const compkv_config* c, Layout* L) {
     L->nchunk[s] = (L->cap_blocks[s] + kChunk - 1) / kChunk;
     L->chunk0[s] = (int)ch;
     ch += (int64_t)H * L->nchunk[s];
-    L->nchunk2[s] = (L->cap_blocks[s] + kChunk2 - 1) / kChunk2;
-    L->n2_first[s] = (int)ch2;
-    ch2 += (int64_t)H * L->nchunk2[s];
     L->ns_first[s] = (int)chs;
     chs += (int64_t)H * ((L->nchunk[s] + 7) / 8);
     if (L->cap_blocks[s] > L->max_cap_blocks) L->max_cap_blocks = L->cap_blocks[s];
   }
   // grids of the scoring and compensation kernels (x dimension)
-  if (ch > 0x7fffffff || ch2 > 0x7fffffff) return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "too many scoring work items");
+  if (ch > 0x7fffffff || chs > 0x7fffffff) return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "too many scoring work items");
   L->rows_per_layer = row;
   L->total_chunks = (int)ch;
-  L->n2_items = (int)ch2;
   L->ns_items = (int)chs;
   L->key_stride = (L->max_cap_blocks + 3) & ~3;
   if (chain_smem_bytes(d, c->r, G, L->key_stride) > kMaxSmem)
     return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "a sequence capacity of %d blocks does not fit the selection in shared memory",
                 L->max_cap_blocks);
   L->K = c->budget_tokens / kBlock;
+  // attention CTAs per unit: one cluster of up to 16, 8 selected blocks per CTA and round
   L->splits = (L->K + kAttendBlocks - 1) / kAttendBlocks;
+  if (L->splits > 16) L->splits = 16;
   L->units = c->batch * H;
   size_t off = 0;
   auto region = [&](size_t* o, size_t bytes) {
@@ -112,14 +110,13 @@ compkv_status make_layout(const compkv_config* c, Layout* L) {
   region(&L->off_status, 16);
   region(&L->off_lnew, (size_t)c->batch * sizeof(int));
   region(&L->off_mcount, (size_t)L->units * sizeof(int));
-  region(&L->off_s2count, (size_t)L->units * sizeof(int));
-  region(&L->off_unit_hist, (size_t)L->units * 256 * sizeof(unsigned));  // everything before chunk_rec is zeroed per fresh start
+  region(&L->off_hist12, (size_t)L->units * 4096 * sizeof(unsigned));  // everything before chunk_rec is zeroed per fresh start
   region(&L->off_chunk_rec, (size_t)L->total_chunks * G * 4 * sizeof(float));
   region(&L->off_chunk_z, (size_t)L->total_chunks * G * kChunk * sizeof(float));
   region(&L->off_chunk_u, (size_t)L->total_chunks * G * kChunk * sizeof(float));
-  region(&L->off_split, (size_t)L->units * L->splits * G * (4 + d) * sizeof(float));
   region(&L->off_unit_ref, (size_t)L->units * G * sizeof(float));
   region(&L->off_unit_acc, (size_t)L->units * G * (d + 4) * sizeof(float));
+  region(&L->off_comp_part, (size_t)L->total_chunks * G * (d + 4) * sizeof(float));
   region(&L->off_unit_nsel, (size_t)L->units * sizeof(int));
   region(&L->off_skeys, (size_t)L->units * L->key_stride * sizeof(uint32_t));
   region(&L->off_sel, (size_t)L->units * L->K * sizeof(int));
@@ -159,6 +156,21 @@ struct compkv_ctx {
 
 namespace {
 
+// Multiprocessors of the current device (queried once per device).
+int device_sms() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < 64) {
+    const int v = cached[dev].load();
+    if (v > 0) return v;
+  }
+  int n = 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+  if (dev >= 0 && dev < 64) cached[dev].store(n);
+  return n;
+}
+
 LayerArgs base_args(const compkv_ctx* c, int layer) {
   LayerArgs a;
   memset(&a, 0, sizeof(a));
@@ -181,21 +193,20 @@ LayerArgs base_args(const compkv_ctx* c, int layer) {
   a.status = reinterpret_cast<int*>(sc + c->lay.off_status);
   a.lnew = reinterpret_cast<int*>(sc + c->lay.off_lnew);
   a.mcount = reinterpret_cast<int*>(sc + c->lay.off_mcount);
-  a.s2count = reinterpret_cast<int*>(sc + c->lay.off_s2count);
-  a.unit_hist = reinterpret_cast<unsigned*>(sc + c->lay.off_unit_hist);
+  a.hist12 = reinterpret_cast<unsigned*>(sc + c->lay.off_hist12);
   a.skeys = reinterpret_cast<uint32_t*>(sc + c->lay.off_skeys);
   a.key_stride = c->lay.key_stride;
   a.total_chunks = c->lay.total_chunks;
-  a.n2_items = c->lay.n2_items;
+  a.sms = device_sms();
   a.ns_items = c->lay.ns_items;
   a.trace = c->trace;
   a.trace_cap = c->trace_cap;
   a.chunk_rec = reinterpret_cast<float*>(sc + c->lay.off_chunk_rec);
   a.chunk_z = reinterpret_cast<float*>(sc + c->lay.off_chunk_z);
   a.chunk_u = reinterpret_cast<float*>(sc + c->lay.off_chunk_u);
-  a.split_rec = reinterpret_cast<float*>(sc + c->lay.off_split);
   a.unit_ref = reinterpret_cast<float*>(sc + c->lay.off_unit_ref);
   a.unit_acc = reinterpret_cast<float*>(sc + c->lay.off_unit_acc);
+  a.comp_part = reinterpret_cast<float*>(sc + c->lay.off_comp_part);
   a.unit_nsel = reinterpret_cast<int*>(sc + c->lay.off_unit_nsel);
   a.sel = reinterpret_cast<int*>(sc + c->lay.off_sel);
   for (int s = 0; s < c->cfg.batch; ++s) {
@@ -203,9 +214,7 @@ LayerArgs base_args(const compkv_ctx* c, int layer) {
     a.cap_blocks[s] = c->lay.cap_blocks[s];
     a.chunk0[s] = c->lay.chunk0[s];
     a.nchunk[s] = c->lay.nchunk[s];
-    a.n2_first[s] = c->lay.n2_first[s];
     a.ns_first[s] = c->lay.ns_first[s];
-    a.nchunk2[s] = c->lay.nchunk2[s];
   }
   return a;
 }

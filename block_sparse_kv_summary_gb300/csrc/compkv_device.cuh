@@ -14,7 +14,6 @@ namespace compkv {
 constexpr int kBlock = 16;        // tokens per KV block (CompKV, "전제와 한계": block size 16)
 constexpr int kMaxBatch = 64;     // sequences per call (launch arguments hold per-sequence tables)
 constexpr int kChunk = 64;        // blocks per scoring work item (and per scoring record)
-constexpr int kChunk2 = 128;      // blocks per compensation work item
 constexpr int kMaxG = 8;
 
 // Device status word codes (mirrors compkv_status).
@@ -45,28 +44,25 @@ struct LayerArgs {
   int score_stride;
   // shape
   int B, Hkv, G, d, r, K;
-  int splits;                 // attention work items per unit (sequence, head)
+  int splits;                 // attention CTAs per unit (one cluster)
   // scratch
   int* status;                // [4]: code, sequence, head, site
   int* lnew;                  // [B] tokens of each sequence in this call (after its append)
   float* chunk_rec;           // [chunk records][G][4]: max a, sum e^(a - max a), max(ln|b| + zbar), -
   float* chunk_z;             // [chunk records][G][kChunk]  zbar per block
   float* chunk_u;             // [chunk records][G][kChunk]  e^(a - max a) * sigma2 per block
-  float* split_rec;           // [units][splits][G][4 + d]: m, l, -, -, acc[d]
   float* unit_ref;            // [units][G]  reference exponent of the compensation weights
   float* unit_acc;            // [units][G][d + 4]: sum_b w vbar_b over all blocks, then sum_b w at [d]
+  float* comp_part;           // [chunk records][G][d + 4]: the chunk's sums with w relative to its own max
   int* unit_nsel;             // [units] selected blocks
   uint32_t* skeys;            // [units][key_stride] S_b as order-preserving keys
   int key_stride;             // max capacity in blocks, rounded up to a multiple of 4
-  unsigned* unit_hist;        // [units][256] exponent histogram of the keys (reset by its reader)
-  int* s2count;               // [units] S items finished (reset by the last)
+  unsigned* hist12;           // [units][4096] histogram of the keys' top 12 bits (reset by the unit's selection)
   int* mcount;                // [units] attention items finished (reset by the last)
   int total_chunks;           // scoring items of the layer (64 blocks)
+  int sms;                    // multiprocessors of the device (persistent grids)
   int ns_items;               // S items of the layer (512 blocks)
-  int n2_items;               // compensation items of the layer (128 blocks)
   int ns_first[kMaxBatch];    // first S item of (s, head 0)
-  int n2_first[kMaxBatch];    // first compensation item of (s, head 0)
-  int nchunk2[kMaxBatch];     // compensation items per (s, head)
   // optional trace of the work items (null: off)
   unsigned long long* trace;  // see compkv_trace
   int trace_cap;

@@ -15,11 +15,14 @@
 //              item's max a, sum e^(a - max a), max(ln|b| + zbar), and per
 //              block u = e^(a - max a) sigma2 and zbar.  The item holding the
 //              newest token appends it first.
-//   2. S items     one CTA per 512 blocks of a unit: LSE_g from the scoring
+//   2a. S items    one CTA per 512 blocks of a unit: LSE_g from the scoring
 //              records, S_b = sum_g u e^(max a - LSE_g) = sum_g phat sigma2 as
-//              order-preserving keys, their exponent histogram; the unit's
-//              last S item selects: forced set + the K-3 largest S_b by an
-//              exponent-first radix select (ties to the lower index).
+//              order-preserving keys, a histogram of their top 12 bits.
+//   2b. select     one CTA per unit: the threshold bin of the K-3 largest
+//              candidates from the histogram, one pass over the unit's keys
+//              for the selection bitmap and the threshold bin's short list,
+//              which is ranked (ties to the lower index); the ascending
+//              selection from the bitmap.
 //      comp items  in the same grid, one CTA per 128 blocks of a unit: their
 //              vbar rows (bulk-copied before the dependency wait, overlapping
 //              the scoring kernel's tail) weighted by w = e^(ln|b| + zbar -
@@ -44,7 +47,9 @@ constexpr int kW = kT / 32;
 constexpr int kPrivBins = 256;     // histogram bins of one radix digit
 constexpr int kListMax = 2048;     // keys in play compacted into a list once at most this many
 constexpr int kRankMax = 512;      // listed keys in play ranked directly once at most this many
-constexpr int kChunkS = 8 * kChunk;  // blocks per S item
+constexpr int kChunkS = 8 * kChunk;  // blocks per S item and per classify item
+constexpr int kDigitShift = 19;      // the classify digit: key bits 30..19 (exponent, 4 mantissa bits)
+constexpr int kHist12 = 1 << (31 - kDigitShift);
 
 template <int D>
 struct InvSqrt;
@@ -76,10 +81,10 @@ __device__ __forceinline__ int chunk_record(const LayerArgs& a, int s, int h, in
   return a.chunk0[s] + h * a.nchunk[s] + c;
 }
 
-// Trace slots: scoring CTAs, S items, compensation items, one selection record
-// per unit, attention CTAs, then 32 phase marks per unit.
+// Trace slots: scoring CTAs, S items, one selection record per unit, attention
+// CTAs, then 32 phase marks per unit.
 __device__ __forceinline__ int slot_items(const LayerArgs& a) { return a.total_chunks; }
-__device__ __forceinline__ int slot_select(const LayerArgs& a) { return a.total_chunks + a.ns_items + a.n2_items; }
+__device__ __forceinline__ int slot_select(const LayerArgs& a) { return a.total_chunks + a.ns_items; }
 __device__ __forceinline__ int slot_attend(const LayerArgs& a) { return slot_select(a) + a.B * a.Hkv; }
 __device__ __forceinline__ int slot_phase(const LayerArgs& a) { return slot_attend(a) + a.B * a.Hkv * a.splits; }
 
@@ -110,303 +115,473 @@ __device__ __forceinline__ unsigned long long trace_phase(const LayerArgs& a, in
 }
 
 // ================================================================== 1. score
-// Lane layout: lane = g * LPG + p; lane p of query head g holds coordinates
-// [p * DPL, (p + 1) * DPL) of q_g in 4-wide chunks, chunk i of the lane at
-// position (i + p) mod NCH so that the LPG lanes reading one kbar row touch
-// different banks.  A block costs a lane DPL FMAs for zbar and a few for
-// sigma2, then log2(LPG) butterfly steps.
-template <int D, int G>
-struct ScoreLayout {
-  static constexpr int LPG = 32 / G;         // lanes per query head
-  static constexpr int DPL = D / LPG;        // coordinates per lane (>= 2)
-  static constexpr int CW = DPL >= 4 ? 4 : DPL;
-  static constexpr int NCH = DPL / CW;       // chunks per lane
-};
+// zbar = q . kbar / sqrt(d) for the chunk's 64 blocks and the G query heads is
+// a small contraction (64 x d times d x G), done on the tensor cores with
+// mma.sync m16n8k8 in tf32 and a three-term split for fp32 accuracy:
+// x = hi + lo with hi = x rounded toward zero to tf32, lo = x - hi (exact),
+// x.y ~ hi.hi' + hi.lo' + lo.hi' (the dropped lo.lo' and the tf32 truncation
+// of lo are ~2^-20 relative).  Warp w takes the 16-block tile w & 3 and the
+// half w >> 2 of the coordinates; heads G..7 of the 8 MMA columns are zero.
+// Thread (gid = lane / 4, tig = lane % 4) holds, per 16-coordinate chunk j,
+// coordinates 16 j + 4 tig .. + 3 of its two rows (one 16-byte load each) and
+// of q_gid; a chunk is two k-steps.  sigma2 = (1/d) sum_t Qsq_t Dbar_t is
+// formed by the warps of the second half: by FMAs for r <= 8, else by a
+// second tf32 contraction over the r groups.
+constexpr int kZS = kChunk + 4;  // row stride of the zbar / sigma2 staging (banks)
 
-// shared memory: kbar rows | Dbar rows | variance scratch (D) | zbar, sigma2 | Qsq (G x r, padded
-// to 4) | 2 mbarriers
-__host__ __device__ inline int score_smem(int D, int r, int G) {
-  return (kChunk * (D + r) + D + 2 * G * kChunk + ((G * r + 3) & ~3)) * 4 + 32;
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+  hi = __float_as_uint(x) & 0xffffe000u;
+  lo = __float_as_uint(x - __uint_as_float(hi)) & 0xffffe000u;
 }
 
+__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// One k-step pair (a 16-coordinate chunk) of the three-term product:
+// x0, x1 = this thread's 4 coordinates of rows gid, gid + 8; y = its 4 of column gid.
+__device__ __forceinline__ void mma_chunk(float (&c)[4], const float4& x0, const float4& x1, const float4& y) {
+  uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
+  // k-step 0: columns tig, tig + 4 = coordinates 0, 1 of the chunk slice
+  split_tf32(x0.x, ah[0], al[0]);
+  split_tf32(x1.x, ah[1], al[1]);
+  split_tf32(x0.y, ah[2], al[2]);
+  split_tf32(x1.y, ah[3], al[3]);
+  split_tf32(y.x, bh0, bl0);
+  split_tf32(y.y, bh1, bl1);
+  mma_tf32(c, al, bh0, bh1);
+  mma_tf32(c, ah, bl0, bl1);
+  mma_tf32(c, ah, bh0, bh1);
+  // k-step 1: coordinates 2, 3
+  split_tf32(x0.z, ah[0], al[0]);
+  split_tf32(x1.z, ah[1], al[1]);
+  split_tf32(x0.w, ah[2], al[2]);
+  split_tf32(x1.w, ah[3], al[3]);
+  split_tf32(y.z, bh0, bl0);
+  split_tf32(y.w, bh1, bl1);
+  mma_tf32(c, al, bh0, bh1);
+  mma_tf32(c, ah, bl0, bl1);
+  mma_tf32(c, ah, bh0, bh1);
+}
+
+// Shared memory of the scoring kernel: one or two stages, each kbar rows (64 x D) |
+// Dbar rows (64 x r) | with the compensation, vbar rows (64 x D); then
+// variance scratch (D) | zbar, sigma2 (G x kZS each) | Qsq (G x r, padded to 4) |
+// partial products (4 tiles x 32 lanes x 4) | with the compensation, weights
+// (G x kZS) | 2 x 3 mbarriers.
+__host__ __device__ inline int score_stage_words(int D, int r, bool comp) {
+  return kChunk * D + kChunk * r + (comp ? kChunk * D : 0);
+}
+// zbar, sigma2, partial products and weights share a region with the append's
+// per-warp partial sums (2 x 8 x D), which are done with before they are needed
+__host__ __device__ inline int score_scratch_words(int D, int G) {
+  const int a = 2 * G * kZS + 512 + G * kZS, b = 2 * 8 * D;
+  return a > b ? a : b;
+}
+__host__ __device__ inline int score_smem(int D, int r, int G, bool comp, int stages) {
+  return (stages * score_stage_words(D, r, comp) + D + score_scratch_words(D, G) + ((G * r + 3) & ~3)) * 4 + 64;
+}
+
+// A scoring item (64 blocks of a unit) and where its rows are.
+struct ScoreChunk {
+  int s, h, c, u, L, N, b0, nb, nt, rec;
+  bool append;
+  int64_t row0;
+};
+
+template <bool APPEND>
+__device__ __forceinline__ ScoreChunk score_chunk(const LayerArgs& a, int idx) {
+  ScoreChunk k;
+  k.s = 0;
+  while (k.s + 1 < a.B && a.chunk0[k.s + 1] <= idx) ++k.s;
+  const int local = idx - a.chunk0[k.s];
+  k.h = local / a.nchunk[k.s];
+  k.c = local % a.nchunk[k.s];
+  k.u = k.s * a.Hkv + k.h;
+  bool fits;
+  k.L = unit_tokens(a, k.s, APPEND, &fits);
+  k.N = ceil_blocks(k.L);
+  k.b0 = k.c * kChunk;
+  k.nb = k.b0 < k.N ? min(kChunk, k.N - k.b0) : 0;
+  k.append = APPEND && fits && k.nb > 0 && k.b0 + k.nb == k.N;
+  k.nt = k.nb - (k.append ? 1 : 0);
+  k.rec = chunk_record(a, k.s, k.h, k.c);
+  k.row0 = row_of(a, k.s, k.h, k.b0);
+  return k;
+}
+
+// CTA i scores items i, i + gridDim.x, ...; with two stages the bulk copies
+// of the next item land in the other stage while this one is scored.
 template <int D, int G, int MODE>
-__global__ void __launch_bounds__(kT, 4) k_score(LayerArgs a) {
+__global__ void __launch_bounds__(kT, 3) k_score(LayerArgs a, int stages) {
   constexpr bool APPEND = (MODE & kFAppend) != 0;
   constexpr bool SCORE = (MODE & kFScore) != 0;
   constexpr bool COMP = (MODE & kFComp) != 0;
-  using SL = ScoreLayout<D, G>;
-  constexpr int LPG = SL::LPG, DPL = SL::DPL, CW = SL::CW, NCH = SL::NCH;
+  constexpr int JH = D / 32;  // 16-coordinate chunks per half of the coordinates
+  constexpr int SV = D;       // vbar row stride
+  constexpr int kHalf = kChunk / 2;
   extern __shared__ __align__(128) float sm[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const unsigned long long t_start = a.trace ? global_ns() : 0ull;
-  int s = 0;
-  while (s + 1 < a.B && a.chunk0[s + 1] <= (int)blockIdx.x) ++s;
-  const int local = blockIdx.x - a.chunk0[s];
-  const int h = local / a.nchunk[s], c = local % a.nchunk[s];
-  const int u = s * a.Hkv + h;
   const int r = a.r;
+  const int stage_words = score_stage_words(D, r, COMP);
+  float* svar = sm + stages * stage_words;
+  float* zs = svar + D;
+  float* ss = zs + G * kZS;
+  float* cx = ss + G * kZS;
+  float* sw = cx + 512;
+  float* sapp = zs;  // the append's per-warp partial sums [2][8][D]
+  float* sqs = zs + score_scratch_words(D, G);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sqs + ((G * r + 3) & ~3));  // [stage][half A, half B, vbar]
+  const bool dbar_bulk = SCORE && (r & 3) == 0;
   pdl_wait();  // the previous work on the stream may have written this cache
-  const unsigned long long t_pdl = a.trace ? global_ns() : 0ull;
-  bool fits;
-  const int L = unit_tokens(a, s, APPEND, &fits);
-  const int N = ceil_blocks(L);
   if (blockIdx.x == 0 && tid < a.B) {
     bool f2;
     a.lnew[tid] = unit_tokens(a, tid, APPEND, &f2);
   }
-  if (COMP && c == 0)
-    for (int i = tid; i < G * (D + 4); i += kT) a.unit_acc[(int64_t)u * G * (D + 4) + i] = 0.f;
   pdl_trigger();
-  const int b0 = c * kChunk;
-  if (b0 >= N) return;
-  const int nb = min(kChunk, N - b0);
-  const bool append = APPEND && fits && b0 + nb == N;
-  const int nt = nb - (append ? 1 : 0);  // rows copied from global memory
-  const int rec = chunk_record(a, s, h, c);
-  float* sk = sm;
-  float* sd = sk + kChunk * D;
-  float* svar = sd + kChunk * r;
-  float* zs = svar + D;
-  float* ss = zs + G * kChunk;
-  float* sqs = ss + G * kChunk;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(sqs + ((G * r + 3) & ~3));
-  const int64_t row0 = row_of(a, s, h, b0);
-  const bool dbar_bulk = SCORE && (r & 3) == 0;
-  constexpr int kHalf = kChunk / 2;
-  const int nA = min(nt, kHalf), nB = nt - nA;
   if (tid == 0) {
-    mbar_init(bar, 1);
-    mbar_init(bar + 1, 1);
+    for (int i = 0; i < 6; ++i) mbar_init(bars + i, 1);
     fence_mbar_init();
-    const uint32_t rowb = (uint32_t)D * 4u + (dbar_bulk ? (uint32_t)r * 4u : 0u);
-    mbar_arrive_expect_tx(bar, (uint32_t)nA * rowb);
-    if (nA > 0) {
-      bulk_g2s(sk, a.kbar + row0 * D, (uint32_t)nA * D * 4u, bar);
-      if (dbar_bulk) bulk_g2s(sd, a.dbar + row0 * r, (uint32_t)nA * r * 4u, bar);
-    }
-    mbar_arrive_expect_tx(bar + 1, (uint32_t)nB * rowb);
-    if (nB > 0) {
-      bulk_g2s(sk + kHalf * D, a.kbar + (row0 + kHalf) * D, (uint32_t)nB * D * 4u, bar + 1);
-      if (dbar_bulk) bulk_g2s(sd + kHalf * r, a.dbar + (row0 + kHalf) * r, (uint32_t)nB * r * 4u, bar + 1);
-    }
-  }
-  // this lane's slice of q_g straight from global memory (L2), while the rows land
-  const int g = lane / LPG, p = lane % LPG;
-  const float* qg_glob = a.q + ((int64_t)s * a.Hkv * G + (int64_t)h * G + g) * D;
-  float qr[NCH][CW];
-#pragma unroll
-  for (int i = 0; i < NCH; ++i) {
-    const int cpos = p * DPL + CW * ((i + p) & (NCH - 1));
-    if (CW == 4) {
-      const float4 x = __ldg(reinterpret_cast<const float4*>(qg_glob + cpos));
-      qr[i][0] = x.x;
-      qr[i][1 % CW] = x.y;
-      qr[i][2 % CW] = x.z;
-      qr[i][3 % CW] = x.w;
-    } else {
-      const float2 x = __ldg(reinterpret_cast<const float2*>(qg_glob + cpos));
-      qr[i][0] = x.x;
-      qr[i][1 % CW] = x.y;
-    }
-  }
-  if (SCORE && (r & 3))
-    for (int i = tid; i < nt * r; i += kT) sd[i] = a.dbar[row0 * r + i];
-  if (append) {
-    // pack the new token and recompute the open block's summary from its
-    // tokens: thread c < D owns key coordinate c, thread D + c value
-    // coordinate c; mean and population variance two-pass in fp32 from the
-    // exact bf16 values (no E[k^2] - E[k]^2 cancellation)
-    const int n = L - kBlock * (N - 1);
-    const int64_t row = row0 + (nb - 1);
-    if (tid < 2 * D) {
-      const bool isk = tid < D;
-      const int cc = isk ? tid : tid - D;
-      const __nv_bfloat16* src = (isk ? a.k : a.v) + row * kBlock * D + cc;
-      const __nv_bfloat16 xn = (isk ? a.k_new : a.v_new)[((int64_t)s * a.Hkv + h) * D + cc];
-      float x[kBlock];
-      float sum = 0.f;
-#pragma unroll
-      for (int j = 0; j < kBlock; ++j) {
-        x[j] = 0.f;
-        if (j < n - 1) x[j] = __bfloat162float(src[j * D]);
-        if (j == n - 1) x[j] = __bfloat162float(xn);
-        sum += x[j];
-      }
-      (isk ? a.k : a.v)[(row * kBlock + n - 1) * D + cc] = xn;
-      const float mean = sum / (float)n;
-      if (isk) {
-        float var = 0.f;
-#pragma unroll
-        for (int j = 0; j < kBlock; ++j)
-          if (j < n) var = fmaf(x[j] - mean, x[j] - mean, var);
-        sk[(nb - 1) * D + cc] = mean;
-        a.kbar[row * D + cc] = mean;
-        svar[cc] = var / (float)n;
-      } else {
-        a.vbar[row * D + cc] = mean;
-      }
-    }
-    __syncthreads();
-    if (tid < r) {
-      // Dbar_t: mean of the variances over coordinate group t = [t*D/r, (t+1)*D/r)
-      const int gs = D / r;
-      float t = 0.f;
-      for (int i = 0; i < gs; ++i) t += svar[tid * gs + i];
-      t /= (float)gs;
-      sd[(nb - 1) * r + tid] = t;
-      a.dbar[row * r + tid] = t;
-    }
   }
   __syncthreads();
-  mbar_wait_bounded(bar, 0, a.status, s, h, 10);
-  const unsigned long long t_a = a.trace ? global_ns() : 0ull;
-  // ---- zbar and sigma2: one block per warp at a time, query heads on lanes
-  // sigma2 weights: lanes whose coordinates lie in one group t (r <= LPG)
-  // weight Dbar_t by their sum of q^2; otherwise lane p takes the groups
-  // [p * rpl, (p + 1) * rpl), rotated like the kbar chunks, with Qsq_{g,t}
-  // from shared memory
-  const int gs = D / r;
-  const bool one_group = r <= LPG;
-  const int rpl = one_group ? 1 : r / LPG;
-  const int t_one = (p * DPL) / gs;
-  float qsq_one = 0.f;
-#pragma unroll
-  for (int i = 0; i < NCH; ++i)
-#pragma unroll
-    for (int j = 0; j < CW; ++j) qsq_one = fmaf(qr[i][j], qr[i][j], qsq_one);
-  if (SCORE && !one_group) {
-    for (int i = tid; i < G * r; i += kT) {
-      const float* qp = a.q + ((int64_t)s * a.Hkv * G + (int64_t)h * G + i / r) * D + (i % r) * gs;
-      float t = 0.f;
-      for (int k = 0; k < gs; ++k) t = fmaf(qp[k], qp[k], t);
-      sqs[i] = t;
-    }
-    __syncthreads();
-  }
-  auto do_block = [&](int blk) {
-    const float* krow = sk + blk * D + p * DPL;
-    float z = 0.f;
-#pragma unroll
-    for (int i = 0; i < NCH; ++i) {
-      const int off = CW * ((i + p) & (NCH - 1));
-      if (CW == 4) {
-        const float4 x = *reinterpret_cast<const float4*>(krow + off);
-        z = fmaf(qr[i][0], x.x, z);
-        z = fmaf(qr[i][1 % CW], x.y, z);
-        z = fmaf(qr[i][2 % CW], x.z, z);
-        z = fmaf(qr[i][3 % CW], x.w, z);
-      } else {
-        const float2 x = *reinterpret_cast<const float2*>(krow + off);
-        z = fmaf(qr[i][0], x.x, z);
-        z = fmaf(qr[i][1 % CW], x.y, z);
+  const int my_n = ((int)blockIdx.x < a.total_chunks) ? (a.total_chunks - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  // post the expected bytes of item k's stage and start its copies
+  auto issue = [&](const ScoreChunk& k, int st) {
+    float* sk = sm + st * stage_words;
+    float* sd = sk + kChunk * D;
+    float* sv = sd + kChunk * r;
+    uint64_t* bar = bars + 3 * st;
+    const int nA = min(k.nt, kHalf), nB = k.nt - nA;
+    if (tid == 0) {
+      const uint32_t rowb = (uint32_t)D * 4u + (dbar_bulk ? (uint32_t)r * 4u : 0u);
+      mbar_arrive_expect_tx(bar, (uint32_t)nA * rowb);
+      if (nA > 0) {
+        bulk_g2s(sk, a.kbar + k.row0 * D, (uint32_t)nA * D * 4u, bar);
+        if (dbar_bulk) bulk_g2s(sd, a.dbar + k.row0 * r, (uint32_t)nA * r * 4u, bar);
       }
+      mbar_arrive_expect_tx(bar + 1, (uint32_t)nB * rowb);
+      if (nB > 0) {
+        bulk_g2s(sk + kHalf * D, a.kbar + (k.row0 + kHalf) * D, (uint32_t)nB * D * 4u, bar + 1);
+        if (dbar_bulk) bulk_g2s(sd + kHalf * r, a.dbar + (k.row0 + kHalf) * r, (uint32_t)nB * r * 4u, bar + 1);
+      }
+      mbar_arrive_expect_tx(bar + 2, COMP ? (uint32_t)k.nt * D * 4u : 0u);
     }
-    float sg = 0.f;
-    if (SCORE) {
-      const float* drow = sd + blk * r;
-      if (one_group) {
-        sg = qsq_one * drow[t_one];
-      } else {
-        const float* qrow = sqs + g * r + p * rpl;
-        const float* dseg = drow + p * rpl;
-        for (int k = 0; k < rpl; ++k) {
-          const int t = (k + p) & (rpl - 1);
-          sg = fmaf(qrow[t], dseg[t], sg);
+    if (COMP && tid == 0 && k.nt > 0) bulk_g2s(sv, a.vbar + k.row0 * D, (uint32_t)k.nt * D * 4u, bar + 2);
+  };
+  ScoreChunk cur = score_chunk<APPEND>(a, blockIdx.x);
+  if (my_n > 0) issue(cur, 0);
+  const int gid = lane >> 2, tig = lane & 3;
+  const int tile = warp & 3, kh = warp >> 2;
+  for (int it = 0; it < my_n; ++it) {
+    const int st = stages == 2 ? (it & 1) : 0;
+    const uint32_t par = (uint32_t)(stages == 2 ? (it >> 1) : it) & 1u;
+    const unsigned long long t_start = a.trace ? global_ns() : 0ull;
+    ScoreChunk nxt;
+    if (it + 1 < my_n) {
+      nxt = score_chunk<APPEND>(a, blockIdx.x + (it + 1) * gridDim.x);
+      if (stages == 2) issue(nxt, st ^ 1);
+    }
+    if (COMP && cur.c == 0)
+      for (int i = tid; i < G * (D + 4); i += kT) a.unit_acc[(int64_t)cur.u * G * (D + 4) + i] = 0.f;
+    if (cur.nb > 0) {
+      const int s = cur.s, h = cur.h, u = cur.u, L = cur.L, N = cur.N, b0 = cur.b0, nb = cur.nb, nt = cur.nt;
+      const int rec = cur.rec;
+      const int64_t row0 = cur.row0;
+      float* sk = sm + st * stage_words;
+      float* sd = sk + kChunk * D;
+      float* sv = sd + kChunk * r;
+      uint64_t* bar = bars + 3 * st;
+      // this thread's coordinates of q_gid (its B fragments) straight from global memory
+      const float* qbase = a.q + ((int64_t)s * a.Hkv * G + (int64_t)h * G) * D;
+      float4 qv[JH];
+#pragma unroll
+      for (int j = 0; j < JH; ++j)
+        qv[j] = gid < G ? __ldg(reinterpret_cast<const float4*>(qbase + gid * D + 16 * (kh * JH + j) + 4 * tig))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (SCORE) {
+        // Qsq_{g,t} = sum of q_g^2 over coordinate group t = [t*D/r, (t+1)*D/r): warp g, 4 coordinates per lane
+        const int gs = D / r;
+        if (warp < G) {
+          const int c4 = 4 * lane;
+          float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (c4 < D) x = __ldg(reinterpret_cast<const float4*>(qbase + warp * D + c4));
+          if (gs >= 4) {
+            float t = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+            for (int o = 1; o < gs / 4; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+            if (c4 < D && (lane & (gs / 4 - 1)) == 0) sqs[warp * r + c4 / gs] = t;
+          } else if (c4 < D) {
+            const float e[4] = {x.x * x.x, x.y * x.y, x.z * x.z, x.w * x.w};
+            for (int k = 0; k < 4; k += gs) {
+              float t = 0.f;
+              for (int i = 0; i < gs; ++i) t += e[k + i];
+              sqs[warp * r + (c4 + k) / gs] = t;
+            }
+          }
         }
       }
-    }
+      if (SCORE && (r & 3))
+        for (int i = tid; i < nt * r; i += kT) sd[i] = a.dbar[row0 * r + i];
+      if (cur.append) {
+        // pack the new token and recompute the open block's summary from its
+        // tokens in one pass of 16-byte loads: thread t < 2D takes token
+        // t / (D/8) and coordinates 8 (t % (D/8)) .. + 7 of K and V; sums over
+        // tokens by shuffles within the warp and per-warp partials in shared
+        // memory; mean and population variance two-pass in fp32 from the
+        // exact bf16 values (no E[k^2] - E[k]^2 cancellation)
+        constexpr int GPT = D / 8;        // threads per token
+        constexpr int TPW = 32 / GPT;     // tokens per warp
+        constexpr int NWA = kBlock / TPW; // warps holding tokens
+        const int n = L - kBlock * (N - 1);
+        const int64_t row = row0 + (nb - 1);
+        const int j = tid / GPT, c8 = 8 * (tid % GPT);
+        const bool act = tid < 2 * D && j < n;
+        float kx[8], vx[8];
+        {
+          uint4 kr = make_uint4(0u, 0u, 0u, 0u), vr = make_uint4(0u, 0u, 0u, 0u);
+          if (act) {
+            const int64_t nw_off = ((int64_t)s * a.Hkv + h) * D + c8;
+            if (j == n - 1) {
+              kr = *reinterpret_cast<const uint4*>(a.k_new + nw_off);
+              vr = *reinterpret_cast<const uint4*>(a.v_new + nw_off);
+              *reinterpret_cast<uint4*>(a.k + (row * kBlock + j) * D + c8) = kr;
+              *reinterpret_cast<uint4*>(a.v + (row * kBlock + j) * D + c8) = vr;
+            } else {
+              kr = *reinterpret_cast<const uint4*>(a.k + (row * kBlock + j) * D + c8);
+              vr = *reinterpret_cast<const uint4*>(a.v + (row * kBlock + j) * D + c8);
+            }
+          }
+          const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w}, vw[4] = {vr.x, vr.y, vr.z, vr.w};
 #pragma unroll
-    for (int o = 1; o < LPG; o <<= 1) {
-      z += __shfl_xor_sync(0xffffffffu, z, o);
-      if (SCORE) sg += __shfl_xor_sync(0xffffffffu, sg, o);
-    }
-    if (p == 0) {
-      zs[g * kChunk + blk] = z * InvSqrt<D>::v;
-      if (SCORE) ss[g * kChunk + blk] = sg / (float)D;
-    }
-  };
+          for (int i = 0; i < 4; ++i) {
+            const float2 kf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw[i]));
+            const float2 vf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vw[i]));
+            kx[2 * i] = kf.x;
+            kx[2 * i + 1] = kf.y;
+            vx[2 * i] = vf.x;
+            vx[2 * i + 1] = vf.y;
+          }
+        }
+        // token sums: lanes GPT apart hold the same coordinates
+        float ks[8], vs[8];
 #pragma unroll
-  for (int it = 0; it < kHalf / kW; ++it) {
-    const int blk = warp + kW * it;
-    if (blk < nb) do_block(blk);
-  }
-  const unsigned long long t_b = a.trace ? global_ns() : 0ull;
-  if (nb > kHalf) {
-    mbar_wait_bounded(bar + 1, 0, a.status, s, h, 13);
+        for (int i = 0; i < 8; ++i) {
+          ks[i] = kx[i];
+          vs[i] = vx[i];
 #pragma unroll
-    for (int it = kHalf / kW; it < kChunk / kW; ++it) {
-      const int blk = warp + kW * it;
-      if (blk < nb) do_block(blk);
-    }
-  }
-  const unsigned long long t_loaded = a.trace ? global_ns() : 0ull;
-  __syncthreads();
-  // ---- per query head: item max and sum of e^a, u per block, max of ln|b| + zbar
-  if (warp < G) {
-    const int gw = warp;
-    float av[2], cv[2];
-    float ma = -INFINITY, mc = -INFINITY;
+          for (int o = GPT; o < 32; o <<= 1) {
+            ks[i] += __shfl_xor_sync(0xffffffffu, ks[i], o);
+            vs[i] += __shfl_xor_sync(0xffffffffu, vs[i], o);
+          }
+        }
+        if (warp < NWA && lane < GPT)
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int blk = lane + 32 * i;
-      av[i] = cv[i] = -INFINITY;
-      if (blk < nb) {
-        const int bb = b0 + blk;
-        const int n = (bb == N - 1) ? L - kBlock * bb : kBlock;
-        cv[i] = ln_n(n) + zs[gw * kChunk + blk];
-        if (SCORE) av[i] = cv[i] + 0.5f * ss[gw * kChunk + blk];
+          for (int i = 0; i < 8; ++i) {
+            sapp[warp * D + c8 + i] = ks[i];
+            sapp[(8 + warp) * D + c8 + i] = vs[i];
+          }
+        __syncthreads();
+        if (tid < D) {
+          float sk_ = 0.f, sv_ = 0.f;
+          for (int w = 0; w < NWA; ++w) {
+            sk_ += sapp[w * D + tid];
+            sv_ += sapp[(8 + w) * D + tid];
+          }
+          const float mk = sk_ / (float)n, mv = sv_ / (float)n;
+          svar[tid] = mk;  // the mean for the second pass
+          sk[(nb - 1) * D + tid] = mk;
+          a.kbar[row * D + tid] = mk;
+          a.vbar[row * D + tid] = mv;
+          if (COMP) sv[(nb - 1) * D + tid] = mv;
+        }
+        __syncthreads();
+        // squared deviations of K from the mean, summed the same way
+        float qd[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float dv = act ? kx[i] - svar[c8 + i] : 0.f;
+          qd[i] = dv * dv;
+#pragma unroll
+          for (int o = GPT; o < 32; o <<= 1) qd[i] += __shfl_xor_sync(0xffffffffu, qd[i], o);
+        }
+        __syncthreads();  // everyone has read the means
+        if (warp < NWA && lane < GPT)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) sapp[warp * D + c8 + i] = qd[i];
+        __syncthreads();
+        if (tid < D) {
+          float t = 0.f;
+          for (int w = 0; w < NWA; ++w) t += sapp[w * D + tid];
+          svar[tid] = t / (float)n;
+        }
+        __syncthreads();
+        if (tid < r) {
+          // Dbar_t: mean of the variances over coordinate group t = [t*D/r, (t+1)*D/r)
+          const int gs = D / r;
+          float t = 0.f;
+          for (int i = 0; i < gs; ++i) t += svar[tid * gs + i];
+          t /= (float)gs;
+          sd[(nb - 1) * r + tid] = t;
+          a.dbar[row * r + tid] = t;
+        }
       }
-      ma = fmaxf(ma, av[i]);
-      mc = fmaxf(mc, cv[i]);
-    }
-    mc = warp_max(mc);
-    float la = 0.f;
-    if (SCORE) {
-      ma = warp_max(ma);
+      __syncthreads();
+      // ---- zbar: this warp's tile and half of the coordinates
+      mbar_wait_bounded(bar + (tile >> 1), par, a.status, s, h, 10 + (tile >> 1));
+      const unsigned long long t_a = a.trace ? global_ns() : 0ull;
+      const int R0 = 16 * tile + gid;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (16 * tile < nb) {
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int blk = lane + 32 * i;
-        const float e = (blk < nb) ? expf(av[i] - ma) : 0.f;
-        la += e;
-        a.chunk_u[((int64_t)rec * G + gw) * kChunk + blk] = (blk < nb) ? e * ss[gw * kChunk + blk] : 0.f;
+        for (int j = 0; j < JH; ++j) {
+          const int col = 16 * (kh * JH + j) + 4 * tig;
+          const float4 x0 = *reinterpret_cast<const float4*>(sk + R0 * D + col);
+          const float4 x1 = *reinterpret_cast<const float4*>(sk + (R0 + 8) * D + col);
+          mma_chunk(acc, x0, x1, qv[j]);
+        }
       }
-      la = warp_sum(la);
-    }
-    if (COMP) {
+      if (kh == 1) *reinterpret_cast<float4*>(cx + (tile * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      const unsigned long long t_b = a.trace ? global_ns() : 0ull;
+      __syncthreads();
+      if (16 * tile < nb) {
+        // C fragment: (row gid, columns 2 tig, 2 tig + 1), (row gid + 8, same columns)
+        const int n0 = 2 * tig, n1 = 2 * tig + 1;
+        if (kh == 0) {
+          const float4 o = *reinterpret_cast<const float4*>(cx + (tile * 32 + lane) * 4);
+          const float z[4] = {acc[0] + o.x, acc[1] + o.y, acc[2] + o.z, acc[3] + o.w};
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int blk = lane + 32 * i;
-        a.chunk_z[((int64_t)rec * G + gw) * kChunk + blk] = (blk < nb) ? zs[gw * kChunk + blk] : 0.f;
+          for (int e = 0; e < 4; ++e) {
+            const int row = R0 + (e >> 1) * 8, n = (e & 1) ? n1 : n0;
+            if (n < G && row < nb) zs[n * kZS + row] = z[e] * InvSqrt<D>::v;
+          }
+        } else if (SCORE) {
+          // sigma2 for the same four (row, head) entries
+          float sg[4] = {0.f, 0.f, 0.f, 0.f};
+          if (r <= 8) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int row = R0 + (e >> 1) * 8, n = (e & 1) ? n1 : n0;
+              if (n < G)
+                for (int t = 0; t < r; ++t) sg[e] = fmaf(sqs[n * r + t], sd[row * r + t], sg[e]);
+            }
+          } else {
+            // tf32 contraction over the groups: rows of Dbar times columns of Qsq
+            for (int j = 0; j < r / 16; ++j) {
+              const int col = 16 * j + 4 * tig;
+              const float4 x0 = *reinterpret_cast<const float4*>(sd + R0 * r + col);
+              const float4 x1 = *reinterpret_cast<const float4*>(sd + (R0 + 8) * r + col);
+              float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
+              if (gid < G) y = *reinterpret_cast<const float4*>(sqs + gid * r + col);
+              mma_chunk(sg, x0, x1, y);
+            }
+          }
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int row = R0 + (e >> 1) * 8, n = (e & 1) ? n1 : n0;
+            if (n < G && row < nb) ss[n * kZS + row] = sg[e] / (float)D;
+          }
+        }
       }
+      const unsigned long long t_loaded = a.trace ? global_ns() : 0ull;
+      __syncthreads();
+      // ---- per query head: item max and sum of e^a, u per block, max of ln|b| + zbar
+      if (warp < G) {
+        const int gw = warp;
+        float av[2], cv[2];
+        float ma = -INFINITY, mc = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int blk = lane + 32 * i;
+          av[i] = cv[i] = -INFINITY;
+          if (blk < nb) {
+            const int bb = b0 + blk;
+            const int n = (bb == N - 1) ? L - kBlock * bb : kBlock;
+            cv[i] = ln_n(n) + zs[gw * kZS + blk];
+            if (SCORE) av[i] = cv[i] + 0.5f * ss[gw * kZS + blk];
+          }
+          ma = fmaxf(ma, av[i]);
+          mc = fmaxf(mc, cv[i]);
+        }
+        mc = warp_max(mc);
+        float la = 0.f;
+        if (SCORE) {
+          ma = warp_max(ma);
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int blk = lane + 32 * i;
+            const float e = (blk < nb) ? expf(av[i] - ma) : 0.f;
+            la += e;
+            a.chunk_u[((int64_t)rec * G + gw) * kChunk + blk] = (blk < nb) ? e * ss[gw * kZS + blk] : 0.f;
+          }
+          la = warp_sum(la);
+        }
+        if (COMP) {
+          // compensation weights w = e^(ln|b| + zbar - mc) of the item's blocks (mc = their max)
+          float wsum = 0.f;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int blk = lane + 32 * i;
+            a.chunk_z[((int64_t)rec * G + gw) * kChunk + blk] = (blk < nb) ? zs[gw * kZS + blk] : 0.f;
+            const float w = (blk < nb) ? expf(cv[i] - mc) : 0.f;
+            sw[gw * kZS + blk] = w;
+            wsum += w;
+          }
+          wsum = warp_sum(wsum);
+          if (lane == 0) a.comp_part[((int64_t)rec * G + gw) * (D + 4) + D] = wsum;
+        }
+        if (lane == 0)
+          *reinterpret_cast<float4*>(a.chunk_rec + ((int64_t)rec * G + gw) * 4) = make_float4(ma, la, mc, 0.f);
+      }
+      if (COMP) {
+        // ---- the item's compensation partial sum_b w_{g,b} vbar_b: out (heads x D) = W (heads x 64) . Vbar (64 x D)
+        // as tf32 MMAs with the three-term split; rows 8..15 of A are zero.  Warp w takes column tiles w, w + 8, ...
+        __syncthreads();
+        mbar_wait_bounded(bar + 2, par, a.status, s, h, 14);
+        for (int nt2 = warp; nt2 < D / 8; nt2 += kW) {
+          float cacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int ks = 0; ks < kChunk / 8; ++ks) {
+            const int k0 = 8 * ks + tig, k1 = k0 + 4;
+            const float w0 = gid < G ? sw[gid * kZS + k0] : 0.f;
+            const float w1 = gid < G ? sw[gid * kZS + k1] : 0.f;
+            const float v0 = k0 < nb ? sv[k0 * SV + 8 * nt2 + gid] : 0.f;
+            const float v1 = k1 < nb ? sv[k1 * SV + 8 * nt2 + gid] : 0.f;
+            uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
+            split_tf32(w0, ah[0], al[0]);
+            split_tf32(w1, ah[2], al[2]);
+            ah[1] = ah[3] = al[1] = al[3] = 0u;
+            split_tf32(v0, bh0, bl0);
+            split_tf32(v1, bh1, bl1);
+            mma_tf32(cacc, al, bh0, bh1);
+            mma_tf32(cacc, ah, bl0, bl1);
+            mma_tf32(cacc, ah, bh0, bh1);
+          }
+          if (gid < G)
+            *reinterpret_cast<float2*>(a.comp_part + ((int64_t)rec * G + gid) * (D + 4) + 8 * nt2 + 2 * tig) =
+                make_float2(cacc[0], cacc[1]);
+        }
+      }
+      if (tid == 0) trace_item(a, blockIdx.x + it * gridDim.x, 0, u, cur.c, t_start, t_loaded, t_start, t_a, t_b);
     }
-    if (lane == 0)
-      *reinterpret_cast<float4*>(a.chunk_rec + ((int64_t)rec * G + gw) * 4) = make_float4(ma, la, mc, 0.f);
+    __syncthreads();  // the stage and the working buffers are free again
+    if (it + 1 < my_n && stages == 1) issue(nxt, 0);
+    cur = nxt;
   }
-  if (tid == 0) trace_item(a, blockIdx.x, 0, u, c, t_start, t_loaded, t_pdl, t_a, t_b);
 }
 
-// ================================================================== 2. S items, selection, compensation
-// Shared memory of the grid (the larger of the two item kinds):
-//   S item:    selection region (keys | per-warp histograms | summed
-//              histogram | list keys | list indices | bitmap | prefix) |
-//              item factors (8 x G) | histogram (256) | misc (32)
-//   comp item: vbar rows (128 x D) | weights (G x 128) | M_g (G) | mbarrier
+// ================================================================== 2. S items, classify items, compensation
+// Shared memory:
+//   S item:        12-bit histogram (4096) | item factors (8 x G)
+//   select CTA:    keys | per-warp histograms | summed histogram | list
+//                  keys | list indices | bitmap | prefix (the fast path uses
+//                  the list and the bitmap); misc (64) at the end
+//   comp item:     vbar rows (128 x D) | weights (G x 128) | M_g (G) | mbarrier
 __host__ __device__ inline int sel_region_words(int key_stride) {
   const int words = (key_stride + 31) / 32 + 4;
   return key_stride + 4 + (kW + 1) * kPrivBins + 2 * (kListMax + 4) + 2 * words;
 }
-__host__ __device__ inline int s_item_smem(int G, int key_stride) {
-  return (((sel_region_words(key_stride) + 3) & ~3) + 8 * G + kPrivBins + 32) * 4;
-}
-__host__ __device__ inline int comp_bar_offset(int D, int G) { return ((kChunk2 * D + G * kChunk2 + G) * 4 + 15) & ~15; }
-__host__ __device__ inline int comp_item_smem(int D, int G) { return comp_bar_offset(D, G) + 16; }
-__host__ __device__ inline int item_grid_smem(int D, int G, int key_stride, bool sel, bool comp) {
-  int m = 0;
-  if (sel) m = s_item_smem(G, key_stride);
-  if (comp && comp_item_smem(D, G) > m) m = comp_item_smem(D, G);
-  return m;
-}
-
 // Warp 0: wbase[w] = set bits in words[0..w), for w < nw; returns the total
 // (in warp 0; other warps get 0).
 __device__ __forceinline__ int word_prefix(const unsigned* words, int* wbase, int nw, int lane, int warp) {
@@ -517,12 +692,17 @@ __device__ __forceinline__ void select_unit(const LayerArgs& a, int u, int s, in
   unsigned long long tp = a.trace ? global_ns() : 0ull;
   int pk = 0;
 
-  // a. the exponent histogram (then cleared for the next call), an empty bitmap
+  // a. the exponent histogram (sums of the 12-bit histogram's bins), an empty bitmap
   {
-    unsigned* gh = a.unit_hist + u * kPrivBins;
+    const uint4* gh = reinterpret_cast<const uint4*>(a.hist12 + (int64_t)u * kHist12);
     if (tid < kPrivBins) {
-      hsum[tid] = __ldcg(gh + tid);
-      gh[tid] = 0u;
+      uint32_t t = 0;
+#pragma unroll
+      for (int k = 0; k < (kHist12 / kPrivBins) / 4; ++k) {
+        const uint4 v = __ldcg(gh + tid * ((kHist12 / kPrivBins) / 4) + k);
+        t += v.x + v.y + v.z + v.w;
+      }
+      hsum[tid] = t;
     }
     for (int w = tid; w < nw; w += kT) words[w] = N <= K ? (w < nw - 1 || (N & 31) == 0 ? ~0u : (1u << (N & 31)) - 1u) : 0u;
   }
@@ -775,23 +955,34 @@ __device__ __forceinline__ void select_unit(const LayerArgs& a, int u, int s, in
   if (tid == 0) tp = trace_phase(a, u, pk++, 4, tp);
 }
 
-// S item: blocks [512 i, 512 i + 512) of a unit.  LSE_g from the unit's
-// scoring records; S_b keys of its blocks; their exponent histogram summed
-// into the unit's; the unit's last S item selects.
-template <int G, int MODE>
-__device__ __forceinline__ void s_item(const LayerArgs& a, int item, unsigned char* smraw, unsigned long long t_start) {
+// S items kernel: blocks [512 i, 512 i + 512) of a unit.  From the unit's
+// scoring records: LSE_g and M_g = max_b (ln|b| + zbar).  With the selection:
+// S_b keys of its blocks and the histogram of the top 12 key bits (exponent
+// and 4 mantissa bits) of the candidates 1..N-3, summed into the unit's.
+// With the compensation: its 8 chunks' partial sums rescaled from their own
+// reference to M_g and added to the unit's accumulator (item 0 records M_g).
+__host__ __device__ inline int s_items_smem(int G) { return (kHist12 + 8 * G + 8 * G + G) * 4; }
+
+template <int D, int G, int MODE>
+__global__ void __launch_bounds__(kT) k_sitems(LayerArgs a) {
   constexpr bool APPEND = (MODE & kFAppend) != 0;
+  constexpr bool SEL = (MODE & kFSelect) != 0;
+  constexpr bool COMP = (MODE & kFComp) != 0;
+  extern __shared__ __align__(128) unsigned char smraw[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const unsigned long long t_start = a.trace ? global_ns() : 0ull;
+  const int item = blockIdx.x;
   int s = 0;
   while (s + 1 < a.B && a.ns_first[s + 1] <= item) ++s;
   const int nper = (a.nchunk[s] + 7) / 8;
   const int local = item - a.ns_first[s];
   const int h = local / nper, ci = local % nper;
   const int u = s * a.Hkv + h;
-  float* fch = reinterpret_cast<float*>(smraw) + ((sel_region_words(a.key_stride) + 3) & ~3);  // [8][G]
-  uint32_t* hist = reinterpret_cast<uint32_t*>(fch + 8 * G);
-  int* misc = reinterpret_cast<int*>(hist + kPrivBins);
-  for (int i = tid; i < kPrivBins; i += kT) hist[i] = 0u;
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smraw);    // [kHist12]
+  float* fch = reinterpret_cast<float*>(hist + kHist12);  // [8][G] e^(max a - LSE_g)
+  float* fcp = fch + 8 * G;                               // [8][G] e^(mc - M_g)
+  if (SEL)
+    for (int i = tid; i < kHist12 / 4; i += kT) reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
   pdl_wait();
   pdl_trigger();
   const unsigned long long t_wait = a.trace ? global_ns() : 0ull;
@@ -800,18 +991,13 @@ __device__ __forceinline__ void s_item(const LayerArgs& a, int item, unsigned ch
   const int N = ceil_blocks(L);
   const int b0 = ci * kChunkS;
   const int nb = b0 < N ? min(kChunkS, N - b0) : 0;
-  if (nb == 0) {
-    if (ci == 0) {  // empty sequence: nothing selected
-      for (int i = tid; i < a.K; i += kT) a.sel[(int64_t)u * a.K + i] = -1;
-      if (tid == 0) a.unit_nsel[u] = 0;
-    }
-    return;
-  }
+  if (nb == 0) return;
   // 1. the u values of the item's blocks (two per thread), in flight while
-  // each query head's warp g forms LSE_g from the unit's records (eight per
-  // lane in flight) and the item's factors e^(max a - LSE_g)
+  // each query head's warp g forms LSE_g and M_g from the unit's records
+  // (eight per lane in flight) and the item's factors
   const int nch = (N + kChunk - 1) / kChunk;
   const int rec0 = chunk_record(a, s, h, 0);
+  const int cs0 = b0 / kChunk;
   float uu[2][G];
 #pragma unroll
   for (int k = 0; k < 2; ++k) {
@@ -820,234 +1006,343 @@ __device__ __forceinline__ void s_item(const LayerArgs& a, int item, unsigned ch
     const int rec = rec0 + b / kChunk;
 #pragma unroll
     for (int g = 0; g < G; ++g)
-      uu[k][g] = blk < nb ? __ldcg(a.chunk_u + ((int64_t)rec * G + g) * kChunk + (b % kChunk)) : 0.f;
+      uu[k][g] = (SEL && blk < nb) ? __ldcg(a.chunk_u + ((int64_t)rec * G + g) * kChunk + (b % kChunk)) : 0.f;
   }
   if (warp < G) {
     const int g = warp;
-    const int cs0 = b0 / kChunk;
-    float M = -INFINITY, S = 0.f, fx = 0.f;
+    float M = -INFINITY, S = 0.f, MC = -INFINITY, fx = 0.f, fz = 0.f;
     int fj = -1;
     for (int c0 = 0; c0 < nch; c0 += 256) {
-      float2 rv[8];
+      float4 rv[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const int c = c0 + lane + 32 * k;
-        rv[k] = c < nch ? __ldcg(reinterpret_cast<const float2*>(a.chunk_rec + ((int64_t)(rec0 + c) * G + g) * 4))
-                        : make_float2(-INFINITY, 0.f);
+        rv[k] = c < nch ? __ldcg(reinterpret_cast<const float4*>(a.chunk_rec + ((int64_t)(rec0 + c) * G + g) * 4))
+                        : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         const int c = c0 + lane + 32 * k;
         if (c >= cs0 && c < cs0 + 8 && c < nch) {
           fx = rv[k].x;
+          fz = rv[k].z;
           fj = c - cs0;
         }
-        if (rv[k].x != -INFINITY) {
+        MC = fmaxf(MC, rv[k].z);
+        if (SEL && rv[k].x != -INFINITY) {
           const float mn = fmaxf(M, rv[k].x);
           S = (M == -INFINITY ? 0.f : S * expf(M - mn)) + rv[k].y * expf(rv[k].x - mn);
           M = mn;
         }
       }
     }
+    MC = warp_max(MC);
+    if (SEL) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float M2 = __shfl_xor_sync(0xffffffffu, M, o), S2 = __shfl_xor_sync(0xffffffffu, S, o);
-      const float Mn = fmaxf(M, M2);
-      if (Mn != -INFINITY) {
-        S = (M == -INFINITY ? 0.f : S * expf(M - Mn)) + (M2 == -INFINITY ? 0.f : S2 * expf(M2 - Mn));
-        M = Mn;
+      for (int o = 16; o > 0; o >>= 1) {
+        const float M2 = __shfl_xor_sync(0xffffffffu, M, o), S2 = __shfl_xor_sync(0xffffffffu, S, o);
+        const float Mn = fmaxf(M, M2);
+        if (Mn != -INFINITY) {
+          S = (M == -INFINITY ? 0.f : S * expf(M - Mn)) + (M2 == -INFINITY ? 0.f : S2 * expf(M2 - Mn));
+          M = Mn;
+        }
+      }
+      const float lg = M + logf(S);
+      if (fj >= 0) fch[fj * G + g] = expf(fx - lg);
+    }
+    if (COMP) {
+      if (fj >= 0) fcp[fj * G + g] = expf(fz - MC);
+      if (ci == 0 && lane == 0) a.unit_ref[u * G + g] = MC;
+    }
+  }
+  __syncthreads();
+  if (SEL) {
+    // 2. S_b = sum_g u_{g,b} e^(max a - LSE_g) = sum_g phat sigma2 as keys
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int blk = tid + kT * k;
+      if (blk >= nb) continue;
+      const int b = b0 + blk;
+      const int cl = blk / kChunk;
+      float S = 0.f;
+#pragma unroll
+      for (int g = 0; g < G; ++g) S = fmaf(uu[k][g], fch[cl * G + g], S);
+      S = fmaxf(S, 0.f);
+      const uint32_t key = __float_as_uint(S);
+      a.skeys[(int64_t)u * a.key_stride + b] = key;
+      if (a.scores) a.scores[(int64_t)u * a.score_stride + b] = S;
+      if (b >= 1 && b <= N - 3) atomicAdd(&hist[key >> kDigitShift], 1u);
+    }
+  }
+  if (COMP) {
+    // 3. the chunks' compensation partials, rescaled to M_g, into the unit's accumulator
+    const int ncl = min(8, nch - cs0);
+    float* ua = a.unit_acc + (int64_t)u * G * (D + 4);
+    for (int i = tid; i < G * (D + 4) / 4; i += kT) {
+      const int g = (4 * i) / (D + 4), col = (4 * i) % (D + 4);
+      float4 v[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        v[j] = j < ncl ? __ldcg(reinterpret_cast<const float4*>(a.comp_part + ((int64_t)(rec0 + cs0 + j) * G + g) * (D + 4) + col))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (j >= ncl) break;
+        const float f = fcp[j * G + g];
+        t.x = fmaf(f, v[j].x, t.x);
+        t.y = fmaf(f, v[j].y, t.y);
+        t.z = fmaf(f, v[j].z, t.z);
+        t.w = fmaf(f, v[j].w, t.w);
+      }
+      if (col < D) {
+        atomicAdd(ua + g * (D + 4) + col, t.x);
+        atomicAdd(ua + g * (D + 4) + col + 1, t.y);
+        atomicAdd(ua + g * (D + 4) + col + 2, t.z);
+        atomicAdd(ua + g * (D + 4) + col + 3, t.w);
+      } else {
+        atomicAdd(ua + g * (D + 4) + D, t.x);  // the weight sums sit at column D
       }
     }
-    const float lg = M + logf(S);
-    if (fj >= 0) fch[fj * G + g] = expf(fx - lg);
   }
-  __syncthreads();
-  // 2. S_b = sum_g u_{g,b} e^(max a - LSE_g) = sum_g phat sigma2 as keys
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int blk = tid + kT * k;
-    if (blk >= nb) continue;
-    const int b = b0 + blk;
-    const int cl = blk / kChunk;
-    float S = 0.f;
-#pragma unroll
-    for (int g = 0; g < G; ++g) S = fmaf(uu[k][g], fch[cl * G + g], S);
-    S = fmaxf(S, 0.f);
-    const uint32_t key = __float_as_uint(S);
-    a.skeys[(int64_t)u * a.key_stride + b] = key;
-    if (a.scores) a.scores[(int64_t)u * a.score_stride + b] = S;
-    if (b >= 1 && b <= N - 3) atomicAdd(&hist[key >> 23], 1u);
-  }
-  __syncthreads();
-  // 3. the item's histogram into the unit's; the unit's last S item selects
-  if (tid < kPrivBins && hist[tid]) atomicAdd(a.unit_hist + u * kPrivBins + tid, hist[tid]);
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int items = (N + kChunkS - 1) / kChunkS;
-    const int prev = atomicAdd(a.s2count + u, 1);
-    misc[31] = prev == items - 1;
-    if (prev == items - 1) a.s2count[u] = 0;
-  }
-  __syncthreads();
-  if (misc[31]) {
-    __threadfence();
-    const unsigned long long t_sel = a.trace ? global_ns() : 0ull;
-    select_unit(a, u, s, h, N, smraw, misc);
-    if (tid == 0) trace_item(a, slot_select(a) + u, 3, u, item, t_sel, t_sel);
+  if (SEL) {
+    __syncthreads();
+    // 4. the item's histogram into the unit's (non-zero bins only)
+    unsigned* gh = a.hist12 + (int64_t)u * kHist12;
+    for (int i = tid; i < kHist12 / 4; i += kT) {
+      const uint4 v = reinterpret_cast<const uint4*>(hist)[i];
+      if (v.x) atomicAdd(gh + 4 * i, v.x);
+      if (v.y) atomicAdd(gh + 4 * i + 1, v.y);
+      if (v.z) atomicAdd(gh + 4 * i + 2, v.z);
+      if (v.w) atomicAdd(gh + 4 * i + 3, v.w);
+    }
   }
   if (tid == 0) trace_item(a, slot_items(a) + blockIdx.x, 7, u, ci, t_start, t_wait);
 }
 
-// Compensation item: blocks [128 i, 128 i + 128) of a unit.  M_g =
-// max_b (ln|b| + zbar) from the unit's scoring records; sum_b w_b vbar_b and
-// sum_b w_b, w_b = e^(ln|b| + zbar_b - M_g), summed into the unit's
-// accumulator.  The vbar rows are bulk-copied before the wait for the scoring
-// kernel (they are final, except the newest block's row, which the scoring
-// kernel rewrites and which is read after the wait).
-template <int D, int G, int MODE>
-__device__ __forceinline__ void comp_item(const LayerArgs& a, int item, unsigned char* smraw, unsigned long long t_start) {
-  constexpr bool APPEND = (MODE & kFAppend) != 0;
-  constexpr int V = D / 32;
+// Selection of unit u by a whole CTA, after every S item.  The unit's 12-bit
+// histogram of candidate keys gives the threshold bin T where the count of
+// larger-or-equal candidates reaches K - 3; one pass over the unit's keys (16-byte
+// loads, batched with the histogram's) marks the forced blocks and the
+// candidates above T (and in T when all of it is needed) in a bitmap and
+// lists T's candidates; those are ranked by (S_b desc, index asc) and the
+// top ones join the bitmap; the bitmap's prefix counts give the ascending
+// selection.  If more candidates share T than the list holds, the full radix
+// selection over the keys runs instead.  With `write_out` the CTA writes the
+// selection list and its size; it then puts the blocks at list positions q
+// with (q / 8) mod C == p into pick[(q / 8 / C) * 8 + q % 8] (-1 past the end,
+// pick holding `npick` entries).
+__host__ __device__ inline int select_smem(int key_stride) { return (sel_region_words(key_stride) + 64) * 4; }
+
+constexpr int kKeyBatch = 33;  // 32-key words per warp in flight (8448 keys per pass)
+
+__device__ __forceinline__ void select_core(const LayerArgs& a, int u, int L, unsigned char* smraw, bool write_out,
+                                            int p, int C, int* pick, int npick) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int s = 0;
-  while (s + 1 < a.B && a.n2_first[s + 1] <= item) ++s;
-  const int local = item - a.n2_first[s];
-  const int h = local / a.nchunk2[s], c2 = local % a.nchunk2[s];
-  const int u = s * a.Hkv + h;
-  bool fits;
-  const int L = unit_tokens(a, s, APPEND, &fits);  // seq_len is written by the last kernel only
+  const int s = u / a.Hkv, h = u % a.Hkv;
+  const int K = a.K;
+  const int stride = a.key_stride;
+  // the full radix selection's layout; the fast path uses its list and bitmap
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smraw);
+  uint32_t* hsum = keys + stride + 4 + kW * kPrivBins;
+  uint32_t* lkey = hsum + kPrivBins;
+  int* lidx = reinterpret_cast<int*>(lkey + kListMax + 4);
+  unsigned* words = reinterpret_cast<unsigned*>(lidx + kListMax + 4);
+  int* wbase = reinterpret_cast<int*>(words + (stride + 31) / 32 + 4);
+  int* misc = reinterpret_cast<int*>(smraw) + select_smem(stride) / 4 - 64;  // [64]
+  int* selrow = a.sel + (int64_t)u * K;
+  unsigned long long tp = a.trace ? global_ns() : 0ull;
   const int N = ceil_blocks(L);
-  const int b0 = c2 * kChunk2;
-  const int nb = b0 < N ? min(kChunk2, N - b0) : 0;
-  const bool newest = APPEND && fits && nb > 0 && b0 + nb == N;
-  const int nt = nb - (newest ? 1 : 0);
-  float* sv = reinterpret_cast<float*>(smraw);
-  float* ws = sv + kChunk2 * D;
-  float* mref = ws + G * kChunk2;
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smraw + comp_bar_offset(D, G));
-  const int64_t row0 = row_of(a, s, h, b0);
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-    mbar_arrive_expect_tx(bar, nt > 0 ? (uint32_t)nt * D * 4u : 0u);
-    if (nt > 0) bulk_g2s(sv, a.vbar + row0 * D, (uint32_t)nt * D * 4u, bar);
-  }
-  pdl_wait();
-  pdl_trigger();
-  const unsigned long long t_wait = a.trace ? global_ns() : 0ull;
-  if (nb == 0) {
-    __syncthreads();
-    mbar_wait_bounded(bar, 0, a.status, s, h, 12);
-    return;
-  }
-  // zbar of the item's blocks (in flight while M_g is formed from the records, eight per lane in flight)
-  const int nch = (N + kChunk - 1) / kChunk;
-  const int rec0 = chunk_record(a, s, h, 0);
-  constexpr int NZ = (G * kChunk2 + kT - 1) / kT;
-  float zv[NZ];
+  const int nw = (N + 31) / 32;
+  const bool all_sel = N <= K;
+  const int need = K - 3;
+  const bool ranked = !all_sel && need > 0;
+  unsigned* gh = a.hist12 + (int64_t)u * kHist12;
+  // 1. the histogram (this thread: bins [kHist12 - 16 (tid + 1), kHist12 - 16 tid)) and the first keys
+  uint32_t c[16];
+  if (ranked) {
+    const uint4* src = reinterpret_cast<const uint4*>(gh + kHist12 - 16 * (tid + 1));
 #pragma unroll
-  for (int k = 0; k < NZ; ++k) {
-    const int i = tid + kT * k;
-    const int g = i / kChunk2, blk = i % kChunk2;
-    const int b = b0 + blk;
-    zv[k] = (i < G * kChunk2 && blk < nb)
-                ? __ldcg(a.chunk_z + ((int64_t)(rec0 + b / kChunk) * G + g) * kChunk + (b % kChunk))
-                : 0.f;
+    for (int k = 0; k < 4; ++k) {
+      const uint4 v = __ldcg(src + k);
+      c[4 * k] = v.x;
+      c[4 * k + 1] = v.y;
+      c[4 * k + 2] = v.z;
+      c[4 * k + 3] = v.w;
+    }
   }
-  if (warp < G) {
-    float m = -INFINITY;
-    for (int c0 = 0; c0 < nch; c0 += 256) {
-      float mv[8];
+  // keys by 32-key words: warp w takes words w, w + 8, ..., one key per lane (coalesced)
+  const uint32_t* ksrc = a.skeys + (int64_t)u * stride;
+  const int nwk = ranked ? nw : 0;
+  uint32_t kv[kKeyBatch];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int c = c0 + lane + 32 * k;
-        mv[k] = c < nch ? __ldcg(a.chunk_rec + ((int64_t)(rec0 + c) * G + warp) * 4 + 2) : -INFINITY;
+  for (int k = 0; k < kKeyBatch; ++k) {
+    const int b = 32 * (warp + kW * k) + lane;
+    kv[k] = (warp + kW * k < nwk && b < N) ? __ldcg(ksrc + b) : 0u;
+  }
+  for (int w = tid; w < nw; w += kT) words[w] = 0u;
+  for (int i = tid; i < npick; i += kT) pick[i] = -1;
+  if (tid == 0) misc[12] = 0;
+  {
+    // consume the keys here so that their loads are issued together, ahead of the scan
+    uint32_t any = 0u;
+#pragma unroll
+    for (int k = 0; k < kKeyBatch; ++k) any |= kv[k];
+    if (any == 0xffffffffu) misc[13] = 1;
+  }
+  // 2. the threshold bin T, scanned from the top; need_T of its candidates are taken
+  int T = 0, need_T = 0;
+  bool take_all = true;
+  if (ranked) {
+    int loc = 0;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) loc += (int)c[k];
+    int total;
+    const int before = cta_exclusive_scan(loc, misc, &total, lane, warp);
+    if (before < need && need <= before + loc) {
+      int run = before;
+#pragma unroll
+      for (int k = 15; k >= 0; --k) {
+        if (run < need && need <= run + (int)c[k]) {
+          misc[8] = kHist12 - 16 * (tid + 1) + k;
+          misc[9] = need - run;
+          misc[10] = (int)c[k];
+        }
+        run += (int)c[k];
+      }
+    }
+  }
+  __syncthreads();
+  if (ranked) {
+    T = misc[8];
+    need_T = misc[9];
+    take_all = misc[10] == need_T;
+  }
+  if (tid == 0 && write_out) tp = trace_phase(a, u, 0, 1, tp);
+  const bool list_ok = !ranked || take_all || misc[10] <= kListMax;
+  if (ranked && list_ok) {
+    // 3. one pass over the keys: bitmap words by ballot, T's candidates listed
+    for (int w0 = 0; w0 < nwk; w0 += kW * kKeyBatch) {
+      if (w0 > 0) {
+#pragma unroll
+        for (int k = 0; k < kKeyBatch; ++k) {
+          const int w = w0 + warp + kW * k, b = 32 * w + lane;
+          kv[k] = (w < nwk && b < N) ? __ldcg(ksrc + b) : 0u;
+        }
       }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) m = fmaxf(m, mv[k]);
+      for (int k = 0; k < kKeyBatch; ++k) {
+        const int w = w0 + warp + kW * k;
+        if (w >= nwk) break;  // warp-uniform
+        const int b = 32 * w + lane;
+        bool sel = false, pend = false;
+        if (b < N) {
+          const bool forced = b == 0 || b >= N - 2;
+          const int dg = (int)(kv[k] >> kDigitShift);
+          sel = forced || dg > T || (dg == T && take_all);
+          pend = !sel && dg == T;
+        }
+        const unsigned word = __ballot_sync(0xffffffffu, sel);
+        if (lane == 0) words[w] = word;
+        const unsigned pb = __ballot_sync(0xffffffffu, pend);
+        if (pb) {
+          int p0 = 0;
+          if (lane == 0) p0 = atomicAdd(misc + 12, __popc(pb));
+          p0 = __shfl_sync(0xffffffffu, p0, 0);
+          if (pend) {
+            const int p = p0 + __popc(pb & ((1u << lane) - 1u));
+            lkey[p] = kv[k];
+            lidx[p] = b;
+          }
+        }
+      }
     }
-    m = warp_max(m);
-    if (lane == 0) {
-      mref[warp] = m;
-      if (c2 == 0) a.unit_ref[u * G + warp] = m;
+    __syncthreads();
+    if (tid == 0 && write_out) tp = trace_phase(a, u, 1, 2, tp);
+    if (!take_all) {
+      // 4. rank T's candidates by (key desc, index asc); 16-byte broadcast reads, padded with sentinels
+      const int m = misc[12];
+      if (tid < 4) {
+        lkey[m + tid] = 0u;
+        lidx[m + tid] = 0x7fffffff;
+      }
+      __syncthreads();
+      const int m4 = (m + 3) & ~3;
+      for (int e = tid; e < m; e += kT) {
+        const uint32_t k0 = lkey[e];
+        const int i0 = lidx[e];
+        int rank = 0;
+#pragma unroll 4
+        for (int f = 0; f < m4; f += 4) {
+          const uint4 kf = *reinterpret_cast<const uint4*>(lkey + f);
+          const int4 xf = *reinterpret_cast<const int4*>(lidx + f);
+          rank += kf.x > k0 || (kf.x == k0 && xf.x < i0);
+          rank += kf.y > k0 || (kf.y == k0 && xf.y < i0);
+          rank += kf.z > k0 || (kf.z == k0 && xf.z < i0);
+          rank += kf.w > k0 || (kf.w == k0 && xf.w < i0);
+        }
+        if (rank < need_T) atomicOr(&words[i0 >> 5], 1u << (i0 & 31));
+      }
+      __syncthreads();
+      if (tid == 0 && write_out) tp = trace_phase(a, u, 2, 9, tp);
+    }
+  } else if (!ranked) {
+    // every block, or only the forced ones (K = 3)
+    for (int w = tid; w < nw; w += kT) {
+      unsigned word = 0u;
+      for (int bit = 0; bit < 32; ++bit) {
+        const int b = 32 * w + bit;
+        if (b < N && (all_sel || b == 0 || b >= N - 2)) word |= 1u << bit;
+      }
+      words[w] = word;
+    }
+    __syncthreads();
+  }
+  if (ranked && !list_ok) {
+    // too many candidates share T: the full radix selection over the keys
+    // (it writes the list and leaves the bitmap and its prefix counts here)
+    __syncthreads();
+    select_unit(a, u, s, h, N, smraw, misc);
+  } else {
+    // 5. prefix counts of the bitmap; the ascending list
+    const int total = word_prefix(words, wbase, nw, lane, warp);
+    const int want = N < K ? N : K;
+    if (write_out && warp == 0 && lane == 0) {
+      if (total != want) set_error(a.status, kDevInternal, s, h, 50);
+      a.unit_nsel[u] = total;
+    }
+    __syncthreads();
+    if (write_out) {
+      for (int w = tid; w < nw; w += kT) {
+        unsigned word = words[w];
+        int pos = wbase[w];
+        while (word) {
+          const int bit = __ffs(word) - 1;
+          if (pos < K) selrow[pos] = 32 * w + bit;
+          ++pos;
+          word &= word - 1u;
+        }
+      }
+      for (int i = want + tid; i < K; i += kT) selrow[i] = -1;
     }
   }
-  if (newest)
-    for (int i = tid; i < D; i += kT) sv[(nb - 1) * D + i] = __ldcg(a.vbar + (row0 + nb - 1) * D + i);
+  // this CTA's picks
+  for (int w = tid; w < nw; w += kT) {
+    unsigned word = words[w];
+    int pos = wbase[w];
+    while (word) {
+      const int bit = __ffs(word) - 1;
+      const int grp = pos >> 3;
+      if (pos < K && grp % C == p) {
+        const int slot = (grp / C) * 8 + (pos & 7);
+        if (slot < npick) pick[slot] = 32 * w + bit;
+      }
+      ++pos;
+      word &= word - 1u;
+    }
+  }
   __syncthreads();
-#pragma unroll
-  for (int k = 0; k < NZ; ++k) {
-    const int i = tid + kT * k;
-    if (i >= G * kChunk2) break;
-    const int g = i / kChunk2, blk = i % kChunk2;
-    float w = 0.f;
-    if (blk < nb) {
-      const int b = b0 + blk;
-      const int n = (b == N - 1) ? L - kBlock * b : kBlock;
-      w = expf(ln_n(n) + zv[k] - mref[g]);
-    }
-    ws[i] = w;
-  }
-  mbar_wait_bounded(bar, 0, a.status, s, h, 11);
-  __syncthreads();
-  float acc[G][V];
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int i = 0; i < V; ++i) acc[g][i] = 0.f;
-  for (int blk = warp; blk < nb; blk += kW) {
-    float vv[V];
-    if (V == 4) {
-      const float4 x = *reinterpret_cast<const float4*>(sv + blk * D + lane * 4);
-      vv[0] = x.x; vv[1] = x.y; vv[2 % V] = x.z; vv[3 % V] = x.w;
-    } else {
-      const float2 x = *reinterpret_cast<const float2*>(sv + blk * D + lane * 2);
-      vv[0] = x.x; vv[1 % V] = x.y;
-    }
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float w = ws[g * kChunk2 + blk];
-#pragma unroll
-      for (int i = 0; i < V; ++i) acc[g][i] = fmaf(w, vv[i], acc[g][i]);
-    }
-  }
-  __syncthreads();
-  float* red = sv;  // [kW][G][D]
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int i = 0; i < V; ++i) red[(warp * G + g) * D + lane * V + i] = acc[g][i];
-  __syncthreads();
-  float* ua = a.unit_acc + (int64_t)u * G * (D + 4);
-  for (int i = tid; i < G * D; i += kT) {
-    float t = 0.f;
-#pragma unroll
-    for (int w = 0; w < kW; ++w) t += red[w * G * D + i];
-    atomicAdd(ua + (i / D) * (D + 4) + (i % D), t);
-  }
-  if (warp < G) {
-    float t = 0.f;
-    for (int blk = lane; blk < kChunk2; blk += 32) t += ws[warp * kChunk2 + blk];
-    t = warp_sum(t);
-    if (lane == 0) atomicAdd(ua + warp * (D + 4) + D, t);
-  }
-  if (tid == 0) trace_item(a, slot_items(a) + blockIdx.x, 2, u, c2, t_start, t_wait);
-}
-
-// The S items come first in the grid so that they are scheduled first.
-template <int D, int G, int MODE>
-__global__ void __launch_bounds__(kT) k_select_comp(LayerArgs a) {
-  constexpr bool SEL = (MODE & kFSelect) != 0;
-  constexpr bool COMP = (MODE & kFComp) != 0;
-  extern __shared__ __align__(128) unsigned char smraw[];
-  const unsigned long long t_start = a.trace ? global_ns() : 0ull;
-  const int ns = SEL ? a.ns_items : 0;
-  if ((int)blockIdx.x < ns) {
-    if (SEL) s_item<G, MODE>(a, blockIdx.x, smraw, t_start);
-  } else if (COMP) {
-    comp_item<D, G, MODE>(a, blockIdx.x - ns, smraw, t_start);
-  }
+  if (tid == 0 && write_out) trace_phase(a, u, 3, 4, tp);
 }
 
 // Sum of NVAL values over the LPB lanes of a lane group (powers of two,
@@ -1083,24 +1378,74 @@ __device__ __forceinline__ float transpose_reduce_warp(float (&v)[P], int lane) 
   return transpose_reduce_lanes<P, 32>(v, lane, idx);
 }
 
-constexpr int kAttendWarps = kAttendBlocks;  // selected blocks per attention CTA (one per warp)
-static_assert(kAttendWarps == kW, "one selected block per warp of an attention CTA");
+// Thread-block cluster helpers (distributed shared memory).
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t peer_smem(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_peer_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float2 ld_peer_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
+  return v;
+}
 
-template <int D, int G, int MODE>
-__global__ void __launch_bounds__(kT) k_attend(LayerArgs a) {
+constexpr int kAT = 256;            // threads of an attention CTA
+constexpr int kAW = kAT / 32;       // its warps: one selected block each per round
+// shared memory: per-warp partials (kAW x G x D, then m and l) | the CTA's partial (G x (D + 4)) |
+// counters; with the selection, that region is first the selection's | then the picked blocks
+__host__ __device__ inline int attend_smem(int D, int G) { return (kAW * G * D + 2 * kAW * G + G * (D + 4) + 4) * 4; }
+__host__ __device__ inline int attend_union_bytes(int D, int G, int key_stride, bool sel) {
+  int m = attend_smem(D, G);
+  if (sel && select_smem(key_stride) > m) m = select_smem(key_stride);
+  return (m + 15) & ~15;
+}
+__host__ __device__ inline int attend_npick(int K, int C, bool loop) { return loop ? ((K + 8 * C - 1) / (8 * C)) * 8 : 8; }
+
+// A cluster of C CTAs per unit (C = a.splits <= 16); CTA rank p takes the
+// selected blocks 8 (it C + p) + warp, it = 0, 1, ...  Each warp keeps a
+// running (m, l, acc) per query head over its blocks: exact softmax terms of
+// the block's tokens, minus the block's own compensation term (the S items
+// summed it for every block).  The CTA combines its warps; the cluster's
+// CTAs then read each other's partials from distributed shared memory, and
+// rank p merges columns of them with the compensation sum into out = acc / l.
+template <int D, int G, int MODE, bool LOOP>
+__global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_attend(LayerArgs a) {
   constexpr bool APPEND = (MODE & kFAppend) != 0;
+  constexpr bool ATT = (MODE & kFAttend) != 0;
   constexpr bool EXTERNAL = (MODE & kFSelect) == 0;  // selection given by the caller
   constexpr int V = D / 32;
   constexpr int TG = G >= 8 ? 2 : ((32 / G) > 16 ? 16 : (32 / G));  // tokens per reduction group
   constexpr int P = TG * G;                                          // 16 or 32 values per group
   constexpr int W = V / 2;                                           // 32-bit words per token slice
   constexpr int NG = kBlock / TG;
-  __shared__ float red_m[kW][G], red_l[kW][G];
-  __shared__ __align__(16) float red_a[kW][G][D];
-  __shared__ int sh_cnt, sh_bad, sh_last;
+  extern __shared__ __align__(16) float asm_[];
+  float* red_a = asm_;                    // [kAW][G][D]
+  float* red_m = red_a + kAW * G * D;     // [kAW][G]
+  float* red_l = red_m + kAW * G;         // [kAW][G]
+  float* cpart = red_l + kAW * G;         // [G][D + 4]: acc, then m at [D], l at [D + 1]
+  int* shi = reinterpret_cast<int*>(cpart + G * (D + 4));  // count, bad
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned long long t_start = a.trace ? global_ns() : 0ull;
-  const int u = blockIdx.x / a.splits, p = blockIdx.x % a.splits;
+  const int C = ATT ? a.splits : 1;
+  const int npick = attend_npick(a.K, C, LOOP);
+  int* pick = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(asm_) +
+                                     attend_union_bytes(D, G, a.key_stride, !EXTERNAL));
+  const int u = blockIdx.x / C;
+  const int p = (int)cluster_rank();
   const int s = u / a.Hkv, h = u % a.Hkv;
   const int K = a.K;
   float qr[G][V];
@@ -1110,8 +1455,8 @@ __global__ void __launch_bounds__(kT) k_attend(LayerArgs a) {
 #pragma unroll
     for (int i = 0; i < V; ++i) qr[g][i] = qg[g * D + lane * V + i] * InvSqrt<D>::v;
   if (tid == 0) {
-    sh_cnt = 0;
-    sh_bad = 0;
+    shi[0] = 0;
+    shi[1] = 0;
   }
   pdl_wait();
   const unsigned long long t_wait = a.trace ? global_ns() : 0ull;
@@ -1119,9 +1464,18 @@ __global__ void __launch_bounds__(kT) k_attend(LayerArgs a) {
   const int* selrow = a.sel + (int64_t)u * K;
   __syncthreads();
   int nsel;
-  if (EXTERNAL) {
+  if (!EXTERNAL) {
+    // the selection, by every CTA of the unit (rank 0 writes the list); this CTA's blocks into pick
+    select_core(a, u, L, reinterpret_cast<unsigned char*>(asm_), p == 0, p, C, pick, npick);
+    nsel = N < K ? N : K;
+    if (!ATT) {
+      for (int i = tid; i < kHist12 / 4; i += kAT)
+        reinterpret_cast<uint4*>(a.hist12 + (int64_t)u * kHist12)[i] = make_uint4(0u, 0u, 0u, 0u);
+      return;
+    }
+  } else {
     int cnt = 0, bad = 0;
-    for (int i = tid; i < K; i += kT) {
+    for (int i = tid; i < K; i += kAT) {
       const int e = __ldcg(selrow + i);
       const int prev = i > 0 ? __ldcg(selrow + i - 1) : -1;
       const bool ok = e >= 0 && e < N && (i == 0 || (prev >= 0 && prev < e));
@@ -1131,14 +1485,12 @@ __global__ void __launch_bounds__(kT) k_attend(LayerArgs a) {
     cnt = __reduce_add_sync(0xffffffffu, cnt);
     bad = __reduce_or_sync(0xffffffffu, bad);
     if (lane == 0) {
-      if (cnt) atomicAdd(&sh_cnt, cnt);
-      if (bad) sh_bad = 1;
+      if (cnt) atomicAdd(shi, cnt);
+      if (bad) shi[1] = 1;
     }
     __syncthreads();
-    nsel = sh_cnt;
-    if (sh_bad && p == 0 && tid == 0) set_error(a.status, kDevBadSelection, s, h, 61);
-  } else {
-    nsel = __ldcg(a.unit_nsel + u);
+    nsel = shi[0];
+    if (shi[1] && p == 0 && tid == 0) set_error(a.status, kDevBadSelection, s, h, 61);
   }
   const bool comp = nsel < N;
   float m[G], l[G], acc[G][V];
@@ -1149,14 +1501,20 @@ __global__ void __launch_bounds__(kT) k_attend(LayerArgs a) {
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[g][i] = 0.f;
   }
-  const int my_i = p * kAttendWarps + warp;
-  int b = -1;
-  if (my_i < K) {
-    const int e = __ldcg(selrow + my_i);
-    const int prev = my_i > 0 ? __ldcg(selrow + my_i - 1) : -1;
-    if (e >= 0 && e < N && (my_i == 0 || (prev >= 0 && prev < e))) b = e;
-  }
-  if (b >= 0) {
+  const int idx = lane & (P - 1);
+  const int jj = idx / G, gl = idx % G;
+  const int rounds = LOOP ? (K + kAW * C - 1) / (kAW * C) : 1;
+  for (int it = 0; it < rounds; ++it) {
+    const int my_i = kAW * (it * C + p) + warp;
+    int b = -1;
+    if (!EXTERNAL) {
+      b = pick[8 * it + warp];
+    } else if (my_i < K) {
+      const int e = __ldcg(selrow + my_i);
+      const int prev = my_i > 0 ? __ldcg(selrow + my_i - 1) : -1;
+      if (e >= 0 && e < N && (my_i == 0 || (prev >= 0 && prev < e))) b = e;
+    }
+    if (b < 0) continue;  // warp-uniform
     const int n = (b == N - 1) ? L - kBlock * b : kBlock;
     const int64_t row = row_of(a, s, h, b);
     const unsigned* kp = reinterpret_cast<const unsigned*>(a.k + row * kBlock * D + lane * V);
@@ -1183,8 +1541,6 @@ __global__ void __launch_bounds__(kT) k_attend(LayerArgs a) {
     for (int i = 0; i < V; ++i) vb[i] = __ldcg(a.vbar + row * D + lane * V + i);
     const float zb_lane = lane < G ? __ldcg(a.chunk_z + ((int64_t)rec * G + lane) * kChunk + (b % kChunk)) : 0.f;
     float zl[NG];
-    const int idx = lane & (P - 1);
-    const int jj = idx / G, gl = idx % G;
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi) {
       float part[P];
@@ -1207,26 +1563,35 @@ __global__ void __launch_bounds__(kT) k_attend(LayerArgs a) {
       }
       zl[gi] = transpose_reduce_warp<P>(part, lane);
     }
+    // the block's max per head, the running max, the rescale of the running sums
     float zmax = -INFINITY;
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi)
       if (gi * TG + jj < n) zmax = fmaxf(zmax, zl[gi]);
 #pragma unroll
     for (int o = G; o < P; o <<= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
+    float mlane = -INFINITY;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float mn = fmaxf(m[g], __shfl_sync(0xffffffffu, zmax, g));
+      const float f = (m[g] == -INFINITY) ? 0.f : expf(m[g] - mn);
+      m[g] = mn;
+      l[g] *= f;
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[g][i] *= f;
+      if (g == gl) mlane = mn;
+    }
     float pl[NG];
     float psum = 0.f;
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi) {
-      pl[gi] = (gi * TG + jj < n) ? expf(zl[gi] - zmax) : 0.f;
+      pl[gi] = (gi * TG + jj < n) ? expf(zl[gi] - mlane) : 0.f;
       psum += pl[gi];
     }
 #pragma unroll
     for (int o = G; o < P; o <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      m[g] = __shfl_sync(0xffffffffu, zmax, g);
-      l[g] = __shfl_sync(0xffffffffu, psum, g);
-    }
+    for (int g = 0; g < G; ++g) l[g] += __shfl_sync(0xffffffffu, psum, g);
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi) {
 #pragma unroll
@@ -1247,7 +1612,7 @@ __global__ void __launch_bounds__(kT) k_attend(LayerArgs a) {
       }
     }
     if (comp) {
-      // remove this block's own compensation term, which kernel 2 summed for every block
+      // remove this block's own compensation term, which the S items summed for every block
       const float lnn = ln_n(n);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -1263,32 +1628,31 @@ __global__ void __launch_bounds__(kT) k_attend(LayerArgs a) {
     }
   }
   const unsigned long long t_comp = a.trace ? global_ns() : 0ull;
-  // merge the warps into this CTA's partial
+  // the CTA's partial: its warps combined
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     if (lane == 0) {
-      red_m[warp][g] = m[g];
-      red_l[warp][g] = l[g];
+      red_m[warp * G + g] = m[g];
+      red_l[warp * G + g] = l[g];
     }
 #pragma unroll
-    for (int i = 0; i < V; ++i) red_a[warp][g][lane * V + i] = acc[g][i];
+    for (int i = 0; i < V; ++i) red_a[(warp * G + g) * D + lane * V + i] = acc[g][i];
   }
   __syncthreads();
-  float* srec = a.split_rec + ((int64_t)u * a.splits + p) * G * (4 + D);
-  for (int i4 = tid; i4 < G * D / 4; i4 += kT) {
+  for (int i4 = tid; i4 < G * D / 4; i4 += kAT) {
     const int g = (4 * i4) / D, col = (4 * i4) % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kW; ++w) M = fmaxf(M, red_m[w][g]);
+    for (int w = 0; w < kAW; ++w) M = fmaxf(M, red_m[w * G + g]);
     float ls = 0.f;
     float4 as = make_float4(0.f, 0.f, 0.f, 0.f);
     if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < kW; ++w) {
-        const float mw = red_m[w][g];
+      for (int w = 0; w < kAW; ++w) {
+        const float mw = red_m[w * G + g];
         const float f = (mw == -INFINITY) ? 0.f : expf(mw - M);
-        ls += red_l[w][g] * f;
-        const float4 x = *reinterpret_cast<const float4*>(&red_a[w][g][col]);
+        ls += red_l[w * G + g] * f;
+        const float4 x = *reinterpret_cast<const float4*>(red_a + (w * G + g) * D + col);
         as.x += x.x * f;
         as.y += x.y * f;
         as.z += x.z * f;
@@ -1296,104 +1660,111 @@ __global__ void __launch_bounds__(kT) k_attend(LayerArgs a) {
       }
     }
     if (col == 0) {
-      srec[g * (4 + D)] = M;
-      srec[g * (4 + D) + 1] = ls;
+      cpart[g * (D + 4) + D] = M;
+      cpart[g * (D + 4) + D + 1] = ls;
     }
-    *reinterpret_cast<float4*>(srec + g * (4 + D) + 4 + col) = as;
+    *reinterpret_cast<float4*>(cpart + g * (D + 4) + col) = as;
+  }
+  if (APPEND && blockIdx.x == 0 && tid == 0)
+    for (int ss = 0; ss < a.B; ++ss) {
+      const int Lold = a.seq_len[ss];
+      if (Lold >= 0 && Lold < a.cap_blocks[ss] * kBlock)
+        a.seq_len[ss] = Lold + 1;
+      else
+        set_error(a.status, kDevCapacity, ss, -1, 42);
+    }
+  // this rank's columns (float4 items) of the output, and their compensation sums (in flight during the barrier)
+  const int items = G * D / 4;
+  const int ipr = (items + C - 1) / C;
+  const int i_lo = p * ipr, i_hi = min(items, i_lo + ipr);
+  const float* ua = a.unit_acc + (int64_t)u * G * (D + 4);
+  float mc = -INFINITY, cl = 0.f;
+  float4 ca = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (comp && tid < i_hi - i_lo) {
+    const int i4 = i_lo + tid, g = (4 * i4) / D, col = (4 * i4) % D;
+    mc = __ldcg(a.unit_ref + u * G + g);
+    cl = __ldcg(ua + g * (D + 4) + D);
+    ca = __ldcg(reinterpret_cast<const float4*>(ua + g * (D + 4) + col));
   }
   const unsigned long long t_rec = a.trace ? global_ns() : 0ull;
-  // the last CTA of the unit merges all partials with the compensation sum
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int prev = atomicAdd(a.mcount + u, 1);
-    sh_last = prev == a.splits - 1;
-    if (sh_last) a.mcount[u] = 0;
-    if (APPEND && blockIdx.x == 0)
-      for (int ss = 0; ss < a.B; ++ss) {
-        const int Lold = a.seq_len[ss];
-        if (Lold >= 0 && Lold < a.cap_blocks[ss] * kBlock)
-          a.seq_len[ss] = Lold + 1;
-        else
-          set_error(a.status, kDevCapacity, ss, -1, 42);
-      }
-  }
-  __syncthreads();
-  if (sh_last) {
-    __threadfence();
-    const float* recs = a.split_rec + (int64_t)u * a.splits * G * (4 + D);
-    const float* ua = a.unit_acc + (int64_t)u * G * (D + 4);
-    float* out = a.out + ((int64_t)s * a.Hkv * G + (int64_t)h * G) * D;
-    const int rs = G * (4 + D);
-    for (int i4 = tid; i4 < G * D / 4; i4 += kT) {
-      const int g = (4 * i4) / D, col = (4 * i4) % D;
+  cluster_sync_all();  // every CTA's partial is in its shared memory (and every CTA is past the selection)
+  if (!EXTERNAL && p == 0)
+    for (int i = tid; i < kHist12 / 4; i += kAT)
+      reinterpret_cast<uint4*>(a.hist12 + (int64_t)u * kHist12)[i] = make_uint4(0u, 0u, 0u, 0u);
+  {
+    // one (column, peer) pair per thread: the peers' partials staged here, then merged per column
+    float* stage = red_a;  // [ipr][C][8]: acc (4), m, l
+    const int npairs = (i_hi - i_lo) * C;
+    for (int pr = tid; pr < npairs; pr += kAT) {
+      const int il = pr / C, q = pr % C;
+      const int i4 = i_lo + il, g = (4 * i4) / D, col = (4 * i4) % D;
+      const float2 ml = ld_peer_f2(peer_smem(cpart + g * (D + 4) + D, (uint32_t)q));
+      const float4 av = ld_peer_f4(peer_smem(cpart + g * (D + 4) + col, (uint32_t)q));
+      *reinterpret_cast<float4*>(stage + pr * 8) = av;
+      *reinterpret_cast<float2*>(stage + pr * 8 + 4) = ml;
+    }
+    __syncthreads();
+    if (tid < i_hi - i_lo) {
+      const int i4 = i_lo + tid, g = (4 * i4) / D, col = (4 * i4) % D;
       float M = -INFINITY, ls = 0.f;
       float4 as = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int q0 = 0; q0 < a.splits; q0 += 8) {
-        float mv[8], lv[8];
-        float4 av[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const int pp = q0 + k;
-          if (pp < a.splits) {
-            const float* rp = recs + (int64_t)pp * rs + g * (4 + D);
-            mv[k] = __ldcg(rp);
-            lv[k] = __ldcg(rp + 1);
-            av[k] = __ldcg(reinterpret_cast<const float4*>(rp + 4 + col));
-          } else {
-            mv[k] = -INFINITY;
-            lv[k] = 0.f;
-            av[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (mv[k] == -INFINITY) continue;
-          const float mn = fmaxf(M, mv[k]);
-          const float fo = (M == -INFINITY) ? 0.f : expf(M - mn);
-          const float fn = expf(mv[k] - mn);
-          ls = ls * fo + lv[k] * fn;
-          as.x = as.x * fo + av[k].x * fn;
-          as.y = as.y * fo + av[k].y * fn;
-          as.z = as.z * fo + av[k].z * fn;
-          as.w = as.w * fo + av[k].w * fn;
-          M = mn;
-        }
+      for (int q = 0; q < C; ++q) {
+        const float* e = stage + (tid * C + q) * 8;
+        const float mq = e[4];
+        if (mq == -INFINITY) continue;
+        const float mn = fmaxf(M, mq);
+        const float fo = (M == -INFINITY) ? 0.f : expf(M - mn);
+        const float fn = expf(mq - mn);
+        ls = ls * fo + e[5] * fn;
+        as.x = as.x * fo + e[0] * fn;
+        as.y = as.y * fo + e[1] * fn;
+        as.z = as.z * fo + e[2] * fn;
+        as.w = as.w * fo + e[3] * fn;
+        M = mn;
       }
-      if (comp) {
-        const float mc = __ldcg(a.unit_ref + u * G + g);
-        if (mc != -INFINITY) {
-          const float cl = __ldcg(ua + g * (D + 4) + D);
-          const float4 ca = __ldcg(reinterpret_cast<const float4*>(ua + g * (D + 4) + col));
-          const float mn = fmaxf(M, mc);
-          const float fo = (M == -INFINITY) ? 0.f : expf(M - mn);
-          const float fn = expf(mc - mn);
-          ls = ls * fo + cl * fn;
-          as.x = as.x * fo + ca.x * fn;
-          as.y = as.y * fo + ca.y * fn;
-          as.z = as.z * fo + ca.z * fn;
-          as.w = as.w * fo + ca.w * fn;
-        }
+      if (comp && mc != -INFINITY) {
+        const float mn = fmaxf(M, mc);
+        const float fo = (M == -INFINITY) ? 0.f : expf(M - mn);
+        const float fn = expf(mc - mn);
+        ls = ls * fo + cl * fn;
+        as.x = as.x * fo + ca.x * fn;
+        as.y = as.y * fo + ca.y * fn;
+        as.z = as.z * fo + ca.z * fn;
+        as.w = as.w * fo + ca.w * fn;
       }
       const float inv = ls > 0.f ? 1.f / ls : 0.f;
+      float* out = a.out + ((int64_t)s * a.Hkv * G + (int64_t)h * G) * D;
       *reinterpret_cast<float4*>(out + g * D + col) = make_float4(as.x * inv, as.y * inv, as.z * inv, as.w * inv);
     }
   }
-  if (tid == 0) trace_item(a, slot_attend(a) + blockIdx.x, sh_last ? 4 : 1, u, p, t_start, t_wait, t_comp, t_rec, 0);
+  cluster_sync_all();  // the peers' reads are done before any CTA of the cluster exits
+  if (tid == 0) trace_item(a, slot_attend(a) + blockIdx.x, p == 0 ? 4 : 1, u, p, t_start, t_wait, t_comp, t_rec, 0);
 }
 
 // ================================================================== launches
-static cudaError_t launch_pdl(const void* fn, dim3 grid, size_t smem, cudaStream_t st, bool pdl, void** args) {
+static cudaError_t launch_pdl(const void* fn, dim3 grid, size_t smem, cudaStream_t st, bool pdl, void** args,
+                              int threads = kT, int cluster = 1) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
-  cfg.blockDim = dim3(kT);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  if (pdl) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  if (cluster > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = (unsigned)cluster;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = na;
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
@@ -1412,32 +1783,51 @@ static cudaError_t ensure_smem(const void* fn, std::atomic<size_t>* configured, 
 
 template <int D, int G, int MODE>
 static cudaError_t launch_chain(const LayerArgs& a_in, cudaStream_t st, int first_pdl) {
-  static std::atomic<size_t> cfg1[64], cfg2[64];
+  static std::atomic<size_t> cfg1[64], cfg2[64], cfg3[64];
   LayerArgs a = a_in;
   void* args[] = {&a};
   constexpr bool SEL = (MODE & kFSelect) != 0;
   constexpr bool COMP = (MODE & kFComp) != 0;
   constexpr bool ATT = (MODE & kFAttend) != 0;
   cudaError_t e;
-  // 1. score: one CTA per 64-block item
+  // 1. score: one CTA per 64-block item (with the compensation: its vbar rows and partial too)
   {
-    const size_t sm = (size_t)score_smem(D, a.r, G);
+    int stages = 1;
+    const size_t sm = (size_t)score_smem(D, a.r, G, COMP, stages);
     const void* fn = reinterpret_cast<const void*>(&k_score<D, G, MODE>);
     if ((e = ensure_smem(fn, cfg1, sm)) != cudaSuccess) return e;
-    if ((e = launch_pdl(fn, dim3(a.total_chunks), sm, st, first_pdl != 0, args)) != cudaSuccess) return e;
+    void* args1[] = {&a, &stages};
+    if ((e = launch_pdl(fn, dim3(a.total_chunks), sm, st, first_pdl != 0, args1)) != cudaSuccess) return e;
   }
-  // 2. S items (512 blocks) then compensation items (128 blocks)
+  // 2a. S items (512 blocks): keys and histogram, compensation partials into the unit's sums
   {
-    const int grid = (SEL ? a.ns_items : 0) + (COMP ? a.n2_items : 0);
-    const size_t sm = (size_t)item_grid_smem(D, G, a.key_stride, SEL, COMP);
-    const void* fn = reinterpret_cast<const void*>(&k_select_comp<D, G, MODE>);
+    const size_t sm = (size_t)s_items_smem(G);
+    const void* fn = reinterpret_cast<const void*>(&k_sitems<D, G, MODE>);
     if ((e = ensure_smem(fn, cfg2, sm)) != cudaSuccess) return e;
-    if ((e = launch_pdl(fn, dim3(grid), sm, st, true, args)) != cudaSuccess) return e;
+    if ((e = launch_pdl(fn, dim3(a.ns_items), sm, st, true, args)) != cudaSuccess) return e;
   }
-  // 3. attention: one CTA per 8 selected blocks
+  // 2b. without the attention: the selection alone, one CTA per unit
+  if (SEL && !ATT) {
+    LayerArgs a1 = a;
+    a1.splits = 1;
+    void* args1[] = {&a1};
+    const size_t sm = (size_t)attend_union_bytes(D, G, a.key_stride, true) + 4 * attend_npick(a.K, 1, false);
+    const void* fn = reinterpret_cast<const void*>(&k_attend<D, G, MODE, false>);
+    if ((e = ensure_smem(fn, cfg3, sm)) != cudaSuccess) return e;
+    if ((e = launch_pdl(fn, dim3(a.B * a.Hkv), sm, st, true, args1, kAT, 1)) != cudaSuccess) return e;
+  }
+  // 3. attention: a cluster of a.splits CTAs (8 selected blocks per CTA and round) per unit
   if (ATT) {
-    const void* fn = reinterpret_cast<const void*>(&k_attend<D, G, MODE>);
-    if ((e = launch_pdl(fn, dim3(a.B * a.Hkv * a.splits), 0, st, true, args)) != cudaSuccess) return e;
+    static std::atomic<size_t> cfg4[64];
+    const bool loop = a.K > kAttendBlocks * a.splits;  // more than one selected block per warp
+    const size_t sm = (size_t)attend_union_bytes(D, G, a.key_stride, SEL) + 4 * attend_npick(a.K, a.splits, loop);
+    static std::atomic<size_t> cfg5[64];
+    const void* fn = loop ? reinterpret_cast<const void*>(&k_attend<D, G, MODE, true>)
+                          : reinterpret_cast<const void*>(&k_attend<D, G, MODE, false>);
+    if ((e = ensure_smem(fn, loop ? cfg5 : cfg4, sm)) != cudaSuccess) return e;
+    if (a.splits > 8 && (e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
+      return e;
+    if ((e = launch_pdl(fn, dim3(a.B * a.Hkv * a.splits), sm, st, true, args, kAT, a.splits)) != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
@@ -1470,8 +1860,10 @@ cudaError_t launch_decode_chain(const LayerArgs& a, int mode, cudaStream_t st, i
 }
 
 size_t chain_smem_bytes(int D, int r, int G, int key_stride) {
-  size_t m = (size_t)score_smem(D, r, G);
-  if ((size_t)item_grid_smem(D, G, key_stride, true, true) > m) m = (size_t)item_grid_smem(D, G, key_stride, true, true);
+  size_t m = (size_t)score_smem(D, r, G, true, 1);
+  if ((size_t)s_items_smem(G) > m) m = (size_t)s_items_smem(G);
+  const size_t at = (size_t)attend_union_bytes(D, G, key_stride, true) + 4 * 264;
+  if (at > m) m = at;
   return m;
 }
 
