@@ -131,7 +131,7 @@ class CompKVCache:
     def launch_count(self) -> int:
         return C.compkv_launch_count(self.ctx)
 
-    def profile(self, enable: bool):
+    def profile(self, enable):
         C.compkv_profile_enable(self.ctx, enable)
 
     def profile_read(self, family):

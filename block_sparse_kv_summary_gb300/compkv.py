@@ -174,11 +174,13 @@ def compkv_launch_count(ctx) -> int:
     return lib().compkv_launch_count(ctx)
 
 
-KERNEL_FAMILIES = {"prefill": 0, "append": 1, "score": 2, "select": 3, "attend": 4, "decode": 5}
+KERNEL_FAMILIES = {"prefill": 0, "append": 1, "score": 2, "select": 3, "attend": 4, "decode": 5,
+                   "k_score": 6, "k_sitems": 7, "k_attend": 8}
 
 
-def compkv_profile_enable(ctx, enable: bool):
-    _check(lib().compkv_profile_enable(ctx, int(bool(enable))), "compkv_profile_enable")
+def compkv_profile_enable(ctx, enable):
+    """enable: False/0 off, True/1 per API call, 2 per call and per kernel of a chain."""
+    _check(lib().compkv_profile_enable(ctx, int(enable)), "compkv_profile_enable")
 
 
 def compkv_profile_read(ctx, family):

@@ -141,7 +141,7 @@ struct compkv_ctx {
   int64_t launches = 0;
   unsigned long long* trace = nullptr;
   int trace_cap = 0;
-  bool prof = false;
+  int prof = 0;  // 0 off, 1 per call, 2 per call and per kernel of a chain
   ProfSlot slots[COMPKV_KERNEL_FAMILIES];
   std::vector<cudaEvent_t> pool;
   ~compkv_ctx() {
@@ -277,11 +277,29 @@ compkv_status launch(compkv_ctx* c, int family, cudaStream_t st, const char* wha
   return COMPKV_OK;
 }
 
+// A decode-step chain (three kernels).  While profiling is on, each kernel is
+// bracketed by its own events too (COMPKV_KERNEL_K_SCORE, _K_SITEMS,
+// _K_ATTEND); the whole call goes under `family`.
 compkv_status launch_chain(compkv_ctx* c, int family, const LayerArgs& a, int mode, cudaStream_t st, const char* what) {
-  return launch(
-      c, family, st, what,
-      [&] { return launch_decode_chain(a, mode, st, 1); },
+  cudaEvent_t ev[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  bool kev = c->prof == 2;
+  for (int i = 0; i < 6 && kev; ++i) kev = (ev[i] = take_event(c)) != nullptr;
+  if (!kev)
+    for (int i = 0; i < 6; ++i)
+      if (ev[i]) c->pool.push_back(ev[i]);
+  const compkv_status r = launch(
+      c, family, st, what, [&] { return launch_decode_chain(a, mode, st, 1, kev ? ev : nullptr); },
       chain_kernels(mode));
+  if (kev) {
+    if (r == COMPKV_OK) {
+      c->slots[COMPKV_KERNEL_K_SCORE].pending.emplace_back(ev[0], ev[1]);
+      c->slots[COMPKV_KERNEL_K_SITEMS].pending.emplace_back(ev[2], ev[3]);
+      c->slots[COMPKV_KERNEL_K_ATTEND].pending.emplace_back(ev[4], ev[5]);
+    } else {
+      for (int i = 0; i < 6; ++i) c->pool.push_back(ev[i]);
+    }
+  }
+  return r;
 }
 
 }  // namespace
@@ -452,7 +470,8 @@ compkv_status compkv_trace(compkv_ctx* c, void* buf, size_t bytes) {
 
 compkv_status compkv_profile_enable(compkv_ctx* c, int enable) {
   if (!c) return fail(COMPKV_ERR_INVALID_ARG, "context is NULL");
-  c->prof = enable != 0;
+  if (enable < 0 || enable > 2) return fail(COMPKV_ERR_INVALID_ARG, "profile level %d not in 0..2", enable);
+  c->prof = enable;
   return COMPKV_OK;
 }
 

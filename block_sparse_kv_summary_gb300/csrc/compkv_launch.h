@@ -30,7 +30,8 @@ cudaError_t launch_append(const LayerArgs& a, cudaStream_t st);
 // kFusedDecode, kFusedScoreSelect (score, select) or kFusedAttend (score for
 // zbar, compensation, attend a caller-given selection).  `first_pdl` lets the
 // first kernel overlap the tail of the previous work on the stream.
-cudaError_t launch_decode_chain(const LayerArgs& a, int mode, cudaStream_t st, int first_pdl);
+// `ev`: null, or six events recorded before and after each of the three kernels.
+cudaError_t launch_decode_chain(const LayerArgs& a, int mode, cudaStream_t st, int first_pdl, cudaEvent_t* ev = nullptr);
 // Kernels a chain of `mode` launches.
 inline int chain_kernels(int mode) { return 3; }
 // Largest dynamic shared memory the chain asks for.

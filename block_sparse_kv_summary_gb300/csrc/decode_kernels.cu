@@ -1132,9 +1132,10 @@ __global__ void __launch_bounds__(kT) k_sitems(LayerArgs a) {
 // selection list and its size; it then puts the blocks at list positions q
 // with (q / 8) mod C == p into pick[(q / 8 / C) * 8 + q % 8] (-1 past the end,
 // pick holding `npick` entries).
-__host__ __device__ inline int select_smem(int key_stride) { return (sel_region_words(key_stride) + 64) * 4; }
-
-constexpr int kKeyBatch = 33;  // 32-key words per warp in flight (8448 keys per pass)
+// shared memory: the full radix selection's region (keys first) | the 12-bit histogram | misc (64) | mbarrier
+__host__ __device__ inline int select_smem(int key_stride) {
+  return (((sel_region_words(key_stride) + 3) & ~3) + kHist12 + 64) * 4 + 16;
+}
 
 __device__ __forceinline__ void select_core(const LayerArgs& a, int u, int L, unsigned char* smraw, bool write_out,
                                             int p, int C, int* pick, int npick) {
@@ -1149,7 +1150,7 @@ __device__ __forceinline__ void select_core(const LayerArgs& a, int u, int L, un
   int* lidx = reinterpret_cast<int*>(lkey + kListMax + 4);
   unsigned* words = reinterpret_cast<unsigned*>(lidx + kListMax + 4);
   int* wbase = reinterpret_cast<int*>(words + (stride + 31) / 32 + 4);
-  int* misc = reinterpret_cast<int*>(smraw) + select_smem(stride) / 4 - 64;  // [64]
+  int* misc = reinterpret_cast<int*>(smraw) + ((sel_region_words(stride) + 3) & ~3) + kHist12;  // [64], then the mbarrier
   int* selrow = a.sel + (int64_t)u * K;
   unsigned long long tp = a.trace ? global_ns() : 0ull;
   const int N = ceil_blocks(L);
@@ -1158,42 +1159,39 @@ __device__ __forceinline__ void select_core(const LayerArgs& a, int u, int L, un
   const int need = K - 3;
   const bool ranked = !all_sel && need > 0;
   unsigned* gh = a.hist12 + (int64_t)u * kHist12;
-  // 1. the histogram (this thread: bins [kHist12 - 16 (tid + 1), kHist12 - 16 tid)) and the first keys
-  uint32_t c[16];
+  uint32_t* hist = reinterpret_cast<uint32_t*>(smraw) + ((sel_region_words(stride) + 3) & ~3);  // [kHist12]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(misc + 64);
+  // 1. the histogram and the unit's keys into shared memory by bulk copies
+  const uint32_t kbytes = ranked ? (uint32_t)((N + 3) & ~3) * 4u : 0u;  // the row is padded to a multiple of 4
+  if (tid == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+    mbar_arrive_expect_tx(bar, ranked ? (uint32_t)kHist12 * 4u + kbytes : 0u);
+    if (ranked) {
+      bulk_g2s(hist, gh, (uint32_t)kHist12 * 4u, bar);
+      bulk_g2s(keys, a.skeys + (int64_t)u * stride, kbytes, bar);
+    }
+  }
+  for (int w = tid; w < nw; w += kT) words[w] = 0u;
+  for (int i = tid; i < npick; i += kT) pick[i] = -1;
+  if (tid == 0) misc[12] = 0;
+  __syncthreads();
+  mbar_wait_bounded(bar, 0, a.status, s, h, 15);
+  // 2. the threshold bin T, scanned from the top (thread t: bins [kHist12 - 16 (t + 1), kHist12 - 16 t));
+  // need_T of its candidates are taken
+  int T = 0, need_T = 0;
+  bool take_all = true;
   if (ranked) {
-    const uint4* src = reinterpret_cast<const uint4*>(gh + kHist12 - 16 * (tid + 1));
+    uint32_t c[16];
+    const uint4* src = reinterpret_cast<const uint4*>(hist + kHist12 - 16 * (tid + 1));
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint4 v = __ldcg(src + k);
+      const uint4 v = src[k];
       c[4 * k] = v.x;
       c[4 * k + 1] = v.y;
       c[4 * k + 2] = v.z;
       c[4 * k + 3] = v.w;
     }
-  }
-  // keys by 32-key words: warp w takes words w, w + 8, ..., one key per lane (coalesced)
-  const uint32_t* ksrc = a.skeys + (int64_t)u * stride;
-  const int nwk = ranked ? nw : 0;
-  uint32_t kv[kKeyBatch];
-#pragma unroll
-  for (int k = 0; k < kKeyBatch; ++k) {
-    const int b = 32 * (warp + kW * k) + lane;
-    kv[k] = (warp + kW * k < nwk && b < N) ? __ldcg(ksrc + b) : 0u;
-  }
-  for (int w = tid; w < nw; w += kT) words[w] = 0u;
-  for (int i = tid; i < npick; i += kT) pick[i] = -1;
-  if (tid == 0) misc[12] = 0;
-  {
-    // consume the keys here so that their loads are issued together, ahead of the scan
-    uint32_t any = 0u;
-#pragma unroll
-    for (int k = 0; k < kKeyBatch; ++k) any |= kv[k];
-    if (any == 0xffffffffu) misc[13] = 1;
-  }
-  // 2. the threshold bin T, scanned from the top; need_T of its candidates are taken
-  int T = 0, need_T = 0;
-  bool take_all = true;
-  if (ranked) {
     int loc = 0;
 #pragma unroll
     for (int k = 0; k < 16; ++k) loc += (int)c[k];
@@ -1201,7 +1199,6 @@ __device__ __forceinline__ void select_core(const LayerArgs& a, int u, int L, un
     const int before = cta_exclusive_scan(loc, misc, &total, lane, warp);
     if (before < need && need <= before + loc) {
       int run = before;
-#pragma unroll
       for (int k = 15; k >= 0; --k) {
         if (run < need && need <= run + (int)c[k]) {
           misc[8] = kHist12 - 16 * (tid + 1) + k;
@@ -1221,39 +1218,48 @@ __device__ __forceinline__ void select_core(const LayerArgs& a, int u, int L, un
   if (tid == 0 && write_out) tp = trace_phase(a, u, 0, 1, tp);
   const bool list_ok = !ranked || take_all || misc[10] <= kListMax;
   if (ranked && list_ok) {
-    // 3. one pass over the keys: bitmap words by ballot, T's candidates listed
-    for (int w0 = 0; w0 < nwk; w0 += kW * kKeyBatch) {
-      if (w0 > 0) {
+    // 3. one pass over the keys: thread t builds words t, t + 256, ... of the
+    // selection bitmap and of T's candidates from 32 keys each (16-byte reads,
+    // rotated by the word so that a warp's reads spread over the banks); then
+    // T's few candidates are listed
+    unsigned* pwords = reinterpret_cast<unsigned*>(wbase);  // its prefix counts come later
+    // key thresholds: selected iff key >= k_sel; in T (and not selected) iff k_lo <= key < k_sel
+    const uint32_t k_lo = (uint32_t)T << kDigitShift;
+    const uint32_t k_sel = take_all ? k_lo : (uint32_t)(T + 1) << kDigitShift;
+    for (int w = tid; w < nw; w += kT) {
+      unsigned sw_ = 0u, pw_ = 0u;
 #pragma unroll
-        for (int k = 0; k < kKeyBatch; ++k) {
-          const int w = w0 + warp + kW * k, b = 32 * w + lane;
-          kv[k] = (w < nwk && b < N) ? __ldcg(ksrc + b) : 0u;
-        }
+      for (int i = 0; i < 8; ++i) {
+        const int c4 = (i + w) & 7;
+        const uint4 k4 = *reinterpret_cast<const uint4*>(keys + 32 * w + 4 * c4);
+        sw_ |= (unsigned)(k4.x >= k_sel) << (4 * c4) | (unsigned)(k4.y >= k_sel) << (4 * c4 + 1) |
+               (unsigned)(k4.z >= k_sel) << (4 * c4 + 2) | (unsigned)(k4.w >= k_sel) << (4 * c4 + 3);
+        pw_ |= (unsigned)(k4.x >= k_lo) << (4 * c4) | (unsigned)(k4.y >= k_lo) << (4 * c4 + 1) |
+               (unsigned)(k4.z >= k_lo) << (4 * c4 + 2) | (unsigned)(k4.w >= k_lo) << (4 * c4 + 3);
       }
-#pragma unroll
-      for (int k = 0; k < kKeyBatch; ++k) {
-        const int w = w0 + warp + kW * k;
-        if (w >= nwk) break;  // warp-uniform
-        const int b = 32 * w + lane;
-        bool sel = false, pend = false;
-        if (b < N) {
-          const bool forced = b == 0 || b >= N - 2;
-          const int dg = (int)(kv[k] >> kDigitShift);
-          sel = forced || dg > T || (dg == T && take_all);
-          pend = !sel && dg == T;
-        }
-        const unsigned word = __ballot_sync(0xffffffffu, sel);
-        if (lane == 0) words[w] = word;
-        const unsigned pb = __ballot_sync(0xffffffffu, pend);
-        if (pb) {
-          int p0 = 0;
-          if (lane == 0) p0 = atomicAdd(misc + 12, __popc(pb));
-          p0 = __shfl_sync(0xffffffffu, p0, 0);
-          if (pend) {
-            const int p = p0 + __popc(pb & ((1u << lane) - 1u));
-            lkey[p] = kv[k];
-            lidx[p] = b;
-          }
+      // blocks past N are not candidates; 0, N - 2, N - 1 are forced
+      const int b0w = 32 * w;
+      const unsigned valid = (N - b0w >= 32) ? 0xffffffffu : ((1u << (N - b0w)) - 1u);
+      unsigned forced = 0u;
+      if (b0w == 0) forced |= 1u;
+      if (N - 2 >= b0w && N - 2 < b0w + 32) forced |= 1u << (N - 2 - b0w);
+      if (N - 1 >= b0w && N - 1 < b0w + 32) forced |= 1u << (N - 1 - b0w);
+      sw_ &= valid;
+      pw_ &= valid & ~sw_ & ~forced;
+      words[w] = sw_ | forced;
+      pwords[w] = pw_;
+    }
+    __syncthreads();
+    for (int w = tid; w < nw; w += kT) {
+      unsigned pw_ = pwords[w];
+      if (pw_) {
+        int p0 = atomicAdd(misc + 12, __popc(pw_));
+        while (pw_) {
+          const int bit = __ffs(pw_) - 1, b = 32 * w + bit;
+          lkey[p0] = keys[b];
+          lidx[p0] = b;
+          ++p0;
+          pw_ &= pw_ - 1u;
         }
       }
     }
@@ -1272,7 +1278,6 @@ __device__ __forceinline__ void select_core(const LayerArgs& a, int u, int L, un
         const uint32_t k0 = lkey[e];
         const int i0 = lidx[e];
         int rank = 0;
-#pragma unroll 4
         for (int f = 0; f < m4; f += 4) {
           const uint4 kf = *reinterpret_cast<const uint4*>(lkey + f);
           const int4 xf = *reinterpret_cast<const int4*>(lidx + f);
@@ -1304,8 +1309,24 @@ __device__ __forceinline__ void select_core(const LayerArgs& a, int u, int L, un
     __syncthreads();
     select_unit(a, u, s, h, N, smraw, misc);
   } else {
-    // 5. prefix counts of the bitmap; the ascending list
-    const int total = word_prefix(words, wbase, nw, lane, warp);
+    // 5. prefix counts of the bitmap (thread t: words [t * per, (t + 1) * per)); the ascending list
+    int total;
+    {
+      const int per = (nw + kT - 1) / kT;
+      int loc = 0;
+      for (int i = 0; i < per; ++i) {
+        const int w = tid * per + i;
+        if (w < nw) loc += __popc(words[w]);
+      }
+      int run = cta_exclusive_scan(loc, misc, &total, lane, warp);
+      for (int i = 0; i < per; ++i) {
+        const int w = tid * per + i;
+        if (w < nw) {
+          wbase[w] = run;
+          run += __popc(words[w]);
+        }
+      }
+    }
     const int want = N < K ? N : K;
     if (write_out && warp == 0 && lane == 0) {
       if (total != want) set_error(a.status, kDevInternal, s, h, 50);
@@ -1782,7 +1803,7 @@ static cudaError_t ensure_smem(const void* fn, std::atomic<size_t>* configured, 
 }
 
 template <int D, int G, int MODE>
-static cudaError_t launch_chain(const LayerArgs& a_in, cudaStream_t st, int first_pdl) {
+static cudaError_t launch_chain(const LayerArgs& a_in, cudaStream_t st, int first_pdl, cudaEvent_t* ev) {
   static std::atomic<size_t> cfg1[64], cfg2[64], cfg3[64];
   LayerArgs a = a_in;
   void* args[] = {&a};
@@ -1797,14 +1818,18 @@ static cudaError_t launch_chain(const LayerArgs& a_in, cudaStream_t st, int firs
     const void* fn = reinterpret_cast<const void*>(&k_score<D, G, MODE>);
     if ((e = ensure_smem(fn, cfg1, sm)) != cudaSuccess) return e;
     void* args1[] = {&a, &stages};
+    if (ev && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return e;
     if ((e = launch_pdl(fn, dim3(a.total_chunks), sm, st, first_pdl != 0, args1)) != cudaSuccess) return e;
+    if (ev && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return e;
   }
   // 2a. S items (512 blocks): keys and histogram, compensation partials into the unit's sums
   {
     const size_t sm = (size_t)s_items_smem(G);
     const void* fn = reinterpret_cast<const void*>(&k_sitems<D, G, MODE>);
     if ((e = ensure_smem(fn, cfg2, sm)) != cudaSuccess) return e;
+    if (ev && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return e;
     if ((e = launch_pdl(fn, dim3(a.ns_items), sm, st, true, args)) != cudaSuccess) return e;
+    if (ev && (e = cudaEventRecord(ev[3], st)) != cudaSuccess) return e;
   }
   // 2b. without the attention: the selection alone, one CTA per unit
   if (SEL && !ATT) {
@@ -1814,7 +1839,9 @@ static cudaError_t launch_chain(const LayerArgs& a_in, cudaStream_t st, int firs
     const size_t sm = (size_t)attend_union_bytes(D, G, a.key_stride, true) + 4 * attend_npick(a.K, 1, false);
     const void* fn = reinterpret_cast<const void*>(&k_attend<D, G, MODE, false>);
     if ((e = ensure_smem(fn, cfg3, sm)) != cudaSuccess) return e;
+    if (ev && (e = cudaEventRecord(ev[4], st)) != cudaSuccess) return e;
     if ((e = launch_pdl(fn, dim3(a.B * a.Hkv), sm, st, true, args1, kAT, 1)) != cudaSuccess) return e;
+    if (ev && (e = cudaEventRecord(ev[5], st)) != cudaSuccess) return e;
   }
   // 3. attention: a cluster of a.splits CTAs (8 selected blocks per CTA and round) per unit
   if (ATT) {
@@ -1827,28 +1854,30 @@ static cudaError_t launch_chain(const LayerArgs& a_in, cudaStream_t st, int firs
     if ((e = ensure_smem(fn, loop ? cfg5 : cfg4, sm)) != cudaSuccess) return e;
     if (a.splits > 8 && (e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
       return e;
+    if (ev && (e = cudaEventRecord(ev[4], st)) != cudaSuccess) return e;
     if ((e = launch_pdl(fn, dim3(a.B * a.Hkv * a.splits), sm, st, true, args, kAT, a.splits)) != cudaSuccess) return e;
+    if (ev && (e = cudaEventRecord(ev[5], st)) != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
 
 template <int D, int G>
-static cudaError_t launch_chain_dg(const LayerArgs& a, int mode, cudaStream_t st, int first_pdl) {
+static cudaError_t launch_chain_dg(const LayerArgs& a, int mode, cudaStream_t st, int first_pdl, cudaEvent_t* ev) {
   switch (mode) {
-    case kFusedDecode: return launch_chain<D, G, kFusedDecode>(a, st, first_pdl);
-    case kFusedScoreSelect: return launch_chain<D, G, kFusedScoreSelect>(a, st, first_pdl);
-    case kFusedAttend: return launch_chain<D, G, kFusedAttend>(a, st, first_pdl);
+    case kFusedDecode: return launch_chain<D, G, kFusedDecode>(a, st, first_pdl, ev);
+    case kFusedScoreSelect: return launch_chain<D, G, kFusedScoreSelect>(a, st, first_pdl, ev);
+    case kFusedAttend: return launch_chain<D, G, kFusedAttend>(a, st, first_pdl, ev);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_decode_chain(const LayerArgs& a, int mode, cudaStream_t st, int first_pdl) {
+cudaError_t launch_decode_chain(const LayerArgs& a, int mode, cudaStream_t st, int first_pdl, cudaEvent_t* ev) {
 #define COMPKV_G(DD)                                                 \
   switch (a.G) {                                                     \
-    case 1: return launch_chain_dg<DD, 1>(a, mode, st, first_pdl);  \
-    case 2: return launch_chain_dg<DD, 2>(a, mode, st, first_pdl);  \
-    case 4: return launch_chain_dg<DD, 4>(a, mode, st, first_pdl);  \
-    case 8: return launch_chain_dg<DD, 8>(a, mode, st, first_pdl);  \
+    case 1: return launch_chain_dg<DD, 1>(a, mode, st, first_pdl, ev);  \
+    case 2: return launch_chain_dg<DD, 2>(a, mode, st, first_pdl, ev);  \
+    case 4: return launch_chain_dg<DD, 4>(a, mode, st, first_pdl, ev);  \
+    case 8: return launch_chain_dg<DD, 8>(a, mode, st, first_pdl, ev);  \
     default: return cudaErrorInvalidValue;                           \
   }
   if (a.d == 128) {

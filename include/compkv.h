@@ -196,13 +196,21 @@ compkv_status compkv_device_status(compkv_ctx *ctx, void *stream);
 /* Kernel launches enqueued by this context since compkv_init (host counter). */
 int64_t compkv_launch_count(const compkv_ctx *ctx);
 
-/* Per-kernel timing (tracing aid, off by default).  While enabled, every
- * kernel the context launches is bracketed by two CUDA events on the launch
- * stream.  compkv_profile_read() synchronises on the recorded events and
+/* Per-kernel timing (tracing aid, off by default).  enable = 1: every API
+ * call that launches kernels is bracketed by two CUDA events on the launch
+ * stream; enable = 2: in addition each kernel of a three-kernel chain is
+ * bracketed on its own (the events between them stop a kernel from launching
+ * early behind its predecessor, so chains run slower); 0 switches it off;
+ * other values give COMPKV_ERR_INVALID_ARG.  compkv_profile_read() synchronises on the recorded events and
  * returns, for one kernel family, the summed device time in milliseconds and
  * the number of launches since the last read (then resets them).  Families:
- * COMPKV_KERNEL_PREFILL, _APPEND, _SCORE, _SELECT, _ATTEND, _DECODE.  Events
- * are host-side CUDA objects; no device memory is allocated. */
+ * COMPKV_KERNEL_PREFILL, _APPEND, _SCORE, _SELECT, _ATTEND, _DECODE time
+ * whole API calls (compkv_prefill, compkv_append, compkv_score_select,
+ * compkv_select, compkv_attend, compkv_decode); a score/select, attend or
+ * decode call launches three kernels, each timed on its own (enable = 2) under
+ * COMPKV_KERNEL_K_SCORE (append + summaries + scores), _K_SITEMS (S and the
+ * compensation sums) and _K_ATTEND (Top-K, attention, joint normalisation).
+ * Events are host-side CUDA objects; no device memory is allocated. */
 enum {
   COMPKV_KERNEL_PREFILL = 0,
   COMPKV_KERNEL_APPEND = 1,
@@ -210,7 +218,10 @@ enum {
   COMPKV_KERNEL_SELECT = 3,
   COMPKV_KERNEL_ATTEND = 4,
   COMPKV_KERNEL_DECODE = 5,
-  COMPKV_KERNEL_FAMILIES = 6
+  COMPKV_KERNEL_K_SCORE = 6,
+  COMPKV_KERNEL_K_SITEMS = 7,
+  COMPKV_KERNEL_K_ATTEND = 8,
+  COMPKV_KERNEL_FAMILIES = 9
 };
 compkv_status compkv_profile_enable(compkv_ctx *ctx, int enable);
 
@@ -220,18 +231,18 @@ compkv_status compkv_profile_enable(compkv_ctx *ctx, int enable);
  * words 1 + 8 i .. 8 + 8 i, for i < (bytes - 8) / 64 (slots beyond are not
  * written):
  *   (cta << 32 | type << 24 | index), unit, t0, t1, t2, x0, x1, x2
- * (times in %globaltimer ns; a scoring CTA's x0 = end of its wait for the
- * previous kernel, x1 = first half of its rows landed, x2 = first half scored).
- * unit = sequence * Hkv + head.  With C scoring items (64 blocks), S
- * S items (512 blocks), I compensation items (128 blocks), U units and A
- * attention CTAs, slots [0, C) hold the scoring CTAs (type 0: t0 start, t1
- * its rows scored, t2 done), [C, C + S + I) the S items (type 7) and the
- * compensation items (type 2) (t0 start, t1 end of the wait for the scoring
- * kernel, t2 done), [C + S + I, ... + U) each unit's selection (type 3, t0 =
- * t1 start), then the attention CTAs (type 1, or 4 for the CTA that merged
- * the unit: t0 start, t1 end of the wait for the selection, x0 partial
- * computed, x1 partial stored), then 32 per unit for the selection's phases
- * (type 5: index = phase, t0..t1 its span; type 6: index = radix level, t0 =
+ * (times in %globaltimer ns, t2 = when the record was written; unit =
+ * sequence * Hkv + head).  With C scoring CTAs (64 blocks each), S S items
+ * (512 blocks each), U units and A attention CTAs (U times the cluster size),
+ * slots [0, C) hold the scoring CTAs (type 0, index = chunk: t0 start, t1 its
+ * summaries and zbar, sigma2 done; x0 start, x1 its k-bar rows landed, x2
+ * its zbar tile computed), [C, C + S) the S items (type 7, index = item of
+ * the unit: t0 start, t1 end of the wait for the scoring kernel), slots
+ * [C + S, C + S + U) are reserved, then the attention CTAs (type 1, or 4 for
+ * cluster rank 0: index = rank, t0 start, t1 end of the wait for the S items,
+ * x0 its attention partial computed, x1 the compensation sums read), then 32
+ * per unit for the selection's phases (type 5: index = phase, t0..t1 its span;
+ * type 6, written by the general radix path only: index = radix level, t0 =
  * keys at the threshold digit, t1 = list length or -1).  A slot a call does
  * not use stays as the caller left it.
  * buf = NULL switches tracing off. */
