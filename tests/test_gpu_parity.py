@@ -172,3 +172,53 @@ def test_device_errors_are_reported():
         run.cache.attend(5, q, sel)
     with pytest.raises(ValueError):
         run.cache.attend(0, q[:, :1], sel)
+
+
+@pytest.mark.parametrize("pattern", ["all_equal", "two_kinds"])
+def test_selection_ties_go_to_the_lower_index(pattern):
+    """Blocks with identical tokens have identical summaries and scores (on both
+    sides: the same operations on the same bytes), so the Top-K boundary falls
+    inside a run of exactly tied keys and only the lower-index rule decides.
+    all_equal: every block the same (4000 blocks: more tied candidates than the
+    fast path lists, so the general radix path runs); two_kinds: block b holds
+    pattern A when b % 5 == 0, else pattern B, every 64-block chunk holding both."""
+    from block_sparse_kv_summary_gb300.cache import CompKVCache
+    Hkv, G, d, r, budget = 2, 4, 128, 4, 1024
+    lens = [16 * 4000, 16 * 200, 16 * 641]
+    cache = CompKVCache(num_layers=1, batch=len(lens), num_kv_heads=Hkv, group_size=G, head_dim=d, r=r,
+                        budget_tokens=budget, capacity_tokens=[L + 16 for L in lens])
+    gen = torch.Generator().manual_seed(11)
+    states = {}
+    for s, L in enumerate(lens):
+        for h in range(Hkv):
+            A = (torch.randn(1, d, generator=gen) + 0.7 * torch.randn(16, d, generator=gen)).to(torch.bfloat16)
+            B = (torch.randn(1, d, generator=gen) + 0.3 * torch.randn(16, d, generator=gen)).to(torch.bfloat16)
+            nb = L // 16
+            blocks = [A if (pattern == "all_equal" or b % 5 == 0) else B for b in range(nb)]
+            K = torch.cat(blocks)
+            V = torch.randn(L, d, generator=gen).to(torch.bfloat16)
+            kv, vv = cache.token_view(0, s, h)
+            kv[:L] = K.cuda()
+            vv[:L] = V.cuda()
+            states[(s, h)] = O.HeadState(K=f64(K), V=f64(V), L=L, r=r).summarise()
+    cache.prefill(0, lens)
+    q = torch.randn(len(lens), Hkv * G, d, generator=gen)
+    sel = cache.score_select(0, q.cuda()).cpu().numpy()
+    Kb = budget // 16
+    q64 = q.numpy().astype(np.float64)
+    for (s, h), st in states.items():
+        S = O.block_scores(q64[s, h * G:(h + 1) * G], st.n, st.kbar, st.Dbar).S
+        N = len(S)
+        # a library matrix product may round identical columns differently in its
+        # edge tiles: give every block its pattern's score so the ties are exact
+        kind = np.array([0 if (pattern == "all_equal" or b % 5 == 0) else 1 for b in range(N)])
+        first = [int(np.nonzero(kind == k)[0][0]) for k in (0, 1) if (kind == k).any()]
+        assert all(np.abs(S[kind == kind[f]] - S[f]).max() <= 1e-12 * S[f] for f in first)
+        S = np.array([S[first[k]] for k in kind])
+        ref = O.select_blocks(S, Kb)
+        if pattern == "all_equal":
+            assert ref.tolist() == list(range(Kb - 2)) + [N - 2, N - 1]
+        exp = np.full(Kb, -1)
+        exp[:len(ref)] = ref
+        assert np.array_equal(sel[s, h], exp), f"unit {(s, h)}:\n gpu {sel[s, h]}\n ref {exp}"
+    assert cache.device_status() == 0
