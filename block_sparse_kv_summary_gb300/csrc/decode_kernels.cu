@@ -115,74 +115,38 @@ __device__ __forceinline__ unsigned long long trace_phase(const LayerArgs& a, in
 }
 
 // ================================================================== 1. score
-// zbar = q . kbar / sqrt(d) for the chunk's 64 blocks and the G query heads is
-// a small contraction (64 x d times d x G), done on the tensor cores with
-// mma.sync m16n8k8 in tf32 and a three-term split for fp32 accuracy:
-// x = hi + lo with hi = x rounded toward zero to tf32, lo = x - hi (exact),
-// x.y ~ hi.hi' + hi.lo' + lo.hi' (the dropped lo.lo' and the tf32 truncation
-// of lo are ~2^-20 relative).  Warp w takes the 16-block tile w & 3 and the
-// half w >> 2 of the coordinates; heads G..7 of the 8 MMA columns are zero.
-// Thread (gid = lane / 4, tig = lane % 4) holds, per 16-coordinate chunk j,
-// coordinates 16 j + 4 tig .. + 3 of its two rows (one 16-byte load each) and
-// of q_gid; a chunk is two k-steps.  sigma2 = (1/d) sum_t Qsq_t Dbar_t is
-// formed by the warps of the second half: by FMAs for r <= 8, else by a
-// second tf32 contraction over the r groups.
-constexpr int kZS = kChunk + 4;  // row stride of the zbar / sigma2 staging (banks)
+// One warp per scoring item (64 blocks of a unit), one warp per CTA, so that
+// nothing in the stream waits on a CTA-wide barrier.  The item's rows arrive
+// in groups of kGB blocks through a private kScoreStages-deep pipeline of 1-D
+// bulk copies (kbar rows, vbar rows, Dbar rows of the group, one mbarrier per
+// stage): while a group is scored the next ones are in flight.
+//
+// Lane l holds coordinates CPL*l .. CPL*l + CPL-1 (CPL = D/32) of the unit's
+// G queries.  A group's zbar partial dots (kGB blocks x G heads per lane) are
+// summed across the warp by a halving butterfly: at each xor step a lane keeps
+// half of its values and receives its partner's partial of that half, so that
+// after five steps lane l holds the full sums of values v = l*VPL .. + VPL-1
+// (VPL = max(1, NV/32), NV = kGB*G; for NV < 32, lanes l with the same
+// l >> log2(32/NV) hold value v = l >> log2(32/NV)), v = block*G + head.
+// sigma2 for r <= 16 is then formed by the lane holding (block, head) from the
+// block's Dbar row; for r >= 32 by the same butterfly over the r groups.
+//
+// Compensation: w_{g,b} = e^(ln|b| + zbar_{g,b} - ref_g) times vbar_b is
+// accumulated per lane over its coordinates; ref_g is the running maximum of
+// ln|b| + zbar over the blocks seen, and the sums are rescaled when it grows,
+// so the item's partial ends relative to mc_g = max_b (ln|b| + zbar).
+constexpr int kGB = 8;            // blocks per pipeline group
+constexpr int kScoreStages = 3;   // groups in flight per warp
 
-__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-  hi = __float_as_uint(x) & 0xffffe000u;
-  lo = __float_as_uint(x - __uint_as_float(hi)) & 0xffffe000u;
+__host__ __device__ inline int score_stage_floats(int D, int r, bool score, bool comp) {
+  return kGB * D + (comp ? kGB * D : 0) + (score ? kGB * ((r + 3) & ~3) : 0);
 }
-
-__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// One k-step pair (a 16-coordinate chunk) of the three-term product:
-// x0, x1 = this thread's 4 coordinates of rows gid, gid + 8; y = its 4 of column gid.
-__device__ __forceinline__ void mma_chunk(float (&c)[4], const float4& x0, const float4& x1, const float4& y) {
-  uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
-  // k-step 0: columns tig, tig + 4 = coordinates 0, 1 of the chunk slice
-  split_tf32(x0.x, ah[0], al[0]);
-  split_tf32(x1.x, ah[1], al[1]);
-  split_tf32(x0.y, ah[2], al[2]);
-  split_tf32(x1.y, ah[3], al[3]);
-  split_tf32(y.x, bh0, bl0);
-  split_tf32(y.y, bh1, bl1);
-  mma_tf32(c, al, bh0, bh1);
-  mma_tf32(c, ah, bl0, bl1);
-  mma_tf32(c, ah, bh0, bh1);
-  // k-step 1: coordinates 2, 3
-  split_tf32(x0.z, ah[0], al[0]);
-  split_tf32(x1.z, ah[1], al[1]);
-  split_tf32(x0.w, ah[2], al[2]);
-  split_tf32(x1.w, ah[3], al[3]);
-  split_tf32(y.z, bh0, bl0);
-  split_tf32(y.w, bh1, bl1);
-  mma_tf32(c, al, bh0, bh1);
-  mma_tf32(c, ah, bl0, bl1);
-  mma_tf32(c, ah, bh0, bh1);
-}
-
-// Shared memory of the scoring kernel: one or two stages, each kbar rows (64 x D) |
-// Dbar rows (64 x r) | with the compensation, vbar rows (64 x D); then
-// variance scratch (D) | zbar, sigma2 (G x kZS each) | Qsq (G x r, padded to 4) |
-// partial products (4 tiles x 32 lanes x 4) | with the compensation, weights
-// (G x kZS) | 2 x 3 mbarriers.
-__host__ __device__ inline int score_stage_words(int D, int r, bool comp) {
-  return kChunk * D + kChunk * r + (comp ? kChunk * D : 0);
-}
-// zbar, sigma2, partial products and weights share a region with the append's
-// per-warp partial sums (2 x 8 x D), which are done with before they are needed
-__host__ __device__ inline int score_scratch_words(int D, int G) {
-  const int a = 2 * G * kZS + 512 + G * kZS, b = 2 * 8 * D;
-  return a > b ? a : b;
-}
-__host__ __device__ inline int score_smem(int D, int r, int G, bool comp, int stages) {
-  return (stages * score_stage_words(D, r, comp) + D + score_scratch_words(D, G) + ((G * r + 3) & ~3)) * 4 + 64;
+// shared memory: stages | zbar [G][64] | sigma2 [G][64] | group weights [kGB][G] |
+// Qsq [G][r] | the appended block's kbar, vbar, Dbar | mbarriers
+__host__ __device__ inline int score_smem(int D, int r, int G, bool score, bool comp) {
+  const int rr = (r + 3) & ~3;
+  return (kScoreStages * score_stage_floats(D, r, score, comp) + 2 * G * kChunk + kGB * G + G * rr + 2 * D + rr) * 4 +
+         8 * kScoreStages + 16;
 }
 
 // A scoring item (64 blocks of a unit) and where its rows are.
@@ -213,362 +177,447 @@ __device__ __forceinline__ ScoreChunk score_chunk(const LayerArgs& a, int idx) {
   return k;
 }
 
-// CTA i scores items i, i + gridDim.x, ...; with two stages the bulk copies
-// of the next item land in the other stage while this one is scored.
+// One halving step of the butterfly: N values per lane -> N/2.
+template <int N>
+__device__ __forceinline__ void halve(float* p, int lane, int o) {
+  const bool up = (lane & o) != 0;
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) {
+    const float send = up ? p[i] : p[i + N / 2];
+    const float keep = up ? p[i + N / 2] : p[i];
+    p[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+  }
+}
+// Sum NV per-lane partials across the warp (layout in the section comment).
+template <int NV>
+__device__ __forceinline__ void butterfly(float (&p)[NV], int lane) {
+  if constexpr (NV >= 2) halve<NV>(p, lane, 16); else p[0] += __shfl_xor_sync(0xffffffffu, p[0], 16);
+  if constexpr (NV >= 4) halve<NV / 2>(p, lane, 8); else p[0] += __shfl_xor_sync(0xffffffffu, p[0], 8);
+  if constexpr (NV >= 8) halve<NV / 4>(p, lane, 4); else p[0] += __shfl_xor_sync(0xffffffffu, p[0], 4);
+  if constexpr (NV >= 16) halve<NV / 8>(p, lane, 2); else p[0] += __shfl_xor_sync(0xffffffffu, p[0], 2);
+  if constexpr (NV >= 32) halve<NV / 16>(p, lane, 1); else p[0] += __shfl_xor_sync(0xffffffffu, p[0], 1);
+}
+
+template <int CPL>
+__device__ __forceinline__ void lds_vec(const float* p, float (&x)[CPL]);
+template <>
+__device__ __forceinline__ void lds_vec<4>(const float* p, float (&x)[4]) {
+  const float4 v = *reinterpret_cast<const float4*>(p);
+  x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+}
+template <>
+__device__ __forceinline__ void lds_vec<2>(const float* p, float (&x)[2]) {
+  const float2 v = *reinterpret_cast<const float2*>(p);
+  x[0] = v.x; x[1] = v.y;
+}
+template <>
+__device__ __forceinline__ void lds_vec<1>(const float* p, float (&x)[1]) { x[0] = *p; }
+
 template <int D, int G, int MODE>
-__global__ void __launch_bounds__(kT, 3) k_score(LayerArgs a, int stages) {
+__global__ void __launch_bounds__(32) k_score(LayerArgs a) {
   constexpr bool APPEND = (MODE & kFAppend) != 0;
   constexpr bool SCORE = (MODE & kFScore) != 0;
   constexpr bool COMP = (MODE & kFComp) != 0;
-  constexpr int JH = D / 32;  // 16-coordinate chunks per half of the coordinates
-  constexpr int SV = D;       // vbar row stride
-  constexpr int kHalf = kChunk / 2;
+  constexpr int CPL = D / 32;                        // coordinates per lane
+  constexpr int NV = kGB * G;                        // (block, head) values of a group
+  constexpr int VPL = NV >= 32 ? NV / 32 : 1;        // values a lane ends with
+  constexpr int SH = NV >= 32 ? 0 : (NV == 16 ? 1 : (NV == 8 ? 2 : 3));  // log2(32 / NV) for NV < 32
   extern __shared__ __align__(128) float sm[];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int r = a.r;
-  const int stage_words = score_stage_words(D, r, COMP);
-  float* svar = sm + stages * stage_words;
-  float* zs = svar + D;
-  float* ss = zs + G * kZS;
-  float* cx = ss + G * kZS;
-  float* sw = cx + 512;
-  float* sapp = zs;  // the append's per-warp partial sums [2][8][D]
-  float* sqs = zs + score_scratch_words(D, G);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sqs + ((G * r + 3) & ~3));  // [stage][half A, half B, vbar]
-  const bool dbar_bulk = SCORE && (r & 3) == 0;
+  const int lane = threadIdx.x;
+  const int r = a.r, rr = (r + 3) & ~3;
+  const int stage_f = score_stage_floats(D, r, SCORE, COMP);
+  float* zs = sm + kScoreStages * stage_f;   // [G][64]
+  float* ss = zs + G * kChunk;               // [G][64]
+  float* sw = ss + G * kChunk;               // [kGB][G]
+  float* sqs = sw + kGB * G;                 // [G][rr]
+  float* pk = sqs + G * rr;                  // appended block: kbar [D], vbar [D], Dbar [rr]
+  float* pv = pk + D;
+  float* pd = pv + D;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(pd + rr);
+  const unsigned long long t_start = a.trace ? global_ns() : 0ull;
   pdl_wait();  // the previous work on the stream may have written this cache
-  if (blockIdx.x == 0 && tid < a.B) {
-    bool f2;
-    a.lnew[tid] = unit_tokens(a, tid, APPEND, &f2);
+  if (blockIdx.x == 0)
+    for (int s = lane; s < a.B; s += 32) {
+      bool f2;
+      a.lnew[s] = unit_tokens(a, s, APPEND, &f2);
+    }
+  const ScoreChunk k = score_chunk<APPEND>(a, blockIdx.x);
+  if (COMP && k.c == 0)
+    for (int i = lane; i < G * (D + 4); i += 32) a.unit_acc[(int64_t)k.u * G * (D + 4) + i] = 0.f;
+  if (k.nb == 0) {
+    pdl_trigger();
+    return;
   }
-  pdl_trigger();
-  if (tid == 0) {
-    for (int i = 0; i < 6; ++i) mbar_init(bars + i, 1);
+  const bool dbar_bulk = SCORE && (r & 3) == 0;
+  const int ng = (k.nb + kGB - 1) / kGB;
+  if (lane == 0) {
+    for (int i = 0; i < kScoreStages; ++i) mbar_init(bars + i, 1);
     fence_mbar_init();
   }
-  __syncthreads();
-  const int my_n = ((int)blockIdx.x < a.total_chunks) ? (a.total_chunks - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
-  // post the expected bytes of item k's stage and start its copies
-  auto issue = [&](const ScoreChunk& k, int st) {
-    float* sk = sm + st * stage_words;
-    float* sd = sk + kChunk * D;
-    float* sv = sd + kChunk * r;
-    uint64_t* bar = bars + 3 * st;
-    const int nA = min(k.nt, kHalf), nB = k.nt - nA;
-    if (tid == 0) {
-      const uint32_t rowb = (uint32_t)D * 4u + (dbar_bulk ? (uint32_t)r * 4u : 0u);
-      mbar_arrive_expect_tx(bar, (uint32_t)nA * rowb);
-      if (nA > 0) {
-        bulk_g2s(sk, a.kbar + k.row0 * D, (uint32_t)nA * D * 4u, bar);
-        if (dbar_bulk) bulk_g2s(sd, a.dbar + k.row0 * r, (uint32_t)nA * r * 4u, bar);
-      }
-      mbar_arrive_expect_tx(bar + 1, (uint32_t)nB * rowb);
-      if (nB > 0) {
-        bulk_g2s(sk + kHalf * D, a.kbar + (k.row0 + kHalf) * D, (uint32_t)nB * D * 4u, bar + 1);
-        if (dbar_bulk) bulk_g2s(sd + kHalf * r, a.dbar + (k.row0 + kHalf) * r, (uint32_t)nB * r * 4u, bar + 1);
-      }
-      mbar_arrive_expect_tx(bar + 2, COMP ? (uint32_t)k.nt * D * 4u : 0u);
+  __syncwarp();
+  // start the copies of group gi into its stage (rows [8 gi, 8 gi + 8) of the item, up to nt)
+  const float* gk = a.kbar + k.row0 * D;
+  const float* gv = a.vbar + k.row0 * D;
+  const float* gd = a.dbar + k.row0 * r;
+  const int nt = k.nt;
+  auto issue = [=](int gi) {
+    if (lane != 0) return;
+    float* st = sm + (gi % kScoreStages) * stage_f;
+    const int rb = gi * kGB, n = max(0, min(kGB, nt - rb));
+    const uint32_t bytes = (uint32_t)n * (uint32_t)(D * 4 * (COMP ? 2 : 1) + (dbar_bulk ? r * 4 : 0));
+    uint64_t* bar = bars + gi % kScoreStages;
+    mbar_arrive_expect_tx(bar, bytes);
+    if (n > 0) {
+      bulk_g2s(st, gk + rb * D, (uint32_t)n * D * 4u, bar);
+      if (COMP) bulk_g2s(st + kGB * D, gv + rb * D, (uint32_t)n * D * 4u, bar);
+      if (dbar_bulk) bulk_g2s(st + kGB * D * (COMP ? 2 : 1), gd + rb * r, (uint32_t)n * r * 4u, bar);
     }
-    if (COMP && tid == 0 && k.nt > 0) bulk_g2s(sv, a.vbar + k.row0 * D, (uint32_t)k.nt * D * 4u, bar + 2);
   };
-  ScoreChunk cur = score_chunk<APPEND>(a, blockIdx.x);
-  if (my_n > 0) issue(cur, 0);
-  const int gid = lane >> 2, tig = lane & 3;
-  const int tile = warp & 3, kh = warp >> 2;
-  for (int it = 0; it < my_n; ++it) {
-    const int st = stages == 2 ? (it & 1) : 0;
-    const uint32_t par = (uint32_t)(stages == 2 ? (it >> 1) : it) & 1u;
-    const unsigned long long t_start = a.trace ? global_ns() : 0ull;
-    ScoreChunk nxt;
-    if (it + 1 < my_n) {
-      nxt = score_chunk<APPEND>(a, blockIdx.x + (it + 1) * gridDim.x);
-      if (stages == 2) issue(nxt, st ^ 1);
+  for (int gi = 0; gi < kScoreStages && gi < ng; ++gi) issue(gi);
+  if (ng <= kScoreStages) pdl_trigger();
+
+  // this lane's coordinates of the G queries
+  const float* qbase = a.q + ((int64_t)k.s * a.Hkv * G + (int64_t)k.h * G) * D;
+  float q[G][CPL];
+#pragma unroll
+  for (int g = 0; g < G; ++g) lds_vec<CPL>(qbase + g * D + CPL * lane, q[g]);  // generic load (global)
+  // Qsq_{g,t} = sum of q_g^2 over coordinate group t = [t*D/r, (t+1)*D/r)
+  if (SCORE) {
+    const int gs = D / r;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      if (gs >= CPL) {
+        float t = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) t = fmaf(q[g][c], q[g][c], t);
+        for (int o = 1; o < gs / CPL; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if ((lane & (gs / CPL - 1)) == 0) sqs[g * rr + (CPL * lane) / gs] = t;
+      } else {
+        float t = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          t = fmaf(q[g][c], q[g][c], t);
+          if ((c + 1) % gs == 0) {
+            sqs[g * rr + (CPL * lane + c) / gs] = t;
+            t = 0.f;
+          }
+        }
+      }
     }
-    if (COMP && cur.c == 0)
-      for (int i = tid; i < G * (D + 4); i += kT) a.unit_acc[(int64_t)cur.u * G * (D + 4) + i] = 0.f;
-    if (cur.nb > 0) {
-      const int s = cur.s, h = cur.h, u = cur.u, L = cur.L, N = cur.N, b0 = cur.b0, nb = cur.nb, nt = cur.nt;
-      const int rec = cur.rec;
-      const int64_t row0 = cur.row0;
-      float* sk = sm + st * stage_words;
-      float* sd = sk + kChunk * D;
-      float* sv = sd + kChunk * r;
-      uint64_t* bar = bars + 3 * st;
-      // this thread's coordinates of q_gid (its B fragments) straight from global memory
-      const float* qbase = a.q + ((int64_t)s * a.Hkv * G + (int64_t)h * G) * D;
-      float4 qv[JH];
-#pragma unroll
-      for (int j = 0; j < JH; ++j)
-        qv[j] = gid < G ? __ldg(reinterpret_cast<const float4*>(qbase + gid * D + 16 * (kh * JH + j) + 4 * tig))
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
-      if (SCORE) {
-        // Qsq_{g,t} = sum of q_g^2 over coordinate group t = [t*D/r, (t+1)*D/r): warp g, 4 coordinates per lane
-        const int gs = D / r;
-        if (warp < G) {
-          const int c4 = 4 * lane;
-          float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (c4 < D) x = __ldg(reinterpret_cast<const float4*>(qbase + warp * D + c4));
-          if (gs >= 4) {
-            float t = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
-            for (int o = 1; o < gs / 4; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-            if (c4 < D && (lane & (gs / 4 - 1)) == 0) sqs[warp * r + c4 / gs] = t;
-          } else if (c4 < D) {
-            const float e[4] = {x.x * x.x, x.y * x.y, x.z * x.z, x.w * x.w};
-            for (int k = 0; k < 4; k += gs) {
-              float t = 0.f;
-              for (int i = 0; i < gs; ++i) t += e[k + i];
-              sqs[warp * r + (c4 + k) / gs] = t;
-            }
-          }
-        }
-      }
-      if (SCORE && (r & 3))
-        for (int i = tid; i < nt * r; i += kT) sd[i] = a.dbar[row0 * r + i];
-      if (cur.append) {
-        // pack the new token and recompute the open block's summary from its
-        // tokens in one pass of 16-byte loads: thread t < 2D takes token
-        // t / (D/8) and coordinates 8 (t % (D/8)) .. + 7 of K and V; sums over
-        // tokens by shuffles within the warp and per-warp partials in shared
-        // memory; mean and population variance two-pass in fp32 from the
-        // exact bf16 values (no E[k^2] - E[k]^2 cancellation)
-        constexpr int GPT = D / 8;        // threads per token
-        constexpr int TPW = 32 / GPT;     // tokens per warp
-        constexpr int NWA = kBlock / TPW; // warps holding tokens
-        const int n = L - kBlock * (N - 1);
-        const int64_t row = row0 + (nb - 1);
-        const int j = tid / GPT, c8 = 8 * (tid % GPT);
-        const bool act = tid < 2 * D && j < n;
-        float kx[8], vx[8];
-        {
-          uint4 kr = make_uint4(0u, 0u, 0u, 0u), vr = make_uint4(0u, 0u, 0u, 0u);
-          if (act) {
-            const int64_t nw_off = ((int64_t)s * a.Hkv + h) * D + c8;
-            if (j == n - 1) {
-              kr = *reinterpret_cast<const uint4*>(a.k_new + nw_off);
-              vr = *reinterpret_cast<const uint4*>(a.v_new + nw_off);
-              *reinterpret_cast<uint4*>(a.k + (row * kBlock + j) * D + c8) = kr;
-              *reinterpret_cast<uint4*>(a.v + (row * kBlock + j) * D + c8) = vr;
-            } else {
-              kr = *reinterpret_cast<const uint4*>(a.k + (row * kBlock + j) * D + c8);
-              vr = *reinterpret_cast<const uint4*>(a.v + (row * kBlock + j) * D + c8);
-            }
-          }
-          const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w}, vw[4] = {vr.x, vr.y, vr.z, vr.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 kf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw[i]));
-            const float2 vf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vw[i]));
-            kx[2 * i] = kf.x;
-            kx[2 * i + 1] = kf.y;
-            vx[2 * i] = vf.x;
-            vx[2 * i + 1] = vf.y;
-          }
-        }
-        // token sums: lanes GPT apart hold the same coordinates
-        float ks[8], vs[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          ks[i] = kx[i];
-          vs[i] = vx[i];
-#pragma unroll
-          for (int o = GPT; o < 32; o <<= 1) {
-            ks[i] += __shfl_xor_sync(0xffffffffu, ks[i], o);
-            vs[i] += __shfl_xor_sync(0xffffffffu, vs[i], o);
-          }
-        }
-        if (warp < NWA && lane < GPT)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            sapp[warp * D + c8 + i] = ks[i];
-            sapp[(8 + warp) * D + c8 + i] = vs[i];
-          }
-        __syncthreads();
-        if (tid < D) {
-          float sk_ = 0.f, sv_ = 0.f;
-          for (int w = 0; w < NWA; ++w) {
-            sk_ += sapp[w * D + tid];
-            sv_ += sapp[(8 + w) * D + tid];
-          }
-          const float mk = sk_ / (float)n, mv = sv_ / (float)n;
-          svar[tid] = mk;  // the mean for the second pass
-          sk[(nb - 1) * D + tid] = mk;
-          a.kbar[row * D + tid] = mk;
-          a.vbar[row * D + tid] = mv;
-          if (COMP) sv[(nb - 1) * D + tid] = mv;
-        }
-        __syncthreads();
-        // squared deviations of K from the mean, summed the same way
-        float qd[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float dv = act ? kx[i] - svar[c8 + i] : 0.f;
-          qd[i] = dv * dv;
-#pragma unroll
-          for (int o = GPT; o < 32; o <<= 1) qd[i] += __shfl_xor_sync(0xffffffffu, qd[i], o);
-        }
-        __syncthreads();  // everyone has read the means
-        if (warp < NWA && lane < GPT)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) sapp[warp * D + c8 + i] = qd[i];
-        __syncthreads();
-        if (tid < D) {
-          float t = 0.f;
-          for (int w = 0; w < NWA; ++w) t += sapp[w * D + tid];
-          svar[tid] = t / (float)n;
-        }
-        __syncthreads();
-        if (tid < r) {
-          // Dbar_t: mean of the variances over coordinate group t = [t*D/r, (t+1)*D/r)
-          const int gs = D / r;
-          float t = 0.f;
-          for (int i = 0; i < gs; ++i) t += svar[tid * gs + i];
-          t /= (float)gs;
-          sd[(nb - 1) * r + tid] = t;
-          a.dbar[row * r + tid] = t;
-        }
-      }
-      __syncthreads();
-      // ---- zbar: this warp's tile and half of the coordinates
-      mbar_wait_bounded(bar + (tile >> 1), par, a.status, s, h, 10 + (tile >> 1));
-      const unsigned long long t_a = a.trace ? global_ns() : 0ull;
-      const int R0 = 16 * tile + gid;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      if (16 * tile < nb) {
-#pragma unroll
-        for (int j = 0; j < JH; ++j) {
-          const int col = 16 * (kh * JH + j) + 4 * tig;
-          const float4 x0 = *reinterpret_cast<const float4*>(sk + R0 * D + col);
-          const float4 x1 = *reinterpret_cast<const float4*>(sk + (R0 + 8) * D + col);
-          mma_chunk(acc, x0, x1, qv[j]);
-        }
-      }
-      if (kh == 1) *reinterpret_cast<float4*>(cx + (tile * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      const unsigned long long t_b = a.trace ? global_ns() : 0ull;
-      __syncthreads();
-      if (16 * tile < nb) {
-        // C fragment: (row gid, columns 2 tig, 2 tig + 1), (row gid + 8, same columns)
-        const int n0 = 2 * tig, n1 = 2 * tig + 1;
-        if (kh == 0) {
-          const float4 o = *reinterpret_cast<const float4*>(cx + (tile * 32 + lane) * 4);
-          const float z[4] = {acc[0] + o.x, acc[1] + o.y, acc[2] + o.z, acc[3] + o.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int row = R0 + (e >> 1) * 8, n = (e & 1) ? n1 : n0;
-            if (n < G && row < nb) zs[n * kZS + row] = z[e] * InvSqrt<D>::v;
-          }
-        } else if (SCORE) {
-          // sigma2 for the same four (row, head) entries
-          float sg[4] = {0.f, 0.f, 0.f, 0.f};
-          if (r <= 8) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int row = R0 + (e >> 1) * 8, n = (e & 1) ? n1 : n0;
-              if (n < G)
-                for (int t = 0; t < r; ++t) sg[e] = fmaf(sqs[n * r + t], sd[row * r + t], sg[e]);
-            }
-          } else {
-            // tf32 contraction over the groups: rows of Dbar times columns of Qsq
-            for (int j = 0; j < r / 16; ++j) {
-              const int col = 16 * j + 4 * tig;
-              const float4 x0 = *reinterpret_cast<const float4*>(sd + R0 * r + col);
-              const float4 x1 = *reinterpret_cast<const float4*>(sd + (R0 + 8) * r + col);
-              float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
-              if (gid < G) y = *reinterpret_cast<const float4*>(sqs + gid * r + col);
-              mma_chunk(sg, x0, x1, y);
-            }
-          }
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int row = R0 + (e >> 1) * 8, n = (e & 1) ? n1 : n0;
-            if (n < G && row < nb) ss[n * kZS + row] = sg[e] / (float)D;
-          }
-        }
-      }
-      const unsigned long long t_loaded = a.trace ? global_ns() : 0ull;
-      __syncthreads();
-      // ---- per query head: item max and sum of e^a, u per block, max of ln|b| + zbar
-      if (warp < G) {
-        const int gw = warp;
-        float av[2], cv[2];
-        float ma = -INFINITY, mc = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int blk = lane + 32 * i;
-          av[i] = cv[i] = -INFINITY;
-          if (blk < nb) {
-            const int bb = b0 + blk;
-            const int n = (bb == N - 1) ? L - kBlock * bb : kBlock;
-            cv[i] = ln_n(n) + zs[gw * kZS + blk];
-            if (SCORE) av[i] = cv[i] + 0.5f * ss[gw * kZS + blk];
-          }
-          ma = fmaxf(ma, av[i]);
-          mc = fmaxf(mc, cv[i]);
-        }
-        mc = warp_max(mc);
-        float la = 0.f;
-        if (SCORE) {
-          ma = warp_max(ma);
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const int blk = lane + 32 * i;
-            const float e = (blk < nb) ? expf(av[i] - ma) : 0.f;
-            la += e;
-            a.chunk_u[((int64_t)rec * G + gw) * kChunk + blk] = (blk < nb) ? e * ss[gw * kZS + blk] : 0.f;
-          }
-          la = warp_sum(la);
-        }
-        if (COMP) {
-          // compensation weights w = e^(ln|b| + zbar - mc) of the item's blocks (mc = their max)
-          float wsum = 0.f;
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const int blk = lane + 32 * i;
-            a.chunk_z[((int64_t)rec * G + gw) * kChunk + blk] = (blk < nb) ? zs[gw * kZS + blk] : 0.f;
-            const float w = (blk < nb) ? expf(cv[i] - mc) : 0.f;
-            sw[gw * kZS + blk] = w;
-            wsum += w;
-          }
-          wsum = warp_sum(wsum);
-          if (lane == 0) a.comp_part[((int64_t)rec * G + gw) * (D + 4) + D] = wsum;
-        }
-        if (lane == 0)
-          *reinterpret_cast<float4*>(a.chunk_rec + ((int64_t)rec * G + gw) * 4) = make_float4(ma, la, mc, 0.f);
-      }
-      if (COMP) {
-        // ---- the item's compensation partial sum_b w_{g,b} vbar_b: out (heads x D) = W (heads x 64) . Vbar (64 x D)
-        // as tf32 MMAs with the three-term split; rows 8..15 of A are zero.  Warp w takes column tiles w, w + 8, ...
-        __syncthreads();
-        mbar_wait_bounded(bar + 2, par, a.status, s, h, 14);
-        for (int nt2 = warp; nt2 < D / 8; nt2 += kW) {
-          float cacc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int ks = 0; ks < kChunk / 8; ++ks) {
-            const int k0 = 8 * ks + tig, k1 = k0 + 4;
-            const float w0 = gid < G ? sw[gid * kZS + k0] : 0.f;
-            const float w1 = gid < G ? sw[gid * kZS + k1] : 0.f;
-            const float v0 = k0 < nb ? sv[k0 * SV + 8 * nt2 + gid] : 0.f;
-            const float v1 = k1 < nb ? sv[k1 * SV + 8 * nt2 + gid] : 0.f;
-            uint32_t ah[4], al[4], bh0, bl0, bh1, bl1;
-            split_tf32(w0, ah[0], al[0]);
-            split_tf32(w1, ah[2], al[2]);
-            ah[1] = ah[3] = al[1] = al[3] = 0u;
-            split_tf32(v0, bh0, bl0);
-            split_tf32(v1, bh1, bl1);
-            mma_tf32(cacc, al, bh0, bh1);
-            mma_tf32(cacc, ah, bl0, bl1);
-            mma_tf32(cacc, ah, bh0, bh1);
-          }
-          if (gid < G)
-            *reinterpret_cast<float2*>(a.comp_part + ((int64_t)rec * G + gid) * (D + 4) + 8 * nt2 + 2 * tig) =
-                make_float2(cacc[0], cacc[1]);
-        }
-      }
-      if (tid == 0) trace_item(a, blockIdx.x + it * gridDim.x, 0, u, cur.c, t_start, t_loaded, t_start, t_a, t_b);
-    }
-    __syncthreads();  // the stage and the working buffers are free again
-    if (it + 1 < my_n && stages == 1) issue(nxt, 0);
-    cur = nxt;
   }
+
+  // ---- append: the item holding the open block packs the new token and
+  // recomputes that block's summary from its tokens (lane = CPL coordinates,
+  // every token; two-pass mean and population variance in fp32 from the
+  // exact bf16 values)
+  const int patched = k.append ? k.nb - 1 : -1;  // item-local block whose rows come from pk, pv, pd
+  if (APPEND && k.append) {
+    const int n = k.L - kBlock * (k.N - 1);
+    const int64_t row = k.row0 + (k.nb - 1);
+    const int c0 = CPL * lane;
+    const int64_t nw_off = ((int64_t)k.s * a.Hkv + k.h) * D + c0;
+    float kx[kBlock][CPL];
+    float ksum[CPL], vsum[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) ksum[c] = vsum[c] = 0.f;
+#pragma unroll
+    for (int j = 0; j < kBlock; ++j) {
+      float kf[CPL], vf[CPL];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) kf[c] = vf[c] = 0.f;
+      if (j < n) {
+        const __nv_bfloat16* ks = (j == n - 1) ? a.k_new + nw_off : a.k + (row * kBlock + j) * D + c0;
+        const __nv_bfloat16* vs = (j == n - 1) ? a.v_new + nw_off : a.v + (row * kBlock + j) * D + c0;
+        load_bf16<CPL>(ks, kf);
+        load_bf16<CPL>(vs, vf);
+        if (j == n - 1) {
+          store_bf16_raw<CPL>(a.k + (row * kBlock + j) * D + c0, a.k_new + nw_off);
+          store_bf16_raw<CPL>(a.v + (row * kBlock + j) * D + c0, a.v_new + nw_off);
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        kx[j][c] = kf[c];
+        ksum[c] += kf[c];
+        vsum[c] += vf[c];
+      }
+    }
+    float var[CPL];
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) {
+      const float mk = ksum[c] / (float)n, mv = vsum[c] / (float)n;
+      pk[c0 + c] = mk;
+      pv[c0 + c] = mv;
+      a.kbar[row * D + c0 + c] = mk;
+      a.vbar[row * D + c0 + c] = mv;
+      float t = 0.f;
+#pragma unroll
+      for (int j = 0; j < kBlock; ++j) {
+        const float dv = j < n ? kx[j][c] - mk : 0.f;
+        t = fmaf(dv, dv, t);
+      }
+      var[c] = t / (float)n;
+    }
+    // Dbar_t: mean of the variances over coordinate group t = [t*D/r, (t+1)*D/r)
+    const int gs = D / r;
+    if (gs >= CPL) {
+      float t = 0.f;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) t += var[c];
+      for (int o = 1; o < gs / CPL; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      if ((lane & (gs / CPL - 1)) == 0) {
+        const float m = t / (float)gs;
+        pd[c0 / gs] = m;
+        a.dbar[row * r + c0 / gs] = m;
+      }
+    } else {
+      float t = 0.f;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        t += var[c];
+        if ((c + 1) % gs == 0) {
+          const float m = t / (float)gs;
+          pd[(c0 + c) / gs] = m;
+          a.dbar[row * r + (c0 + c) / gs] = m;
+          t = 0.f;
+        }
+      }
+    }
+  }
+  __syncwarp();
+  // this lane's values after the butterfly: v = block * G + head
+  int vb[VPL], vg[VPL];
+  const bool primary = NV >= 32 || (lane & ((1 << SH) - 1)) == 0;
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int v = NV >= 32 ? lane * VPL + i : (lane >> SH);
+    vb[i] = v / G;
+    vg[i] = v % G;
+  }
+  constexpr int RPL_MAX = 4;  // Dbar coordinates per lane in the butterfly over the r groups (r = 32 .. 128)
+  // compensation state: per head the reference, per lane its coordinates' sums and its values' weight sums
+  float ref[G], acc[G][CPL], wsl[VPL];
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    ref[g] = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) acc[g][c] = 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) wsl[i] = 0.f;
+
+  for (int gi = 0; gi < ng; ++gi) {
+    const float* st = sm + (gi % kScoreStages) * stage_f;
+    const float* skb = st;
+    const float* svb = st + kGB * D;
+    const float* sdb = st + kGB * D * (COMP ? 2 : 1);
+    const int rb = gi * kGB, nbg = min(kGB, k.nb - rb);
+    mbar_wait_bounded(bars + gi % kScoreStages, (uint32_t)(gi / kScoreStages) & 1u, a.status, k.s, k.h, 10);
+    if (SCORE && !dbar_bulk)
+      for (int i = lane; i < min(kGB, k.nt - rb) * r; i += 32) const_cast<float*>(sdb)[i] = a.dbar[(k.row0 + rb) * r + i];
+    __syncwarp();
+    // zbar partial dots
+    float p[NV];
+#pragma unroll
+    for (int b = 0; b < kGB; ++b) {
+      float x[CPL];
+      const float* rowp = (rb + b == patched) ? pk : skb + b * D;
+      lds_vec<CPL>(rowp + CPL * lane, x);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float t = q[g][0] * x[0];
+#pragma unroll
+        for (int c = 1; c < CPL; ++c) t = fmaf(q[g][c], x[c], t);
+        p[b * G + g] = t;
+      }
+    }
+    butterfly<NV>(p, lane);
+    float zb[VPL], cv[VPL], sg[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int bl = rb + vb[i];
+      const bool ok = vb[i] < nbg;
+      zb[i] = p[i] * InvSqrt<D>::v;
+      const int bg = k.b0 + bl;
+      cv[i] = ok ? ln_n(bg == k.N - 1 ? k.L - kBlock * bg : kBlock) + zb[i] : -INFINITY;
+      sg[i] = 0.f;
+      if (SCORE && r <= 16 && ok) {
+        const float* drow = (bl == patched) ? pd : sdb + vb[i] * r;
+        const float* qsr = sqs + vg[i] * rr;
+        float t = 0.f;
+#pragma unroll
+        for (int tt = 0; tt < 16; ++tt)
+          if (tt < r) t = fmaf(qsr[tt], drow[tt], t);
+        sg[i] = t;
+      }
+    }
+    if (SCORE && r >= 32) {
+      const int rpl = r / 32;
+      float ps[NV];
+#pragma unroll
+      for (int b = 0; b < kGB; ++b) {
+        const float* drow = (rb + b == patched) ? pd : sdb + b * r;
+        float x[RPL_MAX];
+#pragma unroll
+        for (int t = 0; t < RPL_MAX; ++t) x[t] = t < rpl ? drow[rpl * lane + t] : 0.f;
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float t = 0.f;
+#pragma unroll
+          for (int c = 0; c < RPL_MAX; ++c)
+            if (c < rpl) t = fmaf(sqs[g * rr + rpl * lane + c], x[c], t);
+          ps[b * G + g] = t;
+        }
+      }
+      butterfly<NV>(ps, lane);
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) sg[i] = ps[i];
+    }
+    if (primary)
+#pragma unroll
+      for (int i = 0; i < VPL; ++i)
+        if (vb[i] < nbg) {
+          zs[vg[i] * kChunk + rb + vb[i]] = zb[i];
+          if (SCORE) ss[vg[i] * kChunk + rb + vb[i]] = sg[i] / (float)D;
+        }
+    if (COMP) {
+      // the group's maximum of ln|b| + zbar per head (lanes holding the same head)
+      float gm[VPL];
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) gm[i] = cv[i];
+      constexpr int GL = NV >= 32 ? 0 : SH;                                // lowest lane bit of the head
+      constexpr int GB2 = (G / VPL) == 1 ? 0 : ((G / VPL) == 2 ? 1 : ((G / VPL) == 4 ? 2 : 3));  // head bits
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const bool head_bit = o >= (1 << GL) && o < (1 << (GL + GB2));
+        if (!head_bit)
+#pragma unroll
+          for (int i = 0; i < VPL; ++i) gm[i] = fmaxf(gm[i], __shfl_xor_sync(0xffffffffu, gm[i], o));
+      }
+      // every lane learns every head's group maximum and raises its references
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const int src = NV >= 32 ? g / VPL : (g << SH);
+        float m = gm[0];
+#pragma unroll
+        for (int i = 1; i < VPL; ++i)
+          if (g % VPL == i) m = gm[i];
+        m = __shfl_sync(0xffffffffu, m, src);
+        if (m > ref[g]) {  // warp-uniform
+          const float f = ref[g] == -INFINITY ? 0.f : __expf(ref[g] - m);
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) acc[g][c] *= f;
+#pragma unroll
+          for (int i = 0; i < VPL; ++i)
+            if (vg[i] == g) wsl[i] *= f;
+          ref[g] = m;
+        }
+      }
+      // weights of the group's blocks
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        float rg = ref[0];
+#pragma unroll
+        for (int g = 1; g < G; ++g)
+          if (vg[i] == g) rg = ref[g];
+        const float w = vb[i] < nbg ? __expf(cv[i] - rg) : 0.f;
+        if (primary) {
+          sw[vb[i] * G + vg[i]] = w;
+          wsl[i] += w;
+        }
+      }
+      __syncwarp();
+      for (int b = 0; b < nbg; ++b) {
+        float x[CPL], w[G];
+        const float* rowp = (rb + b == patched) ? pv : svb + b * D;
+        lds_vec<CPL>(rowp + CPL * lane, x);
+#pragma unroll
+        for (int g0 = 0; g0 < G; g0 += (G >= 4 ? 4 : G)) {
+          if constexpr (G >= 4) {
+            const float4 t4 = *reinterpret_cast<const float4*>(sw + b * G + g0);
+            w[g0] = t4.x; w[g0 + 1] = t4.y; w[g0 + 2] = t4.z; w[g0 + 3] = t4.w;
+          } else if constexpr (G == 2) {
+            const float2 t2 = *reinterpret_cast<const float2*>(sw + b * G);
+            w[0] = t2.x; w[1] = t2.y;
+          } else {
+            w[0] = sw[b];
+          }
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) acc[g][c] = fmaf(w[g], x[c], acc[g][c]);
+      }
+    }
+    __syncwarp();  // the stage and the weights are free again
+    if (gi + kScoreStages < ng) {
+      issue(gi + kScoreStages);
+      if (gi + kScoreStages == ng - 1) pdl_trigger();
+    }
+  }
+  const unsigned long long t_scored = a.trace ? global_ns() : 0ull;
+  // ---- the item's records, per head
+  const int rec = k.rec;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float av[2], cvv[2], zz[2], s2[2];
+    float ma = -INFINITY, mc = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int blk = lane + 32 * i;
+      av[i] = cvv[i] = -INFINITY;
+      zz[i] = s2[i] = 0.f;
+      if (blk < k.nb) {
+        const int bb = k.b0 + blk;
+        zz[i] = zs[g * kChunk + blk];
+        cvv[i] = ln_n(bb == k.N - 1 ? k.L - kBlock * bb : kBlock) + zz[i];
+        if (SCORE) {
+          s2[i] = ss[g * kChunk + blk];
+          av[i] = cvv[i] + 0.5f * s2[i];
+        }
+      }
+      ma = fmaxf(ma, av[i]);
+      mc = fmaxf(mc, cvv[i]);
+    }
+    mc = warp_max(mc);
+    float la = 0.f;
+    if (SCORE) {
+      ma = warp_max(ma);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int blk = lane + 32 * i;
+        const float e = (blk < k.nb) ? expf(av[i] - ma) : 0.f;
+        la += e;
+        a.chunk_u[((int64_t)rec * G + g) * kChunk + blk] = e * s2[i];
+      }
+      la = warp_sum(la);
+    }
+    if (COMP)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) a.chunk_z[((int64_t)rec * G + g) * kChunk + lane + 32 * i] = zz[i];
+    if (lane == 0) *reinterpret_cast<float4*>(a.chunk_rec + ((int64_t)rec * G + g) * 4) = make_float4(ma, la, mc, 0.f);
+  }
+  if (COMP) {
+    // the partial relative to mc_g = ref_g; weight sums reduced over the lanes holding each head
+    float wt[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) wt[i] = primary ? wsl[i] : 0.f;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float* dst = a.comp_part + ((int64_t)rec * G + g) * (D + 4);
+      if constexpr (CPL == 4)
+        *reinterpret_cast<float4*>(dst + 4 * lane) = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
+      else
+        *reinterpret_cast<float2*>(dst + 2 * lane) = make_float2(acc[g][0], acc[g][1]);
+      float t = 0.f;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i)
+        if (vg[i] == g) t += wt[i];
+      t = warp_sum(t);
+      if (lane == 0) dst[D] = t;
+    }
+  }
+  if (lane == 0) trace_item(a, blockIdx.x, 0, k.u, k.c, t_start, t_scored);
 }
 
 // ================================================================== 2. S items, classify items, compensation
@@ -1811,15 +1860,14 @@ static cudaError_t launch_chain(const LayerArgs& a_in, cudaStream_t st, int firs
   constexpr bool COMP = (MODE & kFComp) != 0;
   constexpr bool ATT = (MODE & kFAttend) != 0;
   cudaError_t e;
-  // 1. score: one CTA per 64-block item (with the compensation: its vbar rows and partial too)
+  // 1. score: one warp (one CTA) per 64-block item
   {
-    int stages = 1;
-    const size_t sm = (size_t)score_smem(D, a.r, G, COMP, stages);
+    constexpr bool SCORE = (MODE & kFScore) != 0;
+    const size_t sm = (size_t)score_smem(D, a.r, G, SCORE, COMP);
     const void* fn = reinterpret_cast<const void*>(&k_score<D, G, MODE>);
     if ((e = ensure_smem(fn, cfg1, sm)) != cudaSuccess) return e;
-    void* args1[] = {&a, &stages};
     if (ev && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return e;
-    if ((e = launch_pdl(fn, dim3(a.total_chunks), sm, st, first_pdl != 0, args1)) != cudaSuccess) return e;
+    if ((e = launch_pdl(fn, dim3(a.total_chunks), sm, st, first_pdl != 0, args, 32)) != cudaSuccess) return e;
     if (ev && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return e;
   }
   // 2a. S items (512 blocks): keys and histogram, compensation partials into the unit's sums
@@ -1889,7 +1937,7 @@ cudaError_t launch_decode_chain(const LayerArgs& a, int mode, cudaStream_t st, i
 }
 
 size_t chain_smem_bytes(int D, int r, int G, int key_stride) {
-  size_t m = (size_t)score_smem(D, r, G, true, 1);
+  size_t m = (size_t)score_smem(D, r, G, true, true);
   if ((size_t)s_items_smem(G) > m) m = (size_t)s_items_smem(G);
   const size_t at = (size_t)attend_union_bytes(D, G, key_stride, true) + 4 * 264;
   if (at > m) m = at;
