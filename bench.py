@@ -298,7 +298,7 @@ def main():
     # ---- device time per call, then per kernel of the chain (library events), separate passes
     kp = min(args.steps, 6400)
     fam_ms = {}
-    for level, fams in ((1, ("decode",)), (2, ("k_score", "k_sitems", "k_attend"))):
+    for level, fams in ((1, ("decode",)), (2, ("k_score", "k_post"))):
         cache.profile(level)
         for fam in fams:
             cache.profile_read(fam)
@@ -346,8 +346,8 @@ def main():
     peak, peak_kind = measured_peaks()
     step_gbs = by["total"] / (us_step_replica * 1e-6) / 1e9
     kernels = {f: {"launches": n, "avg_us": (m * 1e3 / n if n else None)} for f, (m, n) in fam_ms.items()}
-    kernels["decode"]["note"] = "one decode call: the three PDL-chained kernels"
-    for f in ("k_score", "k_sitems", "k_attend"):
+    kernels["decode"]["note"] = "one decode call: the two PDL-chained kernels"
+    for f in ("k_score", "k_post"):
         kernels[f]["note"] = "timed alone (events between the kernels stop their early launch)"
     # the dominant HBM kernel: k_score streams the summaries (kbar, Dbar, vbar) of every block
     ks_us = kernels["k_score"]["avg_us"]

@@ -175,7 +175,7 @@ def compkv_launch_count(ctx) -> int:
 
 
 KERNEL_FAMILIES = {"prefill": 0, "append": 1, "score": 2, "select": 3, "attend": 4, "decode": 5,
-                   "k_score": 6, "k_sitems": 7, "k_attend": 8}
+                   "k_score": 6, "k_post": 7}
 
 
 def compkv_profile_enable(ctx, enable):

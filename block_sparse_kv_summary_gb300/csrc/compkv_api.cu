@@ -35,13 +35,9 @@ struct Layout {
   int64_t rows_per_layer = 0;
   int total_chunks = 0;
   int max_cap_blocks = 0;
-  std::vector<int> ns_first;
-  int ns_items = 0;
-  int K = 0, splits = 0, units = 0, key_stride = 0;
-  size_t off_status = 0, off_lnew = 0, off_mcount = 0, off_hist12 = 0, off_chunk_rec = 0, off_chunk_z = 0,
-         off_chunk_u = 0, off_unit_ref = 0, off_unit_acc = 0, off_comp_part = 0, off_unit_nsel = 0,
-         off_skeys = 0,
-         off_sel = 0, total = 0;
+  int K = 0, splits = 0, units = 0, key_stride = 0, post_cpc = 0;
+  size_t off_status = 0, off_lnew = 0, off_hist12 = 0, off_chunk_rec = 0, off_chunk_z = 0, off_chunk_u = 0,
+         off_comp_part = 0, off_unit_nsel = 0, off_skeys = 0, off_sel = 0, total = 0;
 };
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -75,8 +71,7 @@ compkv_status make_layout(const compkv_config* c, Layout* L) {
   L->seq_row0.resize(c->batch);
   L->chunk0.resize(c->batch);
   L->nchunk.resize(c->batch);
-  L->ns_first.resize(c->batch);
-  int64_t row = 0, ch = 0, chs = 0;
+  int64_t row = 0, ch = 0;
   L->max_cap_blocks = 0;
   for (int s = 0; s < c->batch; ++s) {
     L->seq_row0[s] = row;
@@ -84,23 +79,26 @@ compkv_status make_layout(const compkv_config* c, Layout* L) {
     L->nchunk[s] = (L->cap_blocks[s] + kChunk - 1) / kChunk;
     L->chunk0[s] = (int)ch;
     ch += (int64_t)H * L->nchunk[s];
-    L->ns_first[s] = (int)chs;
-    chs += (int64_t)H * ((L->nchunk[s] + 7) / 8);
     if (L->cap_blocks[s] > L->max_cap_blocks) L->max_cap_blocks = L->cap_blocks[s];
   }
-  // grids of the scoring and compensation kernels (x dimension)
-  if (ch > 0x7fffffff || chs > 0x7fffffff) return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "too many scoring work items");
+  // grid of the scoring kernel (x dimension)
+  if (ch > 0x7fffffff) return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "too many scoring work items");
   L->rows_per_layer = row;
   L->total_chunks = (int)ch;
-  L->ns_items = (int)chs;
   L->key_stride = (L->max_cap_blocks + 3) & ~3;
-  if (chain_smem_bytes(d, c->r, G, L->key_stride) > kMaxSmem)
-    return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "a sequence capacity of %d blocks does not fit the selection in shared memory",
-                L->max_cap_blocks);
   L->K = c->budget_tokens / kBlock;
-  // attention CTAs per unit: one cluster of up to 16, 8 selected blocks per CTA and round
+  // CTAs per unit after the scoring: one cluster of up to 16, 8 selected blocks per CTA and round;
+  // each owns ceil(items / splits) of the unit's scoring items
   L->splits = (L->K + kAttendBlocks - 1) / kAttendBlocks;
   if (L->splits > 16) L->splits = 16;
+  L->post_cpc = 0;
+  for (int s = 0; s < c->batch; ++s) {
+    const int cpc = (L->nchunk[s] + L->splits - 1) / L->splits;
+    if (cpc > L->post_cpc) L->post_cpc = cpc;
+  }
+  if (chain_smem_bytes(d, c->r, G, L->key_stride, L->post_cpc, L->K, L->splits) > kMaxSmem)
+    return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "a sequence capacity of %d blocks does not fit the selection in shared memory",
+                L->max_cap_blocks);
   L->units = c->batch * H;
   size_t off = 0;
   auto region = [&](size_t* o, size_t bytes) {
@@ -109,13 +107,10 @@ compkv_status make_layout(const compkv_config* c, Layout* L) {
   };
   region(&L->off_status, 16);
   region(&L->off_lnew, (size_t)c->batch * sizeof(int));
-  region(&L->off_mcount, (size_t)L->units * sizeof(int));
   region(&L->off_hist12, (size_t)L->units * 4096 * sizeof(unsigned));  // everything before chunk_rec is zeroed per fresh start
   region(&L->off_chunk_rec, (size_t)L->total_chunks * G * 4 * sizeof(float));
   region(&L->off_chunk_z, (size_t)L->total_chunks * G * kChunk * sizeof(float));
   region(&L->off_chunk_u, (size_t)L->total_chunks * G * kChunk * sizeof(float));
-  region(&L->off_unit_ref, (size_t)L->units * G * sizeof(float));
-  region(&L->off_unit_acc, (size_t)L->units * G * (d + 4) * sizeof(float));
   region(&L->off_comp_part, (size_t)L->total_chunks * G * (d + 4) * sizeof(float));
   region(&L->off_unit_nsel, (size_t)L->units * sizeof(int));
   region(&L->off_skeys, (size_t)L->units * L->key_stride * sizeof(uint32_t));
@@ -192,20 +187,17 @@ LayerArgs base_args(const compkv_ctx* c, int layer) {
   char* sc = reinterpret_cast<char*>(c->buf.scratch);
   a.status = reinterpret_cast<int*>(sc + c->lay.off_status);
   a.lnew = reinterpret_cast<int*>(sc + c->lay.off_lnew);
-  a.mcount = reinterpret_cast<int*>(sc + c->lay.off_mcount);
   a.hist12 = reinterpret_cast<unsigned*>(sc + c->lay.off_hist12);
   a.skeys = reinterpret_cast<uint32_t*>(sc + c->lay.off_skeys);
   a.key_stride = c->lay.key_stride;
   a.total_chunks = c->lay.total_chunks;
   a.sms = device_sms();
-  a.ns_items = c->lay.ns_items;
+  a.post_cpc = c->lay.post_cpc;
   a.trace = c->trace;
   a.trace_cap = c->trace_cap;
   a.chunk_rec = reinterpret_cast<float*>(sc + c->lay.off_chunk_rec);
   a.chunk_z = reinterpret_cast<float*>(sc + c->lay.off_chunk_z);
   a.chunk_u = reinterpret_cast<float*>(sc + c->lay.off_chunk_u);
-  a.unit_ref = reinterpret_cast<float*>(sc + c->lay.off_unit_ref);
-  a.unit_acc = reinterpret_cast<float*>(sc + c->lay.off_unit_acc);
   a.comp_part = reinterpret_cast<float*>(sc + c->lay.off_comp_part);
   a.unit_nsel = reinterpret_cast<int*>(sc + c->lay.off_unit_nsel);
   a.sel = reinterpret_cast<int*>(sc + c->lay.off_sel);
@@ -214,7 +206,6 @@ LayerArgs base_args(const compkv_ctx* c, int layer) {
     a.cap_blocks[s] = c->lay.cap_blocks[s];
     a.chunk0[s] = c->lay.chunk0[s];
     a.nchunk[s] = c->lay.nchunk[s];
-    a.ns_first[s] = c->lay.ns_first[s];
   }
   return a;
 }
@@ -278,14 +269,14 @@ compkv_status launch(compkv_ctx* c, int family, cudaStream_t st, const char* wha
 }
 
 // A decode-step chain (three kernels).  While profiling is on, each kernel is
-// bracketed by its own events too (COMPKV_KERNEL_K_SCORE, _K_SITEMS,
-// _K_ATTEND); the whole call goes under `family`.
+// bracketed by its own events too (COMPKV_KERNEL_K_SCORE, _K_POST); the
+// whole call goes under `family`.
 compkv_status launch_chain(compkv_ctx* c, int family, const LayerArgs& a, int mode, cudaStream_t st, const char* what) {
-  cudaEvent_t ev[6] = {nullptr, nullptr, nullptr, nullptr, nullptr, nullptr};
+  cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
   bool kev = c->prof == 2;
-  for (int i = 0; i < 6 && kev; ++i) kev = (ev[i] = take_event(c)) != nullptr;
+  for (int i = 0; i < 4 && kev; ++i) kev = (ev[i] = take_event(c)) != nullptr;
   if (!kev)
-    for (int i = 0; i < 6; ++i)
+    for (int i = 0; i < 4; ++i)
       if (ev[i]) c->pool.push_back(ev[i]);
   const compkv_status r = launch(
       c, family, st, what, [&] { return launch_decode_chain(a, mode, st, 1, kev ? ev : nullptr); },
@@ -293,10 +284,9 @@ compkv_status launch_chain(compkv_ctx* c, int family, const LayerArgs& a, int mo
   if (kev) {
     if (r == COMPKV_OK) {
       c->slots[COMPKV_KERNEL_K_SCORE].pending.emplace_back(ev[0], ev[1]);
-      c->slots[COMPKV_KERNEL_K_SITEMS].pending.emplace_back(ev[2], ev[3]);
-      c->slots[COMPKV_KERNEL_K_ATTEND].pending.emplace_back(ev[4], ev[5]);
+      c->slots[COMPKV_KERNEL_K_POST].pending.emplace_back(ev[2], ev[3]);
     } else {
-      for (int i = 0; i < 6; ++i) c->pool.push_back(ev[i]);
+      for (int i = 0; i < 4; ++i) c->pool.push_back(ev[i]);
     }
   }
   return r;

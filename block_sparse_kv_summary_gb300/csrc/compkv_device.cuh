@@ -51,18 +51,14 @@ struct LayerArgs {
   float* chunk_rec;           // [chunk records][G][4]: max a, sum e^(a - max a), max(ln|b| + zbar), -
   float* chunk_z;             // [chunk records][G][kChunk]  zbar per block
   float* chunk_u;             // [chunk records][G][kChunk]  e^(a - max a) * sigma2 per block
-  float* unit_ref;            // [units][G]  reference exponent of the compensation weights
-  float* unit_acc;            // [units][G][d + 4]: sum_b w vbar_b over all blocks, then sum_b w at [d]
   float* comp_part;           // [chunk records][G][d + 4]: the chunk's sums with w relative to its own max
   int* unit_nsel;             // [units] selected blocks
-  uint32_t* skeys;            // [units][key_stride] S_b as order-preserving keys
+  uint32_t* skeys;            // [units][key_stride] S_b as order-preserving keys (full radix selection only)
   int key_stride;             // max capacity in blocks, rounded up to a multiple of 4
-  unsigned* hist12;           // [units][4096] histogram of the keys' top 12 bits (reset by the unit's selection)
-  int* mcount;                // [units] attention items finished (reset by the last)
+  unsigned* hist12;           // [units][4096] histogram of the keys' top 12 bits (full radix selection only)
   int total_chunks;           // scoring items of the layer (64 blocks)
-  int sms;                    // multiprocessors of the device (persistent grids)
-  int ns_items;               // S items of the layer (512 blocks)
-  int ns_first[kMaxBatch];    // first S item of (s, head 0)
+  int sms;                    // multiprocessors of the device
+  int post_cpc;               // scoring items owned by one CTA of a unit's cluster (max over sequences)
   // optional trace of the work items (null: off)
   unsigned long long* trace;  // see compkv_trace
   int trace_cap;

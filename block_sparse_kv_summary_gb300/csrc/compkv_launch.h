@@ -33,8 +33,8 @@ cudaError_t launch_append(const LayerArgs& a, cudaStream_t st);
 // `ev`: null, or six events recorded before and after each of the three kernels.
 cudaError_t launch_decode_chain(const LayerArgs& a, int mode, cudaStream_t st, int first_pdl, cudaEvent_t* ev = nullptr);
 // Kernels a chain of `mode` launches.
-inline int chain_kernels(int mode) { return 3; }
+inline int chain_kernels(int mode) { return 2; }
 // Largest dynamic shared memory the chain asks for.
-size_t chain_smem_bytes(int D, int r, int G, int key_stride);
+size_t chain_smem_bytes(int D, int r, int G, int key_stride, int post_cpc, int K, int splits);
 
 }  // namespace compkv

@@ -42,12 +42,11 @@
 
 namespace compkv {
 
-constexpr int kT = 256;            // threads per CTA, all three kernels
+constexpr int kT = 256;            // threads of the full radix selection (one CTA)
 constexpr int kW = kT / 32;
 constexpr int kPrivBins = 256;     // histogram bins of one radix digit
 constexpr int kListMax = 2048;     // keys in play compacted into a list once at most this many
 constexpr int kRankMax = 512;      // listed keys in play ranked directly once at most this many
-constexpr int kChunkS = 8 * kChunk;  // blocks per S item and per classify item
 constexpr int kDigitShift = 19;      // the classify digit: key bits 30..19 (exponent, 4 mantissa bits)
 constexpr int kHist12 = 1 << (31 - kDigitShift);
 
@@ -81,11 +80,9 @@ __device__ __forceinline__ int chunk_record(const LayerArgs& a, int s, int h, in
   return a.chunk0[s] + h * a.nchunk[s] + c;
 }
 
-// Trace slots: scoring CTAs, S items, one selection record per unit, attention
-// CTAs, then 32 phase marks per unit.
-__device__ __forceinline__ int slot_items(const LayerArgs& a) { return a.total_chunks; }
-__device__ __forceinline__ int slot_select(const LayerArgs& a) { return a.total_chunks + a.ns_items; }
-__device__ __forceinline__ int slot_attend(const LayerArgs& a) { return slot_select(a) + a.B * a.Hkv; }
+// Trace slots: scoring CTAs, the CTAs of the units' clusters, then 32 phase
+// marks per unit (the full radix selection).
+__device__ __forceinline__ int slot_attend(const LayerArgs& a) { return a.total_chunks; }
 __device__ __forceinline__ int slot_phase(const LayerArgs& a) { return slot_attend(a) + a.B * a.Hkv * a.splits; }
 
 // Record (cta << 32 | type << 24 | index), unit, t0, t1, now, x0, x1, x2 into `slot`.
@@ -242,8 +239,6 @@ __global__ void __launch_bounds__(32) k_score(LayerArgs a) {
       a.lnew[s] = unit_tokens(a, s, APPEND, &f2);
     }
   const ScoreChunk k = score_chunk<APPEND>(a, blockIdx.x);
-  if (COMP && k.c == 0)
-    for (int i = lane; i < G * (D + 4); i += 32) a.unit_acc[(int64_t)k.u * G * (D + 4) + i] = 0.f;
   if (k.nb == 0) {
     pdl_trigger();
     return;
@@ -620,13 +615,11 @@ __global__ void __launch_bounds__(32) k_score(LayerArgs a) {
   if (lane == 0) trace_item(a, blockIdx.x, 0, k.u, k.c, t_start, t_scored);
 }
 
-// ================================================================== 2. S items, classify items, compensation
-// Shared memory:
-//   S item:        12-bit histogram (4096) | item factors (8 x G)
-//   select CTA:    keys | per-warp histograms | summed histogram | list
-//                  keys | list indices | bitmap | prefix (the fast path uses
-//                  the list and the bitmap); misc (64) at the end
-//   comp item:     vbar rows (128 x D) | weights (G x 128) | M_g (G) | mbarrier
+// ================================================================== selection helpers
+// The full radix selection of one unit by one CTA (the rare path when more
+// keys share the threshold bin than the cluster's list holds).  Its shared
+// memory: keys | per-warp histograms | summed histogram | list keys | list
+// indices | bitmap | prefix.
 __host__ __device__ inline int sel_region_words(int key_stride) {
   const int words = (key_stride + 31) / 32 + 4;
   return key_stride + 4 + (kW + 1) * kPrivBins + 2 * (kListMax + 4) + 2 * words;
@@ -1010,415 +1003,6 @@ __device__ __forceinline__ void select_unit(const LayerArgs& a, int u, int s, in
 // and 4 mantissa bits) of the candidates 1..N-3, summed into the unit's.
 // With the compensation: its 8 chunks' partial sums rescaled from their own
 // reference to M_g and added to the unit's accumulator (item 0 records M_g).
-__host__ __device__ inline int s_items_smem(int G) { return (kHist12 + 8 * G + 8 * G + G) * 4; }
-
-template <int D, int G, int MODE>
-__global__ void __launch_bounds__(kT) k_sitems(LayerArgs a) {
-  constexpr bool APPEND = (MODE & kFAppend) != 0;
-  constexpr bool SEL = (MODE & kFSelect) != 0;
-  constexpr bool COMP = (MODE & kFComp) != 0;
-  extern __shared__ __align__(128) unsigned char smraw[];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const unsigned long long t_start = a.trace ? global_ns() : 0ull;
-  const int item = blockIdx.x;
-  int s = 0;
-  while (s + 1 < a.B && a.ns_first[s + 1] <= item) ++s;
-  const int nper = (a.nchunk[s] + 7) / 8;
-  const int local = item - a.ns_first[s];
-  const int h = local / nper, ci = local % nper;
-  const int u = s * a.Hkv + h;
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smraw);    // [kHist12]
-  float* fch = reinterpret_cast<float*>(hist + kHist12);  // [8][G] e^(max a - LSE_g)
-  float* fcp = fch + 8 * G;                               // [8][G] e^(mc - M_g)
-  if (SEL)
-    for (int i = tid; i < kHist12 / 4; i += kT) reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
-  pdl_wait();
-  pdl_trigger();
-  const unsigned long long t_wait = a.trace ? global_ns() : 0ull;
-  bool fits;
-  const int L = unit_tokens(a, s, APPEND, &fits);
-  const int N = ceil_blocks(L);
-  const int b0 = ci * kChunkS;
-  const int nb = b0 < N ? min(kChunkS, N - b0) : 0;
-  if (nb == 0) return;
-  // 1. the u values of the item's blocks (two per thread), in flight while
-  // each query head's warp g forms LSE_g and M_g from the unit's records
-  // (eight per lane in flight) and the item's factors
-  const int nch = (N + kChunk - 1) / kChunk;
-  const int rec0 = chunk_record(a, s, h, 0);
-  const int cs0 = b0 / kChunk;
-  float uu[2][G];
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int blk = tid + kT * k;
-    const int b = b0 + blk;
-    const int rec = rec0 + b / kChunk;
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-      uu[k][g] = (SEL && blk < nb) ? __ldcg(a.chunk_u + ((int64_t)rec * G + g) * kChunk + (b % kChunk)) : 0.f;
-  }
-  if (warp < G) {
-    const int g = warp;
-    float M = -INFINITY, S = 0.f, MC = -INFINITY, fx = 0.f, fz = 0.f;
-    int fj = -1;
-    for (int c0 = 0; c0 < nch; c0 += 256) {
-      float4 rv[8];
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int c = c0 + lane + 32 * k;
-        rv[k] = c < nch ? __ldcg(reinterpret_cast<const float4*>(a.chunk_rec + ((int64_t)(rec0 + c) * G + g) * 4))
-                        : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
-      }
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int c = c0 + lane + 32 * k;
-        if (c >= cs0 && c < cs0 + 8 && c < nch) {
-          fx = rv[k].x;
-          fz = rv[k].z;
-          fj = c - cs0;
-        }
-        MC = fmaxf(MC, rv[k].z);
-        if (SEL && rv[k].x != -INFINITY) {
-          const float mn = fmaxf(M, rv[k].x);
-          S = (M == -INFINITY ? 0.f : S * expf(M - mn)) + rv[k].y * expf(rv[k].x - mn);
-          M = mn;
-        }
-      }
-    }
-    MC = warp_max(MC);
-    if (SEL) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float M2 = __shfl_xor_sync(0xffffffffu, M, o), S2 = __shfl_xor_sync(0xffffffffu, S, o);
-        const float Mn = fmaxf(M, M2);
-        if (Mn != -INFINITY) {
-          S = (M == -INFINITY ? 0.f : S * expf(M - Mn)) + (M2 == -INFINITY ? 0.f : S2 * expf(M2 - Mn));
-          M = Mn;
-        }
-      }
-      const float lg = M + logf(S);
-      if (fj >= 0) fch[fj * G + g] = expf(fx - lg);
-    }
-    if (COMP) {
-      if (fj >= 0) fcp[fj * G + g] = expf(fz - MC);
-      if (ci == 0 && lane == 0) a.unit_ref[u * G + g] = MC;
-    }
-  }
-  __syncthreads();
-  if (SEL) {
-    // 2. S_b = sum_g u_{g,b} e^(max a - LSE_g) = sum_g phat sigma2 as keys
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-      const int blk = tid + kT * k;
-      if (blk >= nb) continue;
-      const int b = b0 + blk;
-      const int cl = blk / kChunk;
-      float S = 0.f;
-#pragma unroll
-      for (int g = 0; g < G; ++g) S = fmaf(uu[k][g], fch[cl * G + g], S);
-      S = fmaxf(S, 0.f);
-      const uint32_t key = __float_as_uint(S);
-      a.skeys[(int64_t)u * a.key_stride + b] = key;
-      if (a.scores) a.scores[(int64_t)u * a.score_stride + b] = S;
-      if (b >= 1 && b <= N - 3) atomicAdd(&hist[key >> kDigitShift], 1u);
-    }
-  }
-  if (COMP) {
-    // 3. the chunks' compensation partials, rescaled to M_g, into the unit's accumulator
-    const int ncl = min(8, nch - cs0);
-    float* ua = a.unit_acc + (int64_t)u * G * (D + 4);
-    for (int i = tid; i < G * (D + 4) / 4; i += kT) {
-      const int g = (4 * i) / (D + 4), col = (4 * i) % (D + 4);
-      float4 v[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        v[j] = j < ncl ? __ldcg(reinterpret_cast<const float4*>(a.comp_part + ((int64_t)(rec0 + cs0 + j) * G + g) * (D + 4) + col))
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j >= ncl) break;
-        const float f = fcp[j * G + g];
-        t.x = fmaf(f, v[j].x, t.x);
-        t.y = fmaf(f, v[j].y, t.y);
-        t.z = fmaf(f, v[j].z, t.z);
-        t.w = fmaf(f, v[j].w, t.w);
-      }
-      if (col < D) {
-        atomicAdd(ua + g * (D + 4) + col, t.x);
-        atomicAdd(ua + g * (D + 4) + col + 1, t.y);
-        atomicAdd(ua + g * (D + 4) + col + 2, t.z);
-        atomicAdd(ua + g * (D + 4) + col + 3, t.w);
-      } else {
-        atomicAdd(ua + g * (D + 4) + D, t.x);  // the weight sums sit at column D
-      }
-    }
-  }
-  if (SEL) {
-    __syncthreads();
-    // 4. the item's histogram into the unit's (non-zero bins only)
-    unsigned* gh = a.hist12 + (int64_t)u * kHist12;
-    for (int i = tid; i < kHist12 / 4; i += kT) {
-      const uint4 v = reinterpret_cast<const uint4*>(hist)[i];
-      if (v.x) atomicAdd(gh + 4 * i, v.x);
-      if (v.y) atomicAdd(gh + 4 * i + 1, v.y);
-      if (v.z) atomicAdd(gh + 4 * i + 2, v.z);
-      if (v.w) atomicAdd(gh + 4 * i + 3, v.w);
-    }
-  }
-  if (tid == 0) trace_item(a, slot_items(a) + blockIdx.x, 7, u, ci, t_start, t_wait);
-}
-
-// Selection of unit u by a whole CTA, after every S item.  The unit's 12-bit
-// histogram of candidate keys gives the threshold bin T where the count of
-// larger-or-equal candidates reaches K - 3; one pass over the unit's keys (16-byte
-// loads, batched with the histogram's) marks the forced blocks and the
-// candidates above T (and in T when all of it is needed) in a bitmap and
-// lists T's candidates; those are ranked by (S_b desc, index asc) and the
-// top ones join the bitmap; the bitmap's prefix counts give the ascending
-// selection.  If more candidates share T than the list holds, the full radix
-// selection over the keys runs instead.  With `write_out` the CTA writes the
-// selection list and its size; it then puts the blocks at list positions q
-// with (q / 8) mod C == p into pick[(q / 8 / C) * 8 + q % 8] (-1 past the end,
-// pick holding `npick` entries).
-// shared memory: the full radix selection's region (keys first) | the 12-bit histogram | misc (64) | mbarrier
-__host__ __device__ inline int select_smem(int key_stride) {
-  return (((sel_region_words(key_stride) + 3) & ~3) + kHist12 + 64) * 4 + 16;
-}
-
-__device__ __forceinline__ void select_core(const LayerArgs& a, int u, int L, unsigned char* smraw, bool write_out,
-                                            int p, int C, int* pick, int npick) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int s = u / a.Hkv, h = u % a.Hkv;
-  const int K = a.K;
-  const int stride = a.key_stride;
-  // the full radix selection's layout; the fast path uses its list and bitmap
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smraw);
-  uint32_t* hsum = keys + stride + 4 + kW * kPrivBins;
-  uint32_t* lkey = hsum + kPrivBins;
-  int* lidx = reinterpret_cast<int*>(lkey + kListMax + 4);
-  unsigned* words = reinterpret_cast<unsigned*>(lidx + kListMax + 4);
-  int* wbase = reinterpret_cast<int*>(words + (stride + 31) / 32 + 4);
-  int* misc = reinterpret_cast<int*>(smraw) + ((sel_region_words(stride) + 3) & ~3) + kHist12;  // [64], then the mbarrier
-  int* selrow = a.sel + (int64_t)u * K;
-  unsigned long long tp = a.trace ? global_ns() : 0ull;
-  const int N = ceil_blocks(L);
-  const int nw = (N + 31) / 32;
-  const bool all_sel = N <= K;
-  const int need = K - 3;
-  const bool ranked = !all_sel && need > 0;
-  unsigned* gh = a.hist12 + (int64_t)u * kHist12;
-  uint32_t* hist = reinterpret_cast<uint32_t*>(smraw) + ((sel_region_words(stride) + 3) & ~3);  // [kHist12]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(misc + 64);
-  // 1. the histogram and the unit's keys into shared memory by bulk copies
-  const uint32_t kbytes = ranked ? (uint32_t)((N + 3) & ~3) * 4u : 0u;  // the row is padded to a multiple of 4
-  if (tid == 0) {
-    mbar_init(bar, 1);
-    fence_mbar_init();
-    mbar_arrive_expect_tx(bar, ranked ? (uint32_t)kHist12 * 4u + kbytes : 0u);
-    if (ranked) {
-      bulk_g2s(hist, gh, (uint32_t)kHist12 * 4u, bar);
-      bulk_g2s(keys, a.skeys + (int64_t)u * stride, kbytes, bar);
-    }
-  }
-  for (int w = tid; w < nw; w += kT) words[w] = 0u;
-  for (int i = tid; i < npick; i += kT) pick[i] = -1;
-  if (tid == 0) misc[12] = 0;
-  __syncthreads();
-  mbar_wait_bounded(bar, 0, a.status, s, h, 15);
-  // 2. the threshold bin T, scanned from the top (thread t: bins [kHist12 - 16 (t + 1), kHist12 - 16 t));
-  // need_T of its candidates are taken
-  int T = 0, need_T = 0;
-  bool take_all = true;
-  if (ranked) {
-    uint32_t c[16];
-    const uint4* src = reinterpret_cast<const uint4*>(hist + kHist12 - 16 * (tid + 1));
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint4 v = src[k];
-      c[4 * k] = v.x;
-      c[4 * k + 1] = v.y;
-      c[4 * k + 2] = v.z;
-      c[4 * k + 3] = v.w;
-    }
-    int loc = 0;
-#pragma unroll
-    for (int k = 0; k < 16; ++k) loc += (int)c[k];
-    int total;
-    const int before = cta_exclusive_scan(loc, misc, &total, lane, warp);
-    if (before < need && need <= before + loc) {
-      int run = before;
-      for (int k = 15; k >= 0; --k) {
-        if (run < need && need <= run + (int)c[k]) {
-          misc[8] = kHist12 - 16 * (tid + 1) + k;
-          misc[9] = need - run;
-          misc[10] = (int)c[k];
-        }
-        run += (int)c[k];
-      }
-    }
-  }
-  __syncthreads();
-  if (ranked) {
-    T = misc[8];
-    need_T = misc[9];
-    take_all = misc[10] == need_T;
-  }
-  if (tid == 0 && write_out) tp = trace_phase(a, u, 0, 1, tp);
-  const bool list_ok = !ranked || take_all || misc[10] <= kListMax;
-  if (ranked && list_ok) {
-    // 3. one pass over the keys: thread t builds words t, t + 256, ... of the
-    // selection bitmap and of T's candidates from 32 keys each (16-byte reads,
-    // rotated by the word so that a warp's reads spread over the banks); then
-    // T's few candidates are listed
-    unsigned* pwords = reinterpret_cast<unsigned*>(wbase);  // its prefix counts come later
-    // key thresholds: selected iff key >= k_sel; in T (and not selected) iff k_lo <= key < k_sel
-    const uint32_t k_lo = (uint32_t)T << kDigitShift;
-    const uint32_t k_sel = take_all ? k_lo : (uint32_t)(T + 1) << kDigitShift;
-    for (int w = tid; w < nw; w += kT) {
-      unsigned sw_ = 0u, pw_ = 0u;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int c4 = (i + w) & 7;
-        const uint4 k4 = *reinterpret_cast<const uint4*>(keys + 32 * w + 4 * c4);
-        sw_ |= (unsigned)(k4.x >= k_sel) << (4 * c4) | (unsigned)(k4.y >= k_sel) << (4 * c4 + 1) |
-               (unsigned)(k4.z >= k_sel) << (4 * c4 + 2) | (unsigned)(k4.w >= k_sel) << (4 * c4 + 3);
-        pw_ |= (unsigned)(k4.x >= k_lo) << (4 * c4) | (unsigned)(k4.y >= k_lo) << (4 * c4 + 1) |
-               (unsigned)(k4.z >= k_lo) << (4 * c4 + 2) | (unsigned)(k4.w >= k_lo) << (4 * c4 + 3);
-      }
-      // blocks past N are not candidates; 0, N - 2, N - 1 are forced
-      const int b0w = 32 * w;
-      const unsigned valid = (N - b0w >= 32) ? 0xffffffffu : ((1u << (N - b0w)) - 1u);
-      unsigned forced = 0u;
-      if (b0w == 0) forced |= 1u;
-      if (N - 2 >= b0w && N - 2 < b0w + 32) forced |= 1u << (N - 2 - b0w);
-      if (N - 1 >= b0w && N - 1 < b0w + 32) forced |= 1u << (N - 1 - b0w);
-      sw_ &= valid;
-      pw_ &= valid & ~sw_ & ~forced;
-      words[w] = sw_ | forced;
-      pwords[w] = pw_;
-    }
-    __syncthreads();
-    for (int w = tid; w < nw; w += kT) {
-      unsigned pw_ = pwords[w];
-      if (pw_) {
-        int p0 = atomicAdd(misc + 12, __popc(pw_));
-        while (pw_) {
-          const int bit = __ffs(pw_) - 1, b = 32 * w + bit;
-          lkey[p0] = keys[b];
-          lidx[p0] = b;
-          ++p0;
-          pw_ &= pw_ - 1u;
-        }
-      }
-    }
-    __syncthreads();
-    if (tid == 0 && write_out) tp = trace_phase(a, u, 1, 2, tp);
-    if (!take_all) {
-      // 4. rank T's candidates by (key desc, index asc); 16-byte broadcast reads, padded with sentinels
-      const int m = misc[12];
-      if (tid < 4) {
-        lkey[m + tid] = 0u;
-        lidx[m + tid] = 0x7fffffff;
-      }
-      __syncthreads();
-      const int m4 = (m + 3) & ~3;
-      for (int e = tid; e < m; e += kT) {
-        const uint32_t k0 = lkey[e];
-        const int i0 = lidx[e];
-        int rank = 0;
-        for (int f = 0; f < m4; f += 4) {
-          const uint4 kf = *reinterpret_cast<const uint4*>(lkey + f);
-          const int4 xf = *reinterpret_cast<const int4*>(lidx + f);
-          rank += kf.x > k0 || (kf.x == k0 && xf.x < i0);
-          rank += kf.y > k0 || (kf.y == k0 && xf.y < i0);
-          rank += kf.z > k0 || (kf.z == k0 && xf.z < i0);
-          rank += kf.w > k0 || (kf.w == k0 && xf.w < i0);
-        }
-        if (rank < need_T) atomicOr(&words[i0 >> 5], 1u << (i0 & 31));
-      }
-      __syncthreads();
-      if (tid == 0 && write_out) tp = trace_phase(a, u, 2, 9, tp);
-    }
-  } else if (!ranked) {
-    // every block, or only the forced ones (K = 3)
-    for (int w = tid; w < nw; w += kT) {
-      unsigned word = 0u;
-      for (int bit = 0; bit < 32; ++bit) {
-        const int b = 32 * w + bit;
-        if (b < N && (all_sel || b == 0 || b >= N - 2)) word |= 1u << bit;
-      }
-      words[w] = word;
-    }
-    __syncthreads();
-  }
-  if (ranked && !list_ok) {
-    // too many candidates share T: the full radix selection over the keys
-    // (it writes the list and leaves the bitmap and its prefix counts here)
-    __syncthreads();
-    select_unit(a, u, s, h, N, smraw, misc);
-  } else {
-    // 5. prefix counts of the bitmap (thread t: words [t * per, (t + 1) * per)); the ascending list
-    int total;
-    {
-      const int per = (nw + kT - 1) / kT;
-      int loc = 0;
-      for (int i = 0; i < per; ++i) {
-        const int w = tid * per + i;
-        if (w < nw) loc += __popc(words[w]);
-      }
-      int run = cta_exclusive_scan(loc, misc, &total, lane, warp);
-      for (int i = 0; i < per; ++i) {
-        const int w = tid * per + i;
-        if (w < nw) {
-          wbase[w] = run;
-          run += __popc(words[w]);
-        }
-      }
-    }
-    const int want = N < K ? N : K;
-    if (write_out && warp == 0 && lane == 0) {
-      if (total != want) set_error(a.status, kDevInternal, s, h, 50);
-      a.unit_nsel[u] = total;
-    }
-    __syncthreads();
-    if (write_out) {
-      for (int w = tid; w < nw; w += kT) {
-        unsigned word = words[w];
-        int pos = wbase[w];
-        while (word) {
-          const int bit = __ffs(word) - 1;
-          if (pos < K) selrow[pos] = 32 * w + bit;
-          ++pos;
-          word &= word - 1u;
-        }
-      }
-      for (int i = want + tid; i < K; i += kT) selrow[i] = -1;
-    }
-  }
-  // this CTA's picks
-  for (int w = tid; w < nw; w += kT) {
-    unsigned word = words[w];
-    int pos = wbase[w];
-    while (word) {
-      const int bit = __ffs(word) - 1;
-      const int grp = pos >> 3;
-      if (pos < K && grp % C == p) {
-        const int slot = (grp / C) * 8 + (pos & 7);
-        if (slot < npick) pick[slot] = 32 * w + bit;
-      }
-      ++pos;
-      word &= word - 1u;
-    }
-  }
-  __syncthreads();
-  if (tid == 0 && write_out) trace_phase(a, u, 3, 4, tp);
-}
-
-// Sum of NVAL values over the LPB lanes of a lane group (powers of two,
-// NVAL <= LPB).  Halving steps at offsets NVAL/2 .. 1 exchange half of the
-// values, then offsets NVAL .. LPB/2 add; lane j ends with the total of value
-// index j % NVAL (returned in `idx`).
 template <int NVAL, int LPB>
 __device__ __forceinline__ float transpose_reduce_lanes(float (&v)[NVAL], int j, int& idx) {
   idx = 0;
@@ -1439,9 +1023,31 @@ __device__ __forceinline__ float transpose_reduce_lanes(float (&v)[NVAL], int j,
   return v[0];
 }
 
-// ================================================================== 3. attend
-// Sum of P values across the warp: lane l ends with the total of value index l % P
-// (lanes l and l + P agree when P = 16).
+// ================================================================== 2. select + attend
+// One cluster of C CTAs per unit (C = a.splits <= 16) takes everything after
+// the scoring kernel.  CTA rank p owns the unit's scoring items
+// [p cpc, (p + 1) cpc) (cpc = ceil(items / C)) and their blocks:
+//   a. LSE_g and M_g = max_b (ln|b| + zbar) from the unit's item records;
+//      S_b = sum_g u_{g,b} e^(max a - LSE_g) = sum_g phat sigma2 of its
+//      blocks as order-preserving keys, a 12-bit histogram of the candidates'
+//      (1 .. N-3) top key bits; its items' compensation partials rescaled to
+//      M_g (the CTA's compensation share).
+//   b. the histograms summed into rank 0's (shared-memory atomics across the
+//      cluster); every CTA finds the threshold bin T where the count of
+//      larger candidates reaches K - 3; its candidates above T are selected,
+//      those in T are listed at rank 0 and ranked by (S_b desc, index asc)
+//      unless the whole bin is needed.  If more than kRankMax share T, rank 0
+//      runs the full radix selection over the keys instead.
+//   c. per-CTA counts give each CTA its offset in the ascending selection; the
+//      CTA writes its part of it, and takes the selected blocks at positions
+//      8 (it C + p) + warp from their owners' shared memory.
+//   d. exact attention over those blocks (one block per warp and round),
+//      minus each block's own compensation term; the CTA's partial joins its
+//      compensation share; the cluster merges the partials through
+//      distributed shared memory into out = acc / l.
+// By Jensen, sum_{j in b} e^{z_j} >= |b| e^{zbar_b}, so removing a selected
+// block's mean term never makes a denominator negative.  If every block is
+// selected the compensation is skipped (the step is dense attention).
 template <int P>
 __device__ __forceinline__ float transpose_reduce_warp(float (&v)[P], int lane) {
   int idx;
@@ -1457,6 +1063,8 @@ __device__ __forceinline__ uint32_t cluster_rank() {
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 __device__ __forceinline__ uint32_t peer_smem(const void* p, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
@@ -1472,78 +1080,545 @@ __device__ __forceinline__ float2 ld_peer_f2(uint32_t addr) {
   asm volatile("ld.shared::cluster.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr));
   return v;
 }
-
-constexpr int kAT = 256;            // threads of an attention CTA
-constexpr int kAW = kAT / 32;       // its warps: one selected block each per round
-// shared memory: per-warp partials (kAW x G x D, then m and l) | the CTA's partial (G x (D + 4)) |
-// counters; with the selection, that region is first the selection's | then the picked blocks
-__host__ __device__ inline int attend_smem(int D, int G) { return (kAW * G * D + 2 * kAW * G + G * (D + 4) + 4) * 4; }
-__host__ __device__ inline int attend_union_bytes(int D, int G, int key_stride, bool sel) {
-  int m = attend_smem(D, G);
-  if (sel && select_smem(key_stride) > m) m = select_smem(key_stride);
-  return (m + 15) & ~15;
+__device__ __forceinline__ uint4 ld_peer_u4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
 }
-__host__ __device__ inline int attend_npick(int K, int C, bool loop) { return loop ? ((K + 8 * C - 1) / (8 * C)) * 8 : 8; }
+__device__ __forceinline__ uint32_t ld_peer_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void st_peer_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_peer_add(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ uint32_t atom_peer_add(uint32_t addr, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
+  return old;
+}
 
-// A cluster of C CTAs per unit (C = a.splits <= 16); CTA rank p takes the
-// selected blocks 8 (it C + p) + warp, it = 0, 1, ...  Each warp keeps a
-// running (m, l, acc) per query head over its blocks: exact softmax terms of
-// the block's tokens, minus the block's own compensation term (the S items
-// summed it for every block).  The CTA combines its warps; the cluster's
-// CTAs then read each other's partials from distributed shared memory, and
-// rank p merges columns of them with the compensation sum into out = acc / l.
+constexpr int kAT = 256;            // threads of a post CTA
+constexpr int kAW = kAT / 32;       // its warps: one selected block each per round
+constexpr int kMiscInts = 64;
+
+// Shared memory of the post kernel, in 4-byte words:
+//   union: selection (histograms [4096] and [256] | keys of the CTA's blocks [cpc * 64] |
+//          bitmap [roundup4(cpc * 2) + 4] | rank-0 list keys, indices [kRankMax + 4] each),
+//          the full radix selection's region (rank 0, rare), or the attention
+//          (per-warp partials [kAW][G][D], m, l [kAW][G])
+//   then: compensation share [G][D + 4] | the C CTAs' selections [C][min(cpc * 64, K)] |
+//   picks [npick] | incoming partials [items per rank][C][8] | item factors [cpc][G] x 2 |
+//   LSE, M [G] x 2 | counts [16] | misc [kMiscInts]
+__host__ __device__ inline int post_bitmap_words(int cpc) { return ((cpc * 2 + 3) & ~3) + 4; }
+struct PostLayout {
+  int u_words, comp, own, own_n, pick, mstage, fch, fcp, lse, mref, cnts, misc, total_words;
+};
+__host__ __device__ inline int attend_smem_words(int D, int G) { return kAW * G * D + 2 * kAW * G + 4; }
+__host__ __device__ inline int post_items_per_rank(int D, int G, int C) { return (G * D / 4 + C - 1) / C; }
+__host__ __device__ inline PostLayout post_layout(int D, int G, int key_stride, int cpc, int K, int npick, bool sel, int C) {
+  PostLayout l;
+  const int selw = kHist12 + 256 + cpc * kChunk + post_bitmap_words(cpc) + 2 * (kRankMax + 4);
+  const int fallback = ((sel_region_words(key_stride) + 3) & ~3) + kMiscInts;
+  int u = attend_smem_words(D, G);
+  if (sel && selw > u) u = selw;
+  if (sel && fallback > u) u = fallback;
+  l.u_words = (u + 3) & ~3;
+  l.comp = l.u_words;
+  l.own = l.comp + G * (D + 4);
+  l.own_n = ((cpc * kChunk < K ? cpc * kChunk : K) + 3) & ~3;
+  l.pick = l.own + C * l.own_n;
+  l.mstage = l.pick + ((npick + 3) & ~3);
+  l.fch = l.mstage + post_items_per_rank(D, G, C) * C * 8;
+  l.fcp = l.fch + ((cpc * G + 3) & ~3);
+  l.lse = l.fcp + ((cpc * G + 3) & ~3);
+  l.mref = l.lse + ((G + 3) & ~3);
+  l.cnts = l.mref + ((G + 3) & ~3);
+  l.misc = l.cnts + 16;
+  l.total_words = l.misc + kMiscInts;
+  return l;
+}
+__host__ __device__ inline int post_npick(int K, int C, bool loop) { return loop ? ((K + 8 * C - 1) / (8 * C)) * 8 : 8; }
+
+// misc slots
+enum : int { kMT = 0, kMAbove, kMCntT, kMListN, kMTotal, kMNsel, kMBad, kMOff };
+
 template <int D, int G, int MODE, bool LOOP>
-__global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_attend(LayerArgs a) {
+__global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_post(LayerArgs a) {
   constexpr bool APPEND = (MODE & kFAppend) != 0;
+  constexpr bool SEL = (MODE & kFSelect) != 0;
+  constexpr bool COMP = (MODE & kFComp) != 0;
   constexpr bool ATT = (MODE & kFAttend) != 0;
-  constexpr bool EXTERNAL = (MODE & kFSelect) == 0;  // selection given by the caller
   constexpr int V = D / 32;
   constexpr int TG = G >= 8 ? 2 : ((32 / G) > 16 ? 16 : (32 / G));  // tokens per reduction group
   constexpr int P = TG * G;                                          // 16 or 32 values per group
   constexpr int W = V / 2;                                           // 32-bit words per token slice
   constexpr int NG = kBlock / TG;
-  extern __shared__ __align__(16) float asm_[];
-  float* red_a = asm_;                    // [kAW][G][D]
-  float* red_m = red_a + kAW * G * D;     // [kAW][G]
-  float* red_l = red_m + kAW * G;         // [kAW][G]
-  float* cpart = red_l + kAW * G;         // [G][D + 4]: acc, then m at [D], l at [D + 1]
-  int* shi = reinterpret_cast<int*>(cpart + G * (D + 4));  // count, bad
+  extern __shared__ __align__(16) float psm[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const unsigned long long t_start = a.trace ? global_ns() : 0ull;
-  const int C = ATT ? a.splits : 1;
-  const int npick = attend_npick(a.K, C, LOOP);
-  int* pick = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(asm_) +
-                                     attend_union_bytes(D, G, a.key_stride, !EXTERNAL));
+  const int C = a.splits;
   const int u = blockIdx.x / C;
   const int p = (int)cluster_rank();
   const int s = u / a.Hkv, h = u % a.Hkv;
   const int K = a.K;
+  const int npick = post_npick(K, C, LOOP);
+  const PostLayout lay = post_layout(D, G, a.key_stride, a.post_cpc, K, npick, SEL, C);
+  // selection phase views
+  uint32_t* hist = reinterpret_cast<uint32_t*>(psm);  // [4096] top 12 key bits, then [256] top 8 (the exponent)
+  uint32_t* chist = hist + kHist12;
+  uint32_t* keys = chist + 256;
+  unsigned* words = keys + a.post_cpc * kChunk;
+  uint32_t* lkey = words + post_bitmap_words(a.post_cpc);
+  int* lidx = reinterpret_cast<int*>(lkey + kRankMax + 4);
+  // attention phase views
+  float* red_a = psm;                     // [kAW][G][D]
+  float* red_m = red_a + kAW * G * D;     // [kAW][G]
+  float* red_l = red_m + kAW * G;         // [kAW][G]
+  // persistent
+  float* ccomp = psm + lay.comp;          // [G][D + 4]: the CTA's compensation share, weight sum at [D]
+  int* selall = reinterpret_cast<int*>(psm + lay.own);  // [C][own_n]: CTA q's selected blocks
+  int* own = selall + p * lay.own_n;
+  float* mstage = psm + lay.mstage;                      // [items per rank][C][8]: acc (4), m, l
+  int* pick = reinterpret_cast<int*>(psm + lay.pick);
+  float* fch = psm + lay.fch;
+  float* fcp = psm + lay.fcp;
+  float* lse = psm + lay.lse;
+  float* mref = psm + lay.mref;
+  int* cnts = reinterpret_cast<int*>(psm + lay.cnts);
+  int* misc = reinterpret_cast<int*>(psm + lay.misc);
+
   float qr[G][V];
-  const float* qg = a.q + ((int64_t)s * a.Hkv * G + (int64_t)h * G) * D;
+  if (ATT) {
+    const float* qg = a.q + ((int64_t)s * a.Hkv * G + (int64_t)h * G) * D;
 #pragma unroll
-  for (int g = 0; g < G; ++g)
+    for (int g = 0; g < G; ++g)
 #pragma unroll
-    for (int i = 0; i < V; ++i) qr[g][i] = qg[g * D + lane * V + i] * InvSqrt<D>::v;
-  if (tid == 0) {
-    shi[0] = 0;
-    shi[1] = 0;
+      for (int i = 0; i < V; ++i) qr[g][i] = qg[g * D + lane * V + i] * InvSqrt<D>::v;
+  }
+  if (SEL) {
+    for (int i = tid; i < (kHist12 + 256) / 4; i += kAT) reinterpret_cast<uint4*>(hist)[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (tid < kMiscInts) misc[tid] = 0;
+    __syncthreads();
+    cluster_arrive();  // rank 0's histogram and list counter are zero before any peer adds to them
+  } else if (tid < kMiscInts) {
+    misc[tid] = 0;
   }
   pdl_wait();
   const unsigned long long t_wait = a.trace ? global_ns() : 0ull;
+  // phase marks of rank 0 (tracing aid): mark k = time since the previous mark
+  unsigned long long tp = t_wait;
+  auto mark = [&](int k) {
+    if (a.trace && p == 0 && tid == 0) tp = trace_phase(a, u, k, k, tp);
+  };
   const int L = a.lnew[s], N = ceil_blocks(L);
-  const int* selrow = a.sel + (int64_t)u * K;
-  __syncthreads();
-  int nsel;
-  if (!EXTERNAL) {
-    // the selection, by every CTA of the unit (rank 0 writes the list); this CTA's blocks into pick
-    select_core(a, u, L, reinterpret_cast<unsigned char*>(asm_), p == 0, p, C, pick, npick);
-    nsel = N < K ? N : K;
-    if (!ATT) {
-      for (int i = tid; i < kHist12 / 4; i += kAT)
-        reinterpret_cast<uint4*>(a.hist12 + (int64_t)u * kHist12)[i] = make_uint4(0u, 0u, 0u, 0u);
-      return;
+  const int nch = (N + kChunk - 1) / kChunk;
+  const int cpc = (nch + C - 1) / C;
+  const int c_lo = min(nch, p * cpc), c_hi = min(nch, c_lo + cpc);
+  const int b_lo = c_lo * kChunk, b_hi = min(N, c_hi * kChunk);
+  const int nown = b_hi - b_lo;
+  const int rec0 = chunk_record(a, s, h, 0);
+  const bool all_sel = N <= K;
+
+  // ---- a. LSE_g, M_g and the factors of this CTA's items (one pass over the
+  // records when they fit eight per lane; the items' own records stay in registers)
+  if ((SEL || COMP) && warp < G) {
+    const int g = warp;
+    float M = -INFINITY, S = 0.f, MC = -INFINITY;
+    float4 rv[8];
+    const int ncap = a.nchunk[s];  // the unit's records (loads issued before the item count is known)
+    for (int c0 = 0; c0 < ncap; c0 += 256) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int c = c0 + lane + 32 * k;
+        rv[k] = c < ncap ? __ldcg(reinterpret_cast<const float4*>(a.chunk_rec + ((int64_t)(rec0 + c) * G + g) * 4))
+                         : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (c0 + lane + 32 * k >= nch) rv[k] = make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+      float mloc = -INFINITY;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        MC = fmaxf(MC, rv[k].z);
+        mloc = fmaxf(mloc, rv[k].x);
+      }
+      if (SEL && mloc != -INFINITY) {
+        float sl = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (rv[k].x != -INFINITY) sl += rv[k].y * __expf(rv[k].x - mloc);
+        const float mn = fmaxf(M, mloc);
+        S = (M == -INFINITY ? 0.f : S * __expf(M - mn)) + sl * __expf(mloc - mn);
+        M = mn;
+      }
     }
+    MC = warp_max(MC);
+    float lg = 0.f;
+    if (SEL) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float M2 = __shfl_xor_sync(0xffffffffu, M, o), S2 = __shfl_xor_sync(0xffffffffu, S, o);
+        const float Mn = fmaxf(M, M2);
+        if (Mn != -INFINITY) {
+          S = (M == -INFINITY ? 0.f : S * __expf(M - Mn)) + (M2 == -INFINITY ? 0.f : S2 * __expf(M2 - Mn));
+          M = Mn;
+        }
+      }
+      lg = M + logf(S);
+    }
+    if (nch <= 256) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int c = lane + 32 * k;
+        if (c >= c_lo && c < c_hi) {
+          if (SEL) fch[(c - c_lo) * G + g] = expf(rv[k].x - lg);
+          if (COMP) fcp[(c - c_lo) * G + g] = expf(rv[k].z - MC);
+        }
+      }
+    } else {
+      for (int j = lane; j < c_hi - c_lo; j += 32) {
+        const float4 r4 = __ldcg(reinterpret_cast<const float4*>(a.chunk_rec + ((int64_t)(rec0 + c_lo + j) * G + g) * 4));
+        if (SEL) fch[j * G + g] = expf(r4.x - lg);
+        if (COMP) fcp[j * G + g] = expf(r4.z - MC);
+      }
+    }
+    if (lane == 0) {
+      lse[g] = lg;
+      mref[g] = MC;
+    }
+  }
+  __syncthreads();
+  mark(1);
+  // ---- a. keys of this CTA's blocks and their histogram; the compensation share
+  if (SEL && (!all_sel || a.scores)) {
+    for (int i0 = tid; i0 < nown; i0 += 4 * kAT) {
+      float uv[4][G];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = i0 + k * kAT, b = b_lo + i;
+        const int rec = rec0 + b / kChunk;
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+          uv[k][g] = i < nown ? __ldcg(a.chunk_u + ((int64_t)rec * G + g) * kChunk + (b % kChunk)) : 0.f;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int i = i0 + k * kAT, b = b_lo + i;
+        if (i >= nown) break;
+        const int cl = b / kChunk - c_lo;
+        float S = 0.f;
+#pragma unroll
+        for (int g = 0; g < G; ++g) S = fmaf(uv[k][g], fch[cl * G + g], S);
+        S = fmaxf(S, 0.f);
+        const uint32_t key = __float_as_uint(S);
+        keys[i] = key;
+        if (a.scores) a.scores[(int64_t)u * a.score_stride + b] = S;
+        if (!all_sel && b >= 1 && b <= N - 3) {
+          atomicAdd(&hist[key >> kDigitShift], 1u);
+          atomicAdd(&chist[key >> 23], 1u);
+        }
+      }
+    }
+  }
+  if (COMP) {
+    for (int i = tid; i < G * (D + 4) / 4; i += kAT) {
+      const int g = (4 * i) / (D + 4), col = (4 * i) % (D + 4);
+      float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int j0 = 0; j0 < c_hi - c_lo; j0 += 16) {
+        float4 v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          v[j] = j0 + j < c_hi - c_lo
+                     ? __ldcg(reinterpret_cast<const float4*>(a.comp_part + ((int64_t)(rec0 + c_lo + j0 + j) * G + g) * (D + 4) + col))
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float f = j0 + j < c_hi - c_lo ? fcp[(j0 + j) * G + g] : 0.f;
+          t.x = fmaf(f, v[j].x, t.x);
+          t.y = fmaf(f, v[j].y, t.y);
+          t.z = fmaf(f, v[j].z, t.z);
+          t.w = fmaf(f, v[j].w, t.w);
+        }
+      }
+      *reinterpret_cast<float4*>(ccomp + g * (D + 4) + col) = t;
+    }
+  }
+  __syncthreads();
+  mark(2);
+
+  // ---- b, c. the selection
+  int nsel = 0;
+  unsigned long long t_sel = 0ull;
+  if (SEL) {
+    const int nwo = (nown + 31) / 32;
+    cluster_wait();  // rank 0's histogram is zero
+    if (!all_sel) {
+      // the cluster's histograms: the exponent bins at rank 0, the 16 fine bins
+      // of exponent e at rank e C / 256.  A CTA adds its counts of bins held
+      // elsewhere (its own are in place; peers add to them meanwhile, so it does
+      // not read those here): thread t < 256 takes exponent t
+      const int own_r = (tid * C) >> 8;
+      if (own_r != p) {
+        const uint4* hv = reinterpret_cast<const uint4*>(hist) + 4 * tid;
+        const uint32_t hr = peer_smem(hist, (uint32_t)own_r);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 v = hv[k];
+          const uint32_t ad = hr + 64u * tid + 16u * k;
+          if (v.x) red_peer_add(ad, v.x);
+          if (v.y) red_peer_add(ad + 4u, v.y);
+          if (v.z) red_peer_add(ad + 8u, v.z);
+          if (v.w) red_peer_add(ad + 12u, v.w);
+        }
+      }
+      if (p != 0) {
+        const uint32_t cs = chist[tid];
+        if (cs) red_peer_add(peer_smem(chist + tid, 0), cs);
+      }
+    }
+    cluster_sync_all();  // rank 0 holds the unit's histogram
+    mark(3);
+    const int need0 = K - 3;
+    bool take_all = true;
+    uint32_t T = 0u;
+    int need = 0;
+    if (!all_sel && need0 > 0) {
+      // the threshold exponent from the top of rank 0's exponent histogram (thread t: exponent 255 - t),
+      // then the fine bin inside it from its 16 fine bins
+      const int ex = 255 - tid;
+      const int loc = (int)ld_peer_u32(peer_smem(chist + ex, 0));
+      int total;
+      const int before = cta_exclusive_scan(loc, misc + kMOff, &total, lane, warp);
+      if (before < need0 && need0 <= before + loc) {
+        uint32_t c16[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 v = ld_peer_u4(peer_smem(hist + 16 * ex + 4 * k, (uint32_t)((ex * C) >> 8)));
+          c16[4 * k] = v.x;
+          c16[4 * k + 1] = v.y;
+          c16[4 * k + 2] = v.z;
+          c16[4 * k + 3] = v.w;
+        }
+        int run = before;
+        for (int k = 15; k >= 0; --k) {
+          if (run < need0 && need0 <= run + (int)c16[k]) {
+            misc[kMT] = 16 * ex + k;
+            misc[kMAbove] = run;
+            misc[kMCntT] = (int)c16[k];
+          }
+          run += (int)c16[k];
+        }
+      }
+      __syncthreads();
+      mark(4);
+      T = (uint32_t)misc[kMT];
+      need = need0 - misc[kMAbove];
+      take_all = misc[kMCntT] == need;
+    }
+    // classify this CTA's blocks (bitmap of the selected ones); the threshold
+    // bin's candidates, when ranking is needed, into this CTA's list
+    for (int w = tid; w < nwo; w += kAT) words[w] = 0u;
+    __syncthreads();
+    for (int i = tid; i < nown; i += kAT) {
+      const int b = b_lo + i;
+      bool sel = all_sel || b == 0 || b == N - 2 || b == N - 1;
+      if (!sel && need0 > 0) {
+        const uint32_t key = keys[i];
+        const uint32_t bin = key >> kDigitShift;
+        if (bin > T || (bin == T && take_all)) {
+          sel = true;
+        } else if (bin == T) {
+          const int slot = atomicAdd(misc + kMListN, 1);
+          if (slot < kRankMax) {
+            lkey[slot] = key;
+            lidx[slot] = b;
+          }
+        }
+      }
+      if (sel) atomicOr(&words[i >> 5], 1u << (i & 31));
+    }
+    if (!take_all) {
+      __syncthreads();
+      mark(5);
+      cluster_sync_all();  // every CTA's list is complete
+      mark(6);
+      // the lists' sizes, then all of them gathered here behind this CTA's own
+      int* lsz = misc + 16;  // the C list sizes
+      if (tid < C) lsz[tid] = (int)ld_peer_u32(peer_smem(misc + kMListN, (uint32_t)tid));
+      __syncthreads();
+      int m = 0, mine0 = 0;
+      for (int q = 0; q < C; ++q) {
+        if (q < p) mine0 += lsz[q];
+        m += lsz[q];
+      }
+      if (a.trace && p == 0 && tid == 0)
+        trace_item(a, slot_phase(a) + u * 32 + 16, 6, u, 0, (unsigned long long)m, (unsigned long long)need,
+                   (unsigned long long)misc[kMCntT], (unsigned long long)misc[kMAbove]);
+      if (m <= kRankMax) {
+        // gather: peer q's entries go to [off_q, off_q + cnt_q); this CTA's own move from [0, cnt_p)
+        // (into the histogram's space: every CTA has read the histograms by now)
+        uint32_t* gkey = hist;
+        int* gidx = reinterpret_cast<int*>(gkey + kRankMax + 4);
+        static_assert(kRankMax <= 2 * kAT, "two gather rounds");
+        uint32_t gk[2], gi[2];
+#pragma unroll
+        for (int r2 = 0; r2 < 2; ++r2) {
+          const int e = tid + r2 * kAT;
+          gk[r2] = 0u;
+          gi[r2] = 0u;
+          if (e < m) {
+            int q = 0, base = 0;
+            while (q + 1 < C && base + lsz[q] <= e) base += lsz[q++];
+            gk[r2] = ld_peer_u32(peer_smem(lkey + (e - base), (uint32_t)q));
+            gi[r2] = ld_peer_u32(peer_smem(lidx + (e - base), (uint32_t)q));
+          }
+        }
+#pragma unroll
+        for (int r2 = 0; r2 < 2; ++r2) {
+          const int e = tid + r2 * kAT;
+          if (e < m) {
+            gkey[e] = gk[r2];
+            gidx[e] = (int)gi[r2];
+          }
+        }
+        if (tid < 4) {
+          gkey[m + tid] = 0u;
+          gidx[m + tid] = 0x7fffffff;
+        }
+        __syncthreads();
+        const int m4 = (m + 3) & ~3;
+        const int cp = lsz[p];
+        for (int e = tid; e < cp; e += kAT) {
+          const uint32_t k0 = gkey[mine0 + e];
+          const int i0 = gidx[mine0 + e];
+          int rank = 0;
+          for (int f = 0; f < m4; f += 4) {
+            const uint4 kf = *reinterpret_cast<const uint4*>(gkey + f);
+            const int4 xf = *reinterpret_cast<const int4*>(gidx + f);
+            rank += (kf.x > k0 || (kf.x == k0 && xf.x < i0));
+            rank += (kf.y > k0 || (kf.y == k0 && xf.y < i0));
+            rank += (kf.z > k0 || (kf.z == k0 && xf.z < i0));
+            rank += (kf.w > k0 || (kf.w == k0 && xf.w < i0));
+          }
+          // the sentinels (key 0, largest index) never rank above a listed key
+          if (rank < need) atomicOr(&words[(i0 - b_lo) >> 5], 1u << ((i0 - b_lo) & 31));
+        }
+        __syncthreads();
+      } else {
+        // more keys share the threshold bin than the lists hold: rank 0 runs the
+        // full radix selection over the unit's keys (written to global memory here)
+        for (int i = tid; i < nown; i += kAT) a.skeys[(int64_t)u * a.key_stride + b_lo + i] = keys[i];
+        for (int i = tid; i < kHist12; i += kAT)
+          if ((((i >> 4) * C) >> 8) == p) a.hist12[(int64_t)u * kHist12 + i] = hist[i];
+        cluster_sync_all();
+        if (p == 0) select_unit(a, u, s, h, N, reinterpret_cast<unsigned char*>(psm), misc + kMiscInts - 8);
+        cluster_sync_all();
+        for (int w = tid; w < nwo; w += kAT) words[w] = 0u;
+        __syncthreads();
+        for (int i = tid; i < K; i += kAT) {
+          const int b = __ldcg(a.sel + (int64_t)u * K + i);
+          if (b >= b_lo && b < b_hi) atomicOr(&words[(b - b_lo) >> 5], 1u << ((b - b_lo) & 31));
+        }
+        __syncthreads();
+      }
+    }
+    __syncthreads();
+    // ascending list of this CTA's selected blocks and its count, into every CTA of the cluster
+    if (warp == 0) {
+      int loc = 0;
+      const int per = (nwo + 31) / 32;
+      for (int k = 0; k < per; ++k) {
+        const int w = per * lane + k;
+        if (w < nwo) loc += __popc(words[w]);
+      }
+      int incl = loc;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int run = incl - loc;
+      for (int k = 0; k < per; ++k) {
+        const int w = per * lane + k;
+        if (w < nwo) {
+          unsigned word = words[w];
+          while (word) {
+            const int bit = __ffs(word) - 1;
+            if (run < lay.own_n) {
+              const int b = b_lo + 32 * w + bit;
+              own[run] = b;
+              for (int q = 0; q < C; ++q)
+                if (q != p) st_peer_u32(peer_smem(own + run, (uint32_t)q), (uint32_t)b);
+            }
+            ++run;
+            word &= word - 1u;
+          }
+        }
+      }
+      const int total_own = __shfl_sync(0xffffffffu, incl, 31);
+      if (lane == 0) misc[kMTotal] = total_own;
+      if (lane < C) st_peer_u32(peer_smem(cnts + p, (uint32_t)lane), (uint32_t)total_own);
+    }
+    __syncthreads();
+    if (ATT) {
+      // the K/V rows (and mean values) of this CTA's selected blocks on their way to L2
+      // while the offsets are exchanged; another CTA of the cluster may attend them
+      for (int e = tid; e < misc[kMTotal] && e < lay.own_n; e += kAT) {
+        const int64_t row = row_of(a, s, h, own[e]);
+        prefetch_l2(a.k + row * kBlock * D, kBlock * D * 2);
+        prefetch_l2(a.v + row * kBlock * D, kBlock * D * 2);
+        if (COMP) prefetch_l2(a.vbar + row * D, D * 4);
+      }
+    }
+    mark(7);
+    cluster_sync_all();  // every CTA holds every count and every list
+    mark(8);
+    int off = 0, tot = 0;
+    for (int q = 0; q < C; ++q) {
+      off += q < p ? cnts[q] : 0;
+      tot += cnts[q];
+    }
+    nsel = tot;
+    int* selrow = a.sel + (int64_t)u * K;
+    const int mine = misc[kMTotal];
+    for (int i = tid; i < mine; i += kAT)
+      if (off + i < K) selrow[off + i] = own[i];
+    if (p == 0) {
+      for (int i = tot + tid; i < K; i += kAT) selrow[i] = -1;
+      if (tid == 0) {
+        a.unit_nsel[u] = tot;
+        if (tot != (N < K ? N : K)) set_error(a.status, kDevInternal, s, h, 50);
+      }
+    }
+    if (ATT) {
+      // this CTA's blocks: positions 8 (it C + p) + w, from their owners' lists
+      for (int e = tid; e < npick; e += kAT) {
+        const int q = 8 * ((e / 8) * C + p) + (e % 8);
+        int b = -1;
+        if (q < tot && q < K) {
+          int r = 0, base = 0;
+          while (r + 1 < C && base + cnts[r] <= q) base += cnts[r++];
+          b = selall[r * lay.own_n + (q - base)];
+        }
+        pick[e] = b;
+      }
+    }
+    t_sel = a.trace ? global_ns() : 0ull;
+    mark(9);
+    if (!ATT) return;  // no peer reads this CTA's shared memory any more
+    __syncthreads();
   } else {
+    // the caller's selection: validated (ascending, inside [0, N)), counted
+    const int* selrow = a.sel + (int64_t)u * K;
     int cnt = 0, bad = 0;
     for (int i = tid; i < K; i += kAT) {
       const int e = __ldcg(selrow + i);
@@ -1555,14 +1630,28 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_attend(LayerArgs a) {
     cnt = __reduce_add_sync(0xffffffffu, cnt);
     bad = __reduce_or_sync(0xffffffffu, bad);
     if (lane == 0) {
-      if (cnt) atomicAdd(shi, cnt);
-      if (bad) shi[1] = 1;
+      if (cnt) atomicAdd(misc + kMNsel, cnt);
+      if (bad) misc[kMBad] = 1;
     }
     __syncthreads();
-    nsel = shi[0];
-    if (shi[1] && p == 0 && tid == 0) set_error(a.status, kDevBadSelection, s, h, 61);
+    nsel = misc[kMNsel];
+    if (misc[kMBad] && p == 0 && tid == 0) set_error(a.status, kDevBadSelection, s, h, 61);
+    for (int e = tid; e < npick; e += kAT) {
+      const int q = 8 * ((e / 8) * C + p) + (e % 8);
+      int b = -1;
+      if (q < K) {
+        const int v = __ldcg(selrow + q);
+        const int prev = q > 0 ? __ldcg(selrow + q - 1) : -1;
+        if (v >= 0 && v < N && (q == 0 || (prev >= 0 && prev < v))) b = v;
+      }
+      pick[e] = b;
+    }
+    __syncthreads();
+    t_sel = a.trace ? global_ns() : 0ull;
   }
-  const bool comp = nsel < N;
+
+  // ---- d. attention over this CTA's blocks
+  const bool comp = COMP && nsel < N;
   float m[G], l[G], acc[G][V];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
@@ -1573,17 +1662,9 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_attend(LayerArgs a) {
   }
   const int idx = lane & (P - 1);
   const int jj = idx / G, gl = idx % G;
-  const int rounds = LOOP ? (K + kAW * C - 1) / (kAW * C) : 1;
+  const int rounds = LOOP ? npick / 8 : 1;
   for (int it = 0; it < rounds; ++it) {
-    const int my_i = kAW * (it * C + p) + warp;
-    int b = -1;
-    if (!EXTERNAL) {
-      b = pick[8 * it + warp];
-    } else if (my_i < K) {
-      const int e = __ldcg(selrow + my_i);
-      const int prev = my_i > 0 ? __ldcg(selrow + my_i - 1) : -1;
-      if (e >= 0 && e < N && (my_i == 0 || (prev >= 0 && prev < e))) b = e;
-    }
+    const int b = pick[8 * it + warp];
     if (b < 0) continue;  // warp-uniform
     const int n = (b == N - 1) ? L - kBlock * b : kBlock;
     const int64_t row = row_of(a, s, h, b);
@@ -1608,8 +1689,8 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_attend(LayerArgs a) {
     const int rec = chunk_record(a, s, h, b / kChunk);
     float vb[V];
 #pragma unroll
-    for (int i = 0; i < V; ++i) vb[i] = __ldcg(a.vbar + row * D + lane * V + i);
-    const float zb_lane = lane < G ? __ldcg(a.chunk_z + ((int64_t)rec * G + lane) * kChunk + (b % kChunk)) : 0.f;
+    for (int i = 0; i < V; ++i) vb[i] = comp ? __ldcg(a.vbar + row * D + lane * V + i) : 0.f;
+    const float zb_lane = (comp && lane < G) ? __ldcg(a.chunk_z + ((int64_t)rec * G + lane) * kChunk + (b % kChunk)) : 0.f;
     float zl[NG];
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi) {
@@ -1644,7 +1725,7 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_attend(LayerArgs a) {
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const float mn = fmaxf(m[g], __shfl_sync(0xffffffffu, zmax, g));
-      const float f = (m[g] == -INFINITY) ? 0.f : expf(m[g] - mn);
+      const float f = (m[g] == -INFINITY) ? 0.f : __expf(m[g] - mn);
       m[g] = mn;
       l[g] *= f;
 #pragma unroll
@@ -1655,7 +1736,7 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_attend(LayerArgs a) {
     float psum = 0.f;
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi) {
-      pl[gi] = (gi * TG + jj < n) ? expf(zl[gi] - mlane) : 0.f;
+      pl[gi] = (gi * TG + jj < n) ? __expf(zl[gi] - mlane) : 0.f;
       psum += pl[gi];
     }
 #pragma unroll
@@ -1682,14 +1763,14 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_attend(LayerArgs a) {
       }
     }
     if (comp) {
-      // remove this block's own compensation term, which the S items summed for every block
+      // remove this block's own compensation term, which the compensation shares hold for every block
       const float lnn = ln_n(n);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         const float e = lnn + __shfl_sync(0xffffffffu, zb_lane, g);
         const float mn = fmaxf(m[g], e);
-        const float fo = (m[g] == -INFINITY) ? 0.f : expf(m[g] - mn);
-        const float fn = expf(e - mn);
+        const float fo = (m[g] == -INFINITY) ? 0.f : __expf(m[g] - mn);
+        const float fn = __expf(e - mn);
         m[g] = mn;
         l[g] = l[g] * fo - fn;
 #pragma unroll
@@ -1697,8 +1778,9 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_attend(LayerArgs a) {
       }
     }
   }
-  const unsigned long long t_comp = a.trace ? global_ns() : 0ull;
-  // the CTA's partial: its warps combined
+  const unsigned long long t_att = a.trace ? global_ns() : 0ull;
+  mark(10);
+  // the CTA's partial: its warps and its compensation share combined
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     if (lane == 0) {
@@ -1709,9 +1791,13 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_attend(LayerArgs a) {
     for (int i = 0; i < V; ++i) red_a[(warp * G + g) * D + lane * V + i] = acc[g][i];
   }
   __syncthreads();
-  for (int i4 = tid; i4 < G * D / 4; i4 += kAT) {
+  // ... pushed, per float4 column item, to the rank that merges that item:
+  // rank r merges items [r ipr, (r + 1) ipr)
+  const int items = G * D / 4;
+  const int ipr = post_items_per_rank(D, G, C);
+  for (int i4 = tid; i4 < items; i4 += kAT) {
     const int g = (4 * i4) / D, col = (4 * i4) % D;
-    float M = -INFINITY;
+    float M = comp ? mref[g] : -INFINITY;
 #pragma unroll
     for (int w = 0; w < kAW; ++w) M = fmaxf(M, red_m[w * G + g]);
     float ls = 0.f;
@@ -1720,7 +1806,7 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_attend(LayerArgs a) {
 #pragma unroll
       for (int w = 0; w < kAW; ++w) {
         const float mw = red_m[w * G + g];
-        const float f = (mw == -INFINITY) ? 0.f : expf(mw - M);
+        const float f = (mw == -INFINITY) ? 0.f : __expf(mw - M);
         ls += red_l[w * G + g] * f;
         const float4 x = *reinterpret_cast<const float4*>(red_a + (w * G + g) * D + col);
         as.x += x.x * f;
@@ -1728,12 +1814,21 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_attend(LayerArgs a) {
         as.z += x.z * f;
         as.w += x.w * f;
       }
+      if (comp) {
+        const float f = __expf(mref[g] - M);
+        const float4 x = *reinterpret_cast<const float4*>(ccomp + g * (D + 4) + col);
+        ls += ccomp[g * (D + 4) + D] * f;
+        as.x += x.x * f;
+        as.y += x.y * f;
+        as.z += x.z * f;
+        as.w += x.w * f;
+      }
     }
-    if (col == 0) {
-      cpart[g * (D + 4) + D] = M;
-      cpart[g * (D + 4) + D + 1] = ls;
-    }
-    *reinterpret_cast<float4*>(cpart + g * (D + 4) + col) = as;
+    const int r = i4 / ipr, il = i4 - r * ipr;
+    const uint32_t dst = peer_smem(mstage + (il * C + p) * 8, (uint32_t)r);
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(dst), "f"(as.x), "f"(as.y), "f"(as.z), "f"(as.w)
+                 : "memory");
+    asm volatile("st.shared::cluster.v2.f32 [%0], {%1,%2};" ::"r"(dst + 16u), "f"(M), "f"(ls) : "memory");
   }
   if (APPEND && blockIdx.x == 0 && tid == 0)
     for (int ss = 0; ss < a.B; ++ss) {
@@ -1743,72 +1838,34 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_attend(LayerArgs a) {
       else
         set_error(a.status, kDevCapacity, ss, -1, 42);
     }
-  // this rank's columns (float4 items) of the output, and their compensation sums (in flight during the barrier)
-  const int items = G * D / 4;
-  const int ipr = (items + C - 1) / C;
+  mark(11);
+  cluster_sync_all();  // every partial of this rank's items is here; no CTA touches a peer's memory after this
+  mark(12);
   const int i_lo = p * ipr, i_hi = min(items, i_lo + ipr);
-  const float* ua = a.unit_acc + (int64_t)u * G * (D + 4);
-  float mc = -INFINITY, cl = 0.f;
-  float4 ca = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (comp && tid < i_hi - i_lo) {
+  if (tid < i_hi - i_lo) {
     const int i4 = i_lo + tid, g = (4 * i4) / D, col = (4 * i4) % D;
-    mc = __ldcg(a.unit_ref + u * G + g);
-    cl = __ldcg(ua + g * (D + 4) + D);
-    ca = __ldcg(reinterpret_cast<const float4*>(ua + g * (D + 4) + col));
-  }
-  const unsigned long long t_rec = a.trace ? global_ns() : 0ull;
-  cluster_sync_all();  // every CTA's partial is in its shared memory (and every CTA is past the selection)
-  if (!EXTERNAL && p == 0)
-    for (int i = tid; i < kHist12 / 4; i += kAT)
-      reinterpret_cast<uint4*>(a.hist12 + (int64_t)u * kHist12)[i] = make_uint4(0u, 0u, 0u, 0u);
-  {
-    // one (column, peer) pair per thread: the peers' partials staged here, then merged per column
-    float* stage = red_a;  // [ipr][C][8]: acc (4), m, l
-    const int npairs = (i_hi - i_lo) * C;
-    for (int pr = tid; pr < npairs; pr += kAT) {
-      const int il = pr / C, q = pr % C;
-      const int i4 = i_lo + il, g = (4 * i4) / D, col = (4 * i4) % D;
-      const float2 ml = ld_peer_f2(peer_smem(cpart + g * (D + 4) + D, (uint32_t)q));
-      const float4 av = ld_peer_f4(peer_smem(cpart + g * (D + 4) + col, (uint32_t)q));
-      *reinterpret_cast<float4*>(stage + pr * 8) = av;
-      *reinterpret_cast<float2*>(stage + pr * 8 + 4) = ml;
-    }
-    __syncthreads();
-    if (tid < i_hi - i_lo) {
-      const int i4 = i_lo + tid, g = (4 * i4) / D, col = (4 * i4) % D;
-      float M = -INFINITY, ls = 0.f;
-      float4 as = make_float4(0.f, 0.f, 0.f, 0.f);
+    const float* e0 = mstage + tid * C * 8;
+    float M = -INFINITY;
+    for (int q = 0; q < C; ++q) M = fmaxf(M, e0[q * 8 + 4]);
+    float ls = 0.f;
+    float4 as = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY)
       for (int q = 0; q < C; ++q) {
-        const float* e = stage + (tid * C + q) * 8;
+        const float* e = e0 + q * 8;
         const float mq = e[4];
-        if (mq == -INFINITY) continue;
-        const float mn = fmaxf(M, mq);
-        const float fo = (M == -INFINITY) ? 0.f : expf(M - mn);
-        const float fn = expf(mq - mn);
-        ls = ls * fo + e[5] * fn;
-        as.x = as.x * fo + e[0] * fn;
-        as.y = as.y * fo + e[1] * fn;
-        as.z = as.z * fo + e[2] * fn;
-        as.w = as.w * fo + e[3] * fn;
-        M = mn;
+        const float f = mq == -INFINITY ? 0.f : __expf(mq - M);
+        ls = fmaf(e[5], f, ls);
+        as.x = fmaf(e[0], f, as.x);
+        as.y = fmaf(e[1], f, as.y);
+        as.z = fmaf(e[2], f, as.z);
+        as.w = fmaf(e[3], f, as.w);
       }
-      if (comp && mc != -INFINITY) {
-        const float mn = fmaxf(M, mc);
-        const float fo = (M == -INFINITY) ? 0.f : expf(M - mn);
-        const float fn = expf(mc - mn);
-        ls = ls * fo + cl * fn;
-        as.x = as.x * fo + ca.x * fn;
-        as.y = as.y * fo + ca.y * fn;
-        as.z = as.z * fo + ca.z * fn;
-        as.w = as.w * fo + ca.w * fn;
-      }
-      const float inv = ls > 0.f ? 1.f / ls : 0.f;
-      float* out = a.out + ((int64_t)s * a.Hkv * G + (int64_t)h * G) * D;
-      *reinterpret_cast<float4*>(out + g * D + col) = make_float4(as.x * inv, as.y * inv, as.z * inv, as.w * inv);
-    }
+    const float inv = ls > 0.f ? 1.f / ls : 0.f;
+    float* out = a.out + ((int64_t)s * a.Hkv * G + (int64_t)h * G) * D;
+    *reinterpret_cast<float4*>(out + g * D + col) = make_float4(as.x * inv, as.y * inv, as.z * inv, as.w * inv);
   }
-  cluster_sync_all();  // the peers' reads are done before any CTA of the cluster exits
-  if (tid == 0) trace_item(a, slot_attend(a) + blockIdx.x, p == 0 ? 4 : 1, u, p, t_start, t_wait, t_comp, t_rec, 0);
+  mark(13);
+  if (tid == 0) trace_item(a, slot_attend(a) + blockIdx.x, p == 0 ? 4 : 1, u, p, t_start, t_wait, t_sel, t_att, 0);
 }
 
 // ================================================================== launches
@@ -1853,7 +1910,7 @@ static cudaError_t ensure_smem(const void* fn, std::atomic<size_t>* configured, 
 
 template <int D, int G, int MODE>
 static cudaError_t launch_chain(const LayerArgs& a_in, cudaStream_t st, int first_pdl, cudaEvent_t* ev) {
-  static std::atomic<size_t> cfg1[64], cfg2[64], cfg3[64];
+  static std::atomic<size_t> cfg1[64], cfg3[64];
   LayerArgs a = a_in;
   void* args[] = {&a};
   constexpr bool SEL = (MODE & kFSelect) != 0;
@@ -1870,41 +1927,20 @@ static cudaError_t launch_chain(const LayerArgs& a_in, cudaStream_t st, int firs
     if ((e = launch_pdl(fn, dim3(a.total_chunks), sm, st, first_pdl != 0, args, 32)) != cudaSuccess) return e;
     if (ev && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return e;
   }
-  // 2a. S items (512 blocks): keys and histogram, compensation partials into the unit's sums
+  // 2. select + attend: a cluster of a.splits CTAs per unit
   {
-    const size_t sm = (size_t)s_items_smem(G);
-    const void* fn = reinterpret_cast<const void*>(&k_sitems<D, G, MODE>);
-    if ((e = ensure_smem(fn, cfg2, sm)) != cudaSuccess) return e;
-    if (ev && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return e;
-    if ((e = launch_pdl(fn, dim3(a.ns_items), sm, st, true, args)) != cudaSuccess) return e;
-    if (ev && (e = cudaEventRecord(ev[3], st)) != cudaSuccess) return e;
-  }
-  // 2b. without the attention: the selection alone, one CTA per unit
-  if (SEL && !ATT) {
-    LayerArgs a1 = a;
-    a1.splits = 1;
-    void* args1[] = {&a1};
-    const size_t sm = (size_t)attend_union_bytes(D, G, a.key_stride, true) + 4 * attend_npick(a.K, 1, false);
-    const void* fn = reinterpret_cast<const void*>(&k_attend<D, G, MODE, false>);
-    if ((e = ensure_smem(fn, cfg3, sm)) != cudaSuccess) return e;
-    if (ev && (e = cudaEventRecord(ev[4], st)) != cudaSuccess) return e;
-    if ((e = launch_pdl(fn, dim3(a.B * a.Hkv), sm, st, true, args1, kAT, 1)) != cudaSuccess) return e;
-    if (ev && (e = cudaEventRecord(ev[5], st)) != cudaSuccess) return e;
-  }
-  // 3. attention: a cluster of a.splits CTAs (8 selected blocks per CTA and round) per unit
-  if (ATT) {
     static std::atomic<size_t> cfg4[64];
-    const bool loop = a.K > kAttendBlocks * a.splits;  // more than one selected block per warp
-    const size_t sm = (size_t)attend_union_bytes(D, G, a.key_stride, SEL) + 4 * attend_npick(a.K, a.splits, loop);
-    static std::atomic<size_t> cfg5[64];
-    const void* fn = loop ? reinterpret_cast<const void*>(&k_attend<D, G, MODE, true>)
-                          : reinterpret_cast<const void*>(&k_attend<D, G, MODE, false>);
-    if ((e = ensure_smem(fn, loop ? cfg5 : cfg4, sm)) != cudaSuccess) return e;
+    const bool loop = ATT && a.K > kAttendBlocks * a.splits;  // more than one selected block per warp
+    const int npick = post_npick(a.K, a.splits, loop);
+    const size_t sm = (size_t)post_layout(D, G, a.key_stride, a.post_cpc, a.K, npick, SEL, a.splits).total_words * 4;
+    const void* fn = loop ? reinterpret_cast<const void*>(&k_post<D, G, MODE, true>)
+                          : reinterpret_cast<const void*>(&k_post<D, G, MODE, false>);
+    if ((e = ensure_smem(fn, loop ? cfg4 : cfg3, sm)) != cudaSuccess) return e;
     if (a.splits > 8 && (e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
       return e;
-    if (ev && (e = cudaEventRecord(ev[4], st)) != cudaSuccess) return e;
+    if (ev && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return e;
     if ((e = launch_pdl(fn, dim3(a.B * a.Hkv * a.splits), sm, st, true, args, kAT, a.splits)) != cudaSuccess) return e;
-    if (ev && (e = cudaEventRecord(ev[5], st)) != cudaSuccess) return e;
+    if (ev && (e = cudaEventRecord(ev[3], st)) != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
@@ -1936,12 +1972,12 @@ cudaError_t launch_decode_chain(const LayerArgs& a, int mode, cudaStream_t st, i
 #undef COMPKV_G
 }
 
-size_t chain_smem_bytes(int D, int r, int G, int key_stride) {
+size_t chain_smem_bytes(int D, int r, int G, int key_stride, int post_cpc, int K, int splits) {
   size_t m = (size_t)score_smem(D, r, G, true, true);
-  if ((size_t)s_items_smem(G) > m) m = (size_t)s_items_smem(G);
-  const size_t at = (size_t)attend_union_bytes(D, G, key_stride, true) + 4 * 264;
-  if (at > m) m = at;
-  return m;
+  const bool loop = K > kAttendBlocks * splits;
+  const size_t pm =
+      (size_t)post_layout(D, G, key_stride, post_cpc, K, post_npick(K, splits, loop), true, splits).total_words * 4;
+  return pm > m ? pm : m;
 }
 
 }  // namespace compkv

@@ -207,9 +207,10 @@ int64_t compkv_launch_count(const compkv_ctx *ctx);
  * COMPKV_KERNEL_PREFILL, _APPEND, _SCORE, _SELECT, _ATTEND, _DECODE time
  * whole API calls (compkv_prefill, compkv_append, compkv_score_select,
  * compkv_select, compkv_attend, compkv_decode); a score/select, attend or
- * decode call launches three kernels, each timed on its own (enable = 2) under
- * COMPKV_KERNEL_K_SCORE (append + summaries + scores), _K_SITEMS (S and the
- * compensation sums) and _K_ATTEND (Top-K, attention, joint normalisation).
+ * decode call launches two kernels, each timed on its own (enable = 2) under
+ * COMPKV_KERNEL_K_SCORE (append + summaries + zbar, sigma2 and the
+ * compensation partials) and COMPKV_KERNEL_K_POST (LSE, S_b, forced set +
+ * Top-K, attention, compensation and the joint normalisation).
  * Events are host-side CUDA objects; no device memory is allocated. */
 enum {
   COMPKV_KERNEL_PREFILL = 0,
@@ -219,9 +220,8 @@ enum {
   COMPKV_KERNEL_ATTEND = 4,
   COMPKV_KERNEL_DECODE = 5,
   COMPKV_KERNEL_K_SCORE = 6,
-  COMPKV_KERNEL_K_SITEMS = 7,
-  COMPKV_KERNEL_K_ATTEND = 8,
-  COMPKV_KERNEL_FAMILIES = 9
+  COMPKV_KERNEL_K_POST = 7,
+  COMPKV_KERNEL_FAMILIES = 8
 };
 compkv_status compkv_profile_enable(compkv_ctx *ctx, int enable);
 
