@@ -36,7 +36,7 @@ struct Layout {
   int total_chunks = 0;
   int max_cap_blocks = 0;
   int K = 0, splits = 0, units = 0, key_stride = 0, post_cpc = 0;
-  size_t off_status = 0, off_lnew = 0, off_hist12 = 0, off_chunk_rec = 0, off_chunk_z = 0, off_chunk_u = 0,
+  size_t off_status = 0, off_lnew = 0, off_hist12 = 0, off_chunk_rec = 0, off_chunk_z = 0, off_chunk_s = 0,
          off_comp_part = 0, off_unit_nsel = 0, off_skeys = 0, off_sel = 0, total = 0;
 };
 
@@ -110,7 +110,7 @@ compkv_status make_layout(const compkv_config* c, Layout* L) {
   region(&L->off_hist12, (size_t)L->units * 4096 * sizeof(unsigned));  // everything before chunk_rec is zeroed per fresh start
   region(&L->off_chunk_rec, (size_t)L->total_chunks * G * 4 * sizeof(float));
   region(&L->off_chunk_z, (size_t)L->total_chunks * G * kChunk * sizeof(float));
-  region(&L->off_chunk_u, (size_t)L->total_chunks * G * kChunk * sizeof(float));
+  region(&L->off_chunk_s, (size_t)L->total_chunks * G * kChunk * sizeof(float));
   region(&L->off_comp_part, (size_t)L->total_chunks * G * (d + 4) * sizeof(float));
   region(&L->off_unit_nsel, (size_t)L->units * sizeof(int));
   region(&L->off_skeys, (size_t)L->units * L->key_stride * sizeof(uint32_t));
@@ -197,7 +197,7 @@ LayerArgs base_args(const compkv_ctx* c, int layer) {
   a.trace_cap = c->trace_cap;
   a.chunk_rec = reinterpret_cast<float*>(sc + c->lay.off_chunk_rec);
   a.chunk_z = reinterpret_cast<float*>(sc + c->lay.off_chunk_z);
-  a.chunk_u = reinterpret_cast<float*>(sc + c->lay.off_chunk_u);
+  a.chunk_s = reinterpret_cast<float*>(sc + c->lay.off_chunk_s);
   a.comp_part = reinterpret_cast<float*>(sc + c->lay.off_comp_part);
   a.unit_nsel = reinterpret_cast<int*>(sc + c->lay.off_unit_nsel);
   a.sel = reinterpret_cast<int*>(sc + c->lay.off_sel);

@@ -50,7 +50,7 @@ struct LayerArgs {
   int* lnew;                  // [B] tokens of each sequence in this call (after its append)
   float* chunk_rec;           // [chunk records][G][4]: max a, sum e^(a - max a), max(ln|b| + zbar), -
   float* chunk_z;             // [chunk records][G][kChunk]  zbar per block
-  float* chunk_u;             // [chunk records][G][kChunk]  e^(a - max a) * sigma2 per block
+  float* chunk_s;             // [chunk records][G][kChunk]  sigma2 per block
   float* comp_part;           // [chunk records][G][d + 4]: the chunk's sums with w relative to its own max
   int* unit_nsel;             // [units] selected blocks
   uint32_t* skeys;            // [units][key_stride] S_b as order-preserving keys (full radix selection only)

@@ -138,11 +138,11 @@ constexpr int kScoreStages = 3;   // groups in flight per warp
 __host__ __device__ inline int score_stage_floats(int D, int r, bool score, bool comp) {
   return kGB * D + (comp ? kGB * D : 0) + (score ? kGB * ((r + 3) & ~3) : 0);
 }
-// shared memory: stages | zbar [G][64] | sigma2 [G][64] | group weights [kGB][G] |
-// Qsq [G][r] | the appended block's kbar, vbar, Dbar | mbarriers
+// shared memory: stages | group weights [kGB][G] | Qsq [G][r] | the appended
+// block's kbar, vbar, Dbar | mbarriers
 __host__ __device__ inline int score_smem(int D, int r, int G, bool score, bool comp) {
   const int rr = (r + 3) & ~3;
-  return (kScoreStages * score_stage_floats(D, r, score, comp) + 2 * G * kChunk + kGB * G + G * rr + 2 * D + rr) * 4 +
+  return (kScoreStages * score_stage_floats(D, r, score, comp) + kGB * G + G * rr + 2 * D + rr) * 4 +
          8 * kScoreStages + 16;
 }
 
@@ -223,9 +223,7 @@ __global__ void __launch_bounds__(32) k_score(LayerArgs a) {
   const int lane = threadIdx.x;
   const int r = a.r, rr = (r + 3) & ~3;
   const int stage_f = score_stage_floats(D, r, SCORE, COMP);
-  float* zs = sm + kScoreStages * stage_f;   // [G][64]
-  float* ss = zs + G * kChunk;               // [G][64]
-  float* sw = ss + G * kChunk;               // [kGB][G]
+  float* sw = sm + kScoreStages * stage_f;   // [kGB][G]
   float* sqs = sw + kGB * G;                 // [G][rr]
   float* pk = sqs + G * rr;                  // appended block: kbar [D], vbar [D], Dbar [rr]
   float* pv = pk + D;
@@ -390,6 +388,14 @@ __global__ void __launch_bounds__(32) k_score(LayerArgs a) {
     vg[i] = v % G;
   }
   constexpr int RPL_MAX = 4;  // Dbar coordinates per lane in the butterfly over the r groups (r = 32 .. 128)
+  // per lane and value: running max of a and sum of e^(a - max) (the item's
+  // logsumexp parts, reduced at the end)
+  float lm[VPL], ll[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    lm[i] = -INFINITY;
+    ll[i] = 0.f;
+  }
   // compensation state: per head the reference, per lane its coordinates' sums and its values' weight sums
   float ref[G], acc[G][CPL], wsl[VPL];
 #pragma unroll
@@ -468,13 +474,22 @@ __global__ void __launch_bounds__(32) k_score(LayerArgs a) {
 #pragma unroll
       for (int i = 0; i < VPL; ++i) sg[i] = ps[i];
     }
-    if (primary)
+    // zbar and sigma2 per (head, block) to the item's records; a = ln|b| + zbar + sigma2 / 2 into the running parts
 #pragma unroll
-      for (int i = 0; i < VPL; ++i)
-        if (vb[i] < nbg) {
-          zs[vg[i] * kChunk + rb + vb[i]] = zb[i];
-          if (SCORE) ss[vg[i] * kChunk + rb + vb[i]] = sg[i] / (float)D;
-        }
+    for (int i = 0; i < VPL; ++i) {
+      const float s2 = sg[i] / (float)D;
+      if (primary && vb[i] < nbg) {
+        const int64_t o = ((int64_t)k.rec * G + vg[i]) * kChunk + rb + vb[i];
+        a.chunk_z[o] = zb[i];
+        if (SCORE) a.chunk_s[o] = s2;
+      }
+      if (SCORE && primary && vb[i] < nbg) {
+        const float av = cv[i] + 0.5f * s2;
+        const float mn = fmaxf(lm[i], av);
+        ll[i] = (lm[i] == -INFINITY ? 0.f : ll[i] * __expf(lm[i] - mn)) + __expf(av - mn);
+        lm[i] = mn;
+      }
+    }
     if (COMP) {
       // the group's maximum of ln|b| + zbar per head (lanes holding the same head)
       float gm[VPL];
@@ -551,47 +566,38 @@ __global__ void __launch_bounds__(32) k_score(LayerArgs a) {
     }
   }
   const unsigned long long t_scored = a.trace ? global_ns() : 0ull;
-  // ---- the item's records, per head
+  // ---- the item's records, per head: (max a, sum e^(a - max a), max(ln|b| + zbar)),
+  // the running parts reduced over the lanes holding that head
   const int rec = k.rec;
+  constexpr int GL = NV >= 32 ? 0 : SH;
+  constexpr int GB2 = (G / VPL) == 1 ? 0 : ((G / VPL) == 2 ? 1 : ((G / VPL) == 4 ? 2 : 3));
+  if (SCORE) {
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    float av[2], cvv[2], zz[2], s2[2];
-    float ma = -INFINITY, mc = -INFINITY;
+    for (int o = 1; o < 32; o <<= 1) {
+      const bool head_bit = o >= (1 << GL) && o < (1 << (GL + GB2));
+      if (!head_bit)
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int blk = lane + 32 * i;
-      av[i] = cvv[i] = -INFINITY;
-      zz[i] = s2[i] = 0.f;
-      if (blk < k.nb) {
-        const int bb = k.b0 + blk;
-        zz[i] = zs[g * kChunk + blk];
-        cvv[i] = ln_n(bb == k.N - 1 ? k.L - kBlock * bb : kBlock) + zz[i];
-        if (SCORE) {
-          s2[i] = ss[g * kChunk + blk];
-          av[i] = cvv[i] + 0.5f * s2[i];
+        for (int i = 0; i < VPL; ++i) {
+          const float m2 = __shfl_xor_sync(0xffffffffu, lm[i], o), l2 = __shfl_xor_sync(0xffffffffu, ll[i], o);
+          const float mn = fmaxf(lm[i], m2);
+          if (mn != -INFINITY) {
+            ll[i] = (lm[i] == -INFINITY ? 0.f : ll[i] * __expf(lm[i] - mn)) + (m2 == -INFINITY ? 0.f : l2 * __expf(m2 - mn));
+            lm[i] = mn;
+          }
         }
-      }
-      ma = fmaxf(ma, av[i]);
-      mc = fmaxf(mc, cvv[i]);
     }
-    mc = warp_max(mc);
-    float la = 0.f;
-    if (SCORE) {
-      ma = warp_max(ma);
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int blk = lane + 32 * i;
-        const float e = (blk < k.nb) ? expf(av[i] - ma) : 0.f;
-        la += e;
-        a.chunk_u[((int64_t)rec * G + g) * kChunk + blk] = e * s2[i];
-      }
-      la = warp_sum(la);
-    }
-    if (COMP)
-#pragma unroll
-      for (int i = 0; i < 2; ++i) a.chunk_z[((int64_t)rec * G + g) * kChunk + lane + 32 * i] = zz[i];
-    if (lane == 0) *reinterpret_cast<float4*>(a.chunk_rec + ((int64_t)rec * G + g) * 4) = make_float4(ma, la, mc, 0.f);
   }
+  // the lane holding (block 0, head g) writes head g's record
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+    if (primary && vb[i] == 0) {
+      float mc = ref[0];
+#pragma unroll
+      for (int g = 1; g < G; ++g)
+        if (vg[i] == g) mc = ref[g];
+      *reinterpret_cast<float4*>(a.chunk_rec + ((int64_t)rec * G + vg[i]) * 4) =
+          make_float4(SCORE ? lm[i] : -INFINITY, SCORE ? ll[i] : 0.f, COMP ? mc : -INFINITY, 0.f);
+    }
   if (COMP) {
     // the partial relative to mc_g = ref_g; weight sums reduced over the lanes holding each head
     float wt[VPL];
@@ -1109,24 +1115,25 @@ __device__ __forceinline__ uint32_t atom_peer_add(uint32_t addr, uint32_t v) {
 constexpr int kAT = 256;            // threads of a post CTA
 constexpr int kAW = kAT / 32;       // its warps: one selected block each per round
 constexpr int kMiscInts = 64;
+constexpr int kTieCap = 64;         // tie-list entries per CTA of the cluster (more: the full radix selection)
 
 // Shared memory of the post kernel, in 4-byte words:
 //   union: selection (histograms [4096] and [256] | keys of the CTA's blocks [cpc * 64] |
-//          bitmap [roundup4(cpc * 2) + 4] | rank-0 list keys, indices [kRankMax + 4] each),
+//          bitmap [roundup4(cpc * 2) + 4] | every CTA's tie list: keys, indices [16][kTieCap] + 4 each),
 //          the full radix selection's region (rank 0, rare), or the attention
 //          (per-warp partials [kAW][G][D], m, l [kAW][G])
 //   then: compensation share [G][D + 4] | the C CTAs' selections [C][min(cpc * 64, K)] |
-//   picks [npick] | incoming partials [items per rank][C][8] | item factors [cpc][G] x 2 |
+//   picks [npick] | incoming partials [items per rank][C][8] | item factors [cpc][G] |
 //   LSE, M [G] x 2 | counts [16] | misc [kMiscInts]
 __host__ __device__ inline int post_bitmap_words(int cpc) { return ((cpc * 2 + 3) & ~3) + 4; }
 struct PostLayout {
-  int u_words, comp, own, own_n, pick, mstage, fch, fcp, lse, mref, cnts, misc, total_words;
+  int u_words, comp, own, own_n, pick, mstage, fcp, lse, mref, cnts, misc, total_words;
 };
 __host__ __device__ inline int attend_smem_words(int D, int G) { return kAW * G * D + 2 * kAW * G + 4; }
 __host__ __device__ inline int post_items_per_rank(int D, int G, int C) { return (G * D / 4 + C - 1) / C; }
 __host__ __device__ inline PostLayout post_layout(int D, int G, int key_stride, int cpc, int K, int npick, bool sel, int C) {
   PostLayout l;
-  const int selw = kHist12 + 256 + cpc * kChunk + post_bitmap_words(cpc) + 2 * (kRankMax + 4);
+  const int selw = kHist12 + 256 + cpc * kChunk + post_bitmap_words(cpc) + 2 * (16 * kTieCap + 4);
   const int fallback = ((sel_region_words(key_stride) + 3) & ~3) + kMiscInts;
   int u = attend_smem_words(D, G);
   if (sel && selw > u) u = selw;
@@ -1137,8 +1144,7 @@ __host__ __device__ inline PostLayout post_layout(int D, int G, int key_stride, 
   l.own_n = ((cpc * kChunk < K ? cpc * kChunk : K) + 3) & ~3;
   l.pick = l.own + C * l.own_n;
   l.mstage = l.pick + ((npick + 3) & ~3);
-  l.fch = l.mstage + post_items_per_rank(D, G, C) * C * 8;
-  l.fcp = l.fch + ((cpc * G + 3) & ~3);
+  l.fcp = l.mstage + post_items_per_rank(D, G, C) * C * 8;
   l.lse = l.fcp + ((cpc * G + 3) & ~3);
   l.mref = l.lse + ((G + 3) & ~3);
   l.cnts = l.mref + ((G + 3) & ~3);
@@ -1178,7 +1184,7 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_post(LayerArgs a) {
   uint32_t* keys = chist + 256;
   unsigned* words = keys + a.post_cpc * kChunk;
   uint32_t* lkey = words + post_bitmap_words(a.post_cpc);
-  int* lidx = reinterpret_cast<int*>(lkey + kRankMax + 4);
+  int* lidx = reinterpret_cast<int*>(lkey + 16 * kTieCap + 4);
   // attention phase views
   float* red_a = psm;                     // [kAW][G][D]
   float* red_m = red_a + kAW * G * D;     // [kAW][G]
@@ -1189,7 +1195,6 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_post(LayerArgs a) {
   int* own = selall + p * lay.own_n;
   float* mstage = psm + lay.mstage;                      // [items per rank][C][8]: acc (4), m, l
   int* pick = reinterpret_cast<int*>(psm + lay.pick);
-  float* fch = psm + lay.fch;
   float* fcp = psm + lay.fcp;
   float* lse = psm + lay.lse;
   float* mref = psm + lay.mref;
@@ -1214,10 +1219,14 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_post(LayerArgs a) {
   }
   pdl_wait();
   const unsigned long long t_wait = a.trace ? global_ns() : 0ull;
-  // phase marks of rank 0 (tracing aid): mark k = time since the previous mark
-  unsigned long long tp = t_wait;
+  // phase marks of rank 0 (tracing aid): mark k = SM clocks since the previous mark
+  unsigned long long tp = clock64();
   auto mark = [&](int k) {
-    if (a.trace && p == 0 && tid == 0) tp = trace_phase(a, u, k, k, tp);
+    if (a.trace && p == 0 && tid == 0) {
+      const unsigned long long c = clock64();
+      trace_item(a, slot_phase(a) + u * 32 + k, 5, u, k, tp, c);
+      tp = c;
+    }
   };
   const int L = a.lnew[s], N = ceil_blocks(L);
   const int nch = (N + kChunk - 1) / kChunk;
@@ -1227,6 +1236,21 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_post(LayerArgs a) {
   const int nown = b_hi - b_lo;
   const int rec0 = chunk_record(a, s, h, 0);
   const bool all_sel = N <= K;
+  const bool want_keys = SEL && (!all_sel || a.scores);
+  // zbar and sigma2 of this thread's first PF blocks, in flight during the LSE pass
+  constexpr int PF = G >= 8 ? 2 : 4;
+  float zv0[PF][G], sv0[PF][G];
+#pragma unroll
+  for (int k = 0; k < PF; ++k) {
+    const int i = tid + k * kAT, b = b_lo + i;
+    const int64_t o = ((int64_t)(rec0 + b / kChunk) * G) * kChunk + (b % kChunk);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const bool ld = want_keys && i < nown;
+      zv0[k][g] = ld ? __ldcg(a.chunk_z + o + g * kChunk) : 0.f;
+      sv0[k][g] = ld ? __ldcg(a.chunk_s + o + g * kChunk) : 0.f;
+    }
+  }
 
   // ---- a. LSE_g, M_g and the factors of this CTA's items (one pass over the
   // records when they fit eight per lane; the items' own records stay in registers)
@@ -1280,14 +1304,12 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_post(LayerArgs a) {
       for (int k = 0; k < 8; ++k) {
         const int c = lane + 32 * k;
         if (c >= c_lo && c < c_hi) {
-          if (SEL) fch[(c - c_lo) * G + g] = expf(rv[k].x - lg);
           if (COMP) fcp[(c - c_lo) * G + g] = expf(rv[k].z - MC);
         }
       }
     } else {
       for (int j = lane; j < c_hi - c_lo; j += 32) {
         const float4 r4 = __ldcg(reinterpret_cast<const float4*>(a.chunk_rec + ((int64_t)(rec0 + c_lo + j) * G + g) * 4));
-        if (SEL) fch[j * G + g] = expf(r4.x - lg);
         if (COMP) fcp[j * G + g] = expf(r4.z - MC);
       }
     }
@@ -1299,25 +1321,29 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_post(LayerArgs a) {
   __syncthreads();
   mark(1);
   // ---- a. keys of this CTA's blocks and their histogram; the compensation share
-  if (SEL && (!all_sel || a.scores)) {
-    for (int i0 = tid; i0 < nown; i0 += 4 * kAT) {
-      float uv[4][G];
+  if (want_keys) {
+    // S_b = sum_g phat sigma2 = sum_g e^(ln|b| + zbar + sigma2/2 - LSE_g) sigma2
+    for (int i0 = tid; i0 < nown; i0 += PF * kAT) {
+      float zv[PF][G], sv[PF][G];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < PF; ++k) {
         const int i = i0 + k * kAT, b = b_lo + i;
-        const int rec = rec0 + b / kChunk;
+        const int64_t o = ((int64_t)(rec0 + b / kChunk) * G) * kChunk + (b % kChunk);
 #pragma unroll
-        for (int g = 0; g < G; ++g)
-          uv[k][g] = i < nown ? __ldcg(a.chunk_u + ((int64_t)rec * G + g) * kChunk + (b % kChunk)) : 0.f;
+        for (int g = 0; g < G; ++g) {
+          const bool ld = i0 != tid && i < nown;
+          zv[k][g] = i0 == tid ? zv0[k][g] : (ld ? __ldcg(a.chunk_z + o + g * kChunk) : 0.f);
+          sv[k][g] = i0 == tid ? sv0[k][g] : (ld ? __ldcg(a.chunk_s + o + g * kChunk) : 0.f);
+        }
       }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < PF; ++k) {
         const int i = i0 + k * kAT, b = b_lo + i;
         if (i >= nown) break;
-        const int cl = b / kChunk - c_lo;
+        const float lnn = ln_n(b == N - 1 ? L - kBlock * b : kBlock);
         float S = 0.f;
 #pragma unroll
-        for (int g = 0; g < G; ++g) S = fmaf(uv[k][g], fch[cl * G + g], S);
+        for (int g = 0; g < G; ++g) S = fmaf(expf(lnn + zv[k][g] + 0.5f * sv[k][g] - lse[g]), sv[k][g], S);
         S = fmaxf(S, 0.f);
         const uint32_t key = __float_as_uint(S);
         keys[i] = key;
@@ -1437,73 +1463,53 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_post(LayerArgs a) {
         if (bin > T || (bin == T && take_all)) {
           sel = true;
         } else if (bin == T) {
+          // into every CTA's copy of this CTA's tie list
           const int slot = atomicAdd(misc + kMListN, 1);
-          if (slot < kRankMax) {
-            lkey[slot] = key;
-            lidx[slot] = b;
-          }
+          if (slot < kTieCap)
+            for (int q = 0; q < C; ++q) {
+              st_peer_u32(peer_smem(lkey + p * kTieCap + slot, (uint32_t)q), key);
+              st_peer_u32(peer_smem(lidx + p * kTieCap + slot, (uint32_t)q), (uint32_t)b);
+            }
         }
       }
       if (sel) atomicOr(&words[i >> 5], 1u << (i & 31));
     }
     if (!take_all) {
       __syncthreads();
-      mark(5);
-      cluster_sync_all();  // every CTA's list is complete
-      mark(6);
-      // the lists' sizes, then all of them gathered here behind this CTA's own
+      // this CTA's tie count into every CTA
       int* lsz = misc + 16;  // the C list sizes
-      if (tid < C) lsz[tid] = (int)ld_peer_u32(peer_smem(misc + kMListN, (uint32_t)tid));
-      __syncthreads();
-      int m = 0, mine0 = 0;
+      if (tid < C) st_peer_u32(peer_smem(lsz + p, (uint32_t)tid), (uint32_t)misc[kMListN]);
+      mark(5);
+      cluster_sync_all();  // every CTA holds every tie list
+      mark(6);
+      int m = 0, mx = 0;
       for (int q = 0; q < C; ++q) {
-        if (q < p) mine0 += lsz[q];
         m += lsz[q];
+        mx = max(mx, lsz[q]);
       }
-      if (a.trace && p == 0 && tid == 0)
-        trace_item(a, slot_phase(a) + u * 32 + 16, 6, u, 0, (unsigned long long)m, (unsigned long long)need,
-                   (unsigned long long)misc[kMCntT], (unsigned long long)misc[kMAbove]);
-      if (m <= kRankMax) {
-        // gather: peer q's entries go to [off_q, off_q + cnt_q); this CTA's own move from [0, cnt_p)
-        // (into the histogram's space: every CTA has read the histograms by now)
-        uint32_t* gkey = hist;
-        int* gidx = reinterpret_cast<int*>(gkey + kRankMax + 4);
-        static_assert(kRankMax <= 2 * kAT, "two gather rounds");
-        uint32_t gk[2], gi[2];
-#pragma unroll
-        for (int r2 = 0; r2 < 2; ++r2) {
-          const int e = tid + r2 * kAT;
-          gk[r2] = 0u;
-          gi[r2] = 0u;
-          if (e < m) {
-            int q = 0, base = 0;
-            while (q + 1 < C && base + lsz[q] <= e) base += lsz[q++];
-            gk[r2] = ld_peer_u32(peer_smem(lkey + (e - base), (uint32_t)q));
-            gi[r2] = ld_peer_u32(peer_smem(lidx + (e - base), (uint32_t)q));
+      if (mx <= kTieCap) {
+        // rank this CTA's entries among all: region q holds lsz[q] entries; the
+        // unused slots hold sentinels (key 0, largest index) that never rank above a listed key
+        for (int e = tid; e < C * kTieCap; e += kAT)
+          if (e % kTieCap >= lsz[e / kTieCap]) {
+            lkey[e] = 0u;
+            lidx[e] = 0x7fffffff;
           }
-        }
-#pragma unroll
-        for (int r2 = 0; r2 < 2; ++r2) {
-          const int e = tid + r2 * kAT;
-          if (e < m) {
-            gkey[e] = gk[r2];
-            gidx[e] = (int)gi[r2];
-          }
-        }
-        if (tid < 4) {
-          gkey[m + tid] = 0u;
-          gidx[m + tid] = 0x7fffffff;
-        }
         __syncthreads();
-        const int m4 = (m + 3) & ~3;
+        mark(21);
+        (void)m;
         const int cp = lsz[p];
         for (int e = tid; e < cp; e += kAT) {
-          const uint32_t k0 = gkey[mine0 + e];
-          const int i0 = gidx[mine0 + e];
+          const uint32_t k0 = lkey[p * kTieCap + e];
+          const int i0 = lidx[p * kTieCap + e];
           int rank = 0;
-          for (int f = 0; f < m4; f += 4) {
-            const uint4 kf = *reinterpret_cast<const uint4*>(gkey + f);
-            const int4 xf = *reinterpret_cast<const int4*>(gidx + f);
+          for (int f = 0; f < C * kTieCap; f += 4) {
+            if (lsz[f / kTieCap] <= f % kTieCap) {  // the rest of region f / kTieCap is empty
+              f = (f / kTieCap) * kTieCap + kTieCap - 4;
+              continue;
+            }
+            const uint4 kf = *reinterpret_cast<const uint4*>(lkey + f);
+            const int4 xf = *reinterpret_cast<const int4*>(lidx + f);
             rank += (kf.x > k0 || (kf.x == k0 && xf.x < i0));
             rank += (kf.y > k0 || (kf.y == k0 && xf.y < i0));
             rank += (kf.z > k0 || (kf.z == k0 && xf.z < i0));
@@ -1564,11 +1570,13 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_post(LayerArgs a) {
           }
         }
       }
+      mark(22);
       const int total_own = __shfl_sync(0xffffffffu, incl, 31);
       if (lane == 0) misc[kMTotal] = total_own;
       if (lane < C) st_peer_u32(peer_smem(cnts + p, (uint32_t)lane), (uint32_t)total_own);
     }
     __syncthreads();
+    mark(23);
     if (ATT) {
       // the K/V rows (and mean values) of this CTA's selected blocks on their way to L2
       // while the offsets are exchanged; another CTA of the cluster may attend them
