@@ -133,7 +133,8 @@ __device__ __forceinline__ unsigned long long trace_phase(const LayerArgs& a, in
 // ln|b| + zbar over the blocks seen, and the sums are rescaled when it grows,
 // so the item's partial ends relative to mc_g = max_b (ln|b| + zbar).
 constexpr int kGB = 8;            // blocks per pipeline group
-constexpr int kScoreStages = 3;   // groups in flight per warp
+constexpr int kScoreStages = 3;   // groups in flight per item
+constexpr int kScoreWarps = 2;    // warps per item: each takes kGB / kScoreWarps blocks of every group
 
 __host__ __device__ inline int score_stage_floats(int D, int r, bool score, bool comp) {
   return kGB * D + (comp ? kGB * D : 0) + (score ? kGB * ((r + 3) & ~3) : 0);
@@ -211,16 +212,17 @@ template <>
 __device__ __forceinline__ void lds_vec<1>(const float* p, float (&x)[1]) { x[0] = *p; }
 
 template <int D, int G, int MODE>
-__global__ void __launch_bounds__(32) k_score(LayerArgs a) {
+__global__ void __launch_bounds__(32 * kScoreWarps) k_score(LayerArgs a) {
   constexpr bool APPEND = (MODE & kFAppend) != 0;
   constexpr bool SCORE = (MODE & kFScore) != 0;
   constexpr bool COMP = (MODE & kFComp) != 0;
   constexpr int CPL = D / 32;                        // coordinates per lane
-  constexpr int NV = kGB * G;                        // (block, head) values of a group
+  constexpr int GBW = kGB / kScoreWarps;              // blocks of a group per warp
+  constexpr int NV = GBW * G;                        // (block, head) values of a warp's share of a group
   constexpr int VPL = NV >= 32 ? NV / 32 : 1;        // values a lane ends with
   constexpr int SH = NV >= 32 ? 0 : (NV == 16 ? 1 : (NV == 8 ? 2 : 3));  // log2(32 / NV) for NV < 32
   extern __shared__ __align__(128) float sm[];
-  const int lane = threadIdx.x;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int r = a.r, rr = (r + 3) & ~3;
   const int stage_f = score_stage_floats(D, r, SCORE, COMP);
   float* sw = sm + kScoreStages * stage_f;   // [kGB][G]
@@ -232,31 +234,35 @@ __global__ void __launch_bounds__(32) k_score(LayerArgs a) {
   const unsigned long long t_start = a.trace ? global_ns() : 0ull;
   pdl_wait();  // the previous work on the stream may have written this cache
   if (blockIdx.x == 0)
-    for (int s = lane; s < a.B; s += 32) {
+    for (int s = threadIdx.x; s < a.B; s += 32 * kScoreWarps) {
       bool f2;
       a.lnew[s] = unit_tokens(a, s, APPEND, &f2);
     }
-  const ScoreChunk k = score_chunk<APPEND>(a, blockIdx.x);
-  if (k.nb == 0) {
-    pdl_trigger();
-    return;
-  }
+  // the item's place in the cache comes from the layout alone: its first
+  // copies start before the sequence length (a dependent load) is known; they
+  // cover the item's rows up to the capacity (the open block's row is replaced
+  // by the append below, rows past the last block are not used)
+  int s0 = 0;
+  while (s0 + 1 < a.B && a.chunk0[s0 + 1] <= (int)blockIdx.x) ++s0;
+  const int loc0 = (int)blockIdx.x - a.chunk0[s0];
+  const int h0 = loc0 / a.nchunk[s0], c0 = loc0 % a.nchunk[s0];
+  const int cap_nb = min(kChunk, a.cap_blocks[s0] - c0 * kChunk);
+  const int64_t row0 = row_of(a, s0, h0, c0 * kChunk);
   const bool dbar_bulk = SCORE && (r & 3) == 0;
-  const int ng = (k.nb + kGB - 1) / kGB;
-  if (lane == 0) {
+  const int ng_cap = (cap_nb + kGB - 1) / kGB;
+  if (threadIdx.x == 0) {
     for (int i = 0; i < kScoreStages; ++i) mbar_init(bars + i, 1);
     fence_mbar_init();
   }
-  __syncwarp();
-  // start the copies of group gi into its stage (rows [8 gi, 8 gi + 8) of the item, up to nt)
-  const float* gk = a.kbar + k.row0 * D;
-  const float* gv = a.vbar + k.row0 * D;
-  const float* gd = a.dbar + k.row0 * r;
-  const int nt = k.nt;
+  __syncthreads();
+  // start the copies of group gi into its stage (rows [8 gi, 8 gi + 8) of the item, up to the capacity)
+  const float* gk = a.kbar + row0 * D;
+  const float* gv = a.vbar + row0 * D;
+  const float* gd = a.dbar + row0 * r;
   auto issue = [=](int gi) {
-    if (lane != 0) return;
+    if (threadIdx.x != 0) return;
     float* st = sm + (gi % kScoreStages) * stage_f;
-    const int rb = gi * kGB, n = max(0, min(kGB, nt - rb));
+    const int rb = gi * kGB, n = max(0, min(kGB, cap_nb - rb));
     const uint32_t bytes = (uint32_t)n * (uint32_t)(D * 4 * (COMP ? 2 : 1) + (dbar_bulk ? r * 4 : 0));
     uint64_t* bar = bars + gi % kScoreStages;
     mbar_arrive_expect_tx(bar, bytes);
@@ -266,8 +272,16 @@ __global__ void __launch_bounds__(32) k_score(LayerArgs a) {
       if (dbar_bulk) bulk_g2s(st + kGB * D * (COMP ? 2 : 1), gd + rb * r, (uint32_t)n * r * 4u, bar);
     }
   };
-  for (int gi = 0; gi < kScoreStages && gi < ng; ++gi) issue(gi);
-  if (ng <= kScoreStages) pdl_trigger();
+  const int pre = min(kScoreStages, ng_cap);
+  for (int gi = 0; gi < pre; ++gi) issue(gi);
+  const ScoreChunk k = score_chunk<APPEND>(a, blockIdx.x);
+  const int ng = (k.nb + kGB - 1) / kGB;
+  if (k.nb == 0 || ng <= kScoreStages) pdl_trigger();
+  if (k.nb == 0) {
+    // nothing to score: let the copies already issued land before the CTA exits
+    for (int gi = 0; gi < pre; ++gi) mbar_wait_bounded(bars + gi, 0u, a.status, k.s, k.h, 11);
+    return;
+  }
 
   // this lane's coordinates of the G queries
   const float* qbase = a.q + ((int64_t)k.s * a.Hkv * G + (int64_t)k.h * G) * D;
@@ -275,7 +289,7 @@ __global__ void __launch_bounds__(32) k_score(LayerArgs a) {
 #pragma unroll
   for (int g = 0; g < G; ++g) lds_vec<CPL>(qbase + g * D + CPL * lane, q[g]);  // generic load (global)
   // Qsq_{g,t} = sum of q_g^2 over coordinate group t = [t*D/r, (t+1)*D/r)
-  if (SCORE) {
+  if (SCORE && wid == 0) {
     const int gs = D / r;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -304,7 +318,7 @@ __global__ void __launch_bounds__(32) k_score(LayerArgs a) {
   // every token; two-pass mean and population variance in fp32 from the
   // exact bf16 values)
   const int patched = k.append ? k.nb - 1 : -1;  // item-local block whose rows come from pk, pv, pd
-  if (APPEND && k.append) {
+  if (APPEND && k.append && wid == 0) {
     const int n = k.L - kBlock * (k.N - 1);
     const int64_t row = k.row0 + (k.nb - 1);
     const int c0 = CPL * lane;
@@ -377,8 +391,8 @@ __global__ void __launch_bounds__(32) k_score(LayerArgs a) {
       }
     }
   }
-  __syncwarp();
-  // this lane's values after the butterfly: v = block * G + head
+  __syncthreads();  // Qsq and the appended block's rows are in place
+  // this lane's values after the butterfly: v = block * G + head (block within this warp's share)
   int vb[VPL], vg[VPL];
   const bool primary = NV >= 32 || (lane & ((1 << SH) - 1)) == 0;
 #pragma unroll
@@ -412,15 +426,23 @@ __global__ void __launch_bounds__(32) k_score(LayerArgs a) {
     const float* skb = st;
     const float* svb = st + kGB * D;
     const float* sdb = st + kGB * D * (COMP ? 2 : 1);
-    const int rb = gi * kGB, nbg = min(kGB, k.nb - rb);
+    float* swr = sw + wid * GBW * G;  // this warp's weights [GBW][G]
+    // this warp's blocks of the group: [rb, rb + nbg), stage rows [wb0, wb0 + nbg)
+    const int wb0 = wid * GBW;
+    const int rb = gi * kGB + wb0, nbg = max(0, min(GBW, k.nb - rb));
     mbar_wait_bounded(bars + gi % kScoreStages, (uint32_t)(gi / kScoreStages) & 1u, a.status, k.s, k.h, 10);
-    if (SCORE && !dbar_bulk)
-      for (int i = lane; i < min(kGB, k.nt - rb) * r; i += 32) const_cast<float*>(sdb)[i] = a.dbar[(k.row0 + rb) * r + i];
-    __syncwarp();
+    if (SCORE && !dbar_bulk) {
+      for (int i = threadIdx.x; i < min(kGB, k.nt - gi * kGB) * r; i += 32 * kScoreWarps)
+        const_cast<float*>(sdb)[i] = a.dbar[(k.row0 + gi * kGB) * r + i];
+      __syncthreads();
+    }
+    skb += wb0 * D;
+    svb += wb0 * D;
+    sdb += wb0 * r;
     // zbar partial dots
     float p[NV];
 #pragma unroll
-    for (int b = 0; b < kGB; ++b) {
+    for (int b = 0; b < GBW; ++b) {
       float x[CPL];
       const float* rowp = (rb + b == patched) ? pk : skb + b * D;
       lds_vec<CPL>(rowp + CPL * lane, x);
@@ -456,7 +478,7 @@ __global__ void __launch_bounds__(32) k_score(LayerArgs a) {
       const int rpl = r / 32;
       float ps[NV];
 #pragma unroll
-      for (int b = 0; b < kGB; ++b) {
+      for (int b = 0; b < GBW; ++b) {
         const float* drow = (rb + b == patched) ? pd : sdb + b * r;
         float x[RPL_MAX];
 #pragma unroll
@@ -532,7 +554,7 @@ __global__ void __launch_bounds__(32) k_score(LayerArgs a) {
           if (vg[i] == g) rg = ref[g];
         const float w = vb[i] < nbg ? __expf(cv[i] - rg) : 0.f;
         if (primary) {
-          sw[vb[i] * G + vg[i]] = w;
+          swr[vb[i] * G + vg[i]] = w;
           wsl[i] += w;
         }
       }
@@ -544,13 +566,13 @@ __global__ void __launch_bounds__(32) k_score(LayerArgs a) {
 #pragma unroll
         for (int g0 = 0; g0 < G; g0 += (G >= 4 ? 4 : G)) {
           if constexpr (G >= 4) {
-            const float4 t4 = *reinterpret_cast<const float4*>(sw + b * G + g0);
+            const float4 t4 = *reinterpret_cast<const float4*>(swr + b * G + g0);
             w[g0] = t4.x; w[g0 + 1] = t4.y; w[g0 + 2] = t4.z; w[g0 + 3] = t4.w;
           } else if constexpr (G == 2) {
-            const float2 t2 = *reinterpret_cast<const float2*>(sw + b * G);
+            const float2 t2 = *reinterpret_cast<const float2*>(swr + b * G);
             w[0] = t2.x; w[1] = t2.y;
           } else {
-            w[0] = sw[b];
+            w[0] = swr[b];
           }
         }
 #pragma unroll
@@ -559,12 +581,14 @@ __global__ void __launch_bounds__(32) k_score(LayerArgs a) {
           for (int c = 0; c < CPL; ++c) acc[g][c] = fmaf(w[g], x[c], acc[g][c]);
       }
     }
-    __syncwarp();  // the stage and the weights are free again
+    __syncthreads();  // the stage and the weights are free again
     if (gi + kScoreStages < ng) {
       issue(gi + kScoreStages);
       if (gi + kScoreStages == ng - 1) pdl_trigger();
     }
   }
+  // copies issued up front for groups past the last block (capacity beyond the length) land before the stages are reused
+  for (int gi = ng; gi < pre; ++gi) mbar_wait_bounded(bars + gi, 0u, a.status, k.s, k.h, 11);
   const unsigned long long t_scored = a.trace ? global_ns() : 0ull;
   // ---- the item's records, per head: (max a, sum e^(a - max a), max(ln|b| + zbar)),
   // the running parts reduced over the lanes holding that head
@@ -587,38 +611,64 @@ __global__ void __launch_bounds__(32) k_score(LayerArgs a) {
         }
     }
   }
-  // the lane holding (block 0, head g) writes head g's record
+  // the warps' parts combined through stage 0 (free now): per head (max a, sum, reference,
+  // weight sum) and the compensation sums; warp 0 writes the item's records
+  float* xr = sm;                       // [kScoreWarps][G][4]
+  float* xa = sm + kScoreWarps * G * 4; // [kScoreWarps][G][D]
+  float wt[VPL];
 #pragma unroll
-  for (int i = 0; i < VPL; ++i)
-    if (primary && vb[i] == 0) {
-      float mc = ref[0];
+  for (int i = 0; i < VPL; ++i) wt[i] = primary ? wsl[i] : 0.f;
 #pragma unroll
-      for (int g = 1; g < G; ++g)
-        if (vg[i] == g) mc = ref[g];
-      *reinterpret_cast<float4*>(a.chunk_rec + ((int64_t)rec * G + vg[i]) * 4) =
-          make_float4(SCORE ? lm[i] : -INFINITY, SCORE ? ll[i] : 0.f, COMP ? mc : -INFINITY, 0.f);
-    }
-  if (COMP) {
-    // the partial relative to mc_g = ref_g; weight sums reduced over the lanes holding each head
-    float wt[VPL];
+  for (int g = 0; g < G; ++g) {
+    float t = 0.f;
 #pragma unroll
-    for (int i = 0; i < VPL; ++i) wt[i] = primary ? wsl[i] : 0.f;
+    for (int i = 0; i < VPL; ++i)
+      if (vg[i] == g) t += wt[i];
+    if (COMP) t = warp_sum(t);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      if (primary && vb[i] == 0 && vg[i] == g)
+        *reinterpret_cast<float4*>(xr + (wid * G + g) * 4) = make_float4(lm[i], ll[i], ref[g], t);
+    if (COMP && wid > 0)
+      for (int c = 0; c < CPL; ++c) xa[(wid * G + g) * D + CPL * lane + c] = acc[g][c];
+  }
+  __syncthreads();
+  if (wid == 0) {
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      float* dst = a.comp_part + ((int64_t)rec * G + g) * (D + 4);
-      if constexpr (CPL == 4)
-        *reinterpret_cast<float4*>(dst + 4 * lane) = make_float4(acc[g][0], acc[g][1], acc[g][2], acc[g][3]);
-      else
-        *reinterpret_cast<float2*>(dst + 2 * lane) = make_float2(acc[g][0], acc[g][1]);
-      float t = 0.f;
+      float M = -INFINITY, Lsum = 0.f, R = -INFINITY, Wsum = 0.f;
+      for (int w = 0; w < kScoreWarps; ++w) {
+        const float4 e = *reinterpret_cast<const float4*>(xr + (w * G + g) * 4);
+        M = fmaxf(M, e.x);
+        R = fmaxf(R, e.z);
+      }
+      float f[kScoreWarps];
+      for (int w = 0; w < kScoreWarps; ++w) {
+        const float4 e = *reinterpret_cast<const float4*>(xr + (w * G + g) * 4);
+        if (e.x != -INFINITY) Lsum += e.y * __expf(e.x - M);
+        f[w] = e.z == -INFINITY ? 0.f : __expf(e.z - R);
+        Wsum += e.w * f[w];
+      }
+      if (lane == 0)
+        *reinterpret_cast<float4*>(a.chunk_rec + ((int64_t)rec * G + g) * 4) =
+            make_float4(SCORE ? M : -INFINITY, SCORE ? Lsum : 0.f, COMP ? R : -INFINITY, 0.f);
+      if (COMP) {
+        float* dst = a.comp_part + ((int64_t)rec * G + g) * (D + 4);
+        float o[CPL];
 #pragma unroll
-      for (int i = 0; i < VPL; ++i)
-        if (vg[i] == g) t += wt[i];
-      t = warp_sum(t);
-      if (lane == 0) dst[D] = t;
+        for (int c = 0; c < CPL; ++c) {
+          o[c] = acc[g][c] * f[0];
+          for (int w = 1; w < kScoreWarps; ++w) o[c] = fmaf(xa[(w * G + g) * D + CPL * lane + c], f[w], o[c]);
+        }
+        if constexpr (CPL == 4)
+          *reinterpret_cast<float4*>(dst + 4 * lane) = make_float4(o[0], o[1], o[2], o[3]);
+        else
+          *reinterpret_cast<float2*>(dst + 2 * lane) = make_float2(o[0], o[1]);
+        if (lane == 0) dst[D] = Wsum;
+      }
     }
   }
-  if (lane == 0) trace_item(a, blockIdx.x, 0, k.u, k.c, t_start, t_scored);
+  if (threadIdx.x == 0) trace_item(a, blockIdx.x, 0, k.u, k.c, t_start, t_scored);
 }
 
 // ================================================================== selection helpers
@@ -1127,7 +1177,7 @@ constexpr int kTieCap = 64;         // tie-list entries per CTA of the cluster (
 //   LSE, M [G] x 2 | counts [16] | misc [kMiscInts]
 __host__ __device__ inline int post_bitmap_words(int cpc) { return ((cpc * 2 + 3) & ~3) + 4; }
 struct PostLayout {
-  int u_words, comp, own, own_n, pick, mstage, fcp, lse, mref, cnts, misc, total_words;
+  int u_words, stg, stg_w, comp, own, own_n, pick, mstage, fcp, lse, mref, cnts, misc, bars, total_words;
 };
 __host__ __device__ inline int attend_smem_words(int D, int G) { return kAW * G * D + 2 * kAW * G + 4; }
 __host__ __device__ inline int post_items_per_rank(int D, int G, int C) { return (G * D / 4 + C - 1) / C; }
@@ -1135,7 +1185,10 @@ __host__ __device__ inline PostLayout post_layout(int D, int G, int key_stride, 
   PostLayout l;
   const int selw = kHist12 + 256 + cpc * kChunk + post_bitmap_words(cpc) + 2 * (16 * kTieCap + 4);
   const int fallback = ((sel_region_words(key_stride) + 3) & ~3) + kMiscInts;
-  int u = attend_smem_words(D, G);
+  // attention: the per-warp partials, then per warp its block's K and V rows (bf16) and z, p [kBlock][G]
+  l.stg = (attend_smem_words(D, G) + 3) & ~3;
+  l.stg_w = kBlock * D + 2 * kBlock * G;
+  int u = l.stg + kAW * l.stg_w;
   if (sel && selw > u) u = selw;
   if (sel && fallback > u) u = fallback;
   l.u_words = (u + 3) & ~3;
@@ -1149,7 +1202,8 @@ __host__ __device__ inline PostLayout post_layout(int D, int G, int key_stride, 
   l.mref = l.lse + ((G + 3) & ~3);
   l.cnts = l.mref + ((G + 3) & ~3);
   l.misc = l.cnts + 16;
-  l.total_words = l.misc + kMiscInts;
+  l.bars = l.misc + kMiscInts;  // kAW mbarriers (8 bytes each)
+  l.total_words = l.bars + 2 * kAW;
   return l;
 }
 __host__ __device__ inline int post_npick(int K, int C, bool loop) { return loop ? ((K + 8 * C - 1) / (8 * C)) * 8 : 8; }
@@ -1158,7 +1212,7 @@ __host__ __device__ inline int post_npick(int K, int C, bool loop) { return loop
 enum : int { kMT = 0, kMAbove, kMCntT, kMListN, kMTotal, kMNsel, kMBad, kMOff };
 
 template <int D, int G, int MODE, bool LOOP>
-__global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_post(LayerArgs a) {
+__global__ void __launch_bounds__(kAT, (LOOP || G >= 8) ? 1 : 2) k_post(LayerArgs a) {
   constexpr bool APPEND = (MODE & kFAppend) != 0;
   constexpr bool SEL = (MODE & kFSelect) != 0;
   constexpr bool COMP = (MODE & kFComp) != 0;
@@ -1194,6 +1248,7 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_post(LayerArgs a) {
   int* selall = reinterpret_cast<int*>(psm + lay.own);  // [C][own_n]: CTA q's selected blocks
   int* own = selall + p * lay.own_n;
   float* mstage = psm + lay.mstage;                      // [items per rank][C][8]: acc (4), m, l
+  uint64_t* pbars = reinterpret_cast<uint64_t*>(psm + lay.bars);
   int* pick = reinterpret_cast<int*>(psm + lay.pick);
   float* fcp = psm + lay.fcp;
   float* lse = psm + lay.lse;
@@ -1201,6 +1256,10 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_post(LayerArgs a) {
   int* cnts = reinterpret_cast<int*>(psm + lay.cnts);
   int* misc = reinterpret_cast<int*>(psm + lay.misc);
 
+  if (ATT && tid == 0) {
+    for (int w = 0; w < kAW; ++w) mbar_init(pbars + w, 1);
+    fence_mbar_init();
+  }
   float qr[G][V];
   if (ATT) {
     const float* qg = a.q + ((int64_t)s * a.Hkv * G + (int64_t)h * G) * D;
@@ -1237,18 +1296,17 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_post(LayerArgs a) {
   const int rec0 = chunk_record(a, s, h, 0);
   const bool all_sel = N <= K;
   const bool want_keys = SEL && (!all_sel || a.scores);
-  // zbar and sigma2 of this thread's first PF blocks, in flight during the LSE pass
-  constexpr int PF = G >= 8 ? 2 : 4;
-  float zv0[PF][G], sv0[PF][G];
-#pragma unroll
-  for (int k = 0; k < PF; ++k) {
-    const int i = tid + k * kAT, b = b_lo + i;
+  // zbar and sigma2 of this thread's first four blocks (4 tid .. 4 tid + 3, one
+  // 16-byte load per head and quantity), in flight during the LSE pass
+  float4 zv0[G], sv0[G];
+  {
+    const int i = 4 * tid, b = b_lo + i;
     const int64_t o = ((int64_t)(rec0 + b / kChunk) * G) * kChunk + (b % kChunk);
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const bool ld = want_keys && i < nown;
-      zv0[k][g] = ld ? __ldcg(a.chunk_z + o + g * kChunk) : 0.f;
-      sv0[k][g] = ld ? __ldcg(a.chunk_s + o + g * kChunk) : 0.f;
+      zv0[g] = ld ? __ldcg(reinterpret_cast<const float4*>(a.chunk_z + o + g * kChunk)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      sv0[g] = ld ? __ldcg(reinterpret_cast<const float4*>(a.chunk_s + o + g * kChunk)) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
 
@@ -1322,28 +1380,26 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_post(LayerArgs a) {
   mark(1);
   // ---- a. keys of this CTA's blocks and their histogram; the compensation share
   if (want_keys) {
-    // S_b = sum_g phat sigma2 = sum_g e^(ln|b| + zbar + sigma2/2 - LSE_g) sigma2
-    for (int i0 = tid; i0 < nown; i0 += PF * kAT) {
-      float zv[PF][G], sv[PF][G];
+    // S_b = sum_g phat sigma2 = sum_g e^(ln|b| + zbar + sigma2/2 - LSE_g) sigma2, four blocks per thread
+    for (int i0 = 4 * tid; i0 < nown; i0 += 4 * kAT) {
+      float zv[G][4], sv[G][4];
+      const int b0 = b_lo + i0;
+      const int64_t o = ((int64_t)(rec0 + b0 / kChunk) * G) * kChunk + (b0 % kChunk);
 #pragma unroll
-      for (int k = 0; k < PF; ++k) {
-        const int i = i0 + k * kAT, b = b_lo + i;
-        const int64_t o = ((int64_t)(rec0 + b / kChunk) * G) * kChunk + (b % kChunk);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const bool ld = i0 != tid && i < nown;
-          zv[k][g] = i0 == tid ? zv0[k][g] : (ld ? __ldcg(a.chunk_z + o + g * kChunk) : 0.f);
-          sv[k][g] = i0 == tid ? sv0[k][g] : (ld ? __ldcg(a.chunk_s + o + g * kChunk) : 0.f);
-        }
+      for (int g = 0; g < G; ++g) {
+        const float4 z4 = i0 == 4 * tid ? zv0[g] : __ldcg(reinterpret_cast<const float4*>(a.chunk_z + o + g * kChunk));
+        const float4 s4 = i0 == 4 * tid ? sv0[g] : __ldcg(reinterpret_cast<const float4*>(a.chunk_s + o + g * kChunk));
+        zv[g][0] = z4.x; zv[g][1] = z4.y; zv[g][2] = z4.z; zv[g][3] = z4.w;
+        sv[g][0] = s4.x; sv[g][1] = s4.y; sv[g][2] = s4.z; sv[g][3] = s4.w;
       }
 #pragma unroll
-      for (int k = 0; k < PF; ++k) {
-        const int i = i0 + k * kAT, b = b_lo + i;
+      for (int k = 0; k < 4; ++k) {
+        const int i = i0 + k, b = b0 + k;
         if (i >= nown) break;
         const float lnn = ln_n(b == N - 1 ? L - kBlock * b : kBlock);
         float S = 0.f;
 #pragma unroll
-        for (int g = 0; g < G; ++g) S = fmaf(expf(lnn + zv[k][g] + 0.5f * sv[k][g] - lse[g]), sv[k][g], S);
+        for (int g = 0; g < G; ++g) S = fmaf(__expf(lnn + zv[g][k] + 0.5f * sv[g][k] - lse[g]), sv[g][k], S);
         S = fmaxf(S, 0.f);
         const uint32_t key = __float_as_uint(S);
         keys[i] = key;
@@ -1671,44 +1727,42 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_post(LayerArgs a) {
   const int idx = lane & (P - 1);
   const int jj = idx / G, gl = idx % G;
   const int rounds = LOOP ? npick / 8 : 1;
+  // this warp's staging: the block's K and V rows (bf16 pairs as words), then z and p [kBlock][G]
+  uint32_t* wk = reinterpret_cast<uint32_t*>(psm + lay.stg + warp * lay.stg_w);
+  uint32_t* wv = wk + kBlock * D / 2;
+  float* wz = reinterpret_cast<float*>(wv + kBlock * D / 2);
+  float* wp = wz + kBlock * G;
+  uint32_t ph = 0u;
+  const int hg = lane % G;  // the head of this lane's softmax entries (lane, lane + 32, ...)
   for (int it = 0; it < rounds; ++it) {
     const int b = pick[8 * it + warp];
     if (b < 0) continue;  // warp-uniform
     const int n = (b == N - 1) ? L - kBlock * b : kBlock;
     const int64_t row = row_of(a, s, h, b);
-    const unsigned* kp = reinterpret_cast<const unsigned*>(a.k + row * kBlock * D + lane * V);
-    const unsigned* vp = reinterpret_cast<const unsigned*>(a.v + row * kBlock * D + lane * V);
-    // every load of the block up front: keys, values, its mean value and zbar
-    unsigned raw[kBlock][W], rawv[kBlock][W];
-#pragma unroll
-    for (int j = 0; j < kBlock; ++j) {
-      if (W == 2) {
-        const uint2 w2 = __ldcg(reinterpret_cast<const uint2*>(kp + j * (D / 2)));
-        raw[j][0] = w2.x;
-        raw[j][W - 1] = w2.y;
-        const uint2 x2 = __ldcg(reinterpret_cast<const uint2*>(vp + j * (D / 2)));
-        rawv[j][0] = x2.x;
-        rawv[j][W - 1] = x2.y;
-      } else {
-        raw[j][0] = __ldcg(kp + j * (D / 2));
-        rawv[j][0] = __ldcg(vp + j * (D / 2));
-      }
+    __syncwarp();  // the staging's previous contents are read
+    if (lane == 0) {
+      mbar_arrive_expect_tx(pbars + warp, 2u * kBlock * D * 2u);
+      bulk_g2s(wk, a.k + row * kBlock * D, kBlock * D * 2u, pbars + warp);
+      bulk_g2s(wv, a.v + row * kBlock * D, kBlock * D * 2u, pbars + warp);
     }
     const int rec = chunk_record(a, s, h, b / kChunk);
     float vb[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) vb[i] = comp ? __ldcg(a.vbar + row * D + lane * V + i) : 0.f;
     const float zb_lane = (comp && lane < G) ? __ldcg(a.chunk_z + ((int64_t)rec * G + lane) * kChunk + (b % kChunk)) : 0.f;
-    float zl[NG];
-#pragma unroll
+    mbar_wait_bounded(pbars + warp, ph, a.status, s, h, 62);
+    ph ^= 1u;
+    // z = q . k / sqrt(d) of the block's tokens, TG tokens at a time (lanes hold V coordinates)
+#pragma unroll 1
     for (int gi = 0; gi < NG; ++gi) {
       float part[P];
 #pragma unroll
       for (int t = 0; t < TG; ++t) {
+        const uint32_t* kr = wk + (gi * TG + t) * (D / 2) + lane * W;
         float kf[V];
 #pragma unroll
         for (int w = 0; w < W; ++w) {
-          const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&raw[gi * TG + t][w]));
+          const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(kr + w));
           kf[2 * w] = x.x;
           kf[2 * w + 1] = x.y;
         }
@@ -1720,15 +1774,20 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_post(LayerArgs a) {
           part[t * G + g] = acc_t;
         }
       }
-      zl[gi] = transpose_reduce_warp<P>(part, lane);
+      const float z = transpose_reduce_warp<P>(part, lane);
+      if (lane < P) wz[(gi * TG + jj) * G + gl] = z;
     }
-    // the block's max per head, the running max, the rescale of the running sums
+    __syncwarp();
+    // per head: the block's max, the running max and the rescale, p = e^(z - max) and its sum
+    constexpr int EPL = (kBlock * G + 31) / 32;  // softmax entries per lane
     float zmax = -INFINITY;
 #pragma unroll
-    for (int gi = 0; gi < NG; ++gi)
-      if (gi * TG + jj < n) zmax = fmaxf(zmax, zl[gi]);
+    for (int k = 0; k < EPL; ++k) {
+      const int e = lane + 32 * k;
+      if (e < kBlock * G && e / G < n) zmax = fmaxf(zmax, wz[e]);
+    }
 #pragma unroll
-    for (int o = G; o < P; o <<= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
+    for (int o = G; o < 32; o <<= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
     float mlane = -INFINITY;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -1738,37 +1797,41 @@ __global__ void __launch_bounds__(kAT, LOOP ? 1 : 2) k_post(LayerArgs a) {
       l[g] *= f;
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[g][i] *= f;
-      if (g == gl) mlane = mn;
+      if (g == hg) mlane = mn;
     }
-    float pl[NG];
     float psum = 0.f;
 #pragma unroll
-    for (int gi = 0; gi < NG; ++gi) {
-      pl[gi] = (gi * TG + jj < n) ? __expf(zl[gi] - mlane) : 0.f;
-      psum += pl[gi];
+    for (int k = 0; k < EPL; ++k) {
+      const int e = lane + 32 * k;
+      if (e < kBlock * G) {
+        const float pe = e / G < n ? __expf(wz[e] - mlane) : 0.f;
+        wp[e] = pe;
+        psum += pe;
+      }
     }
 #pragma unroll
-    for (int o = G; o < P; o <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
+    for (int o = G; o < 32; o <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
 #pragma unroll
     for (int g = 0; g < G; ++g) l[g] += __shfl_sync(0xffffffffu, psum, g);
+    __syncwarp();
+    // acc += p v over the block's tokens
+#pragma unroll 2
+    for (int t = 0; t < n; ++t) {
+      const uint32_t* vr = wv + t * (D / 2) + lane * W;
+      float vf[V];
 #pragma unroll
-    for (int gi = 0; gi < NG; ++gi) {
-#pragma unroll
-      for (int t = 0; t < TG; ++t) {
-        float vf[V];
-#pragma unroll
-        for (int w = 0; w < W; ++w) {
-          const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rawv[gi * TG + t][w]));
-          vf[2 * w] = x.x;
-          vf[2 * w + 1] = x.y;
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          const float pg = __shfl_sync(0xffffffffu, pl[gi], t * G + g);
-#pragma unroll
-          for (int i = 0; i < V; ++i) acc[g][i] = fmaf(pg, vf[i], acc[g][i]);
-        }
+      for (int w = 0; w < W; ++w) {
+        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vr + w));
+        vf[2 * w] = x.x;
+        vf[2 * w + 1] = x.y;
       }
+      float pg[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) pg[g] = wp[t * G + g];
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int i = 0; i < V; ++i) acc[g][i] = fmaf(pg[g], vf[i], acc[g][i]);
     }
     if (comp) {
       // remove this block's own compensation term, which the compensation shares hold for every block
@@ -1932,7 +1995,7 @@ static cudaError_t launch_chain(const LayerArgs& a_in, cudaStream_t st, int firs
     const void* fn = reinterpret_cast<const void*>(&k_score<D, G, MODE>);
     if ((e = ensure_smem(fn, cfg1, sm)) != cudaSuccess) return e;
     if (ev && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return e;
-    if ((e = launch_pdl(fn, dim3(a.total_chunks), sm, st, first_pdl != 0, args, 32)) != cudaSuccess) return e;
+    if ((e = launch_pdl(fn, dim3(a.total_chunks), sm, st, first_pdl != 0, args, 32 * kScoreWarps)) != cudaSuccess) return e;
     if (ev && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return e;
   }
   // 2. select + attend: a cluster of a.splits CTAs per unit

@@ -231,20 +231,19 @@ compkv_status compkv_profile_enable(compkv_ctx *ctx, int enable);
  * words 1 + 8 i .. 8 + 8 i, for i < (bytes - 8) / 64 (slots beyond are not
  * written):
  *   (cta << 32 | type << 24 | index), unit, t0, t1, t2, x0, x1, x2
- * (times in %globaltimer ns, t2 = when the record was written; unit =
- * sequence * Hkv + head).  With C scoring CTAs (64 blocks each), S S items
- * (512 blocks each), U units and A attention CTAs (U times the cluster size),
- * slots [0, C) hold the scoring CTAs (type 0, index = chunk: t0 start, t1 its
- * summaries and zbar, sigma2 done; x0 start, x1 its k-bar rows landed, x2
- * its zbar tile computed), [C, C + S) the S items (type 7, index = item of
- * the unit: t0 start, t1 end of the wait for the scoring kernel), slots
- * [C + S, C + S + U) are reserved, then the attention CTAs (type 1, or 4 for
- * cluster rank 0: index = rank, t0 start, t1 end of the wait for the S items,
- * x0 its attention partial computed, x1 the compensation sums read), then 32
- * per unit for the selection's phases (type 5: index = phase, t0..t1 its span;
- * type 6, written by the general radix path only: index = radix level, t0 =
- * keys at the threshold digit, t1 = list length or -1).  A slot a call does
- * not use stays as the caller left it.
+ * (t2 = %globaltimer ns when the record was written; unit = sequence * Hkv +
+ * head).  With C scoring CTAs (64 blocks each) and U units of S CTAs each
+ * (S = min(16, ceil(K / 8)), one cluster per unit), slots [0, C) hold the scoring CTAs (type 0, index = item of the
+ * layer: t0 start, t1 its blocks scored, in %globaltimer ns), slots
+ * [C, C + U S) the CTAs after the scoring (type 1, or 4 for cluster rank
+ * 0: index = rank; t0 start, t1 end of the wait for the scoring kernel, x0 the
+ * selection known, x1 the attention done, in %globaltimer ns), then 32 per
+ * unit: phase marks of rank 0 (type 5, index = phase: t0, t1 = SM clock
+ * counter at the previous mark and at this one; the full radix selection, a
+ * rare path, writes its own type 5 marks there in %globaltimer ns) and, at
+ * slot 16, the threshold bin's tie list (type 6: t0 = listed entries, t1 =
+ * entries still needed, x0 = keys in the threshold bin, x1 = keys above it).
+ * A slot a call does not use stays as the caller left it.
  * buf = NULL switches tracing off. */
 compkv_status compkv_trace(compkv_ctx *ctx, void *buf, size_t bytes);
 compkv_status compkv_profile_read(compkv_ctx *ctx, int family, double *total_ms, int64_t *launches);
