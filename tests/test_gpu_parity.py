@@ -85,6 +85,16 @@ def test_budgets_and_forced_only(budget):
         check_step(run, 0, sel, out, res)
 
 
+def test_budget_above_one_round():
+    # K = 256 blocks: 16 CTAs per unit, each attends two rounds of 8 blocks
+    wl = _ragged(SHAPES[1], lengths=(5, 1800, 9000), budget=4096, steps=3)
+    run = Run(wl)
+    for step in range(wl.steps):
+        q, sel, out, res = run.decode_step(0)
+        check_step(run, 0, sel, out, res)
+    assert run.cache.device_status() == 0
+
+
 def test_score_select_api_scores():
     wl = _ragged(SHAPES[1], lengths=(70, 3000, 5000), budget=256, steps=2)
     run = Run(wl)
