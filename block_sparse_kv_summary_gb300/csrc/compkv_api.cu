@@ -268,7 +268,7 @@ compkv_status launch(compkv_ctx* c, int family, cudaStream_t st, const char* wha
   return COMPKV_OK;
 }
 
-// A decode-step chain (three kernels).  While profiling is on, each kernel is
+// A decode-step chain (two kernels).  While profiling is on, each kernel is
 // bracketed by its own events too (COMPKV_KERNEL_K_SCORE, _K_POST); the
 // whole call goes under `family`.
 compkv_status launch_chain(compkv_ctx* c, int family, const LayerArgs& a, int mode, cudaStream_t st, const char* what) {

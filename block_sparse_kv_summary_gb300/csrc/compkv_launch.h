@@ -19,18 +19,18 @@ enum FusedFlags : int {
 constexpr int kFusedDecode = kFAppend | kFScore | kFComp | kFSelect | kFAttend;
 constexpr int kFusedScoreSelect = kFScore | kFSelect;
 constexpr int kFusedAttend = kFComp | kFAttend;
-constexpr int kAttendBlocks = 8;  // selected blocks per attention CTA and round (one per warp)
+constexpr int kAttendBlocks = 8;  // selected blocks per CTA of a unit's cluster and round (one per warp)
 
 cudaError_t launch_prefill(const LayerArgs& a, int64_t rows_per_layer, cudaStream_t st);
 cudaError_t launch_append(const LayerArgs& a, cudaStream_t st);
 
-// The decode step as a chain of three kernels on `st` (score with the
-// compensation partials; S items; select and attend), chained with
-// programmatic dependent launch.  `mode` is one of
+// The decode step as a chain of two kernels on `st` (score with the
+// compensation partials; select and attend), chained with programmatic
+// dependent launch.  `mode` is one of
 // kFusedDecode, kFusedScoreSelect (score, select) or kFusedAttend (score for
 // zbar, compensation, attend a caller-given selection).  `first_pdl` lets the
 // first kernel overlap the tail of the previous work on the stream.
-// `ev`: null, or six events recorded before and after each of the three kernels.
+// `ev`: null, or four events recorded before and after each of the two kernels.
 cudaError_t launch_decode_chain(const LayerArgs& a, int mode, cudaStream_t st, int first_pdl, cudaEvent_t* ev = nullptr);
 // Kernels a chain of `mode` launches.
 inline int chain_kernels(int mode) { return 2; }

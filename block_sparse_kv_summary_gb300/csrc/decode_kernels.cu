@@ -1,4 +1,4 @@
-// The CompKV decode step (onedev.kr/papers/157) as three kernels chained with
+// The CompKV decode step (onedev.kr/papers/157) as two kernels chained with
 // programmatic dependent launch.
 //
 // Section "무엇과 다른가" of the CompKV page defines the step per (sequence,
@@ -8,31 +8,20 @@
 // normaliser.  Section "어떻게 쓰나" fuses the open block's summary update
 // with the K/V pack; here that happens in the first kernel.
 //
-//   1. score   one CTA per item of 64 blocks: kbar, Dbar and the unit's
-//              queries staged by 1-D bulk copies (cp.async.bulk, mbarrier) in
-//              two halves; zbar = q.kbar/sqrt(d), sigma2 = (1/d) sum_t
-//              Qsq_t Dbar_t, a = ln|b| + zbar + sigma2/2; per query head the
-//              item's max a, sum e^(a - max a), max(ln|b| + zbar), and per
-//              block u = e^(a - max a) sigma2 and zbar.  The item holding the
-//              newest token appends it first.
-//   2a. S items    one CTA per 512 blocks of a unit: LSE_g from the scoring
-//              records, S_b = sum_g u e^(max a - LSE_g) = sum_g phat sigma2 as
-//              order-preserving keys, a histogram of their top 12 bits.
-//   2b. select     one CTA per unit: the threshold bin of the K-3 largest
-//              candidates from the histogram, one pass over the unit's keys
-//              for the selection bitmap and the threshold bin's short list,
-//              which is ranked (ties to the lower index); the ascending
-//              selection from the bitmap.
-//      comp items  in the same grid, one CTA per 128 blocks of a unit: their
-//              vbar rows (bulk-copied before the dependency wait, overlapping
-//              the scoring kernel's tail) weighted by w = e^(ln|b| + zbar -
-//              M_g), M_g = max_b (ln|b| + zbar), summed into the unit's
-//              accumulator (fp32 atomics) -- over every block.
-//   3. attend  one CTA per 8 selected blocks: exact softmax terms of their
-//              tokens (one block per warp), minus each selected block's own
-//              compensation term (it was summed for every block in 2), as a
-//              partial (m, l, acc); the last CTA of the unit merges the
-//              partials with the compensation sum into out = acc / l.
+//   1. k_score  one CTA (two warps) per item of 64 blocks: the item's kbar,
+//              vbar and Dbar rows streamed through a 3-stage pipeline of 1-D
+//              bulk copies (cp.async.bulk, mbarrier); zbar = q.kbar/sqrt(d),
+//              sigma2 = (1/d) sum_t Qsq_t Dbar_t, a = ln|b| + zbar + sigma2/2;
+//              per block zbar and sigma2, per query head the item's max a,
+//              sum e^(a - max a), max(ln|b| + zbar) and the compensation sums
+//              sum_b w vbar_b, w = e^(ln|b| + zbar - that max).  The item
+//              holding the newest token appends it first.
+//   2. k_post   one thread-block cluster per unit: LSE_g, S_b = sum_g phat
+//              sigma2 as order-preserving keys, the forced set and Top-K
+//              (a cluster-wide histogram threshold, ties ranked exactly),
+//              exact attention over the selected blocks (one per warp) minus
+//              their own compensation terms, the compensation sums of every
+//              block, and the cluster merge into out = acc / l.
 // By Jensen, sum_{j in b} e^{z_j} >= |b| e^{zbar_b}, so removing a selected
 // block's mean term never makes a denominator negative.  If every block is
 // selected the compensation is skipped (the step is dense attention).
@@ -47,7 +36,7 @@ constexpr int kW = kT / 32;
 constexpr int kPrivBins = 256;     // histogram bins of one radix digit
 constexpr int kListMax = 2048;     // keys in play compacted into a list once at most this many
 constexpr int kRankMax = 512;      // listed keys in play ranked directly once at most this many
-constexpr int kDigitShift = 19;      // the classify digit: key bits 30..19 (exponent, 4 mantissa bits)
+constexpr int kDigitShift = 19;      // the histogram digit: key bits 30..19 (exponent, 4 mantissa bits)
 constexpr int kHist12 = 1 << (31 - kDigitShift);
 
 template <int D>
@@ -766,8 +755,8 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int* scratch, int* tota
   return base + incl - v;
 }
 
-// Selection for unit u by its last S item: the unit's keys (S_b as
-// order-preserving bits, S_b >= 0) and the exponent histogram of the
+// Selection for unit u by one CTA: the unit's keys (S_b as
+// order-preserving bits, S_b >= 0) and the 12-bit histogram of the
 // candidates 1..N-3 are complete in global memory.  The selected set is a
 // bitmap; radix select: the exponent digit from the histogram, then 8/8/7
 // mantissa bits over the keys still in play (compacted into a list when they
@@ -1053,12 +1042,9 @@ __device__ __forceinline__ void select_unit(const LayerArgs& a, int u, int s, in
   if (tid == 0) tp = trace_phase(a, u, pk++, 4, tp);
 }
 
-// S items kernel: blocks [512 i, 512 i + 512) of a unit.  From the unit's
-// scoring records: LSE_g and M_g = max_b (ln|b| + zbar).  With the selection:
-// S_b keys of its blocks and the histogram of the top 12 key bits (exponent
-// and 4 mantissa bits) of the candidates 1..N-3, summed into the unit's.
-// With the compensation: its 8 chunks' partial sums rescaled from their own
-// reference to M_g and added to the unit's accumulator (item 0 records M_g).
+// Transposed reduction of NVAL per-lane values over the warp: at each step a
+// lane keeps half of its values and adds its partner's share of that half;
+// lane j ends with the total of value index idx (the bits of j select it).
 template <int NVAL, int LPB>
 __device__ __forceinline__ float transpose_reduce_lanes(float (&v)[NVAL], int j, int& idx) {
   idx = 0;
