@@ -198,7 +198,7 @@ int64_t compkv_launch_count(const compkv_ctx *ctx);
 
 /* Per-kernel timing (tracing aid, off by default).  enable = 1: every API
  * call that launches kernels is bracketed by two CUDA events on the launch
- * stream; enable = 2: in addition each kernel of a three-kernel chain is
+ * stream; enable = 2: in addition each kernel of a two-kernel chain is
  * bracketed on its own (the events between them stop a kernel from launching
  * early behind its predecessor, so chains run slower); 0 switches it off;
  * other values give COMPKV_ERR_INVALID_ARG.  compkv_profile_read() synchronises on the recorded events and
