@@ -128,6 +128,9 @@ class CompKVCache:
     def device_status(self) -> int:
         return C.compkv_device_status(self.ctx, _stream(self.device))
 
+    def selftest_wait_timeout(self):
+        C.compkv_selftest_wait_timeout(self.ctx, _stream(self.device))
+
     def launch_count(self) -> int:
         return C.compkv_launch_count(self.ctx)
 

@@ -57,6 +57,7 @@ _SIGNATURES = [
                                      c_void_p, c_void_p, c_void_p, c_void_p]),
     ("compkv_device_status", c_int, [c_void_p, c_void_p]),
     ("compkv_launch_count", c_int64, [c_void_p]),
+    ("compkv_selftest_wait_timeout", c_int, [c_void_p, c_void_p]),
     ("compkv_profile_enable", c_int, [c_void_p, c_int]),
     ("compkv_trace", c_int, [c_void_p, c_void_p, c_size_t]),
     ("compkv_profile_read", c_int, [c_void_p, c_int, POINTER(ctypes.c_double), POINTER(c_int64)]),
@@ -168,6 +169,11 @@ def compkv_decode_static(cfg, bufs, layer, q, k_new, v_new, out, sel, stream):
 def compkv_device_status(ctx, stream) -> int:
     """Synchronise, read and clear the device status word; returns the status code."""
     return lib().compkv_device_status(ctx, stream)
+
+
+def compkv_selftest_wait_timeout(ctx, stream):
+    """Enqueue the bounded-wait self-test (its wait runs out and records a timeout)."""
+    _check(lib().compkv_selftest_wait_timeout(ctx, stream), "compkv_selftest_wait_timeout")
 
 
 def compkv_launch_count(ctx) -> int:

@@ -442,6 +442,15 @@ compkv_status compkv_device_status(compkv_ctx* c, void* stream) {
 
 int64_t compkv_launch_count(const compkv_ctx* c) { return c ? c->launches : 0; }
 
+compkv_status compkv_selftest_wait_timeout(compkv_ctx* c, void* stream) {
+  if (!c) return fail(COMPKV_ERR_INVALID_ARG, "context is NULL");
+  cudaStream_t st = (cudaStream_t)stream;
+  int* dev = reinterpret_cast<int*>(reinterpret_cast<char*>(c->buf.scratch) + c->lay.off_status);
+  COMPKV_TRY(cuda_status(launch_wait_selftest(dev, st), "wait self-test launch"));
+  c->launches += 1;
+  return COMPKV_OK;
+}
+
 compkv_status compkv_trace(compkv_ctx* c, void* buf, size_t bytes) {
   if (!c) return fail(COMPKV_ERR_INVALID_ARG, "context is NULL");
   if (!buf) {

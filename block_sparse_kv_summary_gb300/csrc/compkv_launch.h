@@ -23,6 +23,8 @@ constexpr int kAttendBlocks = 8;  // selected blocks per CTA of a unit's cluster
 
 cudaError_t launch_prefill(const LayerArgs& a, int64_t rows_per_layer, cudaStream_t st);
 cudaError_t launch_append(const LayerArgs& a, cudaStream_t st);
+// One bounded mbarrier wait that runs out and records kDevTimeout in `status`.
+cudaError_t launch_wait_selftest(int* status, cudaStream_t st);
 
 // The decode step as a chain of two kernels on `st` (score with the
 // compensation partials; select and attend), chained with programmatic

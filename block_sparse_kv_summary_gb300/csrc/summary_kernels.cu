@@ -74,6 +74,23 @@ cudaError_t launch_prefill(const LayerArgs& a, int64_t rows_per_layer, cudaStrea
   return cudaGetLastError();
 }
 
+// A bounded wait that runs out: one thread waits on an mbarrier whose
+// transaction (16 bytes posted, never delivered) nothing completes; the wait
+// gives up after its poll cap and records kDevTimeout in `status`.
+__global__ void wait_selftest_kernel(int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  mbar_arrive_expect_tx(&bar, 16u);
+  mbar_wait_bounded(&bar, 0u, status, -1, -1, 90);
+}
+
+cudaError_t launch_wait_selftest(int* status, cudaStream_t st) {
+  wait_selftest_kernel<<<1, 32, 0, st>>>(status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_append(const LayerArgs& a, cudaStream_t st) {
   const int threads = 32 * a.Hkv;
   if (a.d == 128)

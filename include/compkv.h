@@ -193,6 +193,12 @@ compkv_status compkv_decode_static(const compkv_config *cfg, const compkv_buffer
  * COMPKV_OK or the first device-side error since the last call. */
 compkv_status compkv_device_status(compkv_ctx *ctx, void *stream);
 
+/* Failure-path self-test: enqueues one kernel whose bounded wait on an
+ * mbarrier that nothing completes runs out (after its poll cap; no trap, no
+ * hang) and records COMPKV_ERR_TIMEOUT in the context's status word, which
+ * compkv_device_status() then returns (and clears).  Touches nothing else. */
+compkv_status compkv_selftest_wait_timeout(compkv_ctx *ctx, void *stream);
+
 /* Kernel launches enqueued by this context since compkv_init (host counter). */
 int64_t compkv_launch_count(const compkv_ctx *ctx);
 

@@ -184,6 +184,24 @@ def test_device_errors_are_reported():
         run.cache.attend(0, q[:, :1], sel)
 
 
+def test_bounded_wait_timeout_is_reported():
+    """A device wait that nothing completes gives up after its poll cap: the
+    context's status word reads COMPKV_ERR_TIMEOUT (5), the read clears it, and
+    the context keeps working."""
+    import time
+    wl = _ragged(SHAPES[0], lengths=(30, 40), budget=64, steps=1)
+    run = Run(wl)
+    t0 = time.perf_counter()
+    run.cache.selftest_wait_timeout()
+    assert run.cache.device_status() == 5
+    waited = time.perf_counter() - t0
+    assert run.cache.device_status() == 0
+    q, sel, out, res = run.decode_step(0)
+    check_step(run, 0, sel, out, res)
+    assert run.cache.device_status() == 0
+    print(f"bounded wait gave up after {waited:.3f} s")
+
+
 @pytest.mark.parametrize("pattern", ["all_equal", "two_kinds"])
 def test_selection_ties_go_to_the_lower_index(pattern):
     """Blocks with identical tokens have identical summaries and scores (on both
