@@ -373,8 +373,8 @@ def main():
                    "step_frac_of_peak": step_gbs / peak,
                    "bytes_per_step": by},
         "roofline": {"bound": "hbm",
-                     "kernel": "k_score<128,4,decode> (one warp per 64-block chunk: append, kbar/Dbar/vbar "
-                               "bulk-copy stream, zbar, sigma2, chunk LSE records, compensation partials)",
+                     "kernel": "k_score<128,4,decode> (two warps per 64-block item: append, kbar/Dbar/vbar "
+                               "bulk-copy stream, zbar, sigma2, item LSE records, compensation partials)",
                      "achieved": ks_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": ks_gbs / peak, "traffic": traffic,
                      "algorithmic_bytes_per_launch": by["score_kernel"], "avg_launch_us": ks_us},
