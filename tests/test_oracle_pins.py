@@ -441,3 +441,57 @@ def test_boundary_gap():
     assert O.boundary_gap(S, 4) == pytest.approx(0.25)      # 4 selected, 3 first rejected
     assert O.boundary_gap(S, 5) == pytest.approx(1 / 3)
     assert O.boundary_gap(S, 7) == math.inf
+
+
+# ---------------------------------------------------------------------------
+# The two reference helpers of "어떻게 동작하나": dense softmax attention and
+# the token-level distribution of Mean compensation.
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("L", [1, 16, 40, 130])
+def test_dense_attention_pins(L):
+    rng = np.random.default_rng(100 + L)
+    d, G = 16, 3
+    K, V = rand_cache(rng, L, d)
+    q = rng.standard_normal((G, d)) * 2
+    # a library routine: scipy's softmax over the scaled logits
+    ref = sp_softmax(q @ K.T / math.sqrt(d), axis=1) @ V
+    np.testing.assert_allclose(O.dense_attention(q, K, V), ref, rtol=1e-12, atol=1e-13)
+    # identical keys: every weight is 1/L, the output is the mean value
+    Kc = np.repeat(K[:1], L, axis=0)
+    np.testing.assert_allclose(O.dense_attention(q, Kc, V), np.repeat(V.mean(axis=0)[None], G, axis=0),
+                               rtol=1e-12, atol=1e-13)
+    # one key far ahead of the others: the output is that key's value
+    if L > 1:
+        j = L // 2
+        Kp = K.copy()
+        Kp[j] = q[0] / np.linalg.norm(q[0]) * 200 * math.sqrt(d)
+        np.testing.assert_allclose(O.dense_attention(q[:1], Kp, V)[0], V[j], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("sel", [[0, 3], [1], [0, 2, 4], [4], [0, 1, 2, 3, 4]])
+def test_compensated_token_distribution_pins(sel):
+    rng = np.random.default_rng(47)
+    L, d, r = 75, 8, 2
+    K, V = rand_cache(rng, L, d, scale=0.7)
+    qg = rng.standard_normal(d) * 1.5
+    p_ref, p = _token_level_compensated(qg, K, L, sel)
+    pc = O.compensated_token_distribution(qg, K, L, sel)
+    # an independent construction through scipy's softmax
+    np.testing.assert_allclose(pc, p_ref, rtol=1e-12, atol=1e-15)
+    assert abs(pc.sum() - 1.0) < 1e-12
+    # its KL divergence from the token softmax is the closed-form selection loss
+    np.testing.assert_allclose(O.kl_divergence(pc, p), O.selection_loss_closed_form(qg, K, L, sel), rtol=1e-10)
+    # its expectation of the values is the compensated attention output
+    n, kbar, Dbar, vbar = O.block_summaries(K, V, r)
+    out = O.compkv_attend(qg[None], K, V, sel, n, kbar, vbar)[0]
+    np.testing.assert_allclose(pc @ V, out, rtol=1e-12, atol=1e-13)
+    # without compensation: the softmax restricted to the selected blocks, and
+    # KL = -ln (exact mass of the selected blocks)
+    pn = O.compensated_token_distribution(qg, K, L, sel, compensate=False)
+    logZ, _, _, pm = O.exact_block_stats(qg, K, L)
+    np.testing.assert_allclose(O.kl_divergence(pn, p), -math.log(sum(pm[b] for b in sel)), rtol=1e-10, atol=1e-14)
+    nb = O.block_counts(L)
+    outside = np.ones(L, dtype=bool)
+    for b in sel:
+        outside[16 * b:16 * b + nb[b]] = False
+    assert np.all(pn[outside] == 0.0)
