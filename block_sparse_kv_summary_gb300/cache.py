@@ -24,7 +24,7 @@ class CompKVCache:
     """
 
     def __init__(self, *, num_layers, batch, num_kv_heads, group_size, head_dim, r,
-                 budget_tokens, capacity_tokens, device="cuda"):
+                 budget_tokens, capacity_tokens, device="cuda", variant=0):
         self.device = torch.device(device)
         if self.device.type != "cuda":
             raise RuntimeError("CompKVCache lives in GPU memory; the library has no CPU path")
@@ -32,7 +32,8 @@ class CompKVCache:
             self.device = torch.device("cuda", torch.cuda.current_device())
         caps = [capacity_tokens] * batch if isinstance(capacity_tokens, int) else list(capacity_tokens)
         self.cfg = C.make_config(num_layers, batch, num_kv_heads, group_size, head_dim, r,
-                                 budget_tokens, capacity_tokens=caps)
+                                 budget_tokens, capacity_tokens=caps, variant=variant)
+        self.variant = variant
         self.num_layers, self.batch, self.Hkv, self.G = num_layers, batch, num_kv_heads, group_size
         self.d, self.r, self.K = head_dim, r, budget_tokens // BLOCK
         self.caps = caps
@@ -123,6 +124,22 @@ class CompKVCache:
         C.compkv_decode(self.ctx, layer, self._q(q), self._kv(k_new, "k_new"), self._kv(v_new, "v_new"),
                         self._t(out, "out", torch.float32, (self.batch, self.Hkv * self.G, self.d)),
                         sp, _stream(self.device))
+        return out
+
+    def prepared_decode(self):
+        """A compkv_decode bound to this cache's context and the current stream:
+        call it with (layer, q_ptr, k_ptr, v_ptr, out_ptr, sel_ptr) as plain
+        device addresses; no per-call tensor checks."""
+        return C.PreparedDecode(self.ctx, _stream(self.device))
+
+    def decode_host(self, layer, q, k_new, v_new, out, sel=None):
+        """compkv_decode_host on page-locked CPU tensors (q fp32 [B][Hq][d],
+        k_new/v_new bf16 [B][Hkv][d], out fp32 [B][Hq][d]); returns when out is filled."""
+        for t, name in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (out, "out")):
+            if t.device.type != "cpu" or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous CPU tensor")
+        C.compkv_decode_host(self.ctx, layer, q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), out.data_ptr(),
+                             0 if sel is None else sel.data_ptr(), _stream(self.device))
         return out
 
     def device_status(self) -> int:

@@ -25,7 +25,13 @@ class compkv_config(ctypes.Structure):
     _fields_ = [("num_layers", c_int), ("batch", c_int), ("num_kv_heads", c_int),
                 ("group_size", c_int), ("head_dim", c_int), ("block_size", c_int),
                 ("r", c_int), ("budget_tokens", c_int), ("max_tokens", c_int),
-                ("capacity_tokens", POINTER(c_int))]
+                ("capacity_tokens", POINTER(c_int)), ("variant", c_int)]
+
+
+# ablation bits of compkv_config.variant (include/compkv.h)
+VARIANT_FIRST_ORDER_MASS = 1
+VARIANT_NO_VARIANCE_FACTOR = 2
+VARIANT_NO_COMPENSATION = 4
 
 
 class compkv_buffers(ctypes.Structure):
@@ -53,6 +59,7 @@ _SIGNATURES = [
     ("compkv_score_select", c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
     ("compkv_attend", c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
     ("compkv_decode", c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
+    ("compkv_decode_host", c_int, [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p]),
     ("compkv_decode_static", c_int, [POINTER(compkv_config), POINTER(compkv_buffers), c_int, c_void_p, c_void_p,
                                      c_void_p, c_void_p, c_void_p, c_void_p]),
     ("compkv_device_status", c_int, [c_void_p, c_void_p]),
@@ -104,9 +111,9 @@ def _check(status: int, what: str):
 
 
 def make_config(num_layers, batch, num_kv_heads, group_size, head_dim, r, budget_tokens,
-                max_tokens=0, capacity_tokens=None, block_size=16) -> compkv_config:
+                max_tokens=0, capacity_tokens=None, block_size=16, variant=0) -> compkv_config:
     cfg = compkv_config(num_layers, batch, num_kv_heads, group_size, head_dim, block_size, r,
-                        budget_tokens, max_tokens, None)
+                        budget_tokens, max_tokens, None, variant)
     if capacity_tokens is not None:
         arr = (c_int * len(capacity_tokens))(*capacity_tokens)
         cfg.capacity_tokens = ctypes.cast(arr, POINTER(c_int))
@@ -156,6 +163,27 @@ def compkv_decode(ctx, layer, q, k_new, v_new, out, sel, stream):
     _check(lib().compkv_decode(ctx, layer, q, k_new, v_new, out, sel, stream), "compkv_decode")
 
 
+def compkv_decode_host(ctx, layer, q, k_new, v_new, out, sel, stream):
+    """compkv_decode from host buffers to host buffers (addresses of host memory); synchronises."""
+    _check(lib().compkv_decode_host(ctx, layer, q, k_new, v_new, out, sel, stream), "compkv_decode_host")
+
+
+class PreparedDecode:
+    """compkv_decode with the context and stream bound once: each call passes
+    plain addresses (ints) and pays only the ctypes call and the library's own
+    checks."""
+
+    def __init__(self, ctx, stream):
+        self._fn = lib().compkv_decode
+        self._ctx = c_void_p(ctx)
+        self._stream = c_void_p(stream)
+
+    def __call__(self, layer, q, k_new, v_new, out, sel=None):
+        st = self._fn(self._ctx, layer, q, k_new, v_new, out, sel, self._stream)
+        if st != COMPKV_OK:
+            raise CompKVError(st, f"compkv_decode: {compkv_last_error()}")
+
+
 COMPKV_STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -180,8 +208,8 @@ def compkv_launch_count(ctx) -> int:
     return lib().compkv_launch_count(ctx)
 
 
-KERNEL_FAMILIES = {"prefill": 0, "append": 1, "score": 2, "select": 3, "attend": 4, "decode": 5,
-                   "k_score": 6, "k_post": 7}
+KERNEL_FAMILIES = {"prefill": 0, "append": 1, "score": 2, "attend": 4, "decode": 5,
+                   "k_stream": 6, "k_post": 7}
 
 
 def compkv_profile_enable(ctx, enable):

@@ -26,18 +26,18 @@ compkv_status fail(compkv_status st, const char* fmt, ...) {
   return st;
 }
 
-constexpr size_t kMaxSmem = 232448;  // 227 KiB of shared memory per CTA
+constexpr size_t kMaxSmem = 232448;   // 227 KiB of shared memory per CTA
+constexpr size_t kPostSoft = 113 * 1024;  // two post CTAs per multiprocessor (16-CTA clusters co-resident)
+constexpr int kBpcLimit = 8192;            // blocks of one post CTA at most
 
 struct Layout {
   std::vector<int> cap_blocks;
   std::vector<int64_t> seq_row0;
-  std::vector<int> chunk0, nchunk;
   int64_t rows_per_layer = 0;
-  int total_chunks = 0;
   int max_cap_blocks = 0;
-  int K = 0, splits = 0, units = 0, key_stride = 0, post_cpc = 0;
-  size_t off_status = 0, off_lnew = 0, off_hist12 = 0, off_chunk_rec = 0, off_chunk_z = 0, off_chunk_s = 0,
-         off_comp_part = 0, off_unit_nsel = 0, off_skeys = 0, off_sel = 0, total = 0;
+  int K = 0, C = 0, bpc_max = 0, units = 0, rec_cap = 0;
+  size_t off_status = 0, off_lnew = 0, off_rec = 0, off_comp = 0, off_zs = 0, off_ss = 0, off_sel = 0, off_hq = 0,
+         off_hk = 0, off_hv = 0, off_hout = 0, total = 0;
 };
 
 bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
@@ -60,6 +60,8 @@ compkv_status make_layout(const compkv_config* c, Layout* L) {
   if (c->budget_tokens % kBlock || c->budget_tokens / kBlock < 3 || c->budget_tokens / kBlock > 4096)
     return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "budget_tokens must be a multiple of 16 in 48..65536 (got %d)",
                 c->budget_tokens);
+  if (c->variant & ~(COMPKV_VARIANT_FIRST_ORDER_MASS | COMPKV_VARIANT_NO_VARIANCE_FACTOR | COMPKV_VARIANT_NO_COMPENSATION))
+    return fail(COMPKV_ERR_INVALID_ARG, "variant has unknown bits (got %d)", c->variant);
   L->cap_blocks.resize(c->batch);
   for (int s = 0; s < c->batch; ++s) {
     const int cap = c->capacity_tokens ? c->capacity_tokens[s] : c->max_tokens;
@@ -69,37 +71,32 @@ compkv_status make_layout(const compkv_config* c, Layout* L) {
   }
   const int H = c->num_kv_heads, G = c->group_size, d = c->head_dim;
   L->seq_row0.resize(c->batch);
-  L->chunk0.resize(c->batch);
-  L->nchunk.resize(c->batch);
-  int64_t row = 0, ch = 0;
+  int64_t row = 0;
   L->max_cap_blocks = 0;
   for (int s = 0; s < c->batch; ++s) {
     L->seq_row0[s] = row;
     row += (int64_t)H * L->cap_blocks[s];
-    L->nchunk[s] = (L->cap_blocks[s] + kChunk - 1) / kChunk;
-    L->chunk0[s] = (int)ch;
-    ch += (int64_t)H * L->nchunk[s];
     if (L->cap_blocks[s] > L->max_cap_blocks) L->max_cap_blocks = L->cap_blocks[s];
   }
-  // grid of the scoring kernel (x dimension)
-  if (ch > 0x7fffffff) return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "too many scoring work items");
   L->rows_per_layer = row;
-  L->total_chunks = (int)ch;
-  L->key_stride = (L->max_cap_blocks + 3) & ~3;
   L->K = c->budget_tokens / kBlock;
-  // CTAs per unit after the scoring: one cluster of up to 16, 8 selected blocks per CTA and round;
-  // each owns ceil(items / splits) of the unit's scoring items
-  L->splits = (L->K + kAttendBlocks - 1) / kAttendBlocks;
-  if (L->splits > 16) L->splits = 16;
-  L->post_cpc = 0;
-  for (int s = 0; s < c->batch; ++s) {
-    const int cpc = (L->nchunk[s] + L->splits - 1) / L->splits;
-    if (cpc > L->post_cpc) L->post_cpc = cpc;
-  }
-  if (chain_smem_bytes(d, c->r, G, L->key_stride, L->post_cpc, L->K, L->splits) > kMaxSmem)
-    return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "a sequence capacity of %d blocks does not fit the selection in shared memory",
-                L->max_cap_blocks);
+  // the post kernel's cluster: one selected block per warp and round (8 warps), and every CTA's
+  // share of a unit's blocks in shared memory; smallest C whose shared memory allows two CTAs
+  // per multiprocessor, else the smallest that fits at all
+  const int c0 = (L->K + 7) / 8 < 1 ? 1 : ((L->K + 7) / 8 > kMaxC ? kMaxC : (L->K + 7) / 8);
+  auto bpc_of = [&](int C) { return ((L->max_cap_blocks + C - 1) / C + 3) & ~3; };
+  L->C = 0;
+  for (int C = c0; C <= kMaxC && !L->C; ++C)
+    if (bpc_of(C) <= kBpcLimit && post_smem(d, G, C, bpc_of(C), L->K) <= kPostSoft) L->C = C;
+  for (int C = c0; C <= kMaxC && !L->C; ++C)
+    if (bpc_of(C) <= kBpcLimit && post_smem(d, G, C, bpc_of(C), L->K) <= kMaxSmem) L->C = C;
+  if (!L->C || stream_smem(d, c->r, G) > kMaxSmem)
+    return fail(COMPKV_ERR_UNSUPPORTED_SHAPE,
+                "a sequence capacity of %d blocks does not fit the selection in shared memory", L->max_cap_blocks);
+  L->bpc_max = bpc_of(L->C);
   L->units = c->batch * H;
+  L->rec_cap = kMaxStreamCtas + L->units;
+  const int Gp = pad_g(G);
   size_t off = 0;
   auto region = [&](size_t* o, size_t bytes) {
     *o = off;
@@ -107,14 +104,16 @@ compkv_status make_layout(const compkv_config* c, Layout* L) {
   };
   region(&L->off_status, 16);
   region(&L->off_lnew, (size_t)c->batch * sizeof(int));
-  region(&L->off_hist12, (size_t)L->units * 4096 * sizeof(unsigned));  // everything before chunk_rec is zeroed per fresh start
-  region(&L->off_chunk_rec, (size_t)L->total_chunks * G * 4 * sizeof(float));
-  region(&L->off_chunk_z, (size_t)L->total_chunks * G * kChunk * sizeof(float));
-  region(&L->off_chunk_s, (size_t)L->total_chunks * G * kChunk * sizeof(float));
-  region(&L->off_comp_part, (size_t)L->total_chunks * G * (d + 4) * sizeof(float));
-  region(&L->off_unit_nsel, (size_t)L->units * sizeof(int));
-  region(&L->off_skeys, (size_t)L->units * L->key_stride * sizeof(uint32_t));
+  region(&L->off_rec, (size_t)L->rec_cap * G * 4 * sizeof(float));
+  region(&L->off_comp, (size_t)L->rec_cap * G * d * sizeof(float));
+  region(&L->off_zs, (size_t)row * Gp * sizeof(float));
+  region(&L->off_ss, (size_t)row * Gp * sizeof(float));
   region(&L->off_sel, (size_t)L->units * L->K * sizeof(int));
+  // staging of compkv_decode_host: q, k_new, v_new and out of one call
+  region(&L->off_hq, (size_t)L->units * G * d * sizeof(float));
+  region(&L->off_hk, (size_t)L->units * d * 2);
+  region(&L->off_hv, (size_t)L->units * d * 2);
+  region(&L->off_hout, (size_t)L->units * G * d * sizeof(float));
   L->total = off;
   return COMPKV_OK;
 }
@@ -166,10 +165,30 @@ int device_sms() {
   return n;
 }
 
+// Stream CTAs of the decode chain on the current device for (d, r, G):
+// multiprocessors x resident CTAs, cached per device.
+int device_stream_ctas(int d, int r, int G) {
+  static std::atomic<int> cache[64][2][8][4];  // [dev][d == 128][log2 r][log2 G]
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return kMaxStreamCtas / 4;
+  int lr = 0, lg = 0;
+  while ((1 << lr) < r) ++lr;
+  while ((1 << lg) < G) ++lg;
+  std::atomic<int>& slot = cache[dev][d == 128][lr][lg];
+  int v = slot.load();
+  if (v > 0) return v;
+  const int per = stream_ctas_per_sm(d, r, G);
+  v = device_sms() * (per < 1 ? 1 : per);
+  if (v > kMaxStreamCtas) v = kMaxStreamCtas;
+  if (v < 1) v = 1;
+  slot.store(v);
+  return v;
+}
+
 LayerArgs base_args(const compkv_ctx* c, int layer) {
   LayerArgs a;
   memset(&a, 0, sizeof(a));
-  const int d = c->cfg.head_dim, r = c->cfg.r;
+  const int d = c->cfg.head_dim, r = c->cfg.r, G = c->cfg.group_size;
   const int64_t rows = c->lay.rows_per_layer * (int64_t)layer;
   a.k = reinterpret_cast<__nv_bfloat16*>(c->buf.k) + rows * kBlock * d;
   a.v = reinterpret_cast<__nv_bfloat16*>(c->buf.v) + rows * kBlock * d;
@@ -179,33 +198,28 @@ LayerArgs base_args(const compkv_ctx* c, int layer) {
   a.seq_len = c->buf.seq_len + (int64_t)layer * c->cfg.batch;
   a.B = c->cfg.batch;
   a.Hkv = c->cfg.num_kv_heads;
-  a.G = c->cfg.group_size;
+  a.G = G;
   a.d = d;
   a.r = r;
   a.K = c->lay.K;
-  a.splits = c->lay.splits;
+  a.variant = c->cfg.variant;
+  a.P = device_stream_ctas(d, r, G);
+  a.C = c->lay.C;
+  a.bpc_max = c->lay.bpc_max;
+  a.rec_cap = c->lay.rec_cap;
   char* sc = reinterpret_cast<char*>(c->buf.scratch);
   a.status = reinterpret_cast<int*>(sc + c->lay.off_status);
   a.lnew = reinterpret_cast<int*>(sc + c->lay.off_lnew);
-  a.hist12 = reinterpret_cast<unsigned*>(sc + c->lay.off_hist12);
-  a.skeys = reinterpret_cast<uint32_t*>(sc + c->lay.off_skeys);
-  a.key_stride = c->lay.key_stride;
-  a.total_chunks = c->lay.total_chunks;
-  a.sms = device_sms();
-  a.post_cpc = c->lay.post_cpc;
+  a.rec = reinterpret_cast<float4*>(sc + c->lay.off_rec);
+  a.comp = reinterpret_cast<float*>(sc + c->lay.off_comp);
+  a.zs = reinterpret_cast<float*>(sc + c->lay.off_zs);
+  a.ss = reinterpret_cast<float*>(sc + c->lay.off_ss);
+  a.sel = reinterpret_cast<int*>(sc + c->lay.off_sel);
   a.trace = c->trace;
   a.trace_cap = c->trace_cap;
-  a.chunk_rec = reinterpret_cast<float*>(sc + c->lay.off_chunk_rec);
-  a.chunk_z = reinterpret_cast<float*>(sc + c->lay.off_chunk_z);
-  a.chunk_s = reinterpret_cast<float*>(sc + c->lay.off_chunk_s);
-  a.comp_part = reinterpret_cast<float*>(sc + c->lay.off_comp_part);
-  a.unit_nsel = reinterpret_cast<int*>(sc + c->lay.off_unit_nsel);
-  a.sel = reinterpret_cast<int*>(sc + c->lay.off_sel);
   for (int s = 0; s < c->cfg.batch; ++s) {
     a.seq_row0[s] = c->lay.seq_row0[s];
     a.cap_blocks[s] = c->lay.cap_blocks[s];
-    a.chunk0[s] = c->lay.chunk0[s];
-    a.nchunk[s] = c->lay.nchunk[s];
   }
   return a;
 }
@@ -268,9 +282,9 @@ compkv_status launch(compkv_ctx* c, int family, cudaStream_t st, const char* wha
   return COMPKV_OK;
 }
 
-// A decode-step chain (two kernels).  While profiling is on, each kernel is
-// bracketed by its own events too (COMPKV_KERNEL_K_SCORE, _K_POST); the
-// whole call goes under `family`.
+// A decode-step chain: the stream kernel, then the post kernel.  While
+// profiling is on (level 2), each kernel is bracketed by its own events too
+// (COMPKV_KERNEL_K_STREAM, _K_POST); the whole call goes under `family`.
 compkv_status launch_chain(compkv_ctx* c, int family, const LayerArgs& a, int mode, cudaStream_t st, const char* what) {
   cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
   bool kev = c->prof == 2;
@@ -279,11 +293,21 @@ compkv_status launch_chain(compkv_ctx* c, int family, const LayerArgs& a, int mo
     for (int i = 0; i < 4; ++i)
       if (ev[i]) c->pool.push_back(ev[i]);
   const compkv_status r = launch(
-      c, family, st, what, [&] { return launch_decode_chain(a, mode, st, 1, kev ? ev : nullptr); },
-      chain_kernels(mode));
+      c, family, st, what,
+      [&] {
+        cudaError_t e;
+        if (kev && (e = cudaEventRecord(ev[0], st)) != cudaSuccess) return e;
+        if ((e = launch_stream(a, mode, st, true)) != cudaSuccess) return e;
+        if (kev && (e = cudaEventRecord(ev[1], st)) != cudaSuccess) return e;
+        if (kev && (e = cudaEventRecord(ev[2], st)) != cudaSuccess) return e;
+        if ((e = launch_post(a, mode, st)) != cudaSuccess) return e;
+        if (kev && (e = cudaEventRecord(ev[3], st)) != cudaSuccess) return e;
+        return cudaSuccess;
+      },
+      2);
   if (kev) {
     if (r == COMPKV_OK) {
-      c->slots[COMPKV_KERNEL_K_SCORE].pending.emplace_back(ev[0], ev[1]);
+      c->slots[COMPKV_KERNEL_K_STREAM].pending.emplace_back(ev[0], ev[1]);
       c->slots[COMPKV_KERNEL_K_POST].pending.emplace_back(ev[2], ev[3]);
     } else {
       for (int i = 0; i < 4; ++i) c->pool.push_back(ev[i]);
@@ -426,6 +450,35 @@ compkv_status compkv_decode(compkv_ctx* c, int layer, const float* q, const void
   return COMPKV_OK;
 }
 
+compkv_status compkv_decode_host(compkv_ctx* c, int layer, const float* q_host, const void* k_new_host,
+                                 const void* v_new_host, float* out_host, int* sel_host, void* stream) {
+  COMPKV_TRY(check_call(c, layer));
+  if (!q_host || !k_new_host || !v_new_host || !out_host)
+    return fail(COMPKV_ERR_INVALID_ARG, "q, k_new, v_new and out must not be NULL");
+  cudaStream_t st = (cudaStream_t)stream;
+  char* sc = reinterpret_cast<char*>(c->buf.scratch);
+  const size_t units = (size_t)c->lay.units, d = (size_t)c->cfg.head_dim, G = (size_t)c->cfg.group_size;
+  float* dq = reinterpret_cast<float*>(sc + c->lay.off_hq);
+  void* dk = sc + c->lay.off_hk;
+  void* dv = sc + c->lay.off_hv;
+  float* dout = reinterpret_cast<float*>(sc + c->lay.off_hout);
+  COMPKV_TRY(cuda_status(cudaMemcpyAsync(dq, q_host, units * G * d * 4, cudaMemcpyHostToDevice, st), "q copy"));
+  COMPKV_TRY(cuda_status(cudaMemcpyAsync(dk, k_new_host, units * d * 2, cudaMemcpyHostToDevice, st), "k_new copy"));
+  COMPKV_TRY(cuda_status(cudaMemcpyAsync(dv, v_new_host, units * d * 2, cudaMemcpyHostToDevice, st), "v_new copy"));
+  LayerArgs a = base_args(c, layer);
+  a.q = dq;
+  a.k_new = reinterpret_cast<const __nv_bfloat16*>(dk);
+  a.v_new = reinterpret_cast<const __nv_bfloat16*>(dv);
+  a.out = dout;
+  COMPKV_TRY(launch_chain(c, COMPKV_KERNEL_DECODE, a, kFusedDecode, st, "decode launch"));
+  COMPKV_TRY(cuda_status(cudaMemcpyAsync(out_host, dout, units * G * d * 4, cudaMemcpyDeviceToHost, st), "out copy"));
+  if (sel_host)
+    COMPKV_TRY(cuda_status(cudaMemcpyAsync(sel_host, a.sel, units * (size_t)c->lay.K * 4, cudaMemcpyDeviceToHost, st),
+                           "sel copy"));
+  COMPKV_TRY(cuda_status(cudaStreamSynchronize(st), "stream synchronize"));
+  return COMPKV_OK;
+}
+
 compkv_status compkv_device_status(compkv_ctx* c, void* stream) {
   if (!c) return fail(COMPKV_ERR_INVALID_ARG, "context is NULL");
   cudaStream_t st = (cudaStream_t)stream;
@@ -558,13 +611,15 @@ compkv_status compkv_internal_decode_in(const compkv_config* cfg, const compkv_b
   c.buf.scratch_bytes = scratch_bytes;
   c.lay = L;
   cudaStream_t st = (cudaStream_t)stream;
-  COMPKV_TRY(cuda_status(cudaMemsetAsync(scratch, 0, L.off_chunk_rec, st), "clearing scratch"));
+  COMPKV_TRY(cuda_status(cudaMemsetAsync(scratch, 0, L.off_rec, st), "clearing scratch"));
   LayerArgs a = base_args(&c, layer);
   a.q = q;
   a.k_new = reinterpret_cast<const __nv_bfloat16*>(k_new);
   a.v_new = reinterpret_cast<const __nv_bfloat16*>(v_new);
   a.out = out;
   if (sel) a.sel = sel;
-  COMPKV_TRY(cuda_status(launch_decode_chain(a, kFusedDecode, st, 1), "decode launch"));
+  cudaError_t e = launch_stream(a, kFusedDecode, st, true);
+  if (e == cudaSuccess) e = launch_post(a, kFusedDecode, st);
+  COMPKV_TRY(cuda_status(e, "decode launch"));
   return COMPKV_OK;
 }

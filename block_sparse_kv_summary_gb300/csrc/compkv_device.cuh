@@ -1,8 +1,9 @@
 // Device-side building blocks of the CompKV decode-step kernels (sm_103a).
 //
-// The launch-argument struct, the scratch record layout, inline-PTX wrappers
-// for mbarriers and 1-D bulk (TMA) copies into shared memory, bounded waits
-// that report through the device status word, and warp reductions.
+// The launch-argument struct, the scratch layout shared by the two decode
+// kernels, inline-PTX wrappers for mbarriers, 1-D bulk (TMA) copies, thread
+// block clusters and distributed shared memory, bounded waits that report
+// through the device status word, and warp reductions.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -13,8 +14,8 @@ namespace compkv {
 
 constexpr int kBlock = 16;        // tokens per KV block (CompKV, "전제와 한계": block size 16)
 constexpr int kMaxBatch = 64;     // sequences per call (launch arguments hold per-sequence tables)
-constexpr int kChunk = 64;        // blocks per scoring work item (and per scoring record)
 constexpr int kMaxG = 8;
+constexpr int kMaxC = 16;         // CTAs of one unit's cluster in the post kernel
 
 // Device status word codes (mirrors compkv_status).
 enum DevErr : int {
@@ -23,6 +24,13 @@ enum DevErr : int {
   kDevTimeout = 5,
   kDevBadSelection = 6,
   kDevInternal = 7,
+};
+
+// Ablation switches of "전제와 한계" (bit set = the ablated variant).
+enum Variant : int {
+  kVarFirstOrderMass = 1,    // drop the 1/2 sigma2 term from the mass estimate
+  kVarNoVarianceFactor = 2,  // S_b = sum_g phat (no external variance factor)
+  kVarNoCompensation = 4,    // no Mean compensation: renormalise over the selected blocks
 };
 
 // Per-call arguments, passed by value (fits the kernel parameter space).
@@ -44,37 +52,34 @@ struct LayerArgs {
   int score_stride;
   // shape
   int B, Hkv, G, d, r, K;
-  int splits;                 // attention CTAs per unit (one cluster)
+  int variant;                // Variant bits
+  int P;                      // CTAs of the stream kernel (its grid)
+  int C;                      // CTAs per unit in the post kernel (one cluster)
+  int bpc_max;                // post kernel: blocks of one CTA at most (its shared arrays)
+  int rec_cap;                // segment records the scratch holds
   // scratch
   int* status;                // [4]: code, sequence, head, site
   int* lnew;                  // [B] tokens of each sequence in this call (after its append)
-  float* chunk_rec;           // [chunk records][G][4]: max a, sum e^(a - max a), max(ln|b| + zbar), -
-  float* chunk_z;             // [chunk records][G][kChunk]  zbar per block
-  float* chunk_s;             // [chunk records][G][kChunk]  sigma2 per block
-  float* comp_part;           // [chunk records][G][d + 4]: the chunk's sums with w relative to its own max
-  int* unit_nsel;             // [units] selected blocks
-  uint32_t* skeys;            // [units][key_stride] S_b as order-preserving keys (full radix selection only)
-  int key_stride;             // max capacity in blocks, rounded up to a multiple of 4
-  unsigned* hist12;           // [units][4096] histogram of the keys' top 12 bits (full radix selection only)
-  int total_chunks;           // scoring items of the layer (64 blocks)
-  int sms;                    // multiprocessors of the device
-  int post_cpc;               // scoring items owned by one CTA of a unit's cluster (max over sequences)
+  float4* rec;                // [rec_cap][G]: max a, sum e^(a - max a), compensation reference, weight sum
+  float* comp;                // [rec_cap][G][d]: compensation numerator relative to its reference
+  float* zs;                  // [rows][Gp]: zbar per block and head (Gp = max(G, 4))
+  float* ss;                  // [rows][Gp]: sigma2 per block and head
   // optional trace of the work items (null: off)
-  unsigned long long* trace;  // see compkv_trace
+  unsigned long long* trace;
   int trace_cap;
   // ragged tables
   int64_t seq_row0[kMaxBatch];   // first row of (s, head 0) relative to the layer
   int cap_blocks[kMaxBatch];     // capacity of sequence s in blocks
-  int chunk0[kMaxBatch];         // first chunk record of (s, head 0)
-  int nchunk[kMaxBatch];         // chunk records per (s, head) = ceil(cap / kChunk)
   int lens[kMaxBatch];           // prefill lengths (compkv_prefill only)
 };
+
+__host__ __device__ inline int pad_g(int G) { return G < 4 ? 4 : G; }
 
 __device__ __forceinline__ int64_t row_of(const LayerArgs& a, int s, int h, int b) {
   return a.seq_row0[s] + (int64_t)h * a.cap_blocks[s] + b;
 }
 
-// ---------------------------------------------------------------- tracing
+// ---------------------------------------------------------------- timers
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -108,6 +113,10 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 // 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -117,34 +126,113 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
-// Test for completion of phase `parity`; a waiting thread is suspended (it
-// issues nothing) until the phase completes or about kSuspendNs pass.
-constexpr uint32_t kSuspendNs = 1000000;
+// Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Orders this thread's generic-proxy global writes before later async-proxy
+// (bulk copy) reads of the same memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// One test for completion of phase `parity` (no suspend hint: the hardware
+// decides how long the thread may sleep before the test returns).
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "n"(kSuspendNs)
+      : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
 
-// Wait for phase `parity` of `bar`; gives up after a bounded number of polls
-// (a few seconds at most), records a timeout in the status word and returns
-// false.
-constexpr uint32_t kWaitPolls = 1u << 12;
+// Wait for phase `parity` of `bar`.  Gives up after kWaitNs of %globaltimer
+// (a backstop of kWaitPolls tests bounds it even if the timer stalls), records
+// a timeout in the status word and returns false.  A decode step takes tens
+// of microseconds, so reaching the limit means a copy never arrived.
+constexpr unsigned long long kWaitNs = 50ull * 1000 * 1000;  // 50 ms
+constexpr uint32_t kWaitPolls = 1u << 26;
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status, int s, int h,
                                                   int site) {
-  for (uint32_t i = 0; i < kWaitPolls; ++i)
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 1; i < kWaitPolls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 31) == 0 && global_ns() - t0 > kWaitNs) break;
+  }
   set_error(status, kDevTimeout, s, h, site);
-  // give copies still in flight a second bounded chance to land before the CTA exits
-  for (uint32_t i = 0; i < kWaitPolls; ++i)
-    if (mbar_try_wait(bar, parity)) break;
   return false;
+}
+
+// After a timeout: give the copies this CTA may still have in flight into
+// `bar` a bounded time to land (either phase) before the CTA moves on or exits.
+__device__ __forceinline__ void mbar_drain_bounded(uint64_t* bar) {
+  const unsigned long long t0 = global_ns();
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    if (mbar_try_wait(bar, 0u) && mbar_try_wait(bar, 1u)) return;
+    if ((i & 31) == 0 && global_ns() - t0 > kWaitNs) return;
+  }
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ---------------------------------------------------------------- clusters
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_sync_all() {
+  cluster_arrive();
+  cluster_wait();
+}
+// Address of `p` (this CTA's shared memory) in the shared memory of cluster rank `rank`.
+__device__ __forceinline__ uint32_t peer_smem(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ uint32_t ld_peer_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint2 ld_peer_u2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared::cluster.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint4 ld_peer_u4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared::cluster.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_peer_f4(uint32_t addr) {
+  const uint4 u = ld_peer_u4(addr);
+  return make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w));
+}
+__device__ __forceinline__ void st_peer_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_peer_u2(uint32_t addr, uint2 v) {
+  asm volatile("st.shared::cluster.v2.u32 [%0], {%1,%2};" ::"r"(addr), "r"(v.x), "r"(v.y) : "memory");
+}
+__device__ __forceinline__ void st_peer_f4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void red_peer_add(uint32_t addr, uint32_t v) {
+  asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 // ---------------------------------------------------------------- math helpers
@@ -157,6 +245,14 @@ __device__ __forceinline__ float warp_max(float x) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
   return x;
+}
+
+// Merge two online-softmax parts (max, sum of e^(x - max)); -inf max = empty.
+__device__ __forceinline__ void lse_merge(float& m, float& l, float m2, float l2) {
+  const float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) return;
+  l = (m == -INFINITY ? 0.f : l * __expf(m - mn)) + (m2 == -INFINITY ? 0.f : l2 * __expf(m2 - mn));
+  m = mn;
 }
 
 // bf16 x N -> float x N (N = 2 or 4), from an 8- or 4-byte aligned address.
@@ -187,5 +283,33 @@ __device__ __forceinline__ void store_bf16_raw<2>(__nv_bfloat16* dst, const __nv
 }
 
 __device__ __forceinline__ int ceil_blocks(int L) { return (L + kBlock - 1) / kBlock; }
+
+__device__ __forceinline__ float ln_count(int n) { return n == kBlock ? 2.772588722239781f : logf((float)n); }
+
+// Tokens of sequence s in this call: the stored length, plus one when the
+// call appends and the sequence has room (`fits`).
+__device__ __forceinline__ int call_tokens(int Lold, int cap_blocks, bool append, bool* fits) {
+  const int cap = cap_blocks * kBlock;
+  *fits = Lold >= 0 && Lold < cap;
+  int L = Lold < 0 ? 0 : (Lold > cap ? cap : Lold);
+  if (append && *fits) L += 1;
+  return L;
+}
+
+// ---------------------------------------------------------------- work plan
+// The stream kernel splits every unit (sequence s, KV head h) of the layer
+// into segments of `seg` consecutive blocks (the last one shorter), numbered
+// unit by unit: sequence-major, then head, then position.  seg is the
+// smallest multiple of `sb` with P segments' worth of blocks covering the
+// layer, so there are at most P + units segments.
+struct Plan {
+  int seg;       // blocks per segment
+  int total;     // segments of the layer
+};
+__device__ __forceinline__ int plan_seg(long long blocks_total, int P, int sb) {
+  long long s = (blocks_total + P - 1) / P;
+  s = (s + sb - 1) / sb * sb;
+  return (int)(s < sb ? sb : s);
+}
 
 }  // namespace compkv

@@ -1,0 +1,614 @@
+// The summary stream of the CompKV decode step (onedev.kr/papers/157).
+//
+// Section "무엇과 다른가" scores every 16-token block of a (sequence, KV
+// head) "unit" from its summary {|b|, kbar_b, Dbar_b, vbar_b}:
+//   zbar_{g,b}   = q_g . kbar_b / sqrt(d)
+//   sigma2_{g,b} = (1/d) sum_t (sum_{i in G_t} q_{g,i}^2) (Dbar_b)_t
+//   a_{g,b}      = ln|b| + zbar + sigma2 / 2        (log of the mass estimate)
+// and Mean compensation ("어떻게 동작하나") needs, over the unselected blocks,
+// sum_b |b| e^{zbar_{g,b}} vbar_b and sum_b |b| e^{zbar_{g,b}}.  This kernel
+// streams every summary row of the layer once and leaves, per block, zbar and
+// sigma2, and per segment of blocks the logsumexp parts of a and the
+// compensation sums over all of its blocks (the post kernel removes the
+// selected blocks' own terms).  Section "어떻게 쓰나" fuses the open block's
+// summary update with the K/V pack: the CTA whose segment holds the newest
+// block appends the new token first.
+//
+// Grid: P persistent CTAs of kWarps warps.  The layer's units are cut into
+// segments (decode_common.cuh); CTA i takes segments i, i + P, ...  Within a
+// segment, stage k (SB consecutive blocks: their kbar, vbar and Dbar rows,
+// one 1-D bulk copy each) belongs to warp k % kWarps, which owns kSlots
+// shared-memory slots and issues its own copies, so no warp waits on another
+// while the stream runs.
+//
+// Per stage a warp forms the SB x G partial dots q_g . kbar_b over its lanes'
+// coordinates (lane l holds coordinates CPL*l .. CPL*l + CPL - 1) and sums
+// them across the warp with a halving butterfly: at each xor step a lane keeps
+// half of its values and receives its partner's partial of that half, so the
+// NV = SB*G values end one per lane (or replicated over 32/NV lanes).
+#include "compkv_launch.h"
+#include "decode_common.cuh"
+
+namespace compkv {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kSlots = 2;  // stage slots per warp
+
+template <int D>
+struct InvSqrt;
+template <>
+struct InvSqrt<64> {
+  static constexpr float v = 0.125f;
+};
+template <>
+struct InvSqrt<128> {
+  static constexpr float v = 0.08838834764831845f;
+};
+
+__host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
+// floats of one stage slot: kbar rows | vbar rows | Dbar rows (4 floats per row at least)
+__host__ __device__ inline int stream_slot_floats(int D, int r, int G, bool score, bool comp) {
+  const int sb = stage_blocks(r, G);
+  return sb * D + (comp ? sb * D : 0) + (score ? sb * (r < 4 ? 4 : r) : 0);
+}
+// shared memory: slots | per-warp weights [kWarps][sb][G] | Qsq [G][rr] | the appended
+// block's kbar [D], vbar [D], Dbar [rr] | plan (ints) | mbarriers
+__host__ __device__ inline int stream_smem_bytes(int D, int r, int G, bool score, bool comp) {
+  const int rr = (r + 3) & ~3;
+  const int sb = stage_blocks(r, G);
+  const int floats = kWarps * kSlots * stream_slot_floats(D, r, G, score, comp) + kWarps * sb * G + G * rr + 2 * D + rr;
+  return floats * 4 + (3 * kMaxBatch + 8) * 4 + 8 * (kWarps * kSlots + 2) + 64;
+}
+
+// One halving step of the butterfly: N values per lane -> N/2.
+template <int N>
+__device__ __forceinline__ void halve(float* p, int lane, int o) {
+  const bool up = (lane & o) != 0;
+#pragma unroll
+  for (int i = 0; i < N / 2; ++i) {
+    const float send = up ? p[i] : p[i + N / 2];
+    const float keep = up ? p[i + N / 2] : p[i];
+    p[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+  }
+}
+// Sum NV per-lane partials across the warp.  Afterwards lane l holds the
+// total of value v = l >> log2(32 / NV) (NV <= 32; lanes with equal v agree).
+template <int NV>
+__device__ __forceinline__ void butterfly(float (&p)[NV], int lane) {
+  static_assert(NV <= 32, "one value per lane at most");
+  if constexpr (NV >= 2) halve<NV>(p, lane, 16); else p[0] += __shfl_xor_sync(0xffffffffu, p[0], 16);
+  if constexpr (NV >= 4) halve<NV / 2>(p, lane, 8); else p[0] += __shfl_xor_sync(0xffffffffu, p[0], 8);
+  if constexpr (NV >= 8) halve<NV / 4>(p, lane, 4); else p[0] += __shfl_xor_sync(0xffffffffu, p[0], 4);
+  if constexpr (NV >= 16) halve<NV / 8>(p, lane, 2); else p[0] += __shfl_xor_sync(0xffffffffu, p[0], 2);
+  if constexpr (NV >= 32) halve<NV / 16>(p, lane, 1); else p[0] += __shfl_xor_sync(0xffffffffu, p[0], 1);
+}
+
+template <int CPL>
+__device__ __forceinline__ void lds_vec(const float* p, float (&x)[CPL]);
+template <>
+__device__ __forceinline__ void lds_vec<4>(const float* p, float (&x)[4]) {
+  const float4 v = *reinterpret_cast<const float4*>(p);
+  x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+}
+template <>
+__device__ __forceinline__ void lds_vec<2>(const float* p, float (&x)[2]) {
+  const float2 v = *reinterpret_cast<const float2*>(p);
+  x[0] = v.x; x[1] = v.y;
+}
+
+template <int D, int G, int MODE, int SB, bool RB>
+__global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
+  constexpr bool APPEND = (MODE & kFAppend) != 0;
+  constexpr bool SCORE = (MODE & kFScore) != 0;
+  constexpr bool COMP = (MODE & kFComp) != 0;
+  constexpr bool SELMODE = (MODE & kFSelect) != 0;
+  constexpr int CPL = D / 32;
+  constexpr int NV = SB * G;                  // (block, head) values of a stage
+  constexpr int SH = ilog2(32 / NV);          // lanes per value = 1 << SH
+  constexpr int GB = ilog2(G);                // lane bits that select the head
+  static_assert(NV <= 32, "stage values exceed the warp");
+  extern __shared__ __align__(128) float sm[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int r = a.r, rr = (r + 3) & ~3, rs = r < 4 ? 4 : r;
+  const int Gp = pad_g(G);
+  const int slot_f = stream_slot_floats(D, r, G, SCORE, COMP);
+  float* slots = sm;
+  float* sw = slots + kWarps * kSlots * slot_f;  // [kWarps][SB][G]
+  float* sqs = sw + kWarps * SB * G;             // [G][rr]
+  float* pk = sqs + G * rr;                      // appended block: kbar [D], vbar [D], Dbar [rr]
+  float* pv = pk + D;
+  float* pd = pv + D;
+  int* sL = reinterpret_cast<int*>(pd + rr);     // [kMaxBatch] tokens of each sequence in this call
+  int* sN = sL + kMaxBatch;                      // [kMaxBatch] blocks
+  int* soff = sN + kMaxBatch;                    // [kMaxBatch + 1] first segment of each sequence
+  int* sseg = soff + kMaxBatch + 1;
+  int* sfits = sseg + 1;                         // [2] bit s: sequence s had room for its token
+  int* sbad = sfits + 2;                         // a wait of this CTA ran out
+  uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(sbad + 1) + 7) & ~uintptr_t(7));
+  uint64_t* patch_bar = bars + kWarps * kSlots;
+  if (threadIdx.x < kWarps * kSlots + 1) mbar_init(bars + threadIdx.x, 1);
+  if (threadIdx.x == 0) *sbad = 0;
+  fence_mbar_init();
+  // the previous work on the stream may have written this cache and its lengths
+  pdl_wait();
+  pdl_trigger();
+  if (warp == 0) {
+    const int s0 = lane, s1 = lane + 32;
+    bool f0 = false, f1 = false;
+    if (s0 < a.B) sL[s0] = call_tokens(a.seq_len[s0], a.cap_blocks[s0], APPEND, &f0);
+    if (s1 < a.B) sL[s1] = call_tokens(a.seq_len[s1], a.cap_blocks[s1], APPEND, &f1);
+    const unsigned m0 = __ballot_sync(0xffffffffu, f0), m1 = __ballot_sync(0xffffffffu, f1);
+    if (lane == 0) {
+      sfits[0] = (int)m0;
+      sfits[1] = (int)m1;
+    }
+    __syncwarp();
+    plan_warp(sL, a.B, a.Hkv, a.P, SB, sN, soff, sseg, lane);
+    if (blockIdx.x == 0) {
+      if (s0 < a.B) {
+        a.lnew[s0] = sL[s0];
+        if (APPEND && !f0) set_error(a.status, kDevCapacity, s0, -1, 1);
+      }
+      if (s1 < a.B) {
+        a.lnew[s1] = sL[s1];
+        if (APPEND && !f1) set_error(a.status, kDevCapacity, s1, -1, 1);
+      }
+    }
+  }
+  __syncthreads();
+  const int seg = *sseg, total = soff[a.B];
+  int npatch = 0;     // patches completed in this CTA (phases of patch_bar)
+  uint32_t uses = 0;  // stages this warp has consumed: slot uses % kSlots, phase (uses / kSlots) & 1
+  float* swr = sw + warp * SB * G;
+  // this lane's (block, head) value of a stage
+  const int vv = lane >> SH, vb = vv / G, vg = vv % G;
+  const bool primary = (lane & ((1 << SH) - 1)) == 0;
+
+  for (int si = blockIdx.x; si < total; si += gridDim.x) {
+    int s, h, b0, nb;
+    plan_segment(si, a.B, a.Hkv, sN, soff, seg, &s, &h, &b0, &nb);
+    const int L = sL[s], N = sN[s];
+    const bool fits = ((s < 32 ? sfits[0] >> s : sfits[1] >> (s - 32)) & 1) != 0;
+    const bool append = APPEND && fits && b0 + nb == N;  // this segment holds the open block
+    const int64_t row0 = row_of(a, s, h, b0);
+    const int ns = (nb + SB - 1) / SB;  // stages of the segment
+    const bool comp = COMP && !(a.variant & kVarNoCompensation) && (!SELMODE || N > a.K);
+    const bool dbulk = SCORE && r >= 4;
+    // ---- this warp's copies: its j-th stage of the segment is stage warp + kWarps j
+    auto issue = [&](int k, uint32_t use) {
+      float* st = slots + (warp * kSlots + (int)(use % kSlots)) * slot_f;
+      const int rb = k * SB, n = min(SB, nb - rb);
+      const uint32_t bytes = (uint32_t)n * (uint32_t)(D * 4 * (comp ? 2 : 1) + (dbulk ? r * 4 : 0));
+      uint64_t* bar = bars + warp * kSlots + (use % kSlots);
+      mbar_arrive_expect_tx(bar, bytes);
+      bulk_g2s(st, a.kbar + (row0 + rb) * D, (uint32_t)n * D * 4u, bar);
+      if (comp) bulk_g2s(st + SB * D, a.vbar + (row0 + rb) * D, (uint32_t)n * D * 4u, bar);
+      if (dbulk) bulk_g2s(st + SB * D * (comp ? 2 : 1), a.dbar + (row0 + rb) * r, (uint32_t)n * r * 4u, bar);
+    };
+    const int mine = warp < ns ? (ns - 1 - warp) / kWarps + 1 : 0;  // stages of this warp
+    if (lane == 0)
+      for (int j = 0; j < min(kSlots, mine); ++j) issue(warp + kWarps * j, uses + j);
+    // ---- queries of the unit: this lane's coordinates, scaled by 1/sqrt(d); Qsq by warp 1
+    const float* qbase = a.q + ((int64_t)s * a.Hkv + h) * G * D;
+    float q[G][CPL];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      lds_vec<CPL>(qbase + g * D + CPL * lane, q[g]);  // generic load (global memory)
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) q[g][c] *= InvSqrt<D>::v;
+    }
+    if (SCORE && warp == 1) {
+      // Qsq_{g,t} = sum of q_g^2 over coordinate group t = [t*D/r, (t+1)*D/r) (unscaled q)
+      const int gs = D / r;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        float x[CPL];
+        lds_vec<CPL>(qbase + g * D + CPL * lane, x);
+        if (gs >= CPL) {
+          float t = 0.f;
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) t = fmaf(x[c], x[c], t);
+          for (int o = 1; o < gs / CPL; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+          if ((lane & (gs / CPL - 1)) == 0) sqs[g * rr + (CPL * lane) / gs] = t;
+        } else {
+          float t = 0.f;
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {
+            t = fmaf(x[c], x[c], t);
+            if ((c + 1) % gs == 0) {
+              sqs[g * rr + (CPL * lane + c) / gs] = t;
+              t = 0.f;
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();  // Qsq is in place; the previous segment's patch is no longer read
+    const int patched = append ? (N - 1 - b0) : -1;  // segment-local block whose rows come from pk, pv, pd
+    if (append) ++npatch;
+    // ---- append: warp 0 of the CTA holding the open block packs the new token and
+    // recomputes that block's summary from its tokens (two-pass fp32 mean and
+    // population variance from the exact bf16 values) while the other warps stream
+    if (append && warp == 0) {
+      const int n = L - kBlock * (N - 1);
+      const int64_t row = row_of(a, s, h, N - 1);
+      const int c0 = CPL * lane;
+      const int64_t nw_off = ((int64_t)s * a.Hkv + h) * D + c0;
+      float kx[kBlock][CPL];
+      float ksum[CPL], vsum[CPL];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) ksum[c] = vsum[c] = 0.f;
+#pragma unroll
+      for (int j = 0; j < kBlock; ++j) {
+        float kf[CPL], vf[CPL];
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) kf[c] = vf[c] = 0.f;
+        if (j < n) {
+          const __nv_bfloat16* kp = (j == n - 1) ? a.k_new + nw_off : a.k + (row * kBlock + j) * D + c0;
+          const __nv_bfloat16* vp = (j == n - 1) ? a.v_new + nw_off : a.v + (row * kBlock + j) * D + c0;
+          load_bf16<CPL>(kp, kf);
+          load_bf16<CPL>(vp, vf);
+          if (j == n - 1) {
+            store_bf16_raw<CPL>(a.k + (row * kBlock + j) * D + c0, a.k_new + nw_off);
+            store_bf16_raw<CPL>(a.v + (row * kBlock + j) * D + c0, a.v_new + nw_off);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          kx[j][c] = kf[c];
+          ksum[c] += kf[c];
+          vsum[c] += vf[c];
+        }
+      }
+      float var[CPL];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        const float mk = ksum[c] / (float)n, mv = vsum[c] / (float)n;
+        pk[c0 + c] = mk;
+        pv[c0 + c] = mv;
+        a.kbar[row * D + c0 + c] = mk;
+        a.vbar[row * D + c0 + c] = mv;
+        float t = 0.f;
+#pragma unroll
+        for (int j = 0; j < kBlock; ++j) {
+          const float dv = j < n ? kx[j][c] - mk : 0.f;
+          t = fmaf(dv, dv, t);
+        }
+        var[c] = t / (float)n;
+      }
+      // Dbar_t: mean of the variances over coordinate group t = [t*D/r, (t+1)*D/r)
+      const int gs = D / r;
+      if (gs >= CPL) {
+        float t = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) t += var[c];
+        for (int o = 1; o < gs / CPL; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if ((lane & (gs / CPL - 1)) == 0) {
+          const float m = t / (float)gs;
+          pd[c0 / gs] = m;
+          a.dbar[row * r + c0 / gs] = m;
+        }
+      } else {
+        float t = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          t += var[c];
+          if ((c + 1) % gs == 0) {
+            const float m = t / (float)gs;
+            pd[(c0 + c) / gs] = m;
+            a.dbar[row * r + (c0 + c) / gs] = m;
+            t = 0.f;
+          }
+        }
+      }
+      fence_proxy_async_global();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(patch_bar);
+    }
+
+    // ---- stream this warp's stages
+    float lm = -INFINITY, ll = 0.f;  // this lane's value: running max of a, sum of e^(a - max)
+    float ref[G], acc[G][CPL], wsl = 0.f;  // compensation: per-head reference, numerator, weight sum
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      ref[g] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) acc[g][c] = 0.f;
+    }
+    bool bad = false;
+    bool patch_ready = !append;
+    for (int j = 0; j < mine; ++j) {
+      const int k = warp + kWarps * j;
+      const uint32_t use = uses + j;
+      const float* st = slots + (warp * kSlots + (int)(use % kSlots)) * slot_f;
+      const float* skb = st;
+      const float* svb = st + SB * D;
+      float* sdb = const_cast<float*>(st) + SB * D * (comp ? 2 : 1);
+      const int rb = k * SB, nbs = min(SB, nb - rb);
+      if (!patch_ready && patched >= rb && patched < rb + nbs) {
+        if (!mbar_wait_bounded(patch_bar, (uint32_t)(npatch - 1) & 1u, a.status, s, h, 12)) bad = true;
+        patch_ready = true;
+      }
+      if (SCORE && !dbulk && lane < nbs * r)  // r < 4: the Dbar rows by plain loads, 4 floats per row
+        sdb[(lane / r) * 4 + lane % r] = a.dbar[(row0 + rb) * r + lane];
+      if (bad || !mbar_wait_bounded(bars + warp * kSlots + (use % kSlots), (use / kSlots) & 1u, a.status, s, h, 10)) {
+        bad = true;
+        break;
+      }
+      __syncwarp();
+      // zbar partial dots of the stage's SB blocks and G heads
+      float p[NV];
+#pragma unroll
+      for (int b = 0; b < SB; ++b) {
+        float x[CPL];
+        const float* rowp = (rb + b == patched) ? pk : skb + b * D;
+        lds_vec<CPL>(rowp + CPL * lane, x);
+        if (b >= nbs) {
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) x[c] = 0.f;
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float t = q[g][0] * x[0];
+#pragma unroll
+          for (int c = 1; c < CPL; ++c) t = fmaf(q[g][c], x[c], t);
+          p[b * G + g] = t;
+        }
+      }
+      butterfly<NV>(p, lane);
+      const float zb = p[0];
+      const bool ok = vb < nbs;
+      const int gb = b0 + rb + vb;  // unit-local block of this lane's value
+      const float cv = ok ? ln_count(gb == N - 1 ? L - kBlock * gb : kBlock) + zb : -INFINITY;
+      float s2 = 0.f;
+      if (SCORE) {
+        if constexpr (RB) {
+          // long Dbar rows (r >= 64): lane holds Dbar coordinates [rpl*lane, rpl*lane + rpl)
+          const int rpl = r / 32;
+          float ps[NV];
+#pragma unroll
+          for (int b = 0; b < SB; ++b) {
+            const float* drow = (rb + b == patched) ? pd : sdb + b * rs;
+            float x[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) x[t] = (t < rpl && b < nbs) ? drow[rpl * lane + t] : 0.f;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+              float t = 0.f;
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                if (c < rpl) t = fmaf(sqs[g * rr + rpl * lane + c], x[c], t);
+              ps[b * G + g] = t;
+            }
+          }
+          butterfly<NV>(ps, lane);
+          s2 = ps[0] * (1.f / (float)D);
+        } else {
+          if (ok) {
+            const float* drow = (rb + vb == patched) ? pd : sdb + vb * rs;
+            const float* qsr = sqs + vg * rr;
+            float t = 0.f;
+            if (r <= 16) {
+#pragma unroll
+              for (int tt = 0; tt < 16; ++tt)
+                if (tt < r) t = fmaf(qsr[tt], drow[tt], t);
+            } else {
+              for (int tt = 0; tt < r; tt += 4) {
+                const float4 qv = *reinterpret_cast<const float4*>(qsr + tt);
+                const float4 dv = *reinterpret_cast<const float4*>(drow + tt);
+                t = fmaf(qv.x, dv.x, fmaf(qv.y, dv.y, fmaf(qv.z, dv.z, fmaf(qv.w, dv.w, t))));
+              }
+            }
+            s2 = t * (1.f / (float)D);
+          }
+        }
+      }
+      if (primary && ok) {
+        const int64_t o = (row0 + rb + vb) * Gp + vg;
+        a.zs[o] = zb;
+        if (SCORE) a.ss[o] = s2;
+        if (SCORE) {
+          const float av = cv + ((a.variant & kVarFirstOrderMass) ? 0.f : 0.5f * s2);
+          const float mn = fmaxf(lm, av);
+          ll = (lm == -INFINITY ? 0.f : ll * __expf(lm - mn)) + __expf(av - mn);
+          lm = mn;
+        }
+      }
+      if (comp) {
+        // the stage's maximum of ln|b| + zbar per head: lanes holding one head
+        // differ in the bits outside [SH, SH + GB)
+        float gm = cv;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const bool head_bit = o >= (1 << SH) && o < (1 << (SH + GB));
+          if (!head_bit) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+        }
+        // every lane learns every head's stage maximum (from lane g << SH) and raises its references
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float m = __shfl_sync(0xffffffffu, gm, g << SH);
+          if (m > ref[g]) {  // warp-uniform
+            const float f = ref[g] == -INFINITY ? 0.f : __expf(ref[g] - m);
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) acc[g][c] *= f;
+            if (vg == g) wsl *= f;
+            ref[g] = m;
+          }
+        }
+        // the weight of this lane's value, then acc += w vbar over the stage's blocks
+        float rg = ref[0];
+#pragma unroll
+        for (int g = 1; g < G; ++g)
+          if (vg == g) rg = ref[g];
+        const float w = ok ? __expf(cv - rg) : 0.f;
+        if (primary) {
+          swr[vb * G + vg] = w;
+          wsl += w;
+        }
+        __syncwarp();
+        for (int b = 0; b < nbs; ++b) {
+          float x[CPL], wv[G];
+          const float* rowp = (rb + b == patched) ? pv : svb + b * D;
+          lds_vec<CPL>(rowp + CPL * lane, x);
+#pragma unroll
+          for (int g = 0; g < G; ++g) wv[g] = swr[b * G + g];
+#pragma unroll
+          for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) acc[g][c] = fmaf(wv[g], x[c], acc[g][c]);
+        }
+      }
+      __syncwarp();  // the slot and the weights are read
+      if (lane == 0 && j + kSlots < mine) issue(k + kWarps * kSlots, use + kSlots);
+    }
+    if (bad) {
+      for (int i = 0; i < kSlots; ++i) mbar_drain_bounded(bars + warp * kSlots + i);
+      if (lane == 0) *sbad = 1;
+    }
+    uses += (uint32_t)mine;
+    __syncthreads();  // every stage of the segment is consumed: the slots are free
+    if (*sbad) break;  // a copy never arrived: this CTA stops (the status word holds the timeout)
+
+    // ---- the segment's record: the warps' parts per head combined through the slots
+    float* xr = slots;                   // [kWarps][G][4]
+    float* xa = slots + kWarps * G * 4;  // [kWarps][G][D]
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      float m = -INFINITY, l = 0.f, w = 0.f;
+      if (vg == g && primary) {
+        m = lm;
+        l = ll;
+        w = wsl;
+      }
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o), l2 = __shfl_xor_sync(0xffffffffu, l, o);
+        lse_merge(m, l, m2, l2);
+        w += __shfl_xor_sync(0xffffffffu, w, o);
+      }
+      if (lane == 0) *reinterpret_cast<float4*>(xr + (warp * G + g) * 4) = make_float4(m, l, ref[g], w);
+      if (comp)
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) xa[(warp * G + g) * D + CPL * lane + c] = acc[g][c];
+    }
+    __syncthreads();
+    if (warp < G) {
+      const int g = warp;
+      float M = -INFINITY, Ls = 0.f, R = -INFINITY, Ws = 0.f;
+      for (int w = 0; w < kWarps; ++w) {
+        const float4 e = *reinterpret_cast<const float4*>(xr + (w * G + g) * 4);
+        lse_merge(M, Ls, e.x, e.y);
+        R = fmaxf(R, e.z);
+      }
+      float o[CPL];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) o[c] = 0.f;
+      for (int w = 0; w < kWarps; ++w) {
+        const float4 e = *reinterpret_cast<const float4*>(xr + (w * G + g) * 4);
+        const float f = e.z == -INFINITY ? 0.f : __expf(e.z - R);
+        Ws += e.w * f;
+        if (comp)
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) o[c] = fmaf(xa[(w * G + g) * D + CPL * lane + c], f, o[c]);
+      }
+      if (lane == 0) a.rec[(int64_t)si * G + g] = make_float4(M, Ls, comp ? R : -INFINITY, comp ? Ws : 0.f);
+      if (comp) {
+        float* dst = a.comp + ((int64_t)si * G + g) * D + CPL * lane;
+        if constexpr (CPL == 4)
+          *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+        else
+          *reinterpret_cast<float2*>(dst) = make_float2(o[0], o[1]);
+      }
+    }
+    __syncthreads();  // the slots are free for the next segment
+  }
+}
+
+template <int D, int G, int MODE>
+static const void* stream_fn(int r) {
+  if (long_dbar(r)) return reinterpret_cast<const void*>(&k_stream<D, G, MODE, 4, true>);
+  return reinterpret_cast<const void*>(&k_stream<D, G, MODE, (G >= 8 ? 4 : 8), false>);
+}
+
+template <int D, int G, int MODE>
+static cudaError_t launch_stream_mode(const LayerArgs& a, cudaStream_t st, bool pdl) {
+  constexpr bool SCORE = (MODE & kFScore) != 0;
+  constexpr bool COMP = (MODE & kFComp) != 0;
+  const void* fn = stream_fn<D, G, MODE>(a.r);
+  const size_t smem = (size_t)stream_smem_bytes(D, a.r, G, SCORE, COMP);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  LayerArgs args = a;
+  void* argv[] = {&args};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)a.P);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelExC(&cfg, fn, argv);
+}
+
+template <int D, int G>
+static int ctas_per_sm_dg(int r) {
+  const void* fn = stream_fn<D, G, kFusedDecode>(r);
+  const int smem = stream_smem_bytes(D, r, G, true, true);
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThreads, (size_t)smem) != cudaSuccess) return 1;
+  return n;
+}
+
+int stream_ctas_per_sm(int D, int r, int G) {
+  if (D == 128) {
+    switch (G) {
+      case 1: return ctas_per_sm_dg<128, 1>(r);
+      case 2: return ctas_per_sm_dg<128, 2>(r);
+      case 4: return ctas_per_sm_dg<128, 4>(r);
+      default: return ctas_per_sm_dg<128, 8>(r);
+    }
+  }
+  switch (G) {
+    case 1: return ctas_per_sm_dg<64, 1>(r);
+    case 2: return ctas_per_sm_dg<64, 2>(r);
+    case 4: return ctas_per_sm_dg<64, 4>(r);
+    default: return ctas_per_sm_dg<64, 8>(r);
+  }
+}
+
+template <int D, int G>
+static cudaError_t launch_stream_dg(const LayerArgs& a, int mode, cudaStream_t st, bool pdl) {
+  switch (mode) {
+    case kFusedDecode: return launch_stream_mode<D, G, kFusedDecode>(a, st, pdl);
+    case kFusedScoreSelect: return launch_stream_mode<D, G, kFusedScoreSelect>(a, st, pdl);
+    case kFusedAttend: return launch_stream_mode<D, G, kFusedAttend>(a, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_stream(const LayerArgs& a, int mode, cudaStream_t st, bool pdl) {
+#define COMPKV_G(DD)                                          \
+  switch (a.G) {                                              \
+    case 1: return launch_stream_dg<DD, 1>(a, mode, st, pdl); \
+    case 2: return launch_stream_dg<DD, 2>(a, mode, st, pdl); \
+    case 4: return launch_stream_dg<DD, 4>(a, mode, st, pdl); \
+    case 8: return launch_stream_dg<DD, 8>(a, mode, st, pdl); \
+    default: return cudaErrorInvalidValue;                    \
+  }
+  if (a.d == 128) {
+    COMPKV_G(128)
+  } else {
+    COMPKV_G(64)
+  }
+#undef COMPKV_G
+}
+
+size_t stream_smem(int D, int r, int G) { return (size_t)stream_smem_bytes(D, r, G, true, true); }
+
+}  // namespace compkv

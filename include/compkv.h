@@ -97,7 +97,23 @@ typedef struct {
                                 /* capacity_tokens is NULL                          */
   const int *capacity_tokens;   /* optional host array [batch], each a multiple of  */
                                 /* 16: ragged per-sequence capacities; copied       */
+  int variant;                  /* 0 = CompKV as defined; or an OR of the           */
+                                /* COMPKV_VARIANT_* ablation bits below             */
 } compkv_config;
+
+/* Ablations of the method, named in section "전제와 한계" (assumptions and
+ * limits) of the CompKV page; each bit switches one term off in every call of
+ * a context:
+ *   FIRST_ORDER_MASS    phat uses |b| exp(zbar) instead of |b| exp(zbar + sigma2/2)
+ *                       (no second-order mass correction);
+ *   NO_VARIANCE_FACTOR  S_b = sum_g phat_{g,b} (no external variance factor);
+ *   NO_COMPENSATION     unselected blocks are dropped: the output is softmax
+ *                       attention over the selected blocks alone (with G = 1 the
+ *                       selection is then Top-K by estimated mass, the appendix
+ *                       case of section "어떻게 동작하나"). */
+#define COMPKV_VARIANT_FIRST_ORDER_MASS 1
+#define COMPKV_VARIANT_NO_VARIANCE_FACTOR 2
+#define COMPKV_VARIANT_NO_COMPENSATION 4
 
 typedef struct {
   void  *k;                     /* bf16 [num_layers * rows_per_layer][16][d]         */
@@ -163,6 +179,18 @@ compkv_status compkv_attend(compkv_ctx *ctx, int layer, const float *q, const in
 compkv_status compkv_decode(compkv_ctx *ctx, int layer, const float *q, const void *k_new,
                             const void *v_new, float *out, int *sel, void *stream);
 
+/* Steps 1-5 from host memory to host memory, for callers whose inputs and
+ * outputs live on the host: copies q (fp32 [B][Hq][d]), k_new and v_new (bf16
+ * [B][Hkv][d]) into staging space inside the context's scratch, runs the
+ * decode step of compkv_decode on them, copies out (fp32 [B][Hq][d]) and, when
+ * sel_host is not NULL, the selection (int32 [B][Hkv][K]) back, and
+ * synchronises `stream`: when it returns COMPKV_OK, out_host holds the
+ * result.  Host buffers should be page-locked (cudaHostAlloc) for the copies
+ * to run asynchronously.  Device-side problems are reported by
+ * compkv_device_status as for compkv_decode. */
+compkv_status compkv_decode_host(compkv_ctx *ctx, int layer, const float *q_host, const void *k_new_host,
+                                 const void *v_new_host, float *out_host, int *sel_host, void *stream);
+
 /* Scratch-free decode step.  The CompKV page has no counterpart to this call;
  * it exists for callers that cannot allocate device memory at the time they
  * decode (an engine that reserved the whole GPU for its cache pool at
@@ -205,52 +233,44 @@ int64_t compkv_launch_count(const compkv_ctx *ctx);
 /* Per-kernel timing (tracing aid, off by default).  enable = 1: every API
  * call that launches kernels is bracketed by two CUDA events on the launch
  * stream; enable = 2: in addition each kernel of a two-kernel chain is
- * bracketed on its own (the events between them stop a kernel from launching
- * early behind its predecessor, so chains run slower); 0 switches it off;
- * other values give COMPKV_ERR_INVALID_ARG.  compkv_profile_read() synchronises on the recorded events and
- * returns, for one kernel family, the summed device time in milliseconds and
- * the number of launches since the last read (then resets them).  Families:
- * COMPKV_KERNEL_PREFILL, _APPEND, _SCORE, _SELECT, _ATTEND, _DECODE time
- * whole API calls (compkv_prefill, compkv_append, compkv_score_select,
- * compkv_select, compkv_attend, compkv_decode); a score/select, attend or
- * decode call launches two kernels, each timed on its own (enable = 2) under
- * COMPKV_KERNEL_K_SCORE (append + summaries + zbar, sigma2 and the
- * compensation partials) and COMPKV_KERNEL_K_POST (LSE, S_b, forced set +
- * Top-K, attention, compensation and the joint normalisation).
- * Events are host-side CUDA objects; no device memory is allocated. */
+ * bracketed on its own (the events between them stop the second kernel from
+ * launching early behind the first, so chains run slower); 0 switches it
+ * off; other values give COMPKV_ERR_INVALID_ARG.  compkv_profile_read()
+ * synchronises on the recorded events and returns, for one kernel family, the
+ * summed device time in milliseconds and the number of launches since the
+ * last read (then resets them).  Families COMPKV_KERNEL_PREFILL, _APPEND,
+ * _SCORE, _ATTEND and _DECODE time whole API calls (compkv_prefill,
+ * compkv_append, compkv_score_select, compkv_attend, compkv_decode).  A
+ * score/select, attend or decode call launches two kernels, each timed on its
+ * own (enable = 2) under COMPKV_KERNEL_K_STREAM (append, and the stream over
+ * every block summary: zbar, sigma2, the logsumexp parts and the compensation
+ * sums) and COMPKV_KERNEL_K_POST (LSE, S_b, forced set + Top-K, attention,
+ * compensation and the joint normalisation).  Events are host-side CUDA
+ * objects; no device memory is allocated. */
 enum {
   COMPKV_KERNEL_PREFILL = 0,
   COMPKV_KERNEL_APPEND = 1,
   COMPKV_KERNEL_SCORE = 2,
-  COMPKV_KERNEL_SELECT = 3,
+  COMPKV_KERNEL_SELECT = 3,   /* reserved (no call of its own) */
   COMPKV_KERNEL_ATTEND = 4,
   COMPKV_KERNEL_DECODE = 5,
-  COMPKV_KERNEL_K_SCORE = 6,
+  COMPKV_KERNEL_K_STREAM = 6,
   COMPKV_KERNEL_K_POST = 7,
   COMPKV_KERNEL_FAMILIES = 8
 };
 compkv_status compkv_profile_enable(compkv_ctx *ctx, int enable);
 
-/* Work-item trace of the decode kernels (tracing aid, off by default).
- * buf: caller device memory, 8-byte aligned, `bytes` long, zeroed by the
- * caller before a traced call.  Word 0 is unused; record slot i occupies
- * words 1 + 8 i .. 8 + 8 i, for i < (bytes - 8) / 64 (slots beyond are not
- * written):
- *   (cta << 32 | type << 24 | index), unit, t0, t1, t2, x0, x1, x2
- * (t2 = %globaltimer ns when the record was written; unit = sequence * Hkv +
- * head).  With C scoring CTAs (64 blocks each) and U units of S CTAs each
- * (S = min(16, ceil(K / 8)), one cluster per unit), slots [0, C) hold the scoring CTAs (type 0, index = item of the
- * layer: t0 start, t1 its blocks scored, in %globaltimer ns), slots
- * [C, C + U S) the CTAs after the scoring (type 1, or 4 for cluster rank
- * 0: index = rank; t0 start, t1 end of the wait for the scoring kernel, x0 the
- * selection known, x1 the attention done, in %globaltimer ns), then 32 per
- * unit: phase marks of rank 0 (type 5, index = phase: t0, t1 = SM clock
- * counter at the previous mark and at this one; the full radix selection, a
- * rare path, writes its own type 5 marks there in %globaltimer ns) and, at
- * slot 16, the threshold bin's tie list (type 6: t0 = listed entries, t1 =
- * entries still needed, x0 = keys in the threshold bin, x1 = keys above it).
- * A slot a call does not use stays as the caller left it.
- * buf = NULL switches tracing off. */
+/* Work-item trace of the decode chain's second kernel (tracing aid, off by
+ * default).  buf: caller device memory, 8-byte aligned, `bytes` long, zeroed
+ * by the caller before a traced call.  Word 0 is unused; record slot i
+ * occupies words 1 + 8 i .. 8 + 8 i, for i < (bytes - 8) / 64 (slots beyond
+ * are not written).  With P stream CTAs (slots [0, P) are reserved for them)
+ * and C CTAs per unit, the CTA of blockIdx x of the second kernel writes slot
+ * P + x: (x << 32 | 1 << 24 | cluster rank), unit (= sequence * Hkv + head),
+ * t0 its start, t1 the end of its wait for the stream kernel, t2 the
+ * selection known, t3 the attention done, t4 its end (%globaltimer ns), and
+ * the unit's selected block count.  A slot a call does not use stays as the
+ * caller left it.  buf = NULL switches tracing off. */
 compkv_status compkv_trace(compkv_ctx *ctx, void *buf, size_t bytes);
 compkv_status compkv_profile_read(compkv_ctx *ctx, int family, double *total_ms, int64_t *launches);
 

@@ -25,20 +25,36 @@ def f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
 
 
+# compkv_config.variant bits and the oracle switches they correspond to
+VARIANT_FIRST_ORDER_MASS = 1
+VARIANT_NO_VARIANCE_FACTOR = 2
+VARIANT_NO_COMPENSATION = 4
+
+
+def oracle_flags(variant: int) -> dict:
+    return dict(second_order_mass=not (variant & VARIANT_FIRST_ORDER_MASS),
+                variance_factor=not (variant & VARIANT_NO_VARIANCE_FACTOR),
+                compensate=not (variant & VARIANT_NO_COMPENSATION))
+
+
 class Run:
     """One workload: the GPU cache (prefilled) and oracle states for `heads`.
 
     heads: iterable of (layer, seq, head) the oracle follows, or "all".
+    variant: compkv_config.variant of the cache; the oracle runs the same ablation.
     """
 
-    def __init__(self, wl: synth.Workload, heads="all", device="cuda"):
+    def __init__(self, wl: synth.Workload, heads="all", device="cuda", variant=0):
         from block_sparse_kv_summary_gb300.cache import CompKVCache
         self.wl = wl
+        self.variant = variant
+        self.flags = oracle_flags(variant)
         self.lens = synth.sequence_lengths(wl)
         self.caps = synth.capacity_tokens(wl)
         self.cache = CompKVCache(num_layers=wl.layers, batch=wl.batch, num_kv_heads=wl.num_kv_heads,
                                  group_size=wl.group_size, head_dim=wl.head_dim, r=wl.r,
-                                 budget_tokens=wl.budget_tokens, capacity_tokens=self.caps, device=device)
+                                 budget_tokens=wl.budget_tokens, capacity_tokens=self.caps, device=device,
+                                 variant=variant)
         if heads == "all":
             heads = [(l, s, h) for l in range(wl.layers) for s in range(wl.batch) for h in range(wl.num_kv_heads)]
         self.heads = sorted(set(heads))
@@ -86,13 +102,14 @@ class Run:
             att = 0
             while True:
                 q = synth.queries(wl, layer, s, h, step, att).astype(np.float64)
-                sc = O.block_scores(q, st.n, st.kbar, st.Dbar)
+                sc = O.block_scores(q, st.n, st.kbar, st.Dbar, self.flags["second_order_mass"],
+                                    self.flags["variance_factor"])
                 if O.boundary_gap(sc.S, wl.K_blocks) > GAP:
                     break
                 att += 1
                 assert att < 50, "gap guarantee did not converge"
             attempts[(s, h)] = att
-            results[(s, h)] = O.decode_head(st, q, wl.K_blocks)
+            results[(s, h)] = O.decode_head(st, q, wl.K_blocks, **self.flags)
         q = torch.from_numpy(synth.step_queries(wl, layer, step, attempts)).to(self.cache.device)
         return q, results
 

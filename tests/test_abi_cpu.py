@@ -69,7 +69,8 @@ def cfg(**kw):
     (dict(batch=65), "batch"),
     (dict(num_kv_heads=33), "num_kv_heads"),
     (dict(max_tokens=100), "capacity"),
-    (dict(max_tokens=16 * 50000), "does not fit"),
+    (dict(max_tokens=16 * 140000), "does not fit"),
+    (dict(variant=8), "variant"),
 ])
 def test_config_validation(lib, bad, msg):
     c = cfg(**bad)
