@@ -36,7 +36,7 @@ struct Layout {
   int64_t rows_per_layer = 0;
   int max_cap_blocks = 0;
   int K = 0, C = 0, bpc_max = 0, units = 0, rec_cap = 0;
-  size_t off_status = 0, off_lnew = 0, off_rec = 0, off_comp = 0, off_zs = 0, off_ss = 0, off_sel = 0, off_hq = 0,
+  size_t off_status = 0, off_arrive = 0, off_rec = 0, off_comp = 0, off_zs = 0, off_ss = 0, off_sel = 0, off_hq = 0,
          off_hk = 0, off_hv = 0, off_hout = 0, total = 0;
 };
 
@@ -103,7 +103,7 @@ compkv_status make_layout(const compkv_config* c, Layout* L) {
     off = round256(off + bytes);
   };
   region(&L->off_status, 16);
-  region(&L->off_lnew, (size_t)c->batch * sizeof(int));
+  region(&L->off_arrive, 16);
   region(&L->off_rec, (size_t)L->rec_cap * G * 4 * sizeof(float));
   region(&L->off_comp, (size_t)L->rec_cap * G * d * sizeof(float));
   region(&L->off_zs, (size_t)row * Gp * sizeof(float));
@@ -209,7 +209,7 @@ LayerArgs base_args(const compkv_ctx* c, int layer) {
   a.rec_cap = c->lay.rec_cap;
   char* sc = reinterpret_cast<char*>(c->buf.scratch);
   a.status = reinterpret_cast<int*>(sc + c->lay.off_status);
-  a.lnew = reinterpret_cast<int*>(sc + c->lay.off_lnew);
+  a.arrive = reinterpret_cast<int*>(sc + c->lay.off_arrive);
   a.rec = reinterpret_cast<float4*>(sc + c->lay.off_rec);
   a.comp = reinterpret_cast<float*>(sc + c->lay.off_comp);
   a.zs = reinterpret_cast<float*>(sc + c->lay.off_zs);

@@ -59,7 +59,7 @@ struct LayerArgs {
   int rec_cap;                // segment records the scratch holds
   // scratch
   int* status;                // [4]: code, sequence, head, site
-  int* lnew;                  // [B] tokens of each sequence in this call (after its append)
+  int* arrive;                // [1] post clusters past their reads of seq_len (zero between calls)
   float4* rec;                // [rec_cap][G]: max a, sum e^(a - max a), compensation reference, weight sum
   float* comp;                // [rec_cap][G][d]: compensation numerator relative to its reference
   float* zs;                  // [rows][Gp]: zbar per block and head (Gp = max(G, 4))
@@ -124,6 +124,21 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
       "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
+}
+
+// The same with an L2 cache policy (createpolicy), e.g. evict-first for data
+// read once, so that it does not push the kernels' code and scratch out of L2.
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
 }
 
 // Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.

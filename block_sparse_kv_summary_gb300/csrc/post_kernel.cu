@@ -50,7 +50,7 @@ struct InvSqrtP<128> {
 
 // Shared memory of the post kernel, in 4-byte words.
 struct PostLayout {
-  int zsl, ssl, keys, own, bits, csh, U, hf, he, xexp, xfine, xref, lh, tie, stg, stg_w, red, xm, misc, win, bars, total;
+  int zsl, ssl, keys, own, bits, csh, plan, U, hf, he, xexp, xfine, xref, lh, tie, stg, stg_w, red, xm, misc, win, bars, total;
 };
 __host__ __device__ inline int post_items(int D, int G) { return G * D / 4; }
 __host__ __device__ inline int post_ipr(int D, int G, int C) { return (post_items(D, G) + C - 1) / C; }
@@ -65,6 +65,7 @@ __host__ __device__ inline PostLayout post_layout(int D, int G, int C, int bpc_m
   l.bits = o; o += (bpc_max + 31) / 32 + 4;
   o = (o + 3) & ~3;
   l.csh = o; o += G * D;           // this CTA's share of the compensation numerator [G][D]
+  l.plan = o; o += 3 * kMaxBatch + 4;  // tokens, blocks and first segment of every sequence
   // union: selection (local histograms | exchanged histograms | tie lists) / attention staging / CTA partials
   l.U = o;
   l.hf = o;                        // local 12-bit histogram [4096]; later the tie lists [C][kTieCap] x (key, index)
@@ -78,14 +79,14 @@ __host__ __device__ inline PostLayout post_layout(int D, int G, int C, int bpc_m
   l.stg = o;                       // attention: per warp K, V rows (bf16) and z, p [kBlock][G]
   l.stg_w = kBlock * D + 2 * kBlock * G;
   const int attw = kPW * l.stg_w;
-  const int redw = kPW * G * D + 2 * kPW * G;
+  const int redw = kPW * G * D + 2 * kPW * G + G * (kPW + 1) + 2 * G;
   l.red = o;                       // CTA partials after the attention: [kPW][G][D], m, l [kPW][G]
   int uw = selw > attw ? selw : attw;
   uw = uw > redw ? uw : redw;
   o += (uw + 3) & ~3;
   l.xm = o; o += post_ipr(D, G, C) * C * 8;   // merge staging: [items per rank][C][acc4, m, l, -, -]
   l.win = o; o += kRankMax + 4;               // tie winners in rank order
-  l.misc = o; o += 128;
+  l.misc = o; o += 192;
   l.bars = o; o += 2 * (kPW + 2);
   l.total = o;
   return l;
@@ -101,6 +102,10 @@ enum : int {
   kMCntR = 72,       // int [16]: refinement counts, pushed by the peers
   kMScan = 88,       // int [8]: scan scratch
   kMPlan = 96,       // seg, total
+  kMFits = 100,      // [2] bit s: sequence s had room for its token
+  kMSumOwn = 102, kMNtAll, kMMx, kMWBelow,
+  kMOpre = 112,      // [17] exclusive prefix of the CTAs' own-list counts
+  kMTpre = 132,      // [17] exclusive prefix of the CTAs' tie counts
 };
 
 // Exclusive prefix of `v` over the CTA's kPT threads; `total` receives the
@@ -249,7 +254,7 @@ __device__ __noinline__ void refine_select(const uint32_t* keys, unsigned* bits,
 }
 
 template <int D, int G, int MODE>
-__global__ void __launch_bounds__(kPT, 1) k_post(LayerArgs a) {
+__global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   constexpr bool APPEND = (MODE & kFAppend) != 0;
   constexpr bool SEL = (MODE & kFSelect) != 0;
   constexpr bool ATT = (MODE & kFAttend) != 0;
@@ -288,14 +293,18 @@ __global__ void __launch_bounds__(kPT, 1) k_post(LayerArgs a) {
   float* cW = reinterpret_cast<float*>(misc + kMCW);
   uint64_t* bars = reinterpret_cast<uint64_t*>(psm + lay.bars);  // [kPW] attention, [kPW] = zbar/sigma2 load
   const unsigned long long t_start = a.trace ? global_ns() : 0ull;
+  unsigned long long pmk[7] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
+  auto mark = [&](int k) {
+    if (a.trace) pmk[k] = global_ns();
+  };
 
   // ---- set-up before the stream's results are visible
   if (tid <= kPW) mbar_init(bars + tid, 1);
   fence_mbar_init();
   if (SEL) {
-    for (int i = tid; i < 256 + ((256 + C - 1) / C) * 16 + 3 * 256; i += kPT) xexp[i] = 0u;  // xexp, xfine, xref
+    for (int i = tid; i < 256 + ((256 + C - 1) / C) * 16 + 3 * 256; i += kPT) xexp[i] = 0u;  // (xexp,) xfine, xref
   }
-  if (tid < 128) misc[tid] = 0;
+  if (tid < 192) misc[tid] = 0;
   float qr[G][V];
   if (ATT) {
     const float* qg = a.q + ((int64_t)s * a.Hkv + h) * G * D;
@@ -304,19 +313,21 @@ __global__ void __launch_bounds__(kPT, 1) k_post(LayerArgs a) {
 #pragma unroll
       for (int i = 0; i < V; ++i) qr[g][i] = qg[g * D + lane * V + i] * InvSqrtP<D>::v;
   }
-  __syncthreads();
-  cluster_arrive();  // this CTA's exchange histograms are zero (waited for before the first push)
-  pdl_wait();        // the stream kernel's records, zbar and sigma2 are complete and visible
-  pdl_trigger();     // the next call's kernels may launch (they wait for this grid before reading)
-  const unsigned long long t_wait = a.trace ? global_ns() : 0ull;
-
-  // ---- the plan, as the stream kernel made it
-  int* sL = reinterpret_cast<int*>(psm + lay.U);  // [kMaxBatch] borrowed from the union until the histograms
+  __syncthreads();  // misc is zero before warp 0 fills in the plan
+  // the plan, as the stream kernel makes it, from the lengths before this call
+  // (no kernel of this call writes seq_len before every post CTA has read it)
+  int* sL = reinterpret_cast<int*>(psm + lay.plan);  // [kMaxBatch] tokens of each sequence in this call
   int* sN = sL + kMaxBatch;
   int* soff = sN + kMaxBatch;
   if (warp == 0) {
-    if (lane < a.B) sL[lane] = __ldcg(a.lnew + lane);
-    if (lane + 32 < a.B) sL[lane + 32] = __ldcg(a.lnew + lane + 32);
+    bool f0 = false, f1 = false;
+    if (lane < a.B) sL[lane] = call_tokens(__ldcg(a.seq_len + lane), a.cap_blocks[lane], APPEND, &f0);
+    if (lane + 32 < a.B) sL[lane + 32] = call_tokens(__ldcg(a.seq_len + lane + 32), a.cap_blocks[lane + 32], APPEND, &f1);
+    const unsigned m0 = __ballot_sync(0xffffffffu, f0), m1 = __ballot_sync(0xffffffffu, f1);
+    if (lane == 0) {
+      misc[kMFits] = (int)m0;
+      misc[kMFits + 1] = (int)m1;
+    }
     __syncwarp();
     plan_warp(sL, a.B, a.Hkv, a.P, stage_blocks(a.r, G), sN, soff, misc + kMPlan, lane);
   }
@@ -332,7 +343,10 @@ __global__ void __launch_bounds__(kPT, 1) k_post(LayerArgs a) {
   const bool all_sel = N <= K;
   const bool comp_on = !(a.variant & kVarNoCompensation);
   const bool want_keys = SEL && (!all_sel || a.scores);
-  __syncthreads();  // sL, sN, soff are read (the union is reused below)
+  cluster_arrive();  // this CTA's exchange histograms are zero (waited for before the first push)
+  pdl_wait();        // the stream kernel's records, zbar and sigma2 are complete and visible
+  pdl_trigger();     // the next call's kernels may launch (they wait for this grid before reading)
+  const unsigned long long t_wait = a.trace ? global_ns() : 0ull;
 
   // zbar (and sigma2) of this CTA's blocks into shared memory
   if (tid == 0 && nown > 0 && (want_keys || ATT)) {
@@ -345,9 +359,16 @@ __global__ void __launch_bounds__(kPT, 1) k_post(LayerArgs a) {
   if (want_keys && warp < G) {
     const int g = warp;
     float M = -INFINITY, S = 0.f;
-    for (int k = lane; k < nseg; k += 32) {
-      const float4 e = __ldcg(a.rec + (int64_t)(i0 + k) * G + g);
-      lse_merge(M, S, e.x, e.y);
+#pragma unroll 1
+    for (int k0 = 0; k0 < nseg; k0 += 128) {  // four records per lane in flight at once
+      float4 e[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int k = k0 + lane + 32 * j;
+        e[j] = k < nseg ? __ldcg(a.rec + (int64_t)(i0 + k) * G + g) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) lse_merge(M, S, e[j].x, e[j].y);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -357,37 +378,54 @@ __global__ void __launch_bounds__(kPT, 1) k_post(LayerArgs a) {
     if (lane == 0) lse[g] = M + logf(S);
   }
   // this CTA's share of the compensation sums: segment records p, p + C, ...
-  // rescaled to their common maximum; warp g (< G) forms head g's share
+  // rescaled to their common maximum; thread items (head, column quad), every
+  // load issued before any is used
   const bool comp = ATT && comp_on && (!SEL || !all_sel);
   float* csh = psm + lay.csh;  // [G][D]
-  if (comp && warp < G) {
-    const int g = warp;
-    float R = -INFINITY, Wsum = 0.f, A[V];
+  if (comp) {
+    const int nk = p < nseg ? (nseg - 1 - p) / C + 1 : 0;
+#pragma unroll 1
+    for (int i4 = tid; i4 < G * D / 4; i4 += kPT) {
+      const int g = i4 / (D / 4), col = 4 * (i4 % (D / 4));
+      float R = -INFINITY, Wsum = 0.f;
+      float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+      for (int k0 = 0; k0 < nk; k0 += 4) {
+        float4 e[4], v[4];
 #pragma unroll
-    for (int i = 0; i < V; ++i) A[i] = 0.f;
-    for (int k = p; k < nseg; k += C) {
-      const float4 e = __ldcg(a.rec + (int64_t)(i0 + k) * G + g);
-      if (e.z == -INFINITY) continue;
-      const float mn = fmaxf(R, e.z);
-      const float fo = R == -INFINITY ? 0.f : __expf(R - mn);
-      const float fn = __expf(e.z - mn);
-      const float* src = a.comp + ((int64_t)(i0 + k) * G + g) * D + lane * V;
+        for (int j = 0; j < 4; ++j) {
+          const int rec = i0 + p + C * (k0 + j);
+          const bool ok = k0 + j < nk;
+          e[j] = ok ? __ldcg(a.rec + (int64_t)rec * G + g) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+          v[j] = ok ? __ldcg(reinterpret_cast<const float4*>(a.comp + ((int64_t)rec * G + g) * D + col))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
 #pragma unroll
-      for (int i = 0; i < V; ++i) A[i] = A[i] * fo + __ldcg(src + i) * fn;
-      Wsum = Wsum * fo + e.w * fn;
-      R = mn;
-    }
-#pragma unroll
-    for (int i = 0; i < V; ++i) csh[g * D + lane * V + i] = A[i];
-    if (lane == 0) {
-      cR[g] = R;
-      cW[g] = Wsum;
+        for (int j = 0; j < 4; ++j) {
+          if (e[j].z == -INFINITY) continue;
+          const float mn = fmaxf(R, e[j].z);
+          const float fo = R == -INFINITY ? 0.f : __expf(R - mn);
+          const float fn = __expf(e[j].z - mn);
+          A.x = A.x * fo + v[j].x * fn;
+          A.y = A.y * fo + v[j].y * fn;
+          A.z = A.z * fo + v[j].z * fn;
+          A.w = A.w * fo + v[j].w * fn;
+          Wsum = Wsum * fo + e[j].w * fn;
+          R = mn;
+        }
+      }
+      *reinterpret_cast<float4*>(csh + g * D + col) = A;
+      if (col == 0) {
+        cR[g] = R;
+        cW[g] = Wsum;
+      }
     }
   }
   if (tid == 0 && nown > 0 && (want_keys || ATT)) {
     if (!mbar_wait_bounded(bars + kPW, 0u, a.status, s, h, 20)) misc[kMBad] = 1;
   }
   __syncthreads();  // lse, zsl, ssl in place
+  mark(0);
 
   // ---- a, b. keys, histograms, threshold
   int nsel_own = 0;
@@ -422,36 +460,46 @@ __global__ void __launch_bounds__(kPT, 1) k_post(LayerArgs a) {
     }
     __syncthreads();
   }
+  mark(1);
   cluster_wait();  // every peer's exchange histograms are zero
   if (SEL && !all_sel && need0 > 0) {
-    // push this CTA's counts: exponent bins to rank 0, the 16 fine bins of exponent e to rank e % C
+    // push this CTA's counts: the 16 fine bins of exponent e to rank e % C (no single rank
+    // collects them all)
     {
       const int e = tid;  // kPT == 256 exponents
-      const uint32_t ce = he[e];
-      if (ce) {
-        red_peer_add(peer_smem(xexp + e, 0), ce);
+      if (he[e]) {
         const uint32_t fo = peer_smem(xfine + (e / C) * 16, (uint32_t)(e % C));
+        const uint4* hv = reinterpret_cast<const uint4*>(hf + e * 16);
 #pragma unroll
-        for (int f = 0; f < 16; ++f) {
-          const uint32_t cf = hf[e * 16 + f];
-          if (cf) red_peer_add(fo + 4u * f, cf);
+        for (int k = 0; k < 4; ++k) {
+          const uint4 v = hv[k];
+          if (v.x) red_peer_add(fo + 16u * k, v.x);
+          if (v.y) red_peer_add(fo + 16u * k + 4u, v.y);
+          if (v.z) red_peer_add(fo + 16u * k + 8u, v.z);
+          if (v.w) red_peer_add(fo + 16u * k + 12u, v.w);
         }
       }
     }
-    cluster_sync_all();  // barrier 1: rank 0 holds the exponent histogram, rank e % C the fine bins of e
-    // the threshold exponent from the top of rank 0's histogram (thread t: exponent 255 - t), then the fine bin
+    cluster_sync_all();  // barrier 1: rank e % C holds the cluster's 16 fine bins of exponent e
+    mark(2);
+    // thread t takes exponent 255 - t: its 16 fine bins from their owner, their sum scanned from
+    // the top; the thread where the count of larger keys reaches K - 3 finds the fine bin
     const int ex = 255 - tid;
-    const int c = (int)ld_peer_u32(peer_smem(xexp + ex, 0));
-    int tot;
-    const int before = cta_exclusive_scan(c, misc + kMScan, &tot, lane, warp);
-    if (before < need0 && need0 <= before + c) {
-      uint32_t c16[16];
+    uint32_t c16[16];
+    {
       const uint32_t fo = peer_smem(xfine + (ex / C) * 16, (uint32_t)(ex % C));
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const uint4 v = ld_peer_u4(fo + 16u * k);
         c16[4 * k] = v.x; c16[4 * k + 1] = v.y; c16[4 * k + 2] = v.z; c16[4 * k + 3] = v.w;
       }
+    }
+    int c = 0;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) c += (int)c16[k];
+    int tot;
+    const int before = cta_exclusive_scan(c, misc + kMScan, &tot, lane, warp);
+    if (before < need0 && need0 <= before + c) {
       int run = before;
       for (int k = 15; k >= 0; --k) {
         if (run < need0 && need0 <= run + (int)c16[k]) {
@@ -467,6 +515,7 @@ __global__ void __launch_bounds__(kPT, 1) k_post(LayerArgs a) {
     need = need0 - misc[kMAbove];
     take_all = misc[kMCntT] == need;
   }
+  mark(3);
 
   // ---- c. classification, the exchange of counts and tie lists, the selection
   int tot_sel = 0;     // selected blocks of the unit
@@ -515,13 +564,37 @@ __global__ void __launch_bounds__(kPT, 1) k_post(LayerArgs a) {
           prefetch_l2(a.k + row * kBlock * D, kBlock * D * 2);
           prefetch_l2(a.v + row * kBlock * D, kBlock * D * 2);
         }
+      mark(4);
       cluster_sync_all();  // barrier 2: every CTA holds every count and tie list
-      int mx = 0, nt_all = 0;
-      for (int q = 0; q < C; ++q) {
-        sum_own += cnt[2 * q];
-        mx = max(mx, cnt[2 * q + 1]);
-        nt_all += cnt[2 * q + 1];
+      mark(5);
+      // warp 0: prefix sums of the CTAs' counts (own lists, ties), their totals and the largest tie count
+      int* opre = misc + kMOpre;
+      int* tpre = misc + kMTpre;
+      if (warp == 0) {
+        const int co = lane < C ? cnt[2 * lane] : 0, ct = lane < C ? cnt[2 * lane + 1] : 0;
+        int io = co, it = ct, mxl = ct;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, io, o), y2 = __shfl_up_sync(0xffffffffu, it, o);
+          if (lane >= o) {
+            io += y;
+            it += y2;
+          }
+          mxl = max(mxl, __shfl_xor_sync(0xffffffffu, mxl, o));
+        }
+        if (lane <= C) {
+          opre[lane] = io - co;
+          tpre[lane] = it - ct;
+        }
+        if (lane == 31) {
+          misc[kMSumOwn] = io;
+          misc[kMNtAll] = it;
+        }
+        if (lane == 0) misc[kMMx] = mxl;
       }
+      __syncthreads();
+      sum_own = misc[kMSumOwn];
+      const int nt_all = misc[kMNtAll], mx = misc[kMMx];
       if (!take_all && need > 0 && (mx > kTieCap || nt_all > kRankMax)) {
         // rare: resolve the threshold bin by more radix digits, then exchange the final counts
         refine_select(keys, bits, nown, b_lo, N, T, need, xref, lh, misc, C, p);
@@ -533,36 +606,53 @@ __global__ void __launch_bounds__(kPT, 1) k_post(LayerArgs a) {
         nsel_own = misc[kMOwn];
         if (tid < C) st_peer_u2(peer_smem(cnt + 2 * p, (uint32_t)tid), make_uint2((uint32_t)nsel_own, 0u));
         cluster_sync_all();
-        sum_own = 0;
-        for (int q = 0; q < C; ++q) sum_own += cnt[2 * q];
+        if (warp == 0) {
+          const int co = lane < C ? cnt[2 * lane] : 0;
+          int io = co;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, io, o);
+            if (lane >= o) io += y;
+          }
+          if (lane <= C) opre[lane] = io - co;
+          if (lane == 31) misc[kMSumOwn] = io;
+        }
+        __syncthreads();
+        sum_own = misc[kMSumOwn];
         nwin = 0;
       } else if (!take_all && need > 0) {
-        // rank every tie entry among all (key desc, block asc); the first `need` win, kept in rank order
-        __syncthreads();  // win[] (local tie indices) is read
+        // rank every tie entry among all (key desc, block asc), one warp per entry over a
+        // dense copy of the lists; the first `need` win, kept in rank order
+        uint2* dense = reinterpret_cast<uint2*>(hf + 2 * kMaxC * kTieCap);
         for (int e = tid; e < C * kTieCap; e += kPT) {
           const int q = e / kTieCap, k = e % kTieCap;
-          if (k >= cnt[2 * q + 1]) continue;
-          const uint2 me = tie[e];
+          if (k < cnt[2 * q + 1]) dense[tpre[q] + k] = tie[e];
+        }
+        __syncthreads();
+        for (int j = warp; j < nt_all; j += kPW) {
+          const uint2 me = dense[j];
           int rank = 0;
-          for (int q2 = 0; q2 < C; ++q2) {
-            const int n2 = cnt[2 * q2 + 1];
-            for (int k2 = 0; k2 < n2; ++k2) {
-              const uint2 o = tie[q2 * kTieCap + k2];
-              rank += (o.x > me.x) || (o.x == me.x && o.y < me.y);
-            }
+          for (int j2 = lane; j2 < nt_all; j2 += 32) {
+            const uint2 o = dense[j2];
+            rank += (o.x > me.x) || (o.x == me.x && o.y < me.y);
           }
-          if (rank < need) win[rank] = (int)me.y;
+          rank = __reduce_add_sync(0xffffffffu, rank);
+          if (lane == 0 && rank < need) win[rank] = (int)me.y;
         }
         nwin = need;
         __syncthreads();
       }
       tot_sel = sum_own + nwin;
-      // this CTA's offset in the ascending selection: the lists and winners of the lower ranks
-      int before = 0;
-      for (int q = 0; q < p; ++q) before += cnt[2 * q];
-      for (int k = 0; k < nwin; ++k)
-        if (win[k] < b_lo) ++before;
-      own_base = before;
+      // this CTA's offset in the ascending selection: the lists of the lower ranks and the
+      // tie winners below this CTA's blocks
+      if (warp == 0) {
+        int below = 0;
+        for (int k = lane; k < nwin; k += 32) below += win[k] < b_lo;
+        below = __reduce_add_sync(0xffffffffu, below);
+        if (lane == 0) misc[kMWBelow] = below;
+      }
+      __syncthreads();
+      own_base = opre[p] + misc[kMWBelow];
     } else {
       tot_sel = N;
       sum_own = N;
@@ -573,17 +663,19 @@ __global__ void __launch_bounds__(kPT, 1) k_post(LayerArgs a) {
     for (int e = tid; e < nsel_own; e += kPT) {
       const int b = own[e];
       int pos = own_base + e;
-      for (int k = 0; k < nwin; ++k)
-        if (win[k] >= b_lo && win[k] < b) ++pos;
+      for (int k = 0; k < nwin; ++k) pos += (win[k] >= b_lo && win[k] < b);
       if (pos < K) selrow[pos] = b;
     }
     for (int k = tid; k < nwin; k += kPT) {
       const int b = win[k];
       if (b < b_lo || b >= b_hi) continue;
-      int pos = own_base;
-      for (int e = 0; e < nsel_own; ++e) pos += own[e] < b;
-      for (int k2 = 0; k2 < nwin; ++k2)
-        if (win[k2] >= b_lo && win[k2] < b) ++pos;
+      int lo = 0, hi = nsel_own;  // own blocks below b (the list is ascending)
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (own[mid] < b) lo = mid + 1; else hi = mid;
+      }
+      int pos = own_base + lo;
+      for (int k2 = 0; k2 < nwin; ++k2) pos += (win[k2] >= b_lo && win[k2] < b);
       if (pos < K) selrow[pos] = b;
     }
     if (p == 0) {
@@ -612,6 +704,12 @@ __global__ void __launch_bounds__(kPT, 1) k_post(LayerArgs a) {
     if ((misc[kMBad] & 2) && p == 0 && tid == 0) set_error(a.status, kDevBadSelection, s, h, 61);
   }
   const unsigned long long t_sel = a.trace ? global_ns() : 0ull;
+  if (tid == 0 && a.trace && a.P + (int)(gridDim.x + blockIdx.x) < a.trace_cap) {
+    unsigned long long* rr = a.trace + 1 + 8 * (int64_t)(a.P + gridDim.x + blockIdx.x);
+    rr[0] = ((unsigned long long)blockIdx.x << 32) | (2ull << 24) | (unsigned)misc[kMNtie];
+#pragma unroll
+    for (int k = 0; k < 7; ++k) rr[1 + k] = pmk[k];
+  }
   if (SEL && !ATT) {
     // score/select only: no peer reads this CTA's shared memory after the barrier
     cluster_sync_all();
@@ -652,9 +750,10 @@ __global__ void __launch_bounds__(kPT, 1) k_post(LayerArgs a) {
       if (all_sel) {
         b = j;
       } else if (j < sum_own) {
-        int q = 0, base = 0;
-        while (q + 1 < C && base + cnt[2 * q] <= j) base += cnt[2 * q++];
-        b = (int)ld_peer_u32(peer_smem(own + (j - base), (uint32_t)q));
+        const int* opre = misc + kMOpre;
+        const unsigned bal = __ballot_sync(0xffffffffu, lane < C && opre[lane] <= j);
+        const int q = 31 - __clz(bal);  // the highest CTA whose list starts at or before j
+        b = (int)ld_peer_u32(peer_smem(own + (j - opre[q]), (uint32_t)q));
       } else {
         b = win[j - sum_own];
       }
@@ -669,10 +768,10 @@ __global__ void __launch_bounds__(kPT, 1) k_post(LayerArgs a) {
     const int64_t row = row0 + b;
     __syncwarp();  // the staging's previous contents are read
     if (lane == 0) {
-      fence_proxy_async_global();
       mbar_arrive_expect_tx(bars + warp, 2u * kBlock * D * 2u);
-      bulk_g2s(wk, a.k + row * kBlock * D, kBlock * D * 2u, bars + warp);
-      bulk_g2s(wv, a.v + row * kBlock * D, kBlock * D * 2u, bars + warp);
+      const uint64_t pol = policy_evict_first();
+      bulk_g2s_hint(wk, a.k + row * kBlock * D, kBlock * D * 2u, bars + warp, pol);
+      bulk_g2s_hint(wv, a.v + row * kBlock * D, kBlock * D * 2u, bars + warp, pol);
     }
     float vbr[V];
 #pragma unroll
@@ -811,72 +910,109 @@ __global__ void __launch_bounds__(kPT, 1) k_post(LayerArgs a) {
     for (int i = 0; i < V; ++i) red_a[(warp * G + g) * D + lane * V + i] = acc[g][i];
   }
   __syncthreads();
+  // per head, once: the common maximum of the warps' parts (and the compensation share)
+  // and each part's factor (warp g: lane w takes warp w, lane kPW the share)
+  float* fac = red_l + kPW * G;  // [G][kPW + 1] factors, then [G] maxima and [G] sums
+  float* facM = fac + G * (kPW + 1);
+  float* facL = facM + G;
+  if (warp < G) {
+    const int g = warp;
+    const bool sh = lane == kPW && comp_blk;
+    const float mw = lane < kPW ? red_m[lane * G + g] : (sh ? cR[g] : -INFINITY);
+    const float lw = lane < kPW ? red_l[lane * G + g] : (sh ? cW[g] : 0.f);
+    const float M = warp_max(mw);
+    const float f = (M == -INFINITY || mw == -INFINITY) ? 0.f : __expf(mw - M);
+    const float ls = warp_sum(lw * f);
+    if (lane <= kPW) fac[g * (kPW + 1) + lane] = f;
+    if (lane == 0) {
+      facM[g] = M;
+      facL[g] = ls;
+    }
+  }
+  __syncthreads();
   // per float4 column item: combine, then push to the rank that merges it
   const int items = G * D / 4;
   const int ipr = post_ipr(D, G, C);
   for (int i4 = tid; i4 < items; i4 += kPT) {
     const int g = (4 * i4) / D, col = (4 * i4) % D;
-    float M = comp_blk ? cR[g] : -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kPW; ++w) M = fmaxf(M, red_m[w * G + g]);
-    float ls = 0.f;
     float4 as = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < kPW; ++w) {
-        const float mw = red_m[w * G + g];
-        const float f = (mw == -INFINITY) ? 0.f : __expf(mw - M);
-        ls += red_l[w * G + g] * f;
-        const float4 x = *reinterpret_cast<const float4*>(red_a + (w * G + g) * D + col);
-        as.x += x.x * f;
-        as.y += x.y * f;
-        as.z += x.z * f;
-        as.w += x.w * f;
-      }
-      if (comp_blk && cR[g] != -INFINITY) {
-        const float f = __expf(cR[g] - M);
-        const float4 x = *reinterpret_cast<const float4*>(csh + g * D + col);
-        ls += cW[g] * f;
-        as.x += x.x * f;
-        as.y += x.y * f;
-        as.z += x.z * f;
-        as.w += x.w * f;
-      }
+    for (int w = 0; w < kPW; ++w) {
+      const float f = fac[g * (kPW + 1) + w];
+      const float4 x = *reinterpret_cast<const float4*>(red_a + (w * G + g) * D + col);
+      as.x = fmaf(x.x, f, as.x);
+      as.y = fmaf(x.y, f, as.y);
+      as.z = fmaf(x.z, f, as.z);
+      as.w = fmaf(x.w, f, as.w);
+    }
+    if (comp_blk) {
+      const float f = fac[g * (kPW + 1) + kPW];
+      const float4 x = *reinterpret_cast<const float4*>(csh + g * D + col);
+      as.x = fmaf(x.x, f, as.x);
+      as.y = fmaf(x.y, f, as.y);
+      as.z = fmaf(x.z, f, as.z);
+      as.w = fmaf(x.w, f, as.w);
     }
     const int rk = i4 / ipr, il = i4 - rk * ipr;
     const uint32_t dst = peer_smem(xm + (il * C + p) * 8, (uint32_t)rk);
     st_peer_f4(dst, as);
-    st_peer_u2(dst + 16u, make_uint2(__float_as_uint(M), __float_as_uint(ls)));
-  }
-  if (APPEND && blockIdx.x == 0 && tid < a.B) {
-    // the lengths after this call's append (a sequence at capacity keeps its length)
-    const int Lold = a.seq_len[tid];
-    const int Ln = __ldcg(a.lnew + tid);
-    if (Ln == Lold + 1) a.seq_len[tid] = Ln;
+    st_peer_u2(dst + 16u, make_uint2(__float_as_uint(facM[g]), __float_as_uint(facL[g])));
   }
   cluster_sync_all();  // barrier 3: every partial of this rank's columns is here; no CTA touches a peer after this
-  const int i_lo = p * ipr, i_hi = min(items, i_lo + ipr);
-  if (tid < i_hi - i_lo) {
-    const int i4 = i_lo + tid, g = (4 * i4) / D, col = (4 * i4) % D;
-    const float* e0 = xm + tid * C * 8;
-    float M = -INFINITY;
-    for (int q = 0; q < C; ++q) M = fmaxf(M, e0[q * 8 + 4]);
-    float ls = 0.f;
-    float4 as = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (M != -INFINITY)
-      for (int q = 0; q < C; ++q) {
-        const float* e = e0 + q * 8;
-        const float mq = e[4];
-        const float f = mq == -INFINITY ? 0.f : __expf(mq - M);
-        ls = fmaf(e[5], f, ls);
-        as.x = fmaf(e[0], f, as.x);
-        as.y = fmaf(e[1], f, as.y);
-        as.z = fmaf(e[2], f, as.z);
-        as.w = fmaf(e[3], f, as.w);
+  if (APPEND && p == 0 && tid == 0) {
+    // every CTA of this cluster has read seq_len; the last cluster to get here
+    // writes the lengths after this call's append (a sequence at capacity keeps its own)
+    __threadfence();
+    if (atomicAdd(a.arrive, 1) == (int)(gridDim.x / C) - 1) {
+      for (int x = 0; x < a.B; ++x) {
+        const bool f = ((x < 32 ? misc[kMFits] >> x : misc[kMFits + 1] >> (x - 32)) & 1) != 0;
+        if (f) a.seq_len[x] = sL[x];
       }
-    const float inv = ls > 0.f ? 1.f / ls : 0.f;
-    float* out = a.out + ((int64_t)s * a.Hkv + h) * G * D;
-    *reinterpret_cast<float4*>(out + g * D + col) = make_float4(as.x * inv, as.y * inv, as.z * inv, as.w * inv);
+      a.arrive[0] = 0;
+      __threadfence();
+    }
+  }
+  // this rank's column items: Cp (C rounded up to a power of two) lanes per item, lane q
+  // takes CTA q's partial; the partials are merged across those lanes
+  {
+    const int i_lo = p * ipr, i_hi = min(items, i_lo + ipr);
+    int Cp = 1;
+    while (Cp < C) Cp <<= 1;
+    const int nx = max(0, i_hi - i_lo) * Cp;  // groups of Cp lanes never straddle a warp (Cp divides 32)
+    for (int x0 = warp * 32; x0 < nx; x0 += kPT) {
+      const int x = x0 + lane;
+      const bool live = x < nx;
+      const int il = x / Cp, q = x % Cp;
+      const int i4 = i_lo + il, g = (4 * i4) / D, col = (4 * i4) % D;
+      float4 as = make_float4(0.f, 0.f, 0.f, 0.f);
+      float mq = -INFINITY, lq = 0.f;
+      if (live && q < C) {
+        const float* e = xm + (il * C + q) * 8;
+        as = *reinterpret_cast<const float4*>(e);
+        mq = e[4];
+        lq = e[5];
+      }
+      float M = mq;
+      for (int o = 1; o < Cp; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float f = (M == -INFINITY || mq == -INFINITY) ? 0.f : __expf(mq - M);
+      as.x *= f;
+      as.y *= f;
+      as.z *= f;
+      as.w *= f;
+      lq *= f;
+      for (int o = 1; o < Cp; o <<= 1) {
+        as.x += __shfl_xor_sync(0xffffffffu, as.x, o);
+        as.y += __shfl_xor_sync(0xffffffffu, as.y, o);
+        as.z += __shfl_xor_sync(0xffffffffu, as.z, o);
+        as.w += __shfl_xor_sync(0xffffffffu, as.w, o);
+        lq += __shfl_xor_sync(0xffffffffu, lq, o);
+      }
+      if (live && q == 0) {
+        const float inv = lq > 0.f ? 1.f / lq : 0.f;
+        float* out = a.out + ((int64_t)s * a.Hkv + h) * G * D;
+        *reinterpret_cast<float4*>(out + g * D + col) = make_float4(as.x * inv, as.y * inv, as.z * inv, as.w * inv);
+      }
+    }
   }
   if (tid == 0 && a.trace && a.P + (int)blockIdx.x < a.trace_cap) {
     unsigned long long* rr = a.trace + 1 + 8 * (int64_t)(a.P + blockIdx.x);

@@ -33,7 +33,7 @@ namespace compkv {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = 32 * kWarps;
-constexpr int kSlots = 2;  // stage slots per warp
+constexpr int kSlots = 1;  // stage slots per warp (two CTAs per multiprocessor)
 
 template <int D>
 struct InvSqrt;
@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
   int* sbad = sfits + 2;                         // a wait of this CTA ran out
   uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(sbad + 1) + 7) & ~uintptr_t(7));
   uint64_t* patch_bar = bars + kWarps * kSlots;
+  const unsigned long long t_start = a.trace ? global_ns() : 0ull;
   if (threadIdx.x < kWarps * kSlots + 1) mbar_init(bars + threadIdx.x, 1);
   if (threadIdx.x == 0) *sbad = 0;
   fence_mbar_init();
@@ -146,19 +147,16 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
     }
     __syncwarp();
     plan_warp(sL, a.B, a.Hkv, a.P, SB, sN, soff, sseg, lane);
-    if (blockIdx.x == 0) {
-      if (s0 < a.B) {
-        a.lnew[s0] = sL[s0];
-        if (APPEND && !f0) set_error(a.status, kDevCapacity, s0, -1, 1);
-      }
-      if (s1 < a.B) {
-        a.lnew[s1] = sL[s1];
-        if (APPEND && !f1) set_error(a.status, kDevCapacity, s1, -1, 1);
-      }
+    if (APPEND && blockIdx.x == 0) {
+      if (s0 < a.B && !f0) set_error(a.status, kDevCapacity, s0, -1, 1);
+      if (s1 < a.B && !f1) set_error(a.status, kDevCapacity, s1, -1, 1);
     }
   }
   __syncthreads();
   const int seg = *sseg, total = soff[a.B];
+  const unsigned long long t_plan = a.trace ? global_ns() : 0ull;
+  unsigned long long t_first = 0ull, t_r1 = 0ull, t_r2 = 0ull, t_r3 = 0ull;
+  int nseg_done = 0;
   int npatch = 0;     // patches completed in this CTA (phases of patch_bar)
   uint32_t uses = 0;  // stages this warp has consumed: slot uses % kSlots, phase (uses / kSlots) & 1
   float* swr = sw + warp * SB * G;
@@ -177,15 +175,18 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
     const bool comp = COMP && !(a.variant & kVarNoCompensation) && (!SELMODE || N > a.K);
     const bool dbulk = SCORE && r >= 4;
     // ---- this warp's copies: its j-th stage of the segment is stage warp + kWarps j
+    // the summaries are read once per call: evict-first in L2, so that they do not
+    // push the kernels' code and the small scratch arrays out of it
+    const uint64_t pol = policy_evict_first();
     auto issue = [&](int k, uint32_t use) {
       float* st = slots + (warp * kSlots + (int)(use % kSlots)) * slot_f;
       const int rb = k * SB, n = min(SB, nb - rb);
       const uint32_t bytes = (uint32_t)n * (uint32_t)(D * 4 * (comp ? 2 : 1) + (dbulk ? r * 4 : 0));
       uint64_t* bar = bars + warp * kSlots + (use % kSlots);
       mbar_arrive_expect_tx(bar, bytes);
-      bulk_g2s(st, a.kbar + (row0 + rb) * D, (uint32_t)n * D * 4u, bar);
-      if (comp) bulk_g2s(st + SB * D, a.vbar + (row0 + rb) * D, (uint32_t)n * D * 4u, bar);
-      if (dbulk) bulk_g2s(st + SB * D * (comp ? 2 : 1), a.dbar + (row0 + rb) * r, (uint32_t)n * r * 4u, bar);
+      bulk_g2s_hint(st, a.kbar + (row0 + rb) * D, (uint32_t)n * D * 4u, bar, pol);
+      if (comp) bulk_g2s_hint(st + SB * D, a.vbar + (row0 + rb) * D, (uint32_t)n * D * 4u, bar, pol);
+      if (dbulk) bulk_g2s_hint(st + SB * D * (comp ? 2 : 1), a.dbar + (row0 + rb) * r, (uint32_t)n * r * 4u, bar, pol);
     };
     const int mine = warp < ns ? (ns - 1 - warp) / kWarps + 1 : 0;  // stages of this warp
     if (lane == 0)
@@ -236,47 +237,62 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
       const int64_t row = row_of(a, s, h, N - 1);
       const int c0 = CPL * lane;
       const int64_t nw_off = ((int64_t)s * a.Hkv + h) * D + c0;
-      float kx[kBlock][CPL];
-      float ksum[CPL], vsum[CPL];
+      const __nv_bfloat16* kb = a.k + row * kBlock * D + c0;
+      const __nv_bfloat16* vbp = a.v + row * kBlock * D + c0;
+      // pass 1: the new token into its slot; sums of the keys and values (all loads
+      // independent: one round trip)
+      store_bf16_raw<CPL>(a.k + (row * kBlock + n - 1) * D + c0, a.k_new + nw_off);
+      store_bf16_raw<CPL>(a.v + (row * kBlock + n - 1) * D + c0, a.v_new + nw_off);
+      float ksum[CPL], vsum[CPL], kn[CPL];
+      load_bf16<CPL>(a.k_new + nw_off, kn);
 #pragma unroll
       for (int c = 0; c < CPL; ++c) ksum[c] = vsum[c] = 0.f;
 #pragma unroll
       for (int j = 0; j < kBlock; ++j) {
-        float kf[CPL], vf[CPL];
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) kf[c] = vf[c] = 0.f;
         if (j < n) {
-          const __nv_bfloat16* kp = (j == n - 1) ? a.k_new + nw_off : a.k + (row * kBlock + j) * D + c0;
-          const __nv_bfloat16* vp = (j == n - 1) ? a.v_new + nw_off : a.v + (row * kBlock + j) * D + c0;
-          load_bf16<CPL>(kp, kf);
-          load_bf16<CPL>(vp, vf);
-          if (j == n - 1) {
-            store_bf16_raw<CPL>(a.k + (row * kBlock + j) * D + c0, a.k_new + nw_off);
-            store_bf16_raw<CPL>(a.v + (row * kBlock + j) * D + c0, a.v_new + nw_off);
+          float kf[CPL], vf[CPL];
+          load_bf16<CPL>(j == n - 1 ? a.k_new + nw_off : kb + j * D, kf);
+          load_bf16<CPL>(j == n - 1 ? a.v_new + nw_off : vbp + j * D, vf);
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {
+            ksum[c] += kf[c];
+            vsum[c] += vf[c];
           }
         }
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-          kx[j][c] = kf[c];
-          ksum[c] += kf[c];
-          vsum[c] += vf[c];
-        }
       }
-      float var[CPL];
+      float mk[CPL], var[CPL];
 #pragma unroll
       for (int c = 0; c < CPL; ++c) {
-        const float mk = ksum[c] / (float)n, mv = vsum[c] / (float)n;
-        pk[c0 + c] = mk;
-        pv[c0 + c] = mv;
-        a.kbar[row * D + c0 + c] = mk;
-        a.vbar[row * D + c0 + c] = mv;
-        float t = 0.f;
+        mk[c] = ksum[c] / (float)n;
+        var[c] = 0.f;
+      }
+      // pass 2: population variance about the mean (the old tokens re-read, now cached
+      // close by; the new one kept)
 #pragma unroll
-        for (int j = 0; j < kBlock; ++j) {
-          const float dv = j < n ? kx[j][c] - mk : 0.f;
-          t = fmaf(dv, dv, t);
+      for (int j = 0; j < kBlock; ++j) {
+        if (j < n) {
+          float kf[CPL];
+          if (j == n - 1) {
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) kf[c] = kn[c];
+          } else {
+            load_bf16<CPL>(kb + j * D, kf);
+          }
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {
+            const float dv = kf[c] - mk[c];
+            var[c] = fmaf(dv, dv, var[c]);
+          }
         }
-        var[c] = t / (float)n;
+      }
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        const float mv = vsum[c] / (float)n;
+        var[c] /= (float)n;
+        pk[c0 + c] = mk[c];
+        pv[c0 + c] = mv;
+        a.kbar[row * D + c0 + c] = mk[c];
+        a.vbar[row * D + c0 + c] = mv;
       }
       // Dbar_t: mean of the variances over coordinate group t = [t*D/r, (t+1)*D/r)
       const int gs = D / r;
@@ -469,50 +485,66 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
     }
     uses += (uint32_t)mine;
     __syncthreads();  // every stage of the segment is consumed: the slots are free
+    if (!nseg_done && a.trace) t_first = global_ns();
+    ++nseg_done;
     if (*sbad) break;  // a copy never arrived: this CTA stops (the status word holds the timeout)
 
     // ---- the segment's record: the warps' parts per head combined through the slots
+    // (this runs once per segment: short dependency chains, all heads at once)
     float* xr = slots;                   // [kWarps][G][4]
     float* xa = slots + kWarps * G * 4;  // [kWarps][G][D]
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float m = -INFINITY, l = 0.f, w = 0.f;
-      if (vg == g && primary) {
-        m = lm;
-        l = ll;
-        w = wsl;
-      }
+    {
+      // lanes holding one head differ in the lane bits outside [SH, SH + GB): reduce over those
+      float m = primary ? lm : -INFINITY, l = primary ? ll : 0.f, w = primary ? wsl : 0.f;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
+        if (o >= (1 << SH) && o < (1 << (SH + GB))) continue;
         const float m2 = __shfl_xor_sync(0xffffffffu, m, o), l2 = __shfl_xor_sync(0xffffffffu, l, o);
         lse_merge(m, l, m2, l2);
         w += __shfl_xor_sync(0xffffffffu, w, o);
       }
-      if (lane == 0) *reinterpret_cast<float4*>(xr + (warp * G + g) * 4) = make_float4(m, l, ref[g], w);
-      if (comp)
+      if ((lane & ~(((1 << GB) - 1) << SH)) == 0) {  // lane vg << SH holds head vg
+        float rg = ref[0];
+#pragma unroll
+        for (int gg = 1; gg < G; ++gg)
+          if (vg == gg) rg = ref[gg];
+        *reinterpret_cast<float4*>(xr + (warp * G + vg) * 4) = make_float4(m, l, rg, w);
+      }
+    }
+    if (comp)
+#pragma unroll
+      for (int g = 0; g < G; ++g)
 #pragma unroll
         for (int c = 0; c < CPL; ++c) xa[(warp * G + g) * D + CPL * lane + c] = acc[g][c];
-    }
+    if (nseg_done == 1 && a.trace) t_r1 = global_ns();
     __syncthreads();
+    if (nseg_done == 1 && a.trace) t_r2 = global_ns();
     if (warp < G) {
       const int g = warp;
-      float M = -INFINITY, Ls = 0.f, R = -INFINITY, Ws = 0.f;
-      for (int w = 0; w < kWarps; ++w) {
-        const float4 e = *reinterpret_cast<const float4*>(xr + (w * G + g) * 4);
-        lse_merge(M, Ls, e.x, e.y);
-        R = fmaxf(R, e.z);
+      // lane w < kWarps takes warp w's part; three xor steps combine them
+      float4 e = lane < kWarps ? *reinterpret_cast<const float4*>(xr + (lane * G + g) * 4)
+                               : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+      float M = e.x, Ls = e.y, R = e.z;
+#pragma unroll
+      for (int o = 1; o < kWarps; o <<= 1) {
+        const float M2 = __shfl_xor_sync(0xffffffffu, M, o), L2 = __shfl_xor_sync(0xffffffffu, Ls, o);
+        lse_merge(M, Ls, M2, L2);
+        R = fmaxf(R, __shfl_xor_sync(0xffffffffu, R, o));
       }
+      float fw = (lane < kWarps && e.z != -INFINITY) ? __expf(e.z - R) : 0.f;
+      float Ws = lane < kWarps ? e.w * fw : 0.f;
+#pragma unroll
+      for (int o = 1; o < kWarps; o <<= 1) Ws += __shfl_xor_sync(0xffffffffu, Ws, o);
       float o[CPL];
 #pragma unroll
       for (int c = 0; c < CPL; ++c) o[c] = 0.f;
-      for (int w = 0; w < kWarps; ++w) {
-        const float4 e = *reinterpret_cast<const float4*>(xr + (w * G + g) * 4);
-        const float f = e.z == -INFINITY ? 0.f : __expf(e.z - R);
-        Ws += e.w * f;
-        if (comp)
+      if (comp)
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+          const float f = __shfl_sync(0xffffffffu, fw, w);
 #pragma unroll
           for (int c = 0; c < CPL; ++c) o[c] = fmaf(xa[(w * G + g) * D + CPL * lane + c], f, o[c]);
-      }
+        }
       if (lane == 0) a.rec[(int64_t)si * G + g] = make_float4(M, Ls, comp ? R : -INFINITY, comp ? Ws : 0.f);
       if (comp) {
         float* dst = a.comp + ((int64_t)si * G + g) * D + CPL * lane;
@@ -522,7 +554,19 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
           *reinterpret_cast<float2*>(dst) = make_float2(o[0], o[1]);
       }
     }
+    if (nseg_done == 1 && a.trace) t_r3 = global_ns();
     __syncthreads();  // the slots are free for the next segment
+  }
+  if (threadIdx.x == 0 && a.trace && (int)blockIdx.x < a.trace_cap) {
+    unsigned long long* rr = a.trace + 1 + 8 * (int64_t)blockIdx.x;
+    rr[0] = ((unsigned long long)blockIdx.x << 32) | (unsigned)nseg_done;
+    rr[1] = 0ull;
+    rr[2] = t_start;
+    rr[3] = t_plan;
+    rr[4] = t_first;
+    rr[5] = global_ns();
+    rr[6] = t_r1 - t_first;
+    rr[7] = ((t_r2 - t_r1) << 32) | (t_r3 - t_r2);
   }
 }
 

@@ -260,17 +260,21 @@ enum {
 };
 compkv_status compkv_profile_enable(compkv_ctx *ctx, int enable);
 
-/* Work-item trace of the decode chain's second kernel (tracing aid, off by
- * default).  buf: caller device memory, 8-byte aligned, `bytes` long, zeroed
- * by the caller before a traced call.  Word 0 is unused; record slot i
- * occupies words 1 + 8 i .. 8 + 8 i, for i < (bytes - 8) / 64 (slots beyond
- * are not written).  With P stream CTAs (slots [0, P) are reserved for them)
- * and C CTAs per unit, the CTA of blockIdx x of the second kernel writes slot
- * P + x: (x << 32 | 1 << 24 | cluster rank), unit (= sequence * Hkv + head),
- * t0 its start, t1 the end of its wait for the stream kernel, t2 the
- * selection known, t3 the attention done, t4 its end (%globaltimer ns), and
- * the unit's selected block count.  A slot a call does not use stays as the
- * caller left it.  buf = NULL switches tracing off. */
+/* Work-item trace of the decode chain (tracing aid, off by default).  buf:
+ * caller device memory, 8-byte aligned, `bytes` long, zeroed by the caller
+ * before a traced call.  Word 0 is unused; record slot i occupies words
+ * 1 + 8 i .. 8 + 8 i, for i < (bytes - 8) / 64 (slots beyond are not
+ * written).  Times are %globaltimer nanoseconds.  With P stream CTAs and C
+ * CTAs per unit in the second kernel:
+ *   slot x < P, stream CTA x: (x << 32 | segments it processed), 0, t0 its
+ *     start, t1 its plan known (after waiting for the previous work), t2 its
+ *     first segment done, t3 its end;
+ *   slot P + x, CTA x of the second kernel: (x << 32 | 1 << 24 | cluster
+ *     rank), unit (= sequence * Hkv + head), t0 its start, t1 the end of its
+ *     wait for the stream kernel, t2 the selection known, t3 the attention
+ *     done, t4 its end, and the unit's selected block count.
+ * A slot a call does not use stays as the caller left it.  buf = NULL
+ * switches tracing off. */
 compkv_status compkv_trace(compkv_ctx *ctx, void *buf, size_t bytes);
 compkv_status compkv_profile_read(compkv_ctx *ctx, int family, double *total_ms, int64_t *launches);
 

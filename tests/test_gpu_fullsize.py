@@ -3,10 +3,10 @@ benchmark times: a Llama-3.1-8B-shaped layer at 32K context, a Qwen3-8B-shaped
 layer at 128K over 64 decode steps, a Qwen3-32B-shaped layer at 64K with r = d,
 and 32 layers x 16 ragged sequences (8K-128K).
 
-The oracle follows a sample of (layer, sequence, head) units one by one (its
-fp64 copy of a 128K head is 270 MB); every other unit is checked for what
-holds at any size: its selection is ascending, holds the forced blocks, has
-min(N, K) entries inside [0, N), and its output is finite.
+The oracle follows every unit of the single-layer workloads (its fp64 copy of
+a 128K head is 270 MB) and a sample of the batched one; every other unit is
+checked for what holds at any size: its selection is ascending, holds the
+forced blocks, has min(N, K) entries inside [0, N), and its output is finite.
 """
 import numpy as np
 import pytest
@@ -77,7 +77,7 @@ def test_llama8b_32k():
 
 def test_qwen8b_128k_64_steps():
     wl = synth.WORKLOADS["qwen8b_128k"]
-    run = Run(wl, heads=[(0, 0, 0), (0, 0, 3), (0, 0, 7)])
+    run = Run(wl)                      # all 8 heads, every step
     for step in range(wl.steps):
         q, sel, out, res = run.decode_step(0)
         check_step(run, 0, sel, out, res)
