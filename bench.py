@@ -169,9 +169,25 @@ def ncu_traffic(kernel_file: str, kernel: str, workload: str):
     return rec.get("kernels", {}).get(kernel, {}).get("dram_bytes_per_launch")
 
 
-def bench_workload(name):
+def bench_workload(name, r=None, budget=None, dense=False):
+    """The synth workload behind a bench workload name, with optional overrides:
+    r (variance groups), budget (tokens), or dense (budget covering the whole
+    context: every block selected, i.e. exact attention over the cache)."""
     import synth
     base, changes, R, desc = WORKLOADS[name]
+    changes = dict(changes)
+    if r is not None:
+        changes["r"] = int(r)
+        desc += f"; r overridden to {r}"
+    if dense:
+        wl0 = synth.WORKLOADS[base]
+        top = max(synth.sequence_lengths(wl0)) + changes.get("steps", wl0.steps)
+        budget = ((top + BLOCK - 1) // BLOCK) * BLOCK
+        desc += f"; dense: budget {budget} tokens covers the context (every block selected: exact attention)"
+    elif budget is not None:
+        desc += f"; budget overridden to {budget} tokens"
+    if budget is not None:
+        changes["budget_tokens"] = int(budget)
     wl = synth.small_variant(base, **changes) if changes else synth.WORKLOADS[base]
     return wl, R, desc
 
@@ -205,12 +221,12 @@ class Layers:
     """R independent layer caches of a workload on one GPU, with the inputs of
     every step staged on the device and the call arguments prepared once."""
 
-    def __init__(self, name, device):
+    def __init__(self, name, device, **overrides):
         import torch
 
         import synth
         from block_sparse_kv_summary_gb300.cache import CompKVCache
-        wl, R, desc = bench_workload(name)
+        wl, R, desc = bench_workload(name, **overrides)
         self.name, self.wl, self.desc, self.device = name, wl, desc, device
         self.R = wl.layers if wl.layers > 1 else R
         self.lens = synth.sequence_lengths(wl)
@@ -280,7 +296,7 @@ def _oracle_worker(args):
     return (time.perf_counter() - t0) / steps
 
 
-def oracle_baseline(name, budget_s=8.0, threads=1):
+def oracle_baseline(name, budget_s=8.0, threads=1, **overrides):
     """The fp64 oracle timed on the host on a bounded sample of the workload:
     decode steps of sequence 0 of layer 0.  threads=1: heads one after another
     in this process until `budget_s` of CPU time is spent, scaled to a full
@@ -293,7 +309,7 @@ def oracle_baseline(name, budget_s=8.0, threads=1):
 
     import oracle as O
     import synth
-    wl, _, _ = bench_workload(name)
+    wl, _, _ = bench_workload(name, **overrides)
     lens, caps = synth.sequence_lengths(wl), synth.capacity_tokens(wl)
     s = int(np.argmax(lens)) if wl.batch > 1 else 0
     L0, cap = lens[s], caps[s]
@@ -368,10 +384,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=0)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="qwen8b_128k")
+    ap.add_argument("--r", type=int, default=None, help="override the variance groups r (r sweep)")
+    ap.add_argument("--budget", type=int, default=None, help="override the budget in tokens (budget sweep)")
+    ap.add_argument("--dense", action="store_true",
+                    help="budget covering the whole context: every block selected (exact attention baseline)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     ws, rank, local = dist_env()
-    wl0, _, _ = bench_workload(args.workload)
+    overrides = {"r": args.r, "budget": args.budget, "dense": args.dense}
+    wl0, _, _ = bench_workload(args.workload, **overrides)
     calls_per_step = wl0.layers if wl0.layers > 1 else 1
     if args.steps <= 0:
         args.steps = max(20, 20000 // calls_per_step)
@@ -384,8 +405,8 @@ def main():
     # the CPU baseline first: its worker processes start before any GPU call
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        one_us, one_desc, _, _ = oracle_baseline(args.workload, budget_s=8.0, threads=1)
-        all_us, all_desc, _, all_cores = oracle_baseline(args.workload, budget_s=8.0, threads=8)
+        one_us, one_desc, _, _ = oracle_baseline(args.workload, budget_s=8.0, threads=1, **overrides)
+        all_us, all_desc, _, all_cores = oracle_baseline(args.workload, budget_s=8.0, threads=8, **overrides)
         cpu = {"value": all_us, "unit": UNIT, "cores": all_cores, "kind": "oracle", "sample": all_desc,
                "one_core": {"value": one_us, "unit": UNIT, "cores": 1, "sample": one_desc},
                "host_cores": len(os.sched_getaffinity(0))}
@@ -406,7 +427,7 @@ def main():
     barrier(ws)
     P.lib()
 
-    work = Layers(args.workload, device)
+    work = Layers(args.workload, device, **overrides)
     cache = work.cache
     for _ in range(args.warmup):
         work.step()
@@ -513,7 +534,8 @@ def main():
         "scaling": "weak", "vs_baseline": None, "dtype": "f32 (bf16 K/V, fp32 summaries)",
         "data": "synthetic (seeded generator: per-block centres + LogUniform within-block noise, "
                 "2 outlier channels x5, 3 needles; random queries)",
-        "config": {"workload": work.desc, "name": args.workload,
+        "config": {"workload": work.desc, "name": args.workload, "r": work.wl.r,
+                   "budget_tokens": work.wl.budget_tokens, "dense": bool(args.dense),
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
                    "l2": (f"inputs larger than L2: {work.R} independent layer caches rotated, "
                           f"{hbm_l2 / 1e6:.0f} MB touched between visits of one layer")
@@ -543,9 +565,10 @@ def run_reference(args, ws, rank):
     Each timed step is one full decode call of the workload."""
     if rank != 0:
         return 0
-    wl, _, desc = bench_workload(args.workload)
+    overrides = {"r": args.r, "budget": args.budget, "dense": args.dense}
+    wl, _, desc = bench_workload(args.workload, **overrides)
     t0 = time.perf_counter()
-    us, sample, calls_done, cores = oracle_baseline(args.workload, budget_s=30.0, threads=8)
+    us, sample, calls_done, cores = oracle_baseline(args.workload, budget_s=30.0, threads=8, **overrides)
     wall = time.perf_counter() - t0
     calls = wl.layers if wl.layers > 1 else 1
     us *= calls

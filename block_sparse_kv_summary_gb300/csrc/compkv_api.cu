@@ -57,8 +57,8 @@ compkv_status make_layout(const compkv_config* c, Layout* L) {
   if (c->block_size != kBlock) return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "block_size must be 16 (got %d)", c->block_size);
   if (!is_pow2(c->r) || c->r > c->head_dim || c->head_dim % c->r)
     return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "r must be a power of two dividing head_dim (got %d)", c->r);
-  if (c->budget_tokens % kBlock || c->budget_tokens / kBlock < 3 || c->budget_tokens / kBlock > 4096)
-    return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "budget_tokens must be a multiple of 16 in 48..65536 (got %d)",
+  if (c->budget_tokens % kBlock || c->budget_tokens / kBlock < 3 || c->budget_tokens / kBlock > 65536)
+    return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "budget_tokens must be a multiple of 16 in 48..1048576 (got %d)",
                 c->budget_tokens);
   if (c->variant & ~(COMPKV_VARIANT_FIRST_ORDER_MASS | COMPKV_VARIANT_NO_VARIANCE_FACTOR | COMPKV_VARIANT_NO_COMPENSATION))
     return fail(COMPKV_ERR_INVALID_ARG, "variant has unknown bits (got %d)", c->variant);

@@ -82,7 +82,7 @@ __device__ __forceinline__ int64_t row_of(const LayerArgs& a, int s, int h, int 
 // ---------------------------------------------------------------- timers
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t)::"memory");
   return t;
 }
 

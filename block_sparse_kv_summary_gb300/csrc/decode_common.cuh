@@ -12,16 +12,26 @@ __host__ __device__ constexpr int stage_blocks(int r, int G) { return (r >= 64 |
 // sigma2 by a butterfly over the r groups (long Dbar rows) instead of per value.
 __host__ __device__ constexpr bool long_dbar(int r) { return r >= 64; }
 
-// Per-sequence plan in shared memory, built by warp 0 from the call's token
-// counts Ltok[s] (s < B <= 64):  sN[s] = blocks, soff[s] = first segment of
-// (s, head 0), soff[B] = all segments, *sseg = blocks per segment.  Sequence
-// s has nseg_s = ceil(sN[s] / seg) segments per head.  The caller
-// synchronises the CTA afterwards.
-__device__ __forceinline__ void plan_warp(const int* Ltok, int B, int Hkv, int P, int sb, int* sN, int* soff, int* sseg,
-                                          int lane) {
-  int n0 = 0, n1 = 0;
-  if (lane < B) n0 = ceil_blocks(Ltok[lane]);
-  if (lane + 32 < B) n1 = ceil_blocks(Ltok[lane + 32]);
+// Blocks of sequence s the summary stream reads in this call: all of them,
+// except that a call which appends leaves the open block (the one receiving
+// the new token) to the post kernel, which recomputes its summary; and none
+// when the call selects and every block fits the budget (K >= N) without
+// scores requested: the selection is then every block and nothing of the
+// summaries is needed.
+__device__ __forceinline__ int streamed_blocks(int L, bool appended, bool selects, int K, bool scores) {
+  const int N = ceil_blocks(L);
+  if (selects && N <= K && !scores) return 0;
+  return N - (appended ? 1 : 0);
+}
+
+// Per-sequence plan in shared memory, built by warp 0 from the streamed block
+// counts sN[s] (s < B <= 64): soff[s] = first segment of (s, head 0),
+// soff[B] = all segments, *sseg = blocks per segment.  Sequence s has
+// nseg_s = ceil(sN[s] / seg) segments per head.  The caller synchronises the
+// CTA afterwards.
+__device__ __forceinline__ void plan_warp(const int* sN, int B, int Hkv, int P, int sb, int* soff, int* sseg, int lane) {
+  const int n0 = lane < B ? sN[lane] : 0;
+  const int n1 = lane + 32 < B ? sN[lane + 32] : 0;
   long long tot = (long long)n0 + n1;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
@@ -41,14 +51,8 @@ __device__ __forceinline__ void plan_warp(const int* Ltok, int B, int Hkv, int P
     const int y = __shfl_up_sync(0xffffffffu, i1, o);
     if (lane >= o) i1 += y;
   }
-  if (lane < B) {
-    sN[lane] = n0;
-    soff[lane] = i0 - c0;
-  }
-  if (lane + 32 < B) {
-    sN[lane + 32] = n1;
-    soff[lane + 32] = tot0 + i1 - c1;
-  }
+  if (lane < B) soff[lane] = i0 - c0;
+  if (lane + 32 < B) soff[lane + 32] = tot0 + i1 - c1;
   if (lane == 0) *sseg = seg;
   if (lane == 31) soff[B] = tot0 + (B > 32 ? i1 : 0);
 }

@@ -3,25 +3,34 @@
 //
 // One thread-block cluster of C CTAs per (sequence, KV head) unit.  CTA rank p
 // owns the unit's blocks [p bpc, (p + 1) bpc) (bpc = ceil(N / C) rounded up
-// to 4) and, of the stream's segment records, those with index = p (mod C):
-//   a. LSE_g = logsumexp_b a_{g,b} from all segment records (each CTA alone);
-//      S_b = sum_g phat_{g,b} sigma2_{g,b} ("무엇과 다른가") of its blocks as
-//      order-preserving keys, and their 12-bit histogram (candidates 1..N-3);
-//   b. the histograms summed across the cluster in distributed shared memory
-//      (exponent bins at rank 0, the 16 fine bins of exponent e at rank e % C);
-//      every CTA finds the threshold bin T where the count of larger keys
-//      reaches K - 3 (the forced sink block and the two most recent blocks
-//      take the other three places of the budget);
-//   c. every CTA classifies its own blocks and pushes, in one exchange, its
-//      count of selected blocks and the keys of its blocks in T when T must be
-//      ranked (ties to the lower block index); every CTA ranks those few keys
-//      itself, so after one cluster barrier all CTAs know the whole selection;
-//   d. the selected blocks are spread over the cluster's warps (one block per
-//      warp and round); each warp attends exactly to its block's bf16 K/V and
-//      removes the block's own Mean-compensation term, which the stream added
-//      for every block ("어떻게 동작하나": unselected blocks contribute
-//      |b| e^{zbar} vbar and |b| e^{zbar}); the partials, with the CTA's share
-//      of the compensation sums, merge across the cluster into out = acc / l.
+// to 4) and, of the stream's segment records, those with index = p (mod C).
+//   a. The last warp recomputes the summary of the open block, which this
+//      call's token joins: every CTA its a_g = ln|b| + zbar + sigma2/2 for the
+//      normaliser, and the CTA that owns the block also writes the token and
+//      the block's summary rows.  Meanwhile warp 0 merges the segment records
+//      into LSE_g and warp 1 copies the CTA's zbar and sigma2 rows.
+//   b. S_b = sum_g phat_{g,b} sigma2_{g,b} ("무엇과 다른가") of the CTA's blocks
+//      as order-preserving keys and their 12-bit histogram (candidates
+//      1..N-3), summed across the cluster in distributed shared memory
+//      (exponent counts at rank 0, the 16 fine bins of exponent e at rank
+//      e % C); one warp finds the threshold bin T where the count of larger
+//      keys reaches K - 3 (the forced sink block and the two most recent
+//      blocks take the other three places of the budget).
+//   c. Blocks above T, and the forced ones, are selected for sure: each CTA
+//      lists its own in ascending order and pushes its count, and the keys of
+//      its blocks in T when T must be ranked, to every peer.  Its warps start
+//      on the top eight of its own list at once, while that exchange settles.
+//   d. After the exchange every CTA ranks the keys in T (ties to the lower
+//      block index) and spreads the rest of the work -- own lists longer than
+//      eight and the tie winners -- over the warps left idle, in one order
+//      that every CTA derives alike.
+//   e. A warp attends exactly to one block's bf16 K/V at a time with
+//      tensor-core products (q and the probabilities split into bf16 high and
+//      low parts, fp32 accumulation) and removes the block's own
+//      Mean-compensation term, which the stream added for every block
+//      ("어떻게 동작하나": unselected blocks contribute |b| e^{zbar} vbar and
+//      |b| e^{zbar}); the partials and the CTA's share of the compensation
+//      sums merge across the cluster into out = acc / l.
 // By Jensen, sum_{j in b} e^{z_j} >= |b| e^{zbar_b}, so removing a selected
 // block's mean term never makes a block's net weight negative.  If every
 // block is selected there is no compensation (the step is dense attention).
@@ -48,9 +57,16 @@ struct InvSqrtP<128> {
   static constexpr float v = 0.08838834764831845f;
 };
 
+// Attention staging of one warp: the block's 16 K rows and 16 V rows (bf16;
+// every row padded by 16 bytes, so that the eight rows one ldmatrix reads
+// start in eight different bank quads), then vbar of the block (fp32 [D]).
+__host__ __device__ constexpr int stg_row(int D) { return 2 * D + 16; }
+__host__ __device__ constexpr int stg_bytes(int D) { return 2 * kBlock * stg_row(D) + 4 * D; }
+
 // Shared memory of the post kernel, in 4-byte words.
 struct PostLayout {
-  int zsl, ssl, keys, own, bits, csh, plan, U, hf, he, xexp, xfine, xref, lh, tie, stg, stg_w, red, xm, misc, win, bars, total;
+  int zsl, ssl, stg, red, keys, own, csh, qf, plan, anm, lsep, hf, tie, dense, xexp, xfine, xref, lh, xm, win, misc,
+      bars, total;
 };
 __host__ __device__ inline int post_items(int D, int G) { return G * D / 4; }
 __host__ __device__ inline int post_ipr(int D, int G, int C) { return (post_items(D, G) + C - 1) / C; }
@@ -58,34 +74,36 @@ __host__ __device__ inline PostLayout post_layout(int D, int G, int C, int bpc_m
   PostLayout l;
   const int Gp = pad_g(G);
   int o = 0;
-  l.zsl = o; o += bpc_max * Gp;
-  l.ssl = o; o += bpc_max * Gp;
-  l.keys = o; o += (bpc_max + 3) & ~3;
-  l.own = o; o += ((bpc_max < K ? bpc_max : K) + 7) & ~3;
-  l.bits = o; o += (bpc_max + 31) / 32 + 4;
-  o = (o + 3) & ~3;
-  l.csh = o; o += G * D;           // this CTA's share of the compensation numerator [G][D]
-  l.plan = o; o += 3 * kMaxBatch + 4;  // tokens, blocks and first segment of every sequence
-  // union: selection (local histograms | exchanged histograms | tie lists) / attention staging / CTA partials
-  l.U = o;
-  l.hf = o;                        // local 12-bit histogram [4096]; later the tie lists [C][kTieCap] x (key, index)
-  l.tie = o;
-  l.he = l.hf + kFine;             // local exponent histogram [256]
-  l.xexp = l.he + 256;             // exchanged exponent histogram (rank 0) [256]
-  l.xfine = l.xexp + 256;          // exchanged fine bins of this rank's exponents [ceil(256 / C) * 16]
-  l.xref = l.xfine + ((256 + C - 1) / C) * 16;  // refinement histograms (rank 0) [3][256]
-  l.lh = l.xref + 3 * 256;         // refinement local histogram [256]
-  const int selw = l.lh + 256 - o;
-  l.stg = o;                       // attention: per warp K, V rows (bf16) and z, p [kBlock][G]
-  l.stg_w = kBlock * D + 2 * kBlock * G;
-  const int attw = kPW * l.stg_w;
-  const int redw = kPW * G * D + 2 * kPW * G + G * (kPW + 1) + 2 * G;
-  l.red = o;                       // CTA partials after the attention: [kPW][G][D], m, l [kPW][G]
-  int uw = selw > attw ? selw : attw;
-  uw = uw > redw ? uw : redw;
+  // union: zbar and sigma2 of the CTA's blocks (keys) | attention staging | the warps' partials
+  l.zsl = o;
+  l.ssl = o + bpc_max * Gp;
+  l.stg = o;
+  l.red = o;
+  const int zw = 2 * bpc_max * Gp;
+  const int sw = kPW * stg_bytes(D) / 4;
+  const int rw = kPW * D * 8 + 2 * kPW * 8;  // [kPW][D][8] partial numerators, [kPW][8] maxima and sums
+  int uw = zw > sw ? zw : sw;
+  uw = uw > rw ? uw : rw;
   o += (uw + 3) & ~3;
-  l.xm = o; o += post_ipr(D, G, C) * C * 8;   // merge staging: [items per rank][C][acc4, m, l, -, -]
-  l.win = o; o += kRankMax + 4;               // tie winners in rank order
+  l.keys = o; o += (bpc_max + 3) & ~3;
+  l.own = o; o += ((bpc_max < K ? bpc_max : K) + 3) & ~3;
+  l.csh = o; o += G * D;               // this CTA's share of the compensation numerator [G][D]
+  l.qf = o; o += (D / 16) * 32 * 4;    // q fragments of every lane, per k-step (uint4)
+  l.plan = o; o += 3 * kMaxBatch + 4;  // tokens, streamed blocks and first segment of every sequence
+  l.anm = o; o += kMaxG;               // a_g of the open block
+  l.lsep = o; o += 2 * kMaxG;          // (max, sum) of the records' logsumexp per head
+  // selection: the local fine histogram [4096]; after its push, the tie lists [C][kTieCap]
+  // of (key, block) and their dense copy (or, on the rare path, the selection bitmap)
+  l.hf = o;
+  l.tie = o;
+  l.dense = o + 2 * kMaxC * kTieCap;
+  o += kFine;
+  l.xexp = o; o += 256;                            // exchanged exponent histogram (rank 0)
+  l.xfine = o; o += ((256 + C - 1) / C) * 16;      // exchanged fine bins of this rank's exponents
+  l.xref = o; o += 3 * 256;                        // refinement histograms (rank 0)
+  l.lh = o; o += 256;                              // refinement local histogram
+  l.xm = o; o += post_ipr(D, G, C) * C * 8;        // merge staging: [items per rank][C][acc4, m, l, -, -]
+  l.win = o; o += kRankMax + 4;                    // tie winners in rank order (before: local tie indices)
   l.misc = o; o += 192;
   l.bars = o; o += 2 * (kPW + 2);
   l.total = o;
@@ -94,19 +112,307 @@ __host__ __device__ inline PostLayout post_layout(int D, int G, int C, int bpc_m
 
 // misc slots (ints unless noted)
 enum : int {
-  kMT = 0, kMAbove, kMCntT, kMNtie, kMOwn, kMTake, kMNeed, kMBad, kMNwin, kMTot,
-  kMLse = 16,        // float [8]
+  kMT = 0, kMAbove, kMCntT, kMNtie, kMOwn, kMBad, kMTot,
+  kMWT = 8,          // [8] warp totals of the own-list scan
   kMCR = 24,         // float [8]: compensation reference of this CTA's share
   kMCW = 32,         // float [8]: compensation weight sum of the share
   kMCnt = 40,        // int2 [16]: per CTA (own selected count, tie count), pushed by the peers
   kMCntR = 72,       // int [16]: refinement counts, pushed by the peers
   kMScan = 88,       // int [8]: scan scratch
-  kMPlan = 96,       // seg, total
+  kMPlan = 96,       // blocks per segment
   kMFits = 100,      // [2] bit s: sequence s had room for its token
-  kMSumOwn = 102, kMNtAll, kMMx, kMWBelow,
-  kMOpre = 112,      // [17] exclusive prefix of the CTAs' own-list counts
-  kMTpre = 132,      // [17] exclusive prefix of the CTAs' tie counts
+  kMCntA = 104,      // int [16]: rare path, every CTA's final own count
+  kMR0 = 120,        // int [8]: rare path, the block each warp attended before the exchange
+  kMTpre = 128,      // int [16]: exclusive prefix of the CTAs' tie counts
 };
+
+// ---------------------------------------------------------------- tensor-core pieces
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+// d += A (16 x 16, row) * B (16 x 8, col), bf16 inputs, fp32 accumulation
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// (x, y) as bf16x2 high parts and the bf16x2 of what they leave (x first, in the low half)
+__device__ __forceinline__ void split_bf16(float x, float y, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 hv = __floats2bfloat162_rn(x, y);
+  const float2 hf = __bfloat1622float2(hv);
+  const __nv_bfloat162 lv = __floats2bfloat162_rn(x - hf.x, y - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&hv);
+  lo = *reinterpret_cast<const uint32_t*>(&lv);
+}
+
+// One block of exact attention for the warp's running state.  Lane (r, c) =
+// (lane / 4, lane % 4).  Scores S^T = q K^T as a 16 x 16 product (rows: the
+// query heads, zero beyond G; columns: the 16 tokens), so lane (r, c) holds
+// head r at tokens 2c, 2c+1, 8+2c, 9+2c -- which is also its fragment of the
+// probabilities as the B operand of O^T += V^T P (rows: coordinates, columns:
+// heads).  m, l: head r (every lane of the quad alike).  acc[mt]: O^T at
+// coordinates 16 mt + r (+ 8) for heads 2c, 2c + 1.  With `cb`, the block's
+// compensation term |b| e^{zbar} (zb: zbar of head r) and its vbar (staged
+// after the V rows) come off, in the same rescale.
+template <int D, int G>
+__device__ __forceinline__ void blk_attend(float& m, float& l, float (&acc)[D / 16][4], const uint4* qf,
+                                           const char* stg, int n, bool cb, float zb, int lane) {
+  constexpr int KS = D / 16;
+  constexpr int RB = stg_row(D);
+  const int r = lane >> 2, c = lane & 3;
+  // ldmatrix rows: matrix lane / 8 = (tokens 0-7 | 8-15) x (coordinates +0 | +8)
+  const uint32_t roff = (uint32_t)(((lane >> 4) * 8 + (lane & 7)) * RB + ((lane >> 3) & 1) * 16);
+  const uint32_t kaddr = smem_u32(stg) + roff;
+  const uint32_t vaddr = kaddr + kBlock * RB;
+  float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    uint32_t b0, b1, b2, b3;
+    ldsm_x4(kaddr + 32u * ks, b0, b1, b2, b3);
+    const uint4 qv = qf[ks * 32 + lane];  // high parts (k 2c.., k 8+2c..), low parts
+    mma_bf16(s0, qv.x, 0u, qv.y, 0u, b0, b1);
+    mma_bf16(s1, qv.x, 0u, qv.y, 0u, b2, b3);
+    mma_bf16(s0, qv.z, 0u, qv.w, 0u, b0, b1);
+    mma_bf16(s1, qv.z, 0u, qv.w, 0u, b2, b3);
+  }
+  const float x0 = 2 * c < n ? s0[0] : -INFINITY, x1 = 2 * c + 1 < n ? s0[1] : -INFINITY;
+  const float x2 = 8 + 2 * c < n ? s1[0] : -INFINITY, x3 = 9 + 2 * c < n ? s1[1] : -INFINITY;
+  float bm = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+  bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+  bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+  const bool live = r < G;
+  const float e = (cb && live) ? ln_count(n) + zb : -INFINITY;
+  const float mn = fmaxf(m, fmaxf(bm, e));
+  const float fo = m == -INFINITY ? 0.f : __expf(m - mn);
+  const float fn = (cb && live) ? __expf(e - mn) : 0.f;
+  const float p0 = live ? __expf(x0 - mn) : 0.f, p1 = live ? __expf(x1 - mn) : 0.f;
+  const float p2 = live ? __expf(x2 - mn) : 0.f, p3 = live ? __expf(x3 - mn) : 0.f;
+  float ps = (p0 + p1) + (p2 + p3);
+  ps += __shfl_xor_sync(0xffffffffu, ps, 1);
+  ps += __shfl_xor_sync(0xffffffffu, ps, 2);
+  l = l * fo + ps - fn;
+  m = mn;
+  // the factors of this lane's accumulator columns (heads 2c, 2c+1 live in quads 2c, 2c+1)
+  const float foA = __shfl_sync(0xffffffffu, fo, 8 * c), foB = __shfl_sync(0xffffffffu, fo, 8 * c + 4);
+  const float fnA = __shfl_sync(0xffffffffu, fn, 8 * c), fnB = __shfl_sync(0xffffffffu, fn, 8 * c + 4);
+  uint32_t ph0, pl0, ph1, pl1;
+  split_bf16(p0, p1, ph0, pl0);
+  split_bf16(p2, p3, ph1, pl1);
+  const float* vb = reinterpret_cast<const float*>(stg + 2 * kBlock * RB);
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) {
+    const float v0 = cb ? vb[16 * mt + r] : 0.f, v1 = cb ? vb[16 * mt + 8 + r] : 0.f;
+    acc[mt][0] = fmaf(acc[mt][0], foA, -fnA * v0);
+    acc[mt][1] = fmaf(acc[mt][1], foB, -fnB * v0);
+    acc[mt][2] = fmaf(acc[mt][2], foA, -fnA * v1);
+    acc[mt][3] = fmaf(acc[mt][3], foB, -fnB * v1);
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4_t(vaddr + 32u * mt, a0, a1, a2, a3);
+    mma_bf16(acc[mt], a0, a1, a2, a3, ph0, ph1);
+    mma_bf16(acc[mt], a0, a1, a2, a3, pl0, pl1);
+  }
+}
+
+// ---------------------------------------------------------------- the phases
+// The open block (the one receiving this call's token), by one warp: its
+// summary from the exact bf16 values (two-pass fp32 mean and population
+// variance) and a_g = ln n + zbar_g + sigma2_g / 2, with
+// sigma2_g = (1/d) sum_i q_gi^2 Dbar_t(i) = sum_i qr_gi^2 Dbar_t(i), qr = q / sqrt(d).
+// The owner also stores the token and the block's kbar, vbar and Dbar rows.
+template <int D, int G>
+__device__ __forceinline__ void open_block(const LayerArgs& a, int s, int h, int L, int N, int64_t row0, bool owner,
+                                           float* anm, int lane) {
+  constexpr int V = D / 32;
+  const int n = L - kBlock * (N - 1);
+  const int64_t row = row0 + (N - 1);
+  const int c0 = V * lane;
+  const int64_t nw_off = ((int64_t)s * a.Hkv + h) * D + c0;
+  const __nv_bfloat16* kb = a.k + row * kBlock * D + c0;
+  const __nv_bfloat16* vb = a.v + row * kBlock * D + c0;
+  const float* qg = a.q + ((int64_t)s * a.Hkv + h) * G * D + c0;
+  float qr[G][V];
+#pragma unroll
+  for (int g = 0; g < G; ++g)
+#pragma unroll
+    for (int i = 0; i < V; ++i) qr[g][i] = qg[g * D + i] * InvSqrtP<D>::v;
+  if (owner) {
+    store_bf16_raw<V>(a.k + (row * kBlock + n - 1) * D + c0, a.k_new + nw_off);
+    store_bf16_raw<V>(a.v + (row * kBlock + n - 1) * D + c0, a.v_new + nw_off);
+  }
+  float ksum[V], vsum[V], kn[V];
+  load_bf16<V>(a.k_new + nw_off, kn);
+#pragma unroll
+  for (int c = 0; c < V; ++c) ksum[c] = vsum[c] = 0.f;
+#pragma unroll
+  for (int j = 0; j < kBlock; ++j) {
+    if (j < n) {
+      float kf[V];
+      load_bf16<V>(j == n - 1 ? a.k_new + nw_off : kb + j * D, kf);
+#pragma unroll
+      for (int c = 0; c < V; ++c) ksum[c] += kf[c];
+      if (owner) {
+        float vf[V];
+        load_bf16<V>(j == n - 1 ? a.v_new + nw_off : vb + j * D, vf);
+#pragma unroll
+        for (int c = 0; c < V; ++c) vsum[c] += vf[c];
+      }
+    }
+  }
+  float mk[V], var[V];
+#pragma unroll
+  for (int c = 0; c < V; ++c) {
+    mk[c] = ksum[c] / (float)n;
+    var[c] = 0.f;
+  }
+#pragma unroll
+  for (int j = 0; j < kBlock; ++j) {
+    if (j < n) {
+      float kf[V];
+      if (j == n - 1) {
+#pragma unroll
+        for (int c = 0; c < V; ++c) kf[c] = kn[c];
+      } else {
+        load_bf16<V>(kb + j * D, kf);
+      }
+#pragma unroll
+      for (int c = 0; c < V; ++c) {
+        const float dv = kf[c] - mk[c];
+        var[c] = fmaf(dv, dv, var[c]);
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < V; ++c) {
+    var[c] /= (float)n;
+    if (owner) {
+      a.kbar[row * D + c0 + c] = mk[c];
+      a.vbar[row * D + c0 + c] = vsum[c] / (float)n;
+    }
+  }
+  // Dbar_t over coordinate group t = [t*D/r, (t+1)*D/r); every lane keeps the means of its
+  // own coordinates' groups
+  const int r = a.r, gs = D / r;
+  float dm[V];
+  if (gs >= V) {
+    float t = 0.f;
+#pragma unroll
+    for (int c = 0; c < V; ++c) t += var[c];
+    for (int o = 1; o < gs / V; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    const float mval = t / (float)gs;
+#pragma unroll
+    for (int c = 0; c < V; ++c) dm[c] = mval;
+    if (owner && (lane & (gs / V - 1)) == 0) a.dbar[row * r + c0 / gs] = mval;
+  } else {
+    float t = 0.f;
+#pragma unroll
+    for (int c = 0; c < V; ++c) {
+      t += var[c];
+      if ((c + 1) % gs == 0) {
+        const float mval = t / (float)gs;
+        for (int c2 = c + 1 - gs; c2 <= c; ++c2) dm[c2] = mval;
+        if (owner) a.dbar[row * r + (c0 + c) / gs] = mval;
+        t = 0.f;
+      }
+    }
+  }
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    float z = 0.f, sg = 0.f;
+#pragma unroll
+    for (int c = 0; c < V; ++c) {
+      z = fmaf(qr[g][c], mk[c], z);
+      sg = fmaf(qr[g][c] * qr[g][c], dm[c], sg);
+    }
+    z = warp_sum(z);
+    sg = warp_sum(sg);
+    if (lane == 0) anm[g] = ln_count(n) + z + ((a.variant & kVarFirstOrderMass) ? 0.f : 0.5f * sg);
+  }
+}
+
+// (max, sum) of the logsumexp of a_g over the unit's nseg segment records, by one warp: lane j
+// merges records of head j % G; lanes of one head then merge across the warp.
+template <int G>
+__device__ __forceinline__ void record_lse(const LayerArgs& a, int i0, int nseg, float* lsep, int lane) {
+  float M = -INFINITY, S = 0.f;
+  const int tot = nseg * G;
+  const float4* base = a.rec + (int64_t)i0 * G;
+#pragma unroll 1
+  for (int k0 = 0; k0 < tot; k0 += 128) {  // four records per lane in flight at once
+    float4 e[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int idx = k0 + lane + 32 * j;
+      e[j] = idx < tot ? __ldcg(base + idx) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) lse_merge(M, S, e[j].x, e[j].y);
+  }
+#pragma unroll
+  for (int o = G; o < 32; o <<= 1) {
+    const float M2 = __shfl_xor_sync(0xffffffffu, M, o), S2 = __shfl_xor_sync(0xffffffffu, S, o);
+    lse_merge(M, S, M2, S2);
+  }
+  if (lane < G) {
+    lsep[2 * lane] = M;
+    lsep[2 * lane + 1] = S;
+  }
+}
+
+// This CTA's share of the compensation sums: segment records p, p + C, ...
+// rescaled to their common maximum; thread items (head, column quad), every
+// load of an item issued before any is used.
+template <int D, int G>
+__device__ __forceinline__ void comp_share(const LayerArgs& a, int i0, int nseg, int p, int C, float* csh, float* cR,
+                                           float* cW, int tid) {
+  const int nk = p < nseg ? (nseg - 1 - p) / C + 1 : 0;
+#pragma unroll 1
+  for (int i4 = tid; i4 < G * D / 4; i4 += kPT) {
+    const int g = i4 / (D / 4), col = 4 * (i4 % (D / 4));
+    float R = -INFINITY, Wsum = 0.f;
+    float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+    for (int k0 = 0; k0 < nk; k0 += 4) {
+      float4 e[4], v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int rec = i0 + p + C * (k0 + j);
+        const bool ok = k0 + j < nk;
+        e[j] = ok ? __ldcg(a.rec + (int64_t)rec * G + g) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
+        v[j] = ok ? __ldcg(reinterpret_cast<const float4*>(a.comp + ((int64_t)rec * G + g) * D + col))
+                  : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (e[j].z == -INFINITY) continue;
+        const float mn = fmaxf(R, e[j].z);
+        const float fo = R == -INFINITY ? 0.f : __expf(R - mn);
+        const float fn = __expf(e[j].z - mn);
+        A.x = A.x * fo + v[j].x * fn;
+        A.y = A.y * fo + v[j].y * fn;
+        A.z = A.z * fo + v[j].z * fn;
+        A.w = A.w * fo + v[j].w * fn;
+        Wsum = Wsum * fo + e[j].w * fn;
+        R = mn;
+      }
+    }
+    *reinterpret_cast<float4*>(csh + g * D + col) = A;
+    if (col == 0) {
+      cR[g] = R;
+      cW[g] = Wsum;
+    }
+  }
+}
 
 // Exclusive prefix of `v` over the CTA's kPT threads; `total` receives the
 // sum.  Two CTA barriers.
@@ -163,12 +469,12 @@ __device__ __forceinline__ int bitmap_list(const unsigned* words, int nw, int lo
 }
 
 // Rare path of the selection: more keys share the threshold bin T than the
-// tie lists hold.  The keys in play (own candidates in bin T) are resolved by
+// tie lists hold.  The keys in play (candidates in bin T) are resolved by
 // three more radix digits (bits 18..11, 10..3, 2..0), each a histogram summed
 // at rank 0 with one cluster barrier, and keys equal in every bit go to the
 // lowest block indices (counts exchanged, one more barrier).  Sets the bits of
-// the selected in-play blocks in `bits`.  Called by every thread of every CTA
-// of the cluster.
+// the selected in-play blocks in `bits` (which holds the sure blocks on
+// entry).  Called by every thread of every CTA of the cluster.
 __device__ __noinline__ void refine_select(const uint32_t* keys, unsigned* bits, int nown, int b_lo, int N, uint32_t T,
                                            int need, uint32_t* xref, uint32_t* lh, int* misc, int C, int p) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -258,12 +564,8 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   constexpr bool APPEND = (MODE & kFAppend) != 0;
   constexpr bool SEL = (MODE & kFSelect) != 0;
   constexpr bool ATT = (MODE & kFAttend) != 0;
-  constexpr bool SCORE = (MODE & kFScore) != 0;
-  constexpr int V = D / 32;                                          // coordinates per lane
-  constexpr int TG = G >= 8 ? 2 : ((32 / G) > 16 ? 16 : (32 / G));  // tokens per reduction group
-  constexpr int P = TG * G;                                          // values per group (16 or 32)
-  constexpr int W = V / 2;                                           // 32-bit words of a token slice
-  constexpr int NG = kBlock / TG;
+  constexpr int KS = D / 16;
+  constexpr int RB = stg_row(D);
   extern __shared__ __align__(16) float psm[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int C = a.C;
@@ -277,412 +579,316 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   float* ssl = psm + lay.ssl;
   uint32_t* keys = reinterpret_cast<uint32_t*>(psm + lay.keys);
   int* own = reinterpret_cast<int*>(psm + lay.own);
-  unsigned* bits = reinterpret_cast<unsigned*>(psm + lay.bits);
   uint32_t* hf = reinterpret_cast<uint32_t*>(psm + lay.hf);
-  uint32_t* he = reinterpret_cast<uint32_t*>(psm + lay.he);
+  uint2* tie = reinterpret_cast<uint2*>(psm + lay.tie);     // [C][kTieCap] (key, block), after the histogram push
+  uint2* dense = reinterpret_cast<uint2*>(psm + lay.dense);
   uint32_t* xexp = reinterpret_cast<uint32_t*>(psm + lay.xexp);
   uint32_t* xfine = reinterpret_cast<uint32_t*>(psm + lay.xfine);
   uint32_t* xref = reinterpret_cast<uint32_t*>(psm + lay.xref);
   uint32_t* lh = reinterpret_cast<uint32_t*>(psm + lay.lh);
-  uint2* tie = reinterpret_cast<uint2*>(psm + lay.tie);   // [C][kTieCap] (key, block), after the histograms
   float* xm = psm + lay.xm;
   int* win = reinterpret_cast<int*>(psm + lay.win);
   int* misc = reinterpret_cast<int*>(psm + lay.misc);
-  float* lse = reinterpret_cast<float*>(misc + kMLse);
   float* cR = reinterpret_cast<float*>(misc + kMCR);
   float* cW = reinterpret_cast<float*>(misc + kMCW);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(psm + lay.bars);  // [kPW] attention, [kPW] = zbar/sigma2 load
+  int* cnt = misc + kMCnt;
+  float* anm = psm + lay.anm;
+  float* lsep = psm + lay.lsep;
+  float* csh = psm + lay.csh;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(psm + lay.bars);  // [kPW] attention, [kPW] zbar/sigma2 copy
   const unsigned long long t_start = a.trace ? global_ns() : 0ull;
-  unsigned long long pmk[7] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
+  unsigned long long pmk[14] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
   auto mark = [&](int k) {
     if (a.trace) pmk[k] = global_ns();
   };
 
   // ---- set-up before the stream's results are visible
   if (tid <= kPW) mbar_init(bars + tid, 1);
-  fence_mbar_init();
+  if (tid == 0) fence_mbar_init();
   if (SEL) {
-    for (int i = tid; i < 256 + ((256 + C - 1) / C) * 16 + 3 * 256; i += kPT) xexp[i] = 0u;  // (xexp,) xfine, xref
+    for (int i = tid; i < lay.lh + 256 - lay.hf; i += kPT) hf[i] = 0u;  // hf, xexp, xfine, xref, lh
   }
   if (tid < 192) misc[tid] = 0;
-  float qr[G][V];
+  // q as the A operand of S^T = q K^T, split into bf16 high and low parts: lane (r, c) of
+  // k-step ks holds head r (zero beyond G) at coordinates 16 ks + 2c, +1 and 16 ks + 8 + 2c, +1
+  uint4* qf = reinterpret_cast<uint4*>(psm + lay.qf);
   if (ATT) {
-    const float* qg = a.q + ((int64_t)s * a.Hkv + h) * G * D;
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-      for (int i = 0; i < V; ++i) qr[g][i] = qg[g * D + lane * V + i] * InvSqrtP<D>::v;
+    for (int x = tid; x < KS * 32; x += kPT) {
+      const int ks = x >> 5, r = (x & 31) >> 2, c = x & 3;
+      float2 x0 = make_float2(0.f, 0.f), x1 = make_float2(0.f, 0.f);
+      if (r < G) {
+        const float* qg = a.q + (((int64_t)s * a.Hkv + h) * G + r) * D + 16 * ks + 2 * c;
+        x0 = *reinterpret_cast<const float2*>(qg);
+        x1 = *reinterpret_cast<const float2*>(qg + 8);
+      }
+      uint4 v;
+      split_bf16(x0.x * InvSqrtP<D>::v, x0.y * InvSqrtP<D>::v, v.x, v.z);
+      split_bf16(x1.x * InvSqrtP<D>::v, x1.y * InvSqrtP<D>::v, v.y, v.w);
+      qf[x] = v;
+    }
   }
   __syncthreads();  // misc is zero before warp 0 fills in the plan
   // the plan, as the stream kernel makes it, from the lengths before this call
   // (no kernel of this call writes seq_len before every post CTA has read it)
   int* sL = reinterpret_cast<int*>(psm + lay.plan);  // [kMaxBatch] tokens of each sequence in this call
-  int* sN = sL + kMaxBatch;
+  int* sN = sL + kMaxBatch;                           // [kMaxBatch] blocks the stream read
   int* soff = sN + kMaxBatch;
   if (warp == 0) {
     bool f0 = false, f1 = false;
-    if (lane < a.B) sL[lane] = call_tokens(__ldcg(a.seq_len + lane), a.cap_blocks[lane], APPEND, &f0);
-    if (lane + 32 < a.B) sL[lane + 32] = call_tokens(__ldcg(a.seq_len + lane + 32), a.cap_blocks[lane + 32], APPEND, &f1);
+    if (lane < a.B) {
+      sL[lane] = call_tokens(__ldcg(a.seq_len + lane), a.cap_blocks[lane], APPEND, &f0);
+      sN[lane] = streamed_blocks(sL[lane], APPEND && f0, SEL, a.K, a.scores != nullptr);
+    }
+    if (lane + 32 < a.B) {
+      sL[lane + 32] = call_tokens(__ldcg(a.seq_len + lane + 32), a.cap_blocks[lane + 32], APPEND, &f1);
+      sN[lane + 32] = streamed_blocks(sL[lane + 32], APPEND && f1, SEL, a.K, a.scores != nullptr);
+    }
     const unsigned m0 = __ballot_sync(0xffffffffu, f0), m1 = __ballot_sync(0xffffffffu, f1);
     if (lane == 0) {
       misc[kMFits] = (int)m0;
       misc[kMFits + 1] = (int)m1;
     }
     __syncwarp();
-    plan_warp(sL, a.B, a.Hkv, a.P, stage_blocks(a.r, G), sN, soff, misc + kMPlan, lane);
+    plan_warp(sN, a.B, a.Hkv, a.P, stage_blocks(a.r, G), soff, misc + kMPlan, lane);
   }
   __syncthreads();
   const int seg = misc[kMPlan];
-  const int L = sL[s], N = sN[s];
-  const int nseg = (N + seg - 1) / seg;
+  const int L = sL[s], N = ceil_blocks(L), Ns = sN[s];
+  const bool app = APPEND && (((s < 32 ? misc[kMFits] >> s : misc[kMFits + 1] >> (s - 32)) & 1) != 0);
+  const int nseg = (Ns + seg - 1) / seg;
   const int i0 = soff[s] + h * nseg;                 // the unit's first segment record
   const int bpc = (((N + C - 1) / C) + 3) & ~3;
   const int b_lo = min(N, p * bpc), b_hi = min(N, b_lo + bpc);
   const int nown = b_hi - b_lo;
+  const int nown_z = max(0, min(b_hi, Ns) - b_lo);   // of them with zbar / sigma2 from the stream
   const int64_t row0 = row_of(a, s, h, 0);
   const bool all_sel = N <= K;
-  const bool comp_on = !(a.variant & kVarNoCompensation);
+  const int need0 = K - 3;
   const bool want_keys = SEL && (!all_sel || a.scores);
-  cluster_arrive();  // this CTA's exchange histograms are zero (waited for before the first push)
-  pdl_wait();        // the stream kernel's records, zbar and sigma2 are complete and visible
-  pdl_trigger();     // the next call's kernels may launch (they wait for this grid before reading)
-  const unsigned long long t_wait = a.trace ? global_ns() : 0ull;
+  const bool hist = SEL && !all_sel && need0 > 0;    // the threshold search runs
+  const bool xchg = SEL && !all_sel;                 // the counts are exchanged
+  const bool comp = ATT && !(a.variant & kVarNoCompensation) && (!SEL || !all_sel);
+  const int own_open = app ? (N - 1) / bpc : -1;     // the CTA that appends the new token
+  cluster_arrive();  // this CTA's exchange areas are zero (every peer waits for this before its first push)
 
-  // zbar (and sigma2) of this CTA's blocks into shared memory
-  if (tid == 0 && nown > 0 && (want_keys || ATT)) {
-    const uint32_t bytes = (uint32_t)nown * (uint32_t)Gp * 4u;
-    mbar_arrive_expect_tx(bars + kPW, want_keys ? 2u * bytes : bytes);
-    bulk_g2s(zsl, a.zs + (row0 + b_lo) * Gp, bytes, bars + kPW);
-    if (want_keys) bulk_g2s(ssl, a.ss + (row0 + b_lo) * Gp, bytes, bars + kPW);
-  }
-  // LSE_g over all blocks from the unit's segment records (warp g)
-  if (want_keys && warp < G) {
-    const int g = warp;
-    float M = -INFINITY, S = 0.f;
-#pragma unroll 1
-    for (int k0 = 0; k0 < nseg; k0 += 128) {  // four records per lane in flight at once
-      float4 e[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int k = k0 + lane + 32 * j;
-        e[j] = k < nseg ? __ldcg(a.rec + (int64_t)(i0 + k) * G + g) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) lse_merge(M, S, e[j].x, e[j].y);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float M2 = __shfl_xor_sync(0xffffffffu, M, o), S2 = __shfl_xor_sync(0xffffffffu, S, o);
-      lse_merge(M, S, M2, S2);
-    }
-    if (lane == 0) lse[g] = M + logf(S);
-  }
-  // this CTA's share of the compensation sums: segment records p, p + C, ...
-  // rescaled to their common maximum; thread items (head, column quad), every
-  // load issued before any is used
-  const bool comp = ATT && comp_on && (!SEL || !all_sel);
-  float* csh = psm + lay.csh;  // [G][D]
-  if (comp) {
-    const int nk = p < nseg ? (nseg - 1 - p) / C + 1 : 0;
-#pragma unroll 1
-    for (int i4 = tid; i4 < G * D / 4; i4 += kPT) {
-      const int g = i4 / (D / 4), col = 4 * (i4 % (D / 4));
-      float R = -INFINITY, Wsum = 0.f;
-      float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 1
-      for (int k0 = 0; k0 < nk; k0 += 4) {
-        float4 e[4], v[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int rec = i0 + p + C * (k0 + j);
-          const bool ok = k0 + j < nk;
-          e[j] = ok ? __ldcg(a.rec + (int64_t)rec * G + g) : make_float4(-INFINITY, 0.f, -INFINITY, 0.f);
-          v[j] = ok ? __ldcg(reinterpret_cast<const float4*>(a.comp + ((int64_t)rec * G + g) * D + col))
-                    : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (e[j].z == -INFINITY) continue;
-          const float mn = fmaxf(R, e[j].z);
-          const float fo = R == -INFINITY ? 0.f : __expf(R - mn);
-          const float fn = __expf(e[j].z - mn);
-          A.x = A.x * fo + v[j].x * fn;
-          A.y = A.y * fo + v[j].y * fn;
-          A.z = A.z * fo + v[j].z * fn;
-          A.w = A.w * fo + v[j].w * fn;
-          Wsum = Wsum * fo + e[j].w * fn;
-          R = mn;
-        }
-      }
-      *reinterpret_cast<float4*>(csh + g * D + col) = A;
-      if (col == 0) {
-        cR[g] = R;
-        cW[g] = Wsum;
+  // ---- a. the open block (last warp); LSE over the records (warp 0); zbar, sigma2 rows (warp 1)
+  if (warp == kPW - 1) {
+    if (APPEND && app) open_block<D, G>(a, s, h, L, N, row0, p == own_open, anm, lane);
+    pdl_wait();
+  } else {
+    pdl_wait();  // the stream kernel's records, zbar and sigma2 are complete and visible
+    if (warp == 0 && want_keys) record_lse<G>(a, i0, nseg, lsep, lane);
+    if (warp == 1 && lane == 0 && want_keys && nown_z > 0) {
+      const uint32_t bytes = (uint32_t)nown_z * (uint32_t)Gp * 4u;
+      mbar_arrive_expect_tx(bars + kPW, 2u * bytes);
+      bulk_g2s(zsl, a.zs + (row0 + b_lo) * Gp, bytes, bars + kPW);
+      bulk_g2s(ssl, a.ss + (row0 + b_lo) * Gp, bytes, bars + kPW);
+      if (!mbar_wait_bounded(bars + kPW, 0u, a.status, s, h, 20)) {
+        mbar_drain_bounded(bars + kPW);
+        misc[kMBad] = 1;
       }
     }
   }
-  if (tid == 0 && nown > 0 && (want_keys || ATT)) {
-    if (!mbar_wait_bounded(bars + kPW, 0u, a.status, s, h, 20)) misc[kMBad] = 1;
-  }
-  __syncthreads();  // lse, zsl, ssl in place
+  pdl_trigger();  // the next call's kernels may launch (they wait for this grid before reading)
+  const unsigned long long t_wait = a.trace ? global_ns() : 0ull;
+  __syncthreads();  // LSE parts, a_g of the open block, zsl and ssl in place
   mark(0);
 
-  // ---- a, b. keys, histograms, threshold
-  int nsel_own = 0;
-  uint32_t T = 0xFFFFFFFFu;
-  int need = 0;
-  bool take_all = true;
-  const int need0 = K - 3;
+  // ---- b. keys and the local histogram; each thread a run of consecutive blocks
+  const int cpt = (nown + kPT - 1) / kPT;
+  const int c_lo = min(nown, tid * cpt), c_hi = min(nown, c_lo + cpt);
   if (want_keys) {
-    if (!all_sel) {
-      for (int i = tid; i < kFine + 256; i += kPT) hf[i] = 0u;  // hf and he
-      __syncthreads();
-    }
-    for (int i = tid; i < nown; i += kPT) {
-      const int b = b_lo + i;
-      const float lnn = ln_count(b == N - 1 ? L - kBlock * b : kBlock);
-      float S = 0.f;
+    float lse[G];
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float z = zsl[i * Gp + g], s2 = ssl[i * Gp + g];
-        const float av = lnn + z + ((a.variant & kVarFirstOrderMass) ? 0.f : 0.5f * s2);
-        const float ph = __expf(av - lse[g]);
-        S = fmaf(ph, (a.variant & kVarNoVarianceFactor) ? 1.f : s2, S);
+    for (int g = 0; g < G; ++g) {
+      float M = lsep[2 * g], S = lsep[2 * g + 1];
+      if (app) lse_merge(M, S, anm[g], 1.f);
+      lse[g] = M + logf(S);
+    }
+    for (int i = c_lo; i < c_hi; ++i) {
+      const int b = b_lo + i;
+      float S = 0.f;
+      if (i < nown_z) {  // (the open block, appended in this call, is forced: its S_b is not needed)
+        const float lnn = ln_count(b == N - 1 ? L - kBlock * b : kBlock);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          const float z = zsl[i * Gp + g], s2 = ssl[i * Gp + g];
+          const float av = lnn + z + ((a.variant & kVarFirstOrderMass) ? 0.f : 0.5f * s2);
+          const float ph = __expf(av - lse[g]);
+          S = fmaf(ph, (a.variant & kVarNoVarianceFactor) ? 1.f : s2, S);
+        }
       }
       S = fmaxf(S, 0.f);
       const uint32_t key = __float_as_uint(S);
       keys[i] = key;
       if (a.scores) a.scores[(int64_t)u * a.score_stride + b] = S;
-      if (!all_sel && b >= 1 && b <= N - 3) {
-        atomicAdd(&hf[key >> kDigitShift], 1u);
-        atomicAdd(&he[key >> 23], 1u);
-      }
+      if (hist && b >= 1 && b <= N - 3) atomicAdd(&hf[key >> kDigitShift], 1u);
     }
     __syncthreads();
   }
   mark(1);
-  cluster_wait();  // every peer's exchange histograms are zero
-  if (SEL && !all_sel && need0 > 0) {
-    // push this CTA's counts: the 16 fine bins of exponent e to rank e % C (no single rank
-    // collects them all)
+
+  // ---- the threshold bin T: the histograms summed across the cluster
+  uint32_t T = 0xFFFFFFFFu;
+  int need = 0;
+  bool take_all = true;
+  if (hist) {
+    cluster_wait();  // every peer's exchange areas are zero
     {
+      // thread e: exponent e's count to rank 0, its 16 fine bins to rank e % C
       const int e = tid;  // kPT == 256 exponents
-      if (he[e]) {
+      const uint4* hv = reinterpret_cast<const uint4*>(hf + e * 16);
+      const uint4 f0 = hv[0], f1 = hv[1], f2 = hv[2], f3 = hv[3];
+      const uint32_t ce = f0.x + f0.y + f0.z + f0.w + f1.x + f1.y + f1.z + f1.w + f2.x + f2.y + f2.z + f2.w + f3.x +
+                          f3.y + f3.z + f3.w;
+      if (ce) {
+        red_peer_add(peer_smem(xexp + e, 0), ce);
         const uint32_t fo = peer_smem(xfine + (e / C) * 16, (uint32_t)(e % C));
-        const uint4* hv = reinterpret_cast<const uint4*>(hf + e * 16);
+        const uint4 fv[4] = {f0, f1, f2, f3};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const uint4 v = hv[k];
-          if (v.x) red_peer_add(fo + 16u * k, v.x);
-          if (v.y) red_peer_add(fo + 16u * k + 4u, v.y);
-          if (v.z) red_peer_add(fo + 16u * k + 8u, v.z);
-          if (v.w) red_peer_add(fo + 16u * k + 12u, v.w);
+          if (fv[k].x) red_peer_add(fo + 16u * k, fv[k].x);
+          if (fv[k].y) red_peer_add(fo + 16u * k + 4u, fv[k].y);
+          if (fv[k].z) red_peer_add(fo + 16u * k + 8u, fv[k].z);
+          if (fv[k].w) red_peer_add(fo + 16u * k + 12u, fv[k].w);
         }
       }
     }
-    cluster_sync_all();  // barrier 1: rank e % C holds the cluster's 16 fine bins of exponent e
+    cluster_sync_all();  // barrier 1: rank 0 holds the exponent histogram, rank e % C the fine bins of e
     mark(2);
-    // thread t takes exponent 255 - t: its 16 fine bins from their owner, their sum scanned from
-    // the top; the thread where the count of larger keys reaches K - 3 finds the fine bin
-    const int ex = 255 - tid;
-    uint32_t c16[16];
-    {
-      const uint32_t fo = peer_smem(xfine + (ex / C) * 16, (uint32_t)(ex % C));
+    if (warp == 0) {
+      // lane j: exponents 255 - 8j down to 248 - 8j, from rank 0; the lane where the count of
+      // larger keys reaches need0 reads that exponent's 16 fine bins from their owner
+      const uint32_t ea = peer_smem(xexp + 248 - 8 * lane, 0);
+      const uint4 lo4 = ld_peer_u4(ea), hi4 = ld_peer_u4(ea + 16u);
+      const uint32_t cb[8] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};
+      int c8 = 0;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint4 v = ld_peer_u4(fo + 16u * k);
-        c16[4 * k] = v.x; c16[4 * k + 1] = v.y; c16[4 * k + 2] = v.z; c16[4 * k + 3] = v.w;
+      for (int k = 0; k < 8; ++k) c8 += (int)cb[k];
+      int incl = c8;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
       }
-    }
-    int c = 0;
+      if (incl - c8 < need0 && need0 <= incl) {
+        int run = incl - c8, ex = -1;
 #pragma unroll
-    for (int k = 0; k < 16; ++k) c += (int)c16[k];
-    int tot;
-    const int before = cta_exclusive_scan(c, misc + kMScan, &tot, lane, warp);
-    if (before < need0 && need0 <= before + c) {
-      int run = before;
-      for (int k = 15; k >= 0; --k) {
-        if (run < need0 && need0 <= run + (int)c16[k]) {
-          misc[kMT] = 16 * ex + k;
-          misc[kMAbove] = run;
-          misc[kMCntT] = (int)c16[k];
+        for (int k = 0; k < 8; ++k) {
+          if (ex < 0) {
+            if (run + (int)cb[k] >= need0) ex = 255 - 8 * lane - k;
+            else run += (int)cb[k];
+          }
         }
-        run += (int)c16[k];
+        const uint32_t fo = peer_smem(xfine + (ex / C) * 16, (uint32_t)(ex % C));
+        uint32_t c16[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 v = ld_peer_u4(fo + 16u * k);
+          c16[4 * k] = v.x;
+          c16[4 * k + 1] = v.y;
+          c16[4 * k + 2] = v.z;
+          c16[4 * k + 3] = v.w;
+        }
+#pragma unroll
+        for (int k = 15; k >= 0; --k) {
+          if (run < need0 && need0 <= run + (int)c16[k]) {
+            misc[kMT] = 16 * ex + k;
+            misc[kMAbove] = run;
+            misc[kMCntT] = (int)c16[k];
+          }
+          run += (int)c16[k];
+        }
       }
     }
     __syncthreads();
     T = (uint32_t)misc[kMT];
     need = need0 - misc[kMAbove];
     take_all = misc[kMCntT] == need;
+  } else {
+    cluster_wait();
   }
   mark(3);
 
-  // ---- c. classification, the exchange of counts and tie lists, the selection
-  int tot_sel = 0;     // selected blocks of the unit
-  int sum_own = 0;     // of them in the CTAs' own lists (the rest are tie winners)
-  int nwin = 0;
-  int own_base = 0;    // offset of this CTA's part of the ascending selection
-  const int nwo = (nown + 31) / 32;
-  int* cnt = misc + kMCnt;  // [C] x (own count, tie count)
+  // ---- c. the sure blocks: forced, above T, or in T when T is taken whole; this CTA's ascending list
+  int n_own = 0, ntie = 0;
   if (SEL) {
-    for (int w = tid; w < nwo; w += kPT) bits[w] = 0u;
-    __syncthreads();
-    for (int i = tid; i < nown; i += kPT) {
+    auto sure = [&](int i) -> bool {
       const int b = b_lo + i;
-      bool sl = all_sel || b == 0 || b >= N - 2;
-      if (!sl && need0 > 0) {
-        const uint32_t bin = keys[i] >> kDigitShift;
-        if (bin > T || (bin == T && take_all)) {
-          sl = true;
-        } else if (bin == T) {
-          const int slot = atomicAdd(misc + kMNtie, 1);
-          if (slot < kTieCap) win[slot] = i;  // local indices of this CTA's tie candidates (win is free until the ranking)
-        }
+      if (all_sel || b == 0 || b >= N - 2) return true;
+      if (need0 <= 0) return false;
+      const uint32_t bin = keys[i] >> kDigitShift;
+      return bin > T || (bin == T && take_all);
+    };
+    int cnt_t = 0;
+    for (int i = c_lo; i < c_hi; ++i) {
+      if (sure(i)) {
+        ++cnt_t;
+      } else if (!take_all && (keys[i] >> kDigitShift) == T) {
+        const int slot = atomicAdd(misc + kMNtie, 1);
+        if (slot < kTieCap) win[slot] = i;  // local indices of this CTA's tie candidates
       }
-      if (sl) atomicOr(&bits[i >> 5], 1u << (i & 31));
     }
-    __syncthreads();
-    if (warp == 0) {
-      const int n = bitmap_list(bits, nwo, b_lo, own, nown < K ? nown : K, lane);
-      if (lane == 0) misc[kMOwn] = n;
-    }
-    __syncthreads();
-    nsel_own = misc[kMOwn];
-    const int ntie = misc[kMNtie];
-    if (!all_sel) {
-      // push (own count, tie count) and the tie entries (key, block) to every CTA of the cluster
-      if (tid < C) st_peer_u2(peer_smem(cnt + 2 * p, (uint32_t)tid), make_uint2((uint32_t)nsel_own, (uint32_t)ntie));
-      const int nt = ntie < kTieCap ? ntie : kTieCap;
-      for (int e = tid; e < nt * C; e += kPT) {
-        const int q = e / nt, k = e % nt;
-        const int i = win[k];
-        st_peer_u2(peer_smem(tie + p * kTieCap + k, (uint32_t)q), make_uint2(keys[i], (uint32_t)(b_lo + i)));
-      }
-      if (ATT)
-        for (int e = tid; e < nsel_own; e += kPT) {
-          const int64_t row = row0 + own[e];
-          prefetch_l2(a.k + row * kBlock * D, kBlock * D * 2);
-          prefetch_l2(a.v + row * kBlock * D, kBlock * D * 2);
-        }
-      mark(4);
-      cluster_sync_all();  // barrier 2: every CTA holds every count and tie list
-      mark(5);
-      // warp 0: prefix sums of the CTAs' counts (own lists, ties), their totals and the largest tie count
-      int* opre = misc + kMOpre;
-      int* tpre = misc + kMTpre;
-      if (warp == 0) {
-        const int co = lane < C ? cnt[2 * lane] : 0, ct = lane < C ? cnt[2 * lane + 1] : 0;
-        int io = co, it = ct, mxl = ct;
+    int incl = cnt_t;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int y = __shfl_up_sync(0xffffffffu, io, o), y2 = __shfl_up_sync(0xffffffffu, it, o);
-          if (lane >= o) {
-            io += y;
-            it += y2;
-          }
-          mxl = max(mxl, __shfl_xor_sync(0xffffffffu, mxl, o));
-        }
-        if (lane <= C) {
-          opre[lane] = io - co;
-          tpre[lane] = it - ct;
-        }
-        if (lane == 31) {
-          misc[kMSumOwn] = io;
-          misc[kMNtAll] = it;
-        }
-        if (lane == 0) misc[kMMx] = mxl;
-      }
-      __syncthreads();
-      sum_own = misc[kMSumOwn];
-      const int nt_all = misc[kMNtAll], mx = misc[kMMx];
-      if (!take_all && need > 0 && (mx > kTieCap || nt_all > kRankMax)) {
-        // rare: resolve the threshold bin by more radix digits, then exchange the final counts
-        refine_select(keys, bits, nown, b_lo, N, T, need, xref, lh, misc, C, p);
-        if (warp == 0) {
-          const int n = bitmap_list(bits, nwo, b_lo, own, nown < K ? nown : K, lane);
-          if (lane == 0) misc[kMOwn] = n;
-        }
-        __syncthreads();
-        nsel_own = misc[kMOwn];
-        if (tid < C) st_peer_u2(peer_smem(cnt + 2 * p, (uint32_t)tid), make_uint2((uint32_t)nsel_own, 0u));
-        cluster_sync_all();
-        if (warp == 0) {
-          const int co = lane < C ? cnt[2 * lane] : 0;
-          int io = co;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) misc[kMWT + warp] = incl;
+    __syncthreads();
+    int pos = incl - cnt_t;
 #pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, io, o);
-            if (lane >= o) io += y;
-          }
-          if (lane <= C) opre[lane] = io - co;
-          if (lane == 31) misc[kMSumOwn] = io;
-        }
-        __syncthreads();
-        sum_own = misc[kMSumOwn];
-        nwin = 0;
-      } else if (!take_all && need > 0) {
-        // rank every tie entry among all (key desc, block asc), one warp per entry over a
-        // dense copy of the lists; the first `need` win, kept in rank order
-        uint2* dense = reinterpret_cast<uint2*>(hf + 2 * kMaxC * kTieCap);
-        for (int e = tid; e < C * kTieCap; e += kPT) {
-          const int q = e / kTieCap, k = e % kTieCap;
-          if (k < cnt[2 * q + 1]) dense[tpre[q] + k] = tie[e];
-        }
-        __syncthreads();
-        for (int j = warp; j < nt_all; j += kPW) {
-          const uint2 me = dense[j];
-          int rank = 0;
-          for (int j2 = lane; j2 < nt_all; j2 += 32) {
-            const uint2 o = dense[j2];
-            rank += (o.x > me.x) || (o.x == me.x && o.y < me.y);
-          }
-          rank = __reduce_add_sync(0xffffffffu, rank);
-          if (lane == 0 && rank < need) win[rank] = (int)me.y;
-        }
-        nwin = need;
-        __syncthreads();
+    for (int w = 0; w < kPW; ++w) {
+      const int t = misc[kMWT + w];
+      pos += w < warp ? t : 0;
+      n_own += t;
+    }
+    const int cap = nown < K ? nown : K;
+    for (int i = c_lo; i < c_hi; ++i)
+      if (sure(i)) {
+        if (pos < cap) own[pos] = b_lo + i;
+        ++pos;
       }
-      tot_sel = sum_own + nwin;
-      // this CTA's offset in the ascending selection: the lists of the lower ranks and the
-      // tie winners below this CTA's blocks
-      if (warp == 0) {
-        int below = 0;
-        for (int k = lane; k < nwin; k += 32) below += win[k] < b_lo;
-        below = __reduce_add_sync(0xffffffffu, below);
-        if (lane == 0) misc[kMWBelow] = below;
+    n_own = n_own < cap ? n_own : cap;
+    __syncthreads();  // the own list and the tie count are complete
+    ntie = misc[kMNtie];
+  }
+  mark(4);
+  if (xchg) {
+    // push (own count, tie count) and the tie entries (key, block) to every CTA of the cluster
+    if (tid < C) st_peer_u2(peer_smem(cnt + 2 * p, (uint32_t)tid), make_uint2((uint32_t)n_own, (uint32_t)ntie));
+    const int nt = ntie < kTieCap ? ntie : kTieCap;
+    for (int e = tid; e < nt * C; e += kPT) {
+      const int q = e / nt, k = e % nt;
+      const int i = win[k];
+      st_peer_u2(peer_smem(tie + p * kTieCap + k, (uint32_t)q), make_uint2(keys[i], (uint32_t)(b_lo + i)));
+    }
+    if (ATT) {
+      // blocks that are attended after the exchange: own blocks beyond the top kPW, tie candidates
+      for (int e = tid; e < n_own - kPW; e += kPT) {
+        const int64_t row = row0 + own[e];
+        prefetch_l2(a.k + row * kBlock * D, kBlock * D * 2);
+        prefetch_l2(a.v + row * kBlock * D, kBlock * D * 2);
       }
-      __syncthreads();
-      own_base = opre[p] + misc[kMWBelow];
-    } else {
-      tot_sel = N;
-      sum_own = N;
-      own_base = b_lo;
-    }
-    // the ascending selection: this CTA's blocks and its tie winners, merged
-    int* selrow = a.sel + (int64_t)u * K;
-    for (int e = tid; e < nsel_own; e += kPT) {
-      const int b = own[e];
-      int pos = own_base + e;
-      for (int k = 0; k < nwin; ++k) pos += (win[k] >= b_lo && win[k] < b);
-      if (pos < K) selrow[pos] = b;
-    }
-    for (int k = tid; k < nwin; k += kPT) {
-      const int b = win[k];
-      if (b < b_lo || b >= b_hi) continue;
-      int lo = 0, hi = nsel_own;  // own blocks below b (the list is ascending)
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (own[mid] < b) lo = mid + 1; else hi = mid;
+      for (int e = tid; e < nt; e += kPT) {
+        const int64_t row = row0 + b_lo + win[e];
+        prefetch_l2(a.k + row * kBlock * D, kBlock * D * 2);
+        prefetch_l2(a.v + row * kBlock * D, kBlock * D * 2);
       }
-      int pos = own_base + lo;
-      for (int k2 = 0; k2 < nwin; ++k2) pos += (win[k2] >= b_lo && win[k2] < b);
-      if (pos < K) selrow[pos] = b;
     }
-    if (p == 0) {
-      for (int i = tot_sel + tid; i < K; i += kPT) selrow[i] = -1;
-      if (tid == 0 && tot_sel != (N < K ? N : K)) set_error(a.status, kDevInternal, s, h, 50);
-    }
-  } else {
+    cluster_arrive();  // barrier 2 (waited for after this CTA's first blocks of attention)
+  }
+
+  // ---- d, e. attention: this warp's running state
+  float am = -INFINITY, al = 0.f;
+  float acc[KS][4];
+#pragma unroll
+  for (int mt = 0; mt < KS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+  uint32_t ph = 0u;
+  char* stg = reinterpret_cast<char*>(psm + lay.stg) + warp * stg_bytes(D);
+  int tot_sel = 0;
+  if (ATT && !SEL) {
     // the caller's selection: entries that are not ascending or not inside [0, N) are skipped and reported
     const int* selrow = a.sel + (int64_t)u * K;
     int bad = 0, cntv = 0;
@@ -703,13 +909,241 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
     tot_sel = misc[kMTot];
     if ((misc[kMBad] & 2) && p == 0 && tid == 0) set_error(a.status, kDevBadSelection, s, h, 61);
   }
-  const unsigned long long t_sel = a.trace ? global_ns() : 0ull;
-  if (tid == 0 && a.trace && a.P + (int)(gridDim.x + blockIdx.x) < a.trace_cap) {
-    unsigned long long* rr = a.trace + 1 + 8 * (int64_t)(a.P + gridDim.x + blockIdx.x);
-    rr[0] = ((unsigned long long)blockIdx.x << 32) | (2ull << 24) | (unsigned)misc[kMNtie];
+  const bool comp_blk = comp && (SEL || tot_sel < N);
+  // stage block b into this warp's buffer (rows n..15 zero); returns zbar of head lane / 4
+  auto issue = [&](int b) -> float {
+    const int64_t row = row0 + b;
+    const int n = (b == N - 1) ? L - kBlock * b : kBlock;
+    const bool fresh = APPEND && app && b == N - 1;
+    const bool cb = comp_blk && !fresh;
+    __syncwarp();  // the buffer's previous contents are read
+    if (fresh) {
+      // written in this call by this CTA's last warp (ordinary stores, ordered by the CTA barriers)
+      for (int x = lane; x < 2 * kBlock * (D / 8); x += 32) {
+        const int t = x / (D / 8), w = x % (D / 8);
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if ((t & (kBlock - 1)) < n)
+          v = __ldcg(reinterpret_cast<const uint4*>((t < kBlock ? a.k : a.v) + (row * kBlock + (t & (kBlock - 1))) * D) + w);
+        *reinterpret_cast<uint4*>(stg + t * RB + 16 * w) = v;
+      }
+    } else {
+      const int t = lane & (kBlock - 1);
+      if (t >= n) {
+        uint4* z = reinterpret_cast<uint4*>(stg + lane * RB);
 #pragma unroll
-    for (int k = 0; k < 7; ++k) rr[1 + k] = pmk[k];
+        for (int w = 0; w < D / 8; ++w) z[w] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      // the buffer may hold rows this warp wrote with ordinary stores: order them before the copies
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      if (lane == 0) mbar_arrive_expect_tx(bars + warp, 2u * (uint32_t)n * D * 2u + (cb ? D * 4u : 0u));
+      __syncwarp();
+      const uint64_t pol = policy_evict_first();
+      if (t < n) bulk_g2s_hint(stg + lane * RB, (lane < kBlock ? a.k : a.v) + (row * kBlock + t) * D, D * 2u, bars + warp, pol);
+      if (cb && lane == 0) bulk_g2s_hint(stg + 2 * kBlock * RB, a.vbar + row * D, D * 4u, bars + warp, pol);
+    }
+    return (cb && (lane >> 2) < G) ? __ldcg(a.zs + row * Gp + (lane >> 2)) : 0.f;
+  };
+  auto attend = [&](int b, float zb) {
+    const int n = (b == N - 1) ? L - kBlock * b : kBlock;
+    const bool fresh = APPEND && app && b == N - 1;
+    if (fresh) {
+      __syncwarp();
+    } else {
+      if (!mbar_wait_bounded(bars + warp, ph, a.status, s, h, 62)) {
+        mbar_drain_bounded(bars + warp);
+        misc[kMBad] |= 1;
+        return;
+      }
+      ph ^= 1u;
+    }
+    blk_attend<D, G>(am, al, acc, qf, stg, n, comp_blk && !fresh, zb, lane);
+  };
+
+  if (ATT && SEL) {
+    // this CTA's own sure blocks from the top of its list (the open block, the last, comes first)
+    const int b0 = warp < n_own ? own[n_own - 1 - warp] : -1;
+    if (xchg) misc[kMR0 + warp] = b0;
+    float zb0 = 0.f;
+    if (b0 >= 0) zb0 = issue(b0);
+    if (comp) comp_share<D, G>(a, i0, nseg, p, C, csh, cR, cW, tid);
+    if (b0 >= 0) attend(b0, zb0);
+    if (all_sel) {
+      for (int k = n_own - 1 - warp - kPW; k >= 0 && !(misc[kMBad] & 1); k -= kPW) {
+        const int b = own[k];
+        const float zb = issue(b);
+        attend(b, zb);
+      }
+    }
+  } else if (ATT) {
+    if (comp) comp_share<D, G>(a, i0, nseg, p, C, csh, cR, cW, tid);
+    const int* selrow = a.sel + (int64_t)u * K;
+    for (int rnd = 0;; ++rnd) {
+      const int j = (rnd * C + p) * kPW + warp;
+      if (j >= K || (misc[kMBad] & 1)) break;
+      const int e = __ldcg(selrow + j);
+      const int prev = j > 0 ? __ldcg(selrow + j - 1) : -1;
+      if (!(e >= 0 && e < N && (j == 0 || (prev >= 0 && prev < e)))) continue;  // warp-uniform
+      const float zb = issue(e);
+      attend(e, zb);
+    }
   }
+  mark(5);
+
+  // ---- d. after the exchange: the tie winners and the rest of the work
+  int own_base = b_lo;  // this CTA's offset in the ascending selection
+  int nwin = 0;
+  if (xchg) {
+    cluster_wait();  // barrier 2: every count and tie list is here
+    mark(6);
+    // every warp alike: lane q < C holds CTA q's counts
+    const uint2 cq = lane < C ? *reinterpret_cast<const uint2*>(cnt + 2 * lane) : make_uint2(0u, 0u);
+    const int co = (int)cq.x, ct = (int)cq.y;
+    const int ov = max(0, co - kPW), sp = lane < C ? kPW - min(co, kPW) : 0;
+    int io = co, it = ct, iv = ov, is = sp, mx = ct;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y0 = __shfl_up_sync(0xffffffffu, io, o), y1 = __shfl_up_sync(0xffffffffu, it, o);
+      const int y2 = __shfl_up_sync(0xffffffffu, iv, o), y3 = __shfl_up_sync(0xffffffffu, is, o);
+      if (lane >= o) {
+        io += y0;
+        it += y1;
+        iv += y2;
+        is += y3;
+      }
+      mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    }
+    const int sum_own = __shfl_sync(0xffffffffu, io, 31), nt_all = __shfl_sync(0xffffffffu, it, 31);
+    const int OV = __shfl_sync(0xffffffffu, iv, 31), SP = __shfl_sync(0xffffffffu, is, 31);
+    const int ovx = iv - ov;                                 // lane q: first overflow item of CTA q
+    const int spx_p = __shfl_sync(0xffffffffu, is - sp, p);  // first idle slot of this CTA
+    const int opre_p = __shfl_sync(0xffffffffu, io - co, p);
+    const bool rare = !take_all && need > 0 && (mx > kTieCap || nt_all > kRankMax);
+    if (!rare) {
+      if (!take_all && need > 0) {
+        // rank every tie entry among all (key desc, block asc), one warp per entry over a
+        // dense copy of the lists; the first `need` win, kept in rank order
+        if (warp == 0 && lane < C) misc[kMTpre + lane] = it - ct;
+        __syncthreads();
+        for (int e = tid; e < C * kTieCap; e += kPT) {
+          const int q = e / kTieCap, k = e % kTieCap;
+          if (k < cnt[2 * q + 1]) dense[misc[kMTpre + q] + k] = tie[e];
+        }
+        __syncthreads();
+        for (int j = warp; j < nt_all; j += kPW) {
+          const uint2 me = dense[j];
+          int rank = 0;
+          for (int j2 = lane; j2 < nt_all; j2 += 32) {
+            const uint2 o = dense[j2];
+            rank += (o.x > me.x) || (o.x == me.x && o.y < me.y);
+          }
+          rank = __reduce_add_sync(0xffffffffu, rank);
+          if (lane == 0 && rank < need) win[rank] = (int)me.y;
+        }
+        nwin = need;
+        __syncthreads();
+      }
+      mark(7);
+      tot_sel = sum_own + nwin;
+      // this CTA's offset in the ascending selection: the lists of the lower ranks and the
+      // tie winners below this CTA's blocks
+      int below = 0;
+      for (int k = lane; k < nwin; k += 32) below += win[k] < b_lo;
+      own_base = opre_p + __reduce_add_sync(0xffffffffu, below);
+      if (ATT) {
+        // items: the own lists beyond their top kPW (CTA by CTA), then the winners; slots: the warps
+        // idle before the exchange (CTA by CTA), then every warp round by round
+        const int total = OV + nwin;
+        const int mine0 = min(n_own, kPW);
+        for (int rnd = 0;; ++rnd) {
+          int k;
+          if (rnd == 0) {
+            if (warp < mine0) continue;
+            k = spx_p + warp - mine0;
+          } else {
+            k = SP + ((rnd - 1) * C + p) * kPW + warp;
+          }
+          if (k >= total || (misc[kMBad] & 1)) break;
+          int b;
+          if (k < OV) {
+            const unsigned bal = __ballot_sync(0xffffffffu, lane < C && ov > 0 && ovx <= k);
+            const int q = 31 - __clz(bal);
+            b = (int)ld_peer_u32(peer_smem(own + (k - __shfl_sync(0xffffffffu, ovx, q)), (uint32_t)q));
+          } else {
+            b = win[k - OV];
+          }
+          const float zb = issue(b);
+          attend(b, zb);
+        }
+      }
+    } else {
+      // rare: resolve bin T by more radix digits; every CTA attends its own winners itself
+      unsigned* bits = reinterpret_cast<unsigned*>(dense);
+      const int nwo = (nown + 31) / 32;
+      for (int w = tid; w < nwo; w += kPT) bits[w] = 0u;
+      __syncthreads();
+      for (int e = tid; e < n_own; e += kPT) atomicOr(&bits[(own[e] - b_lo) >> 5], 1u << ((own[e] - b_lo) & 31));
+      __syncthreads();
+      refine_select(keys, bits, nown, b_lo, N, T, need, xref, lh, misc, C, p);
+      if (warp == 0) {
+        const int nl = bitmap_list(bits, nwo, b_lo, own, nown < K ? nown : K, lane);
+        if (lane == 0) misc[kMOwn] = nl;
+      }
+      __syncthreads();
+      n_own = min(misc[kMOwn], nown < K ? nown : K);
+      if (tid < C) st_peer_u32(peer_smem(misc + kMCntA + p, (uint32_t)tid), (uint32_t)n_own);
+      cluster_sync_all();
+      int before = 0, all = 0;
+      for (int q = 0; q < C; ++q) {
+        before += q < p ? misc[kMCntA + q] : 0;
+        all += misc[kMCntA + q];
+      }
+      own_base = before;
+      tot_sel = all;
+      mark(7);
+      if (ATT) {
+        for (int k = warp; k < n_own && !(misc[kMBad] & 1); k += kPW) {
+          const int b = own[k];
+          bool done0 = false;
+#pragma unroll
+          for (int w = 0; w < kPW; ++w) done0 |= misc[kMR0 + w] == b;
+          if (done0) continue;
+          const float zb = issue(b);
+          attend(b, zb);
+        }
+      }
+    }
+  } else if (SEL) {
+    tot_sel = N;
+    own_base = b_lo;
+  }
+  mark(8);
+  if (SEL) {
+    // the ascending selection: this CTA's blocks and the tie winners among them, merged
+    int* selrow = a.sel + (int64_t)u * K;
+    for (int e = tid; e < n_own; e += kPT) {
+      const int b = own[e];
+      int pos = own_base + e;
+      for (int k = 0; k < nwin; ++k) pos += (win[k] >= b_lo && win[k] < b);
+      if (pos < K) selrow[pos] = b;
+    }
+    for (int k = tid; k < nwin; k += kPT) {
+      const int b = win[k];
+      if (b < b_lo || b >= b_hi) continue;
+      int lo = 0, hi = n_own;  // own blocks below b (the list is ascending)
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (own[mid] < b) lo = mid + 1; else hi = mid;
+      }
+      int pos = own_base + lo;
+      for (int k2 = 0; k2 < nwin; ++k2) pos += (win[k2] >= b_lo && win[k2] < b);
+      if (pos < K) selrow[pos] = b;
+    }
+    if (p == 0) {
+      for (int i = tot_sel + tid; i < K; i += kPT) selrow[i] = -1;
+      if (tid == 0 && tot_sel != (N < K ? N : K)) set_error(a.status, kDevInternal, s, h, 50);
+    }
+  }
+  const unsigned long long t_sel = a.trace ? global_ns() : 0ull;
   if (SEL && !ATT) {
     // score/select only: no peer reads this CTA's shared memory after the barrier
     cluster_sync_all();
@@ -720,245 +1154,75 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
     }
     return;
   }
-
-  // ---- d. attention over this CTA's picks: positions (round * C + p) * kPW + warp of the selection
-  // (the CTAs' own lists in rank order, then the tie winners; or the caller's list)
-  const bool comp_blk = comp && tot_sel < N;
-  float m[G], l[G], acc[G][V];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    m[g] = -INFINITY;
-    l[g] = 0.f;
-#pragma unroll
-    for (int i = 0; i < V; ++i) acc[g][i] = 0.f;
-  }
-  const int idx = lane & (P - 1);
-  const int jj = idx / G, gl = idx % G;
-  const int hg = lane % G;  // head of this lane's softmax entries (lane, lane + 32, ...)
-  uint32_t* wk = reinterpret_cast<uint32_t*>(psm + lay.stg + warp * lay.stg_w);
-  uint32_t* wv = wk + kBlock * D / 2;
-  float* wz = reinterpret_cast<float*>(wv + kBlock * D / 2);
-  float* wp = wz + kBlock * G;
-  uint32_t ph = 0u;
-  const int slots_all = (SEL ? tot_sel : K);
-  __syncthreads();  // the union switches from the selection to the attention staging
-  for (int rnd = 0;; ++rnd) {
-    const int j = (rnd * C + p) * kPW + warp;
-    if (j >= slots_all || misc[kMBad] & 1) break;
-    int b = -1;
-    if (SEL) {
-      if (all_sel) {
-        b = j;
-      } else if (j < sum_own) {
-        const int* opre = misc + kMOpre;
-        const unsigned bal = __ballot_sync(0xffffffffu, lane < C && opre[lane] <= j);
-        const int q = 31 - __clz(bal);  // the highest CTA whose list starts at or before j
-        b = (int)ld_peer_u32(peer_smem(own + (j - opre[q]), (uint32_t)q));
-      } else {
-        b = win[j - sum_own];
-      }
-    } else {
-      const int* selrow = a.sel + (int64_t)u * K;
-      const int e = __ldcg(selrow + j);
-      const int prev = j > 0 ? __ldcg(selrow + j - 1) : -1;
-      if (e >= 0 && e < N && (j == 0 || (prev >= 0 && prev < e))) b = e;
-    }
-    if (b < 0) continue;  // warp-uniform
-    const int n = (b == N - 1) ? L - kBlock * b : kBlock;
-    const int64_t row = row0 + b;
-    __syncwarp();  // the staging's previous contents are read
-    if (lane == 0) {
-      mbar_arrive_expect_tx(bars + warp, 2u * kBlock * D * 2u);
-      const uint64_t pol = policy_evict_first();
-      bulk_g2s_hint(wk, a.k + row * kBlock * D, kBlock * D * 2u, bars + warp, pol);
-      bulk_g2s_hint(wv, a.v + row * kBlock * D, kBlock * D * 2u, bars + warp, pol);
-    }
-    float vbr[V];
-#pragma unroll
-    for (int i = 0; i < V; ++i) vbr[i] = comp_blk ? __ldcg(a.vbar + row * D + lane * V + i) : 0.f;
-    // zbar of the block per head, as the stream left it
-    const float zb_lane = (comp_blk && lane < G) ? __ldcg(a.zs + row * Gp + lane) : 0.f;
-    if (!mbar_wait_bounded(bars + warp, ph, a.status, s, h, 62)) {
-      mbar_drain_bounded(bars + warp);
-      misc[kMBad] |= 1;
-      break;
-    }
-    ph ^= 1u;
-    // z = q . k / sqrt(d) of the block's tokens, TG tokens at a time
-#pragma unroll 1
-    for (int gi = 0; gi < NG; ++gi) {
-      float part[P];
-#pragma unroll
-      for (int t = 0; t < TG; ++t) {
-        const uint32_t* kr = wk + (gi * TG + t) * (D / 2) + lane * W;
-        float kf[V];
-#pragma unroll
-        for (int w = 0; w < W; ++w) {
-          const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(kr + w));
-          kf[2 * w] = x.x;
-          kf[2 * w + 1] = x.y;
-        }
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float acc_t = 0.f;
-#pragma unroll
-          for (int i = 0; i < V; ++i) acc_t = fmaf(qr[g][i], kf[i], acc_t);
-          part[t * G + g] = acc_t;
-        }
-      }
-      // transposed reduction: lane j ends with the total of value j & (P - 1)
-#pragma unroll
-      for (int c = P; c > 1; c >>= 1) {
-        const int off = c / 2;
-        const bool up = (idx & off) != 0;
-#pragma unroll
-        for (int i = 0; i < c / 2; ++i) {
-          const float send = up ? part[i] : part[i + c / 2];
-          const float keep = up ? part[i + c / 2] : part[i];
-          part[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-        }
-      }
-#pragma unroll
-      for (int off = P; off < 32; off <<= 1) part[0] += __shfl_xor_sync(0xffffffffu, part[0], off);
-      if (lane < P) wz[(gi * TG + jj) * G + gl] = part[0];
-    }
-    __syncwarp();
-    // per head: the block's max, the running max and the rescale, p = e^(z - max) and its sum
-    constexpr int EPL = (kBlock * G + 31) / 32;
-    float zmax = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < EPL; ++k) {
-      const int e = lane + 32 * k;
-      if (e < kBlock * G && e / G < n) zmax = fmaxf(zmax, wz[e]);
-    }
-#pragma unroll
-    for (int o = G; o < 32; o <<= 1) zmax = fmaxf(zmax, __shfl_xor_sync(0xffffffffu, zmax, o));
-    float mlane = -INFINITY;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      const float mn = fmaxf(m[g], __shfl_sync(0xffffffffu, zmax, g));
-      const float f = (m[g] == -INFINITY) ? 0.f : __expf(m[g] - mn);
-      m[g] = mn;
-      l[g] *= f;
-#pragma unroll
-      for (int i = 0; i < V; ++i) acc[g][i] *= f;
-      if (g == hg) mlane = mn;
-    }
-    float psum = 0.f;
-#pragma unroll
-    for (int k = 0; k < EPL; ++k) {
-      const int e = lane + 32 * k;
-      if (e < kBlock * G) {
-        const float pe = e / G < n ? __expf(wz[e] - mlane) : 0.f;
-        wp[e] = pe;
-        psum += pe;
-      }
-    }
-#pragma unroll
-    for (int o = G; o < 32; o <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, o);
-#pragma unroll
-    for (int g = 0; g < G; ++g) l[g] += __shfl_sync(0xffffffffu, psum, g);
-    __syncwarp();
-    // acc += p v over the block's tokens
-#pragma unroll 2
-    for (int t = 0; t < n; ++t) {
-      const uint32_t* vr = wv + t * (D / 2) + lane * W;
-      float vf[V];
-#pragma unroll
-      for (int w = 0; w < W; ++w) {
-        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(vr + w));
-        vf[2 * w] = x.x;
-        vf[2 * w + 1] = x.y;
-      }
-      float pg[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) pg[g] = wp[t * G + g];
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int i = 0; i < V; ++i) acc[g][i] = fmaf(pg[g], vf[i], acc[g][i]);
-    }
-    if (comp_blk) {
-      // remove this block's own compensation term (the stream added it for every block)
-      const float lnn = ln_count(n);
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float e = lnn + __shfl_sync(0xffffffffu, zb_lane, g);
-        const float mn = fmaxf(m[g], e);
-        const float fo = (m[g] == -INFINITY) ? 0.f : __expf(m[g] - mn);
-        const float fn = __expf(e - mn);
-        m[g] = mn;
-        l[g] = l[g] * fo - fn;
-#pragma unroll
-        for (int i = 0; i < V; ++i) acc[g][i] = acc[g][i] * fo - fn * vbr[i];
-      }
-    }
-  }
   const unsigned long long t_att = a.trace ? global_ns() : 0ull;
-  // ---- the CTA's partial: its warps and (warp 0's registers) its compensation share
+
+  // ---- the CTA's partial: its warps and its compensation share
   __syncthreads();  // the staging is free: the partials reuse the union
-  float* red_a = psm + lay.red;            // [kPW][G][D]
-  float* red_m = red_a + kPW * G * D;      // [kPW][G]
-  float* red_l = red_m + kPW * G;          // [kPW][G]
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    if (lane == 0) {
-      red_m[warp * G + g] = m[g];
-      red_l[warp * G + g] = l[g];
+  float* red_a = psm + lay.red;            // [kPW][8][D]
+  float* red_m = red_a + kPW * D * 8;      // [kPW][8]
+  float* red_l = red_m + kPW * 8;          // [kPW][8]
+  {
+    const int r = lane >> 2, c = lane & 3;
+    if (c == 0 && r < G) {
+      red_m[warp * 8 + r] = am;
+      red_l[warp * 8 + r] = al;
     }
+    float* ra = red_a + (warp * 8 + 2 * c) * D + r;  // head 2c; head 2c + 1 is D further
 #pragma unroll
-    for (int i = 0; i < V; ++i) red_a[(warp * G + g) * D + lane * V + i] = acc[g][i];
-  }
-  __syncthreads();
-  // per head, once: the common maximum of the warps' parts (and the compensation share)
-  // and each part's factor (warp g: lane w takes warp w, lane kPW the share)
-  float* fac = red_l + kPW * G;  // [G][kPW + 1] factors, then [G] maxima and [G] sums
-  float* facM = fac + G * (kPW + 1);
-  float* facL = facM + G;
-  if (warp < G) {
-    const int g = warp;
-    const bool sh = lane == kPW && comp_blk;
-    const float mw = lane < kPW ? red_m[lane * G + g] : (sh ? cR[g] : -INFINITY);
-    const float lw = lane < kPW ? red_l[lane * G + g] : (sh ? cW[g] : 0.f);
-    const float M = warp_max(mw);
-    const float f = (M == -INFINITY || mw == -INFINITY) ? 0.f : __expf(mw - M);
-    const float ls = warp_sum(lw * f);
-    if (lane <= kPW) fac[g * (kPW + 1) + lane] = f;
-    if (lane == 0) {
-      facM[g] = M;
-      facL[g] = ls;
+    for (int mt = 0; mt < KS; ++mt) {
+      if (2 * c < G) {
+        ra[16 * mt] = acc[mt][0];
+        ra[16 * mt + 8] = acc[mt][2];
+      }
+      if (2 * c + 1 < G) {
+        ra[D + 16 * mt] = acc[mt][1];
+        ra[D + 16 * mt + 8] = acc[mt][3];
+      }
     }
   }
   __syncthreads();
-  // per float4 column item: combine, then push to the rank that merges it
+  mark(9);
+  // per float4 column item: the warps' parts (and the share) at their common maximum, pushed to
+  // the rank that merges the item
   const int items = G * D / 4;
   const int ipr = post_ipr(D, G, C);
   for (int i4 = tid; i4 < items; i4 += kPT) {
     const int g = (4 * i4) / D, col = (4 * i4) % D;
-    float4 as = make_float4(0.f, 0.f, 0.f, 0.f);
+    float M = comp_blk ? cR[g] : -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kPW; ++w) {
-      const float f = fac[g * (kPW + 1) + w];
-      const float4 x = *reinterpret_cast<const float4*>(red_a + (w * G + g) * D + col);
-      as.x = fmaf(x.x, f, as.x);
-      as.y = fmaf(x.y, f, as.y);
-      as.z = fmaf(x.z, f, as.z);
-      as.w = fmaf(x.w, f, as.w);
-    }
-    if (comp_blk) {
-      const float f = fac[g * (kPW + 1) + kPW];
-      const float4 x = *reinterpret_cast<const float4*>(csh + g * D + col);
-      as.x = fmaf(x.x, f, as.x);
-      as.y = fmaf(x.y, f, as.y);
-      as.z = fmaf(x.z, f, as.z);
-      as.w = fmaf(x.w, f, as.w);
+    for (int w = 0; w < kPW; ++w) M = fmaxf(M, red_m[w * 8 + g]);
+    float4 as = make_float4(0.f, 0.f, 0.f, 0.f);
+    float Ls = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kPW; ++w) {
+        const float mw = red_m[w * 8 + g];
+        const float f = mw == -INFINITY ? 0.f : __expf(mw - M);
+        Ls = fmaf(f, red_l[w * 8 + g], Ls);
+        const float4 x = *reinterpret_cast<const float4*>(red_a + (w * 8 + g) * D + col);
+        as.x = fmaf(x.x, f, as.x);
+        as.y = fmaf(x.y, f, as.y);
+        as.z = fmaf(x.z, f, as.z);
+        as.w = fmaf(x.w, f, as.w);
+      }
+      if (comp_blk && cR[g] != -INFINITY) {
+        const float f = __expf(cR[g] - M);
+        const float4 x = *reinterpret_cast<const float4*>(csh + g * D + col);
+        Ls = fmaf(f, cW[g], Ls);
+        as.x = fmaf(x.x, f, as.x);
+        as.y = fmaf(x.y, f, as.y);
+        as.z = fmaf(x.z, f, as.z);
+        as.w = fmaf(x.w, f, as.w);
+      }
     }
     const int rk = i4 / ipr, il = i4 - rk * ipr;
     const uint32_t dst = peer_smem(xm + (il * C + p) * 8, (uint32_t)rk);
     st_peer_f4(dst, as);
-    st_peer_u2(dst + 16u, make_uint2(__float_as_uint(facM[g]), __float_as_uint(facL[g])));
+    st_peer_u2(dst + 16u, make_uint2(__float_as_uint(M), __float_as_uint(Ls)));
   }
+  mark(10);
   cluster_sync_all();  // barrier 3: every partial of this rank's columns is here; no CTA touches a peer after this
+  mark(11);
   if (APPEND && p == 0 && tid == 0) {
     // every CTA of this cluster has read seq_len; the last cluster to get here
     // writes the lengths after this call's append (a sequence at capacity keeps its own)
@@ -1012,6 +1276,14 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
         float* out = a.out + ((int64_t)s * a.Hkv + h) * G * D;
         *reinterpret_cast<float4*>(out + g * D + col) = make_float4(as.x * inv, as.y * inv, as.z * inv, as.w * inv);
       }
+    }
+  }
+  mark(12);
+  if (tid == 0 && a.trace && a.P + 3 * (int)gridDim.x < a.trace_cap) {
+    for (int rec = 0; rec < 2; ++rec) {
+      unsigned long long* rr = a.trace + 1 + 8 * (int64_t)(a.P + (1 + rec) * gridDim.x + blockIdx.x);
+      rr[0] = ((unsigned long long)blockIdx.x << 32) | ((2ull + rec) << 24) | (unsigned)(ntie | (n_own << 12));
+      for (int k = 0; k < 7; ++k) rr[1 + k] = pmk[7 * rec + k];
     }
   }
   if (tid == 0 && a.trace && a.P + (int)blockIdx.x < a.trace_cap) {

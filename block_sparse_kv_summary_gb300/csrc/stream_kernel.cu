@@ -10,9 +10,10 @@
 // streams every summary row of the layer once and leaves, per block, zbar and
 // sigma2, and per segment of blocks the logsumexp parts of a and the
 // compensation sums over all of its blocks (the post kernel removes the
-// selected blocks' own terms).  Section "어떻게 쓰나" fuses the open block's
-// summary update with the K/V pack: the CTA whose segment holds the newest
-// block appends the new token first.
+// selected blocks' own terms).  A call that appends leaves the open block
+// (the one receiving the new token) to the post kernel, which packs the token
+// and recomputes that block's summary ("어떻게 쓰나": the fused update of the
+// current block's statistics and the K/V pack).
 //
 // Grid: P persistent CTAs of kWarps warps.  The layer's units are cut into
 // segments (decode_common.cuh); CTA i takes segments i, i + P, ...  Within a
@@ -53,12 +54,13 @@ __host__ __device__ inline int stream_slot_floats(int D, int r, int G, bool scor
   const int sb = stage_blocks(r, G);
   return sb * D + (comp ? sb * D : 0) + (score ? sb * (r < 4 ? 4 : r) : 0);
 }
-// shared memory: slots | per-warp weights [kWarps][sb][G] | Qsq [G][rr] | the appended
-// block's kbar [D], vbar [D], Dbar [rr] | plan (ints) | mbarriers
+// shared memory: slots | per-warp weights [kWarps][sb][G] | per-warp Qsq [kWarps][G][rr] |
+// plan (ints) | mbarriers
 __host__ __device__ inline int stream_smem_bytes(int D, int r, int G, bool score, bool comp) {
   const int rr = (r + 3) & ~3;
   const int sb = stage_blocks(r, G);
-  const int floats = kWarps * kSlots * stream_slot_floats(D, r, G, score, comp) + kWarps * sb * G + G * rr + 2 * D + rr;
+  const int floats = kWarps * kSlots * stream_slot_floats(D, r, G, score, comp) + kWarps * sb * G +
+                     (long_dbar(r) ? 1 : kWarps) * G * rr;
   return floats * 4 + (3 * kMaxBatch + 8) * 4 + 8 * (kWarps * kSlots + 2) + 64;
 }
 
@@ -116,37 +118,35 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
   const int slot_f = stream_slot_floats(D, r, G, SCORE, COMP);
   float* slots = sm;
   float* sw = slots + kWarps * kSlots * slot_f;  // [kWarps][SB][G]
-  float* sqs = sw + kWarps * SB * G;             // [G][rr]
-  float* pk = sqs + G * rr;                      // appended block: kbar [D], vbar [D], Dbar [rr]
-  float* pv = pk + D;
-  float* pd = pv + D;
-  int* sL = reinterpret_cast<int*>(pd + rr);     // [kMaxBatch] tokens of each sequence in this call
-  int* sN = sL + kMaxBatch;                      // [kMaxBatch] blocks
+  float* sqs = sw + kWarps * SB * G;             // [kWarps][G][rr] (one copy per warp; shared when RB)
+  int* sL = reinterpret_cast<int*>(sqs + (RB ? 1 : kWarps) * G * rr);  // [kMaxBatch] tokens of each sequence in this call
+  int* sN = sL + kMaxBatch;                      // [kMaxBatch] blocks streamed
   int* soff = sN + kMaxBatch;                    // [kMaxBatch + 1] first segment of each sequence
   int* sseg = soff + kMaxBatch + 1;
-  int* sfits = sseg + 1;                         // [2] bit s: sequence s had room for its token
-  int* sbad = sfits + 2;                         // a wait of this CTA ran out
+  int* sbad = sseg + 1;                          // a wait of this CTA ran out
   uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(sbad + 1) + 7) & ~uintptr_t(7));
-  uint64_t* patch_bar = bars + kWarps * kSlots;
   const unsigned long long t_start = a.trace ? global_ns() : 0ull;
-  if (threadIdx.x < kWarps * kSlots + 1) mbar_init(bars + threadIdx.x, 1);
-  if (threadIdx.x == 0) *sbad = 0;
-  fence_mbar_init();
+  if (threadIdx.x < kWarps * kSlots) mbar_init(bars + threadIdx.x, 1);
+  if (threadIdx.x == 0) {
+    *sbad = 0;
+    fence_mbar_init();
+  }
   // the previous work on the stream may have written this cache and its lengths
   pdl_wait();
   pdl_trigger();
   if (warp == 0) {
     const int s0 = lane, s1 = lane + 32;
     bool f0 = false, f1 = false;
-    if (s0 < a.B) sL[s0] = call_tokens(a.seq_len[s0], a.cap_blocks[s0], APPEND, &f0);
-    if (s1 < a.B) sL[s1] = call_tokens(a.seq_len[s1], a.cap_blocks[s1], APPEND, &f1);
-    const unsigned m0 = __ballot_sync(0xffffffffu, f0), m1 = __ballot_sync(0xffffffffu, f1);
-    if (lane == 0) {
-      sfits[0] = (int)m0;
-      sfits[1] = (int)m1;
+    if (s0 < a.B) {
+      sL[s0] = call_tokens(a.seq_len[s0], a.cap_blocks[s0], APPEND, &f0);
+      sN[s0] = streamed_blocks(sL[s0], APPEND && f0, SELMODE, a.K, a.scores != nullptr);
+    }
+    if (s1 < a.B) {
+      sL[s1] = call_tokens(a.seq_len[s1], a.cap_blocks[s1], APPEND, &f1);
+      sN[s1] = streamed_blocks(sL[s1], APPEND && f1, SELMODE, a.K, a.scores != nullptr);
     }
     __syncwarp();
-    plan_warp(sL, a.B, a.Hkv, a.P, SB, sN, soff, sseg, lane);
+    plan_warp(sN, a.B, a.Hkv, a.P, SB, soff, sseg, lane);
     if (APPEND && blockIdx.x == 0) {
       if (s0 < a.B && !f0) set_error(a.status, kDevCapacity, s0, -1, 1);
       if (s1 < a.B && !f1) set_error(a.status, kDevCapacity, s1, -1, 1);
@@ -157,9 +157,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
   const unsigned long long t_plan = a.trace ? global_ns() : 0ull;
   unsigned long long t_first = 0ull, t_r1 = 0ull, t_r2 = 0ull, t_r3 = 0ull;
   int nseg_done = 0;
-  int npatch = 0;     // patches completed in this CTA (phases of patch_bar)
   uint32_t uses = 0;  // stages this warp has consumed: slot uses % kSlots, phase (uses / kSlots) & 1
   float* swr = sw + warp * SB * G;
+  float* sqw = RB ? sqs : sqs + warp * G * rr;  // this warp's Qsq [G][rr]
   // this lane's (block, head) value of a stage
   const int vv = lane >> SH, vb = vv / G, vg = vv % G;
   const bool primary = (lane & ((1 << SH) - 1)) == 0;
@@ -167,17 +167,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
   for (int si = blockIdx.x; si < total; si += gridDim.x) {
     int s, h, b0, nb;
     plan_segment(si, a.B, a.Hkv, sN, soff, seg, &s, &h, &b0, &nb);
-    const int L = sL[s], N = sN[s];
-    const bool fits = ((s < 32 ? sfits[0] >> s : sfits[1] >> (s - 32)) & 1) != 0;
-    const bool append = APPEND && fits && b0 + nb == N;  // this segment holds the open block
+    const int L = sL[s], N = ceil_blocks(L);  // N: all blocks (the last may be partial)
     const int64_t row0 = row_of(a, s, h, b0);
     const int ns = (nb + SB - 1) / SB;  // stages of the segment
     const bool comp = COMP && !(a.variant & kVarNoCompensation) && (!SELMODE || N > a.K);
     const bool dbulk = SCORE && r >= 4;
-    // ---- this warp's copies: its j-th stage of the segment is stage warp + kWarps j
     // the summaries are read once per call: evict-first in L2, so that they do not
     // push the kernels' code and the small scratch arrays out of it
     const uint64_t pol = policy_evict_first();
+    // ---- this warp's copies: its j-th stage of the segment is stage warp + kWarps j
     auto issue = [&](int k, uint32_t use) {
       float* st = slots + (warp * kSlots + (int)(use % kSlots)) * slot_f;
       const int rb = k * SB, n = min(SB, nb - rb);
@@ -191,7 +189,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
     const int mine = warp < ns ? (ns - 1 - warp) / kWarps + 1 : 0;  // stages of this warp
     if (lane == 0)
       for (int j = 0; j < min(kSlots, mine); ++j) issue(warp + kWarps * j, uses + j);
-    // ---- queries of the unit: this lane's coordinates, scaled by 1/sqrt(d); Qsq by warp 1
+    // ---- queries of the unit: this lane's coordinates, scaled by 1/sqrt(d); Qsq per warp
+    // (one shared copy, and a CTA barrier, for long Dbar rows)
     const float* qbase = a.q + ((int64_t)s * a.Hkv + h) * G * D;
     float q[G][CPL];
 #pragma unroll
@@ -200,132 +199,37 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
 #pragma unroll
       for (int c = 0; c < CPL; ++c) q[g][c] *= InvSqrt<D>::v;
     }
-    if (SCORE && warp == 1) {
-      // Qsq_{g,t} = sum of q_g^2 over coordinate group t = [t*D/r, (t+1)*D/r) (unscaled q)
+    if (SCORE && (!RB || warp == 1)) {
+      // Qsq_{g,t} = sum of q_g^2 over coordinate group t = [t*D/r, (t+1)*D/r) (q unscaled: x d)
       const int gs = D / r;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        float x[CPL];
-        lds_vec<CPL>(qbase + g * D + CPL * lane, x);
         if (gs >= CPL) {
           float t = 0.f;
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) t = fmaf(x[c], x[c], t);
+          for (int c = 0; c < CPL; ++c) t = fmaf(q[g][c], q[g][c], t);
           for (int o = 1; o < gs / CPL; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-          if ((lane & (gs / CPL - 1)) == 0) sqs[g * rr + (CPL * lane) / gs] = t;
+          if ((lane & (gs / CPL - 1)) == 0) sqw[g * rr + (CPL * lane) / gs] = t * (float)D;
         } else {
           float t = 0.f;
 #pragma unroll
           for (int c = 0; c < CPL; ++c) {
-            t = fmaf(x[c], x[c], t);
+            t = fmaf(q[g][c], q[g][c], t);
             if ((c + 1) % gs == 0) {
-              sqs[g * rr + (CPL * lane + c) / gs] = t;
+              sqw[g * rr + (CPL * lane + c) / gs] = t * (float)D;
               t = 0.f;
             }
           }
         }
       }
     }
-    __syncthreads();  // Qsq is in place; the previous segment's patch is no longer read
-    const int patched = append ? (N - 1 - b0) : -1;  // segment-local block whose rows come from pk, pv, pd
-    if (append) ++npatch;
-    // ---- append: warp 0 of the CTA holding the open block packs the new token and
-    // recomputes that block's summary from its tokens (two-pass fp32 mean and
-    // population variance from the exact bf16 values) while the other warps stream
-    if (append && warp == 0) {
-      const int n = L - kBlock * (N - 1);
-      const int64_t row = row_of(a, s, h, N - 1);
-      const int c0 = CPL * lane;
-      const int64_t nw_off = ((int64_t)s * a.Hkv + h) * D + c0;
-      const __nv_bfloat16* kb = a.k + row * kBlock * D + c0;
-      const __nv_bfloat16* vbp = a.v + row * kBlock * D + c0;
-      // pass 1: the new token into its slot; sums of the keys and values (all loads
-      // independent: one round trip)
-      store_bf16_raw<CPL>(a.k + (row * kBlock + n - 1) * D + c0, a.k_new + nw_off);
-      store_bf16_raw<CPL>(a.v + (row * kBlock + n - 1) * D + c0, a.v_new + nw_off);
-      float ksum[CPL], vsum[CPL], kn[CPL];
-      load_bf16<CPL>(a.k_new + nw_off, kn);
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) ksum[c] = vsum[c] = 0.f;
-#pragma unroll
-      for (int j = 0; j < kBlock; ++j) {
-        if (j < n) {
-          float kf[CPL], vf[CPL];
-          load_bf16<CPL>(j == n - 1 ? a.k_new + nw_off : kb + j * D, kf);
-          load_bf16<CPL>(j == n - 1 ? a.v_new + nw_off : vbp + j * D, vf);
-#pragma unroll
-          for (int c = 0; c < CPL; ++c) {
-            ksum[c] += kf[c];
-            vsum[c] += vf[c];
-          }
-        }
-      }
-      float mk[CPL], var[CPL];
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        mk[c] = ksum[c] / (float)n;
-        var[c] = 0.f;
-      }
-      // pass 2: population variance about the mean (the old tokens re-read, now cached
-      // close by; the new one kept)
-#pragma unroll
-      for (int j = 0; j < kBlock; ++j) {
-        if (j < n) {
-          float kf[CPL];
-          if (j == n - 1) {
-#pragma unroll
-            for (int c = 0; c < CPL; ++c) kf[c] = kn[c];
-          } else {
-            load_bf16<CPL>(kb + j * D, kf);
-          }
-#pragma unroll
-          for (int c = 0; c < CPL; ++c) {
-            const float dv = kf[c] - mk[c];
-            var[c] = fmaf(dv, dv, var[c]);
-          }
-        }
-      }
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        const float mv = vsum[c] / (float)n;
-        var[c] /= (float)n;
-        pk[c0 + c] = mk[c];
-        pv[c0 + c] = mv;
-        a.kbar[row * D + c0 + c] = mk[c];
-        a.vbar[row * D + c0 + c] = mv;
-      }
-      // Dbar_t: mean of the variances over coordinate group t = [t*D/r, (t+1)*D/r)
-      const int gs = D / r;
-      if (gs >= CPL) {
-        float t = 0.f;
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) t += var[c];
-        for (int o = 1; o < gs / CPL; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-        if ((lane & (gs / CPL - 1)) == 0) {
-          const float m = t / (float)gs;
-          pd[c0 / gs] = m;
-          a.dbar[row * r + c0 / gs] = m;
-        }
-      } else {
-        float t = 0.f;
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-          t += var[c];
-          if ((c + 1) % gs == 0) {
-            const float m = t / (float)gs;
-            pd[(c0 + c) / gs] = m;
-            a.dbar[row * r + (c0 + c) / gs] = m;
-            t = 0.f;
-          }
-        }
-      }
-      fence_proxy_async_global();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(patch_bar);
-    }
+    if (RB)
+      __syncthreads();  // the shared Qsq is in place
+    else
+      __syncwarp();     // this warp's Qsq is in place
 
     // ---- stream this warp's stages
-    float lm = -INFINITY, ll = 0.f;  // this lane's value: running max of a, sum of e^(a - max)
+    float lm = -INFINITY, ll = 0.f;        // this lane's value: running max of a, sum of e^(a - max)
     float ref[G], acc[G][CPL], wsl = 0.f;  // compensation: per-head reference, numerator, weight sum
 #pragma unroll
     for (int g = 0; g < G; ++g) {
@@ -334,7 +238,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
       for (int c = 0; c < CPL; ++c) acc[g][c] = 0.f;
     }
     bool bad = false;
-    bool patch_ready = !append;
     for (int j = 0; j < mine; ++j) {
       const int k = warp + kWarps * j;
       const uint32_t use = uses + j;
@@ -343,13 +246,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
       const float* svb = st + SB * D;
       float* sdb = const_cast<float*>(st) + SB * D * (comp ? 2 : 1);
       const int rb = k * SB, nbs = min(SB, nb - rb);
-      if (!patch_ready && patched >= rb && patched < rb + nbs) {
-        if (!mbar_wait_bounded(patch_bar, (uint32_t)(npatch - 1) & 1u, a.status, s, h, 12)) bad = true;
-        patch_ready = true;
-      }
       if (SCORE && !dbulk && lane < nbs * r)  // r < 4: the Dbar rows by plain loads, 4 floats per row
         sdb[(lane / r) * 4 + lane % r] = a.dbar[(row0 + rb) * r + lane];
-      if (bad || !mbar_wait_bounded(bars + warp * kSlots + (use % kSlots), (use / kSlots) & 1u, a.status, s, h, 10)) {
+      if (!mbar_wait_bounded(bars + warp * kSlots + (use % kSlots), (use / kSlots) & 1u, a.status, s, h, 10)) {
         bad = true;
         break;
       }
@@ -359,8 +258,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
 #pragma unroll
       for (int b = 0; b < SB; ++b) {
         float x[CPL];
-        const float* rowp = (rb + b == patched) ? pk : skb + b * D;
-        lds_vec<CPL>(rowp + CPL * lane, x);
+        lds_vec<CPL>(skb + b * D + CPL * lane, x);
         if (b >= nbs) {
 #pragma unroll
           for (int c = 0; c < CPL; ++c) x[c] = 0.f;
@@ -386,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
           float ps[NV];
 #pragma unroll
           for (int b = 0; b < SB; ++b) {
-            const float* drow = (rb + b == patched) ? pd : sdb + b * rs;
+            const float* drow = sdb + b * rs;
             float x[4];
 #pragma unroll
             for (int t = 0; t < 4; ++t) x[t] = (t < rpl && b < nbs) ? drow[rpl * lane + t] : 0.f;
@@ -395,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
               float t = 0.f;
 #pragma unroll
               for (int c = 0; c < 4; ++c)
-                if (c < rpl) t = fmaf(sqs[g * rr + rpl * lane + c], x[c], t);
+                if (c < rpl) t = fmaf(sqw[g * rr + rpl * lane + c], x[c], t);
               ps[b * G + g] = t;
             }
           }
@@ -403,13 +301,18 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
           s2 = ps[0] * (1.f / (float)D);
         } else {
           if (ok) {
-            const float* drow = (rb + vb == patched) ? pd : sdb + vb * rs;
-            const float* qsr = sqs + vg * rr;
+            const float* drow = sdb + vb * rs;
+            const float* qsr = sqw + vg * rr;
             float t = 0.f;
             if (r <= 16) {
 #pragma unroll
-              for (int tt = 0; tt < 16; ++tt)
-                if (tt < r) t = fmaf(qsr[tt], drow[tt], t);
+              for (int tt = 0; tt < 16; tt += 4) {
+                if (tt < r) {
+                  const float4 qv = *reinterpret_cast<const float4*>(qsr + tt);
+                  const float4 dv = *reinterpret_cast<const float4*>(drow + tt);
+                  t = fmaf(qv.x, dv.x, fmaf(qv.y, dv.y, fmaf(qv.z, dv.z, fmaf(qv.w, dv.w, t))));
+                }
+              }
             } else {
               for (int tt = 0; tt < r; tt += 4) {
                 const float4 qv = *reinterpret_cast<const float4*>(qsr + tt);
@@ -424,8 +327,8 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
       if (primary && ok) {
         const int64_t o = (row0 + rb + vb) * Gp + vg;
         a.zs[o] = zb;
-        if (SCORE) a.ss[o] = s2;
         if (SCORE) {
+          a.ss[o] = s2;
           const float av = cv + ((a.variant & kVarFirstOrderMass) ? 0.f : 0.5f * s2);
           const float mn = fmaxf(lm, av);
           ll = (lm == -INFINITY ? 0.f : ll * __expf(lm - mn)) + __expf(av - mn);
@@ -466,8 +369,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
         __syncwarp();
         for (int b = 0; b < nbs; ++b) {
           float x[CPL], wv[G];
-          const float* rowp = (rb + b == patched) ? pv : svb + b * D;
-          lds_vec<CPL>(rowp + CPL * lane, x);
+          lds_vec<CPL>(svb + b * D + CPL * lane, x);
 #pragma unroll
           for (int g = 0; g < G; ++g) wv[g] = swr[b * G + g];
 #pragma unroll

@@ -206,12 +206,17 @@ compkv_status compkv_decode_host(compkv_ctx *ctx, int layer, const float *q_host
  * COMPKV_ERR_UNSUPPORTED_SHAPE and a message naming both sizes.  The call
  * allocates nothing; it enqueues a clear of the array's status word and
  * counters and the decode kernels on `stream`.  The first call on each device
- * (with that device current) looks up the array's device address once; make
- * that first call before any stream capture.  All calls share the one array,
- * so calls whose work overlaps on the GPU (different streams, or several host
- * threads) race and corrupt each other: order them on one stream.  Its
- * device-side checks (a sequence at capacity) have no status read-back:
- * check capacities on the host.  Returns host-side errors like compkv_decode. */
+ * (with that device current) looks up the array's device address once and
+ * keeps it for the life of the process; make that first call before any
+ * stream capture.  A cudaDeviceReset() destroys the array with the context,
+ * and the kept address is then stale: do not call compkv_decode_static after
+ * a reset of a device it has run on.  All calls share the one array, so
+ * calls whose work overlaps on the GPU (different streams, or several host
+ * threads) race and corrupt each other: order them on one stream.  None of
+ * its device-side checks is reported back (a sequence at capacity, a bounded
+ * wait that ran out): the status word is cleared by the next call and no call
+ * reads it, so check capacities on the host.  Returns host-side errors like
+ * compkv_decode. */
 #define COMPKV_STATIC_SCRATCH_BYTES (16u << 20)
 compkv_status compkv_decode_static(const compkv_config *cfg, const compkv_buffers *bufs, int layer,
                                    const float *q, const void *k_new, const void *v_new, float *out,
