@@ -169,7 +169,7 @@ def ncu_traffic(kernel_file: str, kernel: str, workload: str):
     return rec.get("kernels", {}).get(kernel, {}).get("dram_bytes_per_launch")
 
 
-def bench_workload(name, r=None, budget=None, dense=False):
+def bench_workload(name, r=None, budget=None, dense=False, layers=None):
     """The synth workload behind a bench workload name, with optional overrides:
     r (variance groups), budget (tokens), or dense (budget covering the whole
     context: every block selected, i.e. exact attention over the cache)."""
@@ -189,6 +189,9 @@ def bench_workload(name, r=None, budget=None, dense=False):
     if budget is not None:
         changes["budget_tokens"] = int(budget)
     wl = synth.small_variant(base, **changes) if changes else synth.WORKLOADS[base]
+    if layers is not None:
+        R = int(layers)
+        desc += f"; {R} rotated layer cache(s)"
     return wl, R, desc
 
 
@@ -277,6 +280,33 @@ class Layers:
     def step(self):
         for _ in range(self.calls_per_step):
             self.call_once()
+
+
+def trace_spans(cache, work, device, calls=8):
+    """Median over `calls` traced decode calls of each kernel's span inside the chain:
+    the earliest CTA start to the latest CTA end of the stream and of the post kernel."""
+    import torch
+
+    from block_sparse_kv_summary_gb300 import compkv as C
+    buf = torch.zeros(1 + 8 * 8192, dtype=torch.int64, device=device)
+    C.compkv_trace(cache.ctx, buf.data_ptr(), buf.numel() * 8)
+    st, po = [], []
+    try:
+        for _ in range(calls):
+            buf.zero_()
+            work.call_once()
+            torch.cuda.synchronize(device)
+            tr = buf.cpu().numpy()[1:].reshape(-1, 8).astype(np.int64)
+            used = tr[:, 2] != 0
+            kind = (tr[:, 0] >> 24) & 0xff
+            s_rec, p_rec = tr[used & (kind == 0)], tr[used & (kind == 1)]
+            if len(s_rec):
+                st.append((s_rec[:, 5].max() - s_rec[:, 2].min()) / 1e3)
+            if len(p_rec):
+                po.append((p_rec[:, 6].max() - p_rec[:, 2].min()) / 1e3)
+    finally:
+        C.compkv_trace(cache.ctx, 0, 0)
+    return {"k_stream": float(np.median(st)) if st else None, "k_post": float(np.median(po)) if po else None}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -388,10 +418,13 @@ def main():
     ap.add_argument("--budget", type=int, default=None, help="override the budget in tokens (budget sweep)")
     ap.add_argument("--dense", action="store_true",
                     help="budget covering the whole context: every block selected (exact attention baseline)")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="rotated layer caches (profiling runs: 1 keeps the device footprint small)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     ws, rank, local = dist_env()
     overrides = {"r": args.r, "budget": args.budget, "dense": args.dense}
+    layer_override = {"layers": args.layers} if args.layers else {}
     wl0, _, _ = bench_workload(args.workload, **overrides)
     calls_per_step = wl0.layers if wl0.layers > 1 else 1
     if args.steps <= 0:
@@ -427,7 +460,7 @@ def main():
     barrier(ws)
     P.lib()
 
-    work = Layers(args.workload, device, **overrides)
+    work = Layers(args.workload, device, **overrides, **layer_override)
     cache = work.cache
     for _ in range(args.warmup):
         work.step()
@@ -479,6 +512,10 @@ def main():
         fam_ms.update({fam: cache.profile_read(fam) for fam in fams})
         cache.profile(0)
 
+    # ---- in-chain span of each kernel (first CTA start to last CTA end, %globaltimer), from
+    # the device trace of a few calls; informational next to the event times above
+    spans = trace_spans(cache, work, device)
+
     # ---- end to end through compkv_decode_host: pinned host inputs, output back, synchronised per call
     ke = min(args.steps * calls_per_step, 2000)
     R, S = work.R, work.wl.steps
@@ -513,6 +550,8 @@ def main():
     step_gbs = by["total"] / (us_call * 1e-6) / 1e9
     kernels = {f: {"launches": n, "avg_us": (m * 1e3 / n if n else None)} for f, (m, n) in fam_ms.items()}
     kernels["decode"]["note"] = "one decode call: the two PDL-chained kernels"
+    for f in ("k_stream", "k_post"):
+        kernels[f]["span_in_chain_us"] = spans.get(f)
     for f in ("k_stream", "k_post"):
         kernels[f]["note"] = "timed alone (events between the kernels stop the second from launching early)"
     rooflines = {}
@@ -566,6 +605,7 @@ def run_reference(args, ws, rank):
     if rank != 0:
         return 0
     overrides = {"r": args.r, "budget": args.budget, "dense": args.dense}
+    layer_override = {"layers": args.layers} if args.layers else {}
     wl, _, desc = bench_workload(args.workload, **overrides)
     t0 = time.perf_counter()
     us, sample, calls_done, cores = oracle_baseline(args.workload, budget_s=30.0, threads=8, **overrides)
