@@ -299,7 +299,14 @@ __device__ __forceinline__ void store_bf16_raw<2>(__nv_bfloat16* dst, const __nv
 
 __device__ __forceinline__ int ceil_blocks(int L) { return (L + kBlock - 1) / kBlock; }
 
-__device__ __forceinline__ float ln_count(int n) { return n == kBlock ? 2.772588722239781f : logf((float)n); }
+// ln n for the token count n = 1..16 of a block (the log of |b|), as a table:
+// the values are the correctly rounded natural logarithms of the integers.
+static __constant__ float c_ln_count[kBlock + 1] = {
+    0.f,                 0.f,                 0.6931471805599453f, 1.0986122886681098f, 1.3862943611198906f,
+    1.6094379124341003f, 1.791759469228055f,  1.9459101090932196f, 2.0794415416798357f, 2.1972245773362196f,
+    2.302585092994046f,  2.3978952727983707f, 2.4849066497880004f, 2.5649493574615367f, 2.6390573296152584f,
+    2.70805020110221f,   2.772588722239781f};
+__device__ __forceinline__ float ln_count(int n) { return n == kBlock ? 2.772588722239781f : c_ln_count[n]; }
 
 // Tokens of sequence s in this call: the stored length, plus one when the
 // call appends and the sequence has room (`fits`).

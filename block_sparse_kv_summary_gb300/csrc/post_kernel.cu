@@ -225,114 +225,147 @@ __device__ __forceinline__ void blk_attend(float& m, float& l, float (&acc)[D / 
 }
 
 // ---------------------------------------------------------------- the phases
-// The open block (the one receiving this call's token), by one warp: its
-// summary from the exact bf16 values (two-pass fp32 mean and population
-// variance) and a_g = ln n + zbar_g + sigma2_g / 2, with
+// The code of this kernel runs once per call on every multiprocessor it
+// occupies, so its instruction footprint is on the critical path: loops over
+// runtime counts stay rolled, and every piece of work has one call site.
+
+// The open block (the one receiving this call's token), by one warp.  Lane l
+// holds the 8-coordinate chunk c = l % CH (CH = D / 8 chunks of a row) of the
+// tokens TPL (l / CH) .. TPL (l / CH) + TPL - 1 (TPL = D / 16), loaded as
+// 16-byte vectors; sums over the token groups are exchanged by xor shuffles.
+// Mean and population variance are two-pass in fp32 from the exact bf16
+// values; a_g = ln n + zbar_g + sigma2_g / 2 with
 // sigma2_g = (1/d) sum_i q_gi^2 Dbar_t(i) = sum_i qr_gi^2 Dbar_t(i), qr = q / sqrt(d).
-// The owner also stores the token and the block's kbar, vbar and Dbar rows.
+// The owner also stores the token -- and orders the store before the bulk
+// copies that read the block later in this call -- and the block's kbar,
+// vbar and Dbar rows.
 template <int D, int G>
 __device__ __forceinline__ void open_block(const LayerArgs& a, int s, int h, int L, int N, int64_t row0, bool owner,
                                            float* anm, int lane) {
-  constexpr int V = D / 32;
+  constexpr int CH = D / 8;
+  constexpr int TPL = D / 16;
   const int n = L - kBlock * (N - 1);
   const int64_t row = row0 + (N - 1);
-  const int c0 = V * lane;
-  const int64_t nw_off = ((int64_t)s * a.Hkv + h) * D + c0;
-  const __nv_bfloat16* kb = a.k + row * kBlock * D + c0;
-  const __nv_bfloat16* vb = a.v + row * kBlock * D + c0;
-  const float* qg = a.q + ((int64_t)s * a.Hkv + h) * G * D + c0;
-  float qr[G][V];
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int i = 0; i < V; ++i) qr[g][i] = qg[g * D + i] * InvSqrtP<D>::v;
-  if (owner) {
-    store_bf16_raw<V>(a.k + (row * kBlock + n - 1) * D + c0, a.k_new + nw_off);
-    store_bf16_raw<V>(a.v + (row * kBlock + n - 1) * D + c0, a.v_new + nw_off);
+  const int c = lane % CH, tg = lane / CH;
+  const int64_t nw = ((int64_t)s * a.Hkv + h) * D;
+  const uint4* knew = reinterpret_cast<const uint4*>(a.k_new + nw) + c;
+  const uint4* vnew = reinterpret_cast<const uint4*>(a.v_new + nw) + c;
+  uint4* kb = reinterpret_cast<uint4*>(a.k + row * kBlock * D) + c;
+  uint4* vb = reinterpret_cast<uint4*>(a.v + row * kBlock * D) + c;
+  const uint4 kn = *knew, vn = *vnew;
+  if (owner && tg == 0) {
+    kb[(n - 1) * CH] = kn;
+    vb[(n - 1) * CH] = vn;
+    fence_proxy_async_global();
   }
-  float ksum[V], vsum[V], kn[V];
-  load_bf16<V>(a.k_new + nw_off, kn);
+  const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+  uint4 kx[TPL], vx[TPL];
 #pragma unroll
-  for (int c = 0; c < V; ++c) ksum[c] = vsum[c] = 0.f;
-#pragma unroll
-  for (int j = 0; j < kBlock; ++j) {
-    if (j < n) {
-      float kf[V];
-      load_bf16<V>(j == n - 1 ? a.k_new + nw_off : kb + j * D, kf);
-#pragma unroll
-      for (int c = 0; c < V; ++c) ksum[c] += kf[c];
-      if (owner) {
-        float vf[V];
-        load_bf16<V>(j == n - 1 ? a.v_new + nw_off : vb + j * D, vf);
-#pragma unroll
-        for (int c = 0; c < V; ++c) vsum[c] += vf[c];
-      }
-    }
+  for (int i = 0; i < TPL; ++i) {
+    const int j = tg * TPL + i;
+    kx[i] = j < n - 1 ? __ldcg(kb + j * CH) : (j == n - 1 ? kn : z4);
+    vx[i] = !owner ? z4 : (j < n - 1 ? __ldcg(vb + j * CH) : (j == n - 1 ? vn : z4));
   }
-  float mk[V], var[V];
+  float ks[8], vs[8];
 #pragma unroll
-  for (int c = 0; c < V; ++c) {
-    mk[c] = ksum[c] / (float)n;
-    var[c] = 0.f;
-  }
+  for (int e = 0; e < 8; ++e) ks[e] = vs[e] = 0.f;
 #pragma unroll
-  for (int j = 0; j < kBlock; ++j) {
-    if (j < n) {
-      float kf[V];
-      if (j == n - 1) {
+  for (int i = 0; i < TPL; ++i) {
+    const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kx[i]);
+    const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&vx[i]);
 #pragma unroll
-        for (int c = 0; c < V; ++c) kf[c] = kn[c];
-      } else {
-        load_bf16<V>(kb + j * D, kf);
-      }
-#pragma unroll
-      for (int c = 0; c < V; ++c) {
-        const float dv = kf[c] - mk[c];
-        var[c] = fmaf(dv, dv, var[c]);
-      }
+    for (int e = 0; e < 4; ++e) {
+      const float2 kf = __bfloat1622float2(k2[e]), vf = __bfloat1622float2(v2[e]);
+      ks[2 * e] += kf.x;
+      ks[2 * e + 1] += kf.y;
+      vs[2 * e] += vf.x;
+      vs[2 * e + 1] += vf.y;
     }
   }
 #pragma unroll
-  for (int c = 0; c < V; ++c) {
-    var[c] /= (float)n;
-    if (owner) {
-      a.kbar[row * D + c0 + c] = mk[c];
-      a.vbar[row * D + c0 + c] = vsum[c] / (float)n;
+  for (int o = CH; o < 32; o <<= 1)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      ks[e] += __shfl_xor_sync(0xffffffffu, ks[e], o);
+      vs[e] += __shfl_xor_sync(0xffffffffu, vs[e], o);
+    }
+  const float inv = 1.f / (float)n;
+  float mk[8], var[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    mk[e] = ks[e] * inv;
+    var[e] = 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < TPL; ++i) {
+    if (tg * TPL + i < n) {
+      const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kx[i]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 kf = __bfloat1622float2(k2[e]);
+        const float d0 = kf.x - mk[2 * e], d1 = kf.y - mk[2 * e + 1];
+        var[2 * e] = fmaf(d0, d0, var[2 * e]);
+        var[2 * e + 1] = fmaf(d1, d1, var[2 * e + 1]);
+      }
     }
   }
-  // Dbar_t over coordinate group t = [t*D/r, (t+1)*D/r); every lane keeps the means of its
-  // own coordinates' groups
+#pragma unroll
+  for (int o = CH; o < 32; o <<= 1)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) var[e] += __shfl_xor_sync(0xffffffffu, var[e], o);
+  // Dbar_t over coordinate group t = [t*D/r, (t+1)*D/r); dm[e]: the mean of coordinate e's group
   const int r = a.r, gs = D / r;
-  float dm[V];
-  if (gs >= V) {
+  float dm[8];
+  if (gs >= 8) {
     float t = 0.f;
 #pragma unroll
-    for (int c = 0; c < V; ++c) t += var[c];
-    for (int o = 1; o < gs / V; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    const float mval = t / (float)gs;
+    for (int e = 0; e < 8; ++e) t += var[e] * inv;
+#pragma unroll 1
+    for (int o = 1; o < gs / 8; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    const float m = t / (float)gs;
 #pragma unroll
-    for (int c = 0; c < V; ++c) dm[c] = mval;
-    if (owner && (lane & (gs / V - 1)) == 0) a.dbar[row * r + c0 / gs] = mval;
+    for (int e = 0; e < 8; ++e) dm[e] = m;
+    if (owner && tg == 0 && (c & (gs / 8 - 1)) == 0) a.dbar[row * r + (8 * c) / gs] = m;
   } else {
-    float t = 0.f;
+    // gs = 1, 2 or 4: the groups of the chunk's 8 coordinates, by pairwise sums (gs is a power of two)
 #pragma unroll
-    for (int c = 0; c < V; ++c) {
-      t += var[c];
-      if ((c + 1) % gs == 0) {
-        const float mval = t / (float)gs;
-        for (int c2 = c + 1 - gs; c2 <= c; ++c2) dm[c2] = mval;
-        if (owner) a.dbar[row * r + (c0 + c) / gs] = mval;
-        t = 0.f;
-      }
+    for (int e = 0; e < 8; ++e) dm[e] = var[e] * inv;
+    if (gs >= 2) {
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) dm[e] = dm[e + 1] = 0.5f * (dm[e] + dm[e + 1]);
+    }
+    if (gs >= 4) {
+#pragma unroll
+      for (int e = 0; e < 8; e += 4) dm[e] = dm[e + 1] = dm[e + 2] = dm[e + 3] = 0.5f * (dm[e] + dm[e + 2]);
+    }
+    if (owner && tg == 0) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (e % gs == 0) a.dbar[row * r + (8 * c + e) / gs] = dm[e];
     }
   }
+  if (owner && tg == 0) {
+    float4* kr = reinterpret_cast<float4*>(a.kbar + row * D + 8 * c);
+    float4* vr = reinterpret_cast<float4*>(a.vbar + row * D + 8 * c);
+    kr[0] = make_float4(mk[0], mk[1], mk[2], mk[3]);
+    kr[1] = make_float4(mk[4], mk[5], mk[6], mk[7]);
+    vr[0] = make_float4(vs[0] * inv, vs[1] * inv, vs[2] * inv, vs[3] * inv);
+    vr[1] = make_float4(vs[4] * inv, vs[5] * inv, vs[6] * inv, vs[7] * inv);
+  }
+  const float* qg = a.q + ((int64_t)s * a.Hkv + h) * G * D + 8 * c;
 #pragma unroll
   for (int g = 0; g < G; ++g) {
+    const float4 q0 = *reinterpret_cast<const float4*>(qg + g * D);
+    const float4 q1 = *reinterpret_cast<const float4*>(qg + g * D + 4);
+    const float qr[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
     float z = 0.f, sg = 0.f;
+    if (tg == 0) {
 #pragma unroll
-    for (int c = 0; c < V; ++c) {
-      z = fmaf(qr[g][c], mk[c], z);
-      sg = fmaf(qr[g][c] * qr[g][c], dm[c], sg);
+      for (int e = 0; e < 8; ++e) {
+        const float x = qr[e] * InvSqrtP<D>::v;
+        z = fmaf(x, mk[e], z);
+        sg = fmaf(x * x, dm[e], sg);
+      }
     }
     z = warp_sum(z);
     sg = warp_sum(sg);
@@ -358,7 +391,7 @@ __device__ __forceinline__ void record_lse(const LayerArgs& a, int i0, int nseg,
 #pragma unroll
     for (int j = 0; j < 4; ++j) lse_merge(M, S, e[j].x, e[j].y);
   }
-#pragma unroll
+#pragma unroll 1
   for (int o = G; o < 32; o <<= 1) {
     const float M2 = __shfl_xor_sync(0xffffffffu, M, o), S2 = __shfl_xor_sync(0xffffffffu, S, o);
     lse_merge(M, S, M2, S2);
@@ -426,7 +459,7 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int* scratch, int* tota
   if (lane == 31) scratch[warp] = incl;
   __syncthreads();
   int base = 0, all = 0;
-#pragma unroll
+#pragma unroll 1
   for (int w = 0; w < kPW; ++w) {
     const int t = scratch[w];
     base += w < warp ? t : 0;
@@ -439,9 +472,10 @@ __device__ __forceinline__ int cta_exclusive_scan(int v, int* scratch, int* tota
 
 // Warp 0: the ascending list of the set bits of words[0..nw) (bit i = block
 // lo + i) into list[0..cap), returns the count (in warp 0).
-__device__ __forceinline__ int bitmap_list(const unsigned* words, int nw, int lo, int* list, int cap, int lane) {
+__device__ __noinline__ int bitmap_list(const unsigned* words, int nw, int lo, int* list, int cap, int lane) {
   const int per = (nw + 31) / 32;
   int loc = 0;
+#pragma unroll 1
   for (int k = 0; k < per; ++k) {
     const int w = per * lane + k;
     if (w < nw) loc += __popc(words[w]);
@@ -453,6 +487,7 @@ __device__ __forceinline__ int bitmap_list(const unsigned* words, int nw, int lo
     if (lane >= o) incl += y;
   }
   int run = incl - loc;
+#pragma unroll 1
   for (int k = 0; k < per; ++k) {
     const int w = per * lane + k;
     if (w < nw) {
@@ -480,12 +515,15 @@ __device__ __noinline__ void refine_select(const uint32_t* keys, unsigned* bits,
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t pfx = T << kDigitShift, pm = 0xFFFFFFFFu << kDigitShift;
   bool done = false;
+#pragma unroll 1
   for (int level = 1; level <= 3 && !done; ++level) {
     const int shift = level == 1 ? 11 : (level == 2 ? 3 : 0);
     const int nb = level == 3 ? 8 : 256;
     const uint32_t dm = (uint32_t)nb - 1u;
+#pragma unroll 1
     for (int i = tid; i < 256; i += kPT) lh[i] = 0u;
     __syncthreads();
+#pragma unroll 1
     for (int i = tid; i < nown; i += kPT) {
       const int b = b_lo + i;
       if (b < 1 || b > N - 3) continue;
@@ -494,6 +532,7 @@ __device__ __noinline__ void refine_select(const uint32_t* keys, unsigned* bits,
     }
     __syncthreads();
     uint32_t* xr = xref + (level - 1) * 256;
+#pragma unroll 1
     for (int i = tid; i < nb; i += kPT)
       if (lh[i]) red_peer_add(peer_smem(xr + i, 0), lh[i]);
     cluster_sync_all();
@@ -511,6 +550,7 @@ __device__ __noinline__ void refine_select(const uint32_t* keys, unsigned* bits,
     const uint32_t Dg = (uint32_t)misc[kMT];
     const int above = misc[kMAbove], cnt = misc[kMCntT];
     const bool all = cnt == need - above;
+#pragma unroll 1
     for (int i = tid; i < nown; i += kPT) {
       const int b = b_lo + i;
       if (b < 1 || b > N - 3) continue;
@@ -528,6 +568,7 @@ __device__ __noinline__ void refine_select(const uint32_t* keys, unsigned* bits,
   if (!done) {
     // keys equal in every bit: the `need` lowest block indices of the cluster
     int c = 0;
+#pragma unroll 1
     for (int i = tid; i < nown; i += kPT) {
       const int b = b_lo + i;
       if (b < 1 || b > N - 3) continue;
@@ -538,20 +579,20 @@ __device__ __noinline__ void refine_select(const uint32_t* keys, unsigned* bits,
     if (tid < C) st_peer_u32(peer_smem(misc + kMCntR + p, (uint32_t)tid), (uint32_t)tot);
     cluster_sync_all();
     int before = 0;
+#pragma unroll 1
     for (int q = 0; q < p; ++q) before += misc[kMCntR + q];
     int take = need - before;
     take = take < 0 ? 0 : (take > tot ? tot : take);
-    if (warp == 0 && take > 0) {
-      // the first `take` in-play blocks in index order: one lane scans
-      if (lane == 0) {
-        int got = 0;
-        for (int i = 0; i < nown && got < take; ++i) {
-          const int b = b_lo + i;
-          if (b < 1 || b > N - 3) continue;
-          if ((keys[i] & pm) == pfx && !((bits[i >> 5] >> (i & 31)) & 1u)) {
-            bits[i >> 5] |= 1u << (i & 31);
-            ++got;
-          }
+    if (tid == 0 && take > 0) {
+      // the first `take` in-play blocks in index order: one thread scans
+      int got = 0;
+#pragma unroll 1
+      for (int i = 0; i < nown && got < take; ++i) {
+        const int b = b_lo + i;
+        if (b < 1 || b > N - 3) continue;
+        if ((keys[i] & pm) == pfx && !((bits[i >> 5] >> (i & 31)) & 1u)) {
+          bits[i >> 5] |= 1u << (i & 31);
+          ++got;
         }
       }
     }
@@ -565,7 +606,6 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   constexpr bool SEL = (MODE & kFSelect) != 0;
   constexpr bool ATT = (MODE & kFAttend) != 0;
   constexpr int KS = D / 16;
-  constexpr int RB = stg_row(D);
   extern __shared__ __align__(16) float psm[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int C = a.C;
@@ -595,24 +635,30 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   float* anm = psm + lay.anm;
   float* lsep = psm + lay.lsep;
   float* csh = psm + lay.csh;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(psm + lay.bars);  // [kPW] attention, [kPW] zbar/sigma2 copy
+  uint64_t* bars = reinterpret_cast<uint64_t*>(psm + lay.bars);  // [kPW] attention, [1] zbar/sigma2 copy
   const unsigned long long t_start = a.trace ? global_ns() : 0ull;
-  unsigned long long pmk[14] = {0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull, 0ull};
+  // phase marks of the work-item trace: mark k goes to record 1 + k / 7, slot 1 + k % 7
   auto mark = [&](int k) {
-    if (a.trace) pmk[k] = global_ns();
+    if (a.trace && tid == 0) {
+      const int64_t rec = a.P + (int64_t)(1 + k / 7) * gridDim.x + blockIdx.x;
+      if (rec < a.trace_cap) a.trace[1 + 8 * rec + 1 + k % 7] = global_ns();
+    }
   };
 
   // ---- set-up before the stream's results are visible
   if (tid <= kPW) mbar_init(bars + tid, 1);
   if (tid == 0) fence_mbar_init();
-  if (SEL) {
-    for (int i = tid; i < lay.lh + 256 - lay.hf; i += kPT) hf[i] = 0u;  // hf, xexp, xfine, xref, lh
+  if (SEL) {  // hf, xexp, xfine, xref, lh
+    uint4* z = reinterpret_cast<uint4*>(hf);
+#pragma unroll 1
+    for (int i = tid; i < (lay.lh + 256 - lay.hf) / 4; i += kPT) z[i] = make_uint4(0u, 0u, 0u, 0u);
   }
   if (tid < 192) misc[tid] = 0;
   // q as the A operand of S^T = q K^T, split into bf16 high and low parts: lane (r, c) of
   // k-step ks holds head r (zero beyond G) at coordinates 16 ks + 2c, +1 and 16 ks + 8 + 2c, +1
   uint4* qf = reinterpret_cast<uint4*>(psm + lay.qf);
   if (ATT) {
+#pragma unroll 1
     for (int x = tid; x < KS * 32; x += kPT) {
       const int ks = x >> 5, r = (x & 31) >> 2, c = x & 3;
       float2 x0 = make_float2(0.f, 0.f), x1 = make_float2(0.f, 0.f);
@@ -703,8 +749,10 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
     for (int g = 0; g < G; ++g) {
       float M = lsep[2 * g], S = lsep[2 * g + 1];
       if (app) lse_merge(M, S, anm[g], 1.f);
-      lse[g] = M + logf(S);
+      lse[g] = M + __logf(S);
     }
+    const bool fom = (a.variant & kVarFirstOrderMass) != 0, nvf = (a.variant & kVarNoVarianceFactor) != 0;
+#pragma unroll 1
     for (int i = c_lo; i < c_hi; ++i) {
       const int b = b_lo + i;
       float S = 0.f;
@@ -713,9 +761,8 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           const float z = zsl[i * Gp + g], s2 = ssl[i * Gp + g];
-          const float av = lnn + z + ((a.variant & kVarFirstOrderMass) ? 0.f : 0.5f * s2);
-          const float ph = __expf(av - lse[g]);
-          S = fmaf(ph, (a.variant & kVarNoVarianceFactor) ? 1.f : s2, S);
+          const float ph = __expf(lnn + z + (fom ? 0.f : 0.5f * s2) - lse[g]);
+          S = fmaf(ph, nvf ? 1.f : s2, S);
         }
       }
       S = fmaxf(S, 0.f);
@@ -738,20 +785,18 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
       // thread e: exponent e's count to rank 0, its 16 fine bins to rank e % C
       const int e = tid;  // kPT == 256 exponents
       const uint4* hv = reinterpret_cast<const uint4*>(hf + e * 16);
-      const uint4 f0 = hv[0], f1 = hv[1], f2 = hv[2], f3 = hv[3];
-      const uint32_t ce = f0.x + f0.y + f0.z + f0.w + f1.x + f1.y + f1.z + f1.w + f2.x + f2.y + f2.z + f2.w + f3.x +
-                          f3.y + f3.z + f3.w;
+      uint32_t ce = 0;
+#pragma unroll 1
+      for (int k = 0; k < 4; ++k) {
+        const uint4 f = hv[k];
+        ce += f.x + f.y + f.z + f.w;
+      }
       if (ce) {
         red_peer_add(peer_smem(xexp + e, 0), ce);
         const uint32_t fo = peer_smem(xfine + (e / C) * 16, (uint32_t)(e % C));
-        const uint4 fv[4] = {f0, f1, f2, f3};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          if (fv[k].x) red_peer_add(fo + 16u * k, fv[k].x);
-          if (fv[k].y) red_peer_add(fo + 16u * k + 4u, fv[k].y);
-          if (fv[k].z) red_peer_add(fo + 16u * k + 8u, fv[k].z);
-          if (fv[k].w) red_peer_add(fo + 16u * k + 12u, fv[k].w);
-        }
+#pragma unroll 1
+        for (int k = 0; k < 16; ++k)
+          if (hf[e * 16 + k]) red_peer_add(fo + 4u * k, hf[e * 16 + k]);
       }
     }
     cluster_sync_all();  // barrier 1: rank 0 holds the exponent histogram, rank e % C the fine bins of e
@@ -762,9 +807,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
       const uint32_t ea = peer_smem(xexp + 248 - 8 * lane, 0);
       const uint4 lo4 = ld_peer_u4(ea), hi4 = ld_peer_u4(ea + 16u);
       const uint32_t cb[8] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};
-      int c8 = 0;
-#pragma unroll
-      for (int k = 0; k < 8; ++k) c8 += (int)cb[k];
+      const int c8 = (int)(lo4.x + lo4.y + lo4.z + lo4.w + hi4.x + hi4.y + hi4.z + hi4.w);
       int incl = c8;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -821,6 +864,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
       return bin > T || (bin == T && take_all);
     };
     int cnt_t = 0;
+#pragma unroll 1
     for (int i = c_lo; i < c_hi; ++i) {
       if (sure(i)) {
         ++cnt_t;
@@ -829,28 +873,16 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
         if (slot < kTieCap) win[slot] = i;  // local indices of this CTA's tie candidates
       }
     }
-    int incl = cnt_t;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    if (lane == 31) misc[kMWT + warp] = incl;
-    __syncthreads();
-    int pos = incl - cnt_t;
-#pragma unroll
-    for (int w = 0; w < kPW; ++w) {
-      const int t = misc[kMWT + w];
-      pos += w < warp ? t : 0;
-      n_own += t;
-    }
+    int tot;
+    int pos = cta_exclusive_scan(cnt_t, misc + kMWT, &tot, lane, warp);
     const int cap = nown < K ? nown : K;
+#pragma unroll 1
     for (int i = c_lo; i < c_hi; ++i)
       if (sure(i)) {
         if (pos < cap) own[pos] = b_lo + i;
         ++pos;
       }
-    n_own = n_own < cap ? n_own : cap;
+    n_own = tot < cap ? tot : cap;
     __syncthreads();  // the own list and the tie count are complete
     ntie = misc[kMNtie];
   }
@@ -859,6 +891,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
     // push (own count, tie count) and the tie entries (key, block) to every CTA of the cluster
     if (tid < C) st_peer_u2(peer_smem(cnt + 2 * p, (uint32_t)tid), make_uint2((uint32_t)n_own, (uint32_t)ntie));
     const int nt = ntie < kTieCap ? ntie : kTieCap;
+#pragma unroll 1
     for (int e = tid; e < nt * C; e += kPT) {
       const int q = e / nt, k = e % nt;
       const int i = win[k];
@@ -866,18 +899,15 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
     }
     if (ATT) {
       // blocks that are attended after the exchange: own blocks beyond the top kPW, tie candidates
-      for (int e = tid; e < n_own - kPW; e += kPT) {
-        const int64_t row = row0 + own[e];
-        prefetch_l2(a.k + row * kBlock * D, kBlock * D * 2);
-        prefetch_l2(a.v + row * kBlock * D, kBlock * D * 2);
-      }
-      for (int e = tid; e < nt; e += kPT) {
-        const int64_t row = row0 + b_lo + win[e];
+      const int ovf = max(0, n_own - kPW);
+#pragma unroll 1
+      for (int e = tid; e < ovf + nt; e += kPT) {
+        const int64_t row = row0 + (e < ovf ? own[e] : b_lo + win[e - ovf]);
         prefetch_l2(a.k + row * kBlock * D, kBlock * D * 2);
         prefetch_l2(a.v + row * kBlock * D, kBlock * D * 2);
       }
     }
-    cluster_arrive();  // barrier 2 (waited for after this CTA's first blocks of attention)
+    cluster_arrive();  // barrier 2 (waited for once this CTA's first copies are in flight)
   }
 
   // ---- d, e. attention: this warp's running state
@@ -887,14 +917,15 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   for (int mt = 0; mt < KS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
   uint32_t ph = 0u;
   char* stg = reinterpret_cast<char*>(psm + lay.stg) + warp * stg_bytes(D);
+  const int* selrow_in = a.sel + (int64_t)u * K;
   int tot_sel = 0;
   if (ATT && !SEL) {
     // the caller's selection: entries that are not ascending or not inside [0, N) are skipped and reported
-    const int* selrow = a.sel + (int64_t)u * K;
     int bad = 0, cntv = 0;
+#pragma unroll 1
     for (int i = tid; i < K; i += kPT) {
-      const int e = __ldcg(selrow + i);
-      const int prev = i > 0 ? __ldcg(selrow + i - 1) : -1;
+      const int e = __ldcg(selrow_in + i);
+      const int prev = i > 0 ? __ldcg(selrow_in + i - 1) : -1;
       const bool ok = e >= 0 && e < N && (i == 0 || (prev >= 0 && prev < e));
       cntv += ok;
       bad |= (e >= 0 && !ok) || e < -1;
@@ -910,95 +941,59 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
     if ((misc[kMBad] & 2) && p == 0 && tid == 0) set_error(a.status, kDevBadSelection, s, h, 61);
   }
   const bool comp_blk = comp && (SEL || tot_sel < N);
+  auto n_of = [&](int b) { return (b == N - 1) ? L - kBlock * b : kBlock; };
+  // compensation of block b comes off unless this call appended it (the stream skipped it then)
+  auto comp_of = [&](int b) { return comp_blk && !(APPEND && app && b == N - 1); };
   // stage block b into this warp's buffer (rows n..15 zero); returns zbar of head lane / 4
   auto issue = [&](int b) -> float {
     const int64_t row = row0 + b;
-    const int n = (b == N - 1) ? L - kBlock * b : kBlock;
-    const bool fresh = APPEND && app && b == N - 1;
-    const bool cb = comp_blk && !fresh;
+    const int n = n_of(b);
+    const bool cb = comp_of(b);
+    const int t = lane & (kBlock - 1);
     __syncwarp();  // the buffer's previous contents are read
-    if (fresh) {
-      // written in this call by this CTA's last warp (ordinary stores, ordered by the CTA barriers)
-      for (int x = lane; x < 2 * kBlock * (D / 8); x += 32) {
-        const int t = x / (D / 8), w = x % (D / 8);
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if ((t & (kBlock - 1)) < n)
-          v = __ldcg(reinterpret_cast<const uint4*>((t < kBlock ? a.k : a.v) + (row * kBlock + (t & (kBlock - 1))) * D) + w);
-        *reinterpret_cast<uint4*>(stg + t * RB + 16 * w) = v;
-      }
-    } else {
-      const int t = lane & (kBlock - 1);
-      if (t >= n) {
-        uint4* z = reinterpret_cast<uint4*>(stg + lane * RB);
-#pragma unroll
-        for (int w = 0; w < D / 8; ++w) z[w] = make_uint4(0u, 0u, 0u, 0u);
-      }
-      // the buffer may hold rows this warp wrote with ordinary stores: order them before the copies
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      if (lane == 0) mbar_arrive_expect_tx(bars + warp, 2u * (uint32_t)n * D * 2u + (cb ? D * 4u : 0u));
-      __syncwarp();
-      const uint64_t pol = policy_evict_first();
-      if (t < n) bulk_g2s_hint(stg + lane * RB, (lane < kBlock ? a.k : a.v) + (row * kBlock + t) * D, D * 2u, bars + warp, pol);
-      if (cb && lane == 0) bulk_g2s_hint(stg + 2 * kBlock * RB, a.vbar + row * D, D * 4u, bars + warp, pol);
+    if (t >= n) {
+      uint4* z = reinterpret_cast<uint4*>(stg + lane * stg_row(D));
+#pragma unroll 4
+      for (int w = 0; w < D / 8; ++w) z[w] = make_uint4(0u, 0u, 0u, 0u);
     }
+    // the buffer may hold rows this warp wrote with ordinary stores: order them before the copies
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (lane == 0) mbar_arrive_expect_tx(bars + warp, 2u * (uint32_t)n * D * 2u + (cb ? D * 4u : 0u));
+    __syncwarp();
+    const uint64_t pol = policy_evict_first();
+    if (t < n)
+      bulk_g2s_hint(stg + lane * stg_row(D), (lane < kBlock ? a.k : a.v) + (row * kBlock + t) * D, D * 2u, bars + warp,
+                    pol);
+    if (cb && lane == 0) bulk_g2s_hint(stg + 2 * kBlock * stg_row(D), a.vbar + row * D, D * 4u, bars + warp, pol);
     return (cb && (lane >> 2) < G) ? __ldcg(a.zs + row * Gp + (lane >> 2)) : 0.f;
   };
-  auto attend = [&](int b, float zb) {
-    const int n = (b == N - 1) ? L - kBlock * b : kBlock;
-    const bool fresh = APPEND && app && b == N - 1;
-    if (fresh) {
-      __syncwarp();
-    } else {
-      if (!mbar_wait_bounded(bars + warp, ph, a.status, s, h, 62)) {
-        mbar_drain_bounded(bars + warp);
-        misc[kMBad] |= 1;
-        return;
-      }
-      ph ^= 1u;
-    }
-    blk_attend<D, G>(am, al, acc, qf, stg, n, comp_blk && !fresh, zb, lane);
-  };
 
+  // this CTA's own sure blocks from the top of its list (the open block, the last, comes first):
+  // their copies start before the exchange settles
+  const int mine0 = min(n_own, kPW);
+  int b_cur = -1;
+  float zb_cur = 0.f;
   if (ATT && SEL) {
-    // this CTA's own sure blocks from the top of its list (the open block, the last, comes first)
-    const int b0 = warp < n_own ? own[n_own - 1 - warp] : -1;
-    if (xchg) misc[kMR0 + warp] = b0;
-    float zb0 = 0.f;
-    if (b0 >= 0) zb0 = issue(b0);
-    if (comp) comp_share<D, G>(a, i0, nseg, p, C, csh, cR, cW, tid);
-    if (b0 >= 0) attend(b0, zb0);
-    if (all_sel) {
-      for (int k = n_own - 1 - warp - kPW; k >= 0 && !(misc[kMBad] & 1); k -= kPW) {
-        const int b = own[k];
-        const float zb = issue(b);
-        attend(b, zb);
-      }
-    }
-  } else if (ATT) {
-    if (comp) comp_share<D, G>(a, i0, nseg, p, C, csh, cR, cW, tid);
-    const int* selrow = a.sel + (int64_t)u * K;
-    for (int rnd = 0;; ++rnd) {
-      const int j = (rnd * C + p) * kPW + warp;
-      if (j >= K || (misc[kMBad] & 1)) break;
-      const int e = __ldcg(selrow + j);
-      const int prev = j > 0 ? __ldcg(selrow + j - 1) : -1;
-      if (!(e >= 0 && e < N && (j == 0 || (prev >= 0 && prev < e)))) continue;  // warp-uniform
-      const float zb = issue(e);
-      attend(e, zb);
-    }
+    b_cur = warp < n_own ? own[n_own - 1 - warp] : -1;
+    if (xchg) misc[kMR0 + warp] = b_cur;
+    if (b_cur >= 0) zb_cur = issue(b_cur);
   }
+  if (comp) comp_share<D, G>(a, i0, nseg, p, C, csh, cR, cW, tid);
   mark(5);
 
   // ---- d. after the exchange: the tie winners and the rest of the work
   int own_base = b_lo;  // this CTA's offset in the ascending selection
   int nwin = 0;
+  bool rare = false;
+  int OV = 0, SP = 0, spx_p = 0, total = 0, ov = 0, ovx = 0;  // work items of the common path
   if (xchg) {
     cluster_wait();  // barrier 2: every count and tie list is here
     mark(6);
     // every warp alike: lane q < C holds CTA q's counts
     const uint2 cq = lane < C ? *reinterpret_cast<const uint2*>(cnt + 2 * lane) : make_uint2(0u, 0u);
     const int co = (int)cq.x, ct = (int)cq.y;
-    const int ov = max(0, co - kPW), sp = lane < C ? kPW - min(co, kPW) : 0;
+    ov = max(0, co - kPW);
+    const int sp = lane < C ? kPW - min(co, kPW) : 0;
     int io = co, it = ct, iv = ov, is = sp, mx = ct;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -1013,25 +1008,29 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
       mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
     }
     const int sum_own = __shfl_sync(0xffffffffu, io, 31), nt_all = __shfl_sync(0xffffffffu, it, 31);
-    const int OV = __shfl_sync(0xffffffffu, iv, 31), SP = __shfl_sync(0xffffffffu, is, 31);
-    const int ovx = iv - ov;                                 // lane q: first overflow item of CTA q
-    const int spx_p = __shfl_sync(0xffffffffu, is - sp, p);  // first idle slot of this CTA
+    OV = __shfl_sync(0xffffffffu, iv, 31);
+    SP = __shfl_sync(0xffffffffu, is, 31);
+    ovx = iv - ov;                                   // lane q: first overflow item of CTA q
+    spx_p = __shfl_sync(0xffffffffu, is - sp, p);    // first idle slot of this CTA
     const int opre_p = __shfl_sync(0xffffffffu, io - co, p);
-    const bool rare = !take_all && need > 0 && (mx > kTieCap || nt_all > kRankMax);
+    rare = !take_all && need > 0 && (mx > kTieCap || nt_all > kRankMax);
     if (!rare) {
       if (!take_all && need > 0) {
         // rank every tie entry among all (key desc, block asc), one warp per entry over a
         // dense copy of the lists; the first `need` win, kept in rank order
         if (warp == 0 && lane < C) misc[kMTpre + lane] = it - ct;
         __syncthreads();
+#pragma unroll 1
         for (int e = tid; e < C * kTieCap; e += kPT) {
           const int q = e / kTieCap, k = e % kTieCap;
           if (k < cnt[2 * q + 1]) dense[misc[kMTpre + q] + k] = tie[e];
         }
         __syncthreads();
+#pragma unroll 1
         for (int j = warp; j < nt_all; j += kPW) {
           const uint2 me = dense[j];
           int rank = 0;
+#pragma unroll 1
           for (int j2 = lane; j2 < nt_all; j2 += 32) {
             const uint2 o = dense[j2];
             rank += (o.x > me.x) || (o.x == me.x && o.y < me.y);
@@ -1044,43 +1043,21 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
       }
       mark(7);
       tot_sel = sum_own + nwin;
+      total = OV + nwin;
       // this CTA's offset in the ascending selection: the lists of the lower ranks and the
       // tie winners below this CTA's blocks
       int below = 0;
+#pragma unroll 1
       for (int k = lane; k < nwin; k += 32) below += win[k] < b_lo;
       own_base = opre_p + __reduce_add_sync(0xffffffffu, below);
-      if (ATT) {
-        // items: the own lists beyond their top kPW (CTA by CTA), then the winners; slots: the warps
-        // idle before the exchange (CTA by CTA), then every warp round by round
-        const int total = OV + nwin;
-        const int mine0 = min(n_own, kPW);
-        for (int rnd = 0;; ++rnd) {
-          int k;
-          if (rnd == 0) {
-            if (warp < mine0) continue;
-            k = spx_p + warp - mine0;
-          } else {
-            k = SP + ((rnd - 1) * C + p) * kPW + warp;
-          }
-          if (k >= total || (misc[kMBad] & 1)) break;
-          int b;
-          if (k < OV) {
-            const unsigned bal = __ballot_sync(0xffffffffu, lane < C && ov > 0 && ovx <= k);
-            const int q = 31 - __clz(bal);
-            b = (int)ld_peer_u32(peer_smem(own + (k - __shfl_sync(0xffffffffu, ovx, q)), (uint32_t)q));
-          } else {
-            b = win[k - OV];
-          }
-          const float zb = issue(b);
-          attend(b, zb);
-        }
-      }
     } else {
       // rare: resolve bin T by more radix digits; every CTA attends its own winners itself
       unsigned* bits = reinterpret_cast<unsigned*>(dense);
       const int nwo = (nown + 31) / 32;
+#pragma unroll 1
       for (int w = tid; w < nwo; w += kPT) bits[w] = 0u;
       __syncthreads();
+#pragma unroll 1
       for (int e = tid; e < n_own; e += kPT) atomicOr(&bits[(own[e] - b_lo) >> 5], 1u << ((own[e] - b_lo) & 31));
       __syncthreads();
       refine_select(keys, bits, nown, b_lo, N, T, need, xref, lh, misc, C, p);
@@ -1093,6 +1070,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
       if (tid < C) st_peer_u32(peer_smem(misc + kMCntA + p, (uint32_t)tid), (uint32_t)n_own);
       cluster_sync_all();
       int before = 0, all = 0;
+#pragma unroll 1
       for (int q = 0; q < C; ++q) {
         before += q < p ? misc[kMCntA + q] : 0;
         all += misc[kMCntA + q];
@@ -1100,45 +1078,97 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
       own_base = before;
       tot_sel = all;
       mark(7);
-      if (ATT) {
-        for (int k = warp; k < n_own && !(misc[kMBad] & 1); k += kPW) {
-          const int b = own[k];
-          bool done0 = false;
-#pragma unroll
-          for (int w = 0; w < kPW; ++w) done0 |= misc[kMR0 + w] == b;
-          if (done0) continue;
-          const float zb = issue(b);
-          attend(b, zb);
-        }
-      }
     }
   } else if (SEL) {
     tot_sel = N;
     own_base = b_lo;
   }
   mark(8);
+
+  // the next block of this warp's work, round `rd` (-1: none left, -2: skip this round)
+  auto next_block = [&](int rd) -> int {
+    if (!SEL) {  // the caller's selection, spread over the cluster's warps round by round
+      const int j = (rd * C + p) * kPW + warp;
+      if (j >= K) return -1;
+      const int e = __ldcg(selrow_in + j);
+      const int prev = j > 0 ? __ldcg(selrow_in + j - 1) : -1;
+      return (e >= 0 && e < N && (j == 0 || (prev >= 0 && prev < e))) ? e : -2;
+    }
+    if (all_sel) {  // every block: this CTA's own list from the top, kPW per round
+      const int k = n_own - 1 - warp - kPW * rd;
+      return k >= 0 ? own[k] : -1;
+    }
+    if (rare) {  // this CTA's final list, minus the blocks started before the exchange
+      const int k = warp + kPW * rd;
+      if (k >= n_own) return -1;
+      const int b = own[k];
+#pragma unroll 1
+      for (int w = 0; w < kPW; ++w)
+        if (misc[kMR0 + w] == b) return -2;
+      return b;
+    }
+    // items: the own lists beyond their top kPW (CTA by CTA), then the tie winners; slots:
+    // the warps idle before the exchange (CTA by CTA), then every warp round by round
+    const int k = rd == 0 ? spx_p + warp - mine0 : SP + ((rd - 1) * C + p) * kPW + warp;
+    if (k >= total) return -1;
+    if (k < OV) {
+      const unsigned bal = __ballot_sync(0xffffffffu, lane < C && ov > 0 && ovx <= k);
+      const int q = 31 - __clz(bal);
+      return (int)ld_peer_u32(peer_smem(own + (k - __shfl_sync(0xffffffffu, ovx, q)), (uint32_t)q));
+    }
+    return win[k - OV];
+  };
+  if (ATT) {
+    // one loop and one attention site: the block whose copy is in flight, then the next
+    int rd = (SEL && !rare && warp < mine0) ? 1 : 0;
+    for (;;) {
+      if (b_cur >= 0) {
+        if (!mbar_wait_bounded(bars + warp, ph, a.status, s, h, 62)) {
+          mbar_drain_bounded(bars + warp);
+          misc[kMBad] |= 1;
+          break;
+        }
+        ph ^= 1u;
+        blk_attend<D, G>(am, al, acc, qf, stg, n_of(b_cur), comp_of(b_cur), zb_cur, lane);
+      }
+      if (misc[kMBad] & 1) break;
+      int nb = -2;
+#pragma unroll 1
+      while (nb == -2) nb = next_block(rd++);
+      if (nb < 0) break;
+      b_cur = nb;
+      zb_cur = issue(nb);
+    }
+  }
+  mark(9);
   if (SEL) {
     // the ascending selection: this CTA's blocks and the tie winners among them, merged
     int* selrow = a.sel + (int64_t)u * K;
+#pragma unroll 1
     for (int e = tid; e < n_own; e += kPT) {
       const int b = own[e];
       int pos = own_base + e;
+#pragma unroll 1
       for (int k = 0; k < nwin; ++k) pos += (win[k] >= b_lo && win[k] < b);
       if (pos < K) selrow[pos] = b;
     }
+#pragma unroll 1
     for (int k = tid; k < nwin; k += kPT) {
       const int b = win[k];
       if (b < b_lo || b >= b_hi) continue;
       int lo = 0, hi = n_own;  // own blocks below b (the list is ascending)
+#pragma unroll 1
       while (lo < hi) {
         const int mid = (lo + hi) >> 1;
         if (own[mid] < b) lo = mid + 1; else hi = mid;
       }
       int pos = own_base + lo;
+#pragma unroll 1
       for (int k2 = 0; k2 < nwin; ++k2) pos += (win[k2] >= b_lo && win[k2] < b);
       if (pos < K) selrow[pos] = b;
     }
     if (p == 0) {
+#pragma unroll 1
       for (int i = tot_sel + tid; i < K; i += kPT) selrow[i] = -1;
       if (tid == 0 && tot_sel != (N < K ? N : K)) set_error(a.status, kDevInternal, s, h, 50);
     }
@@ -1154,7 +1184,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
     }
     return;
   }
-  const unsigned long long t_att = a.trace ? global_ns() : 0ull;
+  const unsigned long long t_att = t_sel;
 
   // ---- the CTA's partial: its warps and its compensation share
   __syncthreads();  // the staging is free: the partials reuse the union
@@ -1181,11 +1211,12 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
     }
   }
   __syncthreads();
-  mark(9);
+  mark(10);
   // per float4 column item: the warps' parts (and the share) at their common maximum, pushed to
   // the rank that merges the item
   const int items = G * D / 4;
   const int ipr = post_ipr(D, G, C);
+#pragma unroll 1
   for (int i4 = tid; i4 < items; i4 += kPT) {
     const int g = (4 * i4) / D, col = (4 * i4) % D;
     float M = comp_blk ? cR[g] : -INFINITY;
@@ -1194,7 +1225,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
     float4 as = make_float4(0.f, 0.f, 0.f, 0.f);
     float Ls = 0.f;
     if (M != -INFINITY) {
-#pragma unroll
+#pragma unroll 1
       for (int w = 0; w < kPW; ++w) {
         const float mw = red_m[w * 8 + g];
         const float f = mw == -INFINITY ? 0.f : __expf(mw - M);
@@ -1220,14 +1251,15 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
     st_peer_f4(dst, as);
     st_peer_u2(dst + 16u, make_uint2(__float_as_uint(M), __float_as_uint(Ls)));
   }
-  mark(10);
-  cluster_sync_all();  // barrier 3: every partial of this rank's columns is here; no CTA touches a peer after this
   mark(11);
+  cluster_sync_all();  // barrier 3: every partial of this rank's columns is here; no CTA touches a peer after this
+  mark(12);
   if (APPEND && p == 0 && tid == 0) {
     // every CTA of this cluster has read seq_len; the last cluster to get here
     // writes the lengths after this call's append (a sequence at capacity keeps its own)
     __threadfence();
     if (atomicAdd(a.arrive, 1) == (int)(gridDim.x / C) - 1) {
+#pragma unroll 1
       for (int x = 0; x < a.B; ++x) {
         const bool f = ((x < 32 ? misc[kMFits] >> x : misc[kMFits + 1] >> (x - 32)) & 1) != 0;
         if (f) a.seq_len[x] = sL[x];
@@ -1243,6 +1275,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
     int Cp = 1;
     while (Cp < C) Cp <<= 1;
     const int nx = max(0, i_hi - i_lo) * Cp;  // groups of Cp lanes never straddle a warp (Cp divides 32)
+#pragma unroll 1
     for (int x0 = warp * 32; x0 < nx; x0 += kPT) {
       const int x = x0 + lane;
       const bool live = x < nx;
@@ -1257,6 +1290,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
         lq = e[5];
       }
       float M = mq;
+#pragma unroll 1
       for (int o = 1; o < Cp; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
       const float f = (M == -INFINITY || mq == -INFINITY) ? 0.f : __expf(mq - M);
       as.x *= f;
@@ -1264,6 +1298,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
       as.z *= f;
       as.w *= f;
       lq *= f;
+#pragma unroll 1
       for (int o = 1; o < Cp; o <<= 1) {
         as.x += __shfl_xor_sync(0xffffffffu, as.x, o);
         as.y += __shfl_xor_sync(0xffffffffu, as.y, o);
@@ -1278,24 +1313,25 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
       }
     }
   }
-  mark(12);
-  if (tid == 0 && a.trace && a.P + 3 * (int)gridDim.x < a.trace_cap) {
+  mark(13);
+  if (tid == 0 && a.trace) {
     for (int rec = 0; rec < 2; ++rec) {
-      unsigned long long* rr = a.trace + 1 + 8 * (int64_t)(a.P + (1 + rec) * gridDim.x + blockIdx.x);
-      rr[0] = ((unsigned long long)blockIdx.x << 32) | ((2ull + rec) << 24) | (unsigned)(ntie | (n_own << 12));
-      for (int k = 0; k < 7; ++k) rr[1 + k] = pmk[7 * rec + k];
+      const int64_t ri = a.P + (int64_t)(1 + rec) * gridDim.x + blockIdx.x;
+      if (ri < a.trace_cap)
+        a.trace[1 + 8 * ri] = ((unsigned long long)blockIdx.x << 32) | ((2ull + rec) << 24) |
+                              (unsigned)(ntie | (n_own << 12));
     }
-  }
-  if (tid == 0 && a.trace && a.P + (int)blockIdx.x < a.trace_cap) {
-    unsigned long long* rr = a.trace + 1 + 8 * (int64_t)(a.P + blockIdx.x);
-    rr[0] = ((unsigned long long)blockIdx.x << 32) | (1ull << 24) | (unsigned)p;
-    rr[1] = (unsigned long long)u;
-    rr[2] = t_start;
-    rr[3] = t_wait;
-    rr[4] = t_sel;
-    rr[5] = t_att;
-    rr[6] = global_ns();
-    rr[7] = (unsigned long long)tot_sel;
+    if (a.P + (int)blockIdx.x < a.trace_cap) {
+      unsigned long long* rr = a.trace + 1 + 8 * (int64_t)(a.P + blockIdx.x);
+      rr[0] = ((unsigned long long)blockIdx.x << 32) | (1ull << 24) | (unsigned)p;
+      rr[1] = (unsigned long long)u;
+      rr[2] = t_start;
+      rr[3] = t_wait;
+      rr[4] = t_sel;
+      rr[5] = t_att;
+      rr[6] = global_ns();
+      rr[7] = (unsigned long long)tot_sel;
+    }
   }
 }
 
