@@ -36,7 +36,8 @@ struct Layout {
   int64_t rows_per_layer = 0;
   int max_cap_blocks = 0;
   int K = 0, C = 0, bpc_max = 0, units = 0, rec_cap = 0;
-  size_t off_status = 0, off_arrive = 0, off_rec = 0, off_comp = 0, off_zs = 0, off_ss = 0, off_sel = 0, off_hq = 0,
+  size_t off_status = 0, off_arrive = 0, off_rec = 0, off_comp = 0, off_zs = 0, off_ss = 0, off_anm = 0, off_sel = 0,
+         off_hq = 0,
          off_hk = 0, off_hv = 0, off_hout = 0, total = 0;
 };
 
@@ -108,6 +109,7 @@ compkv_status make_layout(const compkv_config* c, Layout* L) {
   region(&L->off_comp, (size_t)L->rec_cap * G * d * sizeof(float));
   region(&L->off_zs, (size_t)row * Gp * sizeof(float));
   region(&L->off_ss, (size_t)row * Gp * sizeof(float));
+  region(&L->off_anm, (size_t)L->units * G * sizeof(float));
   region(&L->off_sel, (size_t)L->units * L->K * sizeof(int));
   // staging of compkv_decode_host: q, k_new, v_new and out of one call
   region(&L->off_hq, (size_t)L->units * G * d * sizeof(float));
@@ -214,6 +216,7 @@ LayerArgs base_args(const compkv_ctx* c, int layer) {
   a.comp = reinterpret_cast<float*>(sc + c->lay.off_comp);
   a.zs = reinterpret_cast<float*>(sc + c->lay.off_zs);
   a.ss = reinterpret_cast<float*>(sc + c->lay.off_ss);
+  a.anm = reinterpret_cast<float*>(sc + c->lay.off_anm);
   a.sel = reinterpret_cast<int*>(sc + c->lay.off_sel);
   a.trace = c->trace;
   a.trace_cap = c->trace_cap;

@@ -53,7 +53,9 @@ struct LayerArgs {
   // shape
   int B, Hkv, G, d, r, K;
   int variant;                // Variant bits
-  int P;                      // CTAs of the stream kernel (its grid)
+  int P;                      // streaming CTAs of the stream kernel (the work plan's CTA count)
+  int Q;                      // leading CTAs of the stream kernel's grid that recompute the open blocks
+                              // (grid = Q + P; Q = 0 when the call appends nothing)
   int C;                      // CTAs per unit in the post kernel (one cluster)
   int bpc_max;                // post kernel: blocks of one CTA at most (its shared arrays)
   int rec_cap;                // segment records the scratch holds
@@ -64,6 +66,7 @@ struct LayerArgs {
   float* comp;                // [rec_cap][G][d]: compensation numerator relative to its reference
   float* zs;                  // [rows][Gp]: zbar per block and head (Gp = max(G, 4))
   float* ss;                  // [rows][Gp]: sigma2 per block and head
+  float* anm;                 // [units][G]: a_g of each unit's open block (this call's token joins it)
   // optional trace of the work items (null: off)
   unsigned long long* trace;
   int trace_cap;

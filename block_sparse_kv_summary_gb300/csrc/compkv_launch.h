@@ -31,6 +31,18 @@ cudaError_t launch_wait_selftest(int* status, cudaStream_t st);
 // cluster of a.C CTAs per (sequence, KV head) for the selection, attention
 // and compensation.  `mode` is kFusedDecode, kFusedScoreSelect or
 // kFusedAttend.
+// A call that appends gives the first Q CTAs of the stream kernel's grid the
+// open blocks (one warp per unit, at most 8 CTAs) and leaves P - Q CTAs to the
+// summary stream; both launches of a chain apply the same split.
+inline void chain_split(LayerArgs& a, int mode) {
+  a.Q = 0;
+  if (mode & kFAppend) {
+    int q = (a.B * a.Hkv + 7) / 8;
+    if (q > 8) q = 8;
+    a.Q = q;
+    a.P = a.P > q ? a.P - q : 1;
+  }
+}
 cudaError_t launch_stream(const LayerArgs& a, int mode, cudaStream_t st, bool pdl);
 cudaError_t launch_post(const LayerArgs& a, int mode, cudaStream_t st);
 

@@ -229,150 +229,6 @@ __device__ __forceinline__ void blk_attend(float& m, float& l, float (&acc)[D / 
 // occupies, so its instruction footprint is on the critical path: loops over
 // runtime counts stay rolled, and every piece of work has one call site.
 
-// The open block (the one receiving this call's token), by one warp.  Lane l
-// holds the 8-coordinate chunk c = l % CH (CH = D / 8 chunks of a row) of the
-// tokens TPL (l / CH) .. TPL (l / CH) + TPL - 1 (TPL = D / 16), loaded as
-// 16-byte vectors; sums over the token groups are exchanged by xor shuffles.
-// Mean and population variance are two-pass in fp32 from the exact bf16
-// values; a_g = ln n + zbar_g + sigma2_g / 2 with
-// sigma2_g = (1/d) sum_i q_gi^2 Dbar_t(i) = sum_i qr_gi^2 Dbar_t(i), qr = q / sqrt(d).
-// The owner also stores the token -- and orders the store before the bulk
-// copies that read the block later in this call -- and the block's kbar,
-// vbar and Dbar rows.
-template <int D, int G>
-__device__ __forceinline__ void open_block(const LayerArgs& a, int s, int h, int L, int N, int64_t row0, bool owner,
-                                           float* anm, int lane) {
-  constexpr int CH = D / 8;
-  constexpr int TPL = D / 16;
-  const int n = L - kBlock * (N - 1);
-  const int64_t row = row0 + (N - 1);
-  const int c = lane % CH, tg = lane / CH;
-  const int64_t nw = ((int64_t)s * a.Hkv + h) * D;
-  const uint4* knew = reinterpret_cast<const uint4*>(a.k_new + nw) + c;
-  const uint4* vnew = reinterpret_cast<const uint4*>(a.v_new + nw) + c;
-  uint4* kb = reinterpret_cast<uint4*>(a.k + row * kBlock * D) + c;
-  uint4* vb = reinterpret_cast<uint4*>(a.v + row * kBlock * D) + c;
-  const uint4 kn = *knew, vn = *vnew;
-  if (owner && tg == 0) {
-    kb[(n - 1) * CH] = kn;
-    vb[(n - 1) * CH] = vn;
-    fence_proxy_async_global();
-  }
-  const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
-  uint4 kx[TPL], vx[TPL];
-#pragma unroll
-  for (int i = 0; i < TPL; ++i) {
-    const int j = tg * TPL + i;
-    kx[i] = j < n - 1 ? __ldcg(kb + j * CH) : (j == n - 1 ? kn : z4);
-    vx[i] = !owner ? z4 : (j < n - 1 ? __ldcg(vb + j * CH) : (j == n - 1 ? vn : z4));
-  }
-  float ks[8], vs[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) ks[e] = vs[e] = 0.f;
-#pragma unroll
-  for (int i = 0; i < TPL; ++i) {
-    const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kx[i]);
-    const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&vx[i]);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 kf = __bfloat1622float2(k2[e]), vf = __bfloat1622float2(v2[e]);
-      ks[2 * e] += kf.x;
-      ks[2 * e + 1] += kf.y;
-      vs[2 * e] += vf.x;
-      vs[2 * e + 1] += vf.y;
-    }
-  }
-#pragma unroll
-  for (int o = CH; o < 32; o <<= 1)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      ks[e] += __shfl_xor_sync(0xffffffffu, ks[e], o);
-      vs[e] += __shfl_xor_sync(0xffffffffu, vs[e], o);
-    }
-  const float inv = 1.f / (float)n;
-  float mk[8], var[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    mk[e] = ks[e] * inv;
-    var[e] = 0.f;
-  }
-#pragma unroll
-  for (int i = 0; i < TPL; ++i) {
-    if (tg * TPL + i < n) {
-      const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kx[i]);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float2 kf = __bfloat1622float2(k2[e]);
-        const float d0 = kf.x - mk[2 * e], d1 = kf.y - mk[2 * e + 1];
-        var[2 * e] = fmaf(d0, d0, var[2 * e]);
-        var[2 * e + 1] = fmaf(d1, d1, var[2 * e + 1]);
-      }
-    }
-  }
-#pragma unroll
-  for (int o = CH; o < 32; o <<= 1)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) var[e] += __shfl_xor_sync(0xffffffffu, var[e], o);
-  // Dbar_t over coordinate group t = [t*D/r, (t+1)*D/r); dm[e]: the mean of coordinate e's group
-  const int r = a.r, gs = D / r;
-  float dm[8];
-  if (gs >= 8) {
-    float t = 0.f;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) t += var[e] * inv;
-#pragma unroll 1
-    for (int o = 1; o < gs / 8; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    const float m = t / (float)gs;
-#pragma unroll
-    for (int e = 0; e < 8; ++e) dm[e] = m;
-    if (owner && tg == 0 && (c & (gs / 8 - 1)) == 0) a.dbar[row * r + (8 * c) / gs] = m;
-  } else {
-    // gs = 1, 2 or 4: the groups of the chunk's 8 coordinates, by pairwise sums (gs is a power of two)
-#pragma unroll
-    for (int e = 0; e < 8; ++e) dm[e] = var[e] * inv;
-    if (gs >= 2) {
-#pragma unroll
-      for (int e = 0; e < 8; e += 2) dm[e] = dm[e + 1] = 0.5f * (dm[e] + dm[e + 1]);
-    }
-    if (gs >= 4) {
-#pragma unroll
-      for (int e = 0; e < 8; e += 4) dm[e] = dm[e + 1] = dm[e + 2] = dm[e + 3] = 0.5f * (dm[e] + dm[e + 2]);
-    }
-    if (owner && tg == 0) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        if (e % gs == 0) a.dbar[row * r + (8 * c + e) / gs] = dm[e];
-    }
-  }
-  if (owner && tg == 0) {
-    float4* kr = reinterpret_cast<float4*>(a.kbar + row * D + 8 * c);
-    float4* vr = reinterpret_cast<float4*>(a.vbar + row * D + 8 * c);
-    kr[0] = make_float4(mk[0], mk[1], mk[2], mk[3]);
-    kr[1] = make_float4(mk[4], mk[5], mk[6], mk[7]);
-    vr[0] = make_float4(vs[0] * inv, vs[1] * inv, vs[2] * inv, vs[3] * inv);
-    vr[1] = make_float4(vs[4] * inv, vs[5] * inv, vs[6] * inv, vs[7] * inv);
-  }
-  const float* qg = a.q + ((int64_t)s * a.Hkv + h) * G * D + 8 * c;
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const float4 q0 = *reinterpret_cast<const float4*>(qg + g * D);
-    const float4 q1 = *reinterpret_cast<const float4*>(qg + g * D + 4);
-    const float qr[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-    float z = 0.f, sg = 0.f;
-    if (tg == 0) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float x = qr[e] * InvSqrtP<D>::v;
-        z = fmaf(x, mk[e], z);
-        sg = fmaf(x * x, dm[e], sg);
-      }
-    }
-    z = warp_sum(z);
-    sg = warp_sum(sg);
-    if (lane == 0) anm[g] = ln_count(n) + z + ((a.variant & kVarFirstOrderMass) ? 0.f : 0.5f * sg);
-  }
-}
-
 // (max, sum) of the logsumexp of a_g over the unit's nseg segment records, by one warp: lane j
 // merges records of head j % G; lanes of one head then merge across the warp.
 template <int G>
@@ -407,10 +263,10 @@ __device__ __forceinline__ void record_lse(const LayerArgs& a, int i0, int nseg,
 // load of an item issued before any is used.
 template <int D, int G>
 __device__ __forceinline__ void comp_share(const LayerArgs& a, int i0, int nseg, int p, int C, float* csh, float* cR,
-                                           float* cW, int tid) {
+                                           float* cW, int t, int nt) {
   const int nk = p < nseg ? (nseg - 1 - p) / C + 1 : 0;
 #pragma unroll 1
-  for (int i4 = tid; i4 < G * D / 4; i4 += kPT) {
+  for (int i4 = t; i4 < G * D / 4; i4 += nt) {
     const int g = i4 / (D / 4), col = 4 * (i4 % (D / 4));
     float R = -INFINITY, Wsum = 0.f;
     float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -637,15 +493,36 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   float* csh = psm + lay.csh;
   uint64_t* bars = reinterpret_cast<uint64_t*>(psm + lay.bars);  // [kPW] attention, [1] zbar/sigma2 copy
   const unsigned long long t_start = a.trace ? global_ns() : 0ull;
+  unsigned long long t_wait = 0ull;
   // phase marks of the work-item trace: mark k goes to record 1 + k / 7, slot 1 + k % 7
-  auto mark = [&](int k) {
-    if (a.trace && tid == 0) {
-      const int64_t rec = a.P + (int64_t)(1 + k / 7) * gridDim.x + blockIdx.x;
-      if (rec < a.trace_cap) a.trace[1 + 8 * rec + 1 + k % 7] = global_ns();
-    }
+  // (kept in shared memory until the end, so that no global store waits in a fence)
+  __shared__ unsigned long long tmk[28];
+  if (a.trace && tid < 28) tmk[tid] = 0ull;
+  auto markt = [&](int k, int t) {
+    if (a.trace && tid == t) tmk[k] = global_ns();
   };
+  auto mark = [&](int k) { markt(k, 0); };
 
-  // ---- set-up before the stream's results are visible
+  // ---- set-up before the stream's results are visible; its global loads are issued together here
+  const int Lold_s = __ldcg(a.seq_len + s);
+  int sl0 = 0, sl1 = 0;
+  if (warp == 0) {
+    if (lane < a.B) sl0 = __ldcg(a.seq_len + lane);
+    if (lane + 32 < a.B) sl1 = __ldcg(a.seq_len + lane + 32);
+  }
+  const float* qunit = a.q + ((int64_t)s * a.Hkv + h) * G * D;
+  const int qr_ = (tid & 31) >> 2, qc_ = tid & 3, qks_ = tid >> 5;
+  float2 qx0 = make_float2(0.f, 0.f), qx1 = make_float2(0.f, 0.f);
+  if (ATT && tid < KS * 32 && qr_ < G) {
+    qx0 = *reinterpret_cast<const float2*>(qunit + qr_ * D + 16 * qks_ + 2 * qc_);
+    qx1 = *reinterpret_cast<const float2*>(qunit + qr_ * D + 16 * qks_ + 8 + 2 * qc_);
+  }
+  bool fits_s = false;
+  const int L = call_tokens(Lold_s, a.cap_blocks[s], APPEND, &fits_s);
+  const bool app = APPEND && fits_s;
+  const int N = ceil_blocks(L);
+  const int bpc = (((N + C - 1) / C) + 3) & ~3;
+  const int64_t row0 = row_of(a, s, h, 0);
   if (tid <= kPW) mbar_init(bars + tid, 1);
   if (tid == 0) fence_mbar_init();
   if (SEL) {  // hf, xexp, xfine, xref, lh
@@ -657,23 +534,14 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   // q as the A operand of S^T = q K^T, split into bf16 high and low parts: lane (r, c) of
   // k-step ks holds head r (zero beyond G) at coordinates 16 ks + 2c, +1 and 16 ks + 8 + 2c, +1
   uint4* qf = reinterpret_cast<uint4*>(psm + lay.qf);
-  if (ATT) {
-#pragma unroll 1
-    for (int x = tid; x < KS * 32; x += kPT) {
-      const int ks = x >> 5, r = (x & 31) >> 2, c = x & 3;
-      float2 x0 = make_float2(0.f, 0.f), x1 = make_float2(0.f, 0.f);
-      if (r < G) {
-        const float* qg = a.q + (((int64_t)s * a.Hkv + h) * G + r) * D + 16 * ks + 2 * c;
-        x0 = *reinterpret_cast<const float2*>(qg);
-        x1 = *reinterpret_cast<const float2*>(qg + 8);
-      }
-      uint4 v;
-      split_bf16(x0.x * InvSqrtP<D>::v, x0.y * InvSqrtP<D>::v, v.x, v.z);
-      split_bf16(x1.x * InvSqrtP<D>::v, x1.y * InvSqrtP<D>::v, v.y, v.w);
-      qf[x] = v;
-    }
+  if (ATT && tid < KS * 32) {  // fragment x = tid (loaded above)
+    uint4 v;
+    split_bf16(qx0.x * InvSqrtP<D>::v, qx0.y * InvSqrtP<D>::v, v.x, v.z);
+    split_bf16(qx1.x * InvSqrtP<D>::v, qx1.y * InvSqrtP<D>::v, v.y, v.w);
+    qf[tid] = v;
   }
   __syncthreads();  // misc is zero before warp 0 fills in the plan
+  markt(25, 0);
   // the plan, as the stream kernel makes it, from the lengths before this call
   // (no kernel of this call writes seq_len before every post CTA has read it)
   int* sL = reinterpret_cast<int*>(psm + lay.plan);  // [kMaxBatch] tokens of each sequence in this call
@@ -682,11 +550,11 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   if (warp == 0) {
     bool f0 = false, f1 = false;
     if (lane < a.B) {
-      sL[lane] = call_tokens(__ldcg(a.seq_len + lane), a.cap_blocks[lane], APPEND, &f0);
+      sL[lane] = call_tokens(sl0, a.cap_blocks[lane], APPEND, &f0);
       sN[lane] = streamed_blocks(sL[lane], APPEND && f0, SEL, a.K, a.scores != nullptr);
     }
     if (lane + 32 < a.B) {
-      sL[lane + 32] = call_tokens(__ldcg(a.seq_len + lane + 32), a.cap_blocks[lane + 32], APPEND, &f1);
+      sL[lane + 32] = call_tokens(sl1, a.cap_blocks[lane + 32], APPEND, &f1);
       sN[lane + 32] = streamed_blocks(sL[lane + 32], APPEND && f1, SEL, a.K, a.scores != nullptr);
     }
     const unsigned m0 = __ballot_sync(0xffffffffu, f0), m1 = __ballot_sync(0xffffffffu, f1);
@@ -698,32 +566,35 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
     plan_warp(sN, a.B, a.Hkv, a.P, stage_blocks(a.r, G), soff, misc + kMPlan, lane);
   }
   __syncthreads();
+  markt(26, 0);
   const int seg = misc[kMPlan];
-  const int L = sL[s], N = ceil_blocks(L), Ns = sN[s];
-  const bool app = APPEND && (((s < 32 ? misc[kMFits] >> s : misc[kMFits + 1] >> (s - 32)) & 1) != 0);
+  const int Ns = sN[s];
   const int nseg = (Ns + seg - 1) / seg;
   const int i0 = soff[s] + h * nseg;                 // the unit's first segment record
-  const int bpc = (((N + C - 1) / C) + 3) & ~3;
   const int b_lo = min(N, p * bpc), b_hi = min(N, b_lo + bpc);
   const int nown = b_hi - b_lo;
   const int nown_z = max(0, min(b_hi, Ns) - b_lo);   // of them with zbar / sigma2 from the stream
-  const int64_t row0 = row_of(a, s, h, 0);
   const bool all_sel = N <= K;
   const int need0 = K - 3;
   const bool want_keys = SEL && (!all_sel || a.scores);
   const bool hist = SEL && !all_sel && need0 > 0;    // the threshold search runs
   const bool xchg = SEL && !all_sel;                 // the counts are exchanged
   const bool comp = ATT && !(a.variant & kVarNoCompensation) && (!SEL || !all_sel);
-  const int own_open = app ? (N - 1) / bpc : -1;     // the CTA that appends the new token
   cluster_arrive();  // this CTA's exchange areas are zero (every peer waits for this before its first push)
+  markt(27, 0);
 
-  // ---- a. the open block (last warp); LSE over the records (warp 0); zbar, sigma2 rows (warp 1)
-  if (warp == kPW - 1) {
-    if (APPEND && app) open_block<D, G>(a, s, h, L, N, row0, p == own_open, anm, lane);
-    pdl_wait();
-  } else {
+  // ---- a. after the stream: LSE over the records and the open block's a_g (warp 0), zbar and
+  // sigma2 rows (warp 1), the compensation share (warps 2..)
+  {
     pdl_wait();  // the stream kernel's records, zbar and sigma2 are complete and visible
-    if (warp == 0 && want_keys) record_lse<G>(a, i0, nseg, lsep, lane);
+    if (a.trace && tid == 0) t_wait = global_ns();
+    if (warp == 0 && want_keys) {
+      if (app && lane < G) anm[lane] = __ldcg(a.anm + (int64_t)u * G + lane);
+      record_lse<G>(a, i0, nseg, lsep, lane);
+    }
+    markt(22, 0);
+    // the CTA's share of the compensation sums, by the warps idle until the keys
+    if (comp && warp >= 2) comp_share<D, G>(a, i0, nseg, p, C, csh, cR, cW, tid - 64, kPT - 64);
     if (warp == 1 && lane == 0 && want_keys && nown_z > 0) {
       const uint32_t bytes = (uint32_t)nown_z * (uint32_t)Gp * 4u;
       mbar_arrive_expect_tx(bars + kPW, 2u * bytes);
@@ -734,9 +605,10 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
         misc[kMBad] = 1;
       }
     }
+    markt(23, 32);
+    markt(24, 64);
   }
   pdl_trigger();  // the next call's kernels may launch (they wait for this grid before reading)
-  const unsigned long long t_wait = a.trace ? global_ns() : 0ull;
   __syncthreads();  // LSE parts, a_g of the open block, zsl and ssl in place
   mark(0);
 
@@ -799,6 +671,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
           if (hf[e * 16 + k]) red_peer_add(fo + 4u * k, hf[e * 16 + k]);
       }
     }
+    mark(14);
     cluster_sync_all();  // barrier 1: rank 0 holds the exponent histogram, rank e % C the fine bins of e
     mark(2);
     if (warp == 0) {
@@ -874,7 +747,9 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
       }
     }
     int tot;
+    mark(19);
     int pos = cta_exclusive_scan(cnt_t, misc + kMWT, &tot, lane, warp);
+    mark(20);
     const int cap = nown < K ? nown : K;
 #pragma unroll 1
     for (int i = c_lo; i < c_hi; ++i)
@@ -897,6 +772,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
       const int i = win[k];
       st_peer_u2(peer_smem(tie + p * kTieCap + k, (uint32_t)q), make_uint2(keys[i], (uint32_t)(b_lo + i)));
     }
+    mark(15);
     if (ATT) {
       // blocks that are attended after the exchange: own blocks beyond the top kPW, tie candidates
       const int ovf = max(0, n_own - kPW);
@@ -907,7 +783,9 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
         prefetch_l2(a.v + row * kBlock * D, kBlock * D * 2);
       }
     }
+    mark(16);
     cluster_arrive();  // barrier 2 (waited for once this CTA's first copies are in flight)
+    mark(17);
   }
 
   // ---- d, e. attention: this warp's running state
@@ -977,8 +855,8 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
     b_cur = warp < n_own ? own[n_own - 1 - warp] : -1;
     if (xchg) misc[kMR0 + warp] = b_cur;
     if (b_cur >= 0) zb_cur = issue(b_cur);
+    mark(18);
   }
-  if (comp) comp_share<D, G>(a, i0, nseg, p, C, csh, cR, cW, tid);
   mark(5);
 
   // ---- d. after the exchange: the tie winners and the rest of the work
@@ -1177,8 +1055,8 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   if (SEL && !ATT) {
     // score/select only: no peer reads this CTA's shared memory after the barrier
     cluster_sync_all();
-    if (tid == 0 && a.trace && a.P + (int)blockIdx.x < a.trace_cap) {
-      unsigned long long* rr = a.trace + 1 + 8 * (int64_t)(a.P + blockIdx.x);
+    if (tid == 0 && a.trace && a.Q + a.P + (int)blockIdx.x < a.trace_cap) {
+      unsigned long long* rr = a.trace + 1 + 8 * (int64_t)(a.Q + a.P + blockIdx.x);
       rr[0] = ((unsigned long long)blockIdx.x << 32) | (1ull << 24) | (unsigned)p;
       rr[1] = (unsigned long long)u; rr[2] = t_start; rr[3] = t_wait; rr[4] = t_sel; rr[5] = t_sel;
     }
@@ -1315,14 +1193,16 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   }
   mark(13);
   if (tid == 0 && a.trace) {
-    for (int rec = 0; rec < 2; ++rec) {
-      const int64_t ri = a.P + (int64_t)(1 + rec) * gridDim.x + blockIdx.x;
-      if (ri < a.trace_cap)
+    for (int rec = 0; rec < 4; ++rec) {
+      const int64_t ri = a.Q + a.P + (int64_t)(1 + rec) * gridDim.x + blockIdx.x;
+      if (ri < a.trace_cap) {
         a.trace[1 + 8 * ri] = ((unsigned long long)blockIdx.x << 32) | ((2ull + rec) << 24) |
                               (unsigned)(ntie | (n_own << 12));
+        for (int k = 0; k < 7; ++k) a.trace[1 + 8 * ri + 1 + k] = tmk[7 * rec + k];
+      }
     }
-    if (a.P + (int)blockIdx.x < a.trace_cap) {
-      unsigned long long* rr = a.trace + 1 + 8 * (int64_t)(a.P + blockIdx.x);
+    if (a.Q + a.P + (int)blockIdx.x < a.trace_cap) {
+      unsigned long long* rr = a.trace + 1 + 8 * (int64_t)(a.Q + a.P + blockIdx.x);
       rr[0] = ((unsigned long long)blockIdx.x << 32) | (1ull << 24) | (unsigned)p;
       rr[1] = (unsigned long long)u;
       rr[2] = t_start;
@@ -1343,6 +1223,7 @@ static cudaError_t launch_post_mode(const LayerArgs& a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (a.C > 8 && (e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess) return e;
   LayerArgs args = a;
+  chain_split(args, MODE);
   void* argv[] = {&args};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(a.B * a.Hkv * a.C));

@@ -100,6 +100,160 @@ __device__ __forceinline__ void lds_vec<2>(const float* p, float (&x)[2]) {
   x[0] = v.x; x[1] = v.y;
 }
 
+// The open block of unit u (the block this call's token joins), by one warp.  Lane l
+// holds the 8-coordinate chunk c = l % CH (CH = D / 8 chunks of a row) of the
+// tokens TPL (l / CH) .. TPL (l / CH) + TPL - 1 (TPL = D / 16), loaded as
+// 16-byte vectors; sums over the token groups are exchanged by xor shuffles.
+// Mean and population variance are two-pass in fp32 from the exact bf16
+// values; a_g = ln n + zbar_g + sigma2_g / 2 with
+// sigma2_g = (1/d) sum_i q_gi^2 Dbar_t(i) = sum_i qr_gi^2 Dbar_t(i), qr = q / sqrt(d).
+// The warp also stores the token and the block's kbar, vbar and Dbar rows,
+// and writes a_g to the scratch for the post kernel.  A sequence at capacity
+// keeps its cache and is reported (status word, site 1).
+template <int D, int G>
+__device__ __noinline__ void open_block_warp(const LayerArgs& a, int u, int lane) {
+  const int s = u / a.Hkv, h = u % a.Hkv;
+  bool fits = false;
+  const int L = call_tokens(__ldcg(a.seq_len + s), a.cap_blocks[s], true, &fits);
+  if (!fits) {
+    if (h == 0 && lane == 0) set_error(a.status, kDevCapacity, s, -1, 1);
+    return;
+  }
+  const int N = ceil_blocks(L);
+  const int64_t row0 = row_of(a, s, h, 0);
+  const bool owner = true;
+  float* anm = a.anm + (int64_t)u * G;
+
+  constexpr int CH = D / 8;
+  constexpr int TPL = D / 16;
+  const int n = L - kBlock * (N - 1);
+  const int64_t row = row0 + (N - 1);
+  const int c = lane % CH, tg = lane / CH;
+  const int64_t nw = ((int64_t)s * a.Hkv + h) * D;
+  const uint4* knew = reinterpret_cast<const uint4*>(a.k_new + nw) + c;
+  const uint4* vnew = reinterpret_cast<const uint4*>(a.v_new + nw) + c;
+  uint4* kb = reinterpret_cast<uint4*>(a.k + row * kBlock * D) + c;
+  uint4* vb = reinterpret_cast<uint4*>(a.v + row * kBlock * D) + c;
+  const uint4 kn = *knew, vn = *vnew;
+  if (owner && tg == 0) {
+    kb[(n - 1) * CH] = kn;
+    vb[(n - 1) * CH] = vn;
+  }
+  const uint4 z4 = make_uint4(0u, 0u, 0u, 0u);
+  uint4 kx[TPL], vx[TPL];
+#pragma unroll
+  for (int i = 0; i < TPL; ++i) {
+    const int j = tg * TPL + i;
+    kx[i] = j < n - 1 ? __ldcg(kb + j * CH) : (j == n - 1 ? kn : z4);
+    vx[i] = !owner ? z4 : (j < n - 1 ? __ldcg(vb + j * CH) : (j == n - 1 ? vn : z4));
+  }
+  float ks[8], vs[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) ks[e] = vs[e] = 0.f;
+#pragma unroll
+  for (int i = 0; i < TPL; ++i) {
+    const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kx[i]);
+    const __nv_bfloat162* v2 = reinterpret_cast<const __nv_bfloat162*>(&vx[i]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 kf = __bfloat1622float2(k2[e]), vf = __bfloat1622float2(v2[e]);
+      ks[2 * e] += kf.x;
+      ks[2 * e + 1] += kf.y;
+      vs[2 * e] += vf.x;
+      vs[2 * e + 1] += vf.y;
+    }
+  }
+#pragma unroll
+  for (int o = CH; o < 32; o <<= 1)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      ks[e] += __shfl_xor_sync(0xffffffffu, ks[e], o);
+      vs[e] += __shfl_xor_sync(0xffffffffu, vs[e], o);
+    }
+  const float inv = 1.f / (float)n;
+  float mk[8], var[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    mk[e] = ks[e] * inv;
+    var[e] = 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < TPL; ++i) {
+    if (tg * TPL + i < n) {
+      const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kx[i]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 kf = __bfloat1622float2(k2[e]);
+        const float d0 = kf.x - mk[2 * e], d1 = kf.y - mk[2 * e + 1];
+        var[2 * e] = fmaf(d0, d0, var[2 * e]);
+        var[2 * e + 1] = fmaf(d1, d1, var[2 * e + 1]);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = CH; o < 32; o <<= 1)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) var[e] += __shfl_xor_sync(0xffffffffu, var[e], o);
+  // Dbar_t over coordinate group t = [t*D/r, (t+1)*D/r); dm[e]: the mean of coordinate e's group
+  const int r = a.r, gs = D / r;
+  float dm[8];
+  if (gs >= 8) {
+    float t = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) t += var[e] * inv;
+#pragma unroll 1
+    for (int o = 1; o < gs / 8; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    const float m = t / (float)gs;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) dm[e] = m;
+    if (owner && tg == 0 && (c & (gs / 8 - 1)) == 0) a.dbar[row * r + (8 * c) / gs] = m;
+  } else {
+    // gs = 1, 2 or 4: the groups of the chunk's 8 coordinates, by pairwise sums (gs is a power of two)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) dm[e] = var[e] * inv;
+    if (gs >= 2) {
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) dm[e] = dm[e + 1] = 0.5f * (dm[e] + dm[e + 1]);
+    }
+    if (gs >= 4) {
+#pragma unroll
+      for (int e = 0; e < 8; e += 4) dm[e] = dm[e + 1] = dm[e + 2] = dm[e + 3] = 0.5f * (dm[e] + dm[e + 2]);
+    }
+    if (owner && tg == 0) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (e % gs == 0) a.dbar[row * r + (8 * c + e) / gs] = dm[e];
+    }
+  }
+  if (owner && tg == 0) {
+    float4* kr = reinterpret_cast<float4*>(a.kbar + row * D + 8 * c);
+    float4* vr = reinterpret_cast<float4*>(a.vbar + row * D + 8 * c);
+    kr[0] = make_float4(mk[0], mk[1], mk[2], mk[3]);
+    kr[1] = make_float4(mk[4], mk[5], mk[6], mk[7]);
+    vr[0] = make_float4(vs[0] * inv, vs[1] * inv, vs[2] * inv, vs[3] * inv);
+    vr[1] = make_float4(vs[4] * inv, vs[5] * inv, vs[6] * inv, vs[7] * inv);
+  }
+  const float* qg = a.q + ((int64_t)s * a.Hkv + h) * G * D + 8 * c;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    const float4 q0 = *reinterpret_cast<const float4*>(qg + g * D);
+    const float4 q1 = *reinterpret_cast<const float4*>(qg + g * D + 4);
+    const float qr[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+    float z = 0.f, sg = 0.f;
+    if (tg == 0) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float x = qr[e] * InvSqrt<D>::v;
+        z = fmaf(x, mk[e], z);
+        sg = fmaf(x * x, dm[e], sg);
+      }
+    }
+    z = warp_sum(z);
+    sg = warp_sum(sg);
+    if (lane == 0) anm[g] = ln_count(n) + z + ((a.variant & kVarFirstOrderMass) ? 0.f : 0.5f * sg);
+  }
+}
+
 template <int D, int G, int MODE, int SB, bool RB>
 __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
   constexpr bool APPEND = (MODE & kFAppend) != 0;
@@ -134,6 +288,27 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
   // the previous work on the stream may have written this cache and its lengths
   pdl_wait();
   pdl_trigger();
+  if ((int)blockIdx.x < a.Q) {
+    // the open blocks: warp w of CTA c takes the units c * kWarps + w + Q * kWarps * k
+    if (APPEND) {
+      const int units = a.B * a.Hkv;
+#pragma unroll 1
+      for (int u = blockIdx.x * kWarps + warp; u < units; u += a.Q * kWarps) open_block_warp<D, G>(a, u, lane);
+    }
+    if (threadIdx.x == 0 && a.trace && (int)blockIdx.x < a.trace_cap) {
+      unsigned long long* rr = a.trace + 1 + 8 * (int64_t)blockIdx.x;
+      rr[0] = ((unsigned long long)blockIdx.x << 32);
+      rr[1] = 0ull;
+      rr[2] = t_start;
+      rr[3] = t_start;
+      rr[4] = t_start;
+      rr[5] = global_ns();
+      rr[6] = 0ull;
+      rr[7] = 0ull;
+    }
+    return;
+  }
+  const int cta = (int)blockIdx.x - a.Q;  // this CTA among the P that stream
   if (warp == 0) {
     const int s0 = lane, s1 = lane + 32;
     bool f0 = false, f1 = false;
@@ -147,10 +322,6 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
     }
     __syncwarp();
     plan_warp(sN, a.B, a.Hkv, a.P, SB, soff, sseg, lane);
-    if (APPEND && blockIdx.x == 0) {
-      if (s0 < a.B && !f0) set_error(a.status, kDevCapacity, s0, -1, 1);
-      if (s1 < a.B && !f1) set_error(a.status, kDevCapacity, s1, -1, 1);
-    }
   }
   __syncthreads();
   const int seg = *sseg, total = soff[a.B];
@@ -164,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
   const int vv = lane >> SH, vb = vv / G, vg = vv % G;
   const bool primary = (lane & ((1 << SH) - 1)) == 0;
 
-  for (int si = blockIdx.x; si < total; si += gridDim.x) {
+  for (int si = cta; si < total; si += a.P) {
     int s, h, b0, nb;
     plan_segment(si, a.B, a.Hkv, sN, soff, seg, &s, &h, &b0, &nb);
     const int L = sL[s], N = ceil_blocks(L);  // N: all blocks (the last may be partial)
@@ -487,9 +658,10 @@ static cudaError_t launch_stream_mode(const LayerArgs& a, cudaStream_t st, bool 
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   LayerArgs args = a;
+  chain_split(args, MODE);
   void* argv[] = {&args};
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)a.P);
+  cfg.gridDim = dim3((unsigned)(args.Q + args.P));
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
