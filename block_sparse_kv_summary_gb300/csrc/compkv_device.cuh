@@ -273,19 +273,21 @@ __device__ __forceinline__ void lse_merge(float& m, float& l, float m2, float l2
   m = mn;
 }
 
-// bf16 x N -> float x N (N = 2 or 4), from an 8- or 4-byte aligned address.
+// bf16 x N -> float x N (N = 2 or 4), from an 8- or 4-byte aligned global
+// address, through L2 only (the rows may have been written by the kernel
+// before, launched with programmatic dependent launch).
 template <int N>
 __device__ __forceinline__ void load_bf16(const __nv_bfloat16* p, float* f);
 template <>
 __device__ __forceinline__ void load_bf16<4>(const __nv_bfloat16* p, float* f) {
-  uint2 u = *reinterpret_cast<const uint2*>(p);
+  uint2 u = __ldcg(reinterpret_cast<const uint2*>(p));
   float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u.x));
   float2 b = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u.y));
   f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
 }
 template <>
 __device__ __forceinline__ void load_bf16<2>(const __nv_bfloat16* p, float* f) {
-  uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+  uint32_t u = __ldcg(reinterpret_cast<const unsigned int*>(p));
   float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162*>(&u));
   f[0] = a.x; f[1] = a.y;
 }
@@ -293,11 +295,11 @@ template <int N>
 __device__ __forceinline__ void store_bf16_raw(__nv_bfloat16* dst, const __nv_bfloat16* src);
 template <>
 __device__ __forceinline__ void store_bf16_raw<4>(__nv_bfloat16* dst, const __nv_bfloat16* src) {
-  *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(src);
+  *reinterpret_cast<uint2*>(dst) = __ldcg(reinterpret_cast<const uint2*>(src));
 }
 template <>
 __device__ __forceinline__ void store_bf16_raw<2>(__nv_bfloat16* dst, const __nv_bfloat16* src) {
-  *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(src);
+  *reinterpret_cast<uint32_t*>(dst) = __ldcg(reinterpret_cast<const unsigned int*>(src));
 }
 
 __device__ __forceinline__ int ceil_blocks(int L) { return (L + kBlock - 1) / kBlock; }

@@ -92,14 +92,14 @@ __host__ __device__ inline PostLayout post_layout(int D, int G, int C, int bpc_m
   l.plan = o; o += 3 * kMaxBatch + 4;  // tokens, streamed blocks and first segment of every sequence
   l.anm = o; o += kMaxG;               // a_g of the open block
   l.lsep = o; o += 2 * kMaxG;          // (max, sum) of the records' logsumexp per head
-  // selection: the local fine histogram [4096]; after its push, the tie lists [C][kTieCap]
-  // of (key, block) and their dense copy (or, on the rare path, the selection bitmap)
+  // selection: the local fine histogram [4096] (read by the peers until barrier 2); after
+  // barrier 2, the dense copy of the cluster's tie lists (or, on the rare path, the selection bitmap)
   l.hf = o;
   l.tie = o;
   l.dense = o + 2 * kMaxC * kTieCap;
   o += kFine;
-  l.xexp = o; o += 256;                            // exchanged exponent histogram (rank 0)
-  l.xfine = o; o += ((256 + C - 1) / C) * 16;      // exchanged fine bins of this rank's exponents
+  l.xexp = o; o += 256;                            // this CTA's counts per 8-bit key prefix (the exponent)
+  l.xfine = o; o += 16 + 2 * kTieCap;              // counts per 4-bit prefix [16]; this CTA's tie list [kTieCap]
   l.xref = o; o += 3 * 256;                        // refinement histograms (rank 0)
   l.lh = o; o += 256;                              // refinement local histogram
   l.xm = o; o += post_ipr(D, G, C) * C * 8;        // merge staging: [items per rank][C][acc4, m, l, -, -]
@@ -124,6 +124,8 @@ enum : int {
   kMCntA = 104,      // int [16]: rare path, every CTA's final own count
   kMR0 = 120,        // int [8]: rare path, the block each warp attended before the exchange
   kMTpre = 128,      // int [16]: exclusive prefix of the CTAs' tie counts
+  kMMine = 160,      // int [2]: this CTA's own-list count and tie count (read by the peers)
+  kMTcnt = 168,      // int [16]: the CTAs' tie counts
 };
 
 // ---------------------------------------------------------------- tensor-core pieces
@@ -359,6 +361,54 @@ __device__ __noinline__ int bitmap_list(const unsigned* words, int nw, int lo, i
   return __shfl_sync(0xffffffffu, incl, 31);
 }
 
+// One level of the cluster-wide threshold search, by one warp.  The 16 counts at
+// `cnt` (the same shared-memory offset in every CTA of the cluster) are summed
+// over the C CTAs -- lane q < C reads CTA q's, a halving butterfly leaves the
+// total of bin l >> 1 in lane l -- and the bin where the count of larger keys,
+// added to `run`, reaches `need` is returned as x, with the count above that
+// bin (including `run`) as y and its own count as z.
+__device__ __noinline__ int3 cluster_level(const uint32_t* cnt, int C, int lane, int need, int run) {
+  uint32_t v[16];
+  if (lane < C) {
+    const uint32_t src = peer_smem(cnt, (uint32_t)lane);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 x = ld_peer_u4(src + 16u * k);
+      v[4 * k] = x.x;
+      v[4 * k + 1] = x.y;
+      v[4 * k + 2] = x.z;
+      v[4 * k + 3] = x.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v[k] = 0u;
+  }
+#pragma unroll
+  for (int o = 16, nv = 16; o >= 2; o >>= 1, nv >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (i < nv / 2) {
+        const uint32_t send = up ? v[i] : v[i + nv / 2];
+        const uint32_t keep = up ? v[i + nv / 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    }
+  }
+  const uint32_t tot = v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);  // bin lane >> 1
+  // count of the bins at and above lane >> 1 (even lanes carry their bin once)
+  uint32_t sfx = (lane & 1) ? 0u : tot;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_down_sync(0xffffffffu, sfx, o);
+    if (lane + o < 32) sfx += y;
+  }
+  const int above = run + (int)(sfx - tot);
+  const bool hit = !(lane & 1) && above < need && need <= above + (int)tot;
+  const int src = __ffs(__ballot_sync(0xffffffffu, hit)) - 1;
+  return make_int3(src >> 1, __shfl_sync(0xffffffffu, above, src), (int)__shfl_sync(0xffffffffu, tot, src));
+}
+
 // Rare path of the selection: more keys share the threshold bin T than the
 // tie lists hold.  The keys in play (candidates in bin T) are resolved by
 // three more radix digits (bits 18..11, 10..3, 2..0), each a histogram summed
@@ -476,7 +526,6 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   uint32_t* keys = reinterpret_cast<uint32_t*>(psm + lay.keys);
   int* own = reinterpret_cast<int*>(psm + lay.own);
   uint32_t* hf = reinterpret_cast<uint32_t*>(psm + lay.hf);
-  uint2* tie = reinterpret_cast<uint2*>(psm + lay.tie);     // [C][kTieCap] (key, block), after the histogram push
   uint2* dense = reinterpret_cast<uint2*>(psm + lay.dense);
   uint32_t* xexp = reinterpret_cast<uint32_t*>(psm + lay.xexp);
   uint32_t* xfine = reinterpret_cast<uint32_t*>(psm + lay.xfine);
@@ -487,7 +536,6 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   int* misc = reinterpret_cast<int*>(psm + lay.misc);
   float* cR = reinterpret_cast<float*>(misc + kMCR);
   float* cW = reinterpret_cast<float*>(misc + kMCW);
-  int* cnt = misc + kMCnt;
   float* anm = psm + lay.anm;
   float* lsep = psm + lay.lsep;
   float* csh = psm + lay.csh;
@@ -514,8 +562,8 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   const int qr_ = (tid & 31) >> 2, qc_ = tid & 3, qks_ = tid >> 5;
   float2 qx0 = make_float2(0.f, 0.f), qx1 = make_float2(0.f, 0.f);
   if (ATT && tid < KS * 32 && qr_ < G) {
-    qx0 = *reinterpret_cast<const float2*>(qunit + qr_ * D + 16 * qks_ + 2 * qc_);
-    qx1 = *reinterpret_cast<const float2*>(qunit + qr_ * D + 16 * qks_ + 8 + 2 * qc_);
+    qx0 = __ldcg(reinterpret_cast<const float2*>(qunit + qr_ * D + 16 * qks_ + 2 * qc_));
+    qx1 = __ldcg(reinterpret_cast<const float2*>(qunit + qr_ * D + 16 * qks_ + 8 + 2 * qc_));
   }
   bool fits_s = false;
   const int L = call_tokens(Lold_s, a.cap_blocks[s], APPEND, &fits_s);
@@ -580,7 +628,6 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   const bool hist = SEL && !all_sel && need0 > 0;    // the threshold search runs
   const bool xchg = SEL && !all_sel;                 // the counts are exchanged
   const bool comp = ATT && !(a.variant & kVarNoCompensation) && (!SEL || !all_sel);
-  cluster_arrive();  // this CTA's exchange areas are zero (every peer waits for this before its first push)
   markt(27, 0);
 
   // ---- a. after the stream: LSE over the records and the open block's a_g (warp 0), zbar and
@@ -652,69 +699,33 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   int need = 0;
   bool take_all = true;
   if (hist) {
-    cluster_wait();  // every peer's exchange areas are zero
+    uint32_t* h2 = xexp;   // counts per 8-bit key prefix (the exponent)
+    uint32_t* h1 = xfine;  // counts per 4-bit key prefix
     {
-      // thread e: exponent e's count to rank 0, its 16 fine bins to rank e % C
-      const int e = tid;  // kPT == 256 exponents
+      // thread e: the 16 fine bins of prefix e
+      const int e = tid;  // kPT == 256 prefixes
       const uint4* hv = reinterpret_cast<const uint4*>(hf + e * 16);
       uint32_t ce = 0;
-#pragma unroll 1
+#pragma unroll
       for (int k = 0; k < 4; ++k) {
         const uint4 f = hv[k];
         ce += f.x + f.y + f.z + f.w;
       }
-      if (ce) {
-        red_peer_add(peer_smem(xexp + e, 0), ce);
-        const uint32_t fo = peer_smem(xfine + (e / C) * 16, (uint32_t)(e % C));
-#pragma unroll 1
-        for (int k = 0; k < 16; ++k)
-          if (hf[e * 16 + k]) red_peer_add(fo + 4u * k, hf[e * 16 + k]);
-      }
+      h2[e] = ce;
+      if (ce) atomicAdd(&h1[e >> 4], ce);
     }
     mark(14);
-    cluster_sync_all();  // barrier 1: rank 0 holds the exponent histogram, rank e % C the fine bins of e
+    cluster_sync_all();  // barrier 1: every CTA's histograms are complete (and every CTA has started)
     mark(2);
     if (warp == 0) {
-      // lane j: exponents 255 - 8j down to 248 - 8j, from rank 0; the lane where the count of
-      // larger keys reaches need0 reads that exponent's 16 fine bins from their owner
-      const uint32_t ea = peer_smem(xexp + 248 - 8 * lane, 0);
-      const uint4 lo4 = ld_peer_u4(ea), hi4 = ld_peer_u4(ea + 16u);
-      const uint32_t cb[8] = {hi4.w, hi4.z, hi4.y, hi4.x, lo4.w, lo4.z, lo4.y, lo4.x};
-      const int c8 = (int)(lo4.x + lo4.y + lo4.z + lo4.w + hi4.x + hi4.y + hi4.z + hi4.w);
-      int incl = c8;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (incl - c8 < need0 && need0 <= incl) {
-        int run = incl - c8, ex = -1;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (ex < 0) {
-            if (run + (int)cb[k] >= need0) ex = 255 - 8 * lane - k;
-            else run += (int)cb[k];
-          }
-        }
-        const uint32_t fo = peer_smem(xfine + (ex / C) * 16, (uint32_t)(ex % C));
-        uint32_t c16[16];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint4 v = ld_peer_u4(fo + 16u * k);
-          c16[4 * k] = v.x;
-          c16[4 * k + 1] = v.y;
-          c16[4 * k + 2] = v.z;
-          c16[4 * k + 3] = v.w;
-        }
-#pragma unroll
-        for (int k = 15; k >= 0; --k) {
-          if (run < need0 && need0 <= run + (int)c16[k]) {
-            misc[kMT] = 16 * ex + k;
-            misc[kMAbove] = run;
-            misc[kMCntT] = (int)c16[k];
-          }
-          run += (int)c16[k];
-        }
+      // three levels of 16 bins over the 12-bit key prefix, each summed over the cluster
+      const int3 l1 = cluster_level(h1, C, lane, need0, 0);
+      const int3 l2 = cluster_level(h2 + 16 * l1.x, C, lane, need0, l1.y);
+      const int3 l3 = cluster_level(hf + 16 * (16 * l1.x + l2.x), C, lane, need0, l2.y);
+      if (lane == 0) {
+        misc[kMT] = 256 * l1.x + 16 * l2.x + l3.x;
+        misc[kMAbove] = l3.y;
+        misc[kMCntT] = l3.z;
       }
     }
     __syncthreads();
@@ -722,7 +733,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
     need = need0 - misc[kMAbove];
     take_all = misc[kMCntT] == need;
   } else {
-    cluster_wait();
+    cluster_sync_all();  // every CTA of the cluster has started before any access to a peer
   }
   mark(3);
 
@@ -763,14 +774,18 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   }
   mark(4);
   if (xchg) {
-    // push (own count, tie count) and the tie entries (key, block) to every CTA of the cluster
-    if (tid < C) st_peer_u2(peer_smem(cnt + 2 * p, (uint32_t)tid), make_uint2((uint32_t)n_own, (uint32_t)ntie));
+    // this CTA's (own count, tie count) and tie entries (key, block), read by every CTA of the
+    // cluster after barrier 2
+    if (tid == 0) {
+      misc[kMMine] = n_own;
+      misc[kMMine + 1] = ntie;
+    }
     const int nt = ntie < kTieCap ? ntie : kTieCap;
+    uint2* tiel = reinterpret_cast<uint2*>(xfine + 16);
 #pragma unroll 1
-    for (int e = tid; e < nt * C; e += kPT) {
-      const int q = e / nt, k = e % nt;
+    for (int k = tid; k < nt; k += kPT) {
       const int i = win[k];
-      st_peer_u2(peer_smem(tie + p * kTieCap + k, (uint32_t)q), make_uint2(keys[i], (uint32_t)(b_lo + i)));
+      tiel[k] = make_uint2(keys[i], (uint32_t)(b_lo + i));
     }
     mark(15);
     if (ATT) {
@@ -868,7 +883,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
     cluster_wait();  // barrier 2: every count and tie list is here
     mark(6);
     // every warp alike: lane q < C holds CTA q's counts
-    const uint2 cq = lane < C ? *reinterpret_cast<const uint2*>(cnt + 2 * lane) : make_uint2(0u, 0u);
+    const uint2 cq = lane < C ? ld_peer_u2(peer_smem(misc + kMMine, (uint32_t)lane)) : make_uint2(0u, 0u);
     const int co = (int)cq.x, ct = (int)cq.y;
     ov = max(0, co - kPW);
     const int sp = lane < C ? kPW - min(co, kPW) : 0;
@@ -896,12 +911,16 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
       if (!take_all && need > 0) {
         // rank every tie entry among all (key desc, block asc), one warp per entry over a
         // dense copy of the lists; the first `need` win, kept in rank order
-        if (warp == 0 && lane < C) misc[kMTpre + lane] = it - ct;
+        if (warp == 0 && lane < C) {
+          misc[kMTpre + lane] = it - ct;
+          misc[kMTcnt + lane] = ct;
+        }
         __syncthreads();
+        const uint2* tiel = reinterpret_cast<const uint2*>(xfine + 16);
 #pragma unroll 1
         for (int e = tid; e < C * kTieCap; e += kPT) {
           const int q = e / kTieCap, k = e % kTieCap;
-          if (k < cnt[2 * q + 1]) dense[misc[kMTpre + q] + k] = tie[e];
+          if (k < misc[kMTcnt + q]) dense[misc[kMTpre + q] + k] = ld_peer_u2(peer_smem(tiel + k, (uint32_t)q));
         }
         __syncthreads();
 #pragma unroll 1

@@ -87,6 +87,22 @@ __device__ __forceinline__ void butterfly(float (&p)[NV], int lane) {
   if constexpr (NV >= 32) halve<NV / 16>(p, lane, 1); else p[0] += __shfl_xor_sync(0xffffffffu, p[0], 1);
 }
 
+// CPL floats of global memory through L2 only: every global input of these
+// kernels may have been written by the kernel before (a chain launched with
+// programmatic dependent launch), so no load may be served by a stale L1 line.
+template <int CPL>
+__device__ __forceinline__ void ldcg_vec(const float* p, float (&x)[CPL]);
+template <>
+__device__ __forceinline__ void ldcg_vec<4>(const float* p, float (&x)[4]) {
+  const float4 v = __ldcg(reinterpret_cast<const float4*>(p));
+  x[0] = v.x; x[1] = v.y; x[2] = v.z; x[3] = v.w;
+}
+template <>
+__device__ __forceinline__ void ldcg_vec<2>(const float* p, float (&x)[2]) {
+  const float2 v = __ldcg(reinterpret_cast<const float2*>(p));
+  x[0] = v.x; x[1] = v.y;
+}
+
 template <int CPL>
 __device__ __forceinline__ void lds_vec(const float* p, float (&x)[CPL]);
 template <>
@@ -134,7 +150,7 @@ __device__ __noinline__ void open_block_warp(const LayerArgs& a, int u, int lane
   const uint4* vnew = reinterpret_cast<const uint4*>(a.v_new + nw) + c;
   uint4* kb = reinterpret_cast<uint4*>(a.k + row * kBlock * D) + c;
   uint4* vb = reinterpret_cast<uint4*>(a.v + row * kBlock * D) + c;
-  const uint4 kn = *knew, vn = *vnew;
+  const uint4 kn = __ldcg(knew), vn = __ldcg(vnew);
   if (owner && tg == 0) {
     kb[(n - 1) * CH] = kn;
     vb[(n - 1) * CH] = vn;
@@ -236,8 +252,8 @@ __device__ __noinline__ void open_block_warp(const LayerArgs& a, int u, int lane
   const float* qg = a.q + ((int64_t)s * a.Hkv + h) * G * D + 8 * c;
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    const float4 q0 = *reinterpret_cast<const float4*>(qg + g * D);
-    const float4 q1 = *reinterpret_cast<const float4*>(qg + g * D + 4);
+    const float4 q0 = __ldcg(reinterpret_cast<const float4*>(qg + g * D));
+    const float4 q1 = __ldcg(reinterpret_cast<const float4*>(qg + g * D + 4));
     const float qr[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
     float z = 0.f, sg = 0.f;
     if (tg == 0) {
@@ -313,11 +329,11 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
     const int s0 = lane, s1 = lane + 32;
     bool f0 = false, f1 = false;
     if (s0 < a.B) {
-      sL[s0] = call_tokens(a.seq_len[s0], a.cap_blocks[s0], APPEND, &f0);
+      sL[s0] = call_tokens(__ldcg(a.seq_len + s0), a.cap_blocks[s0], APPEND, &f0);
       sN[s0] = streamed_blocks(sL[s0], APPEND && f0, SELMODE, a.K, a.scores != nullptr);
     }
     if (s1 < a.B) {
-      sL[s1] = call_tokens(a.seq_len[s1], a.cap_blocks[s1], APPEND, &f1);
+      sL[s1] = call_tokens(__ldcg(a.seq_len + s1), a.cap_blocks[s1], APPEND, &f1);
       sN[s1] = streamed_blocks(sL[s1], APPEND && f1, SELMODE, a.K, a.scores != nullptr);
     }
     __syncwarp();
@@ -366,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
     float q[G][CPL];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      lds_vec<CPL>(qbase + g * D + CPL * lane, q[g]);  // generic load (global memory)
+      ldcg_vec<CPL>(qbase + g * D + CPL * lane, q[g]);
 #pragma unroll
       for (int c = 0; c < CPL; ++c) q[g][c] *= InvSqrt<D>::v;
     }
@@ -418,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
       float* sdb = const_cast<float*>(st) + SB * D * (comp ? 2 : 1);
       const int rb = k * SB, nbs = min(SB, nb - rb);
       if (SCORE && !dbulk && lane < nbs * r)  // r < 4: the Dbar rows by plain loads, 4 floats per row
-        sdb[(lane / r) * 4 + lane % r] = a.dbar[(row0 + rb) * r + lane];
+        sdb[(lane / r) * 4 + lane % r] = __ldcg(a.dbar + (row0 + rb) * r + lane);
       if (!mbar_wait_bounded(bars + warp * kSlots + (use % kSlots), (use / kSlots) & 1u, a.status, s, h, 10)) {
         bad = true;
         break;
@@ -475,7 +491,12 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
             const float* drow = sdb + vb * rs;
             const float* qsr = sqw + vg * rr;
             float t = 0.f;
-            if (r <= 16) {
+            if (r < 4) {
+              // r = 1 or 2: the rows are padded to 4 floats and only the first r are written
+              const float4 qv = *reinterpret_cast<const float4*>(qsr);
+              const float4 dv = *reinterpret_cast<const float4*>(drow);
+              t = r == 2 ? fmaf(qv.x, dv.x, qv.y * dv.y) : qv.x * dv.x;
+            } else if (r <= 16) {
 #pragma unroll
               for (int tt = 0; tt < 16; tt += 4) {
                 if (tt < r) {

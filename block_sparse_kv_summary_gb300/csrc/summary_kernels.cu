@@ -39,7 +39,7 @@ __global__ void append_kernel(LayerArgs a) {
   const int s = blockIdx.x;
   const int h = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int L = a.seq_len[s];
+  const int L = __ldcg(a.seq_len + s);
   const bool fits = L >= 0 && L < a.cap_blocks[s] * kBlock;
   if (h < a.Hkv && fits) {
     const int b = L / kBlock, slot = L % kBlock;
