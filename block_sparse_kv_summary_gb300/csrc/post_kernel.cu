@@ -239,15 +239,15 @@ __device__ __forceinline__ void record_lse(const LayerArgs& a, int i0, int nseg,
   const int tot = nseg * G;
   const float4* base = a.rec + (int64_t)i0 * G;
 #pragma unroll 1
-  for (int k0 = 0; k0 < tot; k0 += 128) {  // four records per lane in flight at once
-    float4 e[4];
+  for (int k0 = 0; k0 < tot; k0 += 256) {  // eight records per lane in flight at once
+    float4 e[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 8; ++j) {
       const int idx = k0 + lane + 32 * j;
       e[j] = idx < tot ? __ldcg(base + idx) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) lse_merge(M, S, e[j].x, e[j].y);
+    for (int j = 0; j < 8; ++j) lse_merge(M, S, e[j].x, e[j].y);
   }
 #pragma unroll 1
   for (int o = G; o < 32; o <<= 1) {
@@ -544,8 +544,8 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   unsigned long long t_wait = 0ull;
   // phase marks of the work-item trace: mark k goes to record 1 + k / 7, slot 1 + k % 7
   // (kept in shared memory until the end, so that no global store waits in a fence)
-  __shared__ unsigned long long tmk[28];
-  if (a.trace && tid < 28) tmk[tid] = 0ull;
+  __shared__ unsigned long long tmk[35];
+  if (a.trace && tid < 35) tmk[tid] = 0ull;
   auto markt = [&](int k, int t) {
     if (a.trace && tid == t) tmk[k] = global_ns();
   };
@@ -720,8 +720,11 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
     if (warp == 0) {
       // three levels of 16 bins over the 12-bit key prefix, each summed over the cluster
       const int3 l1 = cluster_level(h1, C, lane, need0, 0);
+      markt(28, 0);
       const int3 l2 = cluster_level(h2 + 16 * l1.x, C, lane, need0, l1.y);
+      markt(29, 0);
       const int3 l3 = cluster_level(hf + 16 * (16 * l1.x + l2.x), C, lane, need0, l2.y);
+      markt(30, 0);
       if (lane == 0) {
         misc[kMT] = 256 * l1.x + 16 * l2.x + l3.x;
         misc[kMAbove] = l3.y;
@@ -788,16 +791,6 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
       tiel[k] = make_uint2(keys[i], (uint32_t)(b_lo + i));
     }
     mark(15);
-    if (ATT) {
-      // blocks that are attended after the exchange: own blocks beyond the top kPW, tie candidates
-      const int ovf = max(0, n_own - kPW);
-#pragma unroll 1
-      for (int e = tid; e < ovf + nt; e += kPT) {
-        const int64_t row = row0 + (e < ovf ? own[e] : b_lo + win[e - ovf]);
-        prefetch_l2(a.k + row * kBlock * D, kBlock * D * 2);
-        prefetch_l2(a.v + row * kBlock * D, kBlock * D * 2);
-      }
-    }
     mark(16);
     cluster_arrive();  // barrier 2 (waited for once this CTA's first copies are in flight)
     mark(17);
@@ -1015,29 +1008,20 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
     }
     return win[k - OV];
   };
-  if (ATT) {
-    // one loop and one attention site: the block whose copy is in flight, then the next
-    int rd = (SEL && !rare && warp < mine0) ? 1 : 0;
-    for (;;) {
-      if (b_cur >= 0) {
-        if (!mbar_wait_bounded(bars + warp, ph, a.status, s, h, 62)) {
-          mbar_drain_bounded(bars + warp);
-          misc[kMBad] |= 1;
-          break;
-        }
-        ph ^= 1u;
-        blk_attend<D, G>(am, al, acc, qf, stg, n_of(b_cur), comp_of(b_cur), zb_cur, lane);
-      }
-      if (misc[kMBad] & 1) break;
-      int nb = -2;
+  // warps without a block in flight start their first one now; the selection is written while
+  // the copies land
+  int rd = (SEL && !rare && warp < mine0) ? 1 : 0;
+  auto fetch = [&]() -> bool {
+    int nb = -2;
 #pragma unroll 1
-      while (nb == -2) nb = next_block(rd++);
-      if (nb < 0) break;
-      b_cur = nb;
-      zb_cur = issue(nb);
-    }
-  }
-  mark(9);
+    while (nb == -2) nb = next_block(rd++);
+    if (nb < 0) return false;
+    b_cur = nb;
+    zb_cur = issue(nb);
+    return true;
+  };
+  bool have = b_cur >= 0;
+  if (ATT && !have) have = fetch();
   if (SEL) {
     // the ascending selection: this CTA's blocks and the tie winners among them, merged
     int* selrow = a.sel + (int64_t)u * K;
@@ -1070,6 +1054,22 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
       if (tid == 0 && tot_sel != (N < K ? N : K)) set_error(a.status, kDevInternal, s, h, 50);
     }
   }
+  mark(9);
+  if (ATT) {
+    // one attention site: the block whose copy is in flight, then the next
+#pragma unroll 1
+    while (have) {
+      if (!mbar_wait_bounded(bars + warp, ph, a.status, s, h, 62)) {
+        mbar_drain_bounded(bars + warp);
+        misc[kMBad] |= 1;
+        break;
+      }
+      ph ^= 1u;
+      blk_attend<D, G>(am, al, acc, qf, stg, n_of(b_cur), comp_of(b_cur), zb_cur, lane);
+      if (misc[kMBad] & 1) break;
+      have = fetch();
+    }
+  }
   const unsigned long long t_sel = a.trace ? global_ns() : 0ull;
   if (SEL && !ATT) {
     // score/select only: no peer reads this CTA's shared memory after the barrier
@@ -1084,7 +1084,9 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   const unsigned long long t_att = t_sel;
 
   // ---- the CTA's partial: its warps and its compensation share
+  markt(31, 0);
   __syncthreads();  // the staging is free: the partials reuse the union
+  markt(32, 0);
   float* red_a = psm + lay.red;            // [kPW][8][D]
   float* red_m = red_a + kPW * D * 8;      // [kPW][8]
   float* red_l = red_m + kPW * 8;          // [kPW][8]
@@ -1212,12 +1214,12 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   }
   mark(13);
   if (tid == 0 && a.trace) {
-    for (int rec = 0; rec < 4; ++rec) {
+    for (int rec = 0; rec < 5; ++rec) {
       const int64_t ri = a.Q + a.P + (int64_t)(1 + rec) * gridDim.x + blockIdx.x;
       if (ri < a.trace_cap) {
         a.trace[1 + 8 * ri] = ((unsigned long long)blockIdx.x << 32) | ((2ull + rec) << 24) |
                               (unsigned)(ntie | (n_own << 12));
-        for (int k = 0; k < 7; ++k) a.trace[1 + 8 * ri + 1 + k] = tmk[7 * rec + k];
+        for (int k = 0; k < 7; ++k) a.trace[1 + 8 * ri + 1 + k] = 7 * rec + k < 35 ? tmk[7 * rec + k] : 0ull;
       }
     }
     if (a.Q + a.P + (int)blockIdx.x < a.trace_cap) {
