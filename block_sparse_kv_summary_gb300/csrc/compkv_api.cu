@@ -1,5 +1,6 @@
 // C-ABI entry points of libcompkv.so: argument validation, the scratch layout,
 // and the launch sequence of each call.  See include/compkv.h for the contract.
+#include <cuda.h>  // CUtensorMap and its enums (the encoder is fetched through the runtime)
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -134,6 +135,7 @@ struct compkv_ctx {
   compkv_config cfg;
   compkv_buffers buf;
   Layout lay;
+  CUtensorMap tmap_k, tmap_v;  // the whole K and V caches, for the post kernel's block copies
   int64_t launches = 0;
   unsigned long long* trace = nullptr;
   int trace_cap = 0;
@@ -187,9 +189,49 @@ int device_stream_ctas(int d, int r, int G) {
   return v;
 }
 
+// Tensor maps of the whole K and V caches: 2-D (d, tokens) bf16, boxes of
+// 64 x 16 with the 128-byte swizzle (one 16-token block is d / 64 boxes).
+compkv_status make_tensor_maps(compkv_ctx* c) {
+  static std::atomic<void*> encode_fn{nullptr};
+  void* fn = encode_fn.load();
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+      return fail(COMPKV_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    encode_fn.store(fn);
+  }
+  using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  const int d = c->cfg.head_dim;
+  const cuuint64_t tokens = (cuuint64_t)c->cfg.num_layers * (cuuint64_t)c->lay.rows_per_layer * kBlock;
+  if (tokens >= (1ull << 31))
+    return fail(COMPKV_ERR_UNSUPPORTED_SHAPE, "the cache holds %llu token slots; at most 2^31 are addressable",
+                (unsigned long long)tokens);
+  const cuuint64_t dims[2] = {(cuuint64_t)d, tokens};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * 2};
+  const cuuint32_t box[2] = {64, kBlock};
+  const cuuint32_t estr[2] = {1, 1};
+  CUtensorMap* maps[2] = {&c->tmap_k, &c->tmap_v};
+  void* bases[2] = {c->buf.k, c->buf.v};
+  for (int i = 0; i < 2; ++i) {
+    const CUresult r = reinterpret_cast<Encode>(fn)(maps[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, bases[i], dims,
+                                                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(COMPKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  }
+  return COMPKV_OK;
+}
+
 LayerArgs base_args(const compkv_ctx* c, int layer) {
   LayerArgs a;
   memset(&a, 0, sizeof(a));
+  static_assert(sizeof(a.tmap_k) == sizeof(CUtensorMap), "tensor map size");
+  memcpy(a.tmap_k, &c->tmap_k, sizeof(CUtensorMap));
+  memcpy(a.tmap_v, &c->tmap_v, sizeof(CUtensorMap));
+  a.layer_row0 = c->lay.rows_per_layer * (int64_t)layer;
   const int d = c->cfg.head_dim, r = c->cfg.r, G = c->cfg.group_size;
   const int64_t rows = c->lay.rows_per_layer * (int64_t)layer;
   a.k = reinterpret_cast<__nv_bfloat16*>(c->buf.k) + rows * kBlock * d;
@@ -357,6 +399,13 @@ compkv_status compkv_init(const compkv_config* cfg, const compkv_buffers* bufs, 
   c->cfg.capacity_tokens = nullptr;  // copied into the layout
   c->buf = *bufs;
   c->lay = L;
+  {
+    const compkv_status st = make_tensor_maps(c);
+    if (st != COMPKV_OK) {
+      delete c;
+      return st;
+    }
+  }
   cudaError_t e = cudaMemsetAsync(bufs->scratch, 0, L.total, 0);
   if (e == cudaSuccess) e = cudaStreamSynchronize(0);
   if (e != cudaSuccess) {
@@ -613,6 +662,7 @@ compkv_status compkv_internal_decode_in(const compkv_config* cfg, const compkv_b
   c.buf.scratch = scratch;
   c.buf.scratch_bytes = scratch_bytes;
   c.lay = L;
+  COMPKV_TRY(make_tensor_maps(&c));
   cudaStream_t st = (cudaStream_t)stream;
   COMPKV_TRY(cuda_status(cudaMemsetAsync(scratch, 0, L.off_rec, st), "clearing scratch"));
   LayerArgs a = base_args(&c, layer);

@@ -70,6 +70,12 @@ struct LayerArgs {
   // optional trace of the work items (null: off)
   unsigned long long* trace;
   int trace_cap;
+  int64_t layer_row0;            // first row of this layer in the whole cache (tensor-map coordinates)
+  // tensor maps of the whole K and V caches: 2-D (d, tokens), boxes of 64 x 16
+  // bf16 with the 128-byte swizzle; opaque CUtensorMap objects (kernels that
+  // use them take the arguments as a grid constant)
+  alignas(64) unsigned long long tmap_k[16];
+  alignas(64) unsigned long long tmap_v[16];
   // ragged tables
   int64_t seq_row0[kMaxBatch];   // first row of (s, head 0) relative to the layer
   int cap_blocks[kMaxBatch];     // capacity of sequence s in blocks
@@ -142,6 +148,17 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// 2-D tiled tensor copy global -> shared of the box at (x, y) of the tensor map
+// at `tmap` (a grid-constant kernel argument), completion on `bar`; `dst` is
+// 1024-byte aligned (128-byte swizzle) and x * 2 bytes a multiple of 16.
+__device__ __forceinline__ void tma_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
 }
 
 // Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.

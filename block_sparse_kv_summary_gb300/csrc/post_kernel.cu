@@ -57,11 +57,13 @@ struct InvSqrtP<128> {
   static constexpr float v = 0.08838834764831845f;
 };
 
-// Attention staging of one warp: the block's 16 K rows and 16 V rows (bf16;
-// every row padded by 16 bytes, so that the eight rows one ldmatrix reads
-// start in eight different bank quads), then vbar of the block (fp32 [D]).
-__host__ __device__ constexpr int stg_row(int D) { return 2 * D + 16; }
-__host__ __device__ constexpr int stg_bytes(int D) { return 2 * kBlock * stg_row(D) + 4 * D; }
+// Attention staging of one warp, 1024-byte aligned: the block's 16 K rows, then
+// its 16 V rows, each as D / 64 boxes of 16 rows x 128 bytes written by the
+// tensor copy with the 128-byte swizzle (16-byte chunk c of row t lies at
+// chunk c ^ (t % 8), so the eight rows one ldmatrix reads fall in eight
+// different bank quads), then vbar of the block (fp32 [D]).
+__host__ __device__ constexpr int stg_kv(int D) { return kBlock * 2 * D; }  // bytes of the K (or V) boxes
+__host__ __device__ constexpr int stg_bytes(int D) { return (2 * stg_kv(D) + 4 * D + 1023) & ~1023; }
 
 // Shared memory of the post kernel, in 4-byte words.
 struct PostLayout {
@@ -80,7 +82,7 @@ __host__ __device__ inline PostLayout post_layout(int D, int G, int C, int bpc_m
   l.stg = o;
   l.red = o;
   const int zw = 2 * bpc_max * Gp;
-  const int sw = kPW * stg_bytes(D) / 4;
+  const int sw = kPW * stg_bytes(D) / 4 + 256;  // (+ 1 KB to align the staging to 1024 bytes)
   const int rw = kPW * D * 8 + 2 * kPW * 8;  // [kPW][D][8] partial numerators, [kPW][8] maxima and sums
   int uw = zw > sw ? zw : sw;
   uw = uw > rw ? uw : rw;
@@ -171,17 +173,20 @@ template <int D, int G>
 __device__ __forceinline__ void blk_attend(float& m, float& l, float (&acc)[D / 16][4], const uint4* qf,
                                            const char* stg, int n, bool cb, float zb, int lane) {
   constexpr int KS = D / 16;
-  constexpr int RB = stg_row(D);
   const int r = lane >> 2, c = lane & 3;
-  // ldmatrix rows: matrix lane / 8 = (tokens 0-7 | 8-15) x (coordinates +0 | +8)
-  const uint32_t roff = (uint32_t)(((lane >> 4) * 8 + (lane & 7)) * RB + ((lane >> 3) & 1) * 16);
-  const uint32_t kaddr = smem_u32(stg) + roff;
-  const uint32_t vaddr = kaddr + kBlock * RB;
+  // ldmatrix rows: matrix lane / 8 = (tokens 0-7 | 8-15) x (coordinates +0 | +8); the row's
+  // 16-byte chunk 2 ks + hb of k-step ks lies in box ks / 4 at swizzled chunk ((2 ks + hb) % 8) ^ (t % 8)
+  const int t = (lane >> 4) * 8 + (lane & 7), hb = (lane >> 3) & 1, swz = t & 7;
+  const uint32_t kaddr = smem_u32(stg) + (uint32_t)t * 128u;
+  const uint32_t vaddr = kaddr + (uint32_t)stg_kv(D);
+  auto chunk = [&](int ks) -> uint32_t {
+    return (uint32_t)((ks >> 2) * (kBlock * 128) + ((((2 * ks) & 7) + hb) ^ swz) * 16);
+  };
   float s0[4] = {0.f, 0.f, 0.f, 0.f}, s1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int ks = 0; ks < KS; ++ks) {
     uint32_t b0, b1, b2, b3;
-    ldsm_x4(kaddr + 32u * ks, b0, b1, b2, b3);
+    ldsm_x4(kaddr + chunk(ks), b0, b1, b2, b3);
     const uint4 qv = qf[ks * 32 + lane];  // high parts (k 2c.., k 8+2c..), low parts
     mma_bf16(s0, qv.x, 0u, qv.y, 0u, b0, b1);
     mma_bf16(s1, qv.x, 0u, qv.y, 0u, b2, b3);
@@ -211,7 +216,7 @@ __device__ __forceinline__ void blk_attend(float& m, float& l, float (&acc)[D / 
   uint32_t ph0, pl0, ph1, pl1;
   split_bf16(p0, p1, ph0, pl0);
   split_bf16(p2, p3, ph1, pl1);
-  const float* vb = reinterpret_cast<const float*>(stg + 2 * kBlock * RB);
+  const float* vb = reinterpret_cast<const float*>(stg + 2 * stg_kv(D));
 #pragma unroll
   for (int mt = 0; mt < KS; ++mt) {
     const float v0 = cb ? vb[16 * mt + r] : 0.f, v1 = cb ? vb[16 * mt + 8 + r] : 0.f;
@@ -220,7 +225,7 @@ __device__ __forceinline__ void blk_attend(float& m, float& l, float (&acc)[D / 
     acc[mt][2] = fmaf(acc[mt][2], foA, -fnA * v1);
     acc[mt][3] = fmaf(acc[mt][3], foB, -fnB * v1);
     uint32_t a0, a1, a2, a3;
-    ldsm_x4_t(vaddr + 32u * mt, a0, a1, a2, a3);
+    ldsm_x4_t(vaddr + chunk(mt), a0, a1, a2, a3);
     mma_bf16(acc[mt], a0, a1, a2, a3, ph0, ph1);
     mma_bf16(acc[mt], a0, a1, a2, a3, pl0, pl1);
   }
@@ -507,7 +512,7 @@ __device__ __noinline__ void refine_select(const uint32_t* keys, unsigned* bits,
 }
 
 template <int D, int G, int MODE>
-__global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
+__global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerArgs a) {
   constexpr bool APPEND = (MODE & kFAppend) != 0;
   constexpr bool SEL = (MODE & kFSelect) != 0;
   constexpr bool ATT = (MODE & kFAttend) != 0;
@@ -802,7 +807,9 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
 #pragma unroll
   for (int mt = 0; mt < KS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
   uint32_t ph = 0u;
-  char* stg = reinterpret_cast<char*>(psm + lay.stg) + warp * stg_bytes(D);
+  char* stg = reinterpret_cast<char*>(psm + lay.stg);
+  stg += (1024u - (smem_u32(stg) & 1023u)) & 1023u;  // the swizzled boxes want 1024-byte alignment
+  stg += warp * stg_bytes(D);
   const int* selrow_in = a.sel + (int64_t)u * K;
   int tot_sel = 0;
   if (ATT && !SEL) {
@@ -830,28 +837,41 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
   auto n_of = [&](int b) { return (b == N - 1) ? L - kBlock * b : kBlock; };
   // compensation of block b comes off unless this call appended it (the stream skipped it then)
   auto comp_of = [&](int b) { return comp_blk && !(APPEND && app && b == N - 1); };
-  // stage block b into this warp's buffer (rows n..15 zero); returns zbar of head lane / 4
+  // stage block b into this warp's buffer: its 16 K and 16 V rows by 2 D / 64 tensor copies (the
+  // rows past a partial block's tokens are zeroed once they land); returns zbar of head lane / 4
+  bool dirty = false;  // this warp zeroed rows of its buffer with ordinary stores
   auto issue = [&](int b) -> float {
     const int64_t row = row0 + b;
-    const int n = n_of(b);
     const bool cb = comp_of(b);
-    const int t = lane & (kBlock - 1);
     __syncwarp();  // the buffer's previous contents are read
-    if (t >= n) {
-      uint4* z = reinterpret_cast<uint4*>(stg + lane * stg_row(D));
-#pragma unroll 4
-      for (int w = 0; w < D / 8; ++w) z[w] = make_uint4(0u, 0u, 0u, 0u);
+    if (lane == 0) {
+      // ordinary stores into the buffer are ordered before the copies that overwrite it
+      if (dirty) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      const uint64_t pol = policy_evict_first();
+      mbar_arrive_expect_tx(bars + warp, 2u * (uint32_t)stg_kv(D) + (cb ? D * 4u : 0u));
+      const int y = (int)((a.layer_row0 + row) * kBlock);
+#pragma unroll
+      for (int hh = 0; hh < D / 64; ++hh) {
+        tma_2d(stg + hh * kBlock * 128, a.tmap_k, 64 * hh, y, bars + warp, pol);
+        tma_2d(stg + stg_kv(D) + hh * kBlock * 128, a.tmap_v, 64 * hh, y, bars + warp, pol);
+      }
+      if (cb) bulk_g2s_hint(stg + 2 * stg_kv(D), a.vbar + row * D, D * 4u, bars + warp, pol);
     }
-    // the buffer may hold rows this warp wrote with ordinary stores: order them before the copies
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    if (lane == 0) mbar_arrive_expect_tx(bars + warp, 2u * (uint32_t)n * D * 2u + (cb ? D * 4u : 0u));
-    __syncwarp();
-    const uint64_t pol = policy_evict_first();
-    if (t < n)
-      bulk_g2s_hint(stg + lane * stg_row(D), (lane < kBlock ? a.k : a.v) + (row * kBlock + t) * D, D * 2u, bars + warp,
-                    pol);
-    if (cb && lane == 0) bulk_g2s_hint(stg + 2 * kBlock * stg_row(D), a.vbar + row * D, D * 4u, bars + warp, pol);
+    dirty = false;
     return (cb && (lane >> 2) < G) ? __ldcg(a.zs + row * Gp + (lane >> 2)) : 0.f;
+  };
+  // after the copies of block b landed: V rows past its tokens hold whatever follows them in the
+  // cache; zero them (whole rows, so the swizzle does not matter)
+  auto clear_tail = [&](int n) {
+    if (n < kBlock) {
+      for (int x = lane; x < (kBlock - n) * (D / 8); x += 32) {
+        const int t = n + x / (D / 8), j = x % (D / 8);
+        *reinterpret_cast<uint4*>(stg + stg_kv(D) + (j >> 3) * kBlock * 128 + t * 128 + (j & 7) * 16) =
+            make_uint4(0u, 0u, 0u, 0u);
+      }
+      dirty = true;
+      __syncwarp();
+    }
   };
 
   // this CTA's own sure blocks from the top of its list (the open block, the last, comes first):
@@ -1065,6 +1085,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(LayerArgs a) {
         break;
       }
       ph ^= 1u;
+      clear_tail(n_of(b_cur));
       blk_attend<D, G>(am, al, acc, qf, stg, n_of(b_cur), comp_of(b_cur), zb_cur, lane);
       if (misc[kMBad] & 1) break;
       have = fetch();
