@@ -755,45 +755,53 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
       const uint32_t bin = keys[i] >> kDigitShift;
       return bin > T || (bin == T && take_all);
     };
-    int cnt_t = 0;
+    // bitmaps of the sure blocks and of the candidates in bin T (bit i % 32 of word i / 32: block
+    // b_lo + i), one ballot per warp and 32 blocks; then warp 0 lists the sure blocks and warp 1 the
+    // candidates in ascending order (the rare path's radix areas serve as the bitmaps, and are
+    // cleared again afterwards)
+    unsigned* sbits = xref;
+    unsigned* tbits = xref + 256;
 #pragma unroll 1
-    for (int i = c_lo; i < c_hi; ++i) {
-      if (sure(i)) {
-        ++cnt_t;
-      } else if (!take_all && (keys[i] >> kDigitShift) == T) {
-        const int slot = atomicAdd(misc + kMNtie, 1);
-        if (slot < kTieCap) win[slot] = i;  // local indices of this CTA's tie candidates
+    for (int i0 = warp * 32; i0 < nown; i0 += kPT) {
+      const int i = i0 + lane;
+      const bool su = i < nown && sure(i);
+      const bool ti = i < nown && !su && !take_all && (keys[i] >> kDigitShift) == T;
+      const unsigned sb = __ballot_sync(0xffffffffu, su), tb = __ballot_sync(0xffffffffu, ti);
+      if (lane == 0) {
+        sbits[i0 >> 5] = sb;
+        tbits[i0 >> 5] = tb;
       }
     }
-    int tot;
+    __syncthreads();
     mark(19);
-    int pos = cta_exclusive_scan(cnt_t, misc + kMWT, &tot, lane, warp);
-    mark(20);
+    const int nwd = (nown + 31) / 32;
     const int cap = nown < K ? nown : K;
+    if (warp == 0) {
+      const int c = bitmap_list(sbits, nwd, b_lo, own, cap, lane);
+      if (lane == 0) misc[kMOwn] = c;
+    } else if (warp == 1) {
+      // local indices of this CTA's candidates in bin T, and (key, block) of the first kTieCap,
+      // read by every CTA of the cluster after barrier 2
+      const int c = bitmap_list(tbits, nwd, 0, win, kTieCap, lane);
+      if (lane == 0) misc[kMNtie] = c;
+      __syncwarp();
+      uint2* tiel = reinterpret_cast<uint2*>(xfine + 16);
 #pragma unroll 1
-    for (int i = c_lo; i < c_hi; ++i)
-      if (sure(i)) {
-        if (pos < cap) own[pos] = b_lo + i;
-        ++pos;
-      }
-    n_own = tot < cap ? tot : cap;
-    __syncthreads();  // the own list and the tie count are complete
+      for (int k = lane; k < min(c, kTieCap); k += 32) tiel[k] = make_uint2(keys[win[k]], (uint32_t)(b_lo + win[k]));
+    }
+    __syncthreads();  // the own list, the candidates and the tie list are complete
+    mark(20);
+    n_own = min(misc[kMOwn], cap);
     ntie = misc[kMNtie];
+#pragma unroll 1
+    for (int i = tid; i < 3 * 256; i += kPT) xref[i] = 0u;
   }
   mark(4);
   if (xchg) {
-    // this CTA's (own count, tie count) and tie entries (key, block), read by every CTA of the
-    // cluster after barrier 2
+    // this CTA's (own count, tie count), read by every CTA of the cluster after barrier 2
     if (tid == 0) {
       misc[kMMine] = n_own;
       misc[kMMine + 1] = ntie;
-    }
-    const int nt = ntie < kTieCap ? ntie : kTieCap;
-    uint2* tiel = reinterpret_cast<uint2*>(xfine + 16);
-#pragma unroll 1
-    for (int k = tid; k < nt; k += kPT) {
-      const int i = win[k];
-      tiel[k] = make_uint2(keys[i], (uint32_t)(b_lo + i));
     }
     mark(15);
     mark(16);
@@ -1177,7 +1185,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
   if (APPEND && p == 0 && tid == 0) {
     // every CTA of this cluster has read seq_len; the last cluster to get here
     // writes the lengths after this call's append (a sequence at capacity keeps its own)
-    __threadfence();
+    // (each cluster's reads of seq_len were consumed long before its increment)
     if (atomicAdd(a.arrive, 1) == (int)(gridDim.x / C) - 1) {
 #pragma unroll 1
       for (int x = 0; x < a.B; ++x) {
@@ -1185,7 +1193,6 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
         if (f) a.seq_len[x] = sL[x];
       }
       a.arrive[0] = 0;
-      __threadfence();
     }
   }
   // this rank's column items: Cp (C rounded up to a power of two) lanes per item, lane q
