@@ -236,10 +236,12 @@ __device__ __forceinline__ void blk_attend(float& m, float& l, float (&acc)[D / 
 // occupies, so its instruction footprint is on the critical path: loops over
 // runtime counts stay rolled, and every piece of work has one call site.
 
-// (max, sum) of the logsumexp of a_g over the unit's nseg segment records, by one warp: lane j
-// merges records of head j % G; lanes of one head then merge across the warp.
+// LSE_g = logsumexp of a_g over the unit's blocks, from its nseg segment records (and the open
+// block's a_g), by one warp: lane j merges records of head j % G; lanes of one head then merge
+// across the warp; lane g < G writes LSE_g.
 template <int G>
-__device__ __forceinline__ void record_lse(const LayerArgs& a, int i0, int nseg, float* lsep, int lane) {
+__device__ __forceinline__ void record_lse(const LayerArgs& a, int i0, int nseg, float an, bool app, float* lsep,
+                                           int lane) {
   float M = -INFINITY, S = 0.f;
   const int tot = nseg * G;
   const float4* base = a.rec + (int64_t)i0 * G;
@@ -259,9 +261,9 @@ __device__ __forceinline__ void record_lse(const LayerArgs& a, int i0, int nseg,
     const float M2 = __shfl_xor_sync(0xffffffffu, M, o), S2 = __shfl_xor_sync(0xffffffffu, S, o);
     lse_merge(M, S, M2, S2);
   }
-  if (lane < G) {
-    lsep[2 * lane] = M;
-    lsep[2 * lane + 1] = S;
+  if (lane < G) {  // LSE_g, with the open block's a_g (`an`, lane g) when this call appended
+    if (app) lse_merge(M, S, an, 1.f);
+    lsep[lane] = M + __logf(S);
   }
 }
 
@@ -541,7 +543,6 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
   int* misc = reinterpret_cast<int*>(psm + lay.misc);
   float* cR = reinterpret_cast<float*>(misc + kMCR);
   float* cW = reinterpret_cast<float*>(misc + kMCW);
-  float* anm = psm + lay.anm;
   float* lsep = psm + lay.lsep;
   float* csh = psm + lay.csh;
   uint64_t* bars = reinterpret_cast<uint64_t*>(psm + lay.bars);  // [kPW] attention, [1] zbar/sigma2 copy
@@ -641,8 +642,8 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
     pdl_wait();  // the stream kernel's records, zbar and sigma2 are complete and visible
     if (a.trace && tid == 0) t_wait = global_ns();
     if (warp == 0 && want_keys) {
-      if (app && lane < G) anm[lane] = __ldcg(a.anm + (int64_t)u * G + lane);
-      record_lse<G>(a, i0, nseg, lsep, lane);
+      const float an = (app && lane < G) ? __ldcg(a.anm + (int64_t)u * G + lane) : -INFINITY;
+      record_lse<G>(a, i0, nseg, an, app, lsep, lane);
     }
     markt(22, 0);
     // the CTA's share of the compensation sums, by the warps idle until the keys
@@ -670,11 +671,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
   if (want_keys) {
     float lse[G];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float M = lsep[2 * g], S = lsep[2 * g + 1];
-      if (app) lse_merge(M, S, anm[g], 1.f);
-      lse[g] = M + __logf(S);
-    }
+    for (int g = 0; g < G; ++g) lse[g] = lsep[g];
     const bool fom = (a.variant & kVarFirstOrderMass) != 0, nvf = (a.variant & kVarNoVarianceFactor) != 0;
 #pragma unroll 1
     for (int i = c_lo; i < c_hi; ++i) {
@@ -938,11 +935,19 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
         }
         __syncthreads();
         const uint2* tiel = reinterpret_cast<const uint2*>(xfine + 16);
-#pragma unroll 1
-        for (int e = tid; e < C * kTieCap; e += kPT) {
-          const int q = e / kTieCap, k = e % kTieCap;
-          if (k < misc[kMTcnt + q]) dense[misc[kMTpre + q] + k] = ld_peer_u2(peer_smem(tiel + k, (uint32_t)q));
+        static_assert(kMaxC * kTieCap == 4 * kPT, "four tie entries per thread");
+        uint2 tv[4];
+        int td[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {  // every load first, then the stores
+          const int e = tid + j * kPT, q = e / kTieCap, k = e % kTieCap;
+          const bool ok = q < C && k < misc[kMTcnt + q];
+          td[j] = ok ? misc[kMTpre + q] + k : -1;
+          tv[j] = ok ? ld_peer_u2(peer_smem(tiel + k, (uint32_t)q)) : make_uint2(0u, 0u);
         }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (td[j] >= 0) dense[td[j]] = tv[j];
         __syncthreads();
 #pragma unroll 1
         for (int j = warp; j < nt_all; j += kPW) {
@@ -1153,7 +1158,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
     float4 as = make_float4(0.f, 0.f, 0.f, 0.f);
     float Ls = 0.f;
     if (M != -INFINITY) {
-#pragma unroll 1
+#pragma unroll
       for (int w = 0; w < kPW; ++w) {
         const float mw = red_m[w * 8 + g];
         const float f = mw == -INFINITY ? 0.f : __expf(mw - M);
