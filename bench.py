@@ -224,19 +224,23 @@ class Layers:
     """R independent layer caches of a workload on one GPU, with the inputs of
     every step staged on the device and the call arguments prepared once."""
 
-    def __init__(self, name, device, **overrides):
+    def __init__(self, name, device, kv_memory="device", **overrides):
         import torch
 
         import synth
         from block_sparse_kv_summary_gb300.cache import CompKVCache
         wl, R, desc = bench_workload(name, **overrides)
+        if kv_memory == "host":
+            desc += "; K/V rows in page-locked host memory (read over the chip-to-chip link)"
         self.name, self.wl, self.desc, self.device = name, wl, desc, device
         self.R = wl.layers if wl.layers > 1 else R
         self.lens = synth.sequence_lengths(wl)
         self.caps = synth.capacity_tokens(wl)
         B, H, G, d, S = wl.batch, wl.num_kv_heads, wl.group_size, wl.head_dim, wl.steps
         self.cache = CompKVCache(num_layers=self.R, batch=B, num_kv_heads=H, group_size=G, head_dim=d, r=wl.r,
-                                 budget_tokens=wl.budget_tokens, capacity_tokens=self.caps, device=device)
+                                 budget_tokens=wl.budget_tokens, capacity_tokens=self.caps, device=device,
+                                 kv_memory=kv_memory)
+        self.kv_memory = kv_memory
         self.k_new = torch.empty((self.R, S, B, H, d), dtype=torch.bfloat16, device=device)
         self.v_new = torch.empty_like(self.k_new)
         self.q = torch.empty((self.R, S, B, H * G, d), dtype=torch.float32, device=device)
@@ -420,6 +424,8 @@ def main():
                     help="budget covering the whole context: every block selected (exact attention baseline)")
     ap.add_argument("--layers", type=int, default=None,
                     help="rotated layer caches (profiling runs: 1 keeps the device footprint small)")
+    ap.add_argument("--kv-host", action="store_true",
+                    help="K/V rows in page-locked host memory, read by the GPU over the chip-to-chip link")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     ws, rank, local = dist_env()
@@ -460,7 +466,8 @@ def main():
     barrier(ws)
     P.lib()
 
-    work = Layers(args.workload, device, **overrides, **layer_override)
+    work = Layers(args.workload, device, kv_memory="host" if args.kv_host else "device", **overrides,
+                  **layer_override)
     cache = work.cache
     for _ in range(args.warmup):
         work.step()
@@ -579,6 +586,7 @@ def main():
                    "l2": (f"inputs larger than L2: {work.R} independent layer caches rotated, "
                           f"{hbm_l2 / 1e6:.0f} MB touched between visits of one layer")
                    if hbm_l2 > 2 * L2_BYTES else "L2-resident (the workload is smaller than L2)",
+                   "kv_memory": work.kv_memory,
                    "calls_per_step": calls_per_step, "us_per_call": us_call,
                    "hbm_gbs_step": step_gbs, "step_frac_of_peak": step_gbs / peak,
                    "bytes_per_call": by},

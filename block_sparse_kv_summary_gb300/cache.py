@@ -21,10 +21,13 @@ class CompKVCache:
     """A CompKV cache of `num_layers` layers x `batch` sequences on one GPU.
 
     capacity_tokens: an int (every sequence) or a list (ragged), multiples of 16.
+    kv_memory: "device" (the K and V rows in GPU memory, the default) or "host"
+        (in page-locked host memory, which the GPU reads over its chip-to-chip
+        link; the summaries, the scratch and everything else stay in GPU memory).
     """
 
     def __init__(self, *, num_layers, batch, num_kv_heads, group_size, head_dim, r,
-                 budget_tokens, capacity_tokens, device="cuda", variant=0):
+                 budget_tokens, capacity_tokens, device="cuda", variant=0, kv_memory="device"):
         self.device = torch.device(device)
         if self.device.type != "cuda":
             raise RuntimeError("CompKVCache lives in GPU memory; the library has no CPU path")
@@ -44,8 +47,15 @@ class CompKVCache:
         self.rows_per_layer = rows
         total = rows * num_layers
         dev = self.device
-        self.k = torch.zeros((total, BLOCK, head_dim), dtype=torch.bfloat16, device=dev)
-        self.v = torch.zeros((total, BLOCK, head_dim), dtype=torch.bfloat16, device=dev)
+        if kv_memory not in ("device", "host"):
+            raise ValueError(f"kv_memory must be 'device' or 'host', got {kv_memory!r}")
+        self.kv_memory = kv_memory
+        if kv_memory == "host":
+            self.k = torch.zeros((total, BLOCK, head_dim), dtype=torch.bfloat16, pin_memory=True)
+            self.v = torch.zeros((total, BLOCK, head_dim), dtype=torch.bfloat16, pin_memory=True)
+        else:
+            self.k = torch.zeros((total, BLOCK, head_dim), dtype=torch.bfloat16, device=dev)
+            self.v = torch.zeros((total, BLOCK, head_dim), dtype=torch.bfloat16, device=dev)
         self.kbar = torch.zeros((total, head_dim), dtype=torch.float32, device=dev)
         self.vbar = torch.zeros((total, head_dim), dtype=torch.float32, device=dev)
         self.dbar = torch.zeros((total, r), dtype=torch.float32, device=dev)

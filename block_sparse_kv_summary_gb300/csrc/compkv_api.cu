@@ -136,6 +136,7 @@ struct compkv_ctx {
   compkv_buffers buf;
   Layout lay;
   CUtensorMap tmap_k, tmap_v;  // the whole K and V caches, for the post kernel's block copies
+  int kv_host = 0;             // K and V in page-locked host memory (no tensor maps)
   int64_t launches = 0;
   unsigned long long* trace = nullptr;
   int trace_cap = 0;
@@ -192,6 +193,28 @@ int device_stream_ctas(int d, int r, int G) {
 // Tensor maps of the whole K and V caches: 2-D (d, tokens) bf16, boxes of
 // 64 x 16 with the 128-byte swizzle (one 16-token block is d / 64 boxes).
 compkv_status make_tensor_maps(compkv_ctx* c) {
+  // where K and V live: device memory (tensor maps), or page-locked host memory that the device
+  // reaches over the chip-to-chip link (plain 16-byte copies, no tensor maps)
+  int host = 0;
+  for (void* p : {c->buf.k, c->buf.v}) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(COMPKV_ERR_INVALID_ARG, "k / v: not memory the CUDA runtime knows (device or page-locked host)");
+    }
+    if (at.type == cudaMemoryTypeHost) {
+      if (!at.devicePointer || at.devicePointer != p)
+        return fail(COMPKV_ERR_INVALID_ARG, "k / v: host memory not mapped at the same address on the device");
+      host |= 1 << (p == c->buf.v);
+    } else if (at.type != cudaMemoryTypeDevice) {
+      return fail(COMPKV_ERR_INVALID_ARG, "k / v must be device memory or page-locked host memory");
+    }
+  }
+  if (host == 1 || host == 2) return fail(COMPKV_ERR_INVALID_ARG, "k and v must both be in device or in host memory");
+  c->kv_host = host ? 1 : 0;
+  memset(&c->tmap_k, 0, sizeof(c->tmap_k));
+  memset(&c->tmap_v, 0, sizeof(c->tmap_v));
+  if (c->kv_host) return COMPKV_OK;
   static std::atomic<void*> encode_fn{nullptr};
   void* fn = encode_fn.load();
   if (!fn) {
@@ -232,6 +255,7 @@ LayerArgs base_args(const compkv_ctx* c, int layer) {
   memcpy(a.tmap_k, &c->tmap_k, sizeof(CUtensorMap));
   memcpy(a.tmap_v, &c->tmap_v, sizeof(CUtensorMap));
   a.layer_row0 = c->lay.rows_per_layer * (int64_t)layer;
+  a.kv_host = c->kv_host;
   const int d = c->cfg.head_dim, r = c->cfg.r, G = c->cfg.group_size;
   const int64_t rows = c->lay.rows_per_layer * (int64_t)layer;
   a.k = reinterpret_cast<__nv_bfloat16*>(c->buf.k) + rows * kBlock * d;

@@ -71,6 +71,8 @@ struct LayerArgs {
   unsigned long long* trace;
   int trace_cap;
   int64_t layer_row0;            // first row of this layer in the whole cache (tensor-map coordinates)
+  int kv_host;                   // the K and V rows live in page-locked host memory (reached over the
+                                 // chip-to-chip link): blocks are copied by plain 16-byte copies
   // tensor maps of the whole K and V caches: 2-D (d, tokens), boxes of 64 x 16
   // bf16 with the 128-byte swizzle; opaque CUtensorMap objects (kernels that
   // use them take the arguments as a grid constant)
@@ -160,6 +162,15 @@ __device__ __forceinline__ void tma_2d(void* dst, const void* tmap, int x, int y
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
+
+// 16-byte asynchronous copy global -> shared through the load path (any
+// memory the device can load from, host memory included); completion is
+// awaited with cp_async_wait_all.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // Bulk prefetch of `bytes` (a multiple of 16, 16-byte aligned) into L2.
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {

@@ -849,16 +849,33 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
     const int64_t row = row0 + b;
     const bool cb = comp_of(b);
     __syncwarp();  // the buffer's previous contents are read
+    if (a.kv_host) {
+      // K and V in host memory: every lane copies 16-byte chunks of the block's n rows into their
+      // swizzled places (rows past n are masked for K and zeroed for V once the copies land)
+      const int n = n_of(b);
+      const char* kg = reinterpret_cast<const char*>(a.k + row * kBlock * D);
+      const char* vg = reinterpret_cast<const char*>(a.v + row * kBlock * D);
+#pragma unroll 1
+      for (int x = lane; x < n * (D / 8); x += 32) {
+        const int t = x / (D / 8), j = x % (D / 8);
+        const int so = (j >> 3) * kBlock * 128 + t * 128 + (((j & 7) ^ (t & 7)) << 4);
+        cp_async16(stg + so, kg + x * 16);
+        cp_async16(stg + stg_kv(D) + so, vg + x * 16);
+      }
+      cp_async_commit();
+    }
     if (lane == 0) {
       // ordinary stores into the buffer are ordered before the copies that overwrite it
       if (dirty) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       const uint64_t pol = policy_evict_first();
-      mbar_arrive_expect_tx(bars + warp, 2u * (uint32_t)stg_kv(D) + (cb ? D * 4u : 0u));
-      const int y = (int)((a.layer_row0 + row) * kBlock);
+      mbar_arrive_expect_tx(bars + warp, (a.kv_host ? 0u : 2u * (uint32_t)stg_kv(D)) + (cb ? D * 4u : 0u));
+      if (!a.kv_host) {
+        const int y = (int)((a.layer_row0 + row) * kBlock);
 #pragma unroll
-      for (int hh = 0; hh < D / 64; ++hh) {
-        tma_2d(stg + hh * kBlock * 128, a.tmap_k, 64 * hh, y, bars + warp, pol);
-        tma_2d(stg + stg_kv(D) + hh * kBlock * 128, a.tmap_v, 64 * hh, y, bars + warp, pol);
+        for (int hh = 0; hh < D / 64; ++hh) {
+          tma_2d(stg + hh * kBlock * 128, a.tmap_k, 64 * hh, y, bars + warp, pol);
+          tma_2d(stg + stg_kv(D) + hh * kBlock * 128, a.tmap_v, 64 * hh, y, bars + warp, pol);
+        }
       }
       if (cb) bulk_g2s_hint(stg + 2 * stg_kv(D), a.vbar + row * D, D * 4u, bars + warp, pol);
     }
@@ -1098,6 +1115,10 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
         break;
       }
       ph ^= 1u;
+      if (a.kv_host) {  // this lane's copies, then every lane's
+        cp_async_wait_all();
+        __syncwarp();
+      }
       clear_tail(n_of(b_cur));
       blk_attend<D, G>(am, al, acc, qf, stg, n_of(b_cur), comp_of(b_cur), zb_cur, lane);
       if (misc[kMBad] & 1) break;

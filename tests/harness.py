@@ -44,7 +44,7 @@ class Run:
     variant: compkv_config.variant of the cache; the oracle runs the same ablation.
     """
 
-    def __init__(self, wl: synth.Workload, heads="all", device="cuda", variant=0):
+    def __init__(self, wl: synth.Workload, heads="all", device="cuda", variant=0, kv_memory="device"):
         from block_sparse_kv_summary_gb300.cache import CompKVCache
         self.wl = wl
         self.variant = variant
@@ -54,7 +54,7 @@ class Run:
         self.cache = CompKVCache(num_layers=wl.layers, batch=wl.batch, num_kv_heads=wl.num_kv_heads,
                                  group_size=wl.group_size, head_dim=wl.head_dim, r=wl.r,
                                  budget_tokens=wl.budget_tokens, capacity_tokens=self.caps, device=device,
-                                 variant=variant)
+                                 variant=variant, kv_memory=kv_memory)
         if heads == "all":
             heads = [(l, s, h) for l in range(wl.layers) for s in range(wl.batch) for h in range(wl.num_kv_heads)]
         self.heads = sorted(set(heads))
