@@ -115,6 +115,16 @@ typedef struct {
 #define COMPKV_VARIANT_NO_VARIANCE_FACTOR 2
 #define COMPKV_VARIANT_NO_COMPENSATION 4
 
+/* Placement.  kbar, vbar, dbar, seq_len and scratch are device memory.  k and
+ * v are both device memory, or both page-locked host memory mapped at the same
+ * address on the device (cudaHostAlloc / cudaMallocHost): the host placement
+ * is the GB300 form of the page's offloaded cache (section "어떻게 쓰나": KV in
+ * pinned CPU memory), read by the GPU over its chip-to-chip link, while the
+ * summaries stay in GPU memory.  compkv_init recognises the placement from the
+ * pointers and rejects anything else (pageable or managed memory, or k and v
+ * in different places).  In device memory the cache may hold at most 2^31
+ * token slots (num_layers * rows_per_layer * 16): its blocks are read through
+ * tensor maps. */
 typedef struct {
   void  *k;                     /* bf16 [num_layers * rows_per_layer][16][d]         */
   void  *v;                     /* bf16, same shape                                 */
@@ -269,15 +279,19 @@ compkv_status compkv_profile_enable(compkv_ctx *ctx, int enable);
  * caller device memory, 8-byte aligned, `bytes` long, zeroed by the caller
  * before a traced call.  Word 0 is unused; record slot i occupies words
  * 1 + 8 i .. 8 + 8 i, for i < (bytes - 8) / 64 (slots beyond are not
- * written).  Times are %globaltimer nanoseconds.  With P stream CTAs and C
- * CTAs per unit in the second kernel:
- *   slot x < P, stream CTA x: (x << 32 | segments it processed), 0, t0 its
+ * written).  Times are %globaltimer nanoseconds.  With W CTAs in the stream
+ * kernel's grid (in a call that appends, its first CTAs recompute the open
+ * blocks and the rest stream the summaries) and X CTAs (C per unit) in the
+ * second kernel:
+ *   slot x < W, stream CTA x: (x << 32 | segments it processed), 0, t0 its
  *     start, t1 its plan known (after waiting for the previous work), t2 its
  *     first segment done, t3 its end;
- *   slot P + x, CTA x of the second kernel: (x << 32 | 1 << 24 | cluster
+ *   slot W + x, CTA x of the second kernel: (x << 32 | 1 << 24 | cluster
  *     rank), unit (= sequence * Hkv + head), t0 its start, t1 the end of its
- *     wait for the stream kernel, t2 the selection known, t3 the attention
- *     done, t4 its end, and the unit's selected block count.
+ *     wait for the stream kernel, t2 = t3 its attention done, t4 its end, and
+ *     the unit's selected block count;
+ *   slots W + k X + x, k = 1 .. 5: (x << 32 | (k + 1) << 24 | ...) and seven
+ *     phase times of CTA x each (0 for a phase it did not reach).
  * A slot a call does not use stays as the caller left it.  buf = NULL
  * switches tracing off. */
 compkv_status compkv_trace(compkv_ctx *ctx, void *buf, size_t bytes);
