@@ -197,8 +197,9 @@ def bench_workload(name, r=None, budget=None, dense=False, layers=None):
 
 def step_bytes(wl):
     """Algorithmic bytes per decode call, averaged over the workload's steps:
-    the summary rows of every block, the K/V of the selected blocks, q and out
-    (and, per kernel: what the stream reads, what the post kernel reads)."""
+    the summary rows of every block (of the units that select, N > K), the K/V
+    of the selected blocks, q and out (and, per kernel: what the stream reads,
+    what the post kernel reads)."""
     import synth
     d, r, H, G, K = wl.head_dim, wl.r, wl.num_kv_heads, wl.group_size, wl.K_blocks
     summ = sel_kv = stream = post = 0.0
@@ -208,8 +209,9 @@ def step_bytes(wl):
             L = L0 + c + 1
             N = (L + BLOCK - 1) // BLOCK
             n_last = L - BLOCK * (N - 1)
-            summ += H * N * (2 * d + r + 1) * 4
-            stream += H * N * (2 * d + r) * 4
+            if N > K:  # (with every block selected the summaries are not read)
+                summ += H * N * (2 * d + r + 1) * 4
+                stream += H * N * (2 * d + r) * 4
             tok = min(N, K) * BLOCK - (BLOCK - n_last)
             sel_kv += H * tok * d * 2 * 2
             post += H * (tok * d * 2 * 2 + min(N, K) * d * 4)
