@@ -143,8 +143,10 @@ class CompKVCache:
         return C.PreparedDecode(self.ctx, _stream(self.device))
 
     def decode_host(self, layer, q, k_new, v_new, out, sel=None):
-        """compkv_decode_host on page-locked CPU tensors (q fp32 [B][Hq][d],
-        k_new/v_new bf16 [B][Hkv][d], out fp32 [B][Hq][d]); returns when out is filled."""
+        """compkv_decode_host on CPU tensors (q fp32 [B][Hq][d], k_new/v_new bf16
+        [B][Hkv][d], out fp32 [B][Hq][d], sel int32 [B][Hkv][K] or None); returns
+        when out is filled.  Page-locked tensors are read and written by the
+        kernels directly; others are copied."""
         for t, name in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (out, "out")):
             if t.device.type != "cpu" or not t.is_contiguous():
                 raise ValueError(f"{name} must be a contiguous CPU tensor")

@@ -137,6 +137,9 @@ struct compkv_ctx {
   Layout lay;
   CUtensorMap tmap_k, tmap_v;  // the whole K and V caches, for the post kernel's block copies
   int kv_host = 0;             // K and V in page-locked host memory (no tensor maps)
+  // the last host buffers compkv_decode_host found page-locked and mapped (checked once)
+  const void* mapped_seen[8] = {};
+  int mapped_next = 0;
   int64_t launches = 0;
   unsigned long long* trace = nullptr;
   int trace_cap = 0;
@@ -538,19 +541,45 @@ compkv_status compkv_decode_host(compkv_ctx* c, int layer, const float* q_host, 
   void* dk = sc + c->lay.off_hk;
   void* dv = sc + c->lay.off_hv;
   float* dout = reinterpret_cast<float*>(sc + c->lay.off_hout);
-  COMPKV_TRY(cuda_status(cudaMemcpyAsync(dq, q_host, units * G * d * 4, cudaMemcpyHostToDevice, st), "q copy"));
-  COMPKV_TRY(cuda_status(cudaMemcpyAsync(dk, k_new_host, units * d * 2, cudaMemcpyHostToDevice, st), "k_new copy"));
-  COMPKV_TRY(cuda_status(cudaMemcpyAsync(dv, v_new_host, units * d * 2, cudaMemcpyHostToDevice, st), "v_new copy"));
+  const size_t qb = units * G * d * 4, kb = units * d * 2;
   LayerArgs a = base_args(c, layer);
   a.q = dq;
   a.k_new = reinterpret_cast<const __nv_bfloat16*>(dk);
   a.v_new = reinterpret_cast<const __nv_bfloat16*>(dv);
   a.out = dout;
-  COMPKV_TRY(launch_chain(c, COMPKV_KERNEL_DECODE, a, kFusedDecode, st, "decode launch"));
-  COMPKV_TRY(cuda_status(cudaMemcpyAsync(out_host, dout, units * G * d * 4, cudaMemcpyDeviceToHost, st), "out copy"));
-  if (sel_host)
-    COMPKV_TRY(cuda_status(cudaMemcpyAsync(sel_host, a.sel, units * (size_t)c->lay.K * 4, cudaMemcpyDeviceToHost, st),
-                           "sel copy"));
+  // page-locked host buffers (mapped at the same address on the device, 16-byte aligned): the
+  // inputs come in through one small kernel and the kernels write out and the selection straight
+  // into host memory; any other host memory goes through copies
+  auto mapped = [c](const void* p) {
+    for (const void* x : c->mapped_seen)
+      if (x == p) return true;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    const bool ok = at.type == cudaMemoryTypeHost && at.devicePointer == p && aligned(p, 16);
+    if (ok) c->mapped_seen[c->mapped_next++ % 8] = p;
+    return ok;
+  };
+  const bool direct = mapped(q_host) && mapped(k_new_host) && mapped(v_new_host) && mapped(out_host) &&
+                      (!sel_host || mapped(sel_host)) && qb % 16 == 0 && kb % 16 == 0;
+  if (direct) {
+    COMPKV_TRY(cuda_status(launch_stage_in(dq, q_host, qb, dk, k_new_host, kb, dv, v_new_host, kb, st), "input stage"));
+    ++c->launches;
+    a.out = out_host;
+    if (sel_host) a.sel = sel_host;
+    COMPKV_TRY(launch_chain(c, COMPKV_KERNEL_DECODE, a, kFusedDecode, st, "decode launch"));
+  } else {
+    COMPKV_TRY(cuda_status(cudaMemcpyAsync(dq, q_host, qb, cudaMemcpyHostToDevice, st), "q copy"));
+    COMPKV_TRY(cuda_status(cudaMemcpyAsync(dk, k_new_host, kb, cudaMemcpyHostToDevice, st), "k_new copy"));
+    COMPKV_TRY(cuda_status(cudaMemcpyAsync(dv, v_new_host, kb, cudaMemcpyHostToDevice, st), "v_new copy"));
+    COMPKV_TRY(launch_chain(c, COMPKV_KERNEL_DECODE, a, kFusedDecode, st, "decode launch"));
+    COMPKV_TRY(cuda_status(cudaMemcpyAsync(out_host, dout, qb, cudaMemcpyDeviceToHost, st), "out copy"));
+    if (sel_host)
+      COMPKV_TRY(cuda_status(cudaMemcpyAsync(sel_host, a.sel, units * (size_t)c->lay.K * 4, cudaMemcpyDeviceToHost, st),
+                             "sel copy"));
+  }
   COMPKV_TRY(cuda_status(cudaStreamSynchronize(st), "stream synchronize"));
   return COMPKV_OK;
 }

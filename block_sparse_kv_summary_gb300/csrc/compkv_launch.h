@@ -23,6 +23,10 @@ constexpr int kMaxStreamCtas = 1024;   // the stream kernel's grid at most (segm
 
 cudaError_t launch_prefill(const LayerArgs& a, int64_t rows_per_layer, cudaStream_t st);
 cudaError_t launch_append(const LayerArgs& a, cudaStream_t st);
+// Copies three buffers (byte counts multiples of 16, 16-byte aligned) to device memory in one
+// kernel; the sources may be page-locked host memory.
+cudaError_t launch_stage_in(void* d0, const void* s0, size_t b0, void* d1, const void* s1, size_t b1, void* d2,
+                            const void* s2, size_t b2, cudaStream_t st);
 // One bounded mbarrier wait that runs out and records kDevTimeout in `status`.
 cudaError_t launch_wait_selftest(int* status, cudaStream_t st);
 

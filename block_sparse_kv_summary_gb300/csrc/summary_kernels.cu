@@ -91,6 +91,30 @@ cudaError_t launch_wait_selftest(int* status, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// Copies up to three buffers of 16-byte chunks (src may be page-locked host
+// memory the device reads over its link) into device memory, one chunk per
+// thread and step: the inputs of a host-to-host decode call in one launch.
+__global__ void stage_in_kernel(uint4* d0, const uint4* s0, int n0, uint4* d1, const uint4* s1, int n1, uint4* d2,
+                                const uint4* s2, int n2) {
+  const int stride = gridDim.x * blockDim.x;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n0 + n1 + n2; i += stride) {
+    if (i < n0) d0[i] = __ldcg(s0 + i);
+    else if (i < n0 + n1) d1[i - n0] = __ldcg(s1 + i - n0);
+    else d2[i - n0 - n1] = __ldcg(s2 + i - n0 - n1);
+  }
+}
+
+cudaError_t launch_stage_in(void* d0, const void* s0, size_t b0, void* d1, const void* s1, size_t b1, void* d2,
+                            const void* s2, size_t b2, cudaStream_t st) {
+  const int n0 = (int)(b0 / 16), n1 = (int)(b1 / 16), n2 = (int)(b2 / 16);
+  const int n = n0 + n1 + n2;
+  const int threads = 256, blocks = (n + threads - 1) / threads < 8 ? (n + threads - 1) / threads : 8;
+  stage_in_kernel<<<blocks < 1 ? 1 : blocks, threads, 0, st>>>(
+      reinterpret_cast<uint4*>(d0), reinterpret_cast<const uint4*>(s0), n0, reinterpret_cast<uint4*>(d1),
+      reinterpret_cast<const uint4*>(s1), n1, reinterpret_cast<uint4*>(d2), reinterpret_cast<const uint4*>(s2), n2);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_append(const LayerArgs& a, cudaStream_t st) {
   const int threads = 32 * a.Hkv;
   if (a.d == 128)

@@ -190,14 +190,16 @@ compkv_status compkv_decode(compkv_ctx *ctx, int layer, const float *q, const vo
                             const void *v_new, float *out, int *sel, void *stream);
 
 /* Steps 1-5 from host memory to host memory, for callers whose inputs and
- * outputs live on the host: copies q (fp32 [B][Hq][d]), k_new and v_new (bf16
- * [B][Hkv][d]) into staging space inside the context's scratch, runs the
- * decode step of compkv_decode on them, copies out (fp32 [B][Hq][d]) and, when
- * sel_host is not NULL, the selection (int32 [B][Hkv][K]) back, and
- * synchronises `stream`: when it returns COMPKV_OK, out_host holds the
- * result.  Host buffers should be page-locked (cudaHostAlloc) for the copies
- * to run asynchronously.  Device-side problems are reported by
- * compkv_device_status as for compkv_decode. */
+ * outputs live on the host: q (fp32 [B][Hq][d]), k_new and v_new (bf16
+ * [B][Hkv][d]) go into staging space inside the context's scratch, the decode
+ * step of compkv_decode runs on them, out (fp32 [B][Hq][d]) and, when sel_host
+ * is not NULL, the selection (int32 [B][Hkv][K]) come back, and `stream` is
+ * synchronised: when it returns COMPKV_OK, out_host holds the result.  When
+ * every buffer is page-locked host memory mapped at the same address on the
+ * device (cudaHostAlloc) and 16-byte aligned, the inputs come in through one
+ * small kernel and the kernels write out and the selection straight into host
+ * memory; otherwise each buffer is copied with cudaMemcpyAsync.  Device-side
+ * problems are reported by compkv_device_status as for compkv_decode. */
 compkv_status compkv_decode_host(compkv_ctx *ctx, int layer, const float *q_host, const void *k_new_host,
                                  const void *v_new_host, float *out_host, int *sel_host, void *stream);
 

@@ -250,3 +250,27 @@ def test_selection_ties_go_to_the_lower_index(pattern):
         exp[:len(ref)] = ref
         assert np.array_equal(sel[s, h], exp), f"unit {(s, h)}:\n gpu {sel[s, h]}\n ref {exp}"
     assert cache.device_status() == 0
+
+
+@pytest.mark.parametrize("pinned", [True, False], ids=["page-locked", "pageable"])
+def test_decode_host_buffers(pinned):
+    # compkv_decode_host: host inputs to host outputs (page-locked buffers are read and written
+    # by the kernels directly, pageable ones are copied); the oracle decides, and the outputs equal
+    # those of compkv_decode on device buffers of the same cache
+    wl = _ragged(SHAPES[1], lengths=(5, 600, 1800), budget=256, steps=3)
+    dev, host = Run(wl), Run(wl)
+    for step in range(wl.steps):
+        qd, seld, outd, resd = dev.decode_step(0)
+        k_new, v_new = host.new_tokens(0, step)
+        host.oracle_append(0, k_new, v_new)
+        q, res = host.choose_queries(0, step)
+        mk = (lambda t: t.cpu().pin_memory()) if pinned else (lambda t: t.cpu().clone())
+        hq, hk, hv = mk(q), mk(k_new), mk(v_new)
+        hout = mk(torch.zeros_like(outd))
+        hsel = mk(torch.zeros_like(seld))
+        host.cache.decode_host(0, hq, hk, hv, hout, sel=hsel)
+        host.step_no[0] += 1
+        check_step(host, 0, hsel, hout, res)
+        assert torch.equal(hsel, seld.cpu())
+        assert (hout - outd.cpu()).abs().max().item() <= 1e-6
+    assert host.cache.device_status() == 0
