@@ -137,9 +137,6 @@ struct compkv_ctx {
   Layout lay;
   CUtensorMap tmap_k, tmap_v;  // the whole K and V caches, for the post kernel's block copies
   int kv_host = 0;             // K and V in page-locked host memory (no tensor maps)
-  // the last host buffers compkv_decode_host found page-locked and mapped (checked once)
-  const void* mapped_seen[8] = {};
-  int mapped_next = 0;
   int64_t launches = 0;
   unsigned long long* trace = nullptr;
   int trace_cap = 0;
@@ -550,17 +547,15 @@ compkv_status compkv_decode_host(compkv_ctx* c, int layer, const float* q_host, 
   // page-locked host buffers (mapped at the same address on the device, 16-byte aligned): the
   // inputs come in through one small kernel and the kernels write out and the selection straight
   // into host memory; any other host memory goes through copies
-  auto mapped = [c](const void* p) {
-    for (const void* x : c->mapped_seen)
-      if (x == p) return true;
+  // (checked on every call: a buffer freed and its address reused by pageable memory must not
+  // be written by a kernel)
+  auto mapped = [](const void* p) {
     cudaPointerAttributes at;
     if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
       cudaGetLastError();
       return false;
     }
-    const bool ok = at.type == cudaMemoryTypeHost && at.devicePointer == p && aligned(p, 16);
-    if (ok) c->mapped_seen[c->mapped_next++ % 8] = p;
-    return ok;
+    return at.type == cudaMemoryTypeHost && at.devicePointer == p && aligned(p, 16);
   };
   const bool direct = mapped(q_host) && mapped(k_new_host) && mapped(v_new_host) && mapped(out_host) &&
                       (!sel_host || mapped(sel_host)) && qb % 16 == 0 && kb % 16 == 0;
