@@ -136,6 +136,7 @@ struct compkv_ctx {
   compkv_buffers buf;
   Layout lay;
   CUtensorMap tmap_k, tmap_v;  // the whole K and V caches, for the post kernel's block copies
+  int tmap_ok = 0;             // the maps were built
   int kv_host = 0;             // K and V in page-locked host memory (no tensor maps)
   int64_t launches = 0;
   unsigned long long* trace = nullptr;
@@ -214,6 +215,7 @@ compkv_status make_tensor_maps(compkv_ctx* c) {
   c->kv_host = host ? 1 : 0;
   memset(&c->tmap_k, 0, sizeof(c->tmap_k));
   memset(&c->tmap_v, 0, sizeof(c->tmap_v));
+  c->tmap_ok = 0;
   if (c->kv_host) return COMPKV_OK;
   static std::atomic<void*> encode_fn{nullptr};
   void* fn = encode_fn.load();
@@ -245,6 +247,7 @@ compkv_status make_tensor_maps(compkv_ctx* c) {
                                                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(COMPKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
   }
+  c->tmap_ok = 1;
   return COMPKV_OK;
 }
 
@@ -256,6 +259,7 @@ LayerArgs base_args(const compkv_ctx* c, int layer) {
   memcpy(a.tmap_v, &c->tmap_v, sizeof(CUtensorMap));
   a.layer_row0 = c->lay.rows_per_layer * (int64_t)layer;
   a.kv_host = c->kv_host;
+  a.tmap_ok = c->tmap_ok;
   const int d = c->cfg.head_dim, r = c->cfg.r, G = c->cfg.group_size;
   const int64_t rows = c->lay.rows_per_layer * (int64_t)layer;
   a.k = reinterpret_cast<__nv_bfloat16*>(c->buf.k) + rows * kBlock * d;

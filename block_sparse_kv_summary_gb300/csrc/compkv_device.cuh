@@ -73,6 +73,7 @@ struct LayerArgs {
   int64_t layer_row0;            // first row of this layer in the whole cache (tensor-map coordinates)
   int kv_host;                   // the K and V rows live in page-locked host memory (reached over the
                                  // chip-to-chip link): blocks are copied by plain 16-byte copies
+  int tmap_ok;                   // tmap_k / tmap_v were built; without them blocks take the plain copies
   // tensor maps of the whole K and V caches: 2-D (d, tokens), boxes of 64 x 16
   // bf16 with the 128-byte swizzle; opaque CUtensorMap objects (kernels that
   // use them take the arguments as a grid constant)

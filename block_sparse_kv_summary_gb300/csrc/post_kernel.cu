@@ -646,8 +646,6 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
       record_lse<G>(a, i0, nseg, an, app, lsep, lane);
     }
     markt(22, 0);
-    // the CTA's share of the compensation sums, by the warps idle until the keys
-    if (comp && warp >= 2) comp_share<D, G>(a, i0, nseg, p, C, csh, cR, cW, tid - 64, kPT - 64);
     if (warp == 1 && lane == 0 && want_keys && nown_z > 0) {
       const uint32_t bytes = (uint32_t)nown_z * (uint32_t)Gp * 4u;
       mbar_arrive_expect_tx(bars + kPW, 2u * bytes);
@@ -719,7 +717,10 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
     mark(14);
     cluster_sync_all();  // barrier 1: every CTA's histograms are complete (and every CTA has started)
     mark(2);
-    if (warp == 0) {
+    if (warp != 0) {
+      // the CTA's share of the compensation sums, by the warps idle during the threshold search
+      if (comp) comp_share<D, G>(a, i0, nseg, p, C, csh, cR, cW, tid - 32, kPT - 32);
+    } else {
       // three levels of 16 bins over the 12-bit key prefix, each summed over the cluster
       const int3 l1 = cluster_level(h1, C, lane, need0, 0);
       markt(28, 0);
@@ -738,6 +739,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
     need = need0 - misc[kMAbove];
     take_all = misc[kMCntT] == need;
   } else {
+    if (comp) comp_share<D, G>(a, i0, nseg, p, C, csh, cR, cW, tid, kPT);
     cluster_sync_all();  // every CTA of the cluster has started before any access to a peer
   }
   mark(3);
@@ -849,8 +851,9 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
     const int64_t row = row0 + b;
     const bool cb = comp_of(b);
     __syncwarp();  // the buffer's previous contents are read
-    if (a.kv_host) {
-      // K and V in host memory: every lane copies 16-byte chunks of the block's n rows into their
+    const bool plain = a.kv_host || !a.tmap_ok;
+    if (plain) {
+      // K and V in host memory (or no tensor maps): every lane copies 16-byte chunks of the block's n rows into their
       // swizzled places (rows past n are masked for K and zeroed for V once the copies land)
       const int n = n_of(b);
       const char* kg = reinterpret_cast<const char*>(a.k + row * kBlock * D);
@@ -868,8 +871,8 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
       // ordinary stores into the buffer are ordered before the copies that overwrite it
       if (dirty) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       const uint64_t pol = policy_evict_first();
-      mbar_arrive_expect_tx(bars + warp, (a.kv_host ? 0u : 2u * (uint32_t)stg_kv(D)) + (cb ? D * 4u : 0u));
-      if (!a.kv_host) {
+      mbar_arrive_expect_tx(bars + warp, (plain ? 0u : 2u * (uint32_t)stg_kv(D)) + (cb ? D * 4u : 0u));
+      if (!plain) {
         const int y = (int)((a.layer_row0 + row) * kBlock);
 #pragma unroll
         for (int hh = 0; hh < D / 64; ++hh) {
@@ -1115,7 +1118,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
         break;
       }
       ph ^= 1u;
-      if (a.kv_host) {  // this lane's copies, then every lane's
+      if (a.kv_host || !a.tmap_ok) {  // this lane's copies, then every lane's
         cp_async_wait_all();
         __syncwarp();
       }
