@@ -18,9 +18,13 @@
 // Grid: P persistent CTAs of kWarps warps.  The layer's units are cut into
 // segments (decode_common.cuh); CTA i takes segments i, i + P, ...  Within a
 // segment, stage k (SB consecutive blocks: their kbar, vbar and Dbar rows,
-// one 1-D bulk copy each) belongs to warp k % kWarps, which owns kSlots
-// shared-memory slots and issues its own copies, so no warp waits on another
-// while the stream runs.
+// one 1-D bulk copy each) belongs to warp k % kWarps, which owns one
+// shared-memory slot and issues its own copies, so no warp waits on another
+// while the stream runs.  The kbar and Dbar rows and the vbar rows of a stage
+// arrive on two barriers: the next stage's kbar rows are in flight while the
+// warp forms this stage's compensation sums, and its vbar rows while it scores
+// the next stage.  In a call that appends, the first Q CTAs of the grid
+// recompute the units' open blocks instead (one warp per unit).
 //
 // Per stage a warp forms the SB x G partial dots q_g . kbar_b over its lanes'
 // coordinates (lane l holds coordinates CPL*l .. CPL*l + CPL - 1) and sums
@@ -61,7 +65,7 @@ __host__ __device__ inline int stream_smem_bytes(int D, int r, int G, bool score
   const int sb = stage_blocks(r, G);
   const int floats = kWarps * kSlots * stream_slot_floats(D, r, G, score, comp) + kWarps * sb * G +
                      (long_dbar(r) ? 1 : kWarps) * G * rr;
-  return floats * 4 + (3 * kMaxBatch + 8) * 4 + 8 * (kWarps * kSlots + 2) + 64;
+  return floats * 4 + (3 * kMaxBatch + 8) * 4 + 8 * (2 * kWarps * kSlots + 2) + 64;
 }
 
 // One halving step of the butterfly: N values per lane -> N/2.
@@ -296,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
   int* sbad = sseg + 1;                          // a wait of this CTA ran out
   uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(sbad + 1) + 7) & ~uintptr_t(7));
   const unsigned long long t_start = a.trace ? global_ns() : 0ull;
-  if (threadIdx.x < kWarps * kSlots) mbar_init(bars + threadIdx.x, 1);
+  if (threadIdx.x < 2 * kWarps) mbar_init(bars + threadIdx.x, 1);  // per warp: kbar/Dbar copies, vbar copies
   if (threadIdx.x == 0) {
     *sbad = 0;
     fence_mbar_init();
@@ -344,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
   const unsigned long long t_plan = a.trace ? global_ns() : 0ull;
   unsigned long long t_first = 0ull, t_r1 = 0ull, t_r2 = 0ull, t_r3 = 0ull;
   int nseg_done = 0;
-  uint32_t uses = 0;  // stages this warp has consumed: slot uses % kSlots, phase (uses / kSlots) & 1
+  uint32_t usesK = 0, usesV = 0;  // stages whose kbar/Dbar (vbar) this warp has consumed: the barriers' phases
   float* swr = sw + warp * SB * G;
   float* sqw = RB ? sqs : sqs + warp * G * rr;  // this warp's Qsq [G][rr]
   // this lane's (block, head) value of a stage
@@ -362,20 +366,31 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
     // the summaries are read once per call: evict-first in L2, so that they do not
     // push the kernels' code and the small scratch arrays out of it
     const uint64_t pol = policy_evict_first();
-    // ---- this warp's copies: its j-th stage of the segment is stage warp + kWarps j
-    auto issue = [&](int k, uint32_t use) {
-      float* st = slots + (warp * kSlots + (int)(use % kSlots)) * slot_f;
+    // ---- this warp's copies: its j-th stage of the segment is stage warp + kWarps j.  The kbar
+    // and Dbar rows and the vbar rows of a stage arrive on two barriers, so that the next stage's
+    // kbar rows are in flight while this stage's compensation sums are formed, and its vbar rows
+    // while the next stage is scored
+    float* st = slots + warp * slot_f;
+    auto issueK = [&](int k) {
       const int rb = k * SB, n = min(SB, nb - rb);
-      const uint32_t bytes = (uint32_t)n * (uint32_t)(D * 4 * (comp ? 2 : 1) + (dbulk ? r * 4 : 0));
-      uint64_t* bar = bars + warp * kSlots + (use % kSlots);
-      mbar_arrive_expect_tx(bar, bytes);
+      uint64_t* bar = bars + 2 * warp;
+      mbar_arrive_expect_tx(bar, (uint32_t)n * (uint32_t)(D * 4 + (dbulk ? r * 4 : 0)));
       bulk_g2s_hint(st, a.kbar + (row0 + rb) * D, (uint32_t)n * D * 4u, bar, pol);
-      if (comp) bulk_g2s_hint(st + SB * D, a.vbar + (row0 + rb) * D, (uint32_t)n * D * 4u, bar, pol);
       if (dbulk) bulk_g2s_hint(st + SB * D * (comp ? 2 : 1), a.dbar + (row0 + rb) * r, (uint32_t)n * r * 4u, bar, pol);
     };
+    auto issueV = [&](int k) {
+      const int rb = k * SB, n = min(SB, nb - rb);
+      uint64_t* bar = bars + 2 * warp + 1;
+      mbar_arrive_expect_tx(bar, (uint32_t)n * D * 4u);
+      bulk_g2s_hint(st + SB * D, a.vbar + (row0 + rb) * D, (uint32_t)n * D * 4u, bar, pol);
+    };
     const int mine = warp < ns ? (ns - 1 - warp) / kWarps + 1 : 0;  // stages of this warp
-    if (lane == 0)
-      for (int j = 0; j < min(kSlots, mine); ++j) issue(warp + kWarps * j, uses + j);
+    if (lane == 0 && mine > 0) {
+      // (the previous segment's record used the slots with ordinary stores)
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      issueK(warp);
+      if (comp) issueV(warp);
+    }
     // ---- queries of the unit: this lane's coordinates, scaled by 1/sqrt(d); Qsq per warp
     // (one shared copy, and a CTA barrier, for long Dbar rows)
     const float* qbase = a.q + ((int64_t)s * a.Hkv + h) * G * D;
@@ -427,18 +442,17 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
     bool bad = false;
     for (int j = 0; j < mine; ++j) {
       const int k = warp + kWarps * j;
-      const uint32_t use = uses + j;
-      const float* st = slots + (warp * kSlots + (int)(use % kSlots)) * slot_f;
       const float* skb = st;
       const float* svb = st + SB * D;
       float* sdb = const_cast<float*>(st) + SB * D * (comp ? 2 : 1);
       const int rb = k * SB, nbs = min(SB, nb - rb);
       if (SCORE && !dbulk && lane < nbs * r)  // r < 4: the Dbar rows by plain loads, 4 floats per row
         sdb[(lane / r) * 4 + lane % r] = __ldcg(a.dbar + (row0 + rb) * r + lane);
-      if (!mbar_wait_bounded(bars + warp * kSlots + (use % kSlots), (use / kSlots) & 1u, a.status, s, h, 10)) {
+      if (!mbar_wait_bounded(bars + 2 * warp, usesK & 1u, a.status, s, h, 10)) {
         bad = true;
         break;
       }
+      ++usesK;
       __syncwarp();
       // zbar partial dots of the stage's SB blocks and G heads
       float p[NV];
@@ -558,6 +572,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
           swr[vb * G + vg] = w;
           wsl += w;
         }
+      }
+      __syncwarp();  // the kbar and Dbar rows are read (and the weights written): the next stage's may come
+      if (lane == 0 && j + 1 < mine) issueK(k + kWarps);
+      if (comp) {
+        if (!mbar_wait_bounded(bars + 2 * warp + 1, usesV & 1u, a.status, s, h, 11)) {
+          bad = true;
+          break;
+        }
+        ++usesV;
         __syncwarp();
         for (int b = 0; b < nbs; ++b) {
           float x[CPL], wv[G];
@@ -569,15 +592,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
 #pragma unroll
             for (int c = 0; c < CPL; ++c) acc[g][c] = fmaf(wv[g], x[c], acc[g][c]);
         }
+        __syncwarp();  // the vbar rows and the weights are read
+        if (lane == 0 && j + 1 < mine) issueV(k + kWarps);
       }
-      __syncwarp();  // the slot and the weights are read
-      if (lane == 0 && j + kSlots < mine) issue(k + kWarps * kSlots, use + kSlots);
     }
     if (bad) {
-      for (int i = 0; i < kSlots; ++i) mbar_drain_bounded(bars + warp * kSlots + i);
+      mbar_drain_bounded(bars + 2 * warp);
+      mbar_drain_bounded(bars + 2 * warp + 1);
       if (lane == 0) *sbad = 1;
     }
-    uses += (uint32_t)mine;
     __syncthreads();  // every stage of the segment is consumed: the slots are free
     if (!nseg_done && a.trace) t_first = global_ns();
     ++nseg_done;
