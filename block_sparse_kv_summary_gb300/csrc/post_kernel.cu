@@ -253,17 +253,27 @@ __device__ __forceinline__ void record_lse(const LayerArgs& a, int i0, int nseg,
       const int idx = k0 + lane + 32 * j;
       e[j] = idx < tot ? __ldcg(base + idx) : make_float4(-INFINITY, 0.f, 0.f, 0.f);
     }
+    // the eight parts at their common maximum: independent exponentials instead of a chain of merges
+    float mc = e[0].x;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) lse_merge(M, S, e[j].x, e[j].y);
+    for (int j = 1; j < 8; ++j) mc = fmaxf(mc, e[j].x);
+    float sc = 0.f;
+    if (mc != -INFINITY) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sc += e[j].x == -INFINITY ? 0.f : e[j].y * __expf(e[j].x - mc);
+    }
+    lse_merge(M, S, mc, sc);
   }
-#pragma unroll 1
-  for (int o = G; o < 32; o <<= 1) {
-    const float M2 = __shfl_xor_sync(0xffffffffu, M, o), S2 = __shfl_xor_sync(0xffffffffu, S, o);
-    lse_merge(M, S, M2, S2);
-  }
+  // across the lanes of a head: the maximum, then the sums rescaled to it
+  float Mw = M;
+#pragma unroll
+  for (int o = G; o < 32; o <<= 1) Mw = fmaxf(Mw, __shfl_xor_sync(0xffffffffu, Mw, o));
+  float Sw = M == -INFINITY ? 0.f : S * __expf(M - Mw);
+#pragma unroll
+  for (int o = G; o < 32; o <<= 1) Sw += __shfl_xor_sync(0xffffffffu, Sw, o);
   if (lane < G) {  // LSE_g, with the open block's a_g (`an`, lane g) when this call appended
-    if (app) lse_merge(M, S, an, 1.f);
-    lsep[lane] = M + __logf(S);
+    if (app) lse_merge(Mw, Sw, an, 1.f);
+    lsep[lane] = Mw + __logf(Sw);
   }
 }
 
@@ -548,6 +558,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
   uint64_t* bars = reinterpret_cast<uint64_t*>(psm + lay.bars);  // [kPW] attention, [1] zbar/sigma2 copy
   const unsigned long long t_start = a.trace ? global_ns() : 0ull;
   unsigned long long t_wait = 0ull;
+
   // phase marks of the work-item trace: mark k goes to record 1 + k / 7, slot 1 + k % 7
   // (kept in shared memory until the end, so that no global store waits in a fence)
   __shared__ unsigned long long tmk[35];
@@ -694,6 +705,20 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
   }
   mark(1);
 
+  // After barrier 1 every CTA of this cluster has read seq_len (the set-up does); the last
+  // cluster to get there writes the lengths after this call's append (a sequence at capacity
+  // keeps its own).  One thread of rank 0, off the threshold search's path.
+  auto seq_arrive = [&]() {
+    if (atomicAdd(a.arrive, 1) == (int)(gridDim.x / C) - 1) {
+#pragma unroll 1
+      for (int x = 0; x < a.B; ++x) {
+        const bool f = ((x < 32 ? misc[kMFits] >> x : misc[kMFits + 1] >> (x - 32)) & 1) != 0;
+        if (f) a.seq_len[x] = sL[x];
+      }
+      a.arrive[0] = 0;
+    }
+  };
+
   // ---- the threshold bin T: the histograms summed across the cluster
   uint32_t T = 0xFFFFFFFFu;
   int need = 0;
@@ -720,6 +745,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
     if (warp != 0) {
       // the CTA's share of the compensation sums, by the warps idle during the threshold search
       if (comp) comp_share<D, G>(a, i0, nseg, p, C, csh, cR, cW, tid - 32, kPT - 32);
+      if (APPEND && p == 0 && tid == 32) seq_arrive();
     } else {
       // three levels of 16 bins over the 12-bit key prefix, each summed over the cluster
       const int3 l1 = cluster_level(h1, C, lane, need0, 0);
@@ -741,6 +767,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
   } else {
     if (comp) comp_share<D, G>(a, i0, nseg, p, C, csh, cR, cW, tid, kPT);
     cluster_sync_all();  // every CTA of the cluster has started before any access to a peer
+    if (APPEND && p == 0 && tid == 0) seq_arrive();
   }
   mark(3);
 
@@ -969,18 +996,24 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
         for (int j = 0; j < 4; ++j)
           if (td[j] >= 0) dense[td[j]] = tv[j];
         __syncthreads();
-#pragma unroll 1
-        for (int j = warp; j < nt_all; j += kPW) {
-          const uint2 me = dense[j];
-          int rank = 0;
-#pragma unroll 1
-          for (int j2 = lane; j2 < nt_all; j2 += 32) {
+        // entry j by a group of tpe consecutive threads (the most that fit, up to a warp), which
+        // split the comparisons; its rank is the count of entries ahead of it
+        int tpe = 1;
+        while (tpe < 32 && nt_all * 2 * tpe <= kPT) tpe <<= 1;
+        const int j = tid / tpe, part = tid % tpe;
+        const bool live = j < nt_all;
+        const uint2 me = live ? dense[j] : make_uint2(0u, 0u);
+        int rank = 0;
+        if (live) {
+#pragma unroll 4
+          for (int j2 = part; j2 < nt_all; j2 += tpe) {
             const uint2 o = dense[j2];
             rank += (o.x > me.x) || (o.x == me.x && o.y < me.y);
           }
-          rank = __reduce_add_sync(0xffffffffu, rank);
-          if (lane == 0 && rank < need) win[rank] = (int)me.y;
         }
+#pragma unroll 1
+        for (int o = 1; o < tpe; o <<= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
+        if (live && part == 0 && rank < need) win[rank] = (int)me.y;
         nwin = need;
         __syncthreads();
       }
@@ -1076,30 +1109,32 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
   bool have = b_cur >= 0;
   if (ATT && !have) have = fetch();
   if (SEL) {
-    // the ascending selection: this CTA's blocks and the tie winners among them, merged
+    // the ascending selection from own_base on: this CTA's sure blocks, and the tie winners among
+    // its blocks
     int* selrow = a.sel + (int64_t)u * K;
+    if (nwin > 0) {
+      // both as one bitmap of the CTA's blocks (in the fine histogram's place, which no peer
+      // reads after barrier 2), listed in ascending order by warp 0
+      if (warp == 0) {
+        unsigned* bits = hf;
+        const int nwd = (nown + 31) / 32;
 #pragma unroll 1
-    for (int e = tid; e < n_own; e += kPT) {
-      const int b = own[e];
-      int pos = own_base + e;
+        for (int w = lane; w < nwd; w += 32) bits[w] = 0u;
+        __syncwarp();
 #pragma unroll 1
-      for (int k = 0; k < nwin; ++k) pos += (win[k] >= b_lo && win[k] < b);
-      if (pos < K) selrow[pos] = b;
-    }
+        for (int e = lane; e < n_own; e += 32) atomicOr(&bits[(own[e] - b_lo) >> 5], 1u << ((own[e] - b_lo) & 31));
 #pragma unroll 1
-    for (int k = tid; k < nwin; k += kPT) {
-      const int b = win[k];
-      if (b < b_lo || b >= b_hi) continue;
-      int lo = 0, hi = n_own;  // own blocks below b (the list is ascending)
-#pragma unroll 1
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (own[mid] < b) lo = mid + 1; else hi = mid;
+        for (int k = lane; k < nwin; k += 32) {
+          const int b = win[k];
+          if (b >= b_lo && b < b_hi) atomicOr(&bits[(b - b_lo) >> 5], 1u << ((b - b_lo) & 31));
+        }
+        __syncwarp();
+        bitmap_list(bits, nwd, b_lo, selrow + own_base, K - own_base, lane);
       }
-      int pos = own_base + lo;
+    } else {
 #pragma unroll 1
-      for (int k2 = 0; k2 < nwin; ++k2) pos += (win[k2] >= b_lo && win[k2] < b);
-      if (pos < K) selrow[pos] = b;
+      for (int e = tid; e < n_own; e += kPT)
+        if (own_base + e < K) selrow[own_base + e] = own[e];
     }
     if (p == 0) {
 #pragma unroll 1
@@ -1211,19 +1246,6 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
   mark(11);
   cluster_sync_all();  // barrier 3: every partial of this rank's columns is here; no CTA touches a peer after this
   mark(12);
-  if (APPEND && p == 0 && tid == 0) {
-    // every CTA of this cluster has read seq_len; the last cluster to get here
-    // writes the lengths after this call's append (a sequence at capacity keeps its own)
-    // (each cluster's reads of seq_len were consumed long before its increment)
-    if (atomicAdd(a.arrive, 1) == (int)(gridDim.x / C) - 1) {
-#pragma unroll 1
-      for (int x = 0; x < a.B; ++x) {
-        const bool f = ((x < 32 ? misc[kMFits] >> x : misc[kMFits + 1] >> (x - 32)) & 1) != 0;
-        if (f) a.seq_len[x] = sL[x];
-      }
-      a.arrive[0] = 0;
-    }
-  }
   // this rank's column items: Cp (C rounded up to a power of two) lanes per item, lane q
   // takes CTA q's partial; the partials are merged across those lanes
   {
