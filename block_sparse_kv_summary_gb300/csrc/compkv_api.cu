@@ -434,7 +434,14 @@ compkv_status compkv_init(const compkv_config* cfg, const compkv_buffers* bufs, 
       return st;
     }
   }
-  cudaError_t e = cudaMemsetAsync(bufs->scratch, 0, L.total, 0);
+  // the kernels' shared memory limits and cluster size, once for this configuration
+  cudaError_t e = prepare_stream(cfg->head_dim, cfg->r, cfg->group_size);
+  if (e == cudaSuccess) e = prepare_post(cfg->head_dim, cfg->group_size, L.C, L.bpc_max, L.K);
+  if (e != cudaSuccess) {
+    delete c;
+    return cuda_status(e, "setting the kernels' attributes");
+  }
+  e = cudaMemsetAsync(bufs->scratch, 0, L.total, 0);
   if (e == cudaSuccess) e = cudaStreamSynchronize(0);
   if (e != cudaSuccess) {
     delete c;

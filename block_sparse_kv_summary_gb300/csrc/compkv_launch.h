@@ -50,6 +50,20 @@ inline void chain_split(LayerArgs& a, int mode) {
 cudaError_t launch_stream(const LayerArgs& a, int mode, cudaStream_t st, bool pdl);
 cudaError_t launch_post(const LayerArgs& a, int mode, cudaStream_t st);
 
+// Function attributes the launches need, set once per context (compkv_init) instead of on
+// every launch: the dynamic shared memory limit of every mode's stream and post kernel raised
+// (never lowered: another context may need more) to this configuration's, and clusters of
+// more than 8 CTAs allowed.
+inline cudaError_t raise_smem_limit(const void* fn, int smem) {
+  cudaFuncAttributes at;
+  cudaError_t e = cudaFuncGetAttributes(&at, fn);
+  if (e != cudaSuccess) return e;
+  if (at.maxDynamicSharedSizeBytes >= smem) return cudaSuccess;
+  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+}
+cudaError_t prepare_stream(int D, int r, int G);
+cudaError_t prepare_post(int D, int G, int C, int bpc_max, int K);
+
 // Dynamic shared memory of the two kernels.
 size_t stream_smem(int D, int r, int G);
 size_t post_smem(int D, int G, int C, int bpc_max, int K);

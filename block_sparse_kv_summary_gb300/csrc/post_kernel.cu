@@ -4,26 +4,23 @@
 // One thread-block cluster of C CTAs per (sequence, KV head) unit.  CTA rank p
 // owns the unit's blocks [p bpc, (p + 1) bpc) (bpc = ceil(N / C) rounded up
 // to 4) and, of the stream's segment records, those with index = p (mod C).
-//   a. The last warp recomputes the summary of the open block, which this
-//      call's token joins: every CTA its a_g = ln|b| + zbar + sigma2/2 for the
-//      normaliser, and the CTA that owns the block also writes the token and
-//      the block's summary rows.  Meanwhile warp 0 merges the segment records
-//      into LSE_g and warp 1 copies the CTA's zbar and sigma2 rows.
+//   a. After the stream: warp 0 merges the unit's segment records and the
+//      open block's a_g (which the stream kernel recomputed) into LSE_g, and
+//      warp 1 copies the CTA's zbar and sigma2 rows.
 //   b. S_b = sum_g phat_{g,b} sigma2_{g,b} ("무엇과 다른가") of the CTA's blocks
-//      as order-preserving keys and their 12-bit histogram (candidates
-//      1..N-3), summed across the cluster in distributed shared memory
-//      (exponent counts at rank 0, the 16 fine bins of exponent e at rank
-//      e % C); one warp finds the threshold bin T where the count of larger
-//      keys reaches K - 3 (the forced sink block and the two most recent
-//      blocks take the other three places of the budget).
+//      as order-preserving keys and a 12-bit histogram of the candidates
+//      1..N-3.  After a cluster barrier, warp 0 of every CTA reads the peers'
+//      counts in three levels of 16 bins and finds the threshold bin T where
+//      the count of larger keys reaches K - 3 (the forced sink block and the
+//      two most recent blocks take the other three places of the budget).
 //   c. Blocks above T, and the forced ones, are selected for sure: each CTA
-//      lists its own in ascending order and pushes its count, and the keys of
-//      its blocks in T when T must be ranked, to every peer.  Its warps start
-//      on the top eight of its own list at once, while that exchange settles.
-//   d. After the exchange every CTA ranks the keys in T (ties to the lower
-//      block index) and spreads the rest of the work -- own lists longer than
-//      eight and the tie winners -- over the warps left idle, in one order
-//      that every CTA derives alike.
+//      lists its own in ascending order, and the keys of its blocks in T,
+//      for the peers to read after a second cluster barrier.  Its warps start
+//      on the top eight of its own list before that barrier completes.
+//   d. After the barrier every CTA reads the peers' counts and tie lists,
+//      ranks the keys in T (ties to the lower block index) and spreads the
+//      rest of the work -- own lists longer than eight and the tie winners --
+//      over the warps left idle, in one order that every CTA derives alike.
 //   e. A warp attends exactly to one block's bf16 K/V at a time with
 //      tensor-core products (q and the probabilities split into bf16 high and
 //      low parts, fp32 accumulation) and removes the block's own
@@ -1318,10 +1315,8 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
 template <int D, int G, int MODE>
 static cudaError_t launch_post_mode(const LayerArgs& a, cudaStream_t st) {
   const void* fn = reinterpret_cast<const void*>(&k_post<D, G, MODE>);
+  // (shared memory limit and cluster size allowed by prepare_post)
   const size_t smem = (size_t)post_layout(D, G, a.C, a.bpc_max, a.K).total * 4;
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  if (a.C > 8 && (e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess) return e;
   LayerArgs args = a;
   chain_split(args, MODE);
   void* argv[] = {&args};
@@ -1370,5 +1365,38 @@ cudaError_t launch_post(const LayerArgs& a, int mode, cudaStream_t st) {
 }
 
 size_t post_smem(int D, int G, int C, int bpc_max, int K) { return (size_t)post_layout(D, G, C, bpc_max, K).total * 4; }
+
+template <int D, int G, int MODE>
+static cudaError_t prepare_post_mode(int C, int bpc_max, int K) {
+  const void* fn = reinterpret_cast<const void*>(&k_post<D, G, MODE>);
+  cudaError_t e = raise_smem_limit(fn, post_layout(D, G, C, bpc_max, K).total * 4);
+  if (e == cudaSuccess && C > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
+}
+
+template <int D, int G>
+static cudaError_t prepare_post_dg(int C, int bpc_max, int K) {
+  cudaError_t e = prepare_post_mode<D, G, kFusedDecode>(C, bpc_max, K);
+  if (e == cudaSuccess) e = prepare_post_mode<D, G, kFusedScoreSelect>(C, bpc_max, K);
+  if (e == cudaSuccess) e = prepare_post_mode<D, G, kFusedAttend>(C, bpc_max, K);
+  return e;
+}
+
+cudaError_t prepare_post(int D, int G, int C, int bpc_max, int K) {
+#define COMPKV_G(DD)                                        \
+  switch (G) {                                              \
+    case 1: return prepare_post_dg<DD, 1>(C, bpc_max, K);   \
+    case 2: return prepare_post_dg<DD, 2>(C, bpc_max, K);   \
+    case 4: return prepare_post_dg<DD, 4>(C, bpc_max, K);   \
+    case 8: return prepare_post_dg<DD, 8>(C, bpc_max, K);   \
+    default: return cudaErrorInvalidValue;                  \
+  }
+  if (D == 128) {
+    COMPKV_G(128)
+  } else {
+    COMPKV_G(64)
+  }
+#undef COMPKV_G
+}
 
 }  // namespace compkv

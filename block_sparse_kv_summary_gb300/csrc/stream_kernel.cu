@@ -698,9 +698,7 @@ static cudaError_t launch_stream_mode(const LayerArgs& a, cudaStream_t st, bool 
   constexpr bool SCORE = (MODE & kFScore) != 0;
   constexpr bool COMP = (MODE & kFComp) != 0;
   const void* fn = stream_fn<D, G, MODE>(a.r);
-  const size_t smem = (size_t)stream_smem_bytes(D, a.r, G, SCORE, COMP);
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  const size_t smem = (size_t)stream_smem_bytes(D, a.r, G, SCORE, COMP);  // (limit raised by prepare_stream)
   LayerArgs args = a;
   chain_split(args, MODE);
   void* argv[] = {&args};
@@ -772,5 +770,37 @@ cudaError_t launch_stream(const LayerArgs& a, int mode, cudaStream_t st, bool pd
 }
 
 size_t stream_smem(int D, int r, int G) { return (size_t)stream_smem_bytes(D, r, G, true, true); }
+
+template <int D, int G, int MODE>
+static cudaError_t prepare_stream_mode(int r) {
+  constexpr bool SCORE = (MODE & kFScore) != 0;
+  constexpr bool COMP = (MODE & kFComp) != 0;
+  return raise_smem_limit(stream_fn<D, G, MODE>(r), stream_smem_bytes(D, r, G, SCORE, COMP));
+}
+
+template <int D, int G>
+static cudaError_t prepare_stream_dg(int r) {
+  cudaError_t e = prepare_stream_mode<D, G, kFusedDecode>(r);
+  if (e == cudaSuccess) e = prepare_stream_mode<D, G, kFusedScoreSelect>(r);
+  if (e == cudaSuccess) e = prepare_stream_mode<D, G, kFusedAttend>(r);
+  return e;
+}
+
+cudaError_t prepare_stream(int D, int r, int G) {
+#define COMPKV_G(DD)                             \
+  switch (G) {                                   \
+    case 1: return prepare_stream_dg<DD, 1>(r);  \
+    case 2: return prepare_stream_dg<DD, 2>(r);  \
+    case 4: return prepare_stream_dg<DD, 4>(r);  \
+    case 8: return prepare_stream_dg<DD, 8>(r);  \
+    default: return cudaErrorInvalidValue;       \
+  }
+  if (D == 128) {
+    COMPKV_G(128)
+  } else {
+    COMPKV_G(64)
+  }
+#undef COMPKV_G
+}
 
 }  // namespace compkv
