@@ -722,6 +722,11 @@ compkv_status compkv_internal_decode_in(const compkv_config* cfg, const compkv_b
   c.buf.scratch_bytes = scratch_bytes;
   c.lay = L;
   COMPKV_TRY(make_tensor_maps(&c));
+  // no context was initialised for this configuration: the kernels' attributes on every call
+  // (queries, and a set only where a limit is still too low)
+  cudaError_t ea = prepare_stream(cfg->head_dim, cfg->r, cfg->group_size);
+  if (ea == cudaSuccess) ea = prepare_post(cfg->head_dim, cfg->group_size, L.C, L.bpc_max, L.K);
+  COMPKV_TRY(cuda_status(ea, "setting the kernels' attributes"));
   cudaStream_t st = (cudaStream_t)stream;
   COMPKV_TRY(cuda_status(cudaMemsetAsync(scratch, 0, L.off_rec, st), "clearing scratch"));
   LayerArgs a = base_args(&c, layer);

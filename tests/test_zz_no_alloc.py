@@ -78,3 +78,51 @@ def test_static_scratch_rejects_a_configuration_that_does_not_fit():
     bufs = C.compkv_buffers(256, 256, 256, 256, 256, 256, 0, 0)
     with pytest.raises(C.CompKVError, match="static scratch holds"):
         C.compkv_decode_static(cfg, bufs, 0, 256, 256, 256, 256, 0, None)
+
+
+_FRESH = r'''
+import sys, torch
+sys.path.insert(0, sys.argv[1])
+import block_sparse_kv_summary_gb300 as P
+from block_sparse_kv_summary_gb300 import compkv as C
+P.lib()
+# no context is ever initialised in this process: the entry point sets up the kernels itself
+d, G = 128, 4
+cfg = C.make_config(1, 1, 1, G, d, 4, 2048, capacity_tokens=[4096])
+rows = C.compkv_rows_per_layer(cfg)
+dev = torch.device("cuda", 0)
+k = torch.zeros((rows, 16, d), dtype=torch.bfloat16, device=dev)
+v = torch.zeros((rows, 16, d), dtype=torch.bfloat16, device=dev)
+kbar = torch.zeros((rows, d), dtype=torch.float32, device=dev)
+vbar = torch.zeros((rows, d), dtype=torch.float32, device=dev)
+dbar = torch.zeros((rows, 4), dtype=torch.float32, device=dev)
+seq_len = torch.zeros((1, 1), dtype=torch.int32, device=dev)
+bufs = C.compkv_buffers(k.data_ptr(), v.data_ptr(), kbar.data_ptr(), vbar.data_ptr(), dbar.data_ptr(),
+                        seq_len.data_ptr(), 0, 0)
+g = torch.Generator().manual_seed(7)
+q = torch.randn((1, G, d), generator=g).to(dev)
+k_new = torch.randn((1, 1, d), generator=g).to(torch.bfloat16).to(dev)
+v_new = torch.randn((1, 1, d), generator=g).to(torch.bfloat16).to(dev)
+out = torch.full((1, G, d), float("nan"), device=dev)
+sel = torch.full((1, 1, 128), -7, dtype=torch.int32, device=dev)
+C.compkv_decode_static(cfg, bufs, 0, q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), out.data_ptr(),
+                       sel.data_ptr(), torch.cuda.current_stream().cuda_stream)
+torch.cuda.synchronize()
+# one token in the cache: softmax over it is 1, so every head's output is its value row
+want = v_new[0, 0].float().expand(G, d)
+assert torch.equal(out[0], want), (out[0] - want).abs().max().item()
+assert sel[0, 0, 0].item() == 0 and bool((sel[0, 0, 1:] == -1).all())
+assert seq_len.item() == 1
+print("fresh process ok")
+'''
+
+
+def test_static_scratch_in_a_process_without_a_context():
+    # compkv_decode_static must work as the first and only call of a process: it sets the
+    # kernels' shared-memory limits itself (compkv_init does this for the other entry points)
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FRESH, root], capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0 and "fresh process ok" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
