@@ -146,8 +146,11 @@ int64_t compkv_rows_per_layer(const compkv_config *cfg);
 size_t compkv_scratch_bytes(const compkv_config *cfg);
 
 /* Validate cfg and bufs, zero the scratch (synchronously) and create a context.
- * The library keeps the pointers; the caller keeps ownership of every buffer
- * and must keep them alive until compkv_destroy. */
+ * It also sets, on the current device, the decode kernels' dynamic
+ * shared-memory limits (raised, never lowered) and permission for clusters of
+ * more than 8 CTAs, so that calls launch without those driver calls.  The
+ * library keeps the pointers; the caller keeps ownership of every buffer and
+ * must keep them alive until compkv_destroy. */
 compkv_status compkv_init(const compkv_config *cfg, const compkv_buffers *bufs, compkv_ctx **out);
 
 /* First row of (layer, seq, head) and that sequence's capacity in blocks. */
