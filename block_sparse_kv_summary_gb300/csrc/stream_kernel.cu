@@ -274,12 +274,13 @@ __device__ __noinline__ void open_block_warp(const LayerArgs& a, int u, int lane
   }
 }
 
-template <int D, int G, int MODE, int SB, bool RB>
+template <int D, int G, int MODE, int SB, int RPL>
 __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
   constexpr bool APPEND = (MODE & kFAppend) != 0;
   constexpr bool SCORE = (MODE & kFScore) != 0;
   constexpr bool COMP = (MODE & kFComp) != 0;
   constexpr bool SELMODE = (MODE & kFSelect) != 0;
+  constexpr bool RB = RPL > 0;                // long Dbar rows: r = 32 RPL coordinates, RPL per lane
   constexpr int CPL = D / 32;
   constexpr int NV = SB * G;                  // (block, head) values of a stage
   constexpr int SH = ilog2(32 / NV);          // lanes per value = 1 << SH
@@ -480,21 +481,25 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
       float s2 = 0.f;
       if (SCORE) {
         if constexpr (RB) {
-          // long Dbar rows (r >= 64): lane holds Dbar coordinates [rpl*lane, rpl*lane + rpl)
-          const int rpl = r / 32;
+          // long Dbar rows (r = 32 RPL): lane holds Dbar and Qsq coordinates [RPL lane, RPL lane + RPL),
+          // read as one RPL-float vector each (no bank conflicts)
           float ps[NV];
 #pragma unroll
           for (int b = 0; b < SB; ++b) {
-            const float* drow = sdb + b * rs;
-            float x[4];
+            float x[RPL];
+            if (b < nbs) {  // (warp-uniform)
+              lds_vec<RPL>(sdb + b * rs + RPL * lane, x);
+            } else {
 #pragma unroll
-            for (int t = 0; t < 4; ++t) x[t] = (t < rpl && b < nbs) ? drow[rpl * lane + t] : 0.f;
+              for (int t = 0; t < RPL; ++t) x[t] = 0.f;
+            }
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-              float t = 0.f;
+              float w[RPL];
+              lds_vec<RPL>(sqw + g * rr + RPL * lane, w);
+              float t = w[0] * x[0];
 #pragma unroll
-              for (int c = 0; c < 4; ++c)
-                if (c < rpl) t = fmaf(sqw[g * rr + rpl * lane + c], x[c], t);
+              for (int c = 1; c < RPL; ++c) t = fmaf(w[c], x[c], t);
               ps[b * G + g] = t;
             }
           }
@@ -689,8 +694,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
 
 template <int D, int G, int MODE>
 static const void* stream_fn(int r) {
-  if (long_dbar(r)) return reinterpret_cast<const void*>(&k_stream<D, G, MODE, 4, true>);
-  return reinterpret_cast<const void*>(&k_stream<D, G, MODE, (G >= 8 ? 4 : 8), false>);
+  if constexpr (D >= 128)
+    if (r >= 128) return reinterpret_cast<const void*>(&k_stream<D, G, MODE, 4, 4>);
+  if (long_dbar(r)) return reinterpret_cast<const void*>(&k_stream<D, G, MODE, 4, 2>);
+  return reinterpret_cast<const void*>(&k_stream<D, G, MODE, (G >= 8 ? 4 : 8), 0>);
 }
 
 template <int D, int G, int MODE>
