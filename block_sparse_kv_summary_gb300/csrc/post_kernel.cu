@@ -520,7 +520,57 @@ __device__ __noinline__ void refine_select(const uint32_t* keys, unsigned* bits,
   }
 }
 
-template <int D, int G, int MODE>
+// A block's K and V rows by 16-byte asynchronous copies of every lane into their swizzled places
+// (K and V in host memory, or no tensor maps), out of line: the tensor copies are the common case.
+template <int D>
+__device__ __noinline__ void plain_copy(char* stg, const char* kg, const char* vg, int n, int lane) {
+#pragma unroll 1
+  for (int x = lane; x < n * (D / 8); x += 32) {
+    const int t = x / (D / 8), j = x % (D / 8);
+    const int so = (j >> 3) * kBlock * 128 + t * 128 + (((j & 7) ^ (t & 7)) << 4);
+    cp_async16(stg + so, kg + x * 16);
+    cp_async16(stg + stg_kv(D) + so, vg + x * 16);
+  }
+  cp_async_commit();
+}
+
+// The rare path as a whole (more candidates share bin T than the tie lists hold), by every
+// thread of every CTA of the cluster, out of line so that its code stays out of the common
+// path's: the own list with the sure blocks, refined by more radix digits (refine_select)
+// and listed again; the CTAs' counts exchanged.  Returns (own count, this CTA's offset in the
+// ascending selection, the selection's size).
+__device__ __noinline__ int3 rare_select(const uint32_t* keys, unsigned* bits, int* own, int n_own, int nown, int b_lo,
+                                         int N, int K, uint32_t T, int need, uint32_t* xref, uint32_t* lh, int* misc,
+                                         int C, int p) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nwo = (nown + 31) / 32;
+#pragma unroll 1
+  for (int w = tid; w < nwo; w += kPT) bits[w] = 0u;
+  __syncthreads();
+#pragma unroll 1
+  for (int e = tid; e < n_own; e += kPT) atomicOr(&bits[(own[e] - b_lo) >> 5], 1u << ((own[e] - b_lo) & 31));
+  __syncthreads();
+  refine_select(keys, bits, nown, b_lo, N, T, need, xref, lh, misc, C, p);
+  if (warp == 0) {
+    const int nl = bitmap_list(bits, nwo, b_lo, own, nown < K ? nown : K, lane);
+    if (lane == 0) misc[kMOwn] = nl;
+  }
+  __syncthreads();
+  n_own = min(misc[kMOwn], nown < K ? nown : K);
+  if (tid < C) st_peer_u32(peer_smem(misc + kMCntA + p, (uint32_t)tid), (uint32_t)n_own);
+  cluster_sync_all();
+  int before = 0, all = 0;
+#pragma unroll 1
+  for (int q = 0; q < C; ++q) {
+    before += q < p ? misc[kMCntA + q] : 0;
+    all += misc[kMCntA + q];
+  }
+  return make_int3(n_own, before, all);
+}
+
+// TRACE: the work-item trace is recorded (a.trace is set); the instance without it carries no
+// trace code, which matters here because this kernel's code runs once per call.
+template <int D, int G, int MODE, bool TRACE>
 __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerArgs a) {
   constexpr bool APPEND = (MODE & kFAppend) != 0;
   constexpr bool SEL = (MODE & kFSelect) != 0;
@@ -553,15 +603,15 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
   float* lsep = psm + lay.lsep;
   float* csh = psm + lay.csh;
   uint64_t* bars = reinterpret_cast<uint64_t*>(psm + lay.bars);  // [kPW] attention, [1] zbar/sigma2 copy
-  const unsigned long long t_start = a.trace ? global_ns() : 0ull;
+  const unsigned long long t_start = TRACE ? global_ns() : 0ull;
   unsigned long long t_wait = 0ull;
 
   // phase marks of the work-item trace: mark k goes to record 1 + k / 7, slot 1 + k % 7
   // (kept in shared memory until the end, so that no global store waits in a fence)
   __shared__ unsigned long long tmk[35];
-  if (a.trace && tid < 35) tmk[tid] = 0ull;
+  if (TRACE && tid < 35) tmk[tid] = 0ull;
   auto markt = [&](int k, int t) {
-    if (a.trace && tid == t) tmk[k] = global_ns();
+    if (TRACE && tid == t) tmk[k] = global_ns();
   };
   auto mark = [&](int k) { markt(k, 0); };
 
@@ -648,7 +698,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
   // sigma2 rows (warp 1), the compensation share (warps 2..)
   {
     pdl_wait();  // the stream kernel's records, zbar and sigma2 are complete and visible
-    if (a.trace && tid == 0) t_wait = global_ns();
+    if (TRACE && tid == 0) t_wait = global_ns();
     if (warp == 0 && want_keys) {
       const float an = (app && lane < G) ? __ldcg(a.anm + (int64_t)u * G + lane) : -INFINITY;
       record_lse<G>(a, i0, nseg, an, app, lsep, lane);
@@ -879,17 +929,8 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
     if (plain) {
       // K and V in host memory (or no tensor maps): every lane copies 16-byte chunks of the block's n rows into their
       // swizzled places (rows past n are masked for K and zeroed for V once the copies land)
-      const int n = n_of(b);
-      const char* kg = reinterpret_cast<const char*>(a.k + row * kBlock * D);
-      const char* vg = reinterpret_cast<const char*>(a.v + row * kBlock * D);
-#pragma unroll 1
-      for (int x = lane; x < n * (D / 8); x += 32) {
-        const int t = x / (D / 8), j = x % (D / 8);
-        const int so = (j >> 3) * kBlock * 128 + t * 128 + (((j & 7) ^ (t & 7)) << 4);
-        cp_async16(stg + so, kg + x * 16);
-        cp_async16(stg + stg_kv(D) + so, vg + x * 16);
-      }
-      cp_async_commit();
+      plain_copy<D>(stg, reinterpret_cast<const char*>(a.k + row * kBlock * D),
+                    reinterpret_cast<const char*>(a.v + row * kBlock * D), n_of(b), lane);
     }
     if (lane == 0) {
       // ordinary stores into the buffer are ordered before the copies that overwrite it
@@ -1025,31 +1066,11 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
       own_base = opre_p + __reduce_add_sync(0xffffffffu, below);
     } else {
       // rare: resolve bin T by more radix digits; every CTA attends its own winners itself
-      unsigned* bits = reinterpret_cast<unsigned*>(dense);
-      const int nwo = (nown + 31) / 32;
-#pragma unroll 1
-      for (int w = tid; w < nwo; w += kPT) bits[w] = 0u;
-      __syncthreads();
-#pragma unroll 1
-      for (int e = tid; e < n_own; e += kPT) atomicOr(&bits[(own[e] - b_lo) >> 5], 1u << ((own[e] - b_lo) & 31));
-      __syncthreads();
-      refine_select(keys, bits, nown, b_lo, N, T, need, xref, lh, misc, C, p);
-      if (warp == 0) {
-        const int nl = bitmap_list(bits, nwo, b_lo, own, nown < K ? nown : K, lane);
-        if (lane == 0) misc[kMOwn] = nl;
-      }
-      __syncthreads();
-      n_own = min(misc[kMOwn], nown < K ? nown : K);
-      if (tid < C) st_peer_u32(peer_smem(misc + kMCntA + p, (uint32_t)tid), (uint32_t)n_own);
-      cluster_sync_all();
-      int before = 0, all = 0;
-#pragma unroll 1
-      for (int q = 0; q < C; ++q) {
-        before += q < p ? misc[kMCntA + q] : 0;
-        all += misc[kMCntA + q];
-      }
-      own_base = before;
-      tot_sel = all;
+      const int3 rr = rare_select(keys, reinterpret_cast<unsigned*>(dense), own, n_own, nown, b_lo, N, K, T, need,
+                                  xref, lh, misc, C, p);
+      n_own = rr.x;
+      own_base = rr.y;
+      tot_sel = rr.z;
       mark(7);
     }
   } else if (SEL) {
@@ -1160,11 +1181,11 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
       have = fetch();
     }
   }
-  const unsigned long long t_sel = a.trace ? global_ns() : 0ull;
+  const unsigned long long t_sel = TRACE ? global_ns() : 0ull;
   if (SEL && !ATT) {
     // score/select only: no peer reads this CTA's shared memory after the barrier
     cluster_sync_all();
-    if (tid == 0 && a.trace && a.Q + a.P + (int)blockIdx.x < a.trace_cap) {
+    if (TRACE && tid == 0 && a.Q + a.P + (int)blockIdx.x < a.trace_cap) {
       unsigned long long* rr = a.trace + 1 + 8 * (int64_t)(a.Q + a.P + blockIdx.x);
       rr[0] = ((unsigned long long)blockIdx.x << 32) | (1ull << 24) | (unsigned)p;
       rr[1] = (unsigned long long)u; rr[2] = t_start; rr[3] = t_wait; rr[4] = t_sel; rr[5] = t_sel;
@@ -1289,7 +1310,7 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
     }
   }
   mark(13);
-  if (tid == 0 && a.trace) {
+  if (TRACE && tid == 0) {
     for (int rec = 0; rec < 5; ++rec) {
       const int64_t ri = a.Q + a.P + (int64_t)(1 + rec) * gridDim.x + blockIdx.x;
       if (ri < a.trace_cap) {
@@ -1314,7 +1335,8 @@ __global__ void __launch_bounds__(kPT, 2) k_post(const __grid_constant__ LayerAr
 
 template <int D, int G, int MODE>
 static cudaError_t launch_post_mode(const LayerArgs& a, cudaStream_t st) {
-  const void* fn = reinterpret_cast<const void*>(&k_post<D, G, MODE>);
+  const void* fn = a.trace ? reinterpret_cast<const void*>(&k_post<D, G, MODE, true>)
+                           : reinterpret_cast<const void*>(&k_post<D, G, MODE, false>);
   // (shared memory limit and cluster size allowed by prepare_post)
   const size_t smem = (size_t)post_layout(D, G, a.C, a.bpc_max, a.K).total * 4;
   LayerArgs args = a;
@@ -1368,9 +1390,12 @@ size_t post_smem(int D, int G, int C, int bpc_max, int K) { return (size_t)post_
 
 template <int D, int G, int MODE>
 static cudaError_t prepare_post_mode(int C, int bpc_max, int K) {
-  const void* fn = reinterpret_cast<const void*>(&k_post<D, G, MODE>);
-  cudaError_t e = raise_smem_limit(fn, post_layout(D, G, C, bpc_max, K).total * 4);
-  if (e == cudaSuccess && C > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  cudaError_t e = cudaSuccess;
+  for (const void* fn : {reinterpret_cast<const void*>(&k_post<D, G, MODE, false>),
+                         reinterpret_cast<const void*>(&k_post<D, G, MODE, true>)}) {
+    if (e == cudaSuccess) e = raise_smem_limit(fn, post_layout(D, G, C, bpc_max, K).total * 4);
+    if (e == cudaSuccess && C > 8) e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  }
   return e;
 }
 
