@@ -274,7 +274,9 @@ __device__ __noinline__ void open_block_warp(const LayerArgs& a, int u, int lane
   }
 }
 
-template <int D, int G, int MODE, int SB, int RPL>
+// TRACE: the work-item trace is recorded (a.trace is set); the instance without it carries no
+// trace code.
+template <int D, int G, int MODE, int SB, int RPL, bool TRACE>
 __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
   constexpr bool APPEND = (MODE & kFAppend) != 0;
   constexpr bool SCORE = (MODE & kFScore) != 0;
@@ -300,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
   int* sseg = soff + kMaxBatch + 1;
   int* sbad = sseg + 1;                          // a wait of this CTA ran out
   uint64_t* bars = reinterpret_cast<uint64_t*>((reinterpret_cast<uintptr_t>(sbad + 1) + 7) & ~uintptr_t(7));
-  const unsigned long long t_start = a.trace ? global_ns() : 0ull;
+  const unsigned long long t_start = TRACE ? global_ns() : 0ull;
   if (threadIdx.x < 2 * kWarps) mbar_init(bars + threadIdx.x, 1);  // per warp: kbar/Dbar copies, vbar copies
   if (threadIdx.x == 0) {
     *sbad = 0;
@@ -316,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
 #pragma unroll 1
       for (int u = blockIdx.x * kWarps + warp; u < units; u += a.Q * kWarps) open_block_warp<D, G>(a, u, lane);
     }
-    if (threadIdx.x == 0 && a.trace && (int)blockIdx.x < a.trace_cap) {
+    if (TRACE && threadIdx.x == 0 && (int)blockIdx.x < a.trace_cap) {
       unsigned long long* rr = a.trace + 1 + 8 * (int64_t)blockIdx.x;
       rr[0] = ((unsigned long long)blockIdx.x << 32);
       rr[1] = 0ull;
@@ -346,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
   }
   __syncthreads();
   const int seg = *sseg, total = soff[a.B];
-  const unsigned long long t_plan = a.trace ? global_ns() : 0ull;
+  const unsigned long long t_plan = TRACE ? global_ns() : 0ull;
   unsigned long long t_first = 0ull, t_r1 = 0ull, t_r2 = 0ull, t_r3 = 0ull;
   int nseg_done = 0;
   uint32_t usesK = 0, usesV = 0;  // stages whose kbar/Dbar (vbar) this warp has consumed: the barriers' phases
@@ -607,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
       if (lane == 0) *sbad = 1;
     }
     __syncthreads();  // every stage of the segment is consumed: the slots are free
-    if (!nseg_done && a.trace) t_first = global_ns();
+    if (TRACE && !nseg_done) t_first = global_ns();
     ++nseg_done;
     if (*sbad) break;  // a copy never arrived: this CTA stops (the status word holds the timeout)
 
@@ -638,9 +640,9 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
       for (int g = 0; g < G; ++g)
 #pragma unroll
         for (int c = 0; c < CPL; ++c) xa[(warp * G + g) * D + CPL * lane + c] = acc[g][c];
-    if (nseg_done == 1 && a.trace) t_r1 = global_ns();
+    if (TRACE && nseg_done == 1) t_r1 = global_ns();
     __syncthreads();
-    if (nseg_done == 1 && a.trace) t_r2 = global_ns();
+    if (TRACE && nseg_done == 1) t_r2 = global_ns();
     if (warp < G) {
       const int g = warp;
       // lane w < kWarps takes warp w's part; three xor steps combine them
@@ -676,10 +678,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
           *reinterpret_cast<float2*>(dst) = make_float2(o[0], o[1]);
       }
     }
-    if (nseg_done == 1 && a.trace) t_r3 = global_ns();
+    if (TRACE && nseg_done == 1) t_r3 = global_ns();
     __syncthreads();  // the slots are free for the next segment
   }
-  if (threadIdx.x == 0 && a.trace && (int)blockIdx.x < a.trace_cap) {
+  if (TRACE && threadIdx.x == 0 && (int)blockIdx.x < a.trace_cap) {
     unsigned long long* rr = a.trace + 1 + 8 * (int64_t)blockIdx.x;
     rr[0] = ((unsigned long long)blockIdx.x << 32) | (unsigned)nseg_done;
     rr[1] = 0ull;
@@ -692,19 +694,23 @@ __global__ void __launch_bounds__(kThreads, 2) k_stream(LayerArgs a) {
   }
 }
 
-template <int D, int G, int MODE>
-static const void* stream_fn(int r) {
+template <int D, int G, int MODE, bool TRACE>
+static const void* stream_fn_t(int r) {
   if constexpr (D >= 128)
-    if (r >= 128) return reinterpret_cast<const void*>(&k_stream<D, G, MODE, 4, 4>);
-  if (long_dbar(r)) return reinterpret_cast<const void*>(&k_stream<D, G, MODE, 4, 2>);
-  return reinterpret_cast<const void*>(&k_stream<D, G, MODE, (G >= 8 ? 4 : 8), 0>);
+    if (r >= 128) return reinterpret_cast<const void*>(&k_stream<D, G, MODE, 4, 4, TRACE>);
+  if (long_dbar(r)) return reinterpret_cast<const void*>(&k_stream<D, G, MODE, 4, 2, TRACE>);
+  return reinterpret_cast<const void*>(&k_stream<D, G, MODE, (G >= 8 ? 4 : 8), 0, TRACE>);
+}
+template <int D, int G, int MODE>
+static const void* stream_fn(int r, bool trace = false) {
+  return trace ? stream_fn_t<D, G, MODE, true>(r) : stream_fn_t<D, G, MODE, false>(r);
 }
 
 template <int D, int G, int MODE>
 static cudaError_t launch_stream_mode(const LayerArgs& a, cudaStream_t st, bool pdl) {
   constexpr bool SCORE = (MODE & kFScore) != 0;
   constexpr bool COMP = (MODE & kFComp) != 0;
-  const void* fn = stream_fn<D, G, MODE>(a.r);
+  const void* fn = stream_fn<D, G, MODE>(a.r, a.trace != nullptr);
   const size_t smem = (size_t)stream_smem_bytes(D, a.r, G, SCORE, COMP);  // (limit raised by prepare_stream)
   LayerArgs args = a;
   chain_split(args, MODE);
@@ -782,7 +788,10 @@ template <int D, int G, int MODE>
 static cudaError_t prepare_stream_mode(int r) {
   constexpr bool SCORE = (MODE & kFScore) != 0;
   constexpr bool COMP = (MODE & kFComp) != 0;
-  return raise_smem_limit(stream_fn<D, G, MODE>(r), stream_smem_bytes(D, r, G, SCORE, COMP));
+  const int smem = stream_smem_bytes(D, r, G, SCORE, COMP);
+  cudaError_t e = raise_smem_limit(stream_fn<D, G, MODE>(r, false), smem);
+  if (e == cudaSuccess) e = raise_smem_limit(stream_fn<D, G, MODE>(r, true), smem);
+  return e;
 }
 
 template <int D, int G>
