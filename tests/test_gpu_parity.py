@@ -52,6 +52,7 @@ SHAPES = [
     dict(head_dim=128, group_size=2, r=2, num_kv_heads=1),
     dict(head_dim=64, group_size=8, r=64, num_kv_heads=1),
     dict(head_dim=128, group_size=4, r=16, num_kv_heads=2),
+    dict(head_dim=128, group_size=4, r=64, num_kv_heads=2),  # long Dbar rows, two coordinates per lane
 ]
 
 
