@@ -30,7 +30,11 @@
 // coordinates (lane l holds coordinates CPL*l .. CPL*l + CPL - 1) and sums
 // them across the warp with a halving butterfly: at each xor step a lane keeps
 // half of its values and receives its partner's partial of that half, so the
-// NV = SB*G values end one per lane (or replicated over 32/NV lanes).
+// NV = SB*G values end one per lane (or replicated over 32/NV lanes).  With
+// long Dbar rows (r = 32 RPL, RPL = 2 or 4) sigma2 takes the same form: each
+// lane reads its RPL coordinates of the Qsq and Dbar rows as one vector, and a
+// second butterfly sums the partials.  The kernel has an instance that records
+// the work-item trace and one without any trace code.
 #include "compkv_launch.h"
 #include "decode_common.cuh"
 
